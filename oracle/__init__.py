@@ -1,0 +1,141 @@
+"""fp64 CPU oracle for the Complex KDA (CKDA) recurrence -- TEST INFRASTRUCTURE.
+
+Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The CUDA library never calls it and
+shares no code with it.
+
+The arithmetic lives in ``ckda_oracle.c`` (plain C, fp64, token by token, in
+the order of "Kimi Delta Attention: a bounded case study", worked case A/B:
+decay, read, correct, then read out the updated state as on the "Complex KDA"
+discussion slides, frame "CKDA keeps the original gate--delta--readout
+structure").  This module compiles it with gcc and marshals numpy arrays.
+
+Functions and what pins them (tests/test_oracle_pins.py):
+
+* ``fwd`` -- pinned by the worked decay/correction trace (bounded case study,
+  worked case A and B), the one-step rotation R_{pi/2} (discussion slides,
+  "Two reflections make a rotation in one update"), the closed form of Eq. (2)
+  and the one-layer clock of Lemma 24 (paper), the Prop. 2 block, the
+  non-expansiveness bound, the spectrum rule of Thm. 8, orthogonality of
+  signed Householder products (Thm. 1), brute-force products of explicit
+  n x n transition matrices, the sign gauge, channel permutations and the
+  exact-retrieval reduction.
+* ``decode_step`` -- pinned against ``fwd`` token by token and by the same
+  rotation/decay fixtures.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "ckda_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "libckda_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ckda_oracle.c into a shared library next to it (gcc, OpenMP)."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp",
+           "-fno-fast-math", "-ffp-contract=off", _SRC, "-o", tmp]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB_PATH)
+            dp = ctypes.POINTER(ctypes.c_double)
+            ip = ctypes.POINTER(ctypes.c_int32)
+            lib.ckda_oracle_fwd.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, ip,
+                                            ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                            ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                            ctypes.c_double, ctypes.c_int]
+            lib.ckda_oracle_fwd.restype = ctypes.c_int
+            lib.ckda_oracle_decode_step.argtypes = [dp, dp, dp, dp, dp, dp, dp,
+                                                    ctypes.c_int, ctypes.c_int,
+                                                    ctypes.c_int, ctypes.c_int,
+                                                    ctypes.c_double, ctypes.c_int]
+            lib.ckda_oracle_decode_step.restype = ctypes.c_int
+            lib.ckda_oracle_max_threads.argtypes = []
+            lib.ckda_oracle_max_threads.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _f64(x):
+    if x is None:
+        return None
+    if hasattr(x, "detach"):  # torch tensor: widen exactly on the CPU
+        x = x.detach().to("cpu").double().numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _ptr(a):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def max_threads() -> int:
+    return int(_load().ckda_oracle_max_threads())
+
+
+def fwd(q, k, v, alpha, beta, h0=None, cu_seqlens=None, scale=1.0,
+        store_o=True, store_hT=True, nthreads=0):
+    """Token-by-token fp64 recurrence.
+
+    q, k, alpha: [B, H, T, dk]; v: [B, H, T, dv]; beta: [B, H, T];
+    h0: [N, H, dk, dv] or None (zero state); cu_seqlens: [N + 1] int or None.
+    Returns (o [B,H,T,dv] or None, hT [N,H,dk,dv] or None) as fp64 numpy.
+    """
+    lib = _load()
+    q, k, v, alpha, beta, h0 = (_f64(a) for a in (q, k, v, alpha, beta, h0))
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    cu = None
+    N = B
+    if cu_seqlens is not None:
+        if hasattr(cu_seqlens, "detach"):
+            cu_seqlens = cu_seqlens.detach().to("cpu").numpy()
+        cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int32))
+        N = cu.shape[0] - 1
+    o = np.zeros((B, H, T, dv), dtype=np.float64) if store_o else None
+    hT = np.zeros((N, H, dk, dv), dtype=np.float64) if store_hT else None
+    rc = lib.ckda_oracle_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta),
+                             _ptr(h0), _ptr(o), _ptr(hT),
+                             None if cu is None else cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                             int(N if cu is not None else 0), B, H, T, dk, dv,
+                             float(scale), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle fwd: invalid arguments")
+    return o, hT
+
+
+def decode_step(q, k, v, alpha, beta, state, scale=1.0, nthreads=0):
+    """One token on a resident state.  Returns (o [B,H,dv], new_state)."""
+    lib = _load()
+    q, k, v, alpha, beta = (_f64(a) for a in (q, k, v, alpha, beta))
+    S = _f64(state).copy()
+    B, H, dk = q.shape
+    dv = v.shape[-1]
+    o = np.zeros((B, H, dv), dtype=np.float64)
+    rc = lib.ckda_oracle_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta),
+                                     _ptr(S), _ptr(o), B, H, dk, dv, float(scale),
+                                     int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle decode_step: invalid arguments")
+    return o, S

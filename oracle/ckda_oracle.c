@@ -1,0 +1,184 @@
+/*
+ * ckda_oracle.c -- plain fp64 CPU oracle for the Complex KDA (CKDA) recurrence.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the slow, obviously correct
+ * reference that the CUDA path is checked against.  Only the test-suite, the
+ * smoke check and the CPU-baseline leg of the benchmark may load it; the
+ * library path never does.  It shares no code, header or constant with the
+ * CUDA library.
+ *
+ * What it computes (one head, one sequence), in the order the pages state it:
+ *
+ *   H_t = (I - beta_t k_t k_t^T) Diag(alpha_t) H_{t-1} + beta_t k_t v_t^T
+ *   o_t = H_t^T q_t
+ *
+ *   - "Complex KDA" discussion slides, frame "CKDA keeps the original
+ *     gate--delta--readout structure" (the recurrence and the readout of the
+ *     UPDATED state; H_t is n x d_v, rows are key channels).
+ *   - "Complex KDA: Understanding and Enhancing the Expressivity of Kimi Delta
+ *     Attention", App. B.2, Eq. (9): A(x_t) = (I - beta k k^T) Diag(alpha),
+ *     B(x_t) = beta k v^T.
+ *   - "Kimi Delta Attention: a bounded case study", worked case A/B: the same
+ *     update written as three steps -- per-channel decay S' = Diag(a) S
+ *     (row i scaled by a_i), read  v_hat = S'^T k, correct
+ *     S = S' + beta k (v - v_hat)^T.  This oracle follows those three steps
+ *     literally and then reads out o_t = S^T (scale * q_t).
+ *
+ * `scale` multiplies q before the readout; the pages use no scale (1.0).
+ * The oracle does not renormalise k: it consumes exactly the values given.
+ *
+ * Layouts (row-major, contiguous, the same as the C-ABI of the library):
+ *   q, k, alpha : [B, H, T, dk]      v, o : [B, H, T, dv]      beta : [B, H, T]
+ *   h0, hT      : [N, H, dk, dv]     N = B (dense) or num_seqs (packed)
+ *   cu_seqlens  : [num_seqs + 1] token offsets into T when B == 1 (packed
+ *                 variable-length sequences), or NULL for dense [B, H, T].
+ *   h0 == NULL means a zero initial state; hT == NULL means "do not store".
+ *
+ * Parallelism: independent (sequence, head) pairs run on separate OpenMP
+ * threads (same paper, App. B.2 "Heads and layers": heads have separate
+ * states).  Every pair is computed token by token, in order.
+ */
+#include <stddef.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* One token of the recurrence on a state S[dk][dv] (row i = key channel i).
+ * Worked case A/B order: decay, read, correct; then the readout of the
+ * updated state.  `pred` is scratch of length dv. */
+static void ckda_token(double *S, int dk, int dv,
+                       const double *q, const double *k, const double *v,
+                       const double *alpha, double beta, double scale,
+                       double *o, double *pred)
+{
+    /* (1) per-channel decay: S' = Diag(alpha) S  -- row i times alpha_i */
+    for (int i = 0; i < dk; ++i) {
+        double a = alpha[i];
+        double *row = S + (size_t)i * dv;
+        for (int j = 0; j < dv; ++j) row[j] *= a;
+    }
+    /* (2) read: v_hat = S'^T k */
+    for (int j = 0; j < dv; ++j) pred[j] = 0.0;
+    for (int i = 0; i < dk; ++i) {
+        double ki = k[i];
+        const double *row = S + (size_t)i * dv;
+        for (int j = 0; j < dv; ++j) pred[j] += row[j] * ki;
+    }
+    /* (3) compare and correct: S = S' + beta k (v - v_hat)^T */
+    for (int i = 0; i < dk; ++i) {
+        double bk = beta * k[i];
+        double *row = S + (size_t)i * dv;
+        for (int j = 0; j < dv; ++j) row[j] += bk * (v[j] - pred[j]);
+    }
+    /* (4) readout of the updated state: o = S^T (scale q) */
+    if (o) {
+        for (int j = 0; j < dv; ++j) o[j] = 0.0;
+        for (int i = 0; i < dk; ++i) {
+            double qi = scale * q[i];
+            const double *row = S + (size_t)i * dv;
+            for (int j = 0; j < dv; ++j) o[j] += row[j] * qi;
+        }
+    }
+}
+
+/* Runs one (sequence, head) pair over tokens [t0, t0 + len) of the [B,H,T,.]
+ * arrays at batch index b and head h. */
+static void ckda_pair(const double *q, const double *k, const double *v,
+                      const double *alpha, const double *beta,
+                      const double *h0, double *o, double *hT,
+                      int b, int h, int t0, int len,
+                      int H, int T, int dk, int dv, double scale, size_t state_idx)
+{
+    size_t state_elems = (size_t)dk * dv;
+    double *S = (double *)malloc(state_elems * sizeof(double));
+    double *pred = (double *)malloc((size_t)dv * sizeof(double));
+    if (!S || !pred) { free(S); free(pred); return; }
+    if (h0) memcpy(S, h0 + state_idx * state_elems, state_elems * sizeof(double));
+    else memset(S, 0, state_elems * sizeof(double));
+
+    size_t base = ((size_t)b * H + h) * (size_t)T;
+    for (int t = t0; t < t0 + len; ++t) {
+        size_t row = base + (size_t)t;
+        ckda_token(S, dk, dv,
+                   q + row * dk, k + row * dk, v + row * dv,
+                   alpha + row * dk, beta[row], scale,
+                   o ? o + row * dv : NULL, pred);
+    }
+    if (hT) memcpy(hT + state_idx * state_elems, S, state_elems * sizeof(double));
+    free(S);
+    free(pred);
+}
+
+/* Returns 0 on success, -1 on an argument error.  nthreads <= 0 uses the
+ * OpenMP default. */
+int ckda_oracle_fwd(const double *q, const double *k, const double *v,
+                    const double *alpha, const double *beta, const double *h0,
+                    double *o, double *hT, const int32_t *cu_seqlens, int num_seqs,
+                    int B, int H, int T, int dk, int dv, double scale, int nthreads)
+{
+    if (!q || !k || !v || !alpha || !beta) return -1;
+    if (B < 1 || H < 1 || T < 0 || dk < 1 || dv < 1) return -1;
+    int N = B;
+    if (cu_seqlens) {
+        if (B != 1 || num_seqs < 1) return -1;
+        if (cu_seqlens[0] != 0 || cu_seqlens[num_seqs] != T) return -1;
+        for (int s = 0; s < num_seqs; ++s)
+            if (cu_seqlens[s + 1] < cu_seqlens[s]) return -1;
+        N = num_seqs;
+    }
+    long pairs = (long)N * H;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+    for (long p = 0; p < pairs; ++p) {
+        int n = (int)(p / H), h = (int)(p % H);
+        int b = cu_seqlens ? 0 : n;
+        int t0 = cu_seqlens ? cu_seqlens[n] : 0;
+        int len = cu_seqlens ? cu_seqlens[n + 1] - cu_seqlens[n] : T;
+        ckda_pair(q, k, v, alpha, beta, h0, o, hT, b, h, t0, len,
+                  H, T, dk, dv, scale, (size_t)n * H + h);
+    }
+    (void)nthreads;
+    return 0;
+}
+
+/* One decode step on a resident state [B, H, dk, dv], updated in place.
+ * q, k, alpha: [B, H, dk]; v, o: [B, H, dv]; beta: [B, H]. */
+int ckda_oracle_decode_step(const double *q, const double *k, const double *v,
+                            const double *alpha, const double *beta, double *state,
+                            double *o, int B, int H, int dk, int dv, double scale,
+                            int nthreads)
+{
+    if (!q || !k || !v || !alpha || !beta || !state) return -1;
+    if (B < 1 || H < 1 || dk < 1 || dv < 1) return -1;
+    long pairs = (long)B * H;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(static)
+#endif
+    for (long p = 0; p < pairs; ++p) {
+        double *pred = (double *)malloc((size_t)dv * sizeof(double));
+        if (!pred) continue;
+        ckda_token(state + (size_t)p * dk * dv, dk, dv,
+                   q + (size_t)p * dk, k + (size_t)p * dk, v + (size_t)p * dv,
+                   alpha + (size_t)p * dk, beta[p], scale,
+                   o ? o + (size_t)p * dv : NULL, pred);
+        free(pred);
+    }
+    (void)nthreads;
+    return 0;
+}
+
+/* Number of OpenMP threads a parallel region would use (1 without OpenMP). */
+int ckda_oracle_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

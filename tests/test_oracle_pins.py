@@ -1,0 +1,455 @@
+"""Pins of the fp64 oracle to facts the pages and the mathematics fix.
+
+Each test names its source.  Together they are chosen so that a plausible
+mistake in the oracle (a dropped term, a sign, a transposed operand, the
+readout taken before the update, a gate applied to columns instead of rows)
+fails at least one of them.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def one_seq(q, k, v, alpha, beta, h0=None, scale=1.0):
+    """Run the oracle on a single (sequence, head): inputs [T, n] etc."""
+    q, k, v, alpha = (np.asarray(x, dtype=np.float64)[None, None] for x in (q, k, v, alpha))
+    beta = np.asarray(beta, dtype=np.float64)[None, None]
+    if h0 is not None:
+        h0 = np.asarray(h0, dtype=np.float64)[None, None]
+    o, hT = oracle.fwd(q, k, v, alpha, beta, h0, scale=scale)
+    return o[0, 0], hT[0, 0]
+
+
+def transition(alpha, beta, k):
+    """The one-step transition matrix A, read off the oracle: h0 = I, v = 0."""
+    n = len(alpha)
+    z = np.zeros((1, n))
+    _, H1 = one_seq(z, [k], z, [alpha], [beta], h0=np.eye(n))
+    return H1
+
+
+def unit(x):
+    x = np.asarray(x, dtype=np.float64)
+    return x / np.linalg.norm(x)
+
+
+def rand_admissible(rng, n):
+    """alpha in [-1,1]^n (with exact -1, 0, 1 sprinkled in), beta in [0,2], unit k."""
+    a = rng.uniform(-1, 1, n)
+    a[rng.random(n) < 0.15] = -1.0
+    a[rng.random(n) < 0.05] = 0.0
+    a[rng.random(n) < 0.05] = 1.0
+    return a, rng.uniform(0, 2), unit(rng.standard_normal(n))
+
+
+# --- the pages' worked example ------------------------------------------------
+
+def _load_worked_case():
+    s0, traces = None, {}
+    with open(os.path.join(GOLDEN, "bounded_case_study_worked_case.txt")) as f:
+        for line in f:
+            line = line.split("#")[0].strip()
+            if not line:
+                continue
+            if line.startswith("S0"):
+                s0 = np.array([float(x) for x in line.split()[1:]]).reshape(2, 2)
+                continue
+            lhs, rhs = line.split("->")
+            tag, step, beta, k1, k2, v1, v2 = lhs.split()
+            traces.setdefault(tag, []).append(
+                (int(step), float(beta), [float(k1), float(k2)], [float(v1), float(v2)],
+                 np.array([float(x) for x in rhs.split()]).reshape(2, 2)))
+    return s0, traces
+
+
+def test_worked_case_decay_and_correction():
+    """Bounded case study, worked case A (per-channel decay of row i by a_i)
+    and B (exact correction to [4,4], then 4*0.2^2 = 0.160 retained; 3.240 on
+    channel 1)."""
+    s0, traces = _load_worked_case()
+    a = [0.9, 0.2]
+    for tag, steps in traces.items():
+        T = len(steps)
+        beta = [s[1] for s in steps]
+        k = [s[2] for s in steps]
+        v = [s[3] for s in steps]
+        q = np.zeros((T, 2))
+        for t in range(1, T + 1):
+            # state after t steps: run the first t tokens
+            _, hT = one_seq(q[:t], k[:t], v[:t], [a] * t, beta[:t], h0=s0)
+            np.testing.assert_allclose(hT, steps[t - 1][4], rtol=0, atol=1e-12,
+                                       err_msg=f"trace {tag} step {t}")
+
+
+def test_worked_case_readout_is_of_updated_state():
+    """The readout o_t = H_t^T q_t reads the UPDATED state ("Complex KDA"
+    slides, frame "CKDA keeps the original gate--delta--readout structure").
+    With q = e2 at the write step the output is exactly v = [4, 4]."""
+    s0, _ = _load_worked_case()
+    o, _ = one_seq([[0, 0], [0, 1]], [[0, 1], [0, 1]], [[0, 0], [4, 4]],
+                   [[0.9, 0.2]] * 2, [0.0, 1.0], h0=s0)
+    np.testing.assert_allclose(o[1], [4.0, 4.0], atol=1e-12)
+    # and at the decay-only step it is row 2 of Diag(a) S0 = [1.0, 0.2]
+    np.testing.assert_allclose(o[0], [0.0, 0.0], atol=1e-12)
+    o, _ = one_seq([[0, 1]], [[0, 1]], [[0, 0]], [[0.9, 0.2]], [0.0], h0=s0)
+    np.testing.assert_allclose(o[0], [1.0, 0.2], atol=1e-12)
+
+
+def test_scale_multiplies_the_query():
+    rng = np.random.default_rng(5)
+    T, n = 9, 4
+    args = (rng.standard_normal((T, n)), [unit(x) for x in rng.standard_normal((T, n))],
+            rng.standard_normal((T, n)), rng.uniform(-1, 1, (T, n)), rng.uniform(0, 2, T))
+    o1, h1 = one_seq(*args)
+    o2, h2 = one_seq(*args, scale=0.375)
+    np.testing.assert_allclose(o2, 0.375 * o1, rtol=1e-14, atol=1e-14)
+    np.testing.assert_array_equal(h1, h2)
+
+
+# --- closed forms ---------------------------------------------------------------
+
+def test_two_reflections_make_rotation():
+    """"Complex KDA" slides, "Two reflections make a rotation in one update":
+    k = (1,1)/sqrt2, beta = 2, alpha = (-1, 1) gives R_{pi/2}."""
+    with open(os.path.join(GOLDEN, "two_reflections_rotation.txt")) as f:
+        rows = [l.split("#")[0].strip() for l in f if l.split("#")[0].strip()]
+    for row in rows:
+        lhs, rhs = row.split("->")
+        a1, a2, beta, theta = (float(x) for x in lhs.split())
+        want = np.array([float(x) for x in rhs.split()]).reshape(2, 2)
+        A = transition([a1, a2], beta, [math.cos(theta), math.sin(theta)])
+        np.testing.assert_allclose(A, want, atol=1e-15)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_eq2_closed_form_and_discriminant(seed):
+    """Paper Sec. 3, Eq. (2): A = (I - 2kk^T) Diag(alpha, 1), k = (cos t, sin t)
+    = [[-a cos2t, -sin2t], [-a sin2t, cos2t]]; Delta = (1-a)^2 cos^2 2t + 4a;
+    Delta < 0 gives a complex pair of modulus sqrt(-a)."""
+    rng = np.random.default_rng(100 + seed)
+    for _ in range(50):
+        a = rng.uniform(-1, 1)
+        th = rng.uniform(0, math.pi / 2)
+        A = transition([a, 1.0], 2.0, [math.cos(th), math.sin(th)])
+        c2, s2 = math.cos(2 * th), math.sin(2 * th)
+        want = np.array([[-a * c2, -s2], [-a * s2, c2]])
+        np.testing.assert_allclose(A, want, atol=1e-14)
+        delta = (1 - a) ** 2 * c2 ** 2 + 4 * a
+        lam = np.linalg.eigvals(A)
+        if delta < -1e-9:
+            assert np.all(np.abs(lam.imag) > 0)
+            np.testing.assert_allclose(np.abs(lam), math.sqrt(-a), rtol=1e-9)
+        elif delta > 1e-9:
+            assert np.all(np.abs(lam.imag) < 1e-12)
+
+
+def test_lemma24_one_layer_clock():
+    """Paper App. D.2, Lemma 24: beta = 2, alpha = (1, -1), k = (-sin(phi/2),
+    cos(phi/2)) is a rotation by phi; from c0 = e1 the state visits
+    c_i = (cos(pi i/m), sin(pi i/m)) with phi = pi/m and returns after 2m steps."""
+    for m in (1, 2, 3, 5, 8):
+        phi = math.pi / m
+        T = 2 * m
+        k = [[-math.sin(phi / 2), math.cos(phi / 2)]] * T
+        qs = np.eye(2)[np.arange(T) % 2]  # any queries
+        o, hT = one_seq(qs, k, np.zeros((T, 1)), [[1.0, -1.0]] * T, [2.0] * T,
+                        h0=np.array([[1.0], [0.0]]))
+        for i in range(1, T + 1):
+            _, Hi = one_seq(qs[:i], k[:i], np.zeros((i, 1)), [[1.0, -1.0]] * i, [2.0] * i,
+                            h0=np.array([[1.0], [0.0]]))
+            np.testing.assert_allclose(Hi[:, 0], [math.cos(math.pi * i / m),
+                                                  math.sin(math.pi * i / m)], atol=1e-13)
+            np.testing.assert_allclose(o[i - 1, 0], qs[i - 1] @ Hi[:, 0], atol=1e-13)
+        np.testing.assert_allclose(hT[:, 0], [1.0, 0.0], atol=1e-13)
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_prop2_sign_core_block(seed):
+    """Paper Prop. 2 / App. A.2 (Prop. 7), slides backup "separate the sign core
+    from magnitude scaling": with unit gates of mixed sign, (I - beta kk^T) S
+    restricted to span(k-, k+) is [[b c^2 - 1, -b s c], [b s c, 1 - b s^2]] in
+    the basis (k-/|k-|, k+/|k+|), |k-| = cos th, |k+| = sin th; the complement
+    keeps its signs."""
+    rng = np.random.default_rng(200 + seed)
+    n = 6
+    sgn = np.where(rng.random(n) < 0.5, -1.0, 1.0)
+    sgn[0], sgn[1] = -1.0, 1.0
+    th = rng.uniform(0.1, 1.4)
+    beta = rng.uniform(0, 2)
+    um = np.where(sgn < 0, rng.standard_normal(n), 0.0)
+    up = np.where(sgn > 0, rng.standard_normal(n), 0.0)
+    um, up = unit(um), unit(up)
+    k = math.cos(th) * um + math.sin(th) * up
+    A = transition(sgn, beta, k)
+    c, s = math.cos(th), math.sin(th)
+    basis = np.stack([um, up], axis=1)
+    blk = basis.T @ A @ basis
+    np.testing.assert_allclose(blk, [[beta * c * c - 1, -beta * s * c],
+                                     [beta * s * c, 1 - beta * s * s]], atol=1e-13)
+    # A maps the plane to itself
+    np.testing.assert_allclose(A @ basis, basis @ blk, atol=1e-13)
+    # on the orthogonal complement A acts as the sign diagonal
+    P = np.eye(n) - basis @ basis.T
+    np.testing.assert_allclose(A @ P, np.diag(sgn) @ P, atol=1e-13)
+    if abs(beta - 2.0) < 1e-15:
+        pass
+    # at beta = 2 the block is the rotation by 2 theta
+    A2 = transition(sgn, 2.0, k)
+    blk2 = basis.T @ A2 @ basis
+    np.testing.assert_allclose(blk2, [[math.cos(2 * th), -math.sin(2 * th)],
+                                      [math.sin(2 * th), math.cos(2 * th)]], atol=1e-13)
+
+
+def test_eq3_diagonal_as_axis_householders():
+    """Paper Sec. 3, Eq. (3): Diag(alpha) = prod_i (I - (1 - alpha_i) e_i e_i^T).
+    With beta = 1 - alpha_i and k = e_i, the oracle's transition with a unit
+    gate is exactly that axis factor; chaining n such steps gives Diag(alpha)."""
+    rng = np.random.default_rng(7)
+    n = 5
+    alpha = rng.uniform(-1, 1, n)
+    T = n
+    k = np.eye(n)
+    _, H = one_seq(np.zeros((T, n)), k, np.zeros((T, n)), np.ones((T, n)), 1.0 - alpha,
+                   h0=np.eye(n))
+    np.testing.assert_allclose(H, np.diag(alpha), atol=1e-15)
+
+
+# --- invariants -------------------------------------------------------------------
+
+@pytest.mark.parametrize("seed", range(4))
+def test_non_expansive_transition(seed):
+    """Slides, "The transition remains non-expansive and inexpensive":
+    ||A_t||_2 <= ||I - beta kk^T||_2 ||Diag alpha||_2 <= 1; with v = 0 the state
+    norm never grows; additive writes can grow it."""
+    rng = np.random.default_rng(300 + seed)
+    n = 8
+    for _ in range(40):
+        a, b, k = rand_admissible(rng, n)
+        A = transition(a, b, k)
+        assert np.linalg.norm(A, 2) <= 1.0 + 1e-12
+    T = 30
+    ks = [unit(x) for x in rng.standard_normal((T, n))]
+    al = rng.uniform(-1, 1, (T, n))
+    be = rng.uniform(0, 2, T)
+    h0 = rng.standard_normal((n, 3))
+    prev = np.linalg.norm(h0, 2)
+    for t in range(1, T + 1):
+        _, Ht = one_seq(np.zeros((t, n)), ks[:t], np.zeros((t, 3)), al[:t], be[:t], h0=h0)
+        cur = np.linalg.norm(Ht, 2)
+        assert cur <= prev * (1 + 1e-12) + 1e-14
+        prev = cur
+    # a write can increase the norm
+    _, Hw = one_seq(np.zeros((1, n)), [np.eye(n)[0]], [[5.0, 0, 0]], [np.ones(n)], [1.0],
+                    h0=np.zeros((n, 3)))
+    assert np.linalg.norm(Hw, 2) > 4.9
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_spectrum_theorem8(seed):
+    """Paper App. A.3, Thm. 8 (slides table "Both range extensions are needed"):
+    a CKDA transition has at most one non-real conjugate pair; none when
+    beta <= 1 or when every alpha >= 0."""
+    rng = np.random.default_rng(400 + seed)
+    n = 6
+    for _ in range(60):
+        a, b, k = rand_admissible(rng, n)
+        lam = np.linalg.eigvals(transition(a, b, k))
+        assert np.sum(np.abs(lam.imag) > 1e-9) <= 2
+        lam1 = np.linalg.eigvals(transition(a, rng.uniform(0, 1), k))
+        assert np.all(np.abs(lam1.imag) < 1e-9)
+        lam2 = np.linalg.eigvals(transition(np.abs(a), b, k))
+        assert np.all(np.abs(lam2.imag) < 1e-9)
+    # and the pair does occur for the rotation example
+    lam = np.linalg.eigvals(transition([-1.0, 1.0], 2.0, unit([1, 1])))
+    assert np.sum(np.abs(lam.imag) > 0.5) == 2
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_signed_householder_products_are_orthogonal(seed):
+    """Paper Thm. 1 / App. B.3 (signed-Householder family SH_d): with
+    alpha in {-1, 1}^n and beta in {0, 2} every transition is orthogonal, so
+    from h0 = I with v = 0 the final state is orthogonal."""
+    rng = np.random.default_rng(500 + seed)
+    n, T = 7, 40
+    al = np.where(rng.random((T, n)) < 0.5, -1.0, 1.0)
+    be = np.where(rng.random(T) < 0.7, 2.0, 0.0)
+    ks = [unit(x) for x in rng.standard_normal((T, n))]
+    _, H = one_seq(np.zeros((T, n)), ks, np.zeros((T, n)), al, be, h0=np.eye(n))
+    np.testing.assert_allclose(H.T @ H, np.eye(n), atol=1e-12)
+
+
+# --- brute force ---------------------------------------------------------------------
+
+@pytest.mark.parametrize("seed", range(8))
+def test_brute_force_dense_transitions(seed):
+    """Paper Eq. (1) / App. B.2 Eq. (9) with the transition materialised as an
+    explicit n x n matrix, A_t = (I - beta_t k_t k_t^T) Diag(alpha_t), and
+    H_t = A_t H_{t-1} + beta_t k_t v_t^T, o_t = H_t^T q_t."""
+    rng = np.random.default_rng(600 + seed)
+    n = int(rng.integers(1, 9))
+    dv = int(rng.integers(1, 9))
+    T = int(rng.integers(1, 65))
+    q = rng.standard_normal((T, n))
+    k = np.stack([unit(x) for x in rng.standard_normal((T, n))])
+    v = rng.standard_normal((T, dv))
+    al = rng.uniform(-1, 1, (T, n))
+    al[rng.random((T, n)) < 0.1] = -1.0
+    al[rng.random((T, n)) < 0.05] = 0.0
+    be = rng.uniform(0, 2, T)
+    h0 = rng.standard_normal((n, dv)) if seed % 2 else np.zeros((n, dv))
+    o, hT = one_seq(q, k, v, al, be, h0=h0)
+    H = h0.copy()
+    for t in range(T):
+        A = (np.eye(n) - be[t] * np.outer(k[t], k[t])) @ np.diag(al[t])
+        H = A @ H + be[t] * np.outer(k[t], v[t])
+        np.testing.assert_allclose(o[t], H.T @ q[t], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(hT, H, rtol=1e-12, atol=1e-12)
+
+
+def test_homogeneous_product_is_product_of_transitions():
+    """With v = 0 and h0 = I the final state is the ordered product A_T ... A_1."""
+    rng = np.random.default_rng(11)
+    n, T = 5, 20
+    k = np.stack([unit(x) for x in rng.standard_normal((T, n))])
+    al = rng.uniform(-1, 1, (T, n))
+    be = rng.uniform(0, 2, T)
+    _, H = one_seq(np.zeros((T, n)), k, np.zeros((T, n)), al, be, h0=np.eye(n))
+    P = np.eye(n)
+    for t in range(T):
+        P = (np.eye(n) - be[t] * np.outer(k[t], k[t])) @ np.diag(al[t]) @ P
+    np.testing.assert_allclose(H, P, atol=1e-13)
+
+
+# --- equivalences --------------------------------------------------------------------
+
+@pytest.mark.parametrize("seed", range(3))
+def test_sign_gauge_equivalence(seed):
+    """Slides, "Absorb cumulative signs into keys and queries" (paper Lemma 27):
+    with S_t = Diag(sign alpha_t) (sign(0) = +1, paper App. A.2), P_t = S_1..S_t,
+    running on (P_t k_t, P_t q_t, |alpha_t|) gives the same outputs, and the
+    final state is P_T H_T."""
+    rng = np.random.default_rng(700 + seed)
+    n, dv, T = 6, 4, 50
+    q = rng.standard_normal((T, n))
+    k = np.stack([unit(x) for x in rng.standard_normal((T, n))])
+    v = rng.standard_normal((T, dv))
+    al = rng.uniform(-1, 1, (T, n))
+    al[rng.random((T, n)) < 0.1] = 0.0
+    al[rng.random((T, n)) < 0.1] = -1.0
+    be = rng.uniform(0, 2, T)
+    h0 = rng.standard_normal((n, dv))
+    o, hT = one_seq(q, k, v, al, be, h0=h0)
+    s = np.where(al < 0, -1.0, 1.0)
+    P = np.cumprod(s, axis=0)
+    o2, hT2 = one_seq(P * q, P * k, v, np.abs(al), be, h0=h0)
+    np.testing.assert_allclose(o2, o, rtol=1e-11, atol=1e-11)
+    np.testing.assert_allclose(hT2, P[-1][:, None] * hT, rtol=1e-11, atol=1e-11)
+
+
+def test_channel_permutation_equivariance():
+    """Adapted from "On State Reduction in Linear Attention", Prop. 3.1 (an
+    orthogonal change of key/query basis leaves the output unchanged): a
+    permutation commutes with Diag(alpha), so permuting the channels of q, k,
+    alpha and the rows of h0 leaves o unchanged and permutes the rows of hT."""
+    rng = np.random.default_rng(12)
+    n, dv, T = 7, 3, 33
+    q = rng.standard_normal((T, n))
+    k = np.stack([unit(x) for x in rng.standard_normal((T, n))])
+    v = rng.standard_normal((T, dv))
+    al = rng.uniform(-1, 1, (T, n))
+    be = rng.uniform(0, 2, T)
+    h0 = rng.standard_normal((n, dv))
+    perm = rng.permutation(n)
+    o, hT = one_seq(q, k, v, al, be, h0=h0)
+    o2, hT2 = one_seq(q[:, perm], k[:, perm], v, al[:, perm], be, h0=h0[perm])
+    np.testing.assert_allclose(o2, o, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(hT2, hT[perm], rtol=1e-12, atol=1e-12)
+
+
+def test_reductions():
+    """alpha = 1, beta = 0: the state never changes and o_t = h0^T q_t.
+    beta = 1 on a unit key: exact correction, H_t^T k_t = v_t (bounded case
+    study, "Delta correction": the write lands exactly)."""
+    rng = np.random.default_rng(13)
+    n, dv, T = 6, 5, 17
+    q = rng.standard_normal((T, n))
+    k = np.stack([unit(x) for x in rng.standard_normal((T, n))])
+    v = rng.standard_normal((T, dv))
+    h0 = rng.standard_normal((n, dv))
+    o, hT = one_seq(q, k, v, np.ones((T, n)), np.zeros(T), h0=h0)
+    np.testing.assert_allclose(o, q @ h0, atol=1e-13)
+    np.testing.assert_allclose(hT, h0, atol=0)
+    al = rng.uniform(-1, 1, (T, n))
+    o, _ = one_seq(k, k, v, al, np.ones(T), h0=h0)
+    np.testing.assert_allclose(o, v, atol=1e-12)
+    # alpha = 0 on every channel erases the past: the state is the fresh write
+    o, hT = one_seq(q[:1], k[:1], v[:1], np.zeros((1, n)), [0.7], h0=h0)
+    np.testing.assert_allclose(hT, 0.7 * np.outer(k[0], v[0]), atol=1e-14)
+
+
+# --- batching, packing and resume (host logic of the oracle) ----------------------
+
+def test_packed_equals_separate_and_resume_split():
+    rng = np.random.default_rng(14)
+    H, n, dv = 3, 4, 5
+    lengths = [5, 1, 0, 9, 3]
+    Tt = sum(lengths)
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    q = rng.standard_normal((1, H, Tt, n))
+    k = rng.standard_normal((1, H, Tt, n))
+    k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = rng.standard_normal((1, H, Tt, dv))
+    al = rng.uniform(-1, 1, (1, H, Tt, n))
+    be = rng.uniform(0, 2, (1, H, Tt))
+    h0 = rng.standard_normal((len(lengths), H, n, dv))
+    o, hT = oracle.fwd(q, k, v, al, be, h0, cu_seqlens=cu)
+    for s, L in enumerate(lengths):
+        a, b = cu[s], cu[s + 1]
+        o1, h1 = oracle.fwd(q[:, :, a:b], k[:, :, a:b], v[:, :, a:b], al[:, :, a:b],
+                            be[:, :, a:b], h0[s:s + 1])
+        np.testing.assert_array_equal(o[:, :, a:b], o1)
+        np.testing.assert_array_equal(hT[s:s + 1], h1)
+    # resume: fwd(T) == fwd(T1) then fwd(T2, h0 = hT1)
+    sl = slice(0, 9)
+    x = [t[:, :, cu[3]:cu[4]] for t in (q, k, v, al, be)]
+    oa, ha = oracle.fwd(*x, h0[3:4])
+    x1 = [t[:, :, :4] for t in x]
+    x2 = [t[:, :, 4:] for t in x]
+    o1, h1 = oracle.fwd(*x1, h0[3:4])
+    o2, h2 = oracle.fwd(*x2, h1)
+    np.testing.assert_allclose(np.concatenate([o1, o2], axis=2), oa, rtol=0, atol=1e-15)
+    np.testing.assert_allclose(h2, ha, rtol=0, atol=1e-15)
+    del sl
+
+
+def test_decode_step_matches_fwd_token_by_token():
+    rng = np.random.default_rng(15)
+    B, H, n, dv, T = 2, 3, 5, 4, 6
+    q = rng.standard_normal((B, H, T, n))
+    k = rng.standard_normal((B, H, T, n))
+    k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = rng.standard_normal((B, H, T, dv))
+    al = rng.uniform(-1, 1, (B, H, T, n))
+    be = rng.uniform(0, 2, (B, H, T))
+    h0 = rng.standard_normal((B, H, n, dv))
+    o, hT = oracle.fwd(q, k, v, al, be, h0, scale=0.5)
+    S = h0.copy()
+    for t in range(T):
+        ot, S = oracle.decode_step(q[:, :, t], k[:, :, t], v[:, :, t], al[:, :, t],
+                                   be[:, :, t], S, scale=0.5)
+        np.testing.assert_array_equal(ot, o[:, :, t])
+    np.testing.assert_array_equal(S, hT)
+
+
+def test_oracle_rejects_bad_packing():
+    z = np.zeros((1, 1, 4, 2))
+    with pytest.raises(ValueError):
+        oracle.fwd(z, z, z, z, np.zeros((1, 1, 4)), cu_seqlens=[0, 3])
+    with pytest.raises(ValueError):
+        oracle.fwd(z, z, z, z, np.zeros((1, 1, 4)), cu_seqlens=[0, 3, 2, 4])
