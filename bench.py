@@ -1,0 +1,445 @@
+#!/usr/bin/env python
+"""Benchmark of the CKDA forward (and decode step) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step is one ckda_fwd call over the KDA-range workload (B=8, H=16, T=2048,
+dk=dv=128, bf16 I/O, fp32 state, alpha = sigmoid(N(2,1)), beta = sigmoid(N(0,1)),
+h0 = 0), inputs resident in HBM.  The inputs (269 MB) exceed the 129 MB L2,
+so no flush is done between steps.  Prints ONE JSON line on rank 0 with:
+  value     whole-job token-heads/s (B*T*H per step, all ranks) from CUDA events
+  roofline  the forward kernel's algorithmic bytes / its mean event-timed
+            duration against the measured HBM copy bandwidth
+  e2e       the same metric with host (pinned) buffers, H2D and D2H in the
+            timed region
+  cpu_baseline  the fp64 CPU oracle timed on a bounded sample (rank 0, N=1)
+  decode    the decode workload (B=256, H=32, 1000 chained steps): HBM GB/s
+  workloads the full-CKDA and packed workloads (N=1): token-heads/s, roofline
+  clocks    SM clocks and throttle reasons sampled during the timed region
+--impl reference runs the fp64 oracle as the reference arm on the host cores.
+Under torchrun each rank runs its own replica (weak scaling, no collective on
+the data path); timing is max over ranks after a barrier.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "CKDA fwd tokens/s (B×T×H) at d=128 bf16 and % of roofline; decode HBM GB/s"
+UNIT = "tokens/s"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+FALLBACK_HBM_GBS = 6800.0
+
+
+def fwd_bytes(B, H, T, dk, dv, nseq, h0, hT, io_bytes=2):
+    th = B * H * T
+    b = th * ((3 * dk + 2 * dv) * io_bytes + io_bytes)
+    st = nseq * H * dk * dv * 4
+    return b + (st if h0 else 0) + (st if hT else 0)
+
+
+def decode_bytes(B, H, dk, dv, io_bytes=2):
+    return B * H * (2 * dk * dv * 4 + (3 * dk + 2 * dv) * io_bytes + io_bytes)
+
+
+def hbm_peak():
+    try:
+        p = json.load(open(PEAKS_FILE))
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_sources_sha():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "gated_delta_rule_ckda_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        if fn.endswith((".cu", ".cuh")):
+            h.update(fn.encode())
+            h.update(open(os.path.join(csrc, fn), "rb").read())
+    return h.hexdigest()
+
+
+def traffic_for(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel
+    sources are unchanged since it was taken; else None."""
+    try:
+        t = json.load(open(TRAFFIC_FILE))
+    except Exception:
+        return None
+    if t.get("kernel_sources_sha256") != kernel_sources_sha():
+        return None
+    e = t.get("kernels", {}).get(kernel, {}).get(workload)
+    return None if e is None else float(e["dram_bytes_per_launch"])
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons at 100 ms while running."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"ckda_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append((float(f[1]), float(f[2]), float(f[3]), f[5:9]))
+            except ValueError:
+                continue
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        load = [r for r in rows if r[2] > 250.0] or rows
+        sm = sorted(r[0] for r in load)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in load for i, v in enumerate(r[3]) if v == "Active"})
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows), "samples_under_load": len(load),
+                "power_w_max": max(r[2] for r in rows)}
+
+
+def dist_setup():
+    import torch
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, ws):
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------- our arm
+
+def time_steps(step_fn, steps, warmup, ws, stream):
+    """Runs warmup + timed steps; returns (total seconds max over ranks,
+    per-step event durations in ms)."""
+    import torch
+    for _ in range(warmup):
+        step_fn()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for a, b in evs:
+        a.record(stream)
+        step_fn()
+        b.record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    total = t0.elapsed_time(t1) / 1e3
+    per = [a.elapsed_time(b) for a, b in evs]
+    return max_over_ranks(total, ws), per
+
+
+def fwd_case(ck, x, steps, warmup, ws, stream, name):
+    import torch
+    d = x.to("cuda")
+    B, H, T, dk = d.q.shape
+    dv = d.v.shape[-1]
+    N = d.num_seqs
+    o = torch.empty_like(d.v)
+    hT = torch.empty((N, H, dk, dv), dtype=torch.float32, device="cuda")
+    wsp = ck.new_workspace(N if d.cu_seqlens is not None else 0, H, torch.device("cuda"))
+
+    def step():
+        ck.fwd(d.q, d.k, d.v, d.alpha, d.beta, d.h0, d.cu_seqlens, o=o, hT=hT,
+               workspace=wsp, stream=stream)
+
+    step()
+    st = ck.fwd_status(wsp)
+    if st != 0:
+        raise RuntimeError(f"{name}: device status {ck.STATUS.get(st, st)}")
+    total, per = time_steps(step, steps, warmup, ws, stream)
+    th = B * H * T
+    nbytes = fwd_bytes(B, H, T, dk, dv, N, d.h0 is not None, True)
+    launches = 2 if d.cu_seqlens is not None else 1
+    return dict(total=total, per=per, th=th, bytes=nbytes, launches=launches, dev=d, o=o, hT=hT,
+                wsp=wsp)
+
+
+def roofline(nbytes, per_ms, kernel, workload):
+    peak, src = hbm_peak()
+    mean_s = sum(per_ms) / len(per_ms) / 1e3
+    ach = nbytes / mean_s / 1e9
+    return {"bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(ach / peak, 4), "traffic": traffic_for(kernel, workload),
+            "algorithmic_bytes": nbytes, "mean_launch_ms": round(mean_s * 1e3, 4),
+            "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured"
+            else "fallback 6.8 TB/s"}
+
+
+def e2e_fwd(ck, x, steps, ws, stream):
+    """Host (pinned) inputs -> device, ckda_fwd, outputs -> host, all timed."""
+    import torch
+    B, H, T, dk = x.q.shape
+    dv = x.v.shape[-1]
+    N = x.num_seqs
+    hq, hk, hv, ha, hb = (t.pin_memory() for t in (x.q, x.k, x.v, x.alpha, x.beta))
+    dq, dk_, dv_, da, db = (torch.empty_like(t, device="cuda") for t in (hq, hk, hv, ha, hb))
+    o = torch.empty_like(dv_)
+    hT = torch.empty((N, H, dk, dv), dtype=torch.float32, device="cuda")
+    ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    hh = torch.empty(hT.shape, dtype=torch.float32).pin_memory()
+    wsp = ck.new_workspace(0, H, torch.device("cuda"))
+
+    def step():
+        for dst, src in ((dq, hq), (dk_, hk), (dv_, hv), (da, ha), (db, hb)):
+            dst.copy_(src, non_blocking=True)
+        ck.fwd(dq, dk_, dv_, da, db, None, o=o, hT=hT, workspace=wsp, stream=stream)
+        ho.copy_(o, non_blocking=True)
+        hh.copy_(hT, non_blocking=True)
+
+    total, _ = time_steps(step, steps, 2, ws, stream)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, ha, hb))
+    d2h = ho.numel() * ho.element_size() + hh.numel() * 4
+    return {"value": round(ws * B * H * T * steps / total, 1), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps}
+
+
+def decode_case(ck, steps, warmup, ws, stream, pool=32):
+    import torch
+    import synth
+    w = synth.WORKLOADS["ckda_decode"]
+    B, H, d = w["B"], w["H"], w["d"]
+    S = synth.make_decode_state(B, H, d, seed=w["seed"]).cuda()
+    ins = [tuple(t.cuda() for t in synth.make_decode_step(B, H, d, seed=w["seed"], step=i))
+           for i in range(pool)]
+    o = torch.empty((B, H, d), dtype=torch.bfloat16, device="cuda")
+    it = [0]
+
+    def step():
+        q, k, v, a, b = ins[it[0] % pool]
+        it[0] += 1
+        ck.decode_step(q, k, v, a, b, S, o=o, stream=stream)
+
+    total, per = time_steps(step, steps, warmup, ws, stream)
+    nbytes = decode_bytes(B, H, d, d)
+    rl = roofline(nbytes, per, "decode128", "ckda_decode")
+    return {"value": round(ws * nbytes * steps / total / 1e9, 1), "unit": "GB/s",
+            "steps": steps, "ms_per_step": round(total / steps * 1e3, 4),
+            "config": {"workload": "ckda_decode", "B": B, "H": H, "d": d,
+                       "inputs": f"pool of {pool} seeded steps cycled"},
+            "roofline": rl, "gpu_launches": steps}
+
+
+def cpu_baseline(x, target_s=12.0):
+    """The oracle, as it stands, on a bounded sample of the workload's units."""
+    import oracle
+    B, H, T, _ = x.q.shape
+    units = [(b, h) for b in range(B) for h in range(H)]
+    n = min(len(units), max(1, oracle.max_threads()))
+    t_used, th_done, reps = 0.0, 0, 0
+    while True:
+        sel = units[(reps * n) % len(units):][:n]
+        bs = sorted({b for b, _ in sel})
+        hs = sorted({h for _, h in sel})
+        sub = lambda t: t[bs][:, hs]
+        t0 = time.perf_counter()
+        oracle.fwd(sub(x.q), sub(x.k), sub(x.v), sub(x.alpha), sub(x.beta),
+                   None if x.h0 is None else sub(x.h0))
+        dt = time.perf_counter() - t0
+        t_used += dt
+        th_done += len(bs) * len(hs) * T
+        reps += 1
+        if t_used >= target_s or reps >= 50:
+            break
+        if dt < target_s / 8 and n < len(units):
+            n = min(len(units), n * 2)
+    return {"value": round(th_done / t_used, 1), "unit": UNIT, "cores": oracle.max_threads(),
+            "kind": "oracle",
+            "sample": f"{reps} runs over {th_done} token-heads (whole (batch, head) sequences of "
+                      f"T={T}) of the same workload, {t_used:.1f} s, fp64 C + OpenMP"}
+
+
+def run_ours(args):
+    import torch
+    import gated_delta_rule_ckda_gb300 as ck
+    import synth
+    ws, rank, local = dist_setup()
+    ck.lib()
+    stream = torch.cuda.current_stream()
+    name = args.workload
+    x = synth.make_workload(name)
+    clocks = ClockSampler(local)
+    clocks.start()
+    r = fwd_case(ck, x, args.steps, args.warmup, ws, stream, name)
+    clk = clocks.stop()
+    B, H, T, dk = x.q.shape
+    value = ws * r["th"] * args.steps / r["total"]
+    out = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(r["total"] / args.steps * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": name, "B": B, "H": H, "T": T, "dk": dk, "dv": x.v.shape[-1],
+                   "io": "bf16", "state": "fp32", "chunk": 64,
+                   "precision": "bf16 I/O; fp16/bf16 tensor-core operands; fp32 accumulation, "
+                                "gate products, T and state",
+                   "l2": "inputs larger than L2 (no flush)",
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+        "roofline": roofline(r["bytes"], r["per"], "fwd_chunk", name),
+        "gpu_launches": r["launches"] * args.steps,
+        "clocks": clk,
+    }
+    out["e2e"] = e2e_fwd(ck, x, max(3, min(args.steps, args.e2e_steps)), ws, stream)
+    if ws == 1 and not args.no_extras:
+        out["decode"] = decode_case(ck, args.decode_steps, 10, ws, stream)
+        wl = {}
+        for nm, steps in (("ckda_full", 20), ("ckda_varlen", 10)):
+            xx = synth.make_workload(nm)
+            rr = fwd_case(ck, xx, steps, 3, ws, stream, nm)
+            wl[nm] = {"value": round(rr["th"] * steps / rr["total"], 1), "unit": UNIT,
+                      "ms_per_step": round(rr["total"] / steps * 1e3, 4), "steps": steps,
+                      "token_heads": rr["th"],
+                      "roofline": roofline(rr["bytes"], rr["per"], "fwd_chunk", nm)}
+            del xx, rr
+        out["workloads"] = wl
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(x, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(out))
+
+
+# ----------------------------------------------------------- reference arm
+
+def run_reference(args):
+    """The fp64 oracle on the host cores, as the reference arm."""
+    import numpy as np  # noqa: F401
+    import oracle
+    import synth
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    name = args.workload
+    x = synth.make_workload(name)
+    B, H, T, dk = x.q.shape
+    budget = 150.0 / (args.steps + args.warmup)  # seconds per step
+    # one step: whole (batch, head) units, as many as fit the per-step budget
+    probe_t0 = time.perf_counter()
+    sub = lambda t, n: t[:1, :n]
+    oracle.fwd(sub(x.q, 1), sub(x.k, 1), sub(x.v, 1), sub(x.alpha, 1), sub(x.beta, 1))
+    per_unit = time.perf_counter() - probe_t0
+    cores = oracle.max_threads()
+    n_units = int(max(1, min(H, cores * max(1.0, budget / max(per_unit, 1e-6)))))
+    n_units = min(n_units, H)
+    Tm = T
+    if per_unit > budget:  # even one unit is too slow: shorten the sample
+        Tm = max(64, int(T * budget / per_unit))
+    args_ = [t[:1, :n_units, :Tm] for t in (x.q, x.k, x.v, x.alpha, x.beta)]
+    for _ in range(args.warmup):
+        oracle.fwd(*args_)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.fwd(*args_)
+    total = time.perf_counter() - t0
+    th = n_units * Tm * args.steps
+    value = th / total
+    out = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total / args.steps * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "impl": "reference",
+        "config": {"workload": name, "B": B, "H": H, "T": T, "dk": dk, "dv": x.v.shape[-1],
+                   "io": "bf16 inputs widened to fp64", "parallelism": "host cores"},
+        "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": cores,
+                         "kind": "oracle",
+                         "sample": f"each step: {n_units} (batch, head) units x {Tm} tokens of "
+                                   f"the {name} workload"},
+        "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="kda_range",
+                    choices=["kda_range", "ckda_full", "ckda_varlen"])
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--decode-steps", type=int, default=1000)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-extras", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

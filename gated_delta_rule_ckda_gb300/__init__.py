@@ -1,0 +1,192 @@
+"""Python binding of libckda -- the GB300 (sm_103a) Complex KDA recurrence.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of libckda.so (csrc/), called through its C ABI (include/ckda.h).
+PyTorch supplies device memory and streams.  There is no CPU or PyTorch
+fallback: if the library is missing or fails to load, every call raises.
+
+    o, hT = fwd(q, k, v, alpha, beta, h0=None, cu_seqlens=None, scale=1.0)
+    o = decode_step(q, k, v, alpha, beta, state)      # state updated in place
+
+Shapes follow the C ABI: q, k, alpha [B, H, T, dk]; v [B, H, T, dv];
+beta [B, H, T]; h0 / hT fp32 [N, H, dk, dv] with N = B, or the number of
+packed sequences when cu_seqlens (int32 [N + 1], B == 1) is given.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+__all__ = ["fwd", "decode_step", "fwd_status", "workspace_bytes", "selftest_timeout",
+           "lib", "library_path", "CkdaError", "STATUS"]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libckda.so")
+_lock = threading.Lock()
+_lib = None
+
+STATUS = {0: "CKDA_OK", 1: "CKDA_ERR_INVALID_ARG", 2: "CKDA_ERR_UNSUPPORTED",
+          3: "CKDA_ERR_CUDA", 4: "CKDA_ERR_TIMEOUT", 5: "CKDA_ERR_WORKSPACE",
+          6: "CKDA_ERR_RANGE"}
+_F32, _BF16 = 0, 1
+
+
+class CkdaError(RuntimeError):
+    def __init__(self, code, where):
+        self.code = int(code)
+        super().__init__(f"{where}: {STATUS.get(self.code, self.code)}")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def lib():
+    """The loaded libckda (ctypes.CDLL).  Raises if the library is not built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise ImportError(
+                    f"libckda.so is not built ({_LIB_PATH}); run "
+                    "`python -c 'import __graft_entry__ as g; g.build()'`")
+            L = ctypes.CDLL(_LIB_PATH)
+            vp, i32, sz, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_float
+            L.ckda_version.restype = i32
+            L.ckda_version.argtypes = []
+            L.ckda_status_string.restype = ctypes.c_char_p
+            L.ckda_status_string.argtypes = [i32]
+            L.ckda_fwd_workspace_bytes.restype = sz
+            L.ckda_fwd_workspace_bytes.argtypes = [i32, i32]
+            L.ckda_fwd.restype = i32
+            L.ckda_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32,
+                                   i32, i32, i32, i32, i32, i32, f32, i32, vp, sz, vp]
+            L.ckda_fwd_status.restype = i32
+            L.ckda_fwd_status.argtypes = [vp, vp]
+            L.ckda_decode_step.restype = i32
+            L.ckda_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, vp,
+                                           i32, i32, i32, i32, i32, f32, vp]
+            L.ckda_selftest_timeout.restype = i32
+            L.ckda_selftest_timeout.argtypes = [vp, sz, ctypes.c_uint, vp]
+            _lib = L
+    return _lib
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream, device):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _io_dtype(t):
+    if t.dtype == torch.bfloat16:
+        return _BF16
+    if t.dtype == torch.float32:
+        return _F32
+    raise TypeError(f"unsupported I/O dtype {t.dtype} (bf16 or fp32)")
+
+
+def _check(t, name, dtype, shape, device):
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: dtype {t.dtype}, expected {dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    if t.device != device:
+        raise ValueError(f"{name}: on {t.device}, expected {device}")
+
+
+def workspace_bytes(num_seqs: int, H: int) -> int:
+    return int(lib().ckda_fwd_workspace_bytes(int(num_seqs), int(H)))
+
+
+def new_workspace(num_seqs, H, device):
+    n = workspace_bytes(num_seqs, H)
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def fwd(q, k, v, alpha, beta, h0=None, cu_seqlens=None, scale=1.0, chunk_size=0,
+        store_final_state=True, o=None, hT=None, workspace=None, stream=None):
+    """Forward over [B, H, T, d] (or packed) inputs.  Returns (o, hT or None)."""
+    L = lib()
+    device = q.device
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    dt = q.dtype
+    _io_dtype(q)
+    for name, t, shp in (("q", q, (B, H, T, dk)), ("k", k, (B, H, T, dk)),
+                         ("alpha", alpha, (B, H, T, dk)), ("v", v, (B, H, T, dv)),
+                         ("beta", beta, (B, H, T))):
+        _check(t, name, dt, shp, device)
+    N = B
+    if cu_seqlens is not None:
+        N = cu_seqlens.numel() - 1
+        _check(cu_seqlens, "cu_seqlens", torch.int32, (N + 1,), device)
+    if h0 is not None:
+        _check(h0, "h0", torch.float32, (N, H, dk, dv), device)
+    if o is None:
+        o = torch.empty((B, H, T, dv), dtype=dt, device=device)
+    else:
+        _check(o, "o", dt, (B, H, T, dv), device)
+    if store_final_state and hT is None:
+        hT = torch.empty((N, H, dk, dv), dtype=torch.float32, device=device)
+    if hT is not None:
+        _check(hT, "hT", torch.float32, (N, H, dk, dv), device)
+    nseq_ws = N if cu_seqlens is not None else 0
+    if workspace is None:
+        workspace = new_workspace(nseq_ws, H, device)
+    rc = L.ckda_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(h0), _ptr(o),
+                    _ptr(hT), _ptr(cu_seqlens), int(N if cu_seqlens is not None else 0),
+                    B, H, T, dk, dv, _io_dtype(q), float(scale), int(chunk_size),
+                    _ptr(workspace), int(workspace.numel()), _stream_handle(stream, device))
+    if rc != 0:
+        raise CkdaError(rc, "ckda_fwd")
+    fwd.last_workspace = workspace
+    return o, hT
+
+
+def fwd_status(workspace, stream=None) -> int:
+    """Device status of the most recent call on `workspace` (synchronises)."""
+    return int(lib().ckda_fwd_status(_ptr(workspace), _stream_handle(stream, workspace.device)))
+
+
+def decode_step(q, k, v, alpha, beta, state, scale=1.0, o=None, stream=None):
+    """One token per (batch, head); `state` [B, H, dk, dv] fp32 is updated in place."""
+    L = lib()
+    device = q.device
+    B, H, dk = q.shape
+    dv = v.shape[-1]
+    dt = q.dtype
+    _io_dtype(q)
+    for name, t, shp in (("q", q, (B, H, dk)), ("k", k, (B, H, dk)), ("alpha", alpha, (B, H, dk)),
+                         ("v", v, (B, H, dv)), ("beta", beta, (B, H))):
+        _check(t, name, dt, shp, device)
+    _check(state, "state", torch.float32, (B, H, dk, dv), device)
+    if o is None:
+        o = torch.empty((B, H, dv), dtype=dt, device=device)
+    else:
+        _check(o, "o", dt, (B, H, dv), device)
+    rc = L.ckda_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(state),
+                            _ptr(o), B, H, dk, dv, _io_dtype(q), float(scale),
+                            _stream_handle(stream, device))
+    if rc != 0:
+        raise CkdaError(rc, "ckda_decode_step")
+    return o
+
+
+def selftest_timeout(workspace, spin_limit=1000, stream=None) -> int:
+    """Runs the bounded-wait self-test and returns the status it recorded."""
+    L = lib()
+    rc = L.ckda_selftest_timeout(_ptr(workspace), int(workspace.numel()), int(spin_limit),
+                                 _stream_handle(stream, workspace.device))
+    if rc != 0:
+        raise CkdaError(rc, "ckda_selftest_timeout")
+    return fwd_status(workspace, stream)

@@ -1,0 +1,83 @@
+// ckda_internal.cuh -- declarations shared by the translation units of libckda.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include "../../include/ckda.h"
+
+namespace ckda {
+
+// Workspace layout (bytes):
+//   [0, 4)        device status word (int32, a ckda_status; 0 = OK)
+//   [256, ...)    int32 order[num_seqs]: packed sequences, longest first
+constexpr size_t kWsStatusBytes = 256;
+
+// Records a device-side error; the first one wins.
+__device__ __forceinline__ void set_status(int* status, int code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+struct FwdArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* alpha;
+  const void* beta;
+  const float* h0;
+  void* o;
+  float* hT;
+  const int32_t* cu_seqlens;  // device, or nullptr
+  const int32_t* order;       // device work order (packed), or nullptr
+  int* status;                // device status word
+  int num_units_seq;          // N (sequences) -- dense: B
+  int B, H, T, dk, dv;
+  float scale;
+  ckda_dtype io;
+};
+
+// Token-serial CUDA-core forward (any dk, dv <= 128).
+cudaError_t launch_fwd_recurrent(const FwdArgs& a, cudaStream_t s);
+// Chunkwise tcgen05 forward (bf16 I/O, dk = dv = 128, chunk 64).
+cudaError_t launch_fwd_chunk(const FwdArgs& a, cudaStream_t s);
+// Longest-first order of packed sequences.
+cudaError_t launch_seq_order(const int32_t* cu, int n, int32_t* order, cudaStream_t s);
+
+struct DecodeArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* alpha;
+  const void* beta;
+  float* state;
+  void* o;
+  int B, H, dk, dv;
+  float scale;
+  ckda_dtype io;
+};
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
+
+cudaError_t launch_selftest_timeout(int* status, unsigned spin_limit, cudaStream_t s);
+
+// Element loads/stores in the I/O dtype.
+template <typename T>
+__device__ __forceinline__ float ld_io(const T* p);
+template <>
+__device__ __forceinline__ float ld_io<float>(const float* p) {
+  return *p;
+}
+template <>
+__device__ __forceinline__ float ld_io<__nv_bfloat16>(const __nv_bfloat16* p) {
+  return __bfloat162float(*p);
+}
+template <typename T>
+__device__ __forceinline__ void st_io(T* p, float x);
+template <>
+__device__ __forceinline__ void st_io<float>(float* p, float x) {
+  *p = x;
+}
+template <>
+__device__ __forceinline__ void st_io<__nv_bfloat16>(__nv_bfloat16* p, float x) {
+  *p = __float2bfloat16_rn(x);
+}
+
+}  // namespace ckda

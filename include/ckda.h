@@ -1,0 +1,152 @@
+/*
+ * ckda.h -- C ABI of libckda, a GB300 (sm_103a) implementation of the
+ * Complex KDA (CKDA) recurrence.
+ *
+ * The operation (one head of one sequence, state H in R^{dk x dv}, rows are
+ * key channels):
+ *
+ *     H_t = (I - beta_t k_t k_t^T) Diag(alpha_t) H_{t-1} + beta_t k_t v_t^T
+ *     o_t = H_t^T (scale * q_t)
+ *
+ * defined in "Complex KDA: Understanding and Enhancing the Expressivity of
+ * Kimi Delta Attention", Sec. 2 Eq. (1) and App. B.2 Eq. (9), with the
+ * ranges alpha_t in [-1, 1]^dk, beta_t in [0, 2] of Sec. 3 ("CKDA"), unit
+ * keys ||k_t|| = 1, and the readout of the updated state shown on the
+ * paper-discussion slides ("CKDA keeps the original gate--delta--readout
+ * structure").  The pages use no query scale: scale = 1 reproduces them.
+ *
+ * Conventions shared by every call:
+ *   - All tensor arguments are DEVICE pointers to contiguous row-major
+ *     arrays owned by the caller.  The library never allocates, frees or
+ *     synchronises device memory on these paths; every call is asynchronous
+ *     on `stream` (a cudaStream_t passed as void*, NULL = legacy default).
+ *   - Argument errors are detected on the host before anything is launched
+ *     and returned synchronously (CKDA_ERR_INVALID_ARG / _UNSUPPORTED).
+ *     A failed launch returns CKDA_ERR_CUDA.
+ *   - Device-side conditions (a bounded wait that ran out, an fp16 operand
+ *     that overflowed) are written to a status word in the caller's
+ *     workspace and read back with ckda_fwd_status().
+ *   - k is NOT normalised by the library: ||k_t|| = 1 is the caller's
+ *     precondition, as on the pages.  The library accepts any finite k.
+ */
+#ifndef CKDA_H
+#define CKDA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    CKDA_F32 = 0,   /* IEEE fp32 inputs and outputs */
+    CKDA_BF16 = 1   /* bfloat16 inputs and outputs; the state is always fp32 */
+} ckda_dtype;
+
+typedef enum {
+    CKDA_OK = 0,
+    CKDA_ERR_INVALID_ARG = 1,  /* null pointer, bad size, bad cu_seqlens shape */
+    CKDA_ERR_UNSUPPORTED = 2,  /* valid arguments outside what is implemented */
+    CKDA_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed */
+    CKDA_ERR_TIMEOUT = 4,      /* device: a bounded wait ran out (see ckda_fwd_status) */
+    CKDA_ERR_WORKSPACE = 5,    /* workspace missing or smaller than required */
+    CKDA_ERR_RANGE = 6         /* device: an fp16 tensor-core operand overflowed */
+} ckda_status;
+
+/* Version of this ABI: major * 10000 + minor * 100 + patch. */
+int ckda_version(void);
+
+/* Human-readable name of a status code (static storage; never NULL). */
+const char *ckda_status_string(ckda_status s);
+
+/*
+ * Workspace bytes ckda_fwd needs.  num_seqs is the number of packed
+ * sequences (cu_seqlens != NULL) or 0 for the dense layout.  The workspace
+ * holds the device status word and, for packed input, the longest-first
+ * work order of the sequences.  It is scratch: its contents on entry do not
+ * matter (each ckda_fwd first clears the status word on its stream) and
+ * calls that share one workspace must be stream-ordered.
+ */
+size_t ckda_fwd_workspace_bytes(int num_seqs, int H);
+
+/*
+ * Forward over a batch: computes o for every token and the final state of
+ * every (sequence, head).
+ *
+ * Layouts (io = io_dtype element type):
+ *   q, k, alpha : io   [B, H, T, dk]
+ *   v, o        : io   [B, H, T, dv]
+ *   beta        : io   [B, H, T]
+ *   h0, hT      : fp32 [N, H, dk, dv], N = B (dense) or num_seqs (packed)
+ *   cu_seqlens  : int32 [num_seqs + 1] device array, or NULL.  When given,
+ *                 B must be 1 and the sequences are packed along T:
+ *                 sequence n owns tokens [cu_seqlens[n], cu_seqlens[n+1]).
+ *                 The offsets must be non-decreasing with cu_seqlens[0] = 0
+ *                 and cu_seqlens[num_seqs] = T; they are read on the device
+ *                 and not validated there.
+ *   h0 == NULL  : zero initial state.   hT == NULL : final state not stored.
+ *   hT may alias h0 (each (sequence, head) reads its slice before writing).
+ *   o must not alias any input.
+ *
+ * Paths: io_dtype = CKDA_BF16 with dk = dv = 128 runs the chunkwise
+ * tensor-core kernel (chunk_size 0 or 64); every other supported shape
+ * (dk, dv <= 128) runs the token-serial CUDA-core kernel, which has no
+ * chunks (chunk_size 0, 16, 32 or 64 accepted and ignored; results never
+ * depend on it).  scale multiplies q.
+ *
+ * workspace / workspace_bytes: device scratch of at least
+ * ckda_fwd_workspace_bytes(cu_seqlens ? num_seqs : 0, H) bytes, 256-byte
+ * aligned.
+ *
+ * Returns CKDA_OK once the work is enqueued on `stream`.
+ */
+ckda_status ckda_fwd(const void *q, const void *k, const void *v,
+                     const void *alpha, const void *beta, const float *h0,
+                     void *o, float *hT, const int32_t *cu_seqlens, int num_seqs,
+                     int B, int H, int T, int dk, int dv, ckda_dtype io_dtype,
+                     float scale, int chunk_size, void *workspace,
+                     size_t workspace_bytes, void *stream);
+
+/*
+ * Reads (and clears) the device status word of a workspace: waits for
+ * `stream`, then returns CKDA_OK, CKDA_ERR_TIMEOUT or CKDA_ERR_RANGE for the
+ * most recent ckda_fwd (or self-test) enqueued with that workspace.
+ * Returns CKDA_ERR_CUDA if the copy or the stream failed.
+ */
+ckda_status ckda_fwd_status(void *workspace, void *stream);
+
+/*
+ * One decode step: applies one token to a resident state, in place.
+ * The update is the recurrence above with T = 1, computed as in "Kimi Delta
+ * Attention: a bounded case study" (worked case A/B: per-channel decay,
+ * read, correct) followed by the readout of the updated state.
+ *
+ *   q, k, alpha : io   [B, H, dk]
+ *   v, o        : io   [B, H, dv]
+ *   beta        : io   [B, H]
+ *   state       : fp32 [B, H, dk, dv], read and overwritten.
+ *
+ * dk = dv = 128 runs the vectorised bandwidth kernel; other dk, dv <= 128
+ * run the column-per-thread kernel.  Returns CKDA_OK once enqueued.
+ */
+ckda_status ckda_decode_step(const void *q, const void *k, const void *v,
+                             const void *alpha, const void *beta, float *state,
+                             void *o, int B, int H, int dk, int dv,
+                             ckda_dtype io_dtype, float scale, void *stream);
+
+/*
+ * Self-test of the bounded-wait path: launches one block that waits on a
+ * barrier nothing will complete, with a limit of about `spin_limit` polls,
+ * after which it records CKDA_ERR_TIMEOUT in the workspace's status word and
+ * returns.  It never hangs and never faults.  Read the result with
+ * ckda_fwd_status().
+ */
+ckda_status ckda_selftest_timeout(void *workspace, size_t workspace_bytes,
+                                  unsigned int spin_limit, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CKDA_H */

@@ -1,0 +1,109 @@
+"""Host-only checks of the C ABI: the library loads, exports every function
+include/ckda.h declares, and rejects bad arguments before launching anything.
+No call here reaches the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = []
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if not fn.endswith(".h"):
+            continue
+        src = open(os.path.join(ROOT, "include", fn)).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        names += re.findall(r"\b(ckda_\w+)\s*\(", src)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from gated_delta_rule_ckda_gb300 import build
+    build.build()
+    import gated_delta_rule_ckda_gb300 as ck
+    return ck.lib()
+
+
+def test_exports_every_declared_symbol(L):
+    names = declared_functions()
+    assert "ckda_fwd" in names and "ckda_decode_step" in names
+    for n in names:
+        assert hasattr(L, n), f"{n} declared in include/ but not exported"
+
+
+def test_status_strings_and_version(L):
+    assert L.ckda_version() == 10000
+    for code, name in [(0, b"CKDA_OK"), (1, b"CKDA_ERR_INVALID_ARG"), (4, b"CKDA_ERR_TIMEOUT"),
+                       (6, b"CKDA_ERR_RANGE")]:
+        assert L.ckda_status_string(code) == name
+    assert L.ckda_status_string(99) == b"CKDA_ERR_UNKNOWN"
+
+
+def test_workspace_bytes(L):
+    assert L.ckda_fwd_workspace_bytes(0, 16) == 256
+    assert L.ckda_fwd_workspace_bytes(64, 16) == 512
+    assert L.ckda_fwd_workspace_bytes(65, 16) == 768
+
+
+def _fwd(L, **kw):
+    a = dict(q=1, k=1, v=1, alpha=1, beta=1, h0=None, o=1, hT=None, cu=None, num_seqs=0,
+             B=1, H=1, T=4, dk=128, dv=128, io=1, scale=1.0, chunk=0, ws=None, wsb=0,
+             stream=None)
+    a.update(kw)
+    vp = ctypes.c_void_p
+    return L.ckda_fwd(vp(a["q"]), vp(a["k"]), vp(a["v"]), vp(a["alpha"]), vp(a["beta"]),
+                      vp(a["h0"]), vp(a["o"]), vp(a["hT"]), vp(a["cu"]), a["num_seqs"], a["B"],
+                      a["H"], a["T"], a["dk"], a["dv"], a["io"], a["scale"], a["chunk"],
+                      vp(a["ws"]), a["wsb"], vp(a["stream"]))
+
+
+def test_fwd_argument_errors_are_synchronous(L):
+    INV, UNS, WS = 1, 2, 5
+    assert _fwd(L, q=None) == INV
+    assert _fwd(L, o=None) == INV
+    assert _fwd(L, B=0) == INV
+    assert _fwd(L, H=0) == INV
+    assert _fwd(L, T=-1) == INV
+    assert _fwd(L, io=7) == INV
+    assert _fwd(L, scale=float("nan")) == INV
+    assert _fwd(L, cu=16, num_seqs=2, B=2) == INV        # packed needs B == 1
+    assert _fwd(L, cu=16, num_seqs=0) == INV             # packed needs >= 1 sequence
+    assert _fwd(L, num_seqs=3, B=2) == INV
+    assert _fwd(L, dk=129) == UNS
+    assert _fwd(L, dv=256) == UNS
+    assert _fwd(L, chunk=48) == UNS
+    assert _fwd(L, chunk=16) == UNS                       # tensor-core path is chunk 64
+    assert _fwd(L, ws=None) == WS
+    assert _fwd(L, ws=4096, wsb=16) == WS                 # too small
+    assert _fwd(L, ws=4096 + 8, wsb=4096) == WS          # misaligned
+    assert _fwd(L, q=8, ws=4096, wsb=4096) == INV         # TMA base not 16-byte aligned
+
+
+def test_decode_argument_errors_are_synchronous(L):
+    vp = ctypes.c_void_p
+    f = lambda **kw: L.ckda_decode_step(*(vp(kw.get(n, 1)) for n in
+                                          ("q", "k", "v", "alpha", "beta", "state", "o")),
+                                        kw.get("B", 1), kw.get("H", 1), kw.get("dk", 128),
+                                        kw.get("dv", 128), kw.get("io", 1), 1.0, vp(None))
+    assert f(state=None) == 1
+    assert f(B=0) == 1
+    assert f(dk=200) == 2
+    assert f(state=4) == 1  # misaligned state for the vectorised kernel
+    assert f(io=3) == 1
+
+
+def test_selftest_rejects_missing_workspace(L):
+    assert L.ckda_selftest_timeout(None, 0, 10, None) == 5
+
+
+def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    import gated_delta_rule_ckda_gb300 as ck
+    monkeypatch.setattr(ck, "_LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(ck, "_lib", None)
+    with pytest.raises(ImportError):
+        ck.lib()

@@ -1,0 +1,252 @@
+"""GPU parity of ckda_fwd (C ABI) against the fp64 oracle.
+
+Dense and packed inputs, both kernel paths (tensor-core chunkwise for bf16
+d = 128, token-serial CUDA-core otherwise), ragged tails, edge cases, and
+the five named workloads at full size (outputs of the packed workload are
+checked on a sample of sequences chosen to include the longest and shortest).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from metrics import excess_bf16, max_rel, report, rms_rel
+
+pytestmark = pytest.mark.gpu
+
+TOL_F32 = 1e-4
+TOL_BF16 = 2e-2
+
+
+@pytest.fixture(scope="module")
+def ck():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import gated_delta_rule_ckda_gb300 as ck
+    ck.lib()  # raises if the library is missing: no fallback
+    return ck
+
+
+def run_gpu(ck, x, scale=1.0, chunk_size=0, h0_on=True):
+    d = x.to("cuda")
+    o, hT = ck.fwd(d.q, d.k, d.v, d.alpha, d.beta, d.h0 if h0_on else None, d.cu_seqlens,
+                   scale=scale, chunk_size=chunk_size)
+    st = ck.fwd_status(ck.fwd.last_workspace)
+    torch.cuda.synchronize()
+    assert st == 0, f"device status {ck.STATUS.get(st, st)}"
+    return o.cpu(), hT.cpu()
+
+
+def run_oracle(x, scale=1.0, h0_on=True):
+    return oracle.fwd(x.q, x.k, x.v, x.alpha, x.beta, x.h0 if h0_on else None,
+                      cu_seqlens=x.cu_seqlens, scale=scale)
+
+
+def check(o, hT, o_ref, h_ref, bf16, name=""):
+    ro = report(name + " o", o, o_ref, bf16)
+    rh = report(name + " hT", hT, h_ref, False)
+    if bf16:
+        assert ro["excess_bf16"] <= TOL_BF16, ro
+        assert rh["max_rel"] <= TOL_BF16, rh
+        assert ro["rms_rel"] <= 5e-3, ro
+    else:
+        assert ro["max_rel"] <= TOL_F32, ro
+        assert rh["max_rel"] <= TOL_F32, rh
+
+
+# ----------------------------------------------------------------- workloads
+
+def test_tiny_fp32_workload(ck):
+    x = synth.make_workload("tiny_fp32")
+    o, hT = run_gpu(ck, x, chunk_size=16)
+    o_ref, h_ref = run_oracle(x)
+    check(o, hT, o_ref, h_ref, bf16=False, name="tiny_fp32")
+
+
+def test_kda_range_workload_full(ck):
+    x = synth.make_workload("kda_range")
+    o, hT = run_gpu(ck, x)
+    o_ref, h_ref = run_oracle(x)
+    check(o, hT, o_ref, h_ref, bf16=True, name="kda_range")
+
+
+def test_ckda_full_workload_full(ck):
+    x = synth.make_workload("ckda_full")
+    o, hT = run_gpu(ck, x)
+    o_ref, h_ref = run_oracle(x)
+    check(o, hT, o_ref, h_ref, bf16=True, name="ckda_full")
+
+
+def test_ckda_varlen_workload_sampled(ck):
+    """Full packed workload on the GPU; oracle on 8 sequences (longest, shortest
+    and 6 more), compared element by element."""
+    x = synth.make_workload("ckda_varlen")
+    o, hT = run_gpu(ck, x)
+    cu = x.cu_seqlens.numpy()
+    lens = np.diff(cu)
+    order = np.argsort(-lens, kind="stable")
+    pick = sorted(set([int(order[0]), int(order[-1])] + [int(i) for i in order[1:-1:9]][:6]))
+    for s in pick:
+        a, b = int(cu[s]), int(cu[s + 1])
+        sl = lambda t: t[:, :, a:b]
+        o_ref, h_ref = oracle.fwd(sl(x.q), sl(x.k), sl(x.v), sl(x.alpha), sl(x.beta))
+        check(o[:, :, a:b], hT[s:s + 1], o_ref, h_ref, bf16=True, name=f"varlen seq {s} L={b - a}")
+
+
+# --------------------------------------------------- tensor-core path, small
+
+@pytest.mark.parametrize("T", [1, 5, 63, 64, 65, 130, 257])
+def test_chunk_path_ragged(ck, T):
+    x = synth.make_fwd(2, 3, T, 128, dist="ckda", dtype="bf16", h0=True, seed=100 + T)
+    o, hT = run_gpu(ck, x)
+    o_ref, h_ref = run_oracle(x)
+    check(o, hT, o_ref, h_ref, bf16=True, name=f"chunk T={T}")
+
+
+@pytest.mark.parametrize("dist", ["uniform", "kda", "ckda"])
+def test_chunk_path_gate_families(ck, dist):
+    x = synth.make_fwd(1, 4, 300, 128, dist=dist, dtype="bf16", h0=True, seed=7)
+    o, hT = run_gpu(ck, x, scale=0.5)
+    o_ref, h_ref = run_oracle(x, scale=0.5)
+    check(o, hT, o_ref, h_ref, bf16=True, name=f"chunk {dist}")
+
+
+def test_chunk_path_degenerate_gates(ck):
+    """alpha = 0 everywhere (state erased each token), alpha = -1 everywhere
+    with beta = 2 (signed Householder products), beta = 0 (pure decay)."""
+    base = synth.make_fwd(1, 2, 150, 128, dist="ckda", dtype="bf16", h0=True, seed=9)
+    for name, a, b in [("alpha0", torch.zeros_like(base.alpha), base.beta),
+                       ("alpha-1_beta2", -torch.ones_like(base.alpha),
+                        torch.full_like(base.beta, 2.0)),
+                       ("beta0", base.alpha, torch.zeros_like(base.beta)),
+                       ("alpha1_beta0", torch.ones_like(base.alpha), torch.zeros_like(base.beta))]:
+        x = synth.FwdInputs(base.q, base.k, base.v, a, b, base.h0, None)
+        o, hT = run_gpu(ck, x)
+        o_ref, h_ref = run_oracle(x)
+        check(o, hT, o_ref, h_ref, bf16=True, name=name)
+
+
+def test_chunk_path_no_h0_no_hT(ck):
+    x = synth.make_fwd(2, 2, 100, 128, dist="ckda", dtype="bf16", h0=False, seed=11)
+    d = x.to("cuda")
+    o, hT = ck.fwd(d.q, d.k, d.v, d.alpha, d.beta, None, store_final_state=False)
+    assert hT is None
+    o_ref, _ = run_oracle(x)
+    assert excess_bf16(o.cpu(), o_ref) <= TOL_BF16
+
+
+def test_hT_may_alias_h0(ck):
+    x = synth.make_fwd(1, 3, 90, 128, dist="ckda", dtype="bf16", h0=True, seed=12)
+    d = x.to("cuda")
+    st = d.h0.clone()
+    o, hT = ck.fwd(d.q, d.k, d.v, d.alpha, d.beta, st, hT=st)
+    torch.cuda.synchronize()
+    o_ref, h_ref = run_oracle(x)
+    assert max_rel(st.cpu(), h_ref) <= TOL_BF16
+
+
+def test_empty_sequence_dense(ck):
+    x = synth.make_fwd(2, 2, 0, 128, dist="ckda", dtype="bf16", h0=True, seed=13)
+    o, hT = run_gpu(ck, x)
+    assert o.numel() == 0
+    assert torch.equal(hT, x.h0)
+
+
+def test_packed_with_empty_and_short_sequences(ck):
+    lengths = [0, 1, 64, 200, 0, 65, 3]
+    x = synth.make_varlen(lengths, 3, 128, dist="ckda", dtype="bf16", h0=True, seed=14)
+    o, hT = run_gpu(ck, x)
+    o_ref, h_ref = run_oracle(x)
+    check(o, hT, o_ref, h_ref, bf16=True, name="packed edge")
+
+
+def test_packed_equals_separate_calls(ck):
+    lengths = [70, 1, 129, 64]
+    x = synth.make_varlen(lengths, 2, 128, dist="ckda", dtype="bf16", h0=True, seed=15)
+    o, hT = run_gpu(ck, x)
+    cu = x.cu_seqlens.tolist()
+    for s in range(len(lengths)):
+        a, b = cu[s], cu[s + 1]
+        xs = synth.FwdInputs(*(t[:, :, a:b].contiguous() for t in (x.q, x.k, x.v, x.alpha, x.beta)),
+                             x.h0[s:s + 1].contiguous(), None)
+        o1, h1 = run_gpu(ck, xs)
+        # same kernel, same unit, same chunk boundaries: bit-identical
+        assert torch.equal(o1, o[:, :, a:b])
+        assert torch.equal(h1, hT[s:s + 1])
+
+
+def test_resume_split(ck):
+    """fwd(T) == fwd(T1) then fwd(T - T1, h0 = hT1) within the tolerance
+    (bit-identical when T1 is a multiple of the chunk)."""
+    x = synth.make_fwd(1, 2, 320, 128, dist="ckda", dtype="bf16", h0=True, seed=16)
+    o, hT = run_gpu(ck, x)
+    for T1 in (128, 100):
+        p1 = synth.FwdInputs(*(t[:, :, :T1].contiguous() for t in (x.q, x.k, x.v, x.alpha, x.beta)),
+                             x.h0, None)
+        o1, h1 = run_gpu(ck, p1)
+        p2 = synth.FwdInputs(*(t[:, :, T1:].contiguous() for t in (x.q, x.k, x.v, x.alpha, x.beta)),
+                             h1, None)
+        o2, h2 = run_gpu(ck, p2)
+        oc = torch.cat([o1, o2], dim=2)
+        if T1 % 64 == 0:
+            assert torch.equal(oc, o) and torch.equal(h2, hT)
+        else:
+            assert excess_bf16(oc, o.double()) <= TOL_BF16
+            assert max_rel(h2, hT) <= TOL_BF16
+
+
+def test_deterministic(ck):
+    x = synth.make_fwd(2, 4, 200, 128, dist="ckda", dtype="bf16", h0=True, seed=17)
+    o1, h1 = run_gpu(ck, x)
+    o2, h2 = run_gpu(ck, x)
+    assert torch.equal(o1, o2) and torch.equal(h1, h2)
+
+
+# ------------------------------------------------- token-serial CUDA-core path
+
+@pytest.mark.parametrize("d", [16, 32, 64, 128])
+def test_recurrent_path_fp32(ck, d):
+    x = synth.make_fwd(2, 2, 77, d, dist="ckda", dtype="fp32", h0=True, seed=200 + d)
+    o, hT = run_gpu(ck, x, scale=0.7)
+    o_ref, h_ref = run_oracle(x, scale=0.7)
+    check(o, hT, o_ref, h_ref, bf16=False, name=f"fp32 d={d}")
+
+
+def test_recurrent_path_bf16_d64_and_rectangular(ck):
+    x = synth.make_fwd(2, 2, 90, 64, dist="ckda", dtype="bf16", h0=True, seed=300)
+    o, hT = run_gpu(ck, x)
+    o_ref, h_ref = run_oracle(x)
+    check(o, hT, o_ref, h_ref, bf16=True, name="bf16 d=64")
+    x = synth.make_fwd(1, 2, 40, 32, dv=48, dist="uniform", dtype="fp32", h0=True, seed=301)
+    o, hT = run_gpu(ck, x)
+    o_ref, h_ref = run_oracle(x)
+    check(o, hT, o_ref, h_ref, bf16=False, name="fp32 dk=32 dv=48")
+
+
+def test_recurrent_packed_fp32(ck):
+    x = synth.make_varlen([5, 0, 33, 17], 2, 16, dist="uniform", dtype="fp32", h0=True, seed=302)
+    o, hT = run_gpu(ck, x)
+    o_ref, h_ref = run_oracle(x)
+    check(o, hT, o_ref, h_ref, bf16=False, name="fp32 packed")
+
+
+# ------------------------------------------------------------ device status
+
+def test_bounded_wait_reports_timeout(ck):
+    ws = ck.new_workspace(0, 1, torch.device("cuda"))
+    assert ck.selftest_timeout(ws, spin_limit=2000) == 4  # CKDA_ERR_TIMEOUT
+    # the status word is cleared by the read and the context is still usable
+    assert ck.fwd_status(ws) == 0
+    x = synth.make_fwd(1, 1, 10, 128, dist="ckda", dtype="bf16", h0=False, seed=1)
+    run_gpu(ck, x)
+
+
+def test_fp16_range_overflow_is_reported(ck):
+    """v far outside the fp16 range makes U overflow its fp16 operand; the
+    kernel must report CKDA_ERR_RANGE rather than return silently."""
+    x = synth.make_fwd(1, 1, 64, 128, dist="kda", dtype="bf16", h0=False, seed=18)
+    d = x.to("cuda")
+    v = (d.v.float() * 1e6).to(torch.bfloat16)
+    ck.fwd(d.q, d.k, v, d.alpha, d.beta)
+    assert ck.fwd_status(ck.fwd.last_workspace) == 6  # CKDA_ERR_RANGE
