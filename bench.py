@@ -348,10 +348,14 @@ def run_ours(args):
         "clocks": clk,
     }
     out["e2e"] = e2e_fwd(ck, x, max(3, min(args.steps, args.e2e_steps)), ws, stream)
-    if ws == 1 and not args.no_extras:
+    extras = [] if args.no_extras else [e for e in args.extras.split(",") if e and e != "none"]
+    if ws == 1 and "decode" in extras:
         out["decode"] = decode_case(ck, args.decode_steps, 10, ws, stream)
+    if ws == 1 and any(e in extras for e in ("ckda_full", "ckda_varlen")):
         wl = {}
         for nm, steps in (("ckda_full", 20), ("ckda_varlen", 10)):
+            if nm not in extras:
+                continue
             xx = synth.make_workload(nm)
             rr = fwd_case(ck, xx, steps, 3, ws, stream, nm)
             wl[nm] = {"value": round(rr["th"] * steps / rr["total"], 1), "unit": UNIT,
@@ -431,6 +435,8 @@ def main():
     ap.add_argument("--decode-steps", type=int, default=1000)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-extras", action="store_true")
+    ap.add_argument("--extras", default="decode,ckda_full,ckda_varlen",
+                    help="comma list of extra measurements: decode, ckda_full, ckda_varlen")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -27,15 +27,23 @@
 // first separated at tree level L lies in one aligned segment of 2L tokens
 // with s in the lower and t in the upper half, and with m the last position
 // of the lower half Gamma(t<-s) = [prod_{m<r<=t} alpha_r][prod_{s<r<=m}
-// alpha_r]; every level is then one dense contraction of gated operands on
-// the tensor cores.  Two levels share one 128 x 64 MMA tile (3 rounds).
+// alpha_r]: a prefix product within an aligned block of L tokens times an
+// exclusive suffix product within one.  Every level is one dense contraction
+// of gated operands on the tensor cores; two levels share a 128 x 64 MMA tile.
 //
 // Precision: operands of every contraction that touches the state, the
 // Grams and A are fp16 (11-bit significand); T Diag(beta), k * gamma and the
-// raw bf16 inputs are bf16; all accumulation is fp32 in TMEM, T is fp32.
+// raw bf16 inputs are bf16; all accumulation is fp32 in TMEM, gate products
+// and T are fp32.  An fp16 overflow is reported as CKDA_ERR_RANGE.
 //
-// This version runs the phases of a chunk one after another with all 256
-// threads cooperating between barriers; one thread issues every MMA.
+// Warp roles (384 threads):
+//   warps 0-7  PREP: per chunk, gate products, gated Grams, T, W and the
+//              operands of the state step; thread (j, tq) owns channels
+//              8j..8j+7 of tokens 4tq..4tq+3.  Prep of chunk c+1 runs while
+//              the state warps step chunk c.
+//   warps 8-11 STATE: the serial state step on TMEM (thread = TMEM lane = j).
+// Handoffs use release/acquire counters in shared memory; MMA and TMA
+// completion use mbarriers.  Every wait is bounded.
 #include "ckda_internal.cuh"
 #include "sm103.cuh"
 
@@ -46,34 +54,42 @@ namespace ckda {
 namespace {
 
 constexpr int C = 64;
-constexpr int NT = 256;
+constexpr int NPREP = 256;
+constexpr int NSTATE = 128;
+constexpr int NT = NPREP + NSTATE;
+constexpr int BAR_PREP = 1;   // named barrier ids
+constexpr int BAR_STATE = 2;
 
 // ---- shared memory map (bytes from a 1024-aligned base) ----
-constexpr uint32_t S_TQ = 0;        // bf16 q tile     [64 t][128 i]  (TMA)
-constexpr uint32_t S_TK = 16384;    // bf16 k tile
-constexpr uint32_t S_TA = 32768;    // bf16 alpha tile
-constexpr uint32_t S_TV = 49152;    // bf16 v tile     [64 s][128 j]  (MN-major A of U~)
-constexpr uint32_t S_KH = 65536;    // fp16 K^ = (k*rho)^T  [128 i][64 s]  B of H-MMA
-constexpr uint32_t S_WM = 81920;    // fp16 -W          [64 t][128 i]  B of U-MMA
-constexpr uint32_t S_AQ = 98304;    // fp16 A           [64 t][64 s]   B of O-MMA
-constexpr uint32_t S_TB = 106496;   // bf16 T Diag(beta)[64 t][64 s]   B of W/U~
-constexpr uint32_t S_GB = 114688;   // 48 KiB scratch, reused within a chunk:
-constexpr uint32_t S_GX = S_GB;            //   Gram X  fp16 [128 rows][128 i]
-constexpr uint32_t S_GY = S_GB + 32768;    //   Gram Y  fp16 [64 rows][128 i]
-constexpr uint32_t S_TF = S_GB;            //   T       fp32 [64][64]
-constexpr uint32_t S_KGT = S_GB + 16384;   //   (k*gamma)^T bf16 [128 i][64 s]  A of W-MMA
-constexpr uint32_t S_QG = S_GB + 32768;    //   q*gamma fp16 [64 t][128 i]  B of O-MMA
-constexpr uint32_t S_RT = S_GB + 32768;    //   T-inverse temporaries (before q*gamma)
-constexpr uint32_t S_HT = 163840;   // fp16 H^T         [128 j][128 i]  A of U/O
-constexpr uint32_t S_UT = 196608;   // fp16 U^T         [128 j][64 s]   A of O/H
-constexpr uint32_t S_MF = S_UT;     //   M fp32 [64][64] while the Grams are assembled
-constexpr uint32_t S_SMALL = 212992;
-constexpr uint32_t S_BETA = S_SMALL;          // fp32 [64]
-constexpr uint32_t S_GC = S_SMALL + 256;      // fp32 [128] gamma_C
-constexpr uint32_t S_BAR = S_SMALL + 768;     // mbarriers
-constexpr uint32_t S_MISC = S_SMALL + 832;    // tmem base, abort flag
-constexpr uint32_t SMEM_USED = S_SMALL + 1024;
-constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;  // + alignment slack
+constexpr uint32_t S_V = 0;          // bf16 v tile   [64 s][128 j]  MN-major A of U~   (TMA)
+constexpr uint32_t S_HT = 16384;     // fp16 H^T      [128 j][128 i] K-major A of U, O
+constexpr uint32_t S_UT = 49152;     // fp16 U^T      [128 j][64 s]  K-major A of H, O
+constexpr uint32_t S_TB = 65536;     // bf16 T Diag(beta) [64 t][64 s] K-major B of U~, W
+constexpr uint32_t S_W = 73728;      // fp16 -W^T     [128 i][64 t]  MN-major B of U
+constexpr uint32_t S_QG = 90112;     // fp16 q*gamma  [64 t][128 i]  K-major B of O
+constexpr uint32_t S_KH = 106496;    // fp16 k*rho    [64 s][128 i]  MN-major B of H
+constexpr uint32_t S_KGT = 122880;   // bf16 k*gamma  [64 s][128 i]  MN-major A of W
+constexpr uint32_t S_AQ = 139264;    // fp16 A        [64 t][64 s]   K-major B of O   (x2)
+constexpr uint32_t S_GX = 155648;    // fp16 Gram X   [128 rows][128 i] K-major A
+constexpr uint32_t S_GY = 188416;    // fp16 Gram Y   [64 rows][128 i]  K-major B
+// after the Gram MMAs the 48 KiB of X and Y hold the inverse's 64 x 64 tiles
+// (fp16, one 64-column panel each).  A tile read as a 128-row A operand also
+// reads the 8 KiB after it; those rows only feed TMEM lanes that are ignored.
+constexpr uint32_t S_TN = S_GX;              // N: block-strictly-lower part of M
+constexpr uint32_t S_TD = S_GX + 8192;       // D: inverses of the 16 x 16 diagonal blocks
+constexpr uint32_t S_TE = S_GX + 16384;      // E = D N
+constexpr uint32_t S_TG = S_GX + 24576;      // G = I + E^2
+constexpr uint32_t S_TFm = S_GY;             // F = (I - E) G
+constexpr uint32_t S_MD = S_GY + 8192;       // fp32 diagonal 16 x 16 blocks of M [4][16][20]
+constexpr int kMdRow = 20, kMdBlk = 16 * kMdRow;  // padded rows spread the banks
+constexpr uint32_t S_SMALL = 204800;
+constexpr uint32_t S_BETA = S_SMALL;         // fp32 [2][64]
+constexpr uint32_t S_GC = S_SMALL + 512;     // fp32 [2][128] gamma_C
+constexpr uint32_t S_DIAG = S_SMALL + 1536;  // fp32 [16][64] partial q.k
+constexpr uint32_t S_BAR = S_SMALL + 5632;   // mbarriers and counters
+constexpr uint32_t SMEM_USED = S_SMALL + 5888;
+constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;
+static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
 
 // ---- tensor memory columns ----
 constexpr uint32_t T_H = 0;     // H^T fp32 [128 j][128 i]
@@ -83,144 +99,10 @@ constexpr uint32_t T_G = 256;   // 3 Gram tiles [128 x][64 y]
 constexpr uint32_t T_W = 448;   // W^T fp32 [128 i][64 t]
 constexpr uint32_t TMEM_COLS = 512;
 
-constexpr uint32_t TILE_BYTES = 16384;
-
-__device__ __forceinline__ float bf16_at(const uint8_t* tile, int r, int c) {
-  return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(tile + sw128_off(64, r, c)));
-}
-__device__ __forceinline__ float2 bf16x2_at(const uint8_t* tile, int r, int c) {
-  __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(tile + sw128_off(64, r, c));
-  return __bfloat1622float2(v);
-}
-__device__ __forceinline__ bool fp16_ok(float x) { return fabsf(x) <= 65504.f; }
-
-// Builds the Gram operands of one round: levels La (X rows 0..63, Y rows
-// 0..31) and La/2 (X rows 64..127, Y rows 32..63).  X rows per level: 32
-// k-rows then 32 q-rows of the upper-half tokens; Y rows: the lower-half tokens.
-__device__ void build_gram_operands(uint8_t* sm, int La, int lenc) {
-  const int tid = threadIdx.x, cp = tid & 63, grp = tid >> 6;
-  const int c0 = 2 * cp;
-  const uint8_t* tq = sm + S_TQ;
-  const uint8_t* tk = sm + S_TK;
-  const uint8_t* ta = sm + S_TA;
-  const int L = (grp & 1) ? La / 2 : La;
-  if (grp < 2) {
-    uint8_t* X = sm + S_GX;
-    const int xbase = (grp & 1) ? 64 : 0;
-    for (int sg = 0; sg < 32 / L; ++sg) {
-      float f0 = 1.f, f1 = 1.f;
-      for (int w = 0; w < L; ++w) {
-        const int t = sg * 2 * L + L + w;
-        float2 a = t < lenc ? bf16x2_at(ta, t, c0) : make_float2(1.f, 1.f);
-        f0 *= a.x;
-        f1 *= a.y;
-        const float2 kk = bf16x2_at(tk, t, c0);
-        const float2 qq = bf16x2_at(tq, t, c0);
-        const int rk = xbase + sg * L + w;
-        *reinterpret_cast<uint32_t*>(X + sw128_off(128, rk, c0)) = pack_half2(kk.x * f0, kk.y * f1);
-        *reinterpret_cast<uint32_t*>(X + sw128_off(128, rk + 32, c0)) =
-            pack_half2(qq.x * f0, qq.y * f1);
-      }
-    }
-  } else {
-    uint8_t* Y = sm + S_GY;
-    const int ybase = (grp & 1) ? 32 : 0;
-    for (int sg = 0; sg < 32 / L; ++sg) {
-      float b0 = 1.f, b1 = 1.f;
-      for (int w = L - 1; w >= 0; --w) {
-        const int s = sg * 2 * L + w;
-        const float2 kk = bf16x2_at(tk, s, c0);
-        *reinterpret_cast<uint32_t*>(Y + sw128_off(64, ybase + sg * L + w, c0)) =
-            pack_half2(kk.x * b0, kk.y * b1);
-        float2 a = s < lenc ? bf16x2_at(ta, s, c0) : make_float2(1.f, 1.f);
-        b0 *= a.x;
-        b1 *= a.y;
-      }
-    }
-  }
-}
-
-// Reads Gram round r out of TMEM into M (fp32, scaled by beta_t) and A (fp16).
-__device__ void extract_gram(uint8_t* sm, uint32_t tmem, int r) {
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int x = 32 * (warp & 3) + lane;  // X row = TMEM lane
-  const int half = warp >> 2;
-  const int La = 32 >> (2 * r);
-  const bool lvb = x >= 64;
-  const int L = lvb ? La / 2 : La;
-  const int xr = x & 63;
-  const bool qrow = xr >= 32;
-  const int jx = xr & 31;
-  const int t = (jx / L) * 2 * L + L + (jx % L);
-  const uint32_t col0 = T_G + 64 * r + (lvb ? 32 : 0) + 16 * half;
-  uint32_t v[16];
-  tmem_ld32<16>(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + col0, v);
-  tmem_ld_wait();
-  const float* beta = reinterpret_cast<const float*>(sm + S_BETA);
-  float* Mf = reinterpret_cast<float*>(sm + S_MF);
-  uint8_t* AQ = sm + S_AQ;
-#pragma unroll
-  for (int cc = 0; cc < 16; ++cc) {
-    const int jy = 16 * half + cc;
-    if (jy / L != jx / L) continue;
-    const int s = (jy / L) * 2 * L + (jy % L);
-    const float g = __uint_as_float(v[cc]);
-    if (qrow)
-      *reinterpret_cast<__half*>(AQ + sw128_off(64, t, s)) = __float2half_rn(g);
-    else
-      Mf[t * 64 + s] = beta[t] * g;
-  }
-}
-
-// T = (I + M)^-1 for the strictly lower M (fp32), by 16 x 16 blocks:
-// diagonal blocks by forward substitution, then block rows by distance.
-__device__ void invert_unit_lower(uint8_t* sm) {
-  const int tid = threadIdx.x;
-  const float* Mf = reinterpret_cast<const float*>(sm + S_MF);
-  float* Tf = reinterpret_cast<float*>(sm + S_TF);
-  float* R = reinterpret_cast<float*>(sm + S_RT);
-  if (tid < 64) {
-    const int blk = tid >> 4, c = tid & 15, o = 16 * blk;
-    float x[16];
-#pragma unroll
-    for (int t = 0; t < 16; ++t) {
-      float acc = (t == c) ? 1.f : 0.f;
-#pragma unroll
-      for (int s = 0; s < t; ++s) acc = fmaf(-Mf[(o + t) * 64 + o + s], x[s], acc);
-      x[t] = acc;
-    }
-#pragma unroll
-    for (int t = 0; t < 16; ++t) Tf[(o + t) * 64 + o + c] = x[t];
-  }
-  __syncthreads();
-  for (int d = 1; d < 4; ++d) {
-    const int nb = 4 - d;
-    for (int e = tid; e < nb * 256; e += NT) {
-      const int J = e >> 8, I = J + d, a = (e >> 4) & 15, b = e & 15;
-      float acc = 0.f;
-      for (int K = J; K < I; ++K)
-#pragma unroll
-        for (int m = 0; m < 16; ++m)
-          acc = fmaf(Mf[(16 * I + a) * 64 + 16 * K + m], Tf[(16 * K + m) * 64 + 16 * J + b], acc);
-      R[e] = acc;
-    }
-    __syncthreads();
-    for (int e = tid; e < nb * 256; e += NT) {
-      const int J = e >> 8, I = J + d, a = (e >> 4) & 15, b = e & 15;
-      float acc = 0.f;
-#pragma unroll
-      for (int m = 0; m < 16; ++m)
-        acc = fmaf(Tf[(16 * I + a) * 64 + 16 * I + m], R[(J << 8) + (m << 4) + b], acc);
-      Tf[(16 * I + a) * 64 + 16 * J + b] = -acc;
-    }
-    __syncthreads();
-  }
-}
-
 struct Unit {
   long row0;
   int len;
-  size_t sidx;  // offset of this unit's state in h0/hT (elements)
+  size_t sidx;
 };
 
 __device__ __forceinline__ Unit unit_of(const FwdArgs& a) {
@@ -241,34 +123,345 @@ __device__ __forceinline__ Unit unit_of(const FwdArgs& a) {
   return u;
 }
 
+__device__ __forceinline__ void unpack_bf16x8(const uint4& v, float (&f)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+__device__ __forceinline__ uint4 pack_half8(const float (&f)[8]) {
+  return make_uint4(pack_half2(f[0], f[1]), pack_half2(f[2], f[3]), pack_half2(f[4], f[5]),
+                    pack_half2(f[6], f[7]));
+}
+__device__ __forceinline__ uint4 pack_bf8(const float (&f)[8]) {
+  return make_uint4(pack_bf162(f[0], f[1]), pack_bf162(f[2], f[3]), pack_bf162(f[4], f[5]),
+                    pack_bf162(f[6], f[7]));
+}
+// bf16 x 8 -> fp16 x 8 (through fp32; exact in the fp16 normal range)
+__device__ __forceinline__ uint4 bf16x8_to_half8(const uint4& v) {
+  float f[8];
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+  return make_uint4(pack_half2(f[0], f[1]), pack_half2(f[2], f[3]), pack_half2(f[4], f[5]),
+                    pack_half2(f[6], f[7]));
+}
+// x (fp16 x 8) times the gate factors f (fp32 x 8, rounded to fp16) -> fp16 x 8
+__device__ __forceinline__ uint4 hmul8(const uint4& x, const float (&f)[8]) {
+  const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+  uint32_t r[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __half2 a = *reinterpret_cast<const __half2*>(&xs[i]);
+    const __half2 b = __floats2half2_rn(f[2 * i], f[2 * i + 1]);
+    const __half2 p = __hmul2(a, b);
+    r[i] = *reinterpret_cast<const uint32_t*>(&p);
+  }
+  return make_uint4(r[0], r[1], r[2], r[3]);
+}
+// elementwise product of two fp16 x 8 vectors
+__device__ __forceinline__ uint4 hmul8h(const uint4& x, const uint4& y) {
+  uint4 r;
+  const __half2 p0 = __hmul2(*reinterpret_cast<const __half2*>(&x.x), *reinterpret_cast<const __half2*>(&y.x));
+  const __half2 p1 = __hmul2(*reinterpret_cast<const __half2*>(&x.y), *reinterpret_cast<const __half2*>(&y.y));
+  const __half2 p2 = __hmul2(*reinterpret_cast<const __half2*>(&x.z), *reinterpret_cast<const __half2*>(&y.z));
+  const __half2 p3 = __hmul2(*reinterpret_cast<const __half2*>(&x.w), *reinterpret_cast<const __half2*>(&y.w));
+  r.x = *reinterpret_cast<const uint32_t*>(&p0);
+  r.y = *reinterpret_cast<const uint32_t*>(&p1);
+  r.z = *reinterpret_cast<const uint32_t*>(&p2);
+  r.w = *reinterpret_cast<const uint32_t*>(&p3);
+  return r;
+}
+__device__ __forceinline__ uint4 to_half8(const float (&f)[8]) {
+  return make_uint4(pack_half2(f[0], f[1]), pack_half2(f[2], f[3]), pack_half2(f[4], f[5]),
+                    pack_half2(f[6], f[7]));
+}
+// fp16 x 8 -> bf16 x 8
+__device__ __forceinline__ uint4 half8_to_bf8(const uint4& v) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t r[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 t = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+    r[i] = pack_bf162(t.x, t.y);
+  }
+  return make_uint4(r[0], r[1], r[2], r[3]);
+}
+__device__ __forceinline__ float absmax8(const float (&f)[8]) {
+  float m = 0.f;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(f[e]));
+  return m;
+}
+__device__ __forceinline__ void unpack_half8(const uint4& v, float (&f)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 t = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
+}
+// true iff no lane of an fp16 x 8 vector is inf or NaN
+__device__ __forceinline__ bool half8_finite(const uint4& v) {
+  const uint32_t m = 0x7c007c00u;
+  return ((v.x & m) != m) && ((v.y & m) != m) && ((v.z & m) != m) && ((v.w & m) != m) &&
+         (((v.x >> 10) & 0x1f) != 0x1f) && (((v.x >> 26) & 0x1f) != 0x1f) &&
+         (((v.y >> 10) & 0x1f) != 0x1f) && (((v.y >> 26) & 0x1f) != 0x1f) &&
+         (((v.z >> 10) & 0x1f) != 0x1f) && (((v.z >> 26) & 0x1f) != 0x1f) &&
+         (((v.w >> 10) & 0x1f) != 0x1f) && (((v.w >> 26) & 0x1f) != 0x1f);
+}
+__device__ __forceinline__ bool fp16_ok8(const float (&f)[8]) {
+  float m = 0.f;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(f[e]));
+  return m <= 65504.f;  // false for NaN too
+}
+
+// Per-thread state of one prep chunk: tokens t = 4 tq + u, channels 8 j + e.
+// Gate factors are kept as packed fp16 pairs (4 words = 8 channels): they
+// only ever multiply fp16 operands.  gamma_C, which scales the fp32 state,
+// is formed in fp32 separately.
+struct Prep {
+  uint4 k[4], q[4];      // k, q rows as fp16 (8 channels; exact for |x| >= 2^-14)
+  uint4 lp[4], ls[4];    // in-quad inclusive prefix / exclusive suffix products
+  uint4 a1, a2, a3;      // alpha of quad tokens 1, 2, 3 (levels 1 and 2)
+  uint4 F8, F16, F32;    // per level: in-group prefix (upper) or suffix (lower)
+  uint4 E16, X16;        // whole-chunk exclusive prefix / suffix of quad totals
+  int tq;
+
+  // Gate factor of token u of this quad at tree level L: the product of
+  // alpha over (m, t] for an upper-half token, over (s, m] for a lower one.
+  template <int L>
+  __device__ __forceinline__ uint4 factor(int u) const {
+    const int t = 4 * tq + u;
+    const bool upper = (t % (2 * L)) >= L;
+    const uint4 one = make_uint4(0x3c003c00u, 0x3c003c00u, 0x3c003c00u, 0x3c003c00u);
+    if (L == 1) return upper ? (u == 1 ? a1 : a3) : one;
+    if (L == 2) {
+      if (upper) return u == 2 ? a2 : ls[1];  // a2, a2 a3
+      return u == 0 ? a1 : one;
+    }
+    if (L == 4) return upper ? lp[u] : ls[u];
+    const uint4& F = L == 8 ? F8 : (L == 16 ? F16 : F32);
+    return hmul8h(F, upper ? lp[u] : ls[u]);
+  }
+  __device__ __forceinline__ uint4 gamma(int u) const { return hmul8h(E16, lp[u]); }
+  __device__ __forceinline__ uint4 rho(int u) const { return hmul8h(ls[u], X16); }
+};
+
+// Segmented exclusive prefix / suffix products of quad totals within aligned
+// groups of 2, 4, 8, 16 quads, over the 16 quads of a chunk (lanes tq of a
+// 16-wide shuffle segment).  Level L = 8, 16, 32 needs the prefix if this
+// quad is in the upper half of its 2L segment and the suffix otherwise.
+__device__ __forceinline__ void quad_scans(Prep& P, const float (&Bq)[8], float (&E16f)[8]) {
+  const int tq = P.tq;
+  float I[8], J[8], E[8], X[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    I[e] = Bq[e];
+    J[e] = Bq[e];
+    E[e] = 1.f;
+    X[e] = 1.f;
+  }
+#pragma unroll
+  for (int lg = 0; lg < 4; ++lg) {
+    const int g = 1 << lg;
+    const int base = tq & ~(2 * g - 1);
+    const int srcE = base + g - 1;  // last quad of the first half
+    const int srcX = base + g;      // first quad of the second half
+    const bool second = (tq & g) != 0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float vi = __shfl_sync(0xffffffffu, I[e], srcE, 16);
+      const float vj = __shfl_sync(0xffffffffu, J[e], srcX, 16);
+      if (second) E[e] *= vi; else X[e] *= vj;
+      I[e] = E[e] * Bq[e];
+      J[e] = X[e] * Bq[e];
+    }
+    // groups of 2g quads = blocks of 8g tokens serve tree level L = 8g
+    const bool upper = (tq & (2 * g)) != 0;
+    float sel[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) sel[e] = upper ? E[e] : X[e];
+    if (lg == 0) P.F8 = to_half8(sel);
+    if (lg == 1) P.F16 = to_half8(sel);
+    if (lg == 2) P.F32 = to_half8(sel);
+    if (lg == 3) {
+      P.E16 = to_half8(E);
+      P.X16 = to_half8(X);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) E16f[e] = E[e];
+    }
+  }
+}
+
+// Row of token t in level L's operands: upper tokens -> X rank, lower -> Y rank.
+__device__ __forceinline__ int level_rank(int t, int L) {
+  const int seg = t / (2 * L), w = t % (2 * L);
+  return seg * L + (w >= L ? w - L : w);
+}
+
+__device__ __forceinline__ void store16(uint8_t* p, const uint4& v) {
+  *reinterpret_cast<uint4*>(p) = v;
+}
+
+// Builds the Gram operands of one round: levels La (X rows 0..63, Y rows
+// 0..31) and La/2 (X rows 64..127, Y rows 32..63).  X rows of a level are
+// 32 k-rows then 32 q-rows of its upper-half tokens; Y rows its lower-half
+// tokens, each gated by the token's factor at that level.
+template <int L>
+__device__ __forceinline__ void write_level(uint8_t* sm, const Prep& P, int j, int xbase,
+                                            int ybase) {
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int t = 4 * P.tq + u;
+    const bool upper = (t % (2 * L)) >= L;
+    const int rank = level_rank(t, L);
+    const uint4 f = P.factor<L>(u);
+    // |factor| <= 1, so the products stay within the range of k and q
+    if (upper) {
+      store16(sm + S_GX + sw128_chunk(128, xbase + rank, j), hmul8h(P.k[u], f));
+      store16(sm + S_GX + sw128_chunk(128, xbase + 32 + rank, j), hmul8h(P.q[u], f));
+    } else {
+      store16(sm + S_GY + sw128_chunk(64, ybase + rank, j), hmul8h(P.k[u], f));
+    }
+  }
+}
+
+// Reads one tree level out of TMEM (lanes = its X rows) into M (fp32,
+// beta_t scaled) and A (fp16).  Lane x of a level: rows 0..31 are k-rows,
+// 32..63 q-rows of upper rank x & 31; its valid columns are the L sources of
+// its own segment, columns [sg*L, sg*L + L) of the level's 32.
+template <int L>
+__device__ __forceinline__ void extract_level(uint8_t* sm, uint32_t taddr, int xr,
+                                              const float* beta, uint8_t* AQ) {
+  const bool qrow = xr >= 32;
+  const int jr = xr & 31;
+  const int sg = jr / L;
+  const int t = sg * 2 * L + L + (jr % L);
+  const int s0 = sg * 2 * L;  // first source of the segment
+  uint32_t v[32];
+  tmem_ld32<32>(taddr, v);
+  tmem_ld_wait();
+  float g[L];
+#pragma unroll
+  for (int c = 0; c < L; ++c) g[c] = 0.f;
+#pragma unroll
+  for (int sgc = 0; sgc < 32 / L; ++sgc) {
+    if (sgc == sg) {
+#pragma unroll
+      for (int c = 0; c < L; ++c) g[c] = __uint_as_float(v[sgc * L + c]);
+    }
+  }
+  if (qrow) {
+    if (L == 1) {
+      *reinterpret_cast<__half*>(AQ + sw128_off(64, t, s0)) = __float2half_rn(g[0]);
+    } else {
+#pragma unroll
+      for (int c = 0; c < L; c += 2)
+        *reinterpret_cast<uint32_t*>(AQ + sw128_off(64, t, s0 + c)) = pack_half2(g[c], g[c + 1]);
+    }
+  } else {
+    const float bt = beta[t];
+    if (L >= 16) {
+      // pairs in different 16-token blocks: fp16 tile N[t][s]
+#pragma unroll
+      for (int c = 0; c < L; c += 8) {
+        float f[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) f[e] = bt * g[c + e];
+        store16(sm + S_TN + sw128_off(64, t, s0 + c), pack_half8(f));
+      }
+    } else {
+      // pairs inside one 16-token block: fp32 [block][t mod 16][s mod 16]
+      float* Md = reinterpret_cast<float*>(sm + S_MD) + (t >> 4) * kMdBlk + (t & 15) * kMdRow;
+      const int sl = s0 & 15;
+      if (L >= 4) {
+#pragma unroll
+        for (int c = 0; c < L; c += 4)
+          *reinterpret_cast<float4*>(Md + sl + c) =
+              make_float4(bt * g[c], bt * g[c + 1], bt * g[c + 2], bt * g[c + 3]);
+      } else {
+#pragma unroll
+        for (int c = 0; c < L; ++c) Md[sl + c] = bt * g[c];
+      }
+    }
+  }
+}
+
+template <int La>
+__device__ __forceinline__ void extract_round(uint8_t* sm, uint32_t tmem, int r, int wq, int lane,
+                                              const float* beta, uint8_t* AQ) {
+  const int x = 32 * wq + lane;  // warp-uniform level: lanes 0..63 level La, 64..127 La/2
+  const uint32_t base = tmem + ((uint32_t)(32 * wq) << 16) + T_G + 64 * r;
+  if (x < 64)
+    extract_level<La>(sm, base, x & 63, beta, AQ);
+  else
+    extract_level<La / 2>(sm, base + 32, x & 63, beta, AQ);
+}
+
+// Inverses of the four unit-lower 16 x 16 diagonal blocks of I + M, by
+// right-looking substitution (one column per thread), written as fp16 into
+// the diagonal blocks of D.  Threads 0..63.
+__device__ __forceinline__ void invert_diag_blocks(uint8_t* sm, int p) {
+  const int blk = p >> 4, c = p & 15, o = 16 * blk;
+  const float* Md = reinterpret_cast<const float*>(sm + S_MD) + blk * kMdBlk;
+  float x[16];
+#pragma unroll
+  for (int t = 0; t < 16; ++t) x[t] = (t == c) ? 1.f : 0.f;
+#pragma unroll
+  for (int s = 0; s < 15; ++s) {
+#pragma unroll
+    for (int t = s + 1; t < 16; ++t) x[t] = fmaf(-Md[t * kMdRow + s], x[s], x[t]);
+  }
+#pragma unroll
+  for (int t = 0; t < 16; ++t)
+    *reinterpret_cast<__half*>(sm + S_TD + sw128_off(64, o + t, o + c)) = __float2half_rn(x[t]);
+}
+
 __global__ void __launch_bounds__(NT, 1)
-    fwd_chunk_kernel(const __grid_constant__ FwdArgs a, const __grid_constant__ CUtensorMap mq,
-                     const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap ma,
-                     const __grid_constant__ CUtensorMap mv) {
+    fwd_chunk_kernel(const __grid_constant__ FwdArgs a, const __grid_constant__ CUtensorMap mv) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int wq = warp & 3, half = warp >> 2;
-  const uint32_t lane_base = (uint32_t)(32 * wq) << 16;
-  uint64_t* bar_tma = reinterpret_cast<uint64_t*>(sm + S_BAR);
-  uint64_t* bar_mma = bar_tma + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + S_MISC);
-  float* beta_s = reinterpret_cast<float*>(sm + S_BETA);
-  float* gC = reinterpret_cast<float*>(sm + S_GC);
+  uint64_t* bar_v = reinterpret_cast<uint64_t*>(sm + S_BAR);
+  uint64_t* bar_gram = bar_v + 1;
+  uint64_t* bar_w = bar_v + 2;
+  uint64_t* bar_s1 = bar_v + 3;
+  uint64_t* bar_s3 = bar_v + 4;
+  uint64_t* bar_t = bar_v + 5;
+  int* cnt = reinterpret_cast<int*>(sm + S_BAR + 64);
+  int* c_ready = cnt + 0;  // prep -> state: chunks whose operands are complete
+  int* c_gc = cnt + 1;     // prep -> state: chunks whose gamma_C is published
+  int* c_s1 = cnt + 2;     // state -> prep: chunks whose U-MMA completed (TB, W free)
+  int* c_s3 = cnt + 3;     // state -> prep: chunks whose last MMA completed
+  int* s_abort = cnt + 4;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(cnt + 8);
 
   const Unit u = unit_of(a);
   const int nchunks = (u.len + C - 1) / C;
 
   if (tid == 0) {
-    mbar_init(bar_tma, 1);
-    mbar_init(bar_mma, 1);
+    mbar_init(bar_v, 1);
+    mbar_init(bar_gram, 1);
+    mbar_init(bar_w, 1);
+    mbar_init(bar_s1, 1);
+    mbar_init(bar_s3, 1);
+    mbar_init(bar_t, 1);
+    for (int i = 0; i < 8; ++i) cnt[i] = 0;
     fence_mbar_init();
-    tma_prefetch_desc(&mq);
-    tma_prefetch_desc(&mk);
-    tma_prefetch_desc(&ma);
     tma_prefetch_desc(&mv);
   }
+  // A: its upper triangle is never written again, so zero it once
+  for (int e = tid; e < 2 * 8192 / 16; e += NT)
+    reinterpret_cast<uint4*>(sm + S_AQ)[e] = make_uint4(0, 0, 0, 0);
   if (warp == 0) {
     tmem_alloc(tmem_slot, TMEM_COLS);
     tmem_relinquish();
@@ -277,326 +470,545 @@ __global__ void __launch_bounds__(NT, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-
-  auto issue_tiles = [&](int c, bool qka, bool v) {
-    const int y = (int)(u.row0 + (long)c * C);
-    if (qka) {
-      mbar_arrive_expect_tx(bar_tma, 4 * TILE_BYTES);
-      tma_load_2d(sm + S_TQ, &mq, bar_tma, 0, y);
-      tma_load_2d(sm + S_TQ + 8192, &mq, bar_tma, 64, y);
-      tma_load_2d(sm + S_TK, &mk, bar_tma, 0, y);
-      tma_load_2d(sm + S_TK + 8192, &mk, bar_tma, 64, y);
-      tma_load_2d(sm + S_TA, &ma, bar_tma, 0, y);
-      tma_load_2d(sm + S_TA + 8192, &ma, bar_tma, 64, y);
-    }
-    if (v) {
-      tma_load_2d(sm + S_TV, &mv, bar_tma, 0, y);
-      tma_load_2d(sm + S_TV + 8192, &mv, bar_tma, 64, y);
-    }
-  };
-  if (tid == 0 && nchunks > 0) issue_tiles(0, true, true);
-
-  // Initial state: H^T[j][i] = h0[i][j] (or 0) into TMEM and as fp16 into smem.
-  {
-    const int j = 32 * wq + lane;
-    uint8_t* HT = sm + S_HT;
-    for (int c16 = 0; c16 < 4; ++c16) {
-      const int i0 = 64 * half + 16 * c16;
-      uint32_t r[16];
-#pragma unroll
-      for (int e = 0; e < 16; ++e)
-        r[e] = __float_as_uint(a.h0 ? a.h0[u.sidx + (size_t)(i0 + e) * 128 + j] : 0.f);
-      tmem_st32<16>(tmem + lane_base + T_H + i0, r);
-#pragma unroll
-      for (int e = 0; e < 16; e += 8) {
-        uint4 pk;
-        pk.x = pack_half2(__uint_as_float(r[e]), __uint_as_float(r[e + 1]));
-        pk.y = pack_half2(__uint_as_float(r[e + 2]), __uint_as_float(r[e + 3]));
-        pk.z = pack_half2(__uint_as_float(r[e + 4]), __uint_as_float(r[e + 5]));
-        pk.w = pack_half2(__uint_as_float(r[e + 6]), __uint_as_float(r[e + 7]));
-        *reinterpret_cast<uint4*>(HT + sw128_chunk(128, j, (i0 + e) >> 3)) = pk;
-      }
-    }
-    tmem_st_wait();
-  }
-  fence_proxy_async_smem();
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-
-  uint32_t mma_phase = 0;
-  bool ovf = false;
-  bool tma_pending = nchunks > 0;
-  int tma_next = 0;  // chunk whose tiles were issued last
-  bool aborted = false;  // uniform across the block: decided by __syncthreads_or
-  auto wait_mma = [&]() -> bool {
-    const bool ok = mbar_wait(bar_mma, mma_phase);
-    mma_phase ^= 1;
-    if (!ok) set_status(a.status, CKDA_ERR_TIMEOUT);
-    tc_fence_after();
-    aborted = __syncthreads_or(ok ? 0 : 1) != 0;
-    return !aborted;
-  };
-  auto sync_for_mma = [&]() {
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-  };
-
   const uint32_t sb = smem_u32(sm);
-  const uint32_t idx_f16_n64 = idesc_f16(128, 64, 0, 0, 0);
-  const uint32_t idx_f16_n128 = idesc_f16(128, 128, 0, 0, 0);
-  const uint32_t idx_bf16_n64 = idesc_f16(128, 64, 1, 0, 0);
-  const uint32_t idx_bf16_mn_n64 = idesc_f16(128, 64, 1, 1, 0);
+  bool ovf = false;
 
-  for (int c = 0; c < nchunks; ++c) {
-    const int lenc = min(C, u.len - c * C);
-    // ---------------------------------------------------------- tiles of c
-    {
-      const bool ok = mbar_wait(bar_tma, (uint32_t)(c & 1));
-      if (!ok) set_status(a.status, CKDA_ERR_TIMEOUT);
-      aborted = __syncthreads_or(ok ? 0 : 1) != 0;
-      if (aborted) break;
-      tma_pending = false;
-    }
-    if (tid < C) {
-      const long r = u.row0 + (long)c * C + tid;
-      beta_s[tid] = tid < lenc ? ld_io(static_cast<const __nv_bfloat16*>(a.beta) + r) : 0.f;
-    }
-    {  // zero M (fp32) and A (fp16) for this chunk
-      float4* mz = reinterpret_cast<float4*>(sm + S_MF);
-      for (int e = tid; e < 64 * 64 / 4; e += NT) mz[e] = make_float4(0.f, 0.f, 0.f, 0.f);
-      uint4* az = reinterpret_cast<uint4*>(sm + S_AQ);
-      for (int e = tid; e < 8192 / 16; e += NT) az[e] = make_uint4(0, 0, 0, 0);
-    }
-    __syncthreads();
-    // ------------------------------------------------- gated Grams (3 rounds)
+  if (tid < NPREP) {
+    // =================================================================== PREP
+    const int p = tid;
+    const int w = p >> 5;
+    const int j = 2 * w + (lane >> 4);  // channel chunk
+    const int tq = lane & 15;           // token quad
+    const int wq = w & 3, half = w >> 2;
+    const __nv_bfloat16* gq = static_cast<const __nv_bfloat16*>(a.q);
+    const __nv_bfloat16* gk = static_cast<const __nv_bfloat16*>(a.k);
+    const __nv_bfloat16* ga = static_cast<const __nv_bfloat16*>(a.alpha);
+    const __nv_bfloat16* gb = static_cast<const __nv_bfloat16*>(a.beta);
+    uint32_t gram_phase = 0, t_phase = 0;
     bool alive = true;
-    for (int r = 0; r < 3 && alive; ++r) {
-      build_gram_operands(sm, 32 >> (2 * r), lenc);
-      sync_for_mma();
-      if (tid == 0) {
-        for (int k = 0; k < 8; ++k)
-          umma_ss(tmem + T_G + 64 * r, kmajor_desc(sb + S_GX, 128, k),
-                  kmajor_desc(sb + S_GY, 64, k), idx_f16_n64, k > 0);
-        umma_commit(bar_mma);
-      }
-      alive = wait_mma();
-    }
-    if (!alive) break;
-    for (int r = 0; r < 3; ++r) extract_gram(sm, tmem, r);
-    {  // diagonal of A: q_t . k_t
-      const int t = tid >> 2, part = tid & 3;
-      float acc = 0.f;
-      for (int i = 32 * part; i < 32 * part + 32; i += 2) {
-        const float2 qq = bf16x2_at(sm + S_TQ, t, i), kk = bf16x2_at(sm + S_TK, t, i);
-        acc = fmaf(qq.x, kk.x, fmaf(qq.y, kk.y, acc));
-      }
-      acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-      acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-      if (part == 0) *reinterpret_cast<__half*>(sm + S_AQ + sw128_off(64, t, t)) = __float2half_rn(acc);
-    }
-    __syncthreads();
-    // ------------------------------------------------------- T and T Diag(beta)
-    invert_unit_lower(sm);
-    {
-      const float* Tf = reinterpret_cast<const float*>(sm + S_TF);
-      for (int e = tid; e < 64 * 32; e += NT) {
-        const int t = e >> 5, s = 2 * (e & 31);
-        const float v0 = s <= t ? Tf[t * 64 + s] * beta_s[s] : 0.f;
-        const float v1 = s + 1 <= t ? Tf[t * 64 + s + 1] * beta_s[s + 1] : 0.f;
-        *reinterpret_cast<uint32_t*>(sm + S_TB + sw128_off(64, t, s)) = pack_bf162(v0, v1);
-      }
-    }
-    __syncthreads();
-    // --------------------------- (k*gamma)^T, q*gamma, (k*rho)^T and gamma_C
-    if (tid < 128) {
-      const int i = tid;
-      float g = 1.f;
-      uint32_t pk[4];
-      for (int s = 0; s < C; ++s) {
-        const float al = s < lenc ? bf16_at(sm + S_TA, s, i) : 1.f;
-        g *= al;
-        const float kg = bf16_at(sm + S_TK, s, i) * g;
-        const float qg = bf16_at(sm + S_TQ, s, i) * g;
-        if (s < lenc) ovf |= !fp16_ok(qg);
-        *reinterpret_cast<__half*>(sm + S_QG + sw128_off(64, s, i)) = __float2half_rn(qg);
-        const int e = s & 7;
-        if (e & 1) {
-          const float prev = __uint_as_float(pk[e >> 1]);
-          pk[e >> 1] = pack_bf162(prev, kg);
-        } else {
-          pk[e >> 1] = __float_as_uint(kg);
-        }
-        if (e == 7)
-          *reinterpret_cast<uint4*>(sm + S_KGT + sw128_chunk(128, i, s >> 3)) =
-              make_uint4(pk[0], pk[1], pk[2], pk[3]);
-      }
-      gC[i] = g;
-    } else {
-      const int i = tid - 128;
-      float rho = 1.f;
-      float vals[8];
-      for (int s = C - 1; s >= 0; --s) {
-        vals[s & 7] = bf16_at(sm + S_TK, s, i) * rho;
-        const float al = s < lenc ? bf16_at(sm + S_TA, s, i) : 1.f;
-        rho *= al;
-        if ((s & 7) == 0) {
-          uint4 pk;
-          pk.x = pack_half2(vals[0], vals[1]);
-          pk.y = pack_half2(vals[2], vals[3]);
-          pk.z = pack_half2(vals[4], vals[5]);
-          pk.w = pack_half2(vals[6], vals[7]);
-          *reinterpret_cast<uint4*>(sm + S_KH + sw128_chunk(128, i, s >> 3)) = pk;
-        }
-      }
-    }
-    sync_for_mma();
-    // ------------------------------------------------------------ W = TB (k*gamma)
-    if (tid == 0) {
-      for (int k = 0; k < 4; ++k)
-        umma_ss(tmem + T_W, kmajor_desc(sb + S_KGT, 128, k), kmajor_desc(sb + S_TB, 64, k),
-                idx_bf16_n64, k > 0);
-      umma_commit(bar_mma);
-      // q, k, alpha of this chunk are no longer read: prefetch the next chunk's
-      if (c + 1 < nchunks) issue_tiles(c + 1, true, false);
-    }
-    if (!wait_mma()) break;
-    {  // -W as fp16 [t][i]: lane = i, columns = t
-      const int i = 32 * wq + lane;
-      uint32_t v[32];
-      tmem_ld32<32>(tmem + lane_base + T_W + 32 * half, v);
-      tmem_ld_wait();
+    float beta_next[4] = {0.f, 0.f, 0.f, 0.f};
+    if (j == 0 && nchunks > 0) {
+      const int len0 = min(C, u.len);
 #pragma unroll
-      for (int e = 0; e < 32; ++e)
-        *reinterpret_cast<__half*>(sm + S_WM + sw128_off(64, 32 * half + e, i)) =
-            __float2half_rn(-__uint_as_float(v[e]));
-    }
-    {  // H^T <- H^T Diag(gamma_C) in TMEM (column i scaled by gamma_C[i])
-      for (int c16 = 0; c16 < 4; ++c16) {
-        const int i0 = 64 * half + 16 * c16;
-        uint32_t v[16];
-        tmem_ld32<16>(tmem + lane_base + T_H + i0, v);
-        tmem_ld_wait();
-#pragma unroll
-        for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * gC[i0 + e]);
-        tmem_st32<16>(tmem + lane_base + T_H + i0, v);
-      }
-      tmem_st_wait();
-    }
-    sync_for_mma();
-    // ------------------------------- U = TB V - W H ;  O = (q*gamma) H
-    if (tid == 0) {
-      for (int k = 0; k < 4; ++k)
-        umma_ss(tmem + T_U, mnmajor_desc(sb + S_TV, 64, k), kmajor_desc(sb + S_TB, 64, k),
-                idx_bf16_mn_n64, k > 0);
-      for (int k = 0; k < 8; ++k)
-        umma_ss(tmem + T_U, kmajor_desc(sb + S_HT, 128, k), kmajor_desc(sb + S_WM, 64, k),
-                idx_f16_n64, 1);
-      for (int k = 0; k < 8; ++k)
-        umma_ss(tmem + T_O, kmajor_desc(sb + S_HT, 128, k), kmajor_desc(sb + S_QG, 64, k),
-                idx_f16_n64, k > 0);
-      umma_commit(bar_mma);
-    }
-    if (!wait_mma()) break;
-    if (c + 1 < nchunks) {
-      if (tid == 0) issue_tiles(c + 1, false, true);
-      tma_pending = true;
-      tma_next = c + 1;
-    }
-    {  // U^T -> fp16 [j][s]
-      const int j = 32 * wq + lane;
-      uint32_t v[32];
-      tmem_ld32<32>(tmem + lane_base + T_U + 32 * half, v);
-      tmem_ld_wait();
-#pragma unroll
-      for (int e = 0; e < 32; e += 8) {
-        uint4 pk;
-        float f[8];
-#pragma unroll
-        for (int z = 0; z < 8; ++z) {
-          f[z] = __uint_as_float(v[e + z]);
-          ovf |= !fp16_ok(f[z]);
-        }
-        pk.x = pack_half2(f[0], f[1]);
-        pk.y = pack_half2(f[2], f[3]);
-        pk.z = pack_half2(f[4], f[5]);
-        pk.w = pack_half2(f[6], f[7]);
-        *reinterpret_cast<uint4*>(sm + S_UT + sw128_chunk(128, j, (32 * half + e) >> 3)) = pk;
+      for (int uu = 0; uu < 4; ++uu) {
+        const int t = 4 * tq + uu;
+        beta_next[uu] = t < len0 ? __bfloat162float(gb[u.row0 + t]) : 0.f;
       }
     }
-    sync_for_mma();
-    // ------------------------------ O += A U ;  H^T += U^T (k*rho)
-    if (tid == 0) {
+    // waits on an mbarrier fed by this role's MMAs; the AND over the role
+    // decides, uniformly, whether to go on
+    auto prep_wait = [&](uint64_t* bar, uint32_t& phase) -> bool {
+      const bool ok = mbar_wait(bar, phase & 1);
+      ++phase;
+      const bool all = named_and(BAR_PREP, NPREP, ok);
+      tc_fence_after();
+      return all;
+    };
+    auto prep_counter = [&](int* counter, int target) -> bool {
+      const bool ok = wait_counter(counter, target, s_abort);
+      return named_and(BAR_PREP, NPREP, ok);
+    };
+    // the MMA of the inverse chain: D[lanes 0..63] = A (rows 0..63 used) x B
+    auto t_mma = [&](uint32_t d_col, uint32_t a_tile, uint32_t b_tile) {
       for (int k = 0; k < 4; ++k)
-        umma_ss(tmem + T_O, kmajor_desc(sb + S_UT, 128, k), kmajor_desc(sb + S_AQ, 64, k),
-                idx_f16_n64, 1);
-      for (int k = 0; k < 4; ++k)
-        umma_ss(tmem + T_H, kmajor_desc(sb + S_UT, 128, k), kmajor_desc(sb + S_KH, 128, k),
-                idx_f16_n128, 1);
-      umma_commit(bar_mma);
-    }
-    if (!wait_mma()) break;
-    {  // outputs of this chunk: o[t][j] for t < lenc
-      const int j = 32 * wq + lane;
-      uint32_t v[32];
-      tmem_ld32<32>(tmem + lane_base + T_O + 32 * half, v);
-      tmem_ld_wait();
-      __nv_bfloat16* o = static_cast<__nv_bfloat16*>(a.o);
+        umma_ss(tmem + d_col, kmajor_desc(sb + a_tile, 128, k), mnmajor_desc(sb + b_tile, 64, k),
+                idesc_f16(128, 64, 0, 0, 1), k > 0);
+      umma_commit(bar_t);
+    };
+    const bool tconv = wq < 2;  // warps 0,1,4,5 reach TMEM lanes 0..63
+    const int trow = 32 * wq + lane;
+    const uint32_t tl = (uint32_t)(32 * (wq & 1)) << 16;
+
+    for (int c = 0; c < nchunks && alive; ++c) {
+      const int lenc = min(C, u.len - c * C);
+      const int buf = c & 1;
       const long rbase = u.row0 + (long)c * C;
+      // ---- loads: 4 tokens x 8 channels of q, k, alpha (rows past the end of
+      // the sequence are clamped to a valid row and then masked)
+      Prep P;
+      P.tq = tq;
+      float Bq[8];
+      {
+        uint4 rk[4], rq[4], ra[4];
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const int t = 32 * half + e;
-        if (t < lenc) o[(size_t)(rbase + t) * 128 + j] = __float2bfloat16_rn(a.scale * __uint_as_float(v[e]));
+        for (int uu = 0; uu < 4; ++uu) {
+          const int t = min(4 * tq + uu, lenc - 1);
+          const size_t off = (size_t)(rbase + t) * 128 + 8 * j;
+          rk[uu] = __ldg(reinterpret_cast<const uint4*>(gk + off));
+          rq[uu] = __ldg(reinterpret_cast<const uint4*>(gq + off));
+          ra[uu] = __ldg(reinterpret_cast<const uint4*>(ga + off));
+        }
+        float al[4][8];
+        float mx = 0.f;
+#pragma unroll
+        for (int uu = 0; uu < 4; ++uu) {
+          const bool valid = 4 * tq + uu < lenc;
+          float kk[8], qq[8];
+          unpack_bf16x8(rk[uu], kk);
+          unpack_bf16x8(rq[uu], qq);
+          mx = fmaxf(mx, fmaxf(absmax8(kk), absmax8(qq)));
+          P.k[uu] = valid ? to_half8(kk) : make_uint4(0, 0, 0, 0);
+          P.q[uu] = valid ? to_half8(qq) : make_uint4(0, 0, 0, 0);
+          unpack_bf16x8(ra[uu], al[uu]);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) al[uu][e] = valid ? al[uu][e] : 1.f;  // identity transition
+        }
+        ovf |= !(mx <= 65504.f);
+        // in-quad prefix / suffix products (fp32, then packed halves)
+        float lp[8], ls[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) { lp[e] = al[0][e]; ls[e] = 1.f; }
+        P.lp[0] = to_half8(lp);
+#pragma unroll
+        for (int uu = 1; uu < 4; ++uu) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) lp[e] *= al[uu][e];
+          P.lp[uu] = to_half8(lp);
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) Bq[e] = lp[e];
+        P.ls[3] = to_half8(ls);
+#pragma unroll
+        for (int uu = 2; uu >= 0; --uu) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) ls[e] *= al[uu + 1][e];
+          P.ls[uu] = to_half8(ls);
+        }
+        P.a1 = to_half8(al[1]);
+        P.a2 = to_half8(al[2]);
+        P.a3 = to_half8(al[3]);
       }
-    }
-    if (c + 1 < nchunks) {  // H^T -> fp16 [j][i] for the next chunk
-      const int j = 32 * wq + lane;
-      for (int c32 = 0; c32 < 2; ++c32) {
-        const int i0 = 64 * half + 32 * c32;
+      // warm L2 with the next chunk's rows of q, k, alpha (two lines per thread)
+      if (c + 1 < nchunks) {
+        const int t = p & 63, which = p >> 6;
+        if (which < 3 && t < min(C, u.len - (c + 1) * C)) {
+          const __nv_bfloat16* base = which == 0 ? gq : which == 1 ? gk : ga;
+          const char* line = reinterpret_cast<const char*>(base + (size_t)(rbase + C + t) * 128);
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(line));
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(line + 128));
+        }
+      }
+      // beta: this chunk's values were loaded one chunk ahead
+      float* beta_s = reinterpret_cast<float*>(sm + S_BETA) + 64 * buf;
+      if (j == 0) {
+#pragma unroll
+        for (int uu = 0; uu < 4; ++uu) beta_s[4 * tq + uu] = beta_next[uu];
+        if (c + 1 < nchunks) {
+          const int lenn = min(C, u.len - (c + 1) * C);
+#pragma unroll
+          for (int uu = 0; uu < 4; ++uu) {
+            const int t = 4 * tq + uu;
+            beta_next[uu] = t < lenn ? __bfloat162float(gb[rbase + C + t]) : 0.f;
+          }
+        }
+      }
+      // ---- gate products across quads: segmented scans of the quad totals
+      float E16f[8];
+      quad_scans(P, Bq, E16f);
+      // gamma_C (fp32: it scales the fp32 state): the last quad publishes it
+      float* gC = reinterpret_cast<float*>(sm + S_GC) + 128 * buf;
+      if (tq == 15) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) gC[8 * j + e] = E16f[e] * Bq[e];
+      }
+      // k*gamma (bf16, A of the W-MMA; its last reader, the previous W-MMA,
+      // completed inside the previous prep) and the partial q.k diagonal
+      {
+        float* dg = reinterpret_cast<float*>(sm + S_DIAG);
+#pragma unroll
+        for (int uu = 0; uu < 4; ++uu) {
+          const int t = 4 * tq + uu;
+          store16(sm + S_KGT + sw128_chunk(64, t, j), half8_to_bf8(hmul8h(P.k[uu], P.gamma(uu))));
+          float kk[8], qq[8], sacc = 0.f;
+          unpack_half8(P.k[uu], kk);
+          unpack_half8(P.q[uu], qq);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) sacc = fmaf(qq[e], kk[e], sacc);
+          dg[j * 64 + t] = sacc;
+        }
+      }
+      named_sync(BAR_PREP, NPREP);
+      if (p == 0) st_release(c_gc, c + 1);
+
+      // ---- gated Grams: 3 rounds of (write operands, MMA)
+#pragma unroll 1
+      for (int r = 0; r < 3; ++r) {
+        if (r > 0 && !prep_wait(bar_gram, gram_phase)) { alive = false; break; }
+        if (r == 0) {
+          write_level<32>(sm, P, j, 0, 0);
+          write_level<16>(sm, P, j, 64, 32);
+        } else if (r == 1) {
+          write_level<8>(sm, P, j, 0, 0);
+          write_level<4>(sm, P, j, 64, 32);
+        } else {
+          write_level<2>(sm, P, j, 0, 0);
+          write_level<1>(sm, P, j, 64, 32);
+        }
+        fence_proxy_async_smem();
+        named_sync(BAR_PREP, NPREP);
+        if (p == 0) {
+          tc_fence_after();
+          for (int k = 0; k < 8; ++k)
+            umma_ss(tmem + T_G + 64 * r, kmajor_desc(sb + S_GX, 128, k),
+                    kmajor_desc(sb + S_GY, 64, k), idesc_f16(128, 64, 0, 0, 0), k > 0);
+          umma_commit(bar_gram);
+        }
+      }
+      if (!alive) break;
+
+      // ---- q*gamma, k*rho: the previous chunk's last MMA must have read them
+      if (!prep_counter(c_s3, c)) { alive = false; break; }
+#pragma unroll
+      for (int uu = 0; uu < 4; ++uu) {
+        const int t = 4 * tq + uu;
+        store16(sm + S_QG + sw128_chunk(64, t, j), hmul8h(P.q[uu], P.gamma(uu)));
+        store16(sm + S_KH + sw128_chunk(64, t, j), hmul8h(P.k[uu], P.rho(uu)));
+      }
+
+      // ---- the last Gram round, then read all three out
+      if (!prep_wait(bar_gram, gram_phase)) { alive = false; break; }
+      uint8_t* AQ = sm + S_AQ + 8192 * buf;
+      {
+        // zero what the extraction does not write: N on and above the
+        // 16-block diagonal, and D (its diagonal blocks come next)
+        for (int e = p; e < 10 * 32; e += NPREP) {
+          // 10 blocks (I <= J) x 16 rows x 2 chunks of 16 bytes
+          const int blk = e >> 5, rr = (e >> 1) & 15, hh = e & 1;
+          int I = 0, J = blk;
+          if (blk >= 4) { I = 1; J = blk - 3; }
+          if (blk >= 7) { I = 2; J = blk - 5; }
+          if (blk >= 9) { I = 3; J = 3; }
+          store16(sm + S_TN + sw128_chunk(64, 16 * I + rr, 2 * J + hh), make_uint4(0, 0, 0, 0));
+        }
+        for (int e = p; e < 8192 / 16; e += NPREP)
+          store16(sm + S_TD + 16 * e, make_uint4(0, 0, 0, 0));
+      }
+      if (half == 0) {
+        extract_round<32>(sm, tmem, 0, wq, lane, beta_s, AQ);
+      } else {
+        extract_round<8>(sm, tmem, 1, wq, lane, beta_s, AQ);
+        extract_round<2>(sm, tmem, 2, wq, lane, beta_s, AQ);
+      }
+      tc_fence_before();
+      named_sync(BAR_PREP, NPREP);
+      // ---- T = (I + M)^-1 = (I - E)(I + E^2) D with D the inverse of the
+      // block diagonal of I + M and E = D N (E^4 = 0: N is strictly lower by
+      // 16-blocks); the four products run on the tensor cores
+      if (p < 64) {
+        invert_diag_blocks(sm, p);
+      } else if (p < 128) {
+        const int t = p - 64;
+        const float* dg = reinterpret_cast<const float*>(sm + S_DIAG);
+        float sacc = 0.f;
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) sacc += dg[jj * 64 + t];
+        *reinterpret_cast<__half*>(AQ + sw128_off(64, t, t)) = __float2half_rn(sacc);
+      }
+      fence_proxy_async_smem();
+      named_sync(BAR_PREP, NPREP);
+      if (p == 0) { tc_fence_after(); t_mma(T_G, S_TD, S_TN); }        // E = D N
+      if (!prep_wait(bar_t, t_phase)) { alive = false; break; }
+      if (tconv) {
         uint32_t v[32];
-        tmem_ld32<32>(tmem + lane_base + T_H + i0, v);
+        tmem_ld32<32>(tmem + tl + T_G + 32 * half, v);
         tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < 32; e += 8) {
+        for (int z = 0; z < 32; z += 8) {
           float f[8];
 #pragma unroll
-          for (int z = 0; z < 8; ++z) {
-            f[z] = __uint_as_float(v[e + z]);
-            ovf |= !fp16_ok(f[z]);
-          }
-          uint4 pk;
-          pk.x = pack_half2(f[0], f[1]);
-          pk.y = pack_half2(f[2], f[3]);
-          pk.z = pack_half2(f[4], f[5]);
-          pk.w = pack_half2(f[6], f[7]);
-          *reinterpret_cast<uint4*>(sm + S_HT + sw128_chunk(128, j, (i0 + e) >> 3)) = pk;
+          for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(v[z + e]);
+          store16(sm + S_TE + sw128_chunk(64, trow, (32 * half + z) >> 3), pack_half8(f));
         }
       }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      named_sync(BAR_PREP, NPREP);
+      if (p == 0) { tc_fence_after(); t_mma(T_G + 64, S_TE, S_TE); }   // E^2
+      if (!prep_wait(bar_t, t_phase)) { alive = false; break; }
+      float gv[32];  // G = I + E^2, kept for F
+      if (tconv) {
+        uint32_t v[32];
+        tmem_ld32<32>(tmem + tl + T_G + 64 + 32 * half, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int z = 0; z < 32; ++z)
+          gv[z] = __uint_as_float(v[z]) + ((32 * half + z) == trow ? 1.f : 0.f);
+#pragma unroll
+        for (int z = 0; z < 32; z += 8) {
+          float f[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) f[e] = gv[z + e];
+          store16(sm + S_TG + sw128_chunk(64, trow, (32 * half + z) >> 3), pack_half8(f));
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      named_sync(BAR_PREP, NPREP);
+      if (p == 0) { tc_fence_after(); t_mma(T_G + 128, S_TE, S_TG); }  // E G
+      if (!prep_wait(bar_t, t_phase)) { alive = false; break; }
+      if (tconv) {
+        uint32_t v[32];
+        tmem_ld32<32>(tmem + tl + T_G + 128 + 32 * half, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int z = 0; z < 32; z += 8) {
+          float f[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) f[e] = gv[z + e] - __uint_as_float(v[z + e]);  // F = G - E G
+          store16(sm + S_TFm + sw128_chunk(64, trow, (32 * half + z) >> 3), pack_half8(f));
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      named_sync(BAR_PREP, NPREP);
+      if (p == 0) { tc_fence_after(); t_mma(T_W, S_TFm, S_TD); }       // T = F D
+      if (!prep_wait(bar_t, t_phase)) { alive = false; break; }
+      // ---- T Diag(beta) as bf16; TB and W are single-buffered: the previous
+      // chunk's U-MMA must have read them
+      if (!prep_counter(c_s1, c)) { alive = false; break; }
+      if (tconv) {
+        uint32_t v[32];
+        tmem_ld32<32>(tmem + tl + T_W + 32 * half, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int z = 0; z < 32; z += 8) {
+          float f[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int s = 32 * half + z + e;
+            f[e] = s <= trow ? __uint_as_float(v[z + e]) * beta_s[s] : 0.f;
+          }
+          store16(sm + S_TB + sw128_chunk(64, trow, (32 * half + z) >> 3), pack_bf8(f));
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      named_sync(BAR_PREP, NPREP);
+      if (p == 0) {
+        tc_fence_after();
+        // W^T[i][t] = sum_s (k*gamma)[s][i] TB[t][s]
+        for (int k = 0; k < 4; ++k)
+          umma_ss(tmem + T_W, mnmajor_desc(sb + S_KGT, 64, k), kmajor_desc(sb + S_TB, 64, k),
+                  idesc_f16(128, 64, 1, 1, 0), k > 0);
+        umma_commit(bar_w);
+      }
+      {
+        uint32_t wphase = (uint32_t)c;
+        if (!prep_wait(bar_w, wphase)) { alive = false; break; }
+      }
+      {  // -W^T as fp16 [i][t] (MN-major B): lane = i, 32 columns per half
+        const int i = 32 * wq + lane;
+        uint32_t v[32];
+        tmem_ld32<32>(tmem + ((uint32_t)(32 * wq) << 16) + T_W + 32 * half, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int z = 0; z < 32; z += 8) {
+          float f[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) f[e] = -__uint_as_float(v[z + e]);
+          ovf |= !fp16_ok8(f);
+          store16(sm + S_W + sw128_chunk(128, i, (32 * half + z) >> 3), pack_half8(f));
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      named_sync(BAR_PREP, NPREP);
+      if (p == 0) st_release(c_ready, c + 1);
     }
-    sync_for_mma();
+    if (!alive) *reinterpret_cast<volatile int*>(s_abort) = 1;
+  } else {
+    // ================================================================== STATE
+    const int s = tid - NPREP;   // 0..127 = TMEM lane = value column j
+    const int wq = s >> 5;       // warps 8..11 -> lane groups 0..3
+    const uint32_t lb = (uint32_t)(32 * wq) << 16;
+    const bool lead = s == 0;
+    uint8_t* HT = sm + S_HT;
+    float* hT = a.hT;
+    bool alive = true;
+    if (lead && nchunks > 0) {
+      mbar_arrive_expect_tx(bar_v, 16384);
+      tma_load_2d(sm + S_V, &mv, bar_v, 0, (int)u.row0);
+      tma_load_2d(sm + S_V + 8192, &mv, bar_v, 64, (int)u.row0);
+    }
+    // initial state -> TMEM (fp32) and H^T fp16 in smem
+    auto store_HT = [&](int i0, const float (&f)[32]) {
+#pragma unroll
+      for (int z = 0; z < 32; z += 8) {
+        float g[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) g[e] = f[z + e];
+        ovf |= !fp16_ok8(g);
+        store16(HT + sw128_chunk(128, s, (i0 + z) >> 3), pack_half8(g));
+      }
+    };
+    const float* gc_all = reinterpret_cast<const float*>(sm + S_GC);
+    // scales the TMEM state by gamma_C of chunk c (column i times gC[i]) after
+    // writing its unscaled fp16 copy
+    auto convert_and_scale = [&](int c_next, bool from_h0) {
+      const float* gC = gc_all + 128 * (c_next & 1);
+#pragma unroll 1
+      for (int i0 = 0; i0 < 128; i0 += 32) {
+        float f[32];
+        if (from_h0) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            f[e] = a.h0 ? a.h0[u.sidx + (size_t)(i0 + e) * 128 + s] : 0.f;
+        } else {
+          uint32_t v[32];
+          tmem_ld32<32>(tmem + lb + T_H + i0, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(v[e]);
+        }
+        store_HT(i0, f);
+        uint32_t o[16];
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(f[16 * hh + e] * gC[i0 + 16 * hh + e]);
+          tmem_st32<16>(tmem + lb + T_H + i0 + 16 * hh, o);
+        }
+      }
+      tmem_st_wait();
+    };
+    if (nchunks > 0) {
+      const bool ok = wait_counter(c_gc, 1, s_abort);
+      alive = named_and(BAR_STATE, NSTATE, ok);
+      if (alive) convert_and_scale(0, true);
+    } else if (hT) {
+      for (int i = 0; i < 128; ++i)
+        hT[u.sidx + (size_t)i * 128 + s] = a.h0 ? a.h0[u.sidx + (size_t)i * 128 + s] : 0.f;
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    named_sync(BAR_STATE, NSTATE);
+
+    __nv_bfloat16* go = static_cast<__nv_bfloat16*>(a.o);
+    for (int c = 0; c < nchunks && alive; ++c) {
+      const int lenc = min(C, u.len - c * C);
+      const int buf = c & 1;
+      {  // prep operands of chunk c, and its v tile
+        bool ok = wait_counter(c_ready, c + 1, s_abort);
+        if (ok) ok = mbar_wait(bar_v, c & 1);
+        if (!named_and(BAR_STATE, NSTATE, ok)) { alive = false; break; }
+      }
+      if (lead) {
+        tc_fence_after();
+        // U^T = V^T TB^T - H^T W^T
+        for (int k = 0; k < 4; ++k)
+          umma_ss(tmem + T_U, mnmajor_desc(sb + S_V, 64, k), kmajor_desc(sb + S_TB, 64, k),
+                  idesc_f16(128, 64, 1, 1, 0), k > 0);
+        for (int k = 0; k < 8; ++k)
+          umma_ss(tmem + T_U, kmajor_desc(sb + S_HT, 128, k), mnmajor_desc(sb + S_W, 128, k),
+                  idesc_f16(128, 64, 0, 0, 1), 1);
+        umma_commit(bar_s1);
+        // O^T = H^T (q*gamma)^T
+        for (int k = 0; k < 8; ++k)
+          umma_ss(tmem + T_O, kmajor_desc(sb + S_HT, 128, k), kmajor_desc(sb + S_QG, 64, k),
+                  idesc_f16(128, 64, 0, 0, 0), k > 0);
+      }
+      {
+        const bool ok = mbar_wait(bar_s1, c & 1);
+        if (!named_and(BAR_STATE, NSTATE, ok)) { alive = false; break; }
+        tc_fence_after();
+      }
+      if (lead) {
+        st_release(c_s1, c + 1);
+        if (c + 1 < nchunks) {  // the v tile is free: fetch the next one
+          mbar_arrive_expect_tx(bar_v, 16384);
+          tma_load_2d(sm + S_V, &mv, bar_v, 0, (int)(u.row0 + (long)(c + 1) * C));
+          tma_load_2d(sm + S_V + 8192, &mv, bar_v, 64, (int)(u.row0 + (long)(c + 1) * C));
+        }
+      }
+      // U^T -> fp16 [j][s]
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        uint32_t v[32];
+        tmem_ld32<32>(tmem + lb + T_U + 32 * h2, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int z = 0; z < 32; z += 8) {
+          float f[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(v[z + e]);
+          ovf |= !fp16_ok8(f);
+          store16(sm + S_UT + sw128_chunk(128, s, (32 * h2 + z) >> 3), pack_half8(f));
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      named_sync(BAR_STATE, NSTATE);
+      if (lead) {
+        tc_fence_after();
+        // H^T += U^T (k*rho);  O^T += U^T A^T
+        for (int k = 0; k < 4; ++k)
+          umma_ss(tmem + T_H, kmajor_desc(sb + S_UT, 128, k), mnmajor_desc(sb + S_KH, 64, k),
+                  idesc_f16(128, 128, 0, 0, 1), 1);
+        for (int k = 0; k < 4; ++k)
+          umma_ss(tmem + T_O, kmajor_desc(sb + S_UT, 128, k),
+                  kmajor_desc(sb + S_AQ + 8192 * buf, 64, k), idesc_f16(128, 64, 0, 0, 0), 1);
+        umma_commit(bar_s3);
+      }
+      {
+        const bool ok = mbar_wait(bar_s3, c & 1);
+        if (!named_and(BAR_STATE, NSTATE, ok)) { alive = false; break; }
+        tc_fence_after();
+      }
+      if (lead) st_release(c_s3, c + 1);
+      // outputs o[t][j] = scale * O^T[j][t]
+      {
+        const long rbase = u.row0 + (long)c * C;
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          uint32_t v[32];
+          tmem_ld32<32>(tmem + lb + T_O + 32 * h2, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int t = 32 * h2 + e;
+            if (t < lenc)
+              go[(size_t)(rbase + t) * 128 + s] = __float2bfloat16_rn(a.scale * __uint_as_float(v[e]));
+          }
+        }
+      }
+      if (c + 1 < nchunks) {
+        const bool ok = wait_counter(c_gc, c + 2, s_abort);
+        if (!named_and(BAR_STATE, NSTATE, ok)) { alive = false; break; }
+        convert_and_scale(c + 1, false);
+        fence_proxy_async_smem();
+        tc_fence_before();
+        named_sync(BAR_STATE, NSTATE);
+      }
+    }
+    if (alive && nchunks > 0 && hT) {
+      for (int i0 = 0; i0 < 128; i0 += 32) {
+        uint32_t v[32];
+        tmem_ld32<32>(tmem + lb + T_H + i0, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) hT[u.sidx + (size_t)(i0 + e) * 128 + s] = __uint_as_float(v[e]);
+      }
+    }
+    if (!alive) *reinterpret_cast<volatile int*>(s_abort) = 1;
   }
 
-  // ------------------------------------------------------------ final state
-  if (!aborted && a.hT) {
-    const int j = 32 * wq + lane;
-    for (int c32 = 0; c32 < 2; ++c32) {
-      const int i0 = 64 * half + 32 * c32;
-      uint32_t v[32];
-      tmem_ld32<32>(tmem + lane_base + T_H + i0, v);
-      tmem_ld_wait();
-#pragma unroll
-      for (int e = 0; e < 32; ++e) a.hT[u.sidx + (size_t)(i0 + e) * 128 + j] = __uint_as_float(v[e]);
+  // ---------------------------------------------------------------- teardown
+  tc_fence_before();
+  const int any_ovf = __syncthreads_or(ovf ? 1 : 0);
+  if (tid == 0) {
+    if (any_ovf) set_status(a.status, CKDA_ERR_RANGE);
+    if (*reinterpret_cast<volatile int*>(s_abort)) {
+      set_status(a.status, CKDA_ERR_TIMEOUT);
+      // let any MMA or copy still in flight land before the memory is released
+      mbar_wait(bar_gram, 0, 1u << 16);
+      mbar_wait(bar_w, 0, 1u << 16);
+      mbar_wait(bar_s1, 0, 1u << 16);
+      mbar_wait(bar_s3, 0, 1u << 16);
+      mbar_wait(bar_v, 0, 1u << 16);
     }
   }
-  if (__syncthreads_or(ovf ? 1 : 0) && tid == 0) set_status(a.status, CKDA_ERR_RANGE);
-  if (tid == 0 && tma_pending && aborted) {
-    // a load of the next chunk may still be landing in shared memory
-    mbar_wait(bar_tma, (uint32_t)(tma_next & 1));
-  }
-  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
   if (warp == 0) tmem_dealloc(tmem, TMEM_COLS);
 }
 
@@ -634,19 +1046,16 @@ cudaError_t launch_fwd_chunk(const FwdArgs& a, cudaStream_t s) {
   const int units = a.num_units_seq * a.H;
   if (units == 0) return cudaSuccess;
   const uint64_t rows = (uint64_t)a.B * a.H * a.T;
-  CUtensorMap mq, mk, ma, mv;
+  CUtensorMap mv;
   if (rows == 0) {
-    // every sequence is empty: the kernel only copies h0 to hT, no tile is loaded
-    mq = mk = ma = mv = CUtensorMap{};
-  } else if (!make_map(&mq, a.q, rows) || !make_map(&mk, a.k, rows) ||
-             !make_map(&ma, a.alpha, rows) || !make_map(&mv, a.v, rows)) {
+    mv = CUtensorMap{};  // every sequence is empty: no tile is ever loaded
+  } else if (!make_map(&mv, a.v, rows)) {
     return cudaErrorInvalidValue;
   }
-  // per device and cheap: set on every launch
-  cudaError_t attr_err = cudaFuncSetAttribute(
+  cudaError_t err = cudaFuncSetAttribute(
       fwd_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_ALLOC);
-  if (attr_err != cudaSuccess) return attr_err;
-  fwd_chunk_kernel<<<units, NT, SMEM_ALLOC, s>>>(a, mq, mk, ma, mv);
+  if (err != cudaSuccess) return err;
+  fwd_chunk_kernel<<<units, NT, SMEM_ALLOC, s>>>(a, mv);
   return cudaGetLastError();
 }
 

@@ -216,6 +216,40 @@ __device__ __forceinline__ uint64_t mnmajor_desc(uint32_t tile, uint32_t R, int 
   return sw128_desc(tile + (uint32_t)kstep * 2048u, R * 128u, 1024u);
 }
 
+// ------------------------------------------- named barriers and handoffs
+__device__ __forceinline__ void named_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+// Barrier over `nthreads` threads that also returns the AND of `pred` across them.
+__device__ __forceinline__ bool named_and(int id, int nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, %2, %3, p;\n"
+      " selp.u32 %0, 1, 0, q;\n}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+__device__ __forceinline__ void st_release(int* p, int v) {
+  asm volatile("st.release.cta.shared::cta.s32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
+}
+__device__ __forceinline__ int ld_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.cta.shared::cta.s32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+  return v;
+}
+// Waits until *counter >= target or *abort is set; bounded.
+__device__ __forceinline__ bool wait_counter(const int* counter, int target, const int* abort,
+                                             uint32_t limit = (1u << 24)) {
+  for (uint32_t i = 0; i < limit; ++i) {
+    if (ld_acquire(counter) >= target) return true;
+    if (*reinterpret_cast<const volatile int*>(abort)) return false;
+    __nanosleep(32);
+  }
+  return false;
+}
+
 // ------------------------------------------------------ small conversions
 __device__ __forceinline__ uint32_t pack_half2(float a, float b) {
   __half2 h = __floats2half2_rn(a, b);
