@@ -190,3 +190,31 @@ def selftest_timeout(workspace, spin_limit=1000, stream=None) -> int:
     if rc != 0:
         raise CkdaError(rc, "ckda_selftest_timeout")
     return fwd_status(workspace, stream)
+
+
+def fwd_noalloc(q, k, v, alpha, beta, h0=None, cu_seqlens=None, scale=1.0, chunk_size=0,
+                o=None, hT=None, stream=None):
+    """ckda_fwd_noalloc: the forward without a workspace, for callers that may
+    not allocate device memory (its scratch is a fixed array inside libckda).
+    o and hT may be passed in so that the call itself allocates nothing."""
+    L = lib()
+    fn = L.ckda_fwd_noalloc
+    if fn.argtypes is None:
+        vp, i32, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        fn.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32,
+                       i32, i32, i32, i32, i32, i32, f32, i32, vp]
+        fn.restype = i32
+    device = q.device
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    N = B if cu_seqlens is None else cu_seqlens.numel() - 1
+    if o is None:
+        o = torch.empty((B, H, T, dv), dtype=q.dtype, device=device)
+    if hT is None:
+        hT = torch.empty((N, H, dk, dv), dtype=torch.float32, device=device)
+    rc = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(h0), _ptr(o), _ptr(hT),
+            _ptr(cu_seqlens), int(N if cu_seqlens is not None else 0), B, H, T, dk, dv,
+            _io_dtype(q), float(scale), int(chunk_size), _stream_handle(stream, device))
+    if rc != 0:
+        raise CkdaError(rc, "ckda_fwd_noalloc")
+    return o, hT

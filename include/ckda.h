@@ -109,6 +109,36 @@ ckda_status ckda_fwd(const void *q, const void *k, const void *v,
                      size_t workspace_bytes, void *stream);
 
 /*
+ * ckda_fwd for callers that cannot allocate device memory.  The paper has no
+ * counterpart; this is a deployment variant of ckda_fwd.
+ *
+ * Same arguments and results as ckda_fwd, minus the workspace.  It is meant
+ * for callers that may not call cudaMalloc.  One example is a host
+ * application that splits its device memory once at start-up and forbids
+ * later allocation.  Another is a plugin whose host owns the only allocator.
+ * The scratch ckda_fwd would take from a workspace lives instead in a fixed
+ * array in this library's device memory: 256 KiB + 256 B on every GPU that
+ * loads the library, held until the process exits.  Nothing is allocated or
+ * freed per call.
+ *
+ *   - Packed input is limited to num_seqs <= 65536; more returns
+ *     CKDA_ERR_UNSUPPORTED before anything is launched.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current).  Make that first call before any stream capture.
+ *   - Every call shares the one array.  Calls whose GPU work overlaps (on
+ *     different streams, or from several threads at once) race on it and
+ *     must be serialised by the caller.  Each call clears the status word it
+ *     uses and rewrites the work order it reads.
+ *   - Device-side conditions (timeout, fp16 range) are recorded in the shared
+ *     array and are not reported; use ckda_fwd to observe them.
+ */
+ckda_status ckda_fwd_noalloc(const void *q, const void *k, const void *v,
+                             const void *alpha, const void *beta, const float *h0,
+                             void *o, float *hT, const int32_t *cu_seqlens, int num_seqs,
+                             int B, int H, int T, int dk, int dv, ckda_dtype io_dtype,
+                             float scale, int chunk_size, void *stream);
+
+/*
  * Reads (and clears) the device status word of a workspace: waits for
  * `stream`, then returns CKDA_OK, CKDA_ERR_TIMEOUT or CKDA_ERR_RANGE for the
  * most recent ckda_fwd (or self-test) enqueued with that workspace.
