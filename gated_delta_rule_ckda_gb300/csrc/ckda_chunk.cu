@@ -61,28 +61,30 @@ constexpr int BAR_PREP = 1;   // named barrier ids
 constexpr int BAR_STATE = 2;
 
 // ---- shared memory map (bytes from a 1024-aligned base) ----
-constexpr uint32_t S_V = 0;          // bf16 v tile   [64 s][128 j]  MN-major A of U~   (TMA)
-constexpr uint32_t S_HT = 16384;     // fp16 H^T      [128 j][128 i] K-major A of U, O
-constexpr uint32_t S_UT = 49152;     // fp16 U^T      [128 j][64 s]  K-major A of H, O
+constexpr uint32_t S_TQ = 0;         // bf16 q tile   [64 t][128 i]  (TMA, one chunk ahead)
+constexpr uint32_t S_TK = 16384;     // bf16 k tile
+constexpr uint32_t S_TA = 32768;     // bf16 alpha tile
+constexpr uint32_t S_V = 49152;      // bf16 v tile   [64 s][128 j]  MN-major A of U~   (TMA)
 constexpr uint32_t S_TB = 65536;     // bf16 T Diag(beta) [64 t][64 s] K-major B of U~, W
 constexpr uint32_t S_W = 73728;      // fp16 -W^T     [128 i][64 t]  MN-major B of U
 constexpr uint32_t S_QG = 90112;     // fp16 q*gamma  [64 t][128 i]  K-major B of O
 constexpr uint32_t S_KH = 106496;    // fp16 k*rho    [64 s][128 i]  MN-major B of H
 constexpr uint32_t S_KGT = 122880;   // bf16 k*gamma  [64 s][128 i]  MN-major A of W
-constexpr uint32_t S_AQ = 139264;    // fp16 A        [64 t][64 s]   K-major B of O   (x2)
-constexpr uint32_t S_GX = 155648;    // fp16 Gram X   [128 rows][128 i] K-major A
-constexpr uint32_t S_GY = 188416;    // fp16 Gram Y   [64 rows][128 i]  K-major B
+constexpr uint32_t S_AQ = 139264;    // fp16 A        [64 t][64 s]   K-major B of O
+constexpr uint32_t S_GX = 147456;    // fp16 Gram X   [128 rows][128 i] K-major A
+constexpr uint32_t S_GY = 180224;    // fp16 Gram Y   [64 rows][128 i]  K-major B
 // after the Gram MMAs the 48 KiB of X and Y hold the inverse's 64 x 64 tiles
 // (fp16, one 64-column panel each).  A tile read as a 128-row A operand also
 // reads the 8 KiB after it; those rows only feed TMEM lanes that are ignored.
-constexpr uint32_t S_TN = S_GX;              // N: block-strictly-lower part of M
 constexpr uint32_t S_TD = S_GX + 8192;       // D: inverses of the 16 x 16 diagonal blocks
 constexpr uint32_t S_TE = S_GX + 16384;      // E = D N
 constexpr uint32_t S_TG = S_GX + 24576;      // G = I + E^2
 constexpr uint32_t S_TFm = S_GY;             // F = (I - E) G
-constexpr uint32_t S_MD = S_GY + 8192;       // fp32 diagonal 16 x 16 blocks of M [4][16][20]
+// written by the Gram read-out while later Gram MMAs still read X and Y:
+constexpr uint32_t S_TN = 196608;            // fp16 N: block-strictly-lower part of M
+constexpr uint32_t S_MD = 204800;            // fp32 diagonal 16 x 16 blocks of M [4][16][20]
 constexpr int kMdRow = 20, kMdBlk = 16 * kMdRow;  // padded rows spread the banks
-constexpr uint32_t S_SMALL = 204800;
+constexpr uint32_t S_SMALL = 209920;
 constexpr uint32_t S_BETA = S_SMALL;         // fp32 [2][64]
 constexpr uint32_t S_GC = S_SMALL + 512;     // fp32 [2][128] gamma_C
 constexpr uint32_t S_DIAG = S_SMALL + 1536;  // fp32 [16][64] partial q.k
@@ -92,12 +94,16 @@ constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;
 static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
 
 // ---- tensor memory columns ----
-constexpr uint32_t T_H = 0;     // H^T fp32 [128 j][128 i]
-constexpr uint32_t T_U = 128;   // U^T fp32 [128 j][64 t]
-constexpr uint32_t T_O = 192;   // O^T fp32 [128 j][64 t]
-constexpr uint32_t T_G = 256;   // 3 Gram tiles [128 x][64 y]
-constexpr uint32_t T_W = 448;   // W^T fp32 [128 i][64 t]
+constexpr uint32_t T_H = 0;     // H^T fp32 [128 j][128 i]     state accumulator
+constexpr uint32_t T_HA = 128;  // H^T fp16 [128 j][128 i]     A operand (2 per column)
+constexpr uint32_t T_U = 192;   // U^T fp32 [128 j][64 t]
+constexpr uint32_t T_UA = 256;  // U^T fp16 [128 j][64 t]      A operand
+constexpr uint32_t T_O = 288;   // O^T fp32 [128 j][64 t]
+constexpr uint32_t T_G0 = 352;  // Gram rounds alternate G0, G1, G0; the inverse chain
+constexpr uint32_t T_G1 = 416;  //   uses E:G0, E^2:G1, EG:G0, T:G1; then W^T:G0
 constexpr uint32_t TMEM_COLS = 512;
+
+constexpr uint32_t TILE_BYTES = 16384;
 
 struct Unit {
   long row0;
@@ -396,14 +402,24 @@ __device__ __forceinline__ void extract_level(uint8_t* sm, uint32_t taddr, int x
 }
 
 template <int La>
-__device__ __forceinline__ void extract_round(uint8_t* sm, uint32_t tmem, int r, int wq, int lane,
-                                              const float* beta, uint8_t* AQ) {
+__device__ __forceinline__ void extract_round(uint8_t* sm, uint32_t tmem, uint32_t col, int wq,
+                                              int lane, const float* beta, uint8_t* AQ) {
   const int x = 32 * wq + lane;  // warp-uniform level: lanes 0..63 level La, 64..127 La/2
-  const uint32_t base = tmem + ((uint32_t)(32 * wq) << 16) + T_G + 64 * r;
+  const uint32_t base = tmem + ((uint32_t)(32 * wq) << 16) + col;
   if (x < 64)
     extract_level<La>(sm, base, x & 63, beta, AQ);
   else
     extract_level<La / 2>(sm, base + 32, x & 63, beta, AQ);
+}
+
+// D (tmem) (+)= A (tmem) x B (smem), issued by a single thread.
+__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                        uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
 }
 
 // Inverses of the four unit-lower 16 x 16 diagonal blocks of I + M, by
@@ -426,7 +442,9 @@ __device__ __forceinline__ void invert_diag_blocks(uint8_t* sm, int p) {
 }
 
 __global__ void __launch_bounds__(NT, 1)
-    fwd_chunk_kernel(const __grid_constant__ FwdArgs a, const __grid_constant__ CUtensorMap mv) {
+    fwd_chunk_kernel(const __grid_constant__ FwdArgs a, const __grid_constant__ CUtensorMap mq,
+                     const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap ma,
+                     const __grid_constant__ CUtensorMap mv) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -437,6 +455,7 @@ __global__ void __launch_bounds__(NT, 1)
   uint64_t* bar_s1 = bar_v + 3;
   uint64_t* bar_s3 = bar_v + 4;
   uint64_t* bar_t = bar_v + 5;
+  uint64_t* bar_qka = bar_v + 6;
   int* cnt = reinterpret_cast<int*>(sm + S_BAR + 64);
   int* c_ready = cnt + 0;  // prep -> state: chunks whose operands are complete
   int* c_gc = cnt + 1;     // prep -> state: chunks whose gamma_C is published
@@ -455,13 +474,20 @@ __global__ void __launch_bounds__(NT, 1)
     mbar_init(bar_s1, 1);
     mbar_init(bar_s3, 1);
     mbar_init(bar_t, 1);
+    mbar_init(bar_qka, 1);
     for (int i = 0; i < 8; ++i) cnt[i] = 0;
     fence_mbar_init();
+    tma_prefetch_desc(&mq);
+    tma_prefetch_desc(&mk);
+    tma_prefetch_desc(&ma);
     tma_prefetch_desc(&mv);
   }
-  // A: its upper triangle is never written again, so zero it once
-  for (int e = tid; e < 2 * 8192 / 16; e += NT)
+  // A's upper triangle and N's blocks on and above the 16-block diagonal are
+  // never written again, so zero both tiles once
+  for (int e = tid; e < 8192 / 16; e += NT) {
     reinterpret_cast<uint4*>(sm + S_AQ)[e] = make_uint4(0, 0, 0, 0);
+    reinterpret_cast<uint4*>(sm + S_TN)[e] = make_uint4(0, 0, 0, 0);
+  }
   if (warp == 0) {
     tmem_alloc(tmem_slot, TMEM_COLS);
     tmem_relinquish();
@@ -480,9 +506,6 @@ __global__ void __launch_bounds__(NT, 1)
     const int j = 2 * w + (lane >> 4);  // channel chunk
     const int tq = lane & 15;           // token quad
     const int wq = w & 3, half = w >> 2;
-    const __nv_bfloat16* gq = static_cast<const __nv_bfloat16*>(a.q);
-    const __nv_bfloat16* gk = static_cast<const __nv_bfloat16*>(a.k);
-    const __nv_bfloat16* ga = static_cast<const __nv_bfloat16*>(a.alpha);
     const __nv_bfloat16* gb = static_cast<const __nv_bfloat16*>(a.beta);
     uint32_t gram_phase = 0, t_phase = 0;
     bool alive = true;
@@ -495,8 +518,20 @@ __global__ void __launch_bounds__(NT, 1)
         beta_next[uu] = t < len0 ? __bfloat162float(gb[u.row0 + t]) : 0.f;
       }
     }
-    // waits on an mbarrier fed by this role's MMAs; the AND over the role
-    // decides, uniformly, whether to go on
+    // q, k, alpha tiles of chunk cc (issued by one thread)
+    auto issue_qka = [&](int cc) {
+      const int y = (int)(u.row0 + (long)cc * C);
+      mbar_arrive_expect_tx(bar_qka, 3 * TILE_BYTES);
+      tma_load_2d(sm + S_TQ, &mq, bar_qka, 0, y);
+      tma_load_2d(sm + S_TQ + 8192, &mq, bar_qka, 64, y);
+      tma_load_2d(sm + S_TK, &mk, bar_qka, 0, y);
+      tma_load_2d(sm + S_TK + 8192, &mk, bar_qka, 64, y);
+      tma_load_2d(sm + S_TA, &ma, bar_qka, 0, y);
+      tma_load_2d(sm + S_TA + 8192, &ma, bar_qka, 64, y);
+    };
+    if (p == 0 && nchunks > 0) issue_qka(0);
+    // waits on an mbarrier fed by this role's MMAs or copies; the AND over
+    // the role decides, uniformly, whether to go on
     auto prep_wait = [&](uint64_t* bar, uint32_t& phase) -> bool {
       const bool ok = mbar_wait(bar, phase & 1);
       ++phase;
@@ -510,46 +545,55 @@ __global__ void __launch_bounds__(NT, 1)
     };
     // the MMA of the inverse chain: D[lanes 0..63] = A (rows 0..63 used) x B
     auto t_mma = [&](uint32_t d_col, uint32_t a_tile, uint32_t b_tile) {
+      const uint64_t da = kmajor_desc(sb + a_tile, 128, 0), db = mnmajor_desc(sb + b_tile, 64, 0);
+#pragma unroll
       for (int k = 0; k < 4; ++k)
-        umma_ss(tmem + d_col, kmajor_desc(sb + a_tile, 128, k), mnmajor_desc(sb + b_tile, 64, k),
+        umma_ss(tmem + d_col, da + (uint64_t)(2 * k), db + (uint64_t)(128 * k),
                 idesc_f16(128, 64, 0, 0, 1), k > 0);
       umma_commit(bar_t);
+    };
+    const uint64_t d_gx = kmajor_desc(sb + S_GX, 128, 0), d_gy = kmajor_desc(sb + S_GY, 64, 0);
+    auto gram_mma = [&](uint32_t d_col) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k)  // K steps: 32 bytes in a panel, panels R*128 apart
+        umma_ss(tmem + d_col, d_gx + (uint64_t)((k >> 2) * 1024 + (k & 3) * 2),
+                d_gy + (uint64_t)((k >> 2) * 512 + (k & 3) * 2), idesc_f16(128, 64, 0, 0, 0),
+                k > 0);
+      umma_commit(bar_gram);
     };
     const bool tconv = wq < 2;  // warps 0,1,4,5 reach TMEM lanes 0..63
     const int trow = 32 * wq + lane;
     const uint32_t tl = (uint32_t)(32 * (wq & 1)) << 16;
+    const uint32_t tlw = (uint32_t)(32 * wq) << 16;
+    uint8_t* AQ = sm + S_AQ;
 
     for (int c = 0; c < nchunks && alive; ++c) {
       const int lenc = min(C, u.len - c * C);
       const int buf = c & 1;
       const long rbase = u.row0 + (long)c * C;
-      // ---- loads: 4 tokens x 8 channels of q, k, alpha (rows past the end of
-      // the sequence are clamped to a valid row and then masked)
+      // ---- this chunk's q, k, alpha tiles
+      {
+        uint32_t ph = (uint32_t)c;
+        if (!prep_wait(bar_qka, ph)) { alive = false; break; }
+      }
       Prep P;
       P.tq = tq;
       float Bq[8];
       {
-        uint4 rk[4], rq[4], ra[4];
-#pragma unroll
-        for (int uu = 0; uu < 4; ++uu) {
-          const int t = min(4 * tq + uu, lenc - 1);
-          const size_t off = (size_t)(rbase + t) * 128 + 8 * j;
-          rk[uu] = __ldg(reinterpret_cast<const uint4*>(gk + off));
-          rq[uu] = __ldg(reinterpret_cast<const uint4*>(gq + off));
-          ra[uu] = __ldg(reinterpret_cast<const uint4*>(ga + off));
-        }
         float al[4][8];
         float mx = 0.f;
 #pragma unroll
         for (int uu = 0; uu < 4; ++uu) {
-          const bool valid = 4 * tq + uu < lenc;
+          const int t = 4 * tq + uu;
+          const bool valid = t < lenc;
+          const uint32_t off = sw128_chunk(64, t, j);
           float kk[8], qq[8];
-          unpack_bf16x8(rk[uu], kk);
-          unpack_bf16x8(rq[uu], qq);
-          mx = fmaxf(mx, fmaxf(absmax8(kk), absmax8(qq)));
+          unpack_bf16x8(*reinterpret_cast<const uint4*>(sm + S_TK + off), kk);
+          unpack_bf16x8(*reinterpret_cast<const uint4*>(sm + S_TQ + off), qq);
+          unpack_bf16x8(*reinterpret_cast<const uint4*>(sm + S_TA + off), al[uu]);
+          if (valid) mx = fmaxf(mx, fmaxf(absmax8(kk), absmax8(qq)));
           P.k[uu] = valid ? to_half8(kk) : make_uint4(0, 0, 0, 0);
           P.q[uu] = valid ? to_half8(qq) : make_uint4(0, 0, 0, 0);
-          unpack_bf16x8(ra[uu], al[uu]);
 #pragma unroll
           for (int e = 0; e < 8; ++e) al[uu][e] = valid ? al[uu][e] : 1.f;  // identity transition
         }
@@ -578,16 +622,9 @@ __global__ void __launch_bounds__(NT, 1)
         P.a2 = to_half8(al[2]);
         P.a3 = to_half8(al[3]);
       }
-      // warm L2 with the next chunk's rows of q, k, alpha (two lines per thread)
-      if (c + 1 < nchunks) {
-        const int t = p & 63, which = p >> 6;
-        if (which < 3 && t < min(C, u.len - (c + 1) * C)) {
-          const __nv_bfloat16* base = which == 0 ? gq : which == 1 ? gk : ga;
-          const char* line = reinterpret_cast<const char*>(base + (size_t)(rbase + C + t) * 128);
-          asm volatile("prefetch.global.L2 [%0];" ::"l"(line));
-          asm volatile("prefetch.global.L2 [%0];" ::"l"(line + 128));
-        }
-      }
+      // the tiles are consumed: fetch the next chunk's while this one runs
+      named_sync(BAR_PREP, NPREP);
+      if (p == 0 && c + 1 < nchunks) issue_qka(c + 1);
       // beta: this chunk's values were loaded one chunk ahead
       float* beta_s = reinterpret_cast<float*>(sm + S_BETA) + 64 * buf;
       if (j == 0) {
@@ -630,33 +667,20 @@ __global__ void __launch_bounds__(NT, 1)
       named_sync(BAR_PREP, NPREP);
       if (p == 0) st_release(c_gc, c + 1);
 
-      // ---- gated Grams: 3 rounds of (write operands, MMA)
-#pragma unroll 1
-      for (int r = 0; r < 3; ++r) {
-        if (r > 0 && !prep_wait(bar_gram, gram_phase)) { alive = false; break; }
-        if (r == 0) {
-          write_level<32>(sm, P, j, 0, 0);
-          write_level<16>(sm, P, j, 64, 32);
-        } else if (r == 1) {
-          write_level<8>(sm, P, j, 0, 0);
-          write_level<4>(sm, P, j, 64, 32);
-        } else {
-          write_level<2>(sm, P, j, 0, 0);
-          write_level<1>(sm, P, j, 64, 32);
-        }
-        fence_proxy_async_smem();
-        named_sync(BAR_PREP, NPREP);
-        if (p == 0) {
-          tc_fence_after();
-          for (int k = 0; k < 8; ++k)
-            umma_ss(tmem + T_G + 64 * r, kmajor_desc(sb + S_GX, 128, k),
-                    kmajor_desc(sb + S_GY, 64, k), idesc_f16(128, 64, 0, 0, 0), k > 0);
-          umma_commit(bar_gram);
-        }
-      }
-      if (!alive) break;
-
-      // ---- q*gamma, k*rho: the previous chunk's last MMA must have read them
+      // ---- gated Grams: round r writes X/Y, its MMA runs while round r-1
+      // is read out of TMEM (rounds use TMEM G0, G1, G0)
+      write_level<32>(sm, P, j, 0, 0);
+      write_level<16>(sm, P, j, 64, 32);
+      fence_proxy_async_smem();
+      named_sync(BAR_PREP, NPREP);
+      if (p == 0) { tc_fence_after(); gram_mma(T_G0); }
+      if (!prep_wait(bar_gram, gram_phase)) { alive = false; break; }
+      write_level<8>(sm, P, j, 0, 0);
+      write_level<4>(sm, P, j, 64, 32);
+      fence_proxy_async_smem();
+      named_sync(BAR_PREP, NPREP);
+      if (p == 0) { tc_fence_after(); gram_mma(T_G1); }
+      // q*gamma, k*rho: the previous chunk's last MMA must have read them (and A)
       if (!prep_counter(c_s3, c)) { alive = false; break; }
 #pragma unroll
       for (int uu = 0; uu < 4; ++uu) {
@@ -664,31 +688,20 @@ __global__ void __launch_bounds__(NT, 1)
         store16(sm + S_QG + sw128_chunk(64, t, j), hmul8h(P.q[uu], P.gamma(uu)));
         store16(sm + S_KH + sw128_chunk(64, t, j), hmul8h(P.k[uu], P.rho(uu)));
       }
-
-      // ---- the last Gram round, then read all three out
+      if (half == 0) extract_round<32>(sm, tmem, T_G0, wq, lane, beta_s, AQ);
+      tc_fence_before();
       if (!prep_wait(bar_gram, gram_phase)) { alive = false; break; }
-      uint8_t* AQ = sm + S_AQ + 8192 * buf;
-      {
-        // zero what the extraction does not write: N on and above the
-        // 16-block diagonal, and D (its diagonal blocks come next)
-        for (int e = p; e < 10 * 32; e += NPREP) {
-          // 10 blocks (I <= J) x 16 rows x 2 chunks of 16 bytes
-          const int blk = e >> 5, rr = (e >> 1) & 15, hh = e & 1;
-          int I = 0, J = blk;
-          if (blk >= 4) { I = 1; J = blk - 3; }
-          if (blk >= 7) { I = 2; J = blk - 5; }
-          if (blk >= 9) { I = 3; J = 3; }
-          store16(sm + S_TN + sw128_chunk(64, 16 * I + rr, 2 * J + hh), make_uint4(0, 0, 0, 0));
-        }
-        for (int e = p; e < 8192 / 16; e += NPREP)
-          store16(sm + S_TD + 16 * e, make_uint4(0, 0, 0, 0));
-      }
-      if (half == 0) {
-        extract_round<32>(sm, tmem, 0, wq, lane, beta_s, AQ);
-      } else {
-        extract_round<8>(sm, tmem, 1, wq, lane, beta_s, AQ);
-        extract_round<2>(sm, tmem, 2, wq, lane, beta_s, AQ);
-      }
+      write_level<2>(sm, P, j, 0, 0);
+      write_level<1>(sm, P, j, 64, 32);
+      fence_proxy_async_smem();
+      named_sync(BAR_PREP, NPREP);
+      if (p == 0) { tc_fence_after(); gram_mma(T_G0); }
+      if (half == 1) extract_round<8>(sm, tmem, T_G1, wq, lane, beta_s, AQ);
+      tc_fence_before();
+      if (!prep_wait(bar_gram, gram_phase)) { alive = false; break; }
+      // D lives where Gram X was: zero it (its diagonal blocks come next)
+      for (int e = p; e < 8192 / 16; e += NPREP) store16(sm + S_TD + 16 * e, make_uint4(0, 0, 0, 0));
+      if (half == 0) extract_round<2>(sm, tmem, T_G0, wq, lane, beta_s, AQ);
       tc_fence_before();
       named_sync(BAR_PREP, NPREP);
       // ---- T = (I + M)^-1 = (I - E)(I + E^2) D with D the inverse of the
@@ -706,11 +719,11 @@ __global__ void __launch_bounds__(NT, 1)
       }
       fence_proxy_async_smem();
       named_sync(BAR_PREP, NPREP);
-      if (p == 0) { tc_fence_after(); t_mma(T_G, S_TD, S_TN); }        // E = D N
+      if (p == 0) { tc_fence_after(); t_mma(T_G0, S_TD, S_TN); }       // E = D N
       if (!prep_wait(bar_t, t_phase)) { alive = false; break; }
       if (tconv) {
         uint32_t v[32];
-        tmem_ld32<32>(tmem + tl + T_G + 32 * half, v);
+        tmem_ld32<32>(tmem + tl + T_G0 + 32 * half, v);
         tmem_ld_wait();
 #pragma unroll
         for (int z = 0; z < 32; z += 8) {
@@ -723,12 +736,12 @@ __global__ void __launch_bounds__(NT, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       named_sync(BAR_PREP, NPREP);
-      if (p == 0) { tc_fence_after(); t_mma(T_G + 64, S_TE, S_TE); }   // E^2
+      if (p == 0) { tc_fence_after(); t_mma(T_G1, S_TE, S_TE); }       // E^2
       if (!prep_wait(bar_t, t_phase)) { alive = false; break; }
       float gv[32];  // G = I + E^2, kept for F
       if (tconv) {
         uint32_t v[32];
-        tmem_ld32<32>(tmem + tl + T_G + 64 + 32 * half, v);
+        tmem_ld32<32>(tmem + tl + T_G1 + 32 * half, v);
         tmem_ld_wait();
 #pragma unroll
         for (int z = 0; z < 32; ++z)
@@ -744,11 +757,11 @@ __global__ void __launch_bounds__(NT, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       named_sync(BAR_PREP, NPREP);
-      if (p == 0) { tc_fence_after(); t_mma(T_G + 128, S_TE, S_TG); }  // E G
+      if (p == 0) { tc_fence_after(); t_mma(T_G0, S_TE, S_TG); }       // E G
       if (!prep_wait(bar_t, t_phase)) { alive = false; break; }
       if (tconv) {
         uint32_t v[32];
-        tmem_ld32<32>(tmem + tl + T_G + 128 + 32 * half, v);
+        tmem_ld32<32>(tmem + tl + T_G0 + 32 * half, v);
         tmem_ld_wait();
 #pragma unroll
         for (int z = 0; z < 32; z += 8) {
@@ -761,14 +774,14 @@ __global__ void __launch_bounds__(NT, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       named_sync(BAR_PREP, NPREP);
-      if (p == 0) { tc_fence_after(); t_mma(T_W, S_TFm, S_TD); }       // T = F D
+      if (p == 0) { tc_fence_after(); t_mma(T_G1, S_TFm, S_TD); }      // T = F D
       if (!prep_wait(bar_t, t_phase)) { alive = false; break; }
       // ---- T Diag(beta) as bf16; TB and W are single-buffered: the previous
       // chunk's U-MMA must have read them
       if (!prep_counter(c_s1, c)) { alive = false; break; }
       if (tconv) {
         uint32_t v[32];
-        tmem_ld32<32>(tmem + tl + T_W + 32 * half, v);
+        tmem_ld32<32>(tmem + tl + T_G1 + 32 * half, v);
         tmem_ld_wait();
 #pragma unroll
         for (int z = 0; z < 32; z += 8) {
@@ -787,8 +800,10 @@ __global__ void __launch_bounds__(NT, 1)
       if (p == 0) {
         tc_fence_after();
         // W^T[i][t] = sum_s (k*gamma)[s][i] TB[t][s]
+        const uint64_t da = mnmajor_desc(sb + S_KGT, 64, 0), db = kmajor_desc(sb + S_TB, 64, 0);
+#pragma unroll
         for (int k = 0; k < 4; ++k)
-          umma_ss(tmem + T_W, mnmajor_desc(sb + S_KGT, 64, k), kmajor_desc(sb + S_TB, 64, k),
+          umma_ss(tmem + T_G0, da + (uint64_t)(128 * k), db + (uint64_t)(2 * k),
                   idesc_f16(128, 64, 1, 1, 0), k > 0);
         umma_commit(bar_w);
       }
@@ -799,7 +814,7 @@ __global__ void __launch_bounds__(NT, 1)
       {  // -W^T as fp16 [i][t] (MN-major B): lane = i, 32 columns per half
         const int i = 32 * wq + lane;
         uint32_t v[32];
-        tmem_ld32<32>(tmem + ((uint32_t)(32 * wq) << 16) + T_W + 32 * half, v);
+        tmem_ld32<32>(tmem + tlw + T_G0 + 32 * half, v);
         tmem_ld_wait();
 #pragma unroll
         for (int z = 0; z < 32; z += 8) {
@@ -822,28 +837,16 @@ __global__ void __launch_bounds__(NT, 1)
     const int wq = s >> 5;       // warps 8..11 -> lane groups 0..3
     const uint32_t lb = (uint32_t)(32 * wq) << 16;
     const bool lead = s == 0;
-    uint8_t* HT = sm + S_HT;
     float* hT = a.hT;
     bool alive = true;
     if (lead && nchunks > 0) {
-      mbar_arrive_expect_tx(bar_v, 16384);
+      mbar_arrive_expect_tx(bar_v, TILE_BYTES);
       tma_load_2d(sm + S_V, &mv, bar_v, 0, (int)u.row0);
       tma_load_2d(sm + S_V + 8192, &mv, bar_v, 64, (int)u.row0);
     }
-    // initial state -> TMEM (fp32) and H^T fp16 in smem
-    auto store_HT = [&](int i0, const float (&f)[32]) {
-#pragma unroll
-      for (int z = 0; z < 32; z += 8) {
-        float g[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) g[e] = f[z + e];
-        ovf |= !fp16_ok8(g);
-        store16(HT + sw128_chunk(128, s, (i0 + z) >> 3), pack_half8(g));
-      }
-    };
     const float* gc_all = reinterpret_cast<const float*>(sm + S_GC);
-    // scales the TMEM state by gamma_C of chunk c (column i times gC[i]) after
-    // writing its unscaled fp16 copy
+    // H^T as the fp16 A operand (TMEM) and, in TMEM, H^T Diag(gamma_C) of
+    // the chunk about to start (column i times gC[i])
     auto convert_and_scale = [&](int c_next, bool from_h0) {
       const float* gC = gc_all + 128 * (c_next & 1);
 #pragma unroll 1
@@ -860,12 +863,26 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
           for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(v[e]);
         }
-        store_HT(i0, f);
+        uint32_t h[16];
+        float mx = 0.f;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          h[e] = pack_half2(f[2 * e], f[2 * e + 1]);
+          mx = fmaxf(mx, fmaxf(fabsf(f[2 * e]), fabsf(f[2 * e + 1])));
+        }
+        ovf |= !(mx <= 65504.f);
+        tmem_st32<16>(tmem + lb + T_HA + (i0 >> 1), h);
         uint32_t o[16];
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
 #pragma unroll
-          for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(f[16 * hh + e] * gC[i0 + 16 * hh + e]);
+          for (int e = 0; e < 16; e += 4) {
+            const float4 g4 = *reinterpret_cast<const float4*>(gC + i0 + 16 * hh + e);
+            o[e] = __float_as_uint(f[16 * hh + e] * g4.x);
+            o[e + 1] = __float_as_uint(f[16 * hh + e + 1] * g4.y);
+            o[e + 2] = __float_as_uint(f[16 * hh + e + 2] * g4.z);
+            o[e + 3] = __float_as_uint(f[16 * hh + e + 3] * g4.w);
+          }
           tmem_st32<16>(tmem + lb + T_H + i0 + 16 * hh, o);
         }
       }
@@ -879,14 +896,15 @@ __global__ void __launch_bounds__(NT, 1)
       for (int i = 0; i < 128; ++i)
         hT[u.sidx + (size_t)i * 128 + s] = a.h0 ? a.h0[u.sidx + (size_t)i * 128 + s] : 0.f;
     }
-    fence_proxy_async_smem();
     tc_fence_before();
     named_sync(BAR_STATE, NSTATE);
 
+    const uint64_t d_v = mnmajor_desc(sb + S_V, 64, 0), d_tb = kmajor_desc(sb + S_TB, 64, 0);
+    const uint64_t d_w = mnmajor_desc(sb + S_W, 128, 0), d_qg = kmajor_desc(sb + S_QG, 64, 0);
+    const uint64_t d_kh = mnmajor_desc(sb + S_KH, 64, 0), d_aq = kmajor_desc(sb + S_AQ, 64, 0);
     __nv_bfloat16* go = static_cast<__nv_bfloat16*>(a.o);
     for (int c = 0; c < nchunks && alive; ++c) {
       const int lenc = min(C, u.len - c * C);
-      const int buf = c & 1;
       {  // prep operands of chunk c, and its v tile
         bool ok = wait_counter(c_ready, c + 1, s_abort);
         if (ok) ok = mbar_wait(bar_v, c & 1);
@@ -895,17 +913,21 @@ __global__ void __launch_bounds__(NT, 1)
       if (lead) {
         tc_fence_after();
         // U^T = V^T TB^T - H^T W^T
+#pragma unroll
         for (int k = 0; k < 4; ++k)
-          umma_ss(tmem + T_U, mnmajor_desc(sb + S_V, 64, k), kmajor_desc(sb + S_TB, 64, k),
+          umma_ss(tmem + T_U, d_v + (uint64_t)(128 * k), d_tb + (uint64_t)(2 * k),
                   idesc_f16(128, 64, 1, 1, 0), k > 0);
+#pragma unroll
         for (int k = 0; k < 8; ++k)
-          umma_ss(tmem + T_U, kmajor_desc(sb + S_HT, 128, k), mnmajor_desc(sb + S_W, 128, k),
+          umma_ts(tmem + T_U, tmem + T_HA + 8 * k, d_w + (uint64_t)(128 * k),
                   idesc_f16(128, 64, 0, 0, 1), 1);
         umma_commit(bar_s1);
         // O^T = H^T (q*gamma)^T
+#pragma unroll
         for (int k = 0; k < 8; ++k)
-          umma_ss(tmem + T_O, kmajor_desc(sb + S_HT, 128, k), kmajor_desc(sb + S_QG, 64, k),
-                  idesc_f16(128, 64, 0, 0, 0), k > 0);
+          umma_ts(tmem + T_O, tmem + T_HA + 8 * k,
+                  d_qg + (uint64_t)((k >> 2) * 512 + (k & 3) * 2), idesc_f16(128, 64, 0, 0, 0),
+                  k > 0);
       }
       {
         const bool ok = mbar_wait(bar_s1, c & 1);
@@ -915,38 +937,44 @@ __global__ void __launch_bounds__(NT, 1)
       if (lead) {
         st_release(c_s1, c + 1);
         if (c + 1 < nchunks) {  // the v tile is free: fetch the next one
-          mbar_arrive_expect_tx(bar_v, 16384);
+          mbar_arrive_expect_tx(bar_v, TILE_BYTES);
           tma_load_2d(sm + S_V, &mv, bar_v, 0, (int)(u.row0 + (long)(c + 1) * C));
           tma_load_2d(sm + S_V + 8192, &mv, bar_v, 64, (int)(u.row0 + (long)(c + 1) * C));
         }
       }
-      // U^T -> fp16 [j][s]
-#pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {
+      // U^T -> fp16 A operand in TMEM
+      {
         uint32_t v[32];
-        tmem_ld32<32>(tmem + lb + T_U + 32 * h2, v);
-        tmem_ld_wait();
+        float mx = 0.f;
 #pragma unroll
-        for (int z = 0; z < 32; z += 8) {
-          float f[8];
+        for (int h2 = 0; h2 < 2; ++h2) {
+          tmem_ld32<32>(tmem + lb + T_U + 32 * h2, v);
+          tmem_ld_wait();
+          uint32_t hh[16];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(v[z + e]);
-          ovf |= !fp16_ok8(f);
-          store16(sm + S_UT + sw128_chunk(128, s, (32 * h2 + z) >> 3), pack_half8(f));
+          for (int e = 0; e < 16; ++e) {
+            const float x0 = __uint_as_float(v[2 * e]), x1 = __uint_as_float(v[2 * e + 1]);
+            hh[e] = pack_half2(x0, x1);
+            mx = fmaxf(mx, fmaxf(fabsf(x0), fabsf(x1)));
+          }
+          tmem_st32<16>(tmem + lb + T_UA + 16 * h2, hh);
         }
+        ovf |= !(mx <= 65504.f);
+        tmem_st_wait();
       }
-      fence_proxy_async_smem();
       tc_fence_before();
       named_sync(BAR_STATE, NSTATE);
       if (lead) {
         tc_fence_after();
         // H^T += U^T (k*rho);  O^T += U^T A^T
+#pragma unroll
         for (int k = 0; k < 4; ++k)
-          umma_ss(tmem + T_H, kmajor_desc(sb + S_UT, 128, k), mnmajor_desc(sb + S_KH, 64, k),
+          umma_ts(tmem + T_H, tmem + T_UA + 8 * k, d_kh + (uint64_t)(128 * k),
                   idesc_f16(128, 128, 0, 0, 1), 1);
+#pragma unroll
         for (int k = 0; k < 4; ++k)
-          umma_ss(tmem + T_O, kmajor_desc(sb + S_UT, 128, k),
-                  kmajor_desc(sb + S_AQ + 8192 * buf, 64, k), idesc_f16(128, 64, 0, 0, 0), 1);
+          umma_ts(tmem + T_O, tmem + T_UA + 8 * k, d_aq + (uint64_t)(2 * k),
+                  idesc_f16(128, 64, 0, 0, 0), 1);
         umma_commit(bar_s3);
       }
       {
@@ -975,7 +1003,6 @@ __global__ void __launch_bounds__(NT, 1)
         const bool ok = wait_counter(c_gc, c + 2, s_abort);
         if (!named_and(BAR_STATE, NSTATE, ok)) { alive = false; break; }
         convert_and_scale(c + 1, false);
-        fence_proxy_async_smem();
         tc_fence_before();
         named_sync(BAR_STATE, NSTATE);
       }
@@ -1001,10 +1028,12 @@ __global__ void __launch_bounds__(NT, 1)
       set_status(a.status, CKDA_ERR_TIMEOUT);
       // let any MMA or copy still in flight land before the memory is released
       mbar_wait(bar_gram, 0, 1u << 16);
+      mbar_wait(bar_t, 0, 1u << 16);
       mbar_wait(bar_w, 0, 1u << 16);
       mbar_wait(bar_s1, 0, 1u << 16);
       mbar_wait(bar_s3, 0, 1u << 16);
       mbar_wait(bar_v, 0, 1u << 16);
+      mbar_wait(bar_qka, 0, 1u << 16);
     }
   }
   __syncthreads();
@@ -1046,16 +1075,17 @@ cudaError_t launch_fwd_chunk(const FwdArgs& a, cudaStream_t s) {
   const int units = a.num_units_seq * a.H;
   if (units == 0) return cudaSuccess;
   const uint64_t rows = (uint64_t)a.B * a.H * a.T;
-  CUtensorMap mv;
+  CUtensorMap mq, mk, ma, mv;
   if (rows == 0) {
-    mv = CUtensorMap{};  // every sequence is empty: no tile is ever loaded
-  } else if (!make_map(&mv, a.v, rows)) {
+    mq = mk = ma = mv = CUtensorMap{};  // every sequence is empty: no tile is ever loaded
+  } else if (!make_map(&mq, a.q, rows) || !make_map(&mk, a.k, rows) ||
+             !make_map(&ma, a.alpha, rows) || !make_map(&mv, a.v, rows)) {
     return cudaErrorInvalidValue;
   }
   cudaError_t err = cudaFuncSetAttribute(
       fwd_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_ALLOC);
   if (err != cudaSuccess) return err;
-  fwd_chunk_kernel<<<units, NT, SMEM_ALLOC, s>>>(a, mv);
+  fwd_chunk_kernel<<<units, NT, SMEM_ALLOC, s>>>(a, mq, mk, ma, mv);
   return cudaGetLastError();
 }
 
