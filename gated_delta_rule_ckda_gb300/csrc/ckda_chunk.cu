@@ -88,8 +88,9 @@ constexpr uint32_t S_SMALL = 209920;
 constexpr uint32_t S_BETA = S_SMALL;         // fp32 [2][64]
 constexpr uint32_t S_GC = S_SMALL + 512;     // fp32 [2][128] gamma_C
 constexpr uint32_t S_DIAG = S_SMALL + 1536;  // fp32 [16][64] partial q.k
-constexpr uint32_t S_BAR = S_SMALL + 5632;   // mbarriers and counters
-constexpr uint32_t SMEM_USED = S_SMALL + 5888;
+constexpr uint32_t S_TOT = S_SMALL + 5632;   // fp32 [2][16][8] half-chunk gate totals
+constexpr uint32_t S_BAR = S_SMALL + 6656;   // mbarriers
+constexpr uint32_t SMEM_USED = S_SMALL + 6912;
 constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;
 static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
 
@@ -265,8 +266,12 @@ struct Prep {
 // groups of 2, 4, 8, 16 quads, over the 16 quads of a chunk (lanes tq of a
 // 16-wide shuffle segment).  Level L = 8, 16, 32 needs the prefix if this
 // quad is in the upper half of its 2L segment and the suffix otherwise.
-__device__ __forceinline__ void quad_scans(Prep& P, const float (&Bq)[8], float (&E16f)[8]) {
-  const int tq = P.tq;
+// Quads tq_lo = 0..7 of one half of the chunk sit on the 8 lanes of a
+// shuffle segment; the two halves are in different warps and meet through
+// shared memory (`tot`, after a barrier of the prep role).
+__device__ __forceinline__ void quad_scans(Prep& P, const float (&Bq)[8], float (&E16f)[8],
+                                           float* tot, int j) {
+  const int tq = P.tq, tq_lo = tq & 7, tq_hi = tq >> 3;
   float I[8], J[8], E[8], X[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
@@ -276,16 +281,16 @@ __device__ __forceinline__ void quad_scans(Prep& P, const float (&Bq)[8], float 
     X[e] = 1.f;
   }
 #pragma unroll
-  for (int lg = 0; lg < 4; ++lg) {
+  for (int lg = 0; lg < 3; ++lg) {
     const int g = 1 << lg;
-    const int base = tq & ~(2 * g - 1);
+    const int base = tq_lo & ~(2 * g - 1);
     const int srcE = base + g - 1;  // last quad of the first half
     const int srcX = base + g;      // first quad of the second half
-    const bool second = (tq & g) != 0;
+    const bool second = (tq_lo & g) != 0;
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      const float vi = __shfl_sync(0xffffffffu, I[e], srcE, 16);
-      const float vj = __shfl_sync(0xffffffffu, J[e], srcX, 16);
+      const float vi = __shfl_sync(0xffffffffu, I[e], srcE, 8);
+      const float vj = __shfl_sync(0xffffffffu, J[e], srcX, 8);
       if (second) E[e] *= vi; else X[e] *= vj;
       I[e] = E[e] * Bq[e];
       J[e] = X[e] * Bq[e];
@@ -298,13 +303,22 @@ __device__ __forceinline__ void quad_scans(Prep& P, const float (&Bq)[8], float 
     if (lg == 0) P.F8 = to_half8(sel);
     if (lg == 1) P.F16 = to_half8(sel);
     if (lg == 2) P.F32 = to_half8(sel);
-    if (lg == 3) {
-      P.E16 = to_half8(E);
-      P.X16 = to_half8(X);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) E16f[e] = E[e];
-    }
   }
+  // whole chunk: the other half's total comes from the other warp
+  if (tq_lo == 7) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) tot[(tq_hi * 16 + j) * 8 + e] = I[e];
+  }
+  named_sync(1, 256);
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    if (tq_hi) E[e] *= tot[j * 8 + e];           // first half's total
+    else X[e] *= tot[(16 + j) * 8 + e];          // second half's total
+  }
+  P.E16 = to_half8(E);
+  P.X16 = to_half8(X);
+#pragma unroll
+  for (int e = 0; e < 8; ++e) E16f[e] = E[e];
 }
 
 // Row of token t in level L's operands: upper tokens -> X rank, lower -> Y rank.
@@ -368,10 +382,18 @@ __device__ __forceinline__ void extract_level(uint8_t* sm, uint32_t taddr, int x
   if (qrow) {
     if (L == 1) {
       *reinterpret_cast<__half*>(AQ + sw128_off(64, t, s0)) = __float2half_rn(g[0]);
-    } else {
+    } else if (L < 8) {
 #pragma unroll
       for (int c = 0; c < L; c += 2)
         *reinterpret_cast<uint32_t*>(AQ + sw128_off(64, t, s0 + c)) = pack_half2(g[c], g[c + 1]);
+    } else {
+#pragma unroll
+      for (int c = 0; c < L; c += 8) {
+        float f[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) f[e] = g[c + e];
+        store16(AQ + sw128_off(64, t, s0 + c), pack_half8(f));
+      }
     }
   } else {
     const float bt = beta[t];
@@ -456,13 +478,14 @@ __global__ void __launch_bounds__(NT, 1)
   uint64_t* bar_s3 = bar_v + 4;
   uint64_t* bar_t = bar_v + 5;
   uint64_t* bar_qka = bar_v + 6;
-  int* cnt = reinterpret_cast<int*>(sm + S_BAR + 64);
-  int* c_ready = cnt + 0;  // prep -> state: chunks whose operands are complete
-  int* c_gc = cnt + 1;     // prep -> state: chunks whose gamma_C is published
-  int* c_s1 = cnt + 2;     // state -> prep: chunks whose U-MMA completed (TB, W free)
-  int* c_s3 = cnt + 3;     // state -> prep: chunks whose last MMA completed
-  int* s_abort = cnt + 4;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(cnt + 8);
+  // prep -> state handoffs, one barrier per chunk parity so that a waiter can
+  // never fall a whole phase behind: operands of chunk c complete, gamma_C
+  // of chunk c published.  The state -> prep direction uses bar_s1 (TB, W
+  // free) and bar_s3 (q*gamma, k*rho, A free) directly.
+  uint64_t* bar_ready = bar_v + 7;   // [2]
+  uint64_t* bar_gc = bar_v + 9;      // [2]
+  int* s_abort = reinterpret_cast<int*>(sm + S_BAR + 128);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + S_BAR + 136);
 
   const Unit u = unit_of(a);
   const int nchunks = (u.len + C - 1) / C;
@@ -475,7 +498,11 @@ __global__ void __launch_bounds__(NT, 1)
     mbar_init(bar_s3, 1);
     mbar_init(bar_t, 1);
     mbar_init(bar_qka, 1);
-    for (int i = 0; i < 8; ++i) cnt[i] = 0;
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar_ready + i, 1);
+      mbar_init(bar_gc + i, 1);
+    }
+    *s_abort = 0;
     fence_mbar_init();
     tma_prefetch_desc(&mq);
     tma_prefetch_desc(&mk);
@@ -503,8 +530,10 @@ __global__ void __launch_bounds__(NT, 1)
     // =================================================================== PREP
     const int p = tid;
     const int w = p >> 5;
-    const int j = 2 * w + (lane >> 4);  // channel chunk
-    const int tq = lane & 15;           // token quad
+    // a warp holds 8 quads (32 tokens) x 4 channel chunks: its 16-byte tile
+    // accesses then fall on 8 distinct swizzle positions (conflict-free)
+    const int j = 4 * (w >> 1) + (lane >> 3);  // channel chunk
+    const int tq = 8 * (w & 1) + (lane & 7);   // token quad
     const int wq = w & 3, half = w >> 2;
     const __nv_bfloat16* gb = static_cast<const __nv_bfloat16*>(a.beta);
     uint32_t gram_phase = 0, t_phase = 0;
@@ -539,8 +568,10 @@ __global__ void __launch_bounds__(NT, 1)
       tc_fence_after();
       return all;
     };
-    auto prep_counter = [&](int* counter, int target) -> bool {
-      const bool ok = wait_counter(counter, target, s_abort);
+    // waits for the state role's MMA of chunk cc (bar_s1 or bar_s3); nothing
+    // to wait for before the first chunk
+    auto prep_state = [&](uint64_t* bar, int cc) -> bool {
+      const bool ok = cc < 0 ? true : mbar_wait(bar, (uint32_t)(cc & 1));
       return named_and(BAR_PREP, NPREP, ok);
     };
     // the MMA of the inverse chain: D[lanes 0..63] = A (rows 0..63 used) x B
@@ -641,7 +672,7 @@ __global__ void __launch_bounds__(NT, 1)
       }
       // ---- gate products across quads: segmented scans of the quad totals
       float E16f[8];
-      quad_scans(P, Bq, E16f);
+      quad_scans(P, Bq, E16f, reinterpret_cast<float*>(sm + S_TOT), j);
       // gamma_C (fp32: it scales the fp32 state): the last quad publishes it
       float* gC = reinterpret_cast<float*>(sm + S_GC) + 128 * buf;
       if (tq == 15) {
@@ -665,7 +696,7 @@ __global__ void __launch_bounds__(NT, 1)
         }
       }
       named_sync(BAR_PREP, NPREP);
-      if (p == 0) st_release(c_gc, c + 1);
+      if (p == 0) mbar_arrive(bar_gc + (c & 1));
 
       // ---- gated Grams: round r writes X/Y, its MMA runs while round r-1
       // is read out of TMEM (rounds use TMEM G0, G1, G0)
@@ -681,7 +712,7 @@ __global__ void __launch_bounds__(NT, 1)
       named_sync(BAR_PREP, NPREP);
       if (p == 0) { tc_fence_after(); gram_mma(T_G1); }
       // q*gamma, k*rho: the previous chunk's last MMA must have read them (and A)
-      if (!prep_counter(c_s3, c)) { alive = false; break; }
+      if (!prep_state(bar_s3, c - 1)) { alive = false; break; }
 #pragma unroll
       for (int uu = 0; uu < 4; ++uu) {
         const int t = 4 * tq + uu;
@@ -778,7 +809,7 @@ __global__ void __launch_bounds__(NT, 1)
       if (!prep_wait(bar_t, t_phase)) { alive = false; break; }
       // ---- T Diag(beta) as bf16; TB and W are single-buffered: the previous
       // chunk's U-MMA must have read them
-      if (!prep_counter(c_s1, c)) { alive = false; break; }
+      if (!prep_state(bar_s1, c - 1)) { alive = false; break; }
       if (tconv) {
         uint32_t v[32];
         tmem_ld32<32>(tmem + tl + T_G1 + 32 * half, v);
@@ -828,7 +859,7 @@ __global__ void __launch_bounds__(NT, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       named_sync(BAR_PREP, NPREP);
-      if (p == 0) st_release(c_ready, c + 1);
+      if (p == 0) mbar_arrive(bar_ready + (c & 1));
     }
     if (!alive) *reinterpret_cast<volatile int*>(s_abort) = 1;
   } else {
@@ -889,7 +920,7 @@ __global__ void __launch_bounds__(NT, 1)
       tmem_st_wait();
     };
     if (nchunks > 0) {
-      const bool ok = wait_counter(c_gc, 1, s_abort);
+      const bool ok = mbar_wait(bar_gc, 0);
       alive = named_and(BAR_STATE, NSTATE, ok);
       if (alive) convert_and_scale(0, true);
     } else if (hT) {
@@ -906,7 +937,7 @@ __global__ void __launch_bounds__(NT, 1)
     for (int c = 0; c < nchunks && alive; ++c) {
       const int lenc = min(C, u.len - c * C);
       {  // prep operands of chunk c, and its v tile
-        bool ok = wait_counter(c_ready, c + 1, s_abort);
+        bool ok = mbar_wait(bar_ready + (c & 1), (uint32_t)((c >> 1) & 1));
         if (ok) ok = mbar_wait(bar_v, c & 1);
         if (!named_and(BAR_STATE, NSTATE, ok)) { alive = false; break; }
       }
@@ -935,7 +966,6 @@ __global__ void __launch_bounds__(NT, 1)
         tc_fence_after();
       }
       if (lead) {
-        st_release(c_s1, c + 1);
         if (c + 1 < nchunks) {  // the v tile is free: fetch the next one
           mbar_arrive_expect_tx(bar_v, TILE_BYTES);
           tma_load_2d(sm + S_V, &mv, bar_v, 0, (int)(u.row0 + (long)(c + 1) * C));
@@ -982,7 +1012,6 @@ __global__ void __launch_bounds__(NT, 1)
         if (!named_and(BAR_STATE, NSTATE, ok)) { alive = false; break; }
         tc_fence_after();
       }
-      if (lead) st_release(c_s3, c + 1);
       // outputs o[t][j] = scale * O^T[j][t]
       {
         const long rbase = u.row0 + (long)c * C;
@@ -1000,7 +1029,7 @@ __global__ void __launch_bounds__(NT, 1)
         }
       }
       if (c + 1 < nchunks) {
-        const bool ok = wait_counter(c_gc, c + 2, s_abort);
+        const bool ok = mbar_wait(bar_gc + ((c + 1) & 1), (uint32_t)(((c + 1) >> 1) & 1));
         if (!named_and(BAR_STATE, NSTATE, ok)) { alive = false; break; }
         convert_and_scale(c + 1, false);
         tc_fence_before();
@@ -1035,6 +1064,7 @@ __global__ void __launch_bounds__(NT, 1)
       mbar_wait(bar_v, 0, 1u << 16);
       mbar_wait(bar_qka, 0, 1u << 16);
     }
+    (void)s_abort;
   }
   __syncthreads();
   tc_fence_after();
