@@ -59,27 +59,35 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_sources_sha():
+# source files each profiled kernel is built from; a committed DRAM-traffic
+# figure only counts while these files are unchanged
+KERNEL_SOURCES = {
+    "fwd_chunk": ["ckda_chunk.cu", "sm103.cuh", "ckda_internal.cuh"],
+    "decode128": ["ckda_decode.cu", "ckda_internal.cuh"],
+}
+
+
+def kernel_sources_sha(kernel):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "gated_delta_rule_ckda_gb300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
-        if fn.endswith((".cu", ".cuh")):
-            h.update(fn.encode())
-            h.update(open(os.path.join(csrc, fn), "rb").read())
+    for fn in KERNEL_SOURCES[kernel]:
+        h.update(fn.encode())
+        h.update(open(os.path.join(csrc, fn), "rb").read())
     return h.hexdigest()
 
 
 def traffic_for(kernel, workload):
-    """DRAM bytes per launch from the committed ncu summary, if the kernel
+    """DRAM bytes per launch from the committed ncu summary, if the kernel's
     sources are unchanged since it was taken; else None."""
     try:
         t = json.load(open(TRAFFIC_FILE))
+        e = t["kernels"][kernel]
     except Exception:
         return None
-    if t.get("kernel_sources_sha256") != kernel_sources_sha():
+    if e.get("sources_sha256") != kernel_sources_sha(kernel):
         return None
-    e = t.get("kernels", {}).get(kernel, {}).get(workload)
-    return None if e is None else float(e["dram_bytes_per_launch"])
+    w = e.get("workloads", {}).get(workload)
+    return None if w is None else float(w["dram_bytes_per_launch"])
 
 
 class ClockSampler:
