@@ -61,7 +61,10 @@ constexpr int BAR_PREP = 1;   // named barrier ids
 constexpr int BAR_STATE = 2;
 
 // ---- shared memory map (bytes from a 1024-aligned base) ----
-constexpr uint32_t S_TQ = 0;         // bf16 q tile   [64 t][128 i]  (TMA, one chunk ahead)
+// q, k, alpha tiles; once read they hold the second Gram operand buffer
+// (X over q and k, Y over alpha) until the last Gram MMA, then the next
+// chunk's tiles are fetched into them
+constexpr uint32_t S_TQ = 0;         // bf16 q tile   [64 t][128 i]  (TMA)
 constexpr uint32_t S_TK = 16384;     // bf16 k tile
 constexpr uint32_t S_TA = 32768;     // bf16 alpha tile
 constexpr uint32_t S_V = 49152;      // bf16 v tile   [64 s][128 j]  MN-major A of U~   (TMA)
@@ -73,6 +76,8 @@ constexpr uint32_t S_KGT = 122880;   // bf16 k*gamma  [64 s][128 i]  MN-major A 
 constexpr uint32_t S_AQ = 139264;    // fp16 A        [64 t][64 s]   K-major B of O
 constexpr uint32_t S_GX = 147456;    // fp16 Gram X   [128 rows][128 i] K-major A
 constexpr uint32_t S_GY = 180224;    // fp16 Gram Y   [64 rows][128 i]  K-major B
+constexpr uint32_t S_GX2 = S_TQ;     // second Gram buffer (the tile region)
+constexpr uint32_t S_GY2 = S_TA;
 // after the Gram MMAs the 48 KiB of X and Y hold the inverse's 64 x 64 tiles
 // (fp16, one 64-column panel each).  A tile read as a 128-row A operand also
 // reads the 8 KiB after it; those rows only feed TMEM lanes that are ignored.
@@ -100,8 +105,8 @@ constexpr uint32_t T_HA = 128;  // H^T fp16 [128 j][128 i]     A operand (2 per 
 constexpr uint32_t T_U = 192;   // U^T fp32 [128 j][64 t]
 constexpr uint32_t T_UA = 256;  // U^T fp16 [128 j][64 t]      A operand
 constexpr uint32_t T_O = 288;   // O^T fp32 [128 j][64 t]
-constexpr uint32_t T_G0 = 352;  // Gram rounds alternate G0, G1, G0; the inverse chain
-constexpr uint32_t T_G1 = 416;  //   uses E:G0, E^2:G1, EG:G0, T:G1; then W^T:G0
+constexpr uint32_t T_G0 = 352;  // Gram rounds use G0, G1, G0; the inverse chain uses
+constexpr uint32_t T_G1 = 416;  //   E:G1, E^2:G0, EG:G1, T:G0; then W^T:G1 (read by the state)
 constexpr uint32_t TMEM_COLS = 512;
 
 constexpr uint32_t TILE_BYTES = 16384;
@@ -336,8 +341,8 @@ __device__ __forceinline__ void store16(uint8_t* p, const uint4& v) {
 // 32 k-rows then 32 q-rows of its upper-half tokens; Y rows its lower-half
 // tokens, each gated by the token's factor at that level.
 template <int L>
-__device__ __forceinline__ void write_level(uint8_t* sm, const Prep& P, int j, int xbase,
-                                            int ybase) {
+__device__ __forceinline__ void write_level(uint8_t* X, uint8_t* Y, const Prep& P, int j,
+                                            int xbase, int ybase) {
 #pragma unroll
   for (int u = 0; u < 4; ++u) {
     const int t = 4 * P.tq + u;
@@ -346,10 +351,10 @@ __device__ __forceinline__ void write_level(uint8_t* sm, const Prep& P, int j, i
     const uint4 f = P.factor<L>(u);
     // |factor| <= 1, so the products stay within the range of k and q
     if (upper) {
-      store16(sm + S_GX + sw128_chunk(128, xbase + rank, j), hmul8h(P.k[u], f));
-      store16(sm + S_GX + sw128_chunk(128, xbase + 32 + rank, j), hmul8h(P.q[u], f));
+      store16(X + sw128_chunk(128, xbase + rank, j), hmul8h(P.k[u], f));
+      store16(X + sw128_chunk(128, xbase + 32 + rank, j), hmul8h(P.q[u], f));
     } else {
-      store16(sm + S_GY + sw128_chunk(64, ybase + rank, j), hmul8h(P.k[u], f));
+      store16(Y + sw128_chunk(64, ybase + rank, j), hmul8h(P.k[u], f));
     }
   }
 }
@@ -472,7 +477,6 @@ __global__ void __launch_bounds__(NT, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   uint64_t* bar_v = reinterpret_cast<uint64_t*>(sm + S_BAR);
-  uint64_t* bar_gram = bar_v + 1;
   uint64_t* bar_w = bar_v + 2;
   uint64_t* bar_s1 = bar_v + 3;
   uint64_t* bar_s3 = bar_v + 4;
@@ -484,6 +488,9 @@ __global__ void __launch_bounds__(NT, 1)
   // free) and bar_s3 (q*gamma, k*rho, A free) directly.
   uint64_t* bar_ready = bar_v + 7;   // [2]
   uint64_t* bar_gc = bar_v + 9;      // [2]
+  // one barrier per Gram round: rounds 1 and 2 are both in flight before
+  // round 1 is waited for, so a shared barrier could run two phases ahead
+  uint64_t* bar_r = bar_v + 11;      // [3]
   int* s_abort = reinterpret_cast<int*>(sm + S_BAR + 128);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + S_BAR + 136);
 
@@ -492,7 +499,6 @@ __global__ void __launch_bounds__(NT, 1)
 
   if (tid == 0) {
     mbar_init(bar_v, 1);
-    mbar_init(bar_gram, 1);
     mbar_init(bar_w, 1);
     mbar_init(bar_s1, 1);
     mbar_init(bar_s3, 1);
@@ -502,6 +508,7 @@ __global__ void __launch_bounds__(NT, 1)
       mbar_init(bar_ready + i, 1);
       mbar_init(bar_gc + i, 1);
     }
+    for (int i = 0; i < 3; ++i) mbar_init(bar_r + i, 1);
     *s_abort = 0;
     fence_mbar_init();
     tma_prefetch_desc(&mq);
@@ -536,7 +543,7 @@ __global__ void __launch_bounds__(NT, 1)
     const int tq = 8 * (w & 1) + (lane & 7);   // token quad
     const int wq = w & 3, half = w >> 2;
     const __nv_bfloat16* gb = static_cast<const __nv_bfloat16*>(a.beta);
-    uint32_t gram_phase = 0, t_phase = 0;
+    uint32_t t_phase = 0;
     bool alive = true;
     float beta_next[4] = {0.f, 0.f, 0.f, 0.f};
     if (j == 0 && nchunks > 0) {
@@ -583,14 +590,14 @@ __global__ void __launch_bounds__(NT, 1)
                 idesc_f16(128, 64, 0, 0, 1), k > 0);
       umma_commit(bar_t);
     };
-    const uint64_t d_gx = kmajor_desc(sb + S_GX, 128, 0), d_gy = kmajor_desc(sb + S_GY, 64, 0);
-    auto gram_mma = [&](uint32_t d_col) {
+    auto gram_mma = [&](uint32_t d_col, uint32_t xbuf, uint32_t ybuf, uint64_t* bar) {
+      const uint64_t d_gx = kmajor_desc(sb + xbuf, 128, 0), d_gy = kmajor_desc(sb + ybuf, 64, 0);
 #pragma unroll
       for (int k = 0; k < 8; ++k)  // K steps: 32 bytes in a panel, panels R*128 apart
         umma_ss(tmem + d_col, d_gx + (uint64_t)((k >> 2) * 1024 + (k & 3) * 2),
                 d_gy + (uint64_t)((k >> 2) * 512 + (k & 3) * 2), idesc_f16(128, 64, 0, 0, 0),
                 k > 0);
-      umma_commit(bar_gram);
+      umma_commit(bar);
     };
     const bool tconv = wq < 2;  // warps 0,1,4,5 reach TMEM lanes 0..63
     const int trow = 32 * wq + lane;
@@ -598,6 +605,11 @@ __global__ void __launch_bounds__(NT, 1)
     const uint32_t tlw = (uint32_t)(32 * wq) << 16;
     uint8_t* AQ = sm + S_AQ;
 
+    uint8_t* X1 = sm + S_GX;   // Gram operand buffers: the dedicated one and the tile region
+    uint8_t* Y1 = sm + S_GY;
+    uint8_t* X2 = sm + S_GX2;
+    uint8_t* Y2 = sm + S_GY2;
+    float* dg = reinterpret_cast<float*>(sm + S_DIAG);
     for (int c = 0; c < nchunks && alive; ++c) {
       const int lenc = min(C, u.len - c * C);
       const int buf = c & 1;
@@ -612,23 +624,35 @@ __global__ void __launch_bounds__(NT, 1)
       float Bq[8];
       {
         float al[4][8];
-        float mx = 0.f;
+        uint32_t inf_or_nan = 0;
 #pragma unroll
         for (int uu = 0; uu < 4; ++uu) {
           const int t = 4 * tq + uu;
-          const bool valid = t < lenc;
           const uint32_t off = sw128_chunk(64, t, j);
           float kk[8], qq[8];
           unpack_bf16x8(*reinterpret_cast<const uint4*>(sm + S_TK + off), kk);
           unpack_bf16x8(*reinterpret_cast<const uint4*>(sm + S_TQ + off), qq);
           unpack_bf16x8(*reinterpret_cast<const uint4*>(sm + S_TA + off), al[uu]);
-          if (valid) mx = fmaxf(mx, fmaxf(absmax8(kk), absmax8(qq)));
-          P.k[uu] = valid ? to_half8(kk) : make_uint4(0, 0, 0, 0);
-          P.q[uu] = valid ? to_half8(qq) : make_uint4(0, 0, 0, 0);
+          float sacc = 0.f;  // partial q.k over this thread's 8 channels
 #pragma unroll
-          for (int e = 0; e < 8; ++e) al[uu][e] = valid ? al[uu][e] : 1.f;  // identity transition
+          for (int e = 0; e < 8; ++e) sacc = fmaf(qq[e], kk[e], sacc);
+          P.k[uu] = to_half8(kk);
+          P.q[uu] = to_half8(qq);
+          if (lenc < C && t >= lenc) {  // past the end of the sequence: identity transition
+            P.k[uu] = make_uint4(0, 0, 0, 0);
+            P.q[uu] = make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) al[uu][e] = 1.f;
+            sacc = 0.f;
+          }
+          dg[j * 64 + t] = sacc;
+          // an input outside the fp16 range turns into inf here
+          const uint32_t w4[4] = {P.q[uu].x | P.k[uu].x, P.q[uu].y | P.k[uu].y,
+                                  P.q[uu].z | P.k[uu].z, P.q[uu].w | P.k[uu].w};
+#pragma unroll
+          for (int z = 0; z < 4; ++z) inf_or_nan |= __vcmpeq2(w4[z] & 0x7c007c00u, 0x7c007c00u);
         }
-        ovf |= !(mx <= 65504.f);
+        ovf |= inf_or_nan != 0;
         // in-quad prefix / suffix products (fp32, then packed halves)
         float lp[8], ls[8];
 #pragma unroll
@@ -653,9 +677,6 @@ __global__ void __launch_bounds__(NT, 1)
         P.a2 = to_half8(al[2]);
         P.a3 = to_half8(al[3]);
       }
-      // the tiles are consumed: fetch the next chunk's while this one runs
-      named_sync(BAR_PREP, NPREP);
-      if (p == 0 && c + 1 < nchunks) issue_qka(c + 1);
       // beta: this chunk's values were loaded one chunk ahead
       float* beta_s = reinterpret_cast<float*>(sm + S_BETA) + 64 * buf;
       if (j == 0) {
@@ -670,7 +691,8 @@ __global__ void __launch_bounds__(NT, 1)
           }
         }
       }
-      // ---- gate products across quads: segmented scans of the quad totals
+      // ---- gate products across quads (the scan's barrier also ends the
+      // reads of the tile region, which now becomes Gram buffer 2)
       float E16f[8];
       quad_scans(P, Bq, E16f, reinterpret_cast<float*>(sm + S_TOT), j);
       // gamma_C (fp32: it scales the fp32 state): the last quad publishes it
@@ -679,39 +701,35 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
         for (int e = 0; e < 8; ++e) gC[8 * j + e] = E16f[e] * Bq[e];
       }
-      // k*gamma (bf16, A of the W-MMA; its last reader, the previous W-MMA,
-      // completed inside the previous prep) and the partial q.k diagonal
-      {
-        float* dg = reinterpret_cast<float*>(sm + S_DIAG);
-#pragma unroll
-        for (int uu = 0; uu < 4; ++uu) {
-          const int t = 4 * tq + uu;
-          store16(sm + S_KGT + sw128_chunk(64, t, j), half8_to_bf8(hmul8h(P.k[uu], P.gamma(uu))));
-          float kk[8], qq[8], sacc = 0.f;
-          unpack_half8(P.k[uu], kk);
-          unpack_half8(P.q[uu], qq);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) sacc = fmaf(qq[e], kk[e], sacc);
-          dg[j * 64 + t] = sacc;
-        }
+      // ---- Gram round 1: levels 8 and 4 (pairs inside 16-token blocks)
+      write_level<8>(X2, Y2, P, j, 0, 0);
+      write_level<4>(X2, Y2, P, j, 64, 32);
+      fence_proxy_async_smem();
+      named_sync(BAR_PREP, NPREP);
+      if (p == 0) {
+        mbar_arrive(bar_gc + (c & 1));
+        tc_fence_after();
+        gram_mma(T_G0, S_GX2, S_GY2, bar_r + 0);
       }
-      named_sync(BAR_PREP, NPREP);
-      if (p == 0) mbar_arrive(bar_gc + (c & 1));
-
-      // ---- gated Grams: round r writes X/Y, its MMA runs while round r-1
-      // is read out of TMEM (rounds use TMEM G0, G1, G0)
-      write_level<32>(sm, P, j, 0, 0);
-      write_level<16>(sm, P, j, 64, 32);
+      // ---- round 2: levels 2 and 1.  Its TMEM tile G1 last held W of the
+      // previous chunk, which the state warps convert before their U-MMA.
+      write_level<2>(X1, Y1, P, j, 0, 0);
+      write_level<1>(X1, Y1, P, j, 64, 32);
       fence_proxy_async_smem();
-      named_sync(BAR_PREP, NPREP);
-      if (p == 0) { tc_fence_after(); gram_mma(T_G0); }
-      if (!prep_wait(bar_gram, gram_phase)) { alive = false; break; }
-      write_level<8>(sm, P, j, 0, 0);
-      write_level<4>(sm, P, j, 64, 32);
-      fence_proxy_async_smem();
-      named_sync(BAR_PREP, NPREP);
-      if (p == 0) { tc_fence_after(); gram_mma(T_G1); }
-      // q*gamma, k*rho: the previous chunk's last MMA must have read them (and A)
+      if (!prep_state(bar_s1, c - 1)) { alive = false; break; }
+      if (p == 0) { tc_fence_after(); gram_mma(T_G1, S_GX, S_GY, bar_r + 1); }
+      // ---- k*gamma (bf16, A of the W-MMA; the previous W-MMA is done with it)
+      {
+        const bool ok = c == 0 ? true : mbar_wait(bar_w, (uint32_t)((c - 1) & 1));
+        if (!named_and(BAR_PREP, NPREP, ok)) { alive = false; break; }
+      }
+#pragma unroll
+      for (int uu = 0; uu < 4; ++uu) {
+        const int t = 4 * tq + uu;
+        store16(sm + S_KGT + sw128_chunk(64, t, j), half8_to_bf8(hmul8h(P.k[uu], P.gamma(uu))));
+      }
+      // ---- q*gamma, k*rho: the previous chunk's last MMA must have read them
+      // (and A, which the Gram read-out below overwrites)
       if (!prep_state(bar_s3, c - 1)) { alive = false; break; }
 #pragma unroll
       for (int uu = 0; uu < 4; ++uu) {
@@ -719,42 +737,47 @@ __global__ void __launch_bounds__(NT, 1)
         store16(sm + S_QG + sw128_chunk(64, t, j), hmul8h(P.q[uu], P.gamma(uu)));
         store16(sm + S_KH + sw128_chunk(64, t, j), hmul8h(P.k[uu], P.rho(uu)));
       }
-      if (half == 0) extract_round<32>(sm, tmem, T_G0, wq, lane, beta_s, AQ);
-      tc_fence_before();
-      if (!prep_wait(bar_gram, gram_phase)) { alive = false; break; }
-      write_level<2>(sm, P, j, 0, 0);
-      write_level<1>(sm, P, j, 64, 32);
+      // ---- round 3 (levels 32 and 16) goes into buffer 2 once round 1 is done
+      uint32_t rph = (uint32_t)c;
+      if (!prep_wait(bar_r + 0, rph)) { alive = false; break; }
+      if (half == 0) extract_round<8>(sm, tmem, T_G0, wq, lane, beta_s, AQ);
+      write_level<32>(X2, Y2, P, j, 0, 0);
+      write_level<16>(X2, Y2, P, j, 64, 32);
       fence_proxy_async_smem();
-      named_sync(BAR_PREP, NPREP);
-      if (p == 0) { tc_fence_after(); gram_mma(T_G0); }
-      if (half == 1) extract_round<8>(sm, tmem, T_G1, wq, lane, beta_s, AQ);
       tc_fence_before();
-      if (!prep_wait(bar_gram, gram_phase)) { alive = false; break; }
+      named_sync(BAR_PREP, NPREP);
+      if (p == 0) { tc_fence_after(); gram_mma(T_G0, S_GX2, S_GY2, bar_r + 2); }
+      rph = (uint32_t)c;
+      if (!prep_wait(bar_r + 1, rph)) { alive = false; break; }  // round 2
+      if (half == 1) extract_round<2>(sm, tmem, T_G1, wq, lane, beta_s, AQ);
       // D lives where Gram X was: zero it (its diagonal blocks come next)
       for (int e = p; e < 8192 / 16; e += NPREP) store16(sm + S_TD + 16 * e, make_uint4(0, 0, 0, 0));
-      if (half == 0) extract_round<2>(sm, tmem, T_G0, wq, lane, beta_s, AQ);
       tc_fence_before();
       named_sync(BAR_PREP, NPREP);
       // ---- T = (I + M)^-1 = (I - E)(I + E^2) D with D the inverse of the
       // block diagonal of I + M and E = D N (E^4 = 0: N is strictly lower by
-      // 16-blocks); the four products run on the tensor cores
-      if (p < 64) {
-        invert_diag_blocks(sm, p);
-      } else if (p < 128) {
-        const int t = p - 64;
-        const float* dg = reinterpret_cast<const float*>(sm + S_DIAG);
+      // 16-blocks); D is formed while round 3 runs, the products on tensor cores
+      if (p < 64) invert_diag_blocks(sm, p);
+      rph = (uint32_t)c;
+      if (!prep_wait(bar_r + 2, rph)) { alive = false; break; }  // round 3
+      // the tile region is free: fetch the next chunk's q, k, alpha
+      if (p == 0 && c + 1 < nchunks) issue_qka(c + 1);
+      if (half == 0) extract_round<32>(sm, tmem, T_G0, wq, lane, beta_s, AQ);
+      else if (p >= 128 && p < 192) {
+        const int t = p - 128;
         float sacc = 0.f;
 #pragma unroll
         for (int jj = 0; jj < 16; ++jj) sacc += dg[jj * 64 + t];
         *reinterpret_cast<__half*>(AQ + sw128_off(64, t, t)) = __float2half_rn(sacc);
       }
       fence_proxy_async_smem();
+      tc_fence_before();
       named_sync(BAR_PREP, NPREP);
-      if (p == 0) { tc_fence_after(); t_mma(T_G0, S_TD, S_TN); }       // E = D N
+      if (p == 0) { tc_fence_after(); t_mma(T_G1, S_TD, S_TN); }       // E = D N
       if (!prep_wait(bar_t, t_phase)) { alive = false; break; }
       if (tconv) {
         uint32_t v[32];
-        tmem_ld32<32>(tmem + tl + T_G0 + 32 * half, v);
+        tmem_ld32<32>(tmem + tl + T_G1 + 32 * half, v);
         tmem_ld_wait();
 #pragma unroll
         for (int z = 0; z < 32; z += 8) {
@@ -767,12 +790,12 @@ __global__ void __launch_bounds__(NT, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       named_sync(BAR_PREP, NPREP);
-      if (p == 0) { tc_fence_after(); t_mma(T_G1, S_TE, S_TE); }       // E^2
+      if (p == 0) { tc_fence_after(); t_mma(T_G0, S_TE, S_TE); }       // E^2
       if (!prep_wait(bar_t, t_phase)) { alive = false; break; }
       float gv[32];  // G = I + E^2, kept for F
       if (tconv) {
         uint32_t v[32];
-        tmem_ld32<32>(tmem + tl + T_G1 + 32 * half, v);
+        tmem_ld32<32>(tmem + tl + T_G0 + 32 * half, v);
         tmem_ld_wait();
 #pragma unroll
         for (int z = 0; z < 32; ++z)
@@ -788,11 +811,11 @@ __global__ void __launch_bounds__(NT, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       named_sync(BAR_PREP, NPREP);
-      if (p == 0) { tc_fence_after(); t_mma(T_G0, S_TE, S_TG); }       // E G
+      if (p == 0) { tc_fence_after(); t_mma(T_G1, S_TE, S_TG); }       // E G
       if (!prep_wait(bar_t, t_phase)) { alive = false; break; }
       if (tconv) {
         uint32_t v[32];
-        tmem_ld32<32>(tmem + tl + T_G0 + 32 * half, v);
+        tmem_ld32<32>(tmem + tl + T_G1 + 32 * half, v);
         tmem_ld_wait();
 #pragma unroll
         for (int z = 0; z < 32; z += 8) {
@@ -805,14 +828,13 @@ __global__ void __launch_bounds__(NT, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       named_sync(BAR_PREP, NPREP);
-      if (p == 0) { tc_fence_after(); t_mma(T_G1, S_TFm, S_TD); }      // T = F D
+      if (p == 0) { tc_fence_after(); t_mma(T_G0, S_TFm, S_TD); }      // T = F D
       if (!prep_wait(bar_t, t_phase)) { alive = false; break; }
-      // ---- T Diag(beta) as bf16; TB and W are single-buffered: the previous
-      // chunk's U-MMA must have read them
-      if (!prep_state(bar_s1, c - 1)) { alive = false; break; }
+      // ---- T Diag(beta) as bf16 (TB is single-buffered: the previous
+      // chunk's U-MMA read it before this chunk's round 2 was issued)
       if (tconv) {
         uint32_t v[32];
-        tmem_ld32<32>(tmem + tl + T_G1 + 32 * half, v);
+        tmem_ld32<32>(tmem + tl + T_G0 + 32 * half, v);
         tmem_ld_wait();
 #pragma unroll
         for (int z = 0; z < 32; z += 8) {
@@ -830,36 +852,16 @@ __global__ void __launch_bounds__(NT, 1)
       named_sync(BAR_PREP, NPREP);
       if (p == 0) {
         tc_fence_after();
-        // W^T[i][t] = sum_s (k*gamma)[s][i] TB[t][s]
+        // W^T[i][t] = sum_s (k*gamma)[s][i] TB[t][s], into G1; the state warps
+        // read it out
         const uint64_t da = mnmajor_desc(sb + S_KGT, 64, 0), db = kmajor_desc(sb + S_TB, 64, 0);
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          umma_ss(tmem + T_G0, da + (uint64_t)(128 * k), db + (uint64_t)(2 * k),
+          umma_ss(tmem + T_G1, da + (uint64_t)(128 * k), db + (uint64_t)(2 * k),
                   idesc_f16(128, 64, 1, 1, 0), k > 0);
         umma_commit(bar_w);
+        mbar_arrive(bar_ready + (c & 1));
       }
-      {
-        uint32_t wphase = (uint32_t)c;
-        if (!prep_wait(bar_w, wphase)) { alive = false; break; }
-      }
-      {  // -W^T as fp16 [i][t] (MN-major B): lane = i, 32 columns per half
-        const int i = 32 * wq + lane;
-        uint32_t v[32];
-        tmem_ld32<32>(tmem + tlw + T_G0 + 32 * half, v);
-        tmem_ld_wait();
-#pragma unroll
-        for (int z = 0; z < 32; z += 8) {
-          float f[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) f[e] = -__uint_as_float(v[z + e]);
-          ovf |= !fp16_ok8(f);
-          store16(sm + S_W + sw128_chunk(128, i, (32 * half + z) >> 3), pack_half8(f));
-        }
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      named_sync(BAR_PREP, NPREP);
-      if (p == 0) mbar_arrive(bar_ready + (c & 1));
     }
     if (!alive) *reinterpret_cast<volatile int*>(s_abort) = 1;
   } else {
@@ -936,11 +938,36 @@ __global__ void __launch_bounds__(NT, 1)
     __nv_bfloat16* go = static_cast<__nv_bfloat16*>(a.o);
     for (int c = 0; c < nchunks && alive; ++c) {
       const int lenc = min(C, u.len - c * C);
-      {  // prep operands of chunk c, and its v tile
+      {  // prep operands of chunk c, its W^T in TMEM, and its v tile
         bool ok = mbar_wait(bar_ready + (c & 1), (uint32_t)((c >> 1) & 1));
+        if (ok) ok = mbar_wait(bar_w, c & 1);
         if (ok) ok = mbar_wait(bar_v, c & 1);
         if (!named_and(BAR_STATE, NSTATE, ok)) { alive = false; break; }
+        tc_fence_after();
       }
+      {  // -W^T as fp16 [i][t] (MN-major B of the U-MMA): lane = i
+        float mx = 0.f;
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          uint32_t v[32];
+          tmem_ld32<32>(tmem + lb + T_G1 + 32 * h2, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int z = 0; z < 32; z += 8) {
+            float f[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              f[e] = -__uint_as_float(v[z + e]);
+              mx = fmaxf(mx, fabsf(f[e]));
+            }
+            store16(sm + S_W + sw128_chunk(128, s, (32 * h2 + z) >> 3), pack_half8(f));
+          }
+        }
+        ovf |= !(mx <= 65504.f);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      named_sync(BAR_STATE, NSTATE);
       if (lead) {
         tc_fence_after();
         // U^T = V^T TB^T - H^T W^T
@@ -1056,7 +1083,7 @@ __global__ void __launch_bounds__(NT, 1)
     if (*reinterpret_cast<volatile int*>(s_abort)) {
       set_status(a.status, CKDA_ERR_TIMEOUT);
       // let any MMA or copy still in flight land before the memory is released
-      mbar_wait(bar_gram, 0, 1u << 16);
+      for (int i = 0; i < 3; ++i) mbar_wait(bar_r + i, 0, 1u << 16);
       mbar_wait(bar_t, 0, 1u << 16);
       mbar_wait(bar_w, 0, 1u << 16);
       mbar_wait(bar_s1, 0, 1u << 16);
