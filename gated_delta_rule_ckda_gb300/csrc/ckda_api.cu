@@ -39,7 +39,7 @@ __global__ void selftest_timeout_kernel(int* status, unsigned spin_limit) {
     fence_mbar_init();
   }
   __syncthreads();
-  bool ok = mbar_wait(&bar, 0, spin_limit);
+  bool ok = mbar_wait(&bar, 0, spin_limit, 1000u);
   if (!ok && threadIdx.x == 0) set_status(status, CKDA_ERR_TIMEOUT);
 }
 

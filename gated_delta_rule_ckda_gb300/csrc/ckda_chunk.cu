@@ -16,7 +16,7 @@
 //   T  = (I + M)^-1,   TB = T Diag(beta)
 //   W  = TB (k * gamma),           U~ = TB V
 //   U  = U~ - W H
-//   O  = (q * gamma) H + A U                            -> o (scaled)
+//   O  = (q * gamma) H + A U                            -> o
 //   H' = Diag(gamma_C) H + (k * rho)^T U
 //
 // Gate products are formed by multiplication only -- never as a ratio of
@@ -31,19 +31,34 @@
 // exclusive suffix product within one.  Every level is one dense contraction
 // of gated operands on the tensor cores; two levels share a 128 x 64 MMA tile.
 //
+// T is formed from D, the inverses of the 16 x 16 diagonal blocks of I + M
+// (CUDA cores, fp32), and E = D N with N the rest of M: E is strictly lower
+// by blocks, so E^4 = 0 and T = (I + E^2)(I - E) D.  One tensor-core step
+// gives E^2 and F = (I - E) D together (operands [E ; I - E] x [E | D]), the
+// next T = F + E^2 F with F kept in fp32 in tensor memory.
+//
 // Precision: operands of every contraction that touches the state, the
 // Grams and A are fp16 (11-bit significand); T Diag(beta), k * gamma and the
-// raw bf16 inputs are bf16; all accumulation is fp32 in TMEM, gate products
-// and T are fp32.  An fp16 overflow is reported as CKDA_ERR_RANGE.
+// raw bf16 inputs are bf16; all accumulation is fp32 in TMEM.  Gate factors
+// inside a 16-token block are fp16 product chains; block totals, gamma_C and
+// T are fp32.  An fp16 operand that overflows turns into inf and reaches o
+// (or the final state); a non-finite o or final state is reported as
+// CKDA_ERR_RANGE.
 //
-// Warp roles (384 threads):
+// Warp roles (416 threads):
 //   warps 0-7  PREP: per chunk, gate products, gated Grams, T, W and the
-//              operands of the state step; thread (j, tq) owns channels
-//              8j..8j+7 of tokens 4tq..4tq+3.  Prep of chunk c+1 runs while
-//              the state warps step chunk c.
-//   warps 8-11 STATE: the serial state step on TMEM (thread = TMEM lane = j).
-// Handoffs use release/acquire counters in shared memory; MMA and TMA
-// completion use mbarriers.  Every wait is bounded.
+//              operands of the state step.  For the elementwise work thread
+//              (blk, panel, lane) owns channels 64 panel + 2 lane, +1 of the
+//              16 tokens 16 blk .. 16 blk + 15, so every gate product inside
+//              a block is a register chain and every shared-memory access is
+//              a conflict-free 4-byte access at a compile-time swizzle.  Prep
+//              of chunk c+1 runs while the state warps step chunk c.
+//   warps 8-11 STATE: the serial state step on TMEM (thread = TMEM lane = j);
+//              thread 0 issues its MMAs.
+//   warp 12    MMA: one thread issues every tensor-core step of the prep
+//              role, so that no prep warp stalls on an issue.
+// Handoffs are mbarriers (MMA and TMA completion, operand hand-over) and
+// named barriers within a role.  Every wait is bounded.
 #include "ckda_internal.cuh"
 #include "sm103.cuh"
 
@@ -56,58 +71,73 @@ namespace {
 constexpr int C = 64;
 constexpr int NPREP = 256;
 constexpr int NSTATE = 128;
-constexpr int NT = NPREP + NSTATE;
+constexpr int NT = NPREP + NSTATE + 32;
+constexpr int MMA_WARP = (NPREP + NSTATE) / 32;
 constexpr int BAR_PREP = 1;   // named barrier ids
 constexpr int BAR_STATE = 2;
 
 // ---- shared memory map (bytes from a 1024-aligned base) ----
 // q, k, alpha tiles; once read they hold the second Gram operand buffer
-// (X over q and k, Y over alpha) until the last Gram MMA, then the next
+// (X over q and k, Y over alpha) until round 3 is done, then the next
 // chunk's tiles are fetched into them
 constexpr uint32_t S_TQ = 0;         // bf16 q tile   [64 t][128 i]  (TMA)
 constexpr uint32_t S_TK = 16384;     // bf16 k tile
 constexpr uint32_t S_TA = 32768;     // bf16 alpha tile
 constexpr uint32_t S_V = 49152;      // bf16 v tile   [64 s][128 j]  MN-major A of U~   (TMA)
-constexpr uint32_t S_TB = 65536;     // bf16 T Diag(beta) [64 t][64 s] K-major B of U~, W
-constexpr uint32_t S_W = 73728;      // fp16 -W^T     [128 i][64 t]  MN-major B of U
-constexpr uint32_t S_QG = 90112;     // fp16 q*gamma  [64 t][128 i]  K-major B of O
-constexpr uint32_t S_KH = 106496;    // fp16 k*rho    [64 s][128 i]  MN-major B of H
-constexpr uint32_t S_KGT = 122880;   // bf16 k*gamma  [64 s][128 i]  MN-major A of W
-constexpr uint32_t S_AQ = 139264;    // fp16 A        [64 t][64 s]   K-major B of O
-constexpr uint32_t S_GX = 147456;    // fp16 Gram X   [128 rows][128 i] K-major A
-constexpr uint32_t S_GY = 180224;    // fp16 Gram Y   [64 rows][128 i]  K-major B
 constexpr uint32_t S_GX2 = S_TQ;     // second Gram buffer (the tile region)
 constexpr uint32_t S_GY2 = S_TA;
-// after the Gram MMAs the 48 KiB of X and Y hold the inverse's 64 x 64 tiles
-// (fp16, one 64-column panel each).  A tile read as a 128-row A operand also
-// reads the 8 KiB after it; those rows only feed TMEM lanes that are ignored.
-constexpr uint32_t S_TD = S_GX + 8192;       // D: inverses of the 16 x 16 diagonal blocks
-constexpr uint32_t S_TE = S_GX + 16384;      // E = D N
-constexpr uint32_t S_TG = S_GX + 24576;      // G = I + E^2
-constexpr uint32_t S_TFm = S_GY;             // F = (I - E) G
-// written by the Gram read-out while later Gram MMAs still read X and Y:
-constexpr uint32_t S_TN = 196608;            // fp16 N: block-strictly-lower part of M
-constexpr uint32_t S_MD = 204800;            // fp32 diagonal 16 x 16 blocks of M [4][16][20]
+constexpr uint32_t S_GX = 65536;     // fp16 Gram X   [128 rows][128 i] K-major A
+constexpr uint32_t S_GY = 98304;     // fp16 Gram Y   [64 rows][128 i]  K-major B
+// once round 2 is done, the inverse's 64 x 64 fp16 tiles live in Gram X:
+constexpr uint32_t S_TE = S_GX;            // E, then F = (I - E) D
+constexpr uint32_t S_TIE = S_GX + 8192;    // I - E, then E^2
+constexpr uint32_t S_TD = S_GX + 16384;    // D: inverses of the 16 x 16 diagonal blocks
+constexpr uint32_t S_TB = 114688;    // bf16 T Diag(beta) [64 t][64 s]; rows 64..127 ...
+constexpr uint32_t S_Z = S_TB + 8192;      // ... are this zero tile
+constexpr uint32_t S_WQ = 131072;    // fp16 [-W^T | (q*gamma)^T] [128 i][64 t] x 2 panels, MN-major B of [U|O]
+constexpr uint32_t S_AK = 163840;    // fp16 [A ; (k*rho)^T] [64 t + 128 i][64 s]  K-major B of [O|H]
+constexpr uint32_t S_KG = 188416;    // bf16 k*gamma  [64 s][128 i]  MN-major A of W^T
+constexpr uint32_t S_TN = 204800;    // fp16 N: block-strictly-lower part of M [64 t][64 s]
+constexpr uint32_t S_MD = 212992;    // fp32 diagonal 16 x 16 blocks of M [4][16][20]
 constexpr int kMdRow = 20, kMdBlk = 16 * kMdRow;  // padded rows spread the banks
-constexpr uint32_t S_SMALL = 209920;
+constexpr uint32_t S_SMALL = 218112;
 constexpr uint32_t S_BETA = S_SMALL;         // fp32 [2][64]
 constexpr uint32_t S_GC = S_SMALL + 512;     // fp32 [2][128] gamma_C
-constexpr uint32_t S_DIAG = S_SMALL + 1536;  // fp32 [16][64] partial q.k
-constexpr uint32_t S_TOT = S_SMALL + 5632;   // fp32 [2][16][8] half-chunk gate totals
-constexpr uint32_t S_BAR = S_SMALL + 6656;   // mbarriers
-constexpr uint32_t SMEM_USED = S_SMALL + 6912;
+constexpr uint32_t S_DIAG = S_SMALL + 1536;  // fp32 [2 panels][64] partial q.k
+constexpr uint32_t S_TOT = S_SMALL + 2048;   // fp32 [4 blocks][128] block totals of alpha
+constexpr uint32_t S_BAR = S_SMALL + 4096;   // mbarriers
+constexpr uint32_t SMEM_USED = S_SMALL + 4352;
 constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;
 static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
 
 // ---- tensor memory columns ----
-constexpr uint32_t T_H = 0;     // H^T fp32 [128 j][128 i]     state accumulator
-constexpr uint32_t T_HA = 128;  // H^T fp16 [128 j][128 i]     A operand (2 per column)
-constexpr uint32_t T_U = 192;   // U^T fp32 [128 j][64 t]
-constexpr uint32_t T_UA = 256;  // U^T fp16 [128 j][64 t]      A operand
-constexpr uint32_t T_O = 288;   // O^T fp32 [128 j][64 t]
-constexpr uint32_t T_G0 = 352;  // Gram rounds use G0, G1, G0; the inverse chain uses
-constexpr uint32_t T_G1 = 416;  //   E:G1, E^2:G0, EG:G1, T:G0; then W^T:G1 (read by the state)
+// [U | O] is the accumulator of the first state MMA and [O | H] of the second
+constexpr uint32_t T_U = 0;     // U^T fp32 [128 j][64 t]
+constexpr uint32_t T_O = 64;    // O^T fp32 [128 j][64 t]
+constexpr uint32_t T_H = 128;   // H^T fp32 [128 j][128 i]     state accumulator
+constexpr uint32_t T_HA = 256;  // H^T fp16 [128 j][128 i]     A operand (2 per column)
+constexpr uint32_t T_UA = 320;  // U^T fp16 [128 j][64 t]      A operand
+constexpr uint32_t T_G0 = 352;  // prep: Gram rounds G0, G1, G0; then E in G1,
+constexpr uint32_t T_G1 = 416;  //   [E^2 | F] in G0..G1, T in G1, W^T in G1
 constexpr uint32_t TMEM_COLS = 512;
+
+// ---- mbarriers ----
+// prep -> MMA warp "operands ready" and MMA warp -> prep "step done", one
+// pair per tensor-core step of the prep role
+enum Step : int { ST_R1 = 0, ST_R2, ST_R3, ST_E, ST_X, ST_T, ST_W, ST_COUNT };
+enum Bar : int {
+  B_QKA = 0,                   // q, k, alpha tiles (TMA)
+  B_V,                         // v tile (TMA)
+  B_OPS,                       // [ST_COUNT]
+  B_DONE = B_OPS + ST_COUNT,   // [ST_COUNT]; B_DONE + ST_W also covers U~
+  B_S1 = B_DONE + ST_COUNT,    // state: [U | O] MMA done
+  B_S3,                        // state: [O | H] MMA done
+  B_READY,                     // [2] prep -> state: chunk operands in place
+  B_GC = B_READY + 2,          // [2] prep -> state: gamma_C published
+  B_OFREE = B_GC + 2,          // state -> MMA warp: O read out, [U | O] free
+  B_COUNT
+};
+static_assert(B_COUNT * 8 <= 192, "mbarrier area");
 
 constexpr uint32_t TILE_BYTES = 16384;
 
@@ -135,14 +165,6 @@ __device__ __forceinline__ Unit unit_of(const FwdArgs& a) {
   return u;
 }
 
-__device__ __forceinline__ void unpack_bf16x8(const uint4& v, float (&f)[8]) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    f[2 * i] = __uint_as_float(w[i] << 16);
-    f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-  }
-}
 __device__ __forceinline__ uint4 pack_half8(const float (&f)[8]) {
   return make_uint4(pack_half2(f[0], f[1]), pack_half2(f[2], f[3]), pack_half2(f[4], f[5]),
                     pack_half2(f[6], f[7]));
@@ -151,210 +173,175 @@ __device__ __forceinline__ uint4 pack_bf8(const float (&f)[8]) {
   return make_uint4(pack_bf162(f[0], f[1]), pack_bf162(f[2], f[3]), pack_bf162(f[4], f[5]),
                     pack_bf162(f[6], f[7]));
 }
-// bf16 x 8 -> fp16 x 8 (through fp32; exact in the fp16 normal range)
-__device__ __forceinline__ uint4 bf16x8_to_half8(const uint4& v) {
-  float f[8];
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    f[2 * i] = __uint_as_float(w[i] << 16);
-    f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-  }
-  return make_uint4(pack_half2(f[0], f[1]), pack_half2(f[2], f[3]), pack_half2(f[4], f[5]),
-                    pack_half2(f[6], f[7]));
-}
-// x (fp16 x 8) times the gate factors f (fp32 x 8, rounded to fp16) -> fp16 x 8
-__device__ __forceinline__ uint4 hmul8(const uint4& x, const float (&f)[8]) {
-  const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
-  uint32_t r[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const __half2 a = *reinterpret_cast<const __half2*>(&xs[i]);
-    const __half2 b = __floats2half2_rn(f[2 * i], f[2 * i + 1]);
-    const __half2 p = __hmul2(a, b);
-    r[i] = *reinterpret_cast<const uint32_t*>(&p);
-  }
-  return make_uint4(r[0], r[1], r[2], r[3]);
-}
-// elementwise product of two fp16 x 8 vectors
-__device__ __forceinline__ uint4 hmul8h(const uint4& x, const uint4& y) {
-  uint4 r;
-  const __half2 p0 = __hmul2(*reinterpret_cast<const __half2*>(&x.x), *reinterpret_cast<const __half2*>(&y.x));
-  const __half2 p1 = __hmul2(*reinterpret_cast<const __half2*>(&x.y), *reinterpret_cast<const __half2*>(&y.y));
-  const __half2 p2 = __hmul2(*reinterpret_cast<const __half2*>(&x.z), *reinterpret_cast<const __half2*>(&y.z));
-  const __half2 p3 = __hmul2(*reinterpret_cast<const __half2*>(&x.w), *reinterpret_cast<const __half2*>(&y.w));
-  r.x = *reinterpret_cast<const uint32_t*>(&p0);
-  r.y = *reinterpret_cast<const uint32_t*>(&p1);
-  r.z = *reinterpret_cast<const uint32_t*>(&p2);
-  r.w = *reinterpret_cast<const uint32_t*>(&p3);
-  return r;
-}
-__device__ __forceinline__ uint4 to_half8(const float (&f)[8]) {
-  return make_uint4(pack_half2(f[0], f[1]), pack_half2(f[2], f[3]), pack_half2(f[4], f[5]),
-                    pack_half2(f[6], f[7]));
-}
-// fp16 x 8 -> bf16 x 8
-__device__ __forceinline__ uint4 half8_to_bf8(const uint4& v) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  uint32_t r[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float2 t = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
-    r[i] = pack_bf162(t.x, t.y);
-  }
-  return make_uint4(r[0], r[1], r[2], r[3]);
-}
-__device__ __forceinline__ float absmax8(const float (&f)[8]) {
-  float m = 0.f;
-#pragma unroll
-  for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(f[e]));
-  return m;
-}
-__device__ __forceinline__ void unpack_half8(const uint4& v, float (&f)[8]) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float2 t = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
-    f[2 * i] = t.x;
-    f[2 * i + 1] = t.y;
-  }
-}
-// true iff no lane of an fp16 x 8 vector is inf or NaN
-__device__ __forceinline__ bool half8_finite(const uint4& v) {
-  const uint32_t m = 0x7c007c00u;
-  return ((v.x & m) != m) && ((v.y & m) != m) && ((v.z & m) != m) && ((v.w & m) != m) &&
-         (((v.x >> 10) & 0x1f) != 0x1f) && (((v.x >> 26) & 0x1f) != 0x1f) &&
-         (((v.y >> 10) & 0x1f) != 0x1f) && (((v.y >> 26) & 0x1f) != 0x1f) &&
-         (((v.z >> 10) & 0x1f) != 0x1f) && (((v.z >> 26) & 0x1f) != 0x1f) &&
-         (((v.w >> 10) & 0x1f) != 0x1f) && (((v.w >> 26) & 0x1f) != 0x1f);
-}
-__device__ __forceinline__ bool fp16_ok8(const float (&f)[8]) {
-  float m = 0.f;
-#pragma unroll
-  for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(f[e]));
-  return m <= 65504.f;  // false for NaN too
-}
-
-// Per-thread state of one prep chunk: tokens t = 4 tq + u, channels 8 j + e.
-// Gate factors are kept as packed fp16 pairs (4 words = 8 channels): they
-// only ever multiply fp16 operands.  gamma_C, which scales the fp32 state,
-// is formed in fp32 separately.
-struct Prep {
-  uint4 k[4], q[4];      // k, q rows as fp16 (8 channels; exact for |x| >= 2^-14)
-  uint4 lp[4], ls[4];    // in-quad inclusive prefix / exclusive suffix products
-  uint4 a1, a2, a3;      // alpha of quad tokens 1, 2, 3 (levels 1 and 2)
-  uint4 F8, F16, F32;    // per level: in-group prefix (upper) or suffix (lower)
-  uint4 E16, X16;        // whole-chunk exclusive prefix / suffix of quad totals
-  int tq;
-
-  // Gate factor of token u of this quad at tree level L: the product of
-  // alpha over (m, t] for an upper-half token, over (s, m] for a lower one.
-  template <int L>
-  __device__ __forceinline__ uint4 factor(int u) const {
-    const int t = 4 * tq + u;
-    const bool upper = (t % (2 * L)) >= L;
-    const uint4 one = make_uint4(0x3c003c00u, 0x3c003c00u, 0x3c003c00u, 0x3c003c00u);
-    if (L == 1) return upper ? (u == 1 ? a1 : a3) : one;
-    if (L == 2) {
-      if (upper) return u == 2 ? a2 : ls[1];  // a2, a2 a3
-      return u == 0 ? a1 : one;
-    }
-    if (L == 4) return upper ? lp[u] : ls[u];
-    const uint4& F = L == 8 ? F8 : (L == 16 ? F16 : F32);
-    return hmul8h(F, upper ? lp[u] : ls[u]);
-  }
-  __device__ __forceinline__ uint4 gamma(int u) const { return hmul8h(E16, lp[u]); }
-  __device__ __forceinline__ uint4 rho(int u) const { return hmul8h(ls[u], X16); }
-};
-
-// Segmented exclusive prefix / suffix products of quad totals within aligned
-// groups of 2, 4, 8, 16 quads, over the 16 quads of a chunk (lanes tq of a
-// 16-wide shuffle segment).  Level L = 8, 16, 32 needs the prefix if this
-// quad is in the upper half of its 2L segment and the suffix otherwise.
-// Quads tq_lo = 0..7 of one half of the chunk sit on the 8 lanes of a
-// shuffle segment; the two halves are in different warps and meet through
-// shared memory (`tot`, after a barrier of the prep role).
-__device__ __forceinline__ void quad_scans(Prep& P, const float (&Bq)[8], float (&E16f)[8],
-                                           float* tot, int j) {
-  const int tq = P.tq, tq_lo = tq & 7, tq_hi = tq >> 3;
-  float I[8], J[8], E[8], X[8];
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    I[e] = Bq[e];
-    J[e] = Bq[e];
-    E[e] = 1.f;
-    X[e] = 1.f;
-  }
-#pragma unroll
-  for (int lg = 0; lg < 3; ++lg) {
-    const int g = 1 << lg;
-    const int base = tq_lo & ~(2 * g - 1);
-    const int srcE = base + g - 1;  // last quad of the first half
-    const int srcX = base + g;      // first quad of the second half
-    const bool second = (tq_lo & g) != 0;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const float vi = __shfl_sync(0xffffffffu, I[e], srcE, 8);
-      const float vj = __shfl_sync(0xffffffffu, J[e], srcX, 8);
-      if (second) E[e] *= vi; else X[e] *= vj;
-      I[e] = E[e] * Bq[e];
-      J[e] = X[e] * Bq[e];
-    }
-    // groups of 2g quads = blocks of 8g tokens serve tree level L = 8g
-    const bool upper = (tq & (2 * g)) != 0;
-    float sel[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) sel[e] = upper ? E[e] : X[e];
-    if (lg == 0) P.F8 = to_half8(sel);
-    if (lg == 1) P.F16 = to_half8(sel);
-    if (lg == 2) P.F32 = to_half8(sel);
-  }
-  // whole chunk: the other half's total comes from the other warp
-  if (tq_lo == 7) {
-#pragma unroll
-    for (int e = 0; e < 8; ++e) tot[(tq_hi * 16 + j) * 8 + e] = I[e];
-  }
-  named_sync(1, 256);
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    if (tq_hi) E[e] *= tot[j * 8 + e];           // first half's total
-    else X[e] *= tot[(16 + j) * 8 + e];          // second half's total
-  }
-  P.E16 = to_half8(E);
-  P.X16 = to_half8(X);
-#pragma unroll
-  for (int e = 0; e < 8; ++e) E16f[e] = E[e];
-}
-
-// Row of token t in level L's operands: upper tokens -> X rank, lower -> Y rank.
-__device__ __forceinline__ int level_rank(int t, int L) {
-  const int seg = t / (2 * L), w = t % (2 * L);
-  return seg * L + (w >= L ? w - L : w);
-}
-
 __device__ __forceinline__ void store16(uint8_t* p, const uint4& v) {
   *reinterpret_cast<uint4*>(p) = v;
 }
+__device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 
-// Builds the Gram operands of one round: levels La (X rows 0..63, Y rows
-// 0..31) and La/2 (X rows 64..127, Y rows 32..63).  X rows of a level are
-// 32 k-rows then 32 q-rows of its upper-half tokens; Y rows its lower-half
-// tokens, each gated by the token's factor at that level.
-template <int L>
-__device__ __forceinline__ void write_level(uint8_t* X, uint8_t* Y, const Prep& P, int j,
-                                            int xbase, int ybase) {
+// ------------------------------------------------ prep elementwise mapping
+// Thread part of the byte offset of the channel pair (64 panel + 2 lane, +1)
+// in a 128B-swizzled tile of R rows with 64-column panels: the panel, the
+// 16-byte chunk (lane >> 2, bits 4..6) and the word in it.
+template <uint32_t R>
+__device__ __forceinline__ uint32_t pair_tb(int panel, int lane) {
+  return (uint32_t)panel * R * 128u + (((uint32_t)lane >> 2) << 4) + (((uint32_t)lane & 3u) << 2);
+}
+// Offset of that pair in row rowbase + rc (rowbase a multiple of 8, rc a
+// compile-time constant): the row's swizzle is an XOR of bits 4..6.
+__device__ __forceinline__ uint32_t pair_at(uint32_t tb, uint32_t rowbase, uint32_t rc) {
+  return (tb ^ ((rc & 7u) << 4)) + (rowbase + rc) * 128u;
+}
+__device__ __forceinline__ void st_pair(uint8_t* p, __half2 v) {
+  *reinterpret_cast<uint32_t*>(p) = h2u(v);
+}
+
+// One 16-token block of one channel pair: k, scale * q and alpha as fp16
+// pairs, the fp32 partial q.k of each token and the fp32 block total of alpha.
+struct Blk {
+  __half2 a[16], k[16], q[16];
+  float dqk[16];
+  float2 tot;
+};
+// Loads the block from the q, k, alpha tiles.  Tokens at or past `live` (the
+// end of the sequence, relative to the block) become identity transitions.
+template <bool kMask>
+__device__ __forceinline__ void load_block(Blk& B, const uint8_t* sm, int blk, int panel, int lane,
+                                           float scale, int live) {
+  B.tot = make_float2(1.f, 1.f);
+  const uint32_t tb = pair_tb<64>(panel, lane);
 #pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    const int t = 4 * P.tq + u;
-    const bool upper = (t % (2 * L)) >= L;
-    const int rank = level_rank(t, L);
-    const uint4 f = P.factor<L>(u);
-    // |factor| <= 1, so the products stay within the range of k and q
-    if (upper) {
-      store16(X + sw128_chunk(128, xbase + rank, j), hmul8h(P.k[u], f));
-      store16(X + sw128_chunk(128, xbase + 32 + rank, j), hmul8h(P.q[u], f));
-    } else {
-      store16(Y + sw128_chunk(64, ybase + rank, j), hmul8h(P.k[u], f));
+  for (int r = 0; r < 16; ++r) {
+    const uint32_t off = pair_at(tb, 16 * blk, r);
+    const uint32_t kw = *reinterpret_cast<const uint32_t*>(sm + S_TK + off);
+    const uint32_t qw = *reinterpret_cast<const uint32_t*>(sm + S_TQ + off);
+    const uint32_t aw = *reinterpret_cast<const uint32_t*>(sm + S_TA + off);
+    float2 kf = make_float2(__uint_as_float(kw << 16), __uint_as_float(kw & 0xffff0000u));
+    float2 qf = make_float2(__uint_as_float(qw << 16) * scale,
+                            __uint_as_float(qw & 0xffff0000u) * scale);
+    float2 af = make_float2(__uint_as_float(aw << 16), __uint_as_float(aw & 0xffff0000u));
+    if (kMask && r >= live) {
+      kf = make_float2(0.f, 0.f);
+      qf = make_float2(0.f, 0.f);
+      af = make_float2(1.f, 1.f);
+    }
+    B.dqk[r] = fmaf(qf.x, kf.x, qf.y * kf.y);
+    B.k[r] = __float22half2_rn(kf);
+    B.q[r] = __float22half2_rn(qf);
+    B.a[r] = __float22half2_rn(af);
+    B.tot.x *= af.x;
+    B.tot.y *= af.y;
+  }
+}
+// Sums v[r] over the 32 lanes of a warp by halving exchanges; afterwards lanes
+// 2m and 2m+1 both hold the sum for r = m.
+__device__ __forceinline__ float warp_sum16(float (&v)[16], int lane) {
+#pragma unroll
+  for (int w = 16, n = 8; w >= 2; w >>= 1, n >>= 1) {
+    const bool hi = (lane & w) != 0;
+#pragma unroll
+    for (int i = 0; i < n; ++i) {
+      const float send = hi ? v[i] : v[i + n];
+      const float keep = hi ? v[i + n] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+    }
+  }
+  return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
+}
+
+// Gram operands of one tree level L <= 8 (pairs inside a 16-token block):
+// X rows xrow.. (k rows) and xrow+32.. (q rows) of its upper tokens, Y rows
+// yrow.. of its lower tokens, each gated by the token's factor: the product
+// of alpha from the start of its upper half to t, or over (s, end of its
+// lower half].  A block holds 8 upper and 8 lower ranks of every such level.
+template <int L, uint32_t XT, uint32_t YT, int XROW, int YROW>
+__device__ __forceinline__ void write_level_in(uint8_t* sm, const Blk& B, int blk, int panel,
+                                               int lane) {
+  const uint32_t tx = pair_tb<128>(panel, lane), ty = pair_tb<64>(panel, lane);
+  uint8_t* X = sm + XT + 8 * blk * 128;
+  uint8_t* Y = sm + YT + 8 * blk * 128;
+#pragma unroll
+  for (int seg = 0; seg < 16; seg += 2 * L) {
+    const int rk0 = (seg / (2 * L)) * L;
+    __half2 f = B.a[seg + L];
+#pragma unroll
+    for (int uu = 0; uu < L; ++uu) {
+      const int r = seg + L + uu;
+      if (uu > 0) f = __hmul2(f, B.a[r]);
+      st_pair(X + pair_at(tx, XROW, rk0 + uu), __hmul2(B.k[r], f));
+      st_pair(X + pair_at(tx, XROW + 32, rk0 + uu), __hmul2(B.q[r], f));
+    }
+    __half2 b = B.a[seg + L - 1];
+#pragma unroll
+    for (int uu = L - 1; uu >= 0; --uu) {
+      const int r = seg + uu;
+      if (uu < L - 2) b = __hmul2(b, B.a[r + 1]);
+      st_pair(Y + pair_at(ty, YROW, rk0 + uu), uu == L - 1 ? B.k[r] : __hmul2(B.k[r], b));
+    }
+  }
+}
+// Cross-block levels 32 and 16 of block BLK: level 32 into X rows x32 (k),
+// x32 + 32 (q) or Y rows y32, level 16 into x16 / y16.  Block b is upper at
+// level 16 if b is odd and at level 32 if b >= 2.  Upper factors are the
+// running in-block prefix product of alpha (times block 2's total in block 3
+// at level 32); lower factors the running in-block exclusive suffix product
+// (times block 1's total in block 0 at level 32).  Ranks: 16 (b >> 1) + r at
+// level 16, 16 (b mod 2) + r at level 32.
+template <int BLK, uint32_t XT, uint32_t YT>
+__device__ __forceinline__ void write_cross(uint8_t* sm, const Blk& B, __half2 t1, __half2 t2,
+                                            int panel, int lane) {
+  constexpr bool up16 = (BLK & 1) != 0, up32 = BLK >= 2;
+  constexpr int rb16 = 16 * (BLK >> 1), rb32 = 16 * (BLK & 1);
+  constexpr int x32 = 0, x16 = 64, y32 = 0, y16 = 32;
+  const uint32_t tx = pair_tb<128>(panel, lane), ty = pair_tb<64>(panel, lane);
+  uint8_t* X = sm + XT;
+  uint8_t* Y = sm + YT;
+  if (up16 || up32) {
+    __half2 pr = B.a[0];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      if (r > 0) pr = __hmul2(pr, B.a[r]);
+      if (up16) {
+        st_pair(X + pair_at(tx, x16 + rb16, r), __hmul2(B.k[r], pr));
+        st_pair(X + pair_at(tx, x16 + 32 + rb16, r), __hmul2(B.q[r], pr));
+      }
+      if (up32) {
+        const __half2 f = BLK == 3 ? __hmul2(t2, pr) : pr;
+        st_pair(X + pair_at(tx, x32 + rb32, r), __hmul2(B.k[r], f));
+        st_pair(X + pair_at(tx, x32 + 32 + rb32, r), __hmul2(B.q[r], f));
+      }
+    }
+  }
+  if (!up16 || !up32) {
+    __half2 sr = B.a[15];
+#pragma unroll
+    for (int r = 15; r >= 0; --r) {
+      if (r < 14) sr = __hmul2(sr, B.a[r + 1]);
+      if (!up16) st_pair(Y + pair_at(ty, y16 + rb16, r), r == 15 ? B.k[r] : __hmul2(B.k[r], sr));
+      if (!up32) {
+        const __half2 g = BLK == 0 ? (r == 15 ? t1 : __hmul2(sr, t1)) : sr;
+        st_pair(Y + pair_at(ty, y32 + rb32, r),
+                (BLK == 1 && r == 15) ? B.k[r] : __hmul2(B.k[r], g));
+      }
+    }
+  }
+}
+// Rows i0 = 64 panel + 2 lane and i0 + 1 of a transposed [i][t] tile (one
+// 64-column panel, rows of 128 bytes): the 16 tokens of block blk are two
+// 16-byte chunks per row, assembled from the per-token channel pairs.
+__device__ __forceinline__ void store_transposed(uint8_t* tile, const __half2 (&v)[16], int blk,
+                                                 int panel, int lane) {
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    const uint32_t i = (uint32_t)(64 * panel + 2 * lane + e);
+    const uint32_t sel = e ? 0x7632u : 0x5410u;
+#pragma unroll
+    for (int hc = 0; hc < 2; ++hc) {
+      uint32_t w[4];
+#pragma unroll
+      for (int m = 0; m < 4; ++m)
+        w[m] = __byte_perm(h2u(v[8 * hc + 2 * m]), h2u(v[8 * hc + 2 * m + 1]), sel);
+      const uint32_t ch = (uint32_t)(2 * blk + hc);
+      store16(tile + i * 128u + ((ch ^ (i & 7u)) << 4), make_uint4(w[0], w[1], w[2], w[3]));
     }
   }
 }
@@ -468,6 +455,8 @@ __device__ __forceinline__ void invert_diag_blocks(uint8_t* sm, int p) {
     *reinterpret_cast<__half*>(sm + S_TD + sw128_off(64, o + t, o + c)) = __float2half_rn(x[t]);
 }
 
+
+
 __global__ void __launch_bounds__(NT, 1)
     fwd_chunk_kernel(const __grid_constant__ FwdArgs a, const __grid_constant__ CUtensorMap mq,
                      const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap ma,
@@ -476,39 +465,24 @@ __global__ void __launch_bounds__(NT, 1)
   uint8_t* sm = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  uint64_t* bar_v = reinterpret_cast<uint64_t*>(sm + S_BAR);
-  uint64_t* bar_w = bar_v + 2;
-  uint64_t* bar_s1 = bar_v + 3;
-  uint64_t* bar_s3 = bar_v + 4;
-  uint64_t* bar_t = bar_v + 5;
-  uint64_t* bar_qka = bar_v + 6;
-  // prep -> state handoffs, one barrier per chunk parity so that a waiter can
-  // never fall a whole phase behind: operands of chunk c complete, gamma_C
-  // of chunk c published.  The state -> prep direction uses bar_s1 (TB, W
-  // free) and bar_s3 (q*gamma, k*rho, A free) directly.
-  uint64_t* bar_ready = bar_v + 7;   // [2]
-  uint64_t* bar_gc = bar_v + 9;      // [2]
-  // one barrier per Gram round: rounds 1 and 2 are both in flight before
-  // round 1 is waited for, so a shared barrier could run two phases ahead
-  uint64_t* bar_r = bar_v + 11;      // [3]
-  int* s_abort = reinterpret_cast<int*>(sm + S_BAR + 128);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + S_BAR + 136);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + S_BAR);
+  uint64_t* bar_qka = bars + B_QKA;
+  uint64_t* bar_v = bars + B_V;
+  uint64_t* bar_ops = bars + B_OPS;
+  uint64_t* bar_done = bars + B_DONE;
+  uint64_t* bar_s1 = bars + B_S1;
+  uint64_t* bar_s3 = bars + B_S3;
+  uint64_t* bar_ready = bars + B_READY;
+  uint64_t* bar_gc = bars + B_GC;
+  uint64_t* bar_ofree = bars + B_OFREE;
+  int* s_abort = reinterpret_cast<int*>(sm + S_BAR + 192);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + S_BAR + 200);
 
   const Unit u = unit_of(a);
   const int nchunks = (u.len + C - 1) / C;
 
   if (tid == 0) {
-    mbar_init(bar_v, 1);
-    mbar_init(bar_w, 1);
-    mbar_init(bar_s1, 1);
-    mbar_init(bar_s3, 1);
-    mbar_init(bar_t, 1);
-    mbar_init(bar_qka, 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(bar_ready + i, 1);
-      mbar_init(bar_gc + i, 1);
-    }
-    for (int i = 0; i < 3; ++i) mbar_init(bar_r + i, 1);
+    for (int i = 0; i < B_COUNT; ++i) mbar_init(bars + i, 1);
     *s_abort = 0;
     fence_mbar_init();
     tma_prefetch_desc(&mq);
@@ -516,16 +490,18 @@ __global__ void __launch_bounds__(NT, 1)
     tma_prefetch_desc(&ma);
     tma_prefetch_desc(&mv);
   }
-  // A's upper triangle and N's blocks on and above the 16-block diagonal are
-  // never written again, so zero both tiles once
+  // A's upper triangle, N's blocks on and above the 16-block diagonal and the
+  // tile under T Diag(beta) are never written: clear them once
   for (int e = tid; e < 8192 / 16; e += NT) {
-    reinterpret_cast<uint4*>(sm + S_AQ)[e] = make_uint4(0, 0, 0, 0);
+    reinterpret_cast<uint4*>(sm + S_AK)[e] = make_uint4(0, 0, 0, 0);
     reinterpret_cast<uint4*>(sm + S_TN)[e] = make_uint4(0, 0, 0, 0);
+    reinterpret_cast<uint4*>(sm + S_Z)[e] = make_uint4(0, 0, 0, 0);
   }
   if (warp == 0) {
     tmem_alloc(tmem_slot, TMEM_COLS);
     tmem_relinquish();
   }
+  fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -537,24 +513,16 @@ __global__ void __launch_bounds__(NT, 1)
     // =================================================================== PREP
     const int p = tid;
     const int w = p >> 5;
-    // a warp holds 8 quads (32 tokens) x 4 channel chunks: its 16-byte tile
-    // accesses then fall on 8 distinct swizzle positions (conflict-free)
-    const int j = 4 * (w >> 1) + (lane >> 3);  // channel chunk
-    const int tq = 8 * (w & 1) + (lane & 7);   // token quad
-    const int wq = w & 3, half = w >> 2;
+    const int blk = w >> 1, panel = w & 1;     // elementwise mapping
+    const int wq = w & 3, half = w >> 2;       // TMEM lane quarter, column half
+    const int trow = 32 * wq + lane;           // this thread's TMEM lane
+    const uint32_t tl = (uint32_t)(32 * wq) << 16;
     const __nv_bfloat16* gb = static_cast<const __nv_bfloat16*>(a.beta);
-    uint32_t t_phase = 0;
+    const bool beta_lane = panel == 0 && lane < 16;
+    const int bt = 16 * blk + lane;            // token whose beta this lane fetches
     bool alive = true;
-    float beta_next[4] = {0.f, 0.f, 0.f, 0.f};
-    if (j == 0 && nchunks > 0) {
-      const int len0 = min(C, u.len);
-#pragma unroll
-      for (int uu = 0; uu < 4; ++uu) {
-        const int t = 4 * tq + uu;
-        beta_next[uu] = t < len0 ? __bfloat162float(gb[u.row0 + t]) : 0.f;
-      }
-    }
-    // q, k, alpha tiles of chunk cc (issued by one thread)
+    float beta_next = 0.f;
+    if (beta_lane && nchunks > 0 && bt < min(C, u.len)) beta_next = __bfloat162float(gb[u.row0 + bt]);
     auto issue_qka = [&](int cc) {
       const int y = (int)(u.row0 + (long)cc * C);
       mbar_arrive_expect_tx(bar_qka, 3 * TILE_BYTES);
@@ -565,276 +533,186 @@ __global__ void __launch_bounds__(NT, 1)
       tma_load_2d(sm + S_TA, &ma, bar_qka, 0, y);
       tma_load_2d(sm + S_TA + 8192, &ma, bar_qka, 64, y);
     };
-    if (p == 0 && nchunks > 0) issue_qka(0);
-    // waits on an mbarrier fed by this role's MMAs or copies; the AND over
-    // the role decides, uniformly, whether to go on
-    auto prep_wait = [&](uint64_t* bar, uint32_t& phase) -> bool {
-      const bool ok = mbar_wait(bar, phase & 1);
-      ++phase;
+    auto issue_v = [&](int cc) {
+      const int y = (int)(u.row0 + (long)cc * C);
+      mbar_arrive_expect_tx(bar_v, TILE_BYTES);
+      tma_load_2d(sm + S_V, &mv, bar_v, 0, y);
+      tma_load_2d(sm + S_V + 8192, &mv, bar_v, 64, y);
+    };
+    if (p == 0 && nchunks > 0) {
+      issue_qka(0);
+      issue_v(0);
+    }
+    // waits for a completion of chunk cc on `bar` (one phase per chunk); the
+    // AND over the role decides, uniformly, whether to go on
+    auto prep_wait = [&](uint64_t* bar, int cc) -> bool {
+      const bool ok = cc < 0 ? true : mbar_wait(bar, (uint32_t)(cc & 1));
       const bool all = named_and(BAR_PREP, NPREP, ok);
       tc_fence_after();
       return all;
     };
-    // waits for the state role's MMA of chunk cc (bar_s1 or bar_s3); nothing
-    // to wait for before the first chunk
-    auto prep_state = [&](uint64_t* bar, int cc) -> bool {
-      const bool ok = cc < 0 ? true : mbar_wait(bar, (uint32_t)(cc & 1));
-      return named_and(BAR_PREP, NPREP, ok);
+    // hands the operands written so far to the tensor-core step `st`
+    auto handoff = [&](int st) {
+      fence_proxy_async_smem();
+      tc_fence_before();
+      named_sync(BAR_PREP, NPREP);
+      if (p == 0) mbar_arrive(bar_ops + st);
     };
-    // the MMA of the inverse chain: D[lanes 0..63] = A (rows 0..63 used) x B
-    auto t_mma = [&](uint32_t d_col, uint32_t a_tile, uint32_t b_tile) {
-      const uint64_t da = kmajor_desc(sb + a_tile, 128, 0), db = mnmajor_desc(sb + b_tile, 64, 0);
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        umma_ss(tmem + d_col, da + (uint64_t)(2 * k), db + (uint64_t)(128 * k),
-                idesc_f16(128, 64, 0, 0, 1), k > 0);
-      umma_commit(bar_t);
-    };
-    auto gram_mma = [&](uint32_t d_col, uint32_t xbuf, uint32_t ybuf, uint64_t* bar) {
-      const uint64_t d_gx = kmajor_desc(sb + xbuf, 128, 0), d_gy = kmajor_desc(sb + ybuf, 64, 0);
-#pragma unroll
-      for (int k = 0; k < 8; ++k)  // K steps: 32 bytes in a panel, panels R*128 apart
-        umma_ss(tmem + d_col, d_gx + (uint64_t)((k >> 2) * 1024 + (k & 3) * 2),
-                d_gy + (uint64_t)((k >> 2) * 512 + (k & 3) * 2), idesc_f16(128, 64, 0, 0, 0),
-                k > 0);
-      umma_commit(bar);
-    };
-    const bool tconv = wq < 2;  // warps 0,1,4,5 reach TMEM lanes 0..63
-    const int trow = 32 * wq + lane;
-    const uint32_t tl = (uint32_t)(32 * (wq & 1)) << 16;
-    const uint32_t tlw = (uint32_t)(32 * wq) << 16;
-    uint8_t* AQ = sm + S_AQ;
-
-    uint8_t* X1 = sm + S_GX;   // Gram operand buffers: the dedicated one and the tile region
-    uint8_t* Y1 = sm + S_GY;
-    uint8_t* X2 = sm + S_GX2;
-    uint8_t* Y2 = sm + S_GY2;
+    uint8_t* AQ = sm + S_AK;
     float* dg = reinterpret_cast<float*>(sm + S_DIAG);
+    float2* totv = reinterpret_cast<float2*>(sm + S_TOT);
     for (int c = 0; c < nchunks && alive; ++c) {
       const int lenc = min(C, u.len - c * C);
       const int buf = c & 1;
       const long rbase = u.row0 + (long)c * C;
-      // ---- this chunk's q, k, alpha tiles
-      {
-        uint32_t ph = (uint32_t)c;
-        if (!prep_wait(bar_qka, ph)) { alive = false; break; }
-      }
-      Prep P;
-      P.tq = tq;
-      float Bq[8];
-      {
-        float al[4][8];
-        uint32_t inf_or_nan = 0;
-#pragma unroll
-        for (int uu = 0; uu < 4; ++uu) {
-          const int t = 4 * tq + uu;
-          const uint32_t off = sw128_chunk(64, t, j);
-          float kk[8], qq[8];
-          unpack_bf16x8(*reinterpret_cast<const uint4*>(sm + S_TK + off), kk);
-          unpack_bf16x8(*reinterpret_cast<const uint4*>(sm + S_TQ + off), qq);
-          unpack_bf16x8(*reinterpret_cast<const uint4*>(sm + S_TA + off), al[uu]);
-          float sacc = 0.f;  // partial q.k over this thread's 8 channels
-#pragma unroll
-          for (int e = 0; e < 8; ++e) sacc = fmaf(qq[e], kk[e], sacc);
-          P.k[uu] = to_half8(kk);
-          P.q[uu] = to_half8(qq);
-          if (lenc < C && t >= lenc) {  // past the end of the sequence: identity transition
-            P.k[uu] = make_uint4(0, 0, 0, 0);
-            P.q[uu] = make_uint4(0, 0, 0, 0);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) al[uu][e] = 1.f;
-            sacc = 0.f;
-          }
-          dg[j * 64 + t] = sacc;
-          // an input outside the fp16 range turns into inf here
-          const uint32_t w4[4] = {P.q[uu].x | P.k[uu].x, P.q[uu].y | P.k[uu].y,
-                                  P.q[uu].z | P.k[uu].z, P.q[uu].w | P.k[uu].w};
-#pragma unroll
-          for (int z = 0; z < 4; ++z) inf_or_nan |= __vcmpeq2(w4[z] & 0x7c007c00u, 0x7c007c00u);
-        }
-        ovf |= inf_or_nan != 0;
-        // in-quad prefix / suffix products (fp32, then packed halves)
-        float lp[8], ls[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) { lp[e] = al[0][e]; ls[e] = 1.f; }
-        P.lp[0] = to_half8(lp);
-#pragma unroll
-        for (int uu = 1; uu < 4; ++uu) {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) lp[e] *= al[uu][e];
-          P.lp[uu] = to_half8(lp);
-        }
-#pragma unroll
-        for (int e = 0; e < 8; ++e) Bq[e] = lp[e];
-        P.ls[3] = to_half8(ls);
-#pragma unroll
-        for (int uu = 2; uu >= 0; --uu) {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) ls[e] *= al[uu + 1][e];
-          P.ls[uu] = to_half8(ls);
-        }
-        P.a1 = to_half8(al[1]);
-        P.a2 = to_half8(al[2]);
-        P.a3 = to_half8(al[3]);
-      }
-      // beta: this chunk's values were loaded one chunk ahead
+      // beta: this chunk's values were fetched one chunk ahead
       float* beta_s = reinterpret_cast<float*>(sm + S_BETA) + 64 * buf;
-      if (j == 0) {
+      if (beta_lane) {
+        beta_s[bt] = beta_next;
+        beta_next = 0.f;
+        if (c + 1 < nchunks && bt < min(C, u.len - (c + 1) * C))
+          beta_next = __bfloat162float(gb[rbase + C + bt]);
+      }
+      // ---- this chunk's q, k, alpha tiles
+      if (!prep_wait(bar_qka, c)) { alive = false; break; }
+      Blk B;
+      if (lenc == C) load_block<false>(B, sm, blk, panel, lane, a.scale, C);
+      else load_block<true>(B, sm, blk, panel, lane, a.scale, lenc - 16 * blk);
+      {
+        const float sq = warp_sum16(B.dqk, lane);   // q.k over this panel's 64 channels
+        if ((lane & 1) == 0) dg[64 * panel + 16 * blk + (lane >> 1)] = sq;
+      }
+      totv[64 * blk + 32 * panel + lane] = B.tot;
+      // every tile read is done (the tile region becomes Gram buffer 2) and
+      // every block total is visible
+      named_sync(BAR_PREP, NPREP);
+      float2 T4[4];
 #pragma unroll
-        for (int uu = 0; uu < 4; ++uu) beta_s[4 * tq + uu] = beta_next[uu];
-        if (c + 1 < nchunks) {
-          const int lenn = min(C, u.len - (c + 1) * C);
+      for (int b = 0; b < 4; ++b) T4[b] = totv[64 * b + 32 * panel + lane];
+      float2 gbf = make_float2(1.f, 1.f), gaf = make_float2(1.f, 1.f);
 #pragma unroll
-          for (int uu = 0; uu < 4; ++uu) {
-            const int t = 4 * tq + uu;
-            beta_next[uu] = t < lenn ? __bfloat162float(gb[rbase + C + t]) : 0.f;
-          }
+      for (int b = 0; b < 4; ++b) {
+        if (b < blk) { gbf.x *= T4[b].x; gbf.y *= T4[b].y; }
+        if (b > blk) { gaf.x *= T4[b].x; gaf.y *= T4[b].y; }
+      }
+      const __half2 Gb = __float22half2_rn(gbf), Ga = __float22half2_rn(gaf);
+      const __half2 t1 = __float22half2_rn(T4[1]), t2 = __float22half2_rn(T4[2]);
+      // gamma_C (fp32: it scales the fp32 state)
+      float* gC = reinterpret_cast<float*>(sm + S_GC) + 128 * buf;
+      if (blk == 0)
+        reinterpret_cast<float2*>(gC)[32 * panel + lane] =
+            make_float2(T4[0].x * T4[1].x * T4[2].x * T4[3].x, T4[0].y * T4[1].y * T4[2].y * T4[3].y);
+      // ---- Gram round 1: levels 8 and 4 (pairs inside 16-token blocks)
+      write_level_in<8, S_GX2, S_GY2, 0, 0>(sm, B, blk, panel, lane);
+      write_level_in<4, S_GX2, S_GY2, 64, 32>(sm, B, blk, panel, lane);
+      handoff(ST_R1);
+      if (p == 0) mbar_arrive(bar_gc + buf);
+      // ---- round 2: levels 2 and 1 (buffer 1 held the previous chunk's
+      // inverse tiles, all read before its T step completed)
+      write_level_in<2, S_GX, S_GY, 0, 0>(sm, B, blk, panel, lane);
+      write_level_in<1, S_GX, S_GY, 64, 32>(sm, B, blk, panel, lane);
+      handoff(ST_R2);
+      // ---- gamma_t = (earlier blocks' totals) x prefix_t, a running product;
+      // k*gamma (bf16, A of the W^T step; the previous W^T step is done)
+      __half2 gq[16];
+      {
+        __half2 g = Gb;
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+          g = __hmul2(g, B.a[r]);
+          const float2 kg = __half22float2(__hmul2(B.k[r], g));
+          *reinterpret_cast<uint32_t*>(sm + S_KG + pair_at(pair_tb<64>(panel, lane), 16 * blk, r)) =
+              pack_bf162(kg.x, kg.y);
+          gq[r] = __hmul2(B.q[r], g);
         }
       }
-      // ---- gate products across quads (the scan's barrier also ends the
-      // reads of the tile region, which now becomes Gram buffer 2)
-      float E16f[8];
-      quad_scans(P, Bq, E16f, reinterpret_cast<float*>(sm + S_TOT), j);
-      // gamma_C (fp32: it scales the fp32 state): the last quad publishes it
-      float* gC = reinterpret_cast<float*>(sm + S_GC) + 128 * buf;
-      if (tq == 15) {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) gC[8 * j + e] = E16f[e] * Bq[e];
-      }
-      // ---- Gram round 1: levels 8 and 4 (pairs inside 16-token blocks)
-      write_level<8>(X2, Y2, P, j, 0, 0);
-      write_level<4>(X2, Y2, P, j, 64, 32);
-      fence_proxy_async_smem();
-      named_sync(BAR_PREP, NPREP);
-      if (p == 0) {
-        mbar_arrive(bar_gc + (c & 1));
-        tc_fence_after();
-        gram_mma(T_G0, S_GX2, S_GY2, bar_r + 0);
-      }
-      // ---- round 2: levels 2 and 1.  Its TMEM tile G1 last held W of the
-      // previous chunk, which the state warps convert before their U-MMA.
-      write_level<2>(X1, Y1, P, j, 0, 0);
-      write_level<1>(X1, Y1, P, j, 64, 32);
-      fence_proxy_async_smem();
-      if (!prep_state(bar_s1, c - 1)) { alive = false; break; }
-      if (p == 0) { tc_fence_after(); gram_mma(T_G1, S_GX, S_GY, bar_r + 1); }
-      // ---- k*gamma (bf16, A of the W-MMA; the previous W-MMA is done with it)
+      // ---- (q*gamma)^T next to -W^T: the previous chunk's [U | O] MMA read them
+      if (!prep_wait(bar_s1, c - 1)) { alive = false; break; }
+      store_transposed(sm + S_WQ + 16384, gq, blk, panel, lane);
+      // ---- (k*rho)^T under A, rho_s = exclusive suffix x later blocks' totals:
+      // the previous chunk's [O | H] MMA read them (and A, which the Gram
+      // read-out below overwrites)
       {
-        const bool ok = c == 0 ? true : mbar_wait(bar_w, (uint32_t)((c - 1) & 1));
-        if (!named_and(BAR_PREP, NPREP, ok)) { alive = false; break; }
-      }
+        __half2 rr = Ga;
 #pragma unroll
-      for (int uu = 0; uu < 4; ++uu) {
-        const int t = 4 * tq + uu;
-        store16(sm + S_KGT + sw128_chunk(64, t, j), half8_to_bf8(hmul8h(P.k[uu], P.gamma(uu))));
+        for (int r = 15; r >= 0; --r) {
+          if (r < 15) rr = __hmul2(rr, B.a[r + 1]);
+          gq[r] = __hmul2(B.k[r], rr);
+        }
       }
-      // ---- q*gamma, k*rho: the previous chunk's last MMA must have read them
-      // (and A, which the Gram read-out below overwrites)
-      if (!prep_state(bar_s3, c - 1)) { alive = false; break; }
-#pragma unroll
-      for (int uu = 0; uu < 4; ++uu) {
-        const int t = 4 * tq + uu;
-        store16(sm + S_QG + sw128_chunk(64, t, j), hmul8h(P.q[uu], P.gamma(uu)));
-        store16(sm + S_KH + sw128_chunk(64, t, j), hmul8h(P.k[uu], P.rho(uu)));
-      }
+      if (!prep_wait(bar_s3, c - 1)) { alive = false; break; }
+      store_transposed(sm + S_AK + 8192, gq, blk, panel, lane);
       // ---- round 3 (levels 32 and 16) goes into buffer 2 once round 1 is done
-      uint32_t rph = (uint32_t)c;
-      if (!prep_wait(bar_r + 0, rph)) { alive = false; break; }
+      if (!prep_wait(bar_done + ST_R1, c)) { alive = false; break; }
       if (half == 0) extract_round<8>(sm, tmem, T_G0, wq, lane, beta_s, AQ);
-      write_level<32>(X2, Y2, P, j, 0, 0);
-      write_level<16>(X2, Y2, P, j, 64, 32);
-      fence_proxy_async_smem();
-      tc_fence_before();
-      named_sync(BAR_PREP, NPREP);
-      if (p == 0) { tc_fence_after(); gram_mma(T_G0, S_GX2, S_GY2, bar_r + 2); }
-      rph = (uint32_t)c;
-      if (!prep_wait(bar_r + 1, rph)) { alive = false; break; }  // round 2
+      switch (blk) {
+        case 0: write_cross<0, S_GX2, S_GY2>(sm, B, t1, t2, panel, lane); break;
+        case 1: write_cross<1, S_GX2, S_GY2>(sm, B, t1, t2, panel, lane); break;
+        case 2: write_cross<2, S_GX2, S_GY2>(sm, B, t1, t2, panel, lane); break;
+        default: write_cross<3, S_GX2, S_GY2>(sm, B, t1, t2, panel, lane); break;
+      }
+      handoff(ST_R3);
+      if (!prep_wait(bar_done + ST_R2, c)) { alive = false; break; }
       if (half == 1) extract_round<2>(sm, tmem, T_G1, wq, lane, beta_s, AQ);
-      // D lives where Gram X was: zero it (its diagonal blocks come next)
+      // D lives where Gram X was: clear it (its diagonal blocks come next)
       for (int e = p; e < 8192 / 16; e += NPREP) store16(sm + S_TD + 16 * e, make_uint4(0, 0, 0, 0));
       tc_fence_before();
       named_sync(BAR_PREP, NPREP);
-      // ---- T = (I + M)^-1 = (I - E)(I + E^2) D with D the inverse of the
-      // block diagonal of I + M and E = D N (E^4 = 0: N is strictly lower by
-      // 16-blocks); D is formed while round 3 runs, the products on tensor cores
+      // ---- T = (I + M)^-1: D is formed while round 3 runs
       if (p < 64) invert_diag_blocks(sm, p);
-      rph = (uint32_t)c;
-      if (!prep_wait(bar_r + 2, rph)) { alive = false; break; }  // round 3
+      if (!prep_wait(bar_done + ST_R3, c)) { alive = false; break; }
       // the tile region is free: fetch the next chunk's q, k, alpha
       if (p == 0 && c + 1 < nchunks) issue_qka(c + 1);
       if (half == 0) extract_round<32>(sm, tmem, T_G0, wq, lane, beta_s, AQ);
       else if (p >= 128 && p < 192) {
         const int t = p - 128;
-        float sacc = 0.f;
-#pragma unroll
-        for (int jj = 0; jj < 16; ++jj) sacc += dg[jj * 64 + t];
-        *reinterpret_cast<__half*>(AQ + sw128_off(64, t, t)) = __float2half_rn(sacc);
+        *reinterpret_cast<__half*>(AQ + sw128_off(64, t, t)) = __float2half_rn(dg[t] + dg[64 + t]);
       }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      named_sync(BAR_PREP, NPREP);
-      if (p == 0) { tc_fence_after(); t_mma(T_G1, S_TD, S_TN); }       // E = D N
-      if (!prep_wait(bar_t, t_phase)) { alive = false; break; }
-      if (tconv) {
+      handoff(ST_E);                                             // E = D N
+      // ---- E -> [E ; I - E] (rows t of two tiles): lanes 0..63
+      if (!prep_wait(bar_done + ST_E, c)) { alive = false; break; }
+      if (wq < 2) {
         uint32_t v[32];
         tmem_ld32<32>(tmem + tl + T_G1 + 32 * half, v);
         tmem_ld_wait();
+#pragma unroll
+        for (int z = 0; z < 32; z += 8) {
+          float f[8], g[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            f[e] = __uint_as_float(v[z + e]);
+            g[e] = ((32 * half + z + e) == trow ? 1.f : 0.f) - f[e];
+          }
+          const uint32_t ch = (uint32_t)(32 * half + z) >> 3;
+          store16(sm + S_TE + sw128_chunk(64, trow, ch), pack_half8(f));
+          store16(sm + S_TIE + sw128_chunk(64, trow, ch), pack_half8(g));
+        }
+      }
+      handoff(ST_X);                                             // [E^2 | F]
+      // ---- E^2 (G0, lanes 0..63) under F (G1, lanes 64..127)
+      if (!prep_wait(bar_done + ST_X, c)) { alive = false; break; }
+      {
+        const bool e2 = wq < 2;
+        const int r = e2 ? trow : trow - 64;
+        uint32_t v[32];
+        tmem_ld32<32>(tmem + tl + (e2 ? T_G0 : T_G1) + 32 * half, v);
+        tmem_ld_wait();
+        uint8_t* dst = sm + (e2 ? S_TIE : S_TE);
 #pragma unroll
         for (int z = 0; z < 32; z += 8) {
           float f[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(v[z + e]);
-          store16(sm + S_TE + sw128_chunk(64, trow, (32 * half + z) >> 3), pack_half8(f));
+          store16(dst + sw128_chunk(64, r, (uint32_t)(32 * half + z) >> 3), pack_half8(f));
         }
       }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      named_sync(BAR_PREP, NPREP);
-      if (p == 0) { tc_fence_after(); t_mma(T_G0, S_TE, S_TE); }       // E^2
-      if (!prep_wait(bar_t, t_phase)) { alive = false; break; }
-      float gv[32];  // G = I + E^2, kept for F
-      if (tconv) {
-        uint32_t v[32];
-        tmem_ld32<32>(tmem + tl + T_G0 + 32 * half, v);
-        tmem_ld_wait();
-#pragma unroll
-        for (int z = 0; z < 32; ++z)
-          gv[z] = __uint_as_float(v[z]) + ((32 * half + z) == trow ? 1.f : 0.f);
-#pragma unroll
-        for (int z = 0; z < 32; z += 8) {
-          float f[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) f[e] = gv[z + e];
-          store16(sm + S_TG + sw128_chunk(64, trow, (32 * half + z) >> 3), pack_half8(f));
-        }
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      named_sync(BAR_PREP, NPREP);
-      if (p == 0) { tc_fence_after(); t_mma(T_G1, S_TE, S_TG); }       // E G
-      if (!prep_wait(bar_t, t_phase)) { alive = false; break; }
-      if (tconv) {
+      handoff(ST_T);                                             // T = F + E^2 F
+      // ---- T Diag(beta) as bf16: T is in G1, lanes 64..127
+      if (!prep_wait(bar_done + ST_T, c)) { alive = false; break; }
+      if (wq >= 2) {
+        const int r = trow - 64;
         uint32_t v[32];
         tmem_ld32<32>(tmem + tl + T_G1 + 32 * half, v);
-        tmem_ld_wait();
-#pragma unroll
-        for (int z = 0; z < 32; z += 8) {
-          float f[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) f[e] = gv[z + e] - __uint_as_float(v[z + e]);  // F = G - E G
-          store16(sm + S_TFm + sw128_chunk(64, trow, (32 * half + z) >> 3), pack_half8(f));
-        }
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      named_sync(BAR_PREP, NPREP);
-      if (p == 0) { tc_fence_after(); t_mma(T_G0, S_TFm, S_TD); }      // T = F D
-      if (!prep_wait(bar_t, t_phase)) { alive = false; break; }
-      // ---- T Diag(beta) as bf16 (TB is single-buffered: the previous
-      // chunk's U-MMA read it before this chunk's round 2 was issued)
-      if (tconv) {
-        uint32_t v[32];
-        tmem_ld32<32>(tmem + tl + T_G0 + 32 * half, v);
         tmem_ld_wait();
 #pragma unroll
         for (int z = 0; z < 32; z += 8) {
@@ -842,29 +720,34 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             const int s = 32 * half + z + e;
-            f[e] = s <= trow ? __uint_as_float(v[z + e]) * beta_s[s] : 0.f;
+            f[e] = s <= r ? __uint_as_float(v[z + e]) * beta_s[s] : 0.f;
           }
-          store16(sm + S_TB + sw128_chunk(64, trow, (32 * half + z) >> 3), pack_bf8(f));
+          store16(sm + S_TB + sw128_chunk(64, r, (uint32_t)(32 * half + z) >> 3), pack_bf8(f));
+        }
+      }
+      handoff(ST_W);                                             // W^T, and U~ into [U | O]
+      // ---- -W^T (fp16, panel 0 of [-W^T | (q*gamma)^T]): W^T is in G1, lane = i
+      if (!prep_wait(bar_done + ST_W, c)) { alive = false; break; }
+      if (p == 0 && c + 1 < nchunks) issue_v(c + 1);   // U~ has read the v tile
+      {
+        uint32_t v[32];
+        tmem_ld32<32>(tmem + tl + T_G1 + 32 * half, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int z = 0; z < 32; z += 8) {
+          float f[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) f[e] = -__uint_as_float(v[z + e]);
+          store16(sm + S_WQ + sw128_chunk(64, trow, (uint32_t)(32 * half + z) >> 3), pack_half8(f));
         }
       }
       fence_proxy_async_smem();
       tc_fence_before();
       named_sync(BAR_PREP, NPREP);
-      if (p == 0) {
-        tc_fence_after();
-        // W^T[i][t] = sum_s (k*gamma)[s][i] TB[t][s], into G1; the state warps
-        // read it out
-        const uint64_t da = mnmajor_desc(sb + S_KGT, 64, 0), db = kmajor_desc(sb + S_TB, 64, 0);
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          umma_ss(tmem + T_G1, da + (uint64_t)(128 * k), db + (uint64_t)(2 * k),
-                  idesc_f16(128, 64, 1, 1, 0), k > 0);
-        umma_commit(bar_w);
-        mbar_arrive(bar_ready + (c & 1));
-      }
+      if (p == 0) mbar_arrive(bar_ready + buf);
     }
     if (!alive) *reinterpret_cast<volatile int*>(s_abort) = 1;
-  } else {
+  } else if (tid < NPREP + NSTATE) {
     // ================================================================== STATE
     const int s = tid - NPREP;   // 0..127 = TMEM lane = value column j
     const int wq = s >> 5;       // warps 8..11 -> lane groups 0..3
@@ -872,52 +755,39 @@ __global__ void __launch_bounds__(NT, 1)
     const bool lead = s == 0;
     float* hT = a.hT;
     bool alive = true;
-    if (lead && nchunks > 0) {
-      mbar_arrive_expect_tx(bar_v, TILE_BYTES);
-      tma_load_2d(sm + S_V, &mv, bar_v, 0, (int)u.row0);
-      tma_load_2d(sm + S_V + 8192, &mv, bar_v, 64, (int)u.row0);
-    }
     const float* gc_all = reinterpret_cast<const float*>(sm + S_GC);
     // H^T as the fp16 A operand (TMEM) and, in TMEM, H^T Diag(gamma_C) of
     // the chunk about to start (column i times gC[i])
     auto convert_and_scale = [&](int c_next, bool from_h0) {
       const float* gC = gc_all + 128 * (c_next & 1);
 #pragma unroll 1
-      for (int i0 = 0; i0 < 128; i0 += 32) {
-        float f[32];
+      for (int i0 = 0; i0 < 128; i0 += 16) {
+        float f[16];
         if (from_h0) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
+          for (int e = 0; e < 16; ++e)
             f[e] = a.h0 ? a.h0[u.sidx + (size_t)(i0 + e) * 128 + s] : 0.f;
         } else {
-          uint32_t v[32];
-          tmem_ld32<32>(tmem + lb + T_H + i0, v);
+          uint32_t v[16];
+          tmem_ld32<16>(tmem + lb + T_H + i0, v);
           tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(v[e]);
+          for (int e = 0; e < 16; ++e) f[e] = __uint_as_float(v[e]);
         }
-        uint32_t h[16];
-        float mx = 0.f;
+        uint32_t h[8];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          h[e] = pack_half2(f[2 * e], f[2 * e + 1]);
-          mx = fmaxf(mx, fmaxf(fabsf(f[2 * e]), fabsf(f[2 * e + 1])));
-        }
-        ovf |= !(mx <= 65504.f);
-        tmem_st32<16>(tmem + lb + T_HA + (i0 >> 1), h);
+        for (int e = 0; e < 8; ++e) h[e] = pack_half2(f[2 * e], f[2 * e + 1]);
+        tmem_st32<8>(tmem + lb + T_HA + (i0 >> 1), h);
         uint32_t o[16];
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-#pragma unroll
-          for (int e = 0; e < 16; e += 4) {
-            const float4 g4 = *reinterpret_cast<const float4*>(gC + i0 + 16 * hh + e);
-            o[e] = __float_as_uint(f[16 * hh + e] * g4.x);
-            o[e + 1] = __float_as_uint(f[16 * hh + e + 1] * g4.y);
-            o[e + 2] = __float_as_uint(f[16 * hh + e + 2] * g4.z);
-            o[e + 3] = __float_as_uint(f[16 * hh + e + 3] * g4.w);
-          }
-          tmem_st32<16>(tmem + lb + T_H + i0 + 16 * hh, o);
+        for (int e = 0; e < 16; e += 4) {
+          const float4 g4 = *reinterpret_cast<const float4*>(gC + i0 + e);
+          o[e] = __float_as_uint(f[e] * g4.x);
+          o[e + 1] = __float_as_uint(f[e + 1] * g4.y);
+          o[e + 2] = __float_as_uint(f[e + 2] * g4.z);
+          o[e + 3] = __float_as_uint(f[e + 3] * g4.w);
         }
+        tmem_st32<16>(tmem + lb + T_H + i0, o);
       }
       tmem_st_wait();
     };
@@ -932,106 +802,53 @@ __global__ void __launch_bounds__(NT, 1)
     tc_fence_before();
     named_sync(BAR_STATE, NSTATE);
 
-    const uint64_t d_v = mnmajor_desc(sb + S_V, 64, 0), d_tb = kmajor_desc(sb + S_TB, 64, 0);
-    const uint64_t d_w = mnmajor_desc(sb + S_W, 128, 0), d_qg = kmajor_desc(sb + S_QG, 64, 0);
-    const uint64_t d_kh = mnmajor_desc(sb + S_KH, 64, 0), d_aq = kmajor_desc(sb + S_AQ, 64, 0);
     __nv_bfloat16* go = static_cast<__nv_bfloat16*>(a.o);
+    float fin = 0.f;  // becomes NaN once any output is inf or NaN
     for (int c = 0; c < nchunks && alive; ++c) {
       const int lenc = min(C, u.len - c * C);
-      {  // prep operands of chunk c, its W^T in TMEM, and its v tile
+      {  // prep operands of chunk c in shared memory, U~ (and O = 0) in [U | O]
         bool ok = mbar_wait(bar_ready + (c & 1), (uint32_t)((c >> 1) & 1));
-        if (ok) ok = mbar_wait(bar_w, c & 1);
-        if (ok) ok = mbar_wait(bar_v, c & 1);
+        if (ok) ok = mbar_wait(bar_done + ST_W, (uint32_t)(c & 1));
         if (!named_and(BAR_STATE, NSTATE, ok)) { alive = false; break; }
         tc_fence_after();
       }
-      {  // -W^T as fp16 [i][t] (MN-major B of the U-MMA): lane = i
-        float mx = 0.f;
-#pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          uint32_t v[32];
-          tmem_ld32<32>(tmem + lb + T_G1 + 32 * h2, v);
-          tmem_ld_wait();
-#pragma unroll
-          for (int z = 0; z < 32; z += 8) {
-            float f[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              f[e] = -__uint_as_float(v[z + e]);
-              mx = fmaxf(mx, fabsf(f[e]));
-            }
-            store16(sm + S_W + sw128_chunk(128, s, (32 * h2 + z) >> 3), pack_half8(f));
-          }
-        }
-        ovf |= !(mx <= 65504.f);
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      named_sync(BAR_STATE, NSTATE);
       if (lead) {
-        tc_fence_after();
-        // U^T = V^T TB^T - H^T W^T
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          umma_ss(tmem + T_U, d_v + (uint64_t)(128 * k), d_tb + (uint64_t)(2 * k),
-                  idesc_f16(128, 64, 1, 1, 0), k > 0);
+        // [U^T | O^T] += H^T [-W^T | (q*gamma)^T]
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-          umma_ts(tmem + T_U, tmem + T_HA + 8 * k, d_w + (uint64_t)(128 * k),
-                  idesc_f16(128, 64, 0, 0, 1), 1);
+          umma_ts(tmem + T_U, tmem + T_HA + 8 * k, mnmajor_desc(sb + S_WQ, 128, k),
+                  idesc_f16(128, 128, 0, 0, 1), 1);
         umma_commit(bar_s1);
-        // O^T = H^T (q*gamma)^T
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          umma_ts(tmem + T_O, tmem + T_HA + 8 * k,
-                  d_qg + (uint64_t)((k >> 2) * 512 + (k & 3) * 2), idesc_f16(128, 64, 0, 0, 0),
-                  k > 0);
       }
       {
         const bool ok = mbar_wait(bar_s1, c & 1);
         if (!named_and(BAR_STATE, NSTATE, ok)) { alive = false; break; }
         tc_fence_after();
       }
-      if (lead) {
-        if (c + 1 < nchunks) {  // the v tile is free: fetch the next one
-          mbar_arrive_expect_tx(bar_v, TILE_BYTES);
-          tma_load_2d(sm + S_V, &mv, bar_v, 0, (int)(u.row0 + (long)(c + 1) * C));
-          tma_load_2d(sm + S_V + 8192, &mv, bar_v, 64, (int)(u.row0 + (long)(c + 1) * C));
-        }
-      }
       // U^T -> fp16 A operand in TMEM
       {
         uint32_t v[32];
-        float mx = 0.f;
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2) {
           tmem_ld32<32>(tmem + lb + T_U + 32 * h2, v);
           tmem_ld_wait();
           uint32_t hh[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const float x0 = __uint_as_float(v[2 * e]), x1 = __uint_as_float(v[2 * e + 1]);
-            hh[e] = pack_half2(x0, x1);
-            mx = fmaxf(mx, fmaxf(fabsf(x0), fabsf(x1)));
-          }
+          for (int e = 0; e < 16; ++e)
+            hh[e] = pack_half2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
           tmem_st32<16>(tmem + lb + T_UA + 16 * h2, hh);
         }
-        ovf |= !(mx <= 65504.f);
         tmem_st_wait();
       }
       tc_fence_before();
       named_sync(BAR_STATE, NSTATE);
       if (lead) {
         tc_fence_after();
-        // H^T += U^T (k*rho);  O^T += U^T A^T
+        // [O^T | H^T] += U^T [A ; (k*rho)^T]
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          umma_ts(tmem + T_H, tmem + T_UA + 8 * k, d_kh + (uint64_t)(128 * k),
-                  idesc_f16(128, 128, 0, 0, 1), 1);
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          umma_ts(tmem + T_O, tmem + T_UA + 8 * k, d_aq + (uint64_t)(2 * k),
-                  idesc_f16(128, 64, 0, 0, 0), 1);
+          umma_ts(tmem + T_O, tmem + T_UA + 8 * k, kmajor_desc(sb + S_AK, 192, k),
+                  idesc_f16(128, 192, 0, 0, 0), 1);
         umma_commit(bar_s3);
       }
       {
@@ -1039,7 +856,7 @@ __global__ void __launch_bounds__(NT, 1)
         if (!named_and(BAR_STATE, NSTATE, ok)) { alive = false; break; }
         tc_fence_after();
       }
-      // outputs o[t][j] = scale * O^T[j][t]
+      // outputs o[t][j] = O^T[j][t]
       {
         const long rbase = u.row0 + (long)c * C;
 #pragma unroll
@@ -1050,11 +867,17 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             const int t = 32 * h2 + e;
-            if (t < lenc)
-              go[(size_t)(rbase + t) * 128 + s] = __float2bfloat16_rn(a.scale * __uint_as_float(v[e]));
+            const float x = __uint_as_float(v[e]);
+            if (t < lenc) {
+              go[(size_t)(rbase + t) * 128 + s] = __float2bfloat16_rn(x);
+              fin = fmaf(x, 0.f, fin);
+            }
           }
         }
       }
+      tc_fence_before();
+      named_sync(BAR_STATE, NSTATE);
+      if (lead) mbar_arrive(bar_ofree);   // [U | O] may take the next U~
       if (c + 1 < nchunks) {
         const bool ok = mbar_wait(bar_gc + ((c + 1) & 1), (uint32_t)(((c + 1) >> 1) & 1));
         if (!named_and(BAR_STATE, NSTATE, ok)) { alive = false; break; }
@@ -1069,10 +892,84 @@ __global__ void __launch_bounds__(NT, 1)
         tmem_ld32<32>(tmem + lb + T_H + i0, v);
         tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < 32; ++e) hT[u.sidx + (size_t)(i0 + e) * 128 + s] = __uint_as_float(v[e]);
+        for (int e = 0; e < 32; ++e) {
+          const float x = __uint_as_float(v[e]);
+          hT[u.sidx + (size_t)(i0 + e) * 128 + s] = x;
+          fin = fmaf(x, 0.f, fin);
+        }
       }
     }
+    ovf = !(fin == 0.f);
     if (!alive) *reinterpret_cast<volatile int*>(s_abort) = 1;
+  } else if (warp == MMA_WARP) {
+    // ============================================================ MMA ISSUE
+    bool alive = true;
+    if (lane == 0) {
+      const uint32_t id64 = idesc_f16(128, 64, 0, 0, 0);
+      for (int c = 0; c < nchunks && alive; ++c) {
+        const uint32_t ph = (uint32_t)(c & 1);
+        auto wait_ops = [&](int st) -> bool {
+          if (!mbar_wait(bar_ops + st, ph)) return false;
+          tc_fence_after();
+          return true;
+        };
+        // Gram round: D (128 x 64) = X (128 rows) Y^T (64 rows), K = 128
+        auto gram = [&](uint32_t d_col, uint32_t xbuf, uint32_t ybuf) {
+          const uint64_t d_gx = kmajor_desc(sb + xbuf, 128, 0), d_gy = kmajor_desc(sb + ybuf, 64, 0);
+#pragma unroll
+          for (int k = 0; k < 8; ++k)  // K steps: 32 bytes in a panel, panels R*128 apart
+            umma_ss(tmem + d_col, d_gx + (uint64_t)((k >> 2) * 1024 + (k & 3) * 2),
+                    d_gy + (uint64_t)((k >> 2) * 512 + (k & 3) * 2), id64, k > 0);
+        };
+        if (!wait_ops(ST_R1)) { alive = false; break; }
+        gram(T_G0, S_GX2, S_GY2);
+        umma_commit(bar_done + ST_R1);
+        if (!wait_ops(ST_R2)) { alive = false; break; }
+        gram(T_G1, S_GX, S_GY);
+        umma_commit(bar_done + ST_R2);
+        if (!wait_ops(ST_R3)) { alive = false; break; }
+        gram(T_G0, S_GX2, S_GY2);
+        umma_commit(bar_done + ST_R3);
+        // E = D N (rows 0..63 of G1)
+        if (!wait_ops(ST_E)) { alive = false; break; }
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          umma_ss(tmem + T_G1, kmajor_desc(sb + S_TD, 128, k), mnmajor_desc(sb + S_TN, 64, k),
+                  idesc_f16(128, 64, 0, 0, 1), k > 0);
+        umma_commit(bar_done + ST_E);
+        // [E ; I - E] x [E | D]: E^2 in G0 rows 0..63, F = (I - E) D in G1 rows 64..127
+        if (!wait_ops(ST_X)) { alive = false; break; }
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          umma_ss(tmem + T_G0, kmajor_desc(sb + S_TE, 128, k), mnmajor_desc(sb + S_TE, 128, k),
+                  idesc_f16(128, 128, 0, 0, 1), k > 0);
+        umma_commit(bar_done + ST_X);
+        // T = F + E^2 F in G1 rows 64..127 (A rows 64..127 = E^2, B = F)
+        if (!wait_ops(ST_T)) { alive = false; break; }
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          umma_ss(tmem + T_G1, kmajor_desc(sb + S_TE, 128, k), mnmajor_desc(sb + S_TE, 64, k),
+                  idesc_f16(128, 64, 0, 0, 1), 1);
+        umma_commit(bar_done + ST_T);
+        // W^T = (k*gamma)^T TB^T in G1 (lane = i); then [U~^T | 0] = V^T [TB ; 0]^T
+        // into [U | O] once the state has read O of the previous chunk
+        if (!wait_ops(ST_W)) { alive = false; break; }
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          umma_ss(tmem + T_G1, mnmajor_desc(sb + S_KG, 64, k), kmajor_desc(sb + S_TB, 64, k),
+                  idesc_f16(128, 64, 1, 1, 0), k > 0);
+        if (c > 0 && !mbar_wait(bar_ofree, (uint32_t)((c - 1) & 1))) { alive = false; break; }
+        if (!mbar_wait(bar_v, ph)) { alive = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          umma_ss(tmem + T_U, mnmajor_desc(sb + S_V, 64, k), kmajor_desc(sb + S_TB, 128, k),
+                  idesc_f16(128, 128, 1, 1, 0), k > 0);
+        umma_commit(bar_done + ST_W);
+      }
+      if (!alive) *reinterpret_cast<volatile int*>(s_abort) = 1;
+    }
+    __syncwarp();
   }
 
   // ---------------------------------------------------------------- teardown
@@ -1083,15 +980,12 @@ __global__ void __launch_bounds__(NT, 1)
     if (*reinterpret_cast<volatile int*>(s_abort)) {
       set_status(a.status, CKDA_ERR_TIMEOUT);
       // let any MMA or copy still in flight land before the memory is released
-      for (int i = 0; i < 3; ++i) mbar_wait(bar_r + i, 0, 1u << 16);
-      mbar_wait(bar_t, 0, 1u << 16);
-      mbar_wait(bar_w, 0, 1u << 16);
-      mbar_wait(bar_s1, 0, 1u << 16);
-      mbar_wait(bar_s3, 0, 1u << 16);
-      mbar_wait(bar_v, 0, 1u << 16);
-      mbar_wait(bar_qka, 0, 1u << 16);
+      for (int i = 0; i < ST_COUNT; ++i) mbar_wait(bar_done + i, 0, 1u << 12, 1000u);
+      mbar_wait(bar_s1, 0, 1u << 12, 1000u);
+      mbar_wait(bar_s3, 0, 1u << 12, 1000u);
+      mbar_wait(bar_v, 0, 1u << 12, 1000u);
+      mbar_wait(bar_qka, 0, 1u << 12, 1000u);
     }
-    (void)s_abort;
   }
   __syncthreads();
   tc_fence_after();

@@ -31,22 +31,39 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
       "r"(bytes)
       : "memory");
 }
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+// One poll: true once the phase with the given parity has completed.  A
+// thread whose phase is still open sleeps in hardware until it completes or
+// about hint_ns nanoseconds pass, so a waiting warp takes no issue slots
+// from the warps that are working.
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity,
+                                              uint32_t hint_ns) {
   uint32_t ok;
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
       " selp.u32 %0, 1, 0, p;\n}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
       : "memory");
   return ok != 0;
 }
-// Waits for the phase with the given parity to complete.  Gives up after
-// `limit` polls (each try_wait itself suspends for a while) and returns false.
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Waits for the phase with the given parity to complete.  Gives up and
+// returns false after `limit` polls (each sleeping up to hint_ns) or after
+// about one second, whichever comes first.
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
-                                          uint32_t limit = (1u << 24)) {
-  for (uint32_t i = 0; i < limit; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
+                                          uint32_t limit = (1u << 24),
+                                          uint32_t hint_ns = 1000000u) {
+  if (mbar_try_wait(bar, parity, hint_ns)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1; i < limit; ++i) {
+    if (mbar_try_wait(bar, parity, hint_ns)) return true;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  }
   return false;
 }
 
@@ -174,6 +191,13 @@ __device__ __forceinline__ void tmem_ld_wait() {
 template <int N>
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[N]);
 
+template <>
+__device__ __forceinline__ void tmem_st32<8>(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+      : "memory");
+}
 template <>
 __device__ __forceinline__ void tmem_st32<16>(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(
