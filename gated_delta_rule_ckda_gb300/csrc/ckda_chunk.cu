@@ -45,7 +45,7 @@
 // (or the final state); a non-finite o or final state is reported as
 // CKDA_ERR_RANGE.
 //
-// Warp roles (416 threads):
+// Warp roles (512 threads):
 //   warps 0-7  PREP: per chunk, gate products, gated Grams, T, W and the
 //              operands of the state step.  For the elementwise work thread
 //              (blk, panel, lane) owns channels 64 panel + 2 lane, +1 of the
@@ -56,7 +56,8 @@
 //   warps 8-11 STATE: the serial state step on TMEM (thread = TMEM lane = j);
 //              thread 0 issues its MMAs.
 //   warp 12    MMA: one thread issues every tensor-core step of the prep
-//              role, so that no prep warp stalls on an issue.
+//              role, so that no prep warp stalls on an issue, and every copy
+//              into shared memory; warps 13-15 only lend their registers.
 // Handoffs are mbarriers (MMA and TMA completion, operand hand-over) and
 // named barriers within a role.  Every wait is bounded.
 #include "ckda_internal.cuh"
@@ -71,8 +72,16 @@ namespace {
 constexpr int C = 64;
 constexpr int NPREP = 256;
 constexpr int NSTATE = 128;
-constexpr int NT = NPREP + NSTATE + 32;
+// A fourth warpgroup holds the MMA warp; its other three warps only give
+// their registers to the prep warpgroups (setmaxnreg).
+constexpr int NT = NPREP + NSTATE + 128;
 constexpr int MMA_WARP = (NPREP + NSTATE) / 32;
+// Registers per thread: 128 at launch (65536 / 512); the prep warpgroups
+// raise theirs to 144 and the fourth warpgroup lowers its to 96, which adds up
+// to the launch's 512 x 128 exactly (the state warpgroup keeps 128).
+constexpr int kRegsLaunch = 128, kRegsPrep = 144, kRegsAux = 96;
+static_assert(NPREP * (kRegsPrep - kRegsLaunch) <= 128 * (kRegsLaunch - kRegsAux),
+              "register split exceeds what the fourth warpgroup gives up");
 constexpr int BAR_PREP = 1;   // named barrier ids
 constexpr int BAR_STATE = 2;
 
@@ -135,6 +144,7 @@ enum Bar : int {
   B_READY,                     // [2] prep -> state: chunk operands in place
   B_GC = B_READY + 2,          // [2] prep -> state: gamma_C published
   B_OFREE = B_GC + 2,          // state -> MMA warp: O read out, [U | O] free
+  B_BETA,                      // MMA warp -> prep: a chunk's beta is in shared memory
   B_COUNT
 };
 static_assert(B_COUNT * 8 <= 192, "mbarrier area");
@@ -350,9 +360,14 @@ __device__ __forceinline__ void store_transposed(uint8_t* tile, const __half2 (&
 // beta_t scaled) and A (fp16).  Lane x of a level: rows 0..31 are k-rows,
 // 32..63 q-rows of upper rank x & 31; its valid columns are the L sources of
 // its own segment, columns [sg*L, sg*L + L) of the level's 32.
-template <int L>
+// A entries of a level <= 8 read out before the A tile is free (the state's
+// previous [O|H] MMA may still be reading it): up to 8 fp16 values.
+struct AHold {
+  uint32_t h[4];
+};
+template <int L, bool kDefer = false>
 __device__ __forceinline__ void extract_level(uint8_t* sm, uint32_t taddr, int xr,
-                                              const float* beta, uint8_t* AQ) {
+                                              const float* beta, uint8_t* AQ, AHold* hold = nullptr) {
   const bool qrow = xr >= 32;
   const int jr = xr & 31;
   const int sg = jr / L;
@@ -371,7 +386,10 @@ __device__ __forceinline__ void extract_level(uint8_t* sm, uint32_t taddr, int x
       for (int c = 0; c < L; ++c) g[c] = __uint_as_float(v[sgc * L + c]);
     }
   }
-  if (qrow) {
+  if (qrow && kDefer) {
+#pragma unroll
+    for (int c = 0; c < L; c += 2) hold->h[c / 2] = pack_half2(g[c], c + 1 < L ? g[c + 1] : 0.f);
+  } else if (qrow) {
     if (L == 1) {
       *reinterpret_cast<__half*>(AQ + sw128_off(64, t, s0)) = __float2half_rn(g[0]);
     } else if (L < 8) {
@@ -415,15 +433,40 @@ __device__ __forceinline__ void extract_level(uint8_t* sm, uint32_t taddr, int x
   }
 }
 
-template <int La>
+template <int La, bool kDefer = false>
 __device__ __forceinline__ void extract_round(uint8_t* sm, uint32_t tmem, uint32_t col, int wq,
-                                              int lane, const float* beta, uint8_t* AQ) {
+                                              int lane, const float* beta, uint8_t* AQ,
+                                              AHold* hold = nullptr) {
   const int x = 32 * wq + lane;  // warp-uniform level: lanes 0..63 level La, 64..127 La/2
   const uint32_t base = tmem + ((uint32_t)(32 * wq) << 16) + col;
   if (x < 64)
-    extract_level<La>(sm, base, x & 63, beta, AQ);
+    extract_level<La, kDefer>(sm, base, x & 63, beta, AQ, hold);
   else
-    extract_level<La / 2>(sm, base + 32, x & 63, beta, AQ);
+    extract_level<La / 2, kDefer>(sm, base + 32, x & 63, beta, AQ, hold);
+}
+// Writes the A entries a deferred read-out of levels La (lanes 0..63) and
+// La / 2 (lanes 64..127) held back.
+template <int L>
+__device__ __forceinline__ void store_held_level(uint8_t* AQ, int xr, const AHold& hold) {
+  if (xr < 32) return;
+  const int jr = xr & 31, sg = jr / L;
+  const int t = sg * 2 * L + L + (jr % L), s0 = sg * 2 * L;
+  if (L == 8)
+    store16(AQ + sw128_off(64, t, s0), make_uint4(hold.h[0], hold.h[1], hold.h[2], hold.h[3]));
+  else if (L == 4)
+    *reinterpret_cast<uint2*>(AQ + sw128_off(64, t, s0)) = make_uint2(hold.h[0], hold.h[1]);
+  else if (L == 2)
+    *reinterpret_cast<uint32_t*>(AQ + sw128_off(64, t, s0)) = hold.h[0];
+  else
+    *reinterpret_cast<uint16_t*>(AQ + sw128_off(64, t, s0)) = (uint16_t)(hold.h[0] & 0xffffu);
+}
+template <int La>
+__device__ __forceinline__ void store_held(uint8_t* AQ, int wq, int lane, const AHold& hold) {
+  const int x = 32 * wq + lane;
+  if (x < 64)
+    store_held_level<La>(AQ, x & 63, hold);
+  else
+    store_held_level<La / 2>(AQ, x & 63, hold);
 }
 
 // D (tmem) (+)= A (tmem) x B (smem), issued by a single thread.
@@ -436,26 +479,48 @@ __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64
       : "memory");
 }
 
-// Inverses of the four unit-lower 16 x 16 diagonal blocks of I + M, by
-// right-looking substitution (one column per thread), written as fp16 into
-// the diagonal blocks of D.  Threads 0..63.
+// Inverses of the four unit-lower 16 x 16 diagonal blocks of I + M, one
+// column per thread by left-looking substitution: x_c = 1 and, for t > c,
+// x_t = -sum_{s<t} M[t][s] x_s (x_s = 0 for s < c), each row of the block
+// read once as float4s; written as fp16 into the diagonal blocks of D.
+// Threads 0..63.
+__device__ __forceinline__ float f4c(const float4& v, int i) {
+  return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+}
+// Rows are taken four at a time: the four dot products with the earlier
+// rows' x are independent, then a 4 x 4 triangular step finishes the block.
 __device__ __forceinline__ void invert_diag_blocks(uint8_t* sm, int p) {
   const int blk = p >> 4, c = p & 15, o = 16 * blk;
   const float* Md = reinterpret_cast<const float*>(sm + S_MD) + blk * kMdBlk;
   float x[16];
 #pragma unroll
-  for (int t = 0; t < 16; ++t) x[t] = (t == c) ? 1.f : 0.f;
+  for (int ib = 0; ib < 4; ++ib) {
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-  for (int s = 0; s < 15; ++s) {
+    for (int q4 = 0; q4 < ib; ++q4) {
 #pragma unroll
-    for (int t = s + 1; t < 16; ++t) x[t] = fmaf(-Md[t * kMdRow + s], x[s], x[t]);
+      for (int r = 0; r < 4; ++r) {
+        const float4 m = *reinterpret_cast<const float4*>(Md + (4 * ib + r) * kMdRow + 4 * q4);
+        acc[r] = fmaf(m.w, x[4 * q4 + 3],
+                      fmaf(m.z, x[4 * q4 + 2], fmaf(m.y, x[4 * q4 + 1], fmaf(m.x, x[4 * q4], acc[r]))));
+      }
+    }
+    float4 mr[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) mr[r] = *reinterpret_cast<const float4*>(Md + (4 * ib + r) * kMdRow + 4 * ib);
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int t = 4 * ib + r;
+      float a = acc[r];
+#pragma unroll
+      for (int r2 = 0; r2 < r; ++r2) a = fmaf(f4c(mr[r], r2), x[4 * ib + r2], a);
+      x[t] = t < c ? 0.f : (t == c ? 1.f : -a);
+    }
   }
 #pragma unroll
   for (int t = 0; t < 16; ++t)
     *reinterpret_cast<__half*>(sm + S_TD + sw128_off(64, o + t, o + c)) = __float2half_rn(x[t]);
 }
-
-
 
 __global__ void __launch_bounds__(NT, 1)
     fwd_chunk_kernel(const __grid_constant__ FwdArgs a, const __grid_constant__ CUtensorMap mq,
@@ -475,6 +540,7 @@ __global__ void __launch_bounds__(NT, 1)
   uint64_t* bar_ready = bars + B_READY;
   uint64_t* bar_gc = bars + B_GC;
   uint64_t* bar_ofree = bars + B_OFREE;
+  uint64_t* bar_beta = bars + B_BETA;
   int* s_abort = reinterpret_cast<int*>(sm + S_BAR + 192);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + S_BAR + 200);
 
@@ -508,41 +574,21 @@ __global__ void __launch_bounds__(NT, 1)
   const uint32_t tmem = *tmem_slot;
   const uint32_t sb = smem_u32(sm);
   bool ovf = false;
+  if (warp < NPREP / 32) setmaxnreg_inc<kRegsPrep>();
+  else if (warp >= MMA_WARP) setmaxnreg_dec<kRegsAux>();
 
   if (tid < NPREP) {
     // =================================================================== PREP
+    // Iteration c (from -1) finishes chunk c -- E^2, F, T, T Diag(beta), W --
+    // and, in the MMA latencies of those steps, starts chunk c+1: its loads,
+    // gate products and Gram operands, then its Gram rounds, D and E = D N.
     const int p = tid;
     const int w = p >> 5;
     const int blk = w >> 1, panel = w & 1;     // elementwise mapping
     const int wq = w & 3, half = w >> 2;       // TMEM lane quarter, column half
     const int trow = 32 * wq + lane;           // this thread's TMEM lane
     const uint32_t tl = (uint32_t)(32 * wq) << 16;
-    const __nv_bfloat16* gb = static_cast<const __nv_bfloat16*>(a.beta);
-    const bool beta_lane = panel == 0 && lane < 16;
-    const int bt = 16 * blk + lane;            // token whose beta this lane fetches
     bool alive = true;
-    float beta_next = 0.f;
-    if (beta_lane && nchunks > 0 && bt < min(C, u.len)) beta_next = __bfloat162float(gb[u.row0 + bt]);
-    auto issue_qka = [&](int cc) {
-      const int y = (int)(u.row0 + (long)cc * C);
-      mbar_arrive_expect_tx(bar_qka, 3 * TILE_BYTES);
-      tma_load_2d(sm + S_TQ, &mq, bar_qka, 0, y);
-      tma_load_2d(sm + S_TQ + 8192, &mq, bar_qka, 64, y);
-      tma_load_2d(sm + S_TK, &mk, bar_qka, 0, y);
-      tma_load_2d(sm + S_TK + 8192, &mk, bar_qka, 64, y);
-      tma_load_2d(sm + S_TA, &ma, bar_qka, 0, y);
-      tma_load_2d(sm + S_TA + 8192, &ma, bar_qka, 64, y);
-    };
-    auto issue_v = [&](int cc) {
-      const int y = (int)(u.row0 + (long)cc * C);
-      mbar_arrive_expect_tx(bar_v, TILE_BYTES);
-      tma_load_2d(sm + S_V, &mv, bar_v, 0, y);
-      tma_load_2d(sm + S_V + 8192, &mv, bar_v, 64, y);
-    };
-    if (p == 0 && nchunks > 0) {
-      issue_qka(0);
-      issue_v(0);
-    }
     // waits for a completion of chunk cc on `bar` (one phase per chunk); the
     // AND over the role decides, uniformly, whether to go on
     auto prep_wait = [&](uint64_t* bar, int cc) -> bool {
@@ -551,147 +597,83 @@ __global__ void __launch_bounds__(NT, 1)
       tc_fence_after();
       return all;
     };
-    // hands the operands written so far to the tensor-core step `st`
-    auto handoff = [&](int st) {
+    // makes every operand written so far visible to the tensor cores
+    auto publish = [&]() {
       fence_proxy_async_smem();
       tc_fence_before();
       named_sync(BAR_PREP, NPREP);
-      if (p == 0) mbar_arrive(bar_ops + st);
     };
     uint8_t* AQ = sm + S_AK;
     float* dg = reinterpret_cast<float*>(sm + S_DIAG);
     float2* totv = reinterpret_cast<float2*>(sm + S_TOT);
-    for (int c = 0; c < nchunks && alive; ++c) {
-      const int lenc = min(C, u.len - c * C);
-      const int buf = c & 1;
-      const long rbase = u.row0 + (long)c * C;
-      // beta: this chunk's values were fetched one chunk ahead
-      float* beta_s = reinterpret_cast<float*>(sm + S_BETA) + 64 * buf;
-      if (beta_lane) {
-        beta_s[bt] = beta_next;
-        beta_next = 0.f;
-        if (c + 1 < nchunks && bt < min(C, u.len - (c + 1) * C))
-          beta_next = __bfloat162float(gb[rbase + C + bt]);
-      }
-      // ---- this chunk's q, k, alpha tiles
-      if (!prep_wait(bar_qka, c)) { alive = false; break; }
-      Blk B;
-      if (lenc == C) load_block<false>(B, sm, blk, panel, lane, a.scale, C);
-      else load_block<true>(B, sm, blk, panel, lane, a.scale, lenc - 16 * blk);
-      {
+    Blk B;
+    for (int c = -1; c < nchunks && alive; ++c) {
+      const int cn = c + 1;                    // the chunk this iteration starts
+      const bool nx = cn < nchunks, tail = c >= 0;
+      const int lenn = nx ? min(C, u.len - cn * C) : 0;
+      float* beta_c = reinterpret_cast<float*>(sm + S_BETA) + 64 * (c & 1);
+      float* beta_n = reinterpret_cast<float*>(sm + S_BETA) + 64 * (cn & 1);
+      // ---- chunk cn: q, k, alpha (the MMA warp fetches the tiles and beta)
+      if (nx) {
+        if (!prep_wait(bar_qka, cn)) { alive = false; break; }
+        if (lenn == C) load_block<false>(B, sm, blk, panel, lane, a.scale, C);
+        else load_block<true>(B, sm, blk, panel, lane, a.scale, lenn - 16 * blk);
         const float sq = warp_sum16(B.dqk, lane);   // q.k over this panel's 64 channels
         if ((lane & 1) == 0) dg[64 * panel + 16 * blk + (lane >> 1)] = sq;
+        totv[64 * blk + 32 * panel + lane] = B.tot;
       }
-      totv[64 * blk + 32 * panel + lane] = B.tot;
-      // every tile read is done (the tile region becomes Gram buffer 2) and
-      // every block total is visible
-      named_sync(BAR_PREP, NPREP);
-      float2 T4[4];
+      // ---- chunk c: E -> [E ; I - E] (rows t of two tiles): lanes 0..63
+      if (tail) {
+        if (!prep_wait(bar_done + ST_E, c)) { alive = false; break; }
+        if (wq < 2) {
+          uint32_t v[32];
+          tmem_ld32<32>(tmem + tl + T_G1 + 32 * half, v);
+          tmem_ld_wait();
 #pragma unroll
-      for (int b = 0; b < 4; ++b) T4[b] = totv[64 * b + 32 * panel + lane];
-      float2 gbf = make_float2(1.f, 1.f), gaf = make_float2(1.f, 1.f);
+          for (int z = 0; z < 32; z += 8) {
+            float f[8], g[8];
 #pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        if (b < blk) { gbf.x *= T4[b].x; gbf.y *= T4[b].y; }
-        if (b > blk) { gaf.x *= T4[b].x; gaf.y *= T4[b].y; }
-      }
-      const __half2 Gb = __float22half2_rn(gbf), Ga = __float22half2_rn(gaf);
-      const __half2 t1 = __float22half2_rn(T4[1]), t2 = __float22half2_rn(T4[2]);
-      // gamma_C (fp32: it scales the fp32 state)
-      float* gC = reinterpret_cast<float*>(sm + S_GC) + 128 * buf;
-      if (blk == 0)
-        reinterpret_cast<float2*>(gC)[32 * panel + lane] =
-            make_float2(T4[0].x * T4[1].x * T4[2].x * T4[3].x, T4[0].y * T4[1].y * T4[2].y * T4[3].y);
-      // ---- Gram round 1: levels 8 and 4 (pairs inside 16-token blocks)
-      write_level_in<8, S_GX2, S_GY2, 0, 0>(sm, B, blk, panel, lane);
-      write_level_in<4, S_GX2, S_GY2, 64, 32>(sm, B, blk, panel, lane);
-      handoff(ST_R1);
-      if (p == 0) mbar_arrive(bar_gc + buf);
-      // ---- round 2: levels 2 and 1 (buffer 1 held the previous chunk's
-      // inverse tiles, all read before its T step completed)
-      write_level_in<2, S_GX, S_GY, 0, 0>(sm, B, blk, panel, lane);
-      write_level_in<1, S_GX, S_GY, 64, 32>(sm, B, blk, panel, lane);
-      handoff(ST_R2);
-      // ---- gamma_t = (earlier blocks' totals) x prefix_t, a running product;
-      // k*gamma (bf16, A of the W^T step; the previous W^T step is done)
-      __half2 gq[16];
-      {
-        __half2 g = Gb;
-#pragma unroll
-        for (int r = 0; r < 16; ++r) {
-          g = __hmul2(g, B.a[r]);
-          const float2 kg = __half22float2(__hmul2(B.k[r], g));
-          *reinterpret_cast<uint32_t*>(sm + S_KG + pair_at(pair_tb<64>(panel, lane), 16 * blk, r)) =
-              pack_bf162(kg.x, kg.y);
-          gq[r] = __hmul2(B.q[r], g);
-        }
-      }
-      // ---- (q*gamma)^T next to -W^T: the previous chunk's [U | O] MMA read them
-      if (!prep_wait(bar_s1, c - 1)) { alive = false; break; }
-      store_transposed(sm + S_WQ + 16384, gq, blk, panel, lane);
-      // ---- (k*rho)^T under A, rho_s = exclusive suffix x later blocks' totals:
-      // the previous chunk's [O | H] MMA read them (and A, which the Gram
-      // read-out below overwrites)
-      {
-        __half2 rr = Ga;
-#pragma unroll
-        for (int r = 15; r >= 0; --r) {
-          if (r < 15) rr = __hmul2(rr, B.a[r + 1]);
-          gq[r] = __hmul2(B.k[r], rr);
-        }
-      }
-      if (!prep_wait(bar_s3, c - 1)) { alive = false; break; }
-      store_transposed(sm + S_AK + 8192, gq, blk, panel, lane);
-      // ---- round 3 (levels 32 and 16) goes into buffer 2 once round 1 is done
-      if (!prep_wait(bar_done + ST_R1, c)) { alive = false; break; }
-      if (half == 0) extract_round<8>(sm, tmem, T_G0, wq, lane, beta_s, AQ);
-      switch (blk) {
-        case 0: write_cross<0, S_GX2, S_GY2>(sm, B, t1, t2, panel, lane); break;
-        case 1: write_cross<1, S_GX2, S_GY2>(sm, B, t1, t2, panel, lane); break;
-        case 2: write_cross<2, S_GX2, S_GY2>(sm, B, t1, t2, panel, lane); break;
-        default: write_cross<3, S_GX2, S_GY2>(sm, B, t1, t2, panel, lane); break;
-      }
-      handoff(ST_R3);
-      if (!prep_wait(bar_done + ST_R2, c)) { alive = false; break; }
-      if (half == 1) extract_round<2>(sm, tmem, T_G1, wq, lane, beta_s, AQ);
-      // D lives where Gram X was: clear it (its diagonal blocks come next)
-      for (int e = p; e < 8192 / 16; e += NPREP) store16(sm + S_TD + 16 * e, make_uint4(0, 0, 0, 0));
-      tc_fence_before();
-      named_sync(BAR_PREP, NPREP);
-      // ---- T = (I + M)^-1: D is formed while round 3 runs
-      if (p < 64) invert_diag_blocks(sm, p);
-      if (!prep_wait(bar_done + ST_R3, c)) { alive = false; break; }
-      // the tile region is free: fetch the next chunk's q, k, alpha
-      if (p == 0 && c + 1 < nchunks) issue_qka(c + 1);
-      if (half == 0) extract_round<32>(sm, tmem, T_G0, wq, lane, beta_s, AQ);
-      else if (p >= 128 && p < 192) {
-        const int t = p - 128;
-        *reinterpret_cast<__half*>(AQ + sw128_off(64, t, t)) = __float2half_rn(dg[t] + dg[64 + t]);
-      }
-      handoff(ST_E);                                             // E = D N
-      // ---- E -> [E ; I - E] (rows t of two tiles): lanes 0..63
-      if (!prep_wait(bar_done + ST_E, c)) { alive = false; break; }
-      if (wq < 2) {
-        uint32_t v[32];
-        tmem_ld32<32>(tmem + tl + T_G1 + 32 * half, v);
-        tmem_ld_wait();
-#pragma unroll
-        for (int z = 0; z < 32; z += 8) {
-          float f[8], g[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            f[e] = __uint_as_float(v[z + e]);
-            g[e] = ((32 * half + z + e) == trow ? 1.f : 0.f) - f[e];
+            for (int e = 0; e < 8; ++e) {
+              f[e] = __uint_as_float(v[z + e]);
+              g[e] = ((32 * half + z + e) == trow ? 1.f : 0.f) - f[e];
+            }
+            const uint32_t ch = (uint32_t)(32 * half + z) >> 3;
+            store16(sm + S_TE + sw128_chunk(64, trow, ch), pack_half8(f));
+            store16(sm + S_TIE + sw128_chunk(64, trow, ch), pack_half8(g));
           }
-          const uint32_t ch = (uint32_t)(32 * half + z) >> 3;
-          store16(sm + S_TE + sw128_chunk(64, trow, ch), pack_half8(f));
-          store16(sm + S_TIE + sw128_chunk(64, trow, ch), pack_half8(g));
         }
       }
-      handoff(ST_X);                                             // [E^2 | F]
-      // ---- E^2 (G0, lanes 0..63) under F (G1, lanes 64..127)
-      if (!prep_wait(bar_done + ST_X, c)) { alive = false; break; }
-      {
+      // (also: chunk cn's tile reads are done -- the tile region becomes Gram
+      // buffer 2 -- and its block totals are visible)
+      publish();
+      if (tail && p == 0) mbar_arrive(bar_ops + ST_X);           // [E^2 | F]
+      __half2 Gb, Ga, t1, t2;
+      if (nx) {
+        float2 T4[4];
+#pragma unroll
+        for (int b = 0; b < 4; ++b) T4[b] = totv[64 * b + 32 * panel + lane];
+        float2 gbf = make_float2(1.f, 1.f), gaf = make_float2(1.f, 1.f);
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          if (b < blk) { gbf.x *= T4[b].x; gbf.y *= T4[b].y; }
+          if (b > blk) { gaf.x *= T4[b].x; gaf.y *= T4[b].y; }
+        }
+        Gb = __float22half2_rn(gbf);
+        Ga = __float22half2_rn(gaf);
+        t1 = __float22half2_rn(T4[1]);
+        t2 = __float22half2_rn(T4[2]);
+        // gamma_C (fp32: it scales the fp32 state)
+        float* gC = reinterpret_cast<float*>(sm + S_GC) + 128 * (cn & 1);
+        if (blk == 0)
+          reinterpret_cast<float2*>(gC)[32 * panel + lane] = make_float2(
+              T4[0].x * T4[1].x * T4[2].x * T4[3].x, T4[0].y * T4[1].y * T4[2].y * T4[3].y);
+        // Gram round 1 of chunk cn: levels 8 and 4 (pairs inside 16-token blocks)
+        write_level_in<8, S_GX2, S_GY2, 0, 0>(sm, B, blk, panel, lane);
+        write_level_in<4, S_GX2, S_GY2, 64, 32>(sm, B, blk, panel, lane);
+      }
+      // ---- chunk c: E^2 (G0, lanes 0..63) under F (G1, lanes 64..127)
+      if (tail) {
+        if (!prep_wait(bar_done + ST_X, c)) { alive = false; break; }
         const bool e2 = wq < 2;
         const int r = e2 ? trow : trow - 64;
         uint32_t v[32];
@@ -706,30 +688,45 @@ __global__ void __launch_bounds__(NT, 1)
           store16(dst + sw128_chunk(64, r, (uint32_t)(32 * half + z) >> 3), pack_half8(f));
         }
       }
-      handoff(ST_T);                                             // T = F + E^2 F
-      // ---- T Diag(beta) as bf16: T is in G1, lanes 64..127
-      if (!prep_wait(bar_done + ST_T, c)) { alive = false; break; }
-      if (wq >= 2) {
-        const int r = trow - 64;
-        uint32_t v[32];
-        tmem_ld32<32>(tmem + tl + T_G1 + 32 * half, v);
-        tmem_ld_wait();
-#pragma unroll
-        for (int z = 0; z < 32; z += 8) {
-          float f[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int s = 32 * half + z + e;
-            f[e] = s <= r ? __uint_as_float(v[z + e]) * beta_s[s] : 0.f;
-          }
-          store16(sm + S_TB + sw128_chunk(64, r, (uint32_t)(32 * half + z) >> 3), pack_bf8(f));
+      publish();
+      if (p == 0) {
+        if (tail) mbar_arrive(bar_ops + ST_T);                   // T = F + E^2 F
+        if (nx) {
+          mbar_arrive(bar_ops + ST_R1);                          // round 1 of chunk cn (G0 is free)
+          mbar_arrive(bar_gc + (cn & 1));
         }
       }
-      handoff(ST_W);                                             // W^T, and U~ into [U | O]
-      // ---- -W^T (fp16, panel 0 of [-W^T | (q*gamma)^T]): W^T is in G1, lane = i
-      if (!prep_wait(bar_done + ST_W, c)) { alive = false; break; }
-      if (p == 0 && c + 1 < nchunks) issue_v(c + 1);   // U~ has read the v tile
-      {
+      // ---- chunk c: T Diag(beta) as bf16 (T is in G1, lanes 64..127); then
+      // round 2 of chunk cn into buffer 1, whose inverse tiles T has read
+      if (tail) {
+        if (!prep_wait(bar_done + ST_T, c)) { alive = false; break; }
+        if (wq >= 2) {
+          const int r = trow - 64;
+          uint32_t v[32];
+          tmem_ld32<32>(tmem + tl + T_G1 + 32 * half, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int z = 0; z < 32; z += 8) {
+            float f[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const int s = 32 * half + z + e;
+              f[e] = s <= r ? __uint_as_float(v[z + e]) * beta_c[s] : 0.f;
+            }
+            store16(sm + S_TB + sw128_chunk(64, r, (uint32_t)(32 * half + z) >> 3), pack_bf8(f));
+          }
+        }
+      }
+      if (nx) {
+        write_level_in<2, S_GX, S_GY, 0, 0>(sm, B, blk, panel, lane);
+        write_level_in<1, S_GX, S_GY, 64, 32>(sm, B, blk, panel, lane);
+      }
+      publish();
+      if (tail && p == 0) mbar_arrive(bar_ops + ST_W);           // W^T, and U~ into [U | O]
+      // ---- chunk c: -W^T (fp16, panel 0 of [-W^T | (q*gamma)^T]; W^T is in
+      // G1, lane = i); then chunk c is ready for the state step
+      if (tail) {
+        if (!prep_wait(bar_done + ST_W, c)) { alive = false; break; }
         uint32_t v[32];
         tmem_ld32<32>(tmem + tl + T_G1 + 32 * half, v);
         tmem_ld_wait();
@@ -741,10 +738,78 @@ __global__ void __launch_bounds__(NT, 1)
           store16(sm + S_WQ + sw128_chunk(64, trow, (uint32_t)(32 * half + z) >> 3), pack_half8(f));
         }
       }
-      fence_proxy_async_smem();
+      publish();
+      if (p == 0) {
+        if (tail) mbar_arrive(bar_ready + (c & 1));
+        if (nx) mbar_arrive(bar_ops + ST_R2);                    // round 2 of chunk cn (G1 is free)
+      }
+      if (!nx) break;
+      // =============== the rest of chunk cn: its k*gamma, (q*gamma)^T,
+      // (k*rho)^T, the Gram read-outs, D and E = D N
+      // gamma_t = (earlier blocks' totals) x prefix_t, a running product;
+      // k*gamma (bf16, A of the W^T step; chunk c's W^T step is done)
+      __half2 gq[16];
+      {
+        __half2 g = Gb;
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+          g = __hmul2(g, B.a[r]);
+          const float2 kg = __half22float2(__hmul2(B.k[r], g));
+          *reinterpret_cast<uint32_t*>(sm + S_KG + pair_at(pair_tb<64>(panel, lane), 16 * blk, r)) =
+              pack_bf162(kg.x, kg.y);
+          gq[r] = __hmul2(B.q[r], g);
+        }
+      }
+      // round 3 (levels 32 and 16) goes into buffer 2 once round 1 is done; the
+      // A entries of round 1 wait for the state to release the A tile
+      {  // round 1 done; chunk cn's beta (first used by the read-out) in place
+        bool ok = mbar_wait(bar_done + ST_R1, (uint32_t)(cn & 1));
+        if (ok) ok = mbar_wait(bar_beta, (uint32_t)(cn & 1));
+        if (!named_and(BAR_PREP, NPREP, ok)) { alive = false; break; }
+        tc_fence_after();
+      }
+      AHold held;
+      if (half == 0) extract_round<8, true>(sm, tmem, T_G0, wq, lane, beta_n, AQ, &held);
+      switch (blk) {
+        case 0: write_cross<0, S_GX2, S_GY2>(sm, B, t1, t2, panel, lane); break;
+        case 1: write_cross<1, S_GX2, S_GY2>(sm, B, t1, t2, panel, lane); break;
+        case 2: write_cross<2, S_GX2, S_GY2>(sm, B, t1, t2, panel, lane); break;
+        default: write_cross<3, S_GX2, S_GY2>(sm, B, t1, t2, panel, lane); break;
+      }
+      publish();
+      if (p == 0) mbar_arrive(bar_ops + ST_R3);
+      // (q*gamma)^T next to -W^T: chunk c's [U | O] MMA has read them
+      if (!prep_wait(bar_s1, c)) { alive = false; break; }
+      store_transposed(sm + S_WQ + 16384, gq, blk, panel, lane);
+      // (k*rho)^T under A, rho_s = exclusive suffix x later blocks' totals:
+      // chunk c's [O | H] MMA has read them and A
+      {
+        __half2 rr = Ga;
+#pragma unroll
+        for (int r = 15; r >= 0; --r) {
+          if (r < 15) rr = __hmul2(rr, B.a[r + 1]);
+          gq[r] = __hmul2(B.k[r], rr);
+        }
+      }
+      if (!prep_wait(bar_s3, c)) { alive = false; break; }
+      store_transposed(sm + S_AK + 8192, gq, blk, panel, lane);
+      if (half == 0) store_held<8>(AQ, wq, lane, held);
+      if (!prep_wait(bar_done + ST_R2, cn)) { alive = false; break; }
+      if (half == 1) extract_round<2>(sm, tmem, T_G1, wq, lane, beta_n, AQ);
+      // D lives in Gram buffer 1: clear it (its diagonal blocks come next)
+      for (int e = p; e < 8192 / 16; e += NPREP) store16(sm + S_TD + 16 * e, make_uint4(0, 0, 0, 0));
       tc_fence_before();
       named_sync(BAR_PREP, NPREP);
-      if (p == 0) mbar_arrive(bar_ready + buf);
+      // T = (I + M)^-1: D is formed while round 3 runs
+      if (p < 64) invert_diag_blocks(sm, p);
+      if (!prep_wait(bar_done + ST_R3, cn)) { alive = false; break; }
+      if (half == 0) extract_round<32>(sm, tmem, T_G0, wq, lane, beta_n, AQ);
+      else if (p >= 128 && p < 192) {
+        const int t = p - 128;
+        *reinterpret_cast<__half*>(AQ + sw128_off(64, t, t)) = __float2half_rn(dg[t] + dg[64 + t]);
+      }
+      publish();
+      if (p == 0) mbar_arrive(bar_ops + ST_E);                   // E = D N
     }
     if (!alive) *reinterpret_cast<volatile int*>(s_abort) = 1;
   } else if (tid < NPREP + NSTATE) {
@@ -903,69 +968,149 @@ __global__ void __launch_bounds__(NT, 1)
     if (!alive) *reinterpret_cast<volatile int*>(s_abort) = 1;
   } else if (warp == MMA_WARP) {
     // ============================================================ MMA ISSUE
+    // Same iteration structure as the prep role: iteration c issues chunk c's
+    // E^2 | F, T and W^T (+ U~) steps and chunk c+1's Gram rounds and E, in
+    // the order the prep role hands their operands over.
+    // The same thread also issues every tile copy: q, k, alpha of chunk
+    // cc + 1 once round 3 of chunk cc (the last reader of the tile region) is
+    // done, v of chunk cc + 1 once U~ of chunk cc is, and L2 prefetches one
+    // chunk further ahead -- a copy instruction can wait for room in the copy
+    // queue, which must not hold up a prep warp.
     bool alive = true;
     if (lane == 0) {
       const uint32_t id64 = idesc_f16(128, 64, 0, 0, 0);
-      for (int c = 0; c < nchunks && alive; ++c) {
-        const uint32_t ph = (uint32_t)(c & 1);
-        auto wait_ops = [&](int st) -> bool {
-          if (!mbar_wait(bar_ops + st, ph)) return false;
-          tc_fence_after();
-          return true;
-        };
-        // Gram round: D (128 x 64) = X (128 rows) Y^T (64 rows), K = 128
-        auto gram = [&](uint32_t d_col, uint32_t xbuf, uint32_t ybuf) {
-          const uint64_t d_gx = kmajor_desc(sb + xbuf, 128, 0), d_gy = kmajor_desc(sb + ybuf, 64, 0);
+      auto issue_qka = [&](int cc) {
+        const int y = (int)(u.row0 + (long)cc * C);
+        mbar_arrive_expect_tx(bar_qka, 3 * TILE_BYTES);
+        tma_load_2d(sm + S_TQ, &mq, bar_qka, 0, y);
+        tma_load_2d(sm + S_TQ + 8192, &mq, bar_qka, 64, y);
+        tma_load_2d(sm + S_TK, &mk, bar_qka, 0, y);
+        tma_load_2d(sm + S_TK + 8192, &mk, bar_qka, 64, y);
+        tma_load_2d(sm + S_TA, &ma, bar_qka, 0, y);
+        tma_load_2d(sm + S_TA + 8192, &ma, bar_qka, 64, y);
+      };
+      auto issue_v = [&](int cc) {
+        const int y = (int)(u.row0 + (long)cc * C);
+        mbar_arrive_expect_tx(bar_v, TILE_BYTES);
+        tma_load_2d(sm + S_V, &mv, bar_v, 0, y);
+        tma_load_2d(sm + S_V + 8192, &mv, bar_v, 64, y);
+      };
+      auto prefetch_l2 = [&](int cc) {
+        const int y = (int)(u.row0 + (long)cc * C);
 #pragma unroll
-          for (int k = 0; k < 8; ++k)  // K steps: 32 bytes in a panel, panels R*128 apart
-            umma_ss(tmem + d_col, d_gx + (uint64_t)((k >> 2) * 1024 + (k & 3) * 2),
-                    d_gy + (uint64_t)((k >> 2) * 512 + (k & 3) * 2), id64, k > 0);
-        };
-        if (!wait_ops(ST_R1)) { alive = false; break; }
-        gram(T_G0, S_GX2, S_GY2);
-        umma_commit(bar_done + ST_R1);
-        if (!wait_ops(ST_R2)) { alive = false; break; }
-        gram(T_G1, S_GX, S_GY);
-        umma_commit(bar_done + ST_R2);
-        if (!wait_ops(ST_R3)) { alive = false; break; }
-        gram(T_G0, S_GX2, S_GY2);
-        umma_commit(bar_done + ST_R3);
-        // E = D N (rows 0..63 of G1)
-        if (!wait_ops(ST_E)) { alive = false; break; }
+        for (int x0 = 0; x0 < 128; x0 += 64) {
+          tma_prefetch_2d_l2(&mq, x0, y);
+          tma_prefetch_2d_l2(&mk, x0, y);
+          tma_prefetch_2d_l2(&ma, x0, y);
+          tma_prefetch_2d_l2(&mv, x0, y);
+        }
+      };
+      // beta of chunk cc into its parity buffer: all loads in flight at once,
+      // then published with a release arrive
+      const __nv_bfloat16* gbeta = static_cast<const __nv_bfloat16*>(a.beta);
+      auto load_beta = [&](int cc) {
+        const int len = min(C, u.len - cc * C);
+        const __nv_bfloat16* src = gbeta + u.row0 + (long)cc * C;
+        float* dst = reinterpret_cast<float*>(sm + S_BETA) + 64 * (cc & 1);
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          umma_ss(tmem + T_G1, kmajor_desc(sb + S_TD, 128, k), mnmajor_desc(sb + S_TN, 64, k),
-                  idesc_f16(128, 64, 0, 0, 1), k > 0);
-        umma_commit(bar_done + ST_E);
-        // [E ; I - E] x [E | D]: E^2 in G0 rows 0..63, F = (I - E) D in G1 rows 64..127
-        if (!wait_ops(ST_X)) { alive = false; break; }
+        for (int t0 = 0; t0 < 64; t0 += 32) {
+          float b[32];
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          umma_ss(tmem + T_G0, kmajor_desc(sb + S_TE, 128, k), mnmajor_desc(sb + S_TE, 128, k),
-                  idesc_f16(128, 128, 0, 0, 1), k > 0);
-        umma_commit(bar_done + ST_X);
-        // T = F + E^2 F in G1 rows 64..127 (A rows 64..127 = E^2, B = F)
-        if (!wait_ops(ST_T)) { alive = false; break; }
+          for (int t = 0; t < 32; ++t) b[t] = t0 + t < len ? __bfloat162float(src[t0 + t]) : 0.f;
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          umma_ss(tmem + T_G1, kmajor_desc(sb + S_TE, 128, k), mnmajor_desc(sb + S_TE, 64, k),
-                  idesc_f16(128, 64, 0, 0, 1), 1);
-        umma_commit(bar_done + ST_T);
-        // W^T = (k*gamma)^T TB^T in G1 (lane = i); then [U~^T | 0] = V^T [TB ; 0]^T
-        // into [U | O] once the state has read O of the previous chunk
-        if (!wait_ops(ST_W)) { alive = false; break; }
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          umma_ss(tmem + T_G1, mnmajor_desc(sb + S_KG, 64, k), kmajor_desc(sb + S_TB, 64, k),
-                  idesc_f16(128, 64, 1, 1, 0), k > 0);
-        if (c > 0 && !mbar_wait(bar_ofree, (uint32_t)((c - 1) & 1))) { alive = false; break; }
-        if (!mbar_wait(bar_v, ph)) { alive = false; break; }
+          for (int t = 0; t < 32; ++t) dst[t0 + t] = b[t];
+        }
+        mbar_arrive(bar_beta);
+      };
+      if (nchunks > 0) {
+        issue_qka(0);
+        issue_v(0);
+        if (nchunks > 1) prefetch_l2(1);
+        load_beta(0);
+      }
+      auto wait_ops = [&](int st, int cc) -> bool {
+        if (!mbar_wait(bar_ops + st, (uint32_t)(cc & 1))) return false;
         tc_fence_after();
+        return true;
+      };
+      // Gram round: D (128 x 64) = X (128 rows) Y^T (64 rows), K = 128
+      auto gram = [&](uint32_t d_col, uint32_t xbuf, uint32_t ybuf) {
+        const uint64_t d_gx = kmajor_desc(sb + xbuf, 128, 0), d_gy = kmajor_desc(sb + ybuf, 64, 0);
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          umma_ss(tmem + T_U, mnmajor_desc(sb + S_V, 64, k), kmajor_desc(sb + S_TB, 128, k),
-                  idesc_f16(128, 128, 1, 1, 0), k > 0);
-        umma_commit(bar_done + ST_W);
+        for (int k = 0; k < 8; ++k)  // K steps: 32 bytes in a panel, panels R*128 apart
+          umma_ss(tmem + d_col, d_gx + (uint64_t)((k >> 2) * 1024 + (k & 3) * 2),
+                  d_gy + (uint64_t)((k >> 2) * 512 + (k & 3) * 2), id64, k > 0);
+      };
+      for (int c = -1; c < nchunks && alive; ++c) {
+        const int cn = c + 1;
+        const bool nx = cn < nchunks, tail = c >= 0;
+        if (tail) {
+          // [E ; I - E] x [E | D]: E^2 in G0 rows 0..63, F = (I - E) D in G1 rows 64..127
+          if (!wait_ops(ST_X, c)) { alive = false; break; }
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            umma_ss(tmem + T_G0, kmajor_desc(sb + S_TE, 128, k), mnmajor_desc(sb + S_TE, 128, k),
+                    idesc_f16(128, 128, 0, 0, 1), k > 0);
+          umma_commit(bar_done + ST_X);
+          // T = F + E^2 F in G1 rows 64..127 (A rows 64..127 = E^2, B = F)
+          if (!wait_ops(ST_T, c)) { alive = false; break; }
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            umma_ss(tmem + T_G1, kmajor_desc(sb + S_TE, 128, k), mnmajor_desc(sb + S_TE, 64, k),
+                    idesc_f16(128, 64, 0, 0, 1), 1);
+          umma_commit(bar_done + ST_T);
+        }
+        if (nx) {
+          if (!wait_ops(ST_R1, cn)) { alive = false; break; }
+          gram(T_G0, S_GX2, S_GY2);
+          umma_commit(bar_done + ST_R1);
+        }
+        if (tail) {
+          // W^T = (k*gamma)^T TB^T in G1 (lane = i); then [U~^T | 0] = V^T [TB ; 0]^T
+          // into [U | O] once the state has read O of the previous chunk
+          if (!wait_ops(ST_W, c)) { alive = false; break; }
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            umma_ss(tmem + T_G1, mnmajor_desc(sb + S_KG, 64, k), kmajor_desc(sb + S_TB, 64, k),
+                    idesc_f16(128, 64, 1, 1, 0), k > 0);
+          if (c > 0 && !mbar_wait(bar_ofree, (uint32_t)((c - 1) & 1))) { alive = false; break; }
+          if (!mbar_wait(bar_v, (uint32_t)(c & 1))) { alive = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            umma_ss(tmem + T_U, mnmajor_desc(sb + S_V, 64, k), kmajor_desc(sb + S_TB, 128, k),
+                    idesc_f16(128, 128, 1, 1, 0), k > 0);
+          umma_commit(bar_done + ST_W);
+          // U~ was the last reader of the v tile
+          if (nx) {
+            if (!mbar_wait(bar_done + ST_W, (uint32_t)(c & 1))) { alive = false; break; }
+            issue_v(cn);
+          }
+        }
+        if (nx) {
+          if (!wait_ops(ST_R2, cn)) { alive = false; break; }
+          gram(T_G1, S_GX, S_GY);
+          umma_commit(bar_done + ST_R2);
+          if (!wait_ops(ST_R3, cn)) { alive = false; break; }
+          gram(T_G0, S_GX2, S_GY2);
+          umma_commit(bar_done + ST_R3);
+          // round 3 was the last reader of the tile region: fetch chunk cn+1's
+          // q, k, alpha now, a whole chunk of work ahead of their use
+          if (cn + 1 < nchunks) {
+            if (!mbar_wait(bar_done + ST_R3, (uint32_t)(cn & 1))) { alive = false; break; }
+            issue_qka(cn + 1);
+            if (cn + 2 < nchunks) prefetch_l2(cn + 2);
+          }
+          // E = D N (rows 0..63 of G1)
+          if (!wait_ops(ST_E, cn)) { alive = false; break; }
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            umma_ss(tmem + T_G1, kmajor_desc(sb + S_TD, 128, k), mnmajor_desc(sb + S_TN, 64, k),
+                    idesc_f16(128, 64, 0, 0, 1), k > 0);
+          umma_commit(bar_done + ST_E);
+          // chunk cn+1's beta buffer was last read by chunk cn-1's T Diag(beta)
+          if (cn + 1 < nchunks) load_beta(cn + 1);
+        }
       }
       if (!alive) *reinterpret_cast<volatile int*>(s_abort) = 1;
     }

@@ -92,6 +92,13 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
       : "memory");
 }
+// Prefetches a box of a tiled tensor into L2 (no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_2d_l2(const CUtensorMap* map, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
+}
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -238,6 +245,18 @@ __device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile, uint32_t R, int k
 //   the k-th 16-row K step starts 2048 bytes further.
 __device__ __forceinline__ uint64_t mnmajor_desc(uint32_t tile, uint32_t R, int kstep) {
   return sw128_desc(tile + (uint32_t)kstep * 2048u, R * 128u, 1024u);
+}
+
+// ----------------------------------------------------- register split
+// Executed by all threads of a warpgroup: raises / lowers the registers each
+// of its threads holds (the block's total stays what it was launched with).
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 // ------------------------------------------- named barriers and handoffs
