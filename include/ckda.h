@@ -51,7 +51,8 @@ typedef enum {
     CKDA_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed */
     CKDA_ERR_TIMEOUT = 4,      /* device: a bounded wait ran out (see ckda_fwd_status) */
     CKDA_ERR_WORKSPACE = 5,    /* workspace missing or smaller than required */
-    CKDA_ERR_RANGE = 6         /* device: an fp16 tensor-core operand overflowed */
+    CKDA_ERR_RANGE = 6         /* device: an fp16 tensor-core operand overflowed, seen as a
+                                  non-finite o or final state (also non-finite inputs) */
 } ckda_status;
 
 /* Version of this ABI: major * 10000 + minor * 100 + patch. */
@@ -167,7 +168,8 @@ ckda_status ckda_decode_step(const void *q, const void *k, const void *v,
 
 /*
  * Self-test of the bounded-wait path: launches one block that waits on a
- * barrier nothing will complete, with a limit of about `spin_limit` polls,
+ * barrier nothing will complete, with a limit of `spin_limit` polls (each
+ * sleeping up to about a microsecond, the whole wait at most about a second),
  * after which it records CKDA_ERR_TIMEOUT in the workspace's status word and
  * returns.  It never hangs and never faults.  Read the result with
  * ckda_fwd_status().
