@@ -800,15 +800,23 @@ __global__ void __launch_bounds__(NT, 1)
       for (int e = p; e < 8192 / 16; e += NPREP) store16(sm + S_TD + 16 * e, make_uint4(0, 0, 0, 0));
       tc_fence_before();
       named_sync(BAR_PREP, NPREP);
-      // T = (I + M)^-1: D is formed while round 3 runs
-      if (p < 64) invert_diag_blocks(sm, p);
-      if (!prep_wait(bar_done + ST_R3, cn)) { alive = false; break; }
-      if (half == 0) extract_round<32>(sm, tmem, T_G0, wq, lane, beta_n, AQ);
-      else if (p >= 128 && p < 192) {
-        const int t = p - 128;
+      // T = (I + M)^-1: warps 0-1 invert D's diagonal blocks while warps 2-5
+      // (one per TMEM lane quarter) read round 3 out and warps 6-7 add up A's
+      // diagonal
+      bool ok = true;
+      if (w < 2) {
+        invert_diag_blocks(sm, p);
+      } else if (w < 6) {
+        ok = mbar_wait(bar_done + ST_R3, (uint32_t)(cn & 1));
+        tc_fence_after();
+        if (ok) extract_round<32>(sm, tmem, T_G0, wq, lane, beta_n, AQ);
+      } else {
+        const int t = p - 192;
         *reinterpret_cast<__half*>(AQ + sw128_off(64, t, t)) = __float2half_rn(dg[t] + dg[64 + t]);
       }
-      publish();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      if (!named_and(BAR_PREP, NPREP, ok)) { alive = false; break; }
       if (p == 0) mbar_arrive(bar_ops + ST_E);                   // E = D N
     }
     if (!alive) *reinterpret_cast<volatile int*>(s_abort) = 1;
