@@ -138,13 +138,12 @@ enum Bar : int {
   B_QKA = 0,                   // q, k, alpha tiles (TMA)
   B_V,                         // v tile (TMA)
   B_OPS,                       // [ST_COUNT]
-  B_DONE = B_OPS + ST_COUNT,   // [ST_COUNT]; B_DONE + ST_W also covers U~
+  B_DONE = B_OPS + ST_COUNT,   // [ST_COUNT]
   B_S1 = B_DONE + ST_COUNT,    // state: [U | O] MMA done
   B_S3,                        // state: [O | H] MMA done
   B_READY,                     // [2] prep -> state: chunk operands in place
   B_GC = B_READY + 2,          // [2] prep -> state: gamma_C published
-  B_OFREE = B_GC + 2,          // state -> MMA warp: O read out, [U | O] free
-  B_BETA,                      // MMA warp -> prep: a chunk's beta is in shared memory
+  B_BETA = B_GC + 2,           // MMA warp -> prep: a chunk's beta is in shared memory
   B_COUNT
 };
 static_assert(B_COUNT * 8 <= 192, "mbarrier area");
@@ -539,7 +538,6 @@ __global__ void __launch_bounds__(NT, 1)
   uint64_t* bar_s3 = bars + B_S3;
   uint64_t* bar_ready = bars + B_READY;
   uint64_t* bar_gc = bars + B_GC;
-  uint64_t* bar_ofree = bars + B_OFREE;
   uint64_t* bar_beta = bars + B_BETA;
   int* s_abort = reinterpret_cast<int*>(sm + S_BAR + 192);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + S_BAR + 200);
@@ -722,7 +720,7 @@ __global__ void __launch_bounds__(NT, 1)
         write_level_in<1, S_GX, S_GY, 64, 32>(sm, B, blk, panel, lane);
       }
       publish();
-      if (tail && p == 0) mbar_arrive(bar_ops + ST_W);           // W^T, and U~ into [U | O]
+      if (tail && p == 0) mbar_arrive(bar_ops + ST_W);           // W^T
       // ---- chunk c: -W^T (fp16, panel 0 of [-W^T | (q*gamma)^T]; W^T is in
       // G1, lane = i); then chunk c is ready for the state step
       if (tail) {
@@ -879,14 +877,18 @@ __global__ void __launch_bounds__(NT, 1)
     float fin = 0.f;  // becomes NaN once any output is inf or NaN
     for (int c = 0; c < nchunks && alive; ++c) {
       const int lenc = min(C, u.len - c * C);
-      {  // prep operands of chunk c in shared memory, U~ (and O = 0) in [U | O]
+      {  // prep operands of chunk c in shared memory, and its v tile
         bool ok = mbar_wait(bar_ready + (c & 1), (uint32_t)((c >> 1) & 1));
-        if (ok) ok = mbar_wait(bar_done + ST_W, (uint32_t)(c & 1));
+        if (ok) ok = mbar_wait(bar_v, (uint32_t)(c & 1));
         if (!named_and(BAR_STATE, NSTATE, ok)) { alive = false; break; }
         tc_fence_after();
       }
       if (lead) {
-        // [U^T | O^T] += H^T [-W^T | (q*gamma)^T]
+        // [U~^T | 0] = V^T [TB ; 0]^T, then [U^T | O^T] += H^T [-W^T | (q*gamma)^T]
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          umma_ss(tmem + T_U, mnmajor_desc(sb + S_V, 64, k), kmajor_desc(sb + S_TB, 128, k),
+                  idesc_f16(128, 128, 1, 1, 0), k > 0);
 #pragma unroll
         for (int k = 0; k < 8; ++k)
           umma_ts(tmem + T_U, tmem + T_HA + 8 * k, mnmajor_desc(sb + S_WQ, 128, k),
@@ -897,6 +899,12 @@ __global__ void __launch_bounds__(NT, 1)
         const bool ok = mbar_wait(bar_s1, c & 1);
         if (!named_and(BAR_STATE, NSTATE, ok)) { alive = false; break; }
         tc_fence_after();
+      }
+      if (lead && c + 1 < nchunks) {  // the v tile is free: fetch the next one
+        const int y = (int)(u.row0 + (long)(c + 1) * C);
+        mbar_arrive_expect_tx(bar_v, TILE_BYTES);
+        tma_load_2d(sm + S_V, &mv, bar_v, 0, y);
+        tma_load_2d(sm + S_V + 8192, &mv, bar_v, 64, y);
       }
       // U^T -> fp16 A operand in TMEM
       {
@@ -950,7 +958,6 @@ __global__ void __launch_bounds__(NT, 1)
       }
       tc_fence_before();
       named_sync(BAR_STATE, NSTATE);
-      if (lead) mbar_arrive(bar_ofree);   // [U | O] may take the next U~
       if (c + 1 < nchunks) {
         const bool ok = mbar_wait(bar_gc + ((c + 1) & 1), (uint32_t)(((c + 1) >> 1) & 1));
         if (!named_and(BAR_STATE, NSTATE, ok)) { alive = false; break; }
@@ -977,13 +984,13 @@ __global__ void __launch_bounds__(NT, 1)
   } else if (warp == MMA_WARP) {
     // ============================================================ MMA ISSUE
     // Same iteration structure as the prep role: iteration c issues chunk c's
-    // E^2 | F, T and W^T (+ U~) steps and chunk c+1's Gram rounds and E, in
-    // the order the prep role hands their operands over.
-    // The same thread also issues every tile copy: q, k, alpha of chunk
-    // cc + 1 once round 3 of chunk cc (the last reader of the tile region) is
-    // done, v of chunk cc + 1 once U~ of chunk cc is, and L2 prefetches one
-    // chunk further ahead -- a copy instruction can wait for room in the copy
-    // queue, which must not hold up a prep warp.
+    // E^2 | F, T and W^T steps and chunk c+1's Gram rounds and E, in the
+    // order the prep role hands their operands over.
+    // The same thread also issues the q, k, alpha copies (chunk cc + 1 once
+    // round 3 of chunk cc, the last reader of the tile region, is done), L2
+    // prefetches one chunk further ahead, and beta -- a copy instruction can
+    // wait for room in the copy queue, which must not hold up a prep warp.
+    // (The state warps fetch each next v tile themselves.)
     bool alive = true;
     if (lane == 0) {
       const uint32_t id64 = idesc_f16(128, 64, 0, 0, 0);
@@ -1074,26 +1081,13 @@ __global__ void __launch_bounds__(NT, 1)
           umma_commit(bar_done + ST_R1);
         }
         if (tail) {
-          // W^T = (k*gamma)^T TB^T in G1 (lane = i); then [U~^T | 0] = V^T [TB ; 0]^T
-          // into [U | O] once the state has read O of the previous chunk
+          // W^T = (k*gamma)^T TB^T in G1 (lane = i)
           if (!wait_ops(ST_W, c)) { alive = false; break; }
 #pragma unroll
           for (int k = 0; k < 4; ++k)
             umma_ss(tmem + T_G1, mnmajor_desc(sb + S_KG, 64, k), kmajor_desc(sb + S_TB, 64, k),
                     idesc_f16(128, 64, 1, 1, 0), k > 0);
-          if (c > 0 && !mbar_wait(bar_ofree, (uint32_t)((c - 1) & 1))) { alive = false; break; }
-          if (!mbar_wait(bar_v, (uint32_t)(c & 1))) { alive = false; break; }
-          tc_fence_after();
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            umma_ss(tmem + T_U, mnmajor_desc(sb + S_V, 64, k), kmajor_desc(sb + S_TB, 128, k),
-                    idesc_f16(128, 128, 1, 1, 0), k > 0);
           umma_commit(bar_done + ST_W);
-          // U~ was the last reader of the v tile
-          if (nx) {
-            if (!mbar_wait(bar_done + ST_W, (uint32_t)(c & 1))) { alive = false; break; }
-            issue_v(cn);
-          }
         }
         if (nx) {
           if (!wait_ops(ST_R2, cn)) { alive = false; break; }
