@@ -243,25 +243,20 @@ def roofline(nbytes, per_ms, kernel, workload):
 
 
 def e2e_fwd(ck, x, steps, ws, stream):
-    """Host (pinned) inputs -> device, ckda_fwd, outputs -> host, all timed."""
+    """Host (pinned) inputs -> ckda_fwd_host -> host outputs, the whole call
+    timed: it copies each slice of tokens in, computes it and copies its o
+    out, the copies of one slice overlapping the computation of another."""
     import torch
     B, H, T, dk = x.q.shape
     dv = x.v.shape[-1]
-    N = x.num_seqs
     hq, hk, hv, ha, hb = (t.pin_memory() for t in (x.q, x.k, x.v, x.alpha, x.beta))
-    dq, dk_, dv_, da, db = (torch.empty_like(t, device="cuda") for t in (hq, hk, hv, ha, hb))
-    o = torch.empty_like(dv_)
-    hT = torch.empty((N, H, dk, dv), dtype=torch.float32, device="cuda")
-    ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
-    hh = torch.empty(hT.shape, dtype=torch.float32).pin_memory()
-    wsp = ck.new_workspace(0, H, torch.device("cuda"))
+    ho = torch.empty((B, H, T, dv), dtype=x.q.dtype).pin_memory()
+    hh = torch.empty((B, H, dk, dv), dtype=torch.float32).pin_memory()
+    scratch = torch.empty(ck.host_scratch_bytes(B, H, T, dk, dv, x.q.dtype), dtype=torch.uint8,
+                          device="cuda")
 
     def step():
-        for dst, src in ((dq, hq), (dk_, hk), (dv_, hv), (da, ha), (db, hb)):
-            dst.copy_(src, non_blocking=True)
-        ck.fwd(dq, dk_, dv_, da, db, None, o=o, hT=hT, workspace=wsp, stream=stream)
-        ho.copy_(o, non_blocking=True)
-        hh.copy_(hT, non_blocking=True)
+        ck.fwd_host(hq, hk, hv, ha, hb, None, o=ho, hT=hh, scratch=scratch, stream=stream)
 
     total, _ = time_steps(step, steps, 2, ws, stream)
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, ha, hb))

@@ -20,8 +20,8 @@ import threading
 
 import torch
 
-__all__ = ["fwd", "decode_step", "fwd_status", "workspace_bytes", "selftest_timeout",
-           "lib", "library_path", "CkdaError", "STATUS"]
+__all__ = ["fwd", "fwd_host", "decode_step", "fwd_status", "workspace_bytes",
+           "host_scratch_bytes", "selftest_timeout", "lib", "library_path", "CkdaError", "STATUS"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libckda.so")
@@ -71,6 +71,11 @@ def lib():
                                            i32, i32, i32, i32, i32, f32, vp]
             L.ckda_selftest_timeout.restype = i32
             L.ckda_selftest_timeout.argtypes = [vp, sz, ctypes.c_uint, vp]
+            L.ckda_fwd_host_scratch_bytes.restype = sz
+            L.ckda_fwd_host_scratch_bytes.argtypes = [i32, i32, i32, i32, i32, i32, i32]
+            L.ckda_fwd_host.restype = i32
+            L.ckda_fwd_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
+                                        i32, f32, i32, vp, sz, vp]
             _lib = L
     return _lib
 
@@ -156,6 +161,50 @@ def fwd(q, k, v, alpha, beta, h0=None, cu_seqlens=None, scale=1.0, chunk_size=0,
 def fwd_status(workspace, stream=None) -> int:
     """Device status of the most recent call on `workspace` (synchronises)."""
     return int(lib().ckda_fwd_status(_ptr(workspace), _stream_handle(stream, workspace.device)))
+
+
+def host_scratch_bytes(B, H, T, dk, dv, dtype=torch.bfloat16, slice_tokens=0) -> int:
+    io = _BF16 if dtype == torch.bfloat16 else _F32
+    return int(lib().ckda_fwd_host_scratch_bytes(B, H, T, dk, dv, io, int(slice_tokens)))
+
+
+def fwd_host(q, k, v, alpha, beta, h0=None, scale=1.0, slice_tokens=0, o=None, hT=None,
+             store_final_state=True, scratch=None, stream=None, device=None):
+    """ckda_fwd_host: the dense forward with every tensor in host memory (CPU
+    tensors; pinned memory copies at full speed).  The copies of one slice of
+    tokens overlap the computation of another.  Returns (o, hT or None) as CPU
+    tensors; they are complete once `stream` is (this call does not wait)."""
+    L = lib()
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    dt = q.dtype
+    io = _io_dtype(q)
+    cpu = torch.device("cpu")
+    for name, t, shp in (("q", q, (B, H, T, dk)), ("k", k, (B, H, T, dk)),
+                         ("alpha", alpha, (B, H, T, dk)), ("v", v, (B, H, T, dv)),
+                         ("beta", beta, (B, H, T))):
+        _check(t, name, dt, shp, cpu)
+    if h0 is not None:
+        _check(h0, "h0", torch.float32, (B, H, dk, dv), cpu)
+    if o is None:
+        o = torch.empty((B, H, T, dv), dtype=dt).pin_memory()
+    else:
+        _check(o, "o", dt, (B, H, T, dv), cpu)
+    if store_final_state and hT is None:
+        hT = torch.empty((B, H, dk, dv), dtype=torch.float32).pin_memory()
+    if hT is not None:
+        _check(hT, "hT", torch.float32, (B, H, dk, dv), cpu)
+    need = host_scratch_bytes(B, H, T, dk, dv, dt, slice_tokens)
+    if scratch is None:
+        scratch = torch.empty(need, dtype=torch.uint8, device=device)
+    rc = L.ckda_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(h0), _ptr(o),
+                         _ptr(hT), B, H, T, dk, dv, io, float(scale), int(slice_tokens),
+                         _ptr(scratch), int(scratch.numel()), _stream_handle(stream, device))
+    if rc != 0:
+        raise CkdaError(rc, "ckda_fwd_host")
+    fwd_host.last_scratch = scratch
+    return o, hT
 
 
 def decode_step(q, k, v, alpha, beta, state, scale=1.0, o=None, stream=None):

@@ -140,6 +140,40 @@ ckda_status ckda_fwd_noalloc(const void *q, const void *k, const void *v,
                              float scale, int chunk_size, void *stream);
 
 /*
+ * Forward over HOST buffers: the operation of ckda_fwd for the dense layout,
+ * with every tensor argument in host memory (page-locked memory gives full
+ * copy bandwidth; pageable memory works, slower).  Same layouts and dtypes
+ * as ckda_fwd: q, k, alpha [B, H, T, dk]; v, o [B, H, T, dv]; beta
+ * [B, H, T]; h0, hT fp32 [B, H, dk, dv] (h0 == NULL: zero state; hT == NULL:
+ * not stored).  Packed sequences are not accepted here.
+ *
+ * The token axis is processed in slices of `slice_tokens` tokens (a multiple
+ * of 64; 0 picks about T / 4, at least 512): the copy of slice s to the device
+ * overlaps the computation of slice s - 1 and the copy of slice s - 2's o
+ * back, on two internal streams and the caller's `stream`.  Each
+ * (sequence, head) carries its fp32 state between slices in device memory,
+ * and slices end on chunk boundaries, so o and hT equal those of one
+ * ckda_fwd over the whole sequence.
+ *
+ * dev_scratch / dev_scratch_bytes: caller-owned device memory of at least
+ * ckda_fwd_host_scratch_bytes(...) bytes, 256-byte aligned; it holds the
+ * device copies of two slices, the carried state and a status word (read it
+ * with ckda_fwd_status(dev_scratch, stream)).  Calls that share a scratch
+ * must be ordered on their streams.
+ *
+ * Returns CKDA_OK once the work is enqueued on `stream`; o and hT in host
+ * memory are complete when `stream` is.  The internal streams are shared by
+ * the calls of a process on one device (enqueueing is serialised).
+ */
+size_t ckda_fwd_host_scratch_bytes(int B, int H, int T, int dk, int dv, ckda_dtype io_dtype,
+                                   int slice_tokens);
+ckda_status ckda_fwd_host(const void *q, const void *k, const void *v,
+                          const void *alpha, const void *beta, const float *h0,
+                          void *o, float *hT, int B, int H, int T, int dk, int dv,
+                          ckda_dtype io_dtype, float scale, int slice_tokens,
+                          void *dev_scratch, size_t dev_scratch_bytes, void *stream);
+
+/*
  * Reads (and clears) the device status word of a workspace: waits for
  * `stream`, then returns CKDA_OK, CKDA_ERR_TIMEOUT or CKDA_ERR_RANGE for the
  * most recent ckda_fwd (or self-test) enqueued with that workspace.

@@ -97,6 +97,47 @@ def test_decode_argument_errors_are_synchronous(L):
     assert f(io=3) == 1
 
 
+def test_fwd_host_argument_errors_are_synchronous(L):
+    """ckda_fwd_host rejects bad arguments, slices and scratch before any copy."""
+    vp = ctypes.c_void_p
+    B, H, T, d = 2, 3, 200, 128
+    need = L.ckda_fwd_host_scratch_bytes(B, H, T, d, d, 1, 64)
+
+    def f(**kw):
+        return L.ckda_fwd_host(*(vp(kw.get(n, 16)) for n in ("q", "k", "v", "alpha", "beta")),
+                               vp(kw.get("h0")), vp(kw.get("o", 16)), vp(kw.get("hT")),
+                               kw.get("B", B), kw.get("H", H), kw.get("T", T), kw.get("dk", d),
+                               kw.get("dv", d), kw.get("io", 1), kw.get("scale", 1.0),
+                               kw.get("slice", 64), vp(kw.get("ws", 4096)),
+                               kw.get("wsb", need), vp(None))
+    assert f(q=None) == 1
+    assert f(o=None) == 1
+    assert f(B=0) == 1
+    assert f(io=5) == 1
+    assert f(slice=100) == 1                              # not a multiple of 64
+    assert f(slice=-64) == 1
+    assert f(scale=float("nan")) == 1
+    assert f(dk=130) == 2
+    assert f(ws=None) == 5
+    assert f(wsb=need - 1) == 5                           # too small
+    assert f(ws=4096 + 16) == 5                           # misaligned
+
+
+def test_fwd_host_scratch_bytes(L):
+    """Two slice buffers (q, k, alpha, v, beta, o) plus the carried state and
+    the status word; the automatic slice is about T / 4, at least 512."""
+    f = L.ckda_fwd_host_scratch_bytes
+    B, H, d = 2, 3, 128
+    up = lambda x: (x + 255) // 256 * 256
+    for T, sl, ts in ((1000, 64, 64), (1000, 128, 128), (2048, 0, 512), (8192, 0, 2048),
+                      (1000, 0, 512), (100, 0, 128)):
+        rows = B * H * ts
+        buf = 4 * up(rows * d * 2) + up(rows * 2) + up(rows * d * 2)
+        assert f(B, H, T, d, d, 1, sl) == 256 + up(B * H * d * d * 4) + 2 * buf, (T, sl)
+    assert f(B, H, 1000, d, d, 1, 100) == 0
+    assert f(0, H, 1000, d, d, 1, 64) == 0
+
+
 def test_selftest_rejects_missing_workspace(L):
     assert L.ckda_selftest_timeout(None, 0, 10, None) == 5
 
