@@ -46,18 +46,20 @@
 // CKDA_ERR_RANGE.
 //
 // Warp roles (512 threads):
-//   warps 0-7  PREP: per chunk, gate products, gated Grams, T, W and the
-//              operands of the state step.  For the elementwise work thread
-//              (blk, panel, lane) owns channels 64 panel + 2 lane, +1 of the
-//              16 tokens 16 blk .. 16 blk + 15, so every gate product inside
-//              a block is a register chain and every shared-memory access is
-//              a conflict-free 4-byte access at a compile-time swizzle.  Prep
-//              of chunk c+1 runs while the state warps step chunk c.
-//   warps 8-11 STATE: the serial state step on TMEM (thread = TMEM lane = j);
-//              thread 0 issues its MMAs.
-//   warp 12    MMA: one thread issues every tensor-core step of the prep
-//              role, so that no prep warp stalls on an issue, and every copy
-//              into shared memory; warps 13-15 only lend their registers.
+//   warps 0-7   PREP: per chunk, gate products, the gated Grams and their
+//               read-outs, D and the operands of the state step.  For the
+//               elementwise work thread (blk, panel, lane) owns channels
+//               64 panel + 2 lane, +1 of the 16 tokens 16 blk .. 16 blk + 15,
+//               so every gate product inside a block is a register chain and
+//               every shared-memory access is a conflict-free 4-byte access at
+//               a compile-time swizzle.
+//   warps 8-11  STATE: the serial state step on TMEM (thread = TMEM lane = j);
+//               thread 0 issues its MMAs.
+//   warps 12-15 INVERSE CHAIN: once the prep role has handed chunk c's E = D N
+//               over, they finish T and W^T (thread = TMEM lane) while the
+//               prep role starts chunk c+1.  Lane 0 of warp 12 issues every
+//               tensor-core step outside the state role and every copy into
+//               shared memory, so that no prep warp stalls on an issue.
 // Handoffs are mbarriers (MMA and TMA completion, operand hand-over) and
 // named barriers within a role.  Every wait is bounded.
 #include "ckda_internal.cuh"
@@ -72,8 +74,8 @@ namespace {
 constexpr int C = 64;
 constexpr int NPREP = 256;
 constexpr int NSTATE = 128;
-// A fourth warpgroup holds the MMA warp; its other three warps only give
-// their registers to the prep warpgroups (setmaxnreg).
+// A fourth warpgroup finishes each chunk's inverse chain and issues the
+// prep role's tensor-core steps and copies.
 constexpr int NT = NPREP + NSTATE + 128;
 constexpr int MMA_WARP = (NPREP + NSTATE) / 32;
 // Registers per thread: 128 at launch (65536 / 512); the prep warpgroups
@@ -82,8 +84,10 @@ constexpr int MMA_WARP = (NPREP + NSTATE) / 32;
 constexpr int kRegsLaunch = 128, kRegsPrep = 144, kRegsAux = 96;
 static_assert(NPREP * (kRegsPrep - kRegsLaunch) <= 128 * (kRegsLaunch - kRegsAux),
               "register split exceeds what the fourth warpgroup gives up");
+constexpr int NTAIL = 128;    // the fourth warpgroup
 constexpr int BAR_PREP = 1;   // named barrier ids
 constexpr int BAR_STATE = 2;
+constexpr int BAR_TAIL = 3;
 
 // ---- shared memory map (bytes from a 1024-aligned base) ----
 // q, k, alpha tiles; once read they hold the second Gram operand buffer
@@ -97,14 +101,14 @@ constexpr uint32_t S_GX2 = S_TQ;     // second Gram buffer (the tile region)
 constexpr uint32_t S_GY2 = S_TA;
 constexpr uint32_t S_GX = 65536;     // fp16 Gram X   [128 rows][128 i] K-major A
 constexpr uint32_t S_GY = 98304;     // fp16 Gram Y   [64 rows][128 i]  K-major B
-// once round 2 is done, the inverse's 64 x 64 fp16 tiles live in Gram X:
+// once round 3 is done, the inverse's 64 x 64 fp16 tiles E and I - E live
+// in Gram X:
 constexpr uint32_t S_TE = S_GX;            // E, then F = (I - E) D
 constexpr uint32_t S_TIE = S_GX + 8192;    // I - E, then E^2
-constexpr uint32_t S_TD = S_GX + 16384;    // D: inverses of the 16 x 16 diagonal blocks
-constexpr uint32_t S_TB = 114688;    // bf16 T Diag(beta) [64 t][64 s]; rows 64..127 ...
-constexpr uint32_t S_Z = S_TB + 8192;      // ... are this zero tile
+constexpr uint32_t S_TB = 114688;    // bf16 T Diag(beta) [64 t][64 s]
+constexpr uint32_t S_TD = S_TB + 8192;     // fp16 D: inverses of the 16 x 16 diagonal blocks
 constexpr uint32_t S_WQ = 131072;    // fp16 [-W^T | (q*gamma)^T] [128 i][64 t] x 2 panels, MN-major B of [U|O]
-constexpr uint32_t S_AK = 163840;    // fp16 [A ; (k*rho)^T] [64 t + 128 i][64 s]  K-major B of [O|H]
+constexpr uint32_t S_AK = 163840;    // fp16 [A ; (k*rho)^T] [64 t + 128 i][64 s]  K-major B of O, H
 constexpr uint32_t S_KG = 188416;    // bf16 k*gamma  [64 s][128 i]  MN-major A of W^T
 constexpr uint32_t S_TN = 204800;    // fp16 N: block-strictly-lower part of M [64 t][64 s]
 constexpr uint32_t S_MD = 212992;    // fp32 diagonal 16 x 16 blocks of M [4][16][20]
@@ -115,9 +119,11 @@ constexpr uint32_t S_GC = S_SMALL + 512;     // fp32 [2][128] gamma_C
 constexpr uint32_t S_DIAG = S_SMALL + 1536;  // fp32 [2 panels][64] partial q.k
 constexpr uint32_t S_TOT = S_SMALL + 2048;   // fp32 [4 blocks][128] block totals of alpha
 constexpr uint32_t S_BAR = S_SMALL + 4096;   // mbarriers
-constexpr uint32_t SMEM_USED = S_SMALL + 4352;
+constexpr uint32_t S_A2 = 223232;    // fp16 A of odd chunks [64 t][64 s] (even chunks' is S_AK's top)
+constexpr uint32_t SMEM_USED = S_A2 + 8192;
 constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;
 static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
+static_assert(S_A2 >= S_SMALL + 4352 && S_A2 % 1024 == 0, "second A tile");
 
 // ---- tensor memory columns ----
 // [U | O] is the accumulator of the first state MMA and [O | H] of the second
@@ -131,8 +137,8 @@ constexpr uint32_t T_G1 = 416;  //   [E^2 | F] in G0..G1, T in G1, W^T in G1
 constexpr uint32_t TMEM_COLS = 512;
 
 // ---- mbarriers ----
-// prep -> MMA warp "operands ready" and MMA warp -> prep "step done", one
-// pair per tensor-core step of the prep role
+// prep -> issuer "operands ready" (Gram rounds and E) and MMA -> waiters
+// "step done", one pair per tensor-core step outside the state role
 enum Step : int { ST_R1 = 0, ST_R2, ST_R3, ST_E, ST_X, ST_T, ST_W, ST_COUNT };
 enum Bar : int {
   B_QKA = 0,                   // q, k, alpha tiles (TMA)
@@ -141,9 +147,9 @@ enum Bar : int {
   B_DONE = B_OPS + ST_COUNT,   // [ST_COUNT]
   B_S1 = B_DONE + ST_COUNT,    // state: [U | O] MMA done
   B_S3,                        // state: [O | H] MMA done
-  B_READY,                     // [2] prep -> state: chunk operands in place
+  B_READY,                     // [2] prep and warp 12 -> state: chunk operands in place
   B_GC = B_READY + 2,          // [2] prep -> state: gamma_C published
-  B_BETA = B_GC + 2,           // MMA warp -> prep: a chunk's beta is in shared memory
+  B_BETA = B_GC + 2,           // warp 12 -> prep: a chunk's beta is in shared memory (32 arrivals)
   B_COUNT
 };
 static_assert(B_COUNT * 8 <= 192, "mbarrier area");
@@ -359,14 +365,9 @@ __device__ __forceinline__ void store_transposed(uint8_t* tile, const __half2 (&
 // beta_t scaled) and A (fp16).  Lane x of a level: rows 0..31 are k-rows,
 // 32..63 q-rows of upper rank x & 31; its valid columns are the L sources of
 // its own segment, columns [sg*L, sg*L + L) of the level's 32.
-// A entries of a level <= 8 read out before the A tile is free (the state's
-// previous [O|H] MMA may still be reading it): up to 8 fp16 values.
-struct AHold {
-  uint32_t h[4];
-};
-template <int L, bool kDefer = false>
+template <int L>
 __device__ __forceinline__ void extract_level(uint8_t* sm, uint32_t taddr, int xr,
-                                              const float* beta, uint8_t* AQ, AHold* hold = nullptr) {
+                                              const float* beta, uint8_t* AQ) {
   const bool qrow = xr >= 32;
   const int jr = xr & 31;
   const int sg = jr / L;
@@ -385,10 +386,7 @@ __device__ __forceinline__ void extract_level(uint8_t* sm, uint32_t taddr, int x
       for (int c = 0; c < L; ++c) g[c] = __uint_as_float(v[sgc * L + c]);
     }
   }
-  if (qrow && kDefer) {
-#pragma unroll
-    for (int c = 0; c < L; c += 2) hold->h[c / 2] = pack_half2(g[c], c + 1 < L ? g[c + 1] : 0.f);
-  } else if (qrow) {
+  if (qrow) {
     if (L == 1) {
       *reinterpret_cast<__half*>(AQ + sw128_off(64, t, s0)) = __float2half_rn(g[0]);
     } else if (L < 8) {
@@ -432,42 +430,16 @@ __device__ __forceinline__ void extract_level(uint8_t* sm, uint32_t taddr, int x
   }
 }
 
-template <int La, bool kDefer = false>
+template <int La>
 __device__ __forceinline__ void extract_round(uint8_t* sm, uint32_t tmem, uint32_t col, int wq,
-                                              int lane, const float* beta, uint8_t* AQ,
-                                              AHold* hold = nullptr) {
+                                              int lane, const float* beta, uint8_t* AQ) {
   const int x = 32 * wq + lane;  // warp-uniform level: lanes 0..63 level La, 64..127 La/2
   const uint32_t base = tmem + ((uint32_t)(32 * wq) << 16) + col;
   if (x < 64)
-    extract_level<La, kDefer>(sm, base, x & 63, beta, AQ, hold);
+    extract_level<La>(sm, base, x & 63, beta, AQ);
   else
-    extract_level<La / 2, kDefer>(sm, base + 32, x & 63, beta, AQ, hold);
+    extract_level<La / 2>(sm, base + 32, x & 63, beta, AQ);
 }
-// Writes the A entries a deferred read-out of levels La (lanes 0..63) and
-// La / 2 (lanes 64..127) held back.
-template <int L>
-__device__ __forceinline__ void store_held_level(uint8_t* AQ, int xr, const AHold& hold) {
-  if (xr < 32) return;
-  const int jr = xr & 31, sg = jr / L;
-  const int t = sg * 2 * L + L + (jr % L), s0 = sg * 2 * L;
-  if (L == 8)
-    store16(AQ + sw128_off(64, t, s0), make_uint4(hold.h[0], hold.h[1], hold.h[2], hold.h[3]));
-  else if (L == 4)
-    *reinterpret_cast<uint2*>(AQ + sw128_off(64, t, s0)) = make_uint2(hold.h[0], hold.h[1]);
-  else if (L == 2)
-    *reinterpret_cast<uint32_t*>(AQ + sw128_off(64, t, s0)) = hold.h[0];
-  else
-    *reinterpret_cast<uint16_t*>(AQ + sw128_off(64, t, s0)) = (uint16_t)(hold.h[0] & 0xffffu);
-}
-template <int La>
-__device__ __forceinline__ void store_held(uint8_t* AQ, int wq, int lane, const AHold& hold) {
-  const int x = 32 * wq + lane;
-  if (x < 64)
-    store_held_level<La>(AQ, x & 63, hold);
-  else
-    store_held_level<La / 2>(AQ, x & 63, hold);
-}
-
 // D (tmem) (+)= A (tmem) x B (smem), issued by a single thread.
 __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                         uint32_t idesc, uint32_t accumulate) {
@@ -546,7 +518,8 @@ __global__ void __launch_bounds__(NT, 1)
   const int nchunks = (u.len + C - 1) / C;
 
   if (tid == 0) {
-    for (int i = 0; i < B_COUNT; ++i) mbar_init(bars + i, 1);
+    for (int i = 0; i < B_COUNT; ++i)
+      mbar_init(bars + i, i == B_BETA ? 32 : (i == B_READY || i == B_READY + 1) ? 2 : 1);
     *s_abort = 0;
     fence_mbar_init();
     tma_prefetch_desc(&mq);
@@ -554,12 +527,12 @@ __global__ void __launch_bounds__(NT, 1)
     tma_prefetch_desc(&ma);
     tma_prefetch_desc(&mv);
   }
-  // A's upper triangle, N's blocks on and above the 16-block diagonal and the
-  // tile under T Diag(beta) are never written: clear them once
+  // A's upper triangle and N's blocks on and above the 16-block diagonal are
+  // never written: clear them once
   for (int e = tid; e < 8192 / 16; e += NT) {
     reinterpret_cast<uint4*>(sm + S_AK)[e] = make_uint4(0, 0, 0, 0);
+    reinterpret_cast<uint4*>(sm + S_A2)[e] = make_uint4(0, 0, 0, 0);
     reinterpret_cast<uint4*>(sm + S_TN)[e] = make_uint4(0, 0, 0, 0);
-    reinterpret_cast<uint4*>(sm + S_Z)[e] = make_uint4(0, 0, 0, 0);
   }
   if (warp == 0) {
     tmem_alloc(tmem_slot, TMEM_COLS);
@@ -575,17 +548,28 @@ __global__ void __launch_bounds__(NT, 1)
   if (warp < NPREP / 32) setmaxnreg_inc<kRegsPrep>();
   else if (warp >= MMA_WARP) setmaxnreg_dec<kRegsAux>();
 
+  // q, k, alpha tiles of chunk cc (one thread)
+  auto issue_qka = [&](int cc) {
+    const int y = (int)(u.row0 + (long)cc * C);
+    mbar_arrive_expect_tx(bar_qka, 3 * TILE_BYTES);
+    tma_load_2d(sm + S_TQ, &mq, bar_qka, 0, y);
+    tma_load_2d(sm + S_TQ + 8192, &mq, bar_qka, 64, y);
+    tma_load_2d(sm + S_TK, &mk, bar_qka, 0, y);
+    tma_load_2d(sm + S_TK + 8192, &mk, bar_qka, 64, y);
+    tma_load_2d(sm + S_TA, &ma, bar_qka, 0, y);
+    tma_load_2d(sm + S_TA + 8192, &ma, bar_qka, 64, y);
+  };
+
   if (tid < NPREP) {
     // =================================================================== PREP
-    // Iteration c (from -1) finishes chunk c -- E^2, F, T, T Diag(beta), W --
-    // and, in the MMA latencies of those steps, starts chunk c+1: its loads,
-    // gate products and Gram operands, then its Gram rounds, D and E = D N.
+    // Chunk cn: loads, gate products, the Gram rounds and their read-outs and
+    // D; E = D N is handed to the fourth warpgroup, which finishes the chunk
+    // (T, W) while this role stores the chunk's operands of the state step
+    // (once the state has released their tiles) and starts the next chunk.
     const int p = tid;
     const int w = p >> 5;
     const int blk = w >> 1, panel = w & 1;     // elementwise mapping
     const int wq = w & 3, half = w >> 2;       // TMEM lane quarter, column half
-    const int trow = 32 * wq + lane;           // this thread's TMEM lane
-    const uint32_t tl = (uint32_t)(32 * wq) << 16;
     bool alive = true;
     // waits for a completion of chunk cc on `bar` (one phase per chunk); the
     // AND over the role decides, uniformly, whether to go on
@@ -601,52 +585,31 @@ __global__ void __launch_bounds__(NT, 1)
       tc_fence_before();
       named_sync(BAR_PREP, NPREP);
     };
-    uint8_t* AQ = sm + S_AK;
     float* dg = reinterpret_cast<float*>(sm + S_DIAG);
     float2* totv = reinterpret_cast<float2*>(sm + S_TOT);
     Blk B;
-    for (int c = -1; c < nchunks && alive; ++c) {
-      const int cn = c + 1;                    // the chunk this iteration starts
-      const bool nx = cn < nchunks, tail = c >= 0;
-      const int lenn = nx ? min(C, u.len - cn * C) : 0;
-      float* beta_c = reinterpret_cast<float*>(sm + S_BETA) + 64 * (c & 1);
+    for (int cn = 0; cn < nchunks && alive; ++cn) {
+      const int c = cn - 1;                    // the chunk the fourth warpgroup finishes meanwhile
+      const int lenn = min(C, u.len - cn * C);
+      // A alternates between two tiles by chunk parity, so that its entries
+      // are written as they are read out (the state's step two chunks back
+      // was the last reader of this one)
+      uint8_t* AQ = sm + ((cn & 1) ? S_A2 : S_AK);
       float* beta_n = reinterpret_cast<float*>(sm + S_BETA) + 64 * (cn & 1);
-      // ---- chunk cn: q, k, alpha (the MMA warp fetches the tiles and beta)
-      if (nx) {
-        if (!prep_wait(bar_qka, cn)) { alive = false; break; }
-        if (lenn == C) load_block<false>(B, sm, blk, panel, lane, a.scale, C);
-        else load_block<true>(B, sm, blk, panel, lane, a.scale, lenn - 16 * blk);
+      // ---- q, k, alpha
+      if (!prep_wait(bar_qka, cn)) { alive = false; break; }
+      if (lenn == C) load_block<false>(B, sm, blk, panel, lane, a.scale, C);
+      else load_block<true>(B, sm, blk, panel, lane, a.scale, lenn - 16 * blk);
+      {
         const float sq = warp_sum16(B.dqk, lane);   // q.k over this panel's 64 channels
         if ((lane & 1) == 0) dg[64 * panel + 16 * blk + (lane >> 1)] = sq;
-        totv[64 * blk + 32 * panel + lane] = B.tot;
       }
-      // ---- chunk c: E -> [E ; I - E] (rows t of two tiles): lanes 0..63
-      if (tail) {
-        if (!prep_wait(bar_done + ST_E, c)) { alive = false; break; }
-        if (wq < 2) {
-          uint32_t v[32];
-          tmem_ld32<32>(tmem + tl + T_G1 + 32 * half, v);
-          tmem_ld_wait();
-#pragma unroll
-          for (int z = 0; z < 32; z += 8) {
-            float f[8], g[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              f[e] = __uint_as_float(v[z + e]);
-              g[e] = ((32 * half + z + e) == trow ? 1.f : 0.f) - f[e];
-            }
-            const uint32_t ch = (uint32_t)(32 * half + z) >> 3;
-            store16(sm + S_TE + sw128_chunk(64, trow, ch), pack_half8(f));
-            store16(sm + S_TIE + sw128_chunk(64, trow, ch), pack_half8(g));
-          }
-        }
-      }
-      // (also: chunk cn's tile reads are done -- the tile region becomes Gram
-      // buffer 2 -- and its block totals are visible)
-      publish();
-      if (tail && p == 0) mbar_arrive(bar_ops + ST_X);           // [E^2 | F]
+      totv[64 * blk + 32 * panel + lane] = B.tot;
+      // (block totals visible; the tile reads are done, so the tile region
+      // becomes Gram buffer 2)
+      named_sync(BAR_PREP, NPREP);
       __half2 Gb, Ga, t1, t2;
-      if (nx) {
+      {
         float2 T4[4];
 #pragma unroll
         for (int b = 0; b < 4; ++b) T4[b] = totv[64 * b + 32 * panel + lane];
@@ -665,88 +628,46 @@ __global__ void __launch_bounds__(NT, 1)
         if (blk == 0)
           reinterpret_cast<float2*>(gC)[32 * panel + lane] = make_float2(
               T4[0].x * T4[1].x * T4[2].x * T4[3].x, T4[0].y * T4[1].y * T4[2].y * T4[3].y);
-        // Gram round 1 of chunk cn: levels 8 and 4 (pairs inside 16-token blocks)
-        write_level_in<8, S_GX2, S_GY2, 0, 0>(sm, B, blk, panel, lane);
-        write_level_in<4, S_GX2, S_GY2, 64, 32>(sm, B, blk, panel, lane);
       }
-      // ---- chunk c: E^2 (G0, lanes 0..63) under F (G1, lanes 64..127)
-      if (tail) {
-        if (!prep_wait(bar_done + ST_X, c)) { alive = false; break; }
-        const bool e2 = wq < 2;
-        const int r = e2 ? trow : trow - 64;
-        uint32_t v[32];
-        tmem_ld32<32>(tmem + tl + (e2 ? T_G0 : T_G1) + 32 * half, v);
-        tmem_ld_wait();
-        uint8_t* dst = sm + (e2 ? S_TIE : S_TE);
-#pragma unroll
-        for (int z = 0; z < 32; z += 8) {
-          float f[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(v[z + e]);
-          store16(dst + sw128_chunk(64, r, (uint32_t)(32 * half + z) >> 3), pack_half8(f));
-        }
-      }
+      // Gram round 1: levels 8 and 4 (pairs inside 16-token blocks), buffer 2
+      write_level_in<8, S_GX2, S_GY2, 0, 0>(sm, B, blk, panel, lane);
+      write_level_in<4, S_GX2, S_GY2, 64, 32>(sm, B, blk, panel, lane);
       publish();
       if (p == 0) {
-        if (tail) mbar_arrive(bar_ops + ST_T);                   // T = F + E^2 F
-        if (nx) {
-          mbar_arrive(bar_ops + ST_R1);                          // round 1 of chunk cn (G0 is free)
-          mbar_arrive(bar_gc + (cn & 1));
-        }
+        mbar_arrive(bar_ops + ST_R1);
+        mbar_arrive(bar_gc + (cn & 1));
       }
-      // ---- chunk c: T Diag(beta) as bf16 (T is in G1, lanes 64..127); then
-      // round 2 of chunk cn into buffer 1, whose inverse tiles T has read
-      if (tail) {
-        if (!prep_wait(bar_done + ST_T, c)) { alive = false; break; }
-        if (wq >= 2) {
-          const int r = trow - 64;
-          uint32_t v[32];
-          tmem_ld32<32>(tmem + tl + T_G1 + 32 * half, v);
-          tmem_ld_wait();
-#pragma unroll
-          for (int z = 0; z < 32; z += 8) {
-            float f[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const int s = 32 * half + z + e;
-              f[e] = s <= r ? __uint_as_float(v[z + e]) * beta_c[s] : 0.f;
-            }
-            store16(sm + S_TB + sw128_chunk(64, r, (uint32_t)(32 * half + z) >> 3), pack_bf8(f));
-          }
-        }
-      }
-      if (nx) {
-        write_level_in<2, S_GX, S_GY, 0, 0>(sm, B, blk, panel, lane);
-        write_level_in<1, S_GX, S_GY, 64, 32>(sm, B, blk, panel, lane);
+      // Gram round 3 (levels 32 and 16) into buffer 1, once the previous
+      // chunk's T step has read its E and I - E tiles there
+      if (!prep_wait(bar_done + ST_T, c)) { alive = false; break; }
+      switch (blk) {
+        case 0: write_cross<0, S_GX, S_GY>(sm, B, t1, t2, panel, lane); break;
+        case 1: write_cross<1, S_GX, S_GY>(sm, B, t1, t2, panel, lane); break;
+        case 2: write_cross<2, S_GX, S_GY>(sm, B, t1, t2, panel, lane); break;
+        default: write_cross<3, S_GX, S_GY>(sm, B, t1, t2, panel, lane); break;
       }
       publish();
-      if (tail && p == 0) mbar_arrive(bar_ops + ST_W);           // W^T
-      // ---- chunk c: -W^T (fp16, panel 0 of [-W^T | (q*gamma)^T]; W^T is in
-      // G1, lane = i); then chunk c is ready for the state step
-      if (tail) {
-        if (!prep_wait(bar_done + ST_W, c)) { alive = false; break; }
-        uint32_t v[32];
-        tmem_ld32<32>(tmem + tl + T_G1 + 32 * half, v);
-        tmem_ld_wait();
-#pragma unroll
-        for (int z = 0; z < 32; z += 8) {
-          float f[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) f[e] = -__uint_as_float(v[z + e]);
-          store16(sm + S_WQ + sw128_chunk(64, trow, (uint32_t)(32 * half + z) >> 3), pack_half8(f));
-        }
+      if (p == 0) mbar_arrive(bar_ops + ST_R3);
+      // round 1 done (and the chunk's beta, first used by the read-out, in
+      // place): warps 0-3 read it out while the rest start round 2 (levels 2
+      // and 1) in buffer 2
+      {
+        bool ok = mbar_wait(bar_done + ST_R1, (uint32_t)(cn & 1));
+        if (ok) ok = mbar_wait(bar_beta, (uint32_t)(cn & 1));
+        if (!named_and(BAR_PREP, NPREP, ok)) { alive = false; break; }
+        tc_fence_after();
       }
+      if (half == 0) extract_round<8>(sm, tmem, T_G0, wq, lane, beta_n, AQ);
+      write_level_in<2, S_GX2, S_GY2, 0, 0>(sm, B, blk, panel, lane);
+      write_level_in<1, S_GX2, S_GY2, 64, 32>(sm, B, blk, panel, lane);
       publish();
-      if (p == 0) {
-        if (tail) mbar_arrive(bar_ready + (c & 1));
-        if (nx) mbar_arrive(bar_ops + ST_R2);                    // round 2 of chunk cn (G1 is free)
-      }
-      if (!nx) break;
-      // =============== the rest of chunk cn: its k*gamma, (q*gamma)^T,
-      // (k*rho)^T, the Gram read-outs, D and E = D N
+      if (p == 0) mbar_arrive(bar_ops + ST_R2);                  // (G0 has been read out)
       // gamma_t = (earlier blocks' totals) x prefix_t, a running product;
-      // k*gamma (bf16, A of the W^T step; chunk c's W^T step is done)
-      __half2 gq[16];
+      // k*gamma (bf16, A of the W^T step: the previous chunk's has read it);
+      // (q*gamma) and (k*rho), rho_s = exclusive suffix x later blocks'
+      // totals, stay in registers until the state releases their tiles
+      if (!prep_wait(bar_done + ST_W, c)) { alive = false; break; }
+      __half2 gq[16], kr[16];
       {
         __half2 g = Gb;
 #pragma unroll
@@ -757,44 +678,19 @@ __global__ void __launch_bounds__(NT, 1)
               pack_bf162(kg.x, kg.y);
           gq[r] = __hmul2(B.q[r], g);
         }
-      }
-      // round 3 (levels 32 and 16) goes into buffer 2 once round 1 is done; the
-      // A entries of round 1 wait for the state to release the A tile
-      {  // round 1 done; chunk cn's beta (first used by the read-out) in place
-        bool ok = mbar_wait(bar_done + ST_R1, (uint32_t)(cn & 1));
-        if (ok) ok = mbar_wait(bar_beta, (uint32_t)(cn & 1));
-        if (!named_and(BAR_PREP, NPREP, ok)) { alive = false; break; }
-        tc_fence_after();
-      }
-      AHold held;
-      if (half == 0) extract_round<8, true>(sm, tmem, T_G0, wq, lane, beta_n, AQ, &held);
-      switch (blk) {
-        case 0: write_cross<0, S_GX2, S_GY2>(sm, B, t1, t2, panel, lane); break;
-        case 1: write_cross<1, S_GX2, S_GY2>(sm, B, t1, t2, panel, lane); break;
-        case 2: write_cross<2, S_GX2, S_GY2>(sm, B, t1, t2, panel, lane); break;
-        default: write_cross<3, S_GX2, S_GY2>(sm, B, t1, t2, panel, lane); break;
-      }
-      publish();
-      if (p == 0) mbar_arrive(bar_ops + ST_R3);
-      // (q*gamma)^T next to -W^T: chunk c's [U | O] MMA has read them
-      if (!prep_wait(bar_s1, c)) { alive = false; break; }
-      store_transposed(sm + S_WQ + 16384, gq, blk, panel, lane);
-      // (k*rho)^T under A, rho_s = exclusive suffix x later blocks' totals:
-      // chunk c's [O | H] MMA has read them and A
-      {
         __half2 rr = Ga;
 #pragma unroll
         for (int r = 15; r >= 0; --r) {
           if (r < 15) rr = __hmul2(rr, B.a[r + 1]);
-          gq[r] = __hmul2(B.k[r], rr);
+          kr[r] = __hmul2(B.k[r], rr);
         }
       }
-      if (!prep_wait(bar_s3, c)) { alive = false; break; }
-      store_transposed(sm + S_AK + 8192, gq, blk, panel, lane);
-      if (half == 0) store_held<8>(AQ, wq, lane, held);
+      // round 2 done: warps 4-7 read it out; the tile region is free, so
+      // chunk cn+1's q, k, alpha are fetched now; D (in its own tile) is
+      // cleared for its diagonal blocks
       if (!prep_wait(bar_done + ST_R2, cn)) { alive = false; break; }
-      if (half == 1) extract_round<2>(sm, tmem, T_G1, wq, lane, beta_n, AQ);
-      // D lives in Gram buffer 1: clear it (its diagonal blocks come next)
+      if (p == 0 && cn + 1 < nchunks) issue_qka(cn + 1);
+      if (half == 1) extract_round<2>(sm, tmem, T_G0, wq, lane, beta_n, AQ);
       for (int e = p; e < 8192 / 16; e += NPREP) store16(sm + S_TD + 16 * e, make_uint4(0, 0, 0, 0));
       tc_fence_before();
       named_sync(BAR_PREP, NPREP);
@@ -807,7 +703,7 @@ __global__ void __launch_bounds__(NT, 1)
       } else if (w < 6) {
         ok = mbar_wait(bar_done + ST_R3, (uint32_t)(cn & 1));
         tc_fence_after();
-        if (ok) extract_round<32>(sm, tmem, T_G0, wq, lane, beta_n, AQ);
+        if (ok) extract_round<32>(sm, tmem, T_G1, wq, lane, beta_n, AQ);
       } else {
         const int t = p - 192;
         *reinterpret_cast<__half*>(AQ + sw128_off(64, t, t)) = __float2half_rn(dg[t] + dg[64 + t]);
@@ -816,6 +712,15 @@ __global__ void __launch_bounds__(NT, 1)
       tc_fence_before();
       if (!named_and(BAR_PREP, NPREP, ok)) { alive = false; break; }
       if (p == 0) mbar_arrive(bar_ops + ST_E);                   // E = D N
+      // the state step's operands: (q*gamma)^T next to -W^T once the previous
+      // chunk's [U | O] MMA has read them, (k*rho)^T once its [O | H] MMAs have
+      if (!prep_wait(bar_s1, c)) { alive = false; break; }
+      store_transposed(sm + S_WQ + 16384, gq, blk, panel, lane);
+      if (!prep_wait(bar_s3, c)) { alive = false; break; }
+      store_transposed(sm + S_AK + 8192, kr, blk, panel, lane);
+      fence_proxy_async_smem();
+      named_sync(BAR_PREP, NPREP);
+      if (p == 0) mbar_arrive(bar_ready + (cn & 1));             // (with warp 12's)
     }
     if (!alive) *reinterpret_cast<volatile int*>(s_abort) = 1;
   } else if (tid < NPREP + NSTATE) {
@@ -877,6 +782,13 @@ __global__ void __launch_bounds__(NT, 1)
     float fin = 0.f;  // becomes NaN once any output is inf or NaN
     for (int c = 0; c < nchunks && alive; ++c) {
       const int lenc = min(C, u.len - c * C);
+      {  // O starts from zero (the previous chunk's has been read out)
+        const uint32_t z[16] = {0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll
+        for (int i0 = 0; i0 < 64; i0 += 16) tmem_st32<16>(tmem + lb + T_O + i0, z);
+        tmem_st_wait();
+        tc_fence_before();
+      }
       {  // prep operands of chunk c in shared memory, and its v tile
         bool ok = mbar_wait(bar_ready + (c & 1), (uint32_t)((c >> 1) & 1));
         if (ok) ok = mbar_wait(bar_v, (uint32_t)(c & 1));
@@ -884,11 +796,11 @@ __global__ void __launch_bounds__(NT, 1)
         tc_fence_after();
       }
       if (lead) {
-        // [U~^T | 0] = V^T [TB ; 0]^T, then [U^T | O^T] += H^T [-W^T | (q*gamma)^T]
+        // U~^T = V^T TB^T, then [U^T | O^T] += H^T [-W^T | (q*gamma)^T]
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          umma_ss(tmem + T_U, mnmajor_desc(sb + S_V, 64, k), kmajor_desc(sb + S_TB, 128, k),
-                  idesc_f16(128, 128, 1, 1, 0), k > 0);
+          umma_ss(tmem + T_U, mnmajor_desc(sb + S_V, 64, k), kmajor_desc(sb + S_TB, 64, k),
+                  idesc_f16(128, 64, 1, 1, 0), k > 0);
 #pragma unroll
         for (int k = 0; k < 8; ++k)
           umma_ts(tmem + T_U, tmem + T_HA + 8 * k, mnmajor_desc(sb + S_WQ, 128, k),
@@ -925,11 +837,16 @@ __global__ void __launch_bounds__(NT, 1)
       named_sync(BAR_STATE, NSTATE);
       if (lead) {
         tc_fence_after();
-        // [O^T | H^T] += U^T [A ; (k*rho)^T]
+        // O^T += U^T A^T (A of this chunk's parity), H^T += U^T (k*rho)
+        const uint32_t sa = (c & 1) ? S_A2 : S_AK;
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          umma_ts(tmem + T_O, tmem + T_UA + 8 * k, kmajor_desc(sb + S_AK, 192, k),
-                  idesc_f16(128, 192, 0, 0, 0), 1);
+          umma_ts(tmem + T_O, tmem + T_UA + 8 * k, kmajor_desc(sb + sa, 64, k),
+                  idesc_f16(128, 64, 0, 0, 0), 1);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          umma_ts(tmem + T_H, tmem + T_UA + 8 * k, kmajor_desc(sb + S_AK + 8192, 128, k),
+                  idesc_f16(128, 128, 0, 0, 0), 1);
         umma_commit(bar_s3);
       }
       {
@@ -981,142 +898,254 @@ __global__ void __launch_bounds__(NT, 1)
     }
     ovf = !(fin == 0.f);
     if (!alive) *reinterpret_cast<volatile int*>(s_abort) = 1;
-  } else if (warp == MMA_WARP) {
-    // ============================================================ MMA ISSUE
-    // Same iteration structure as the prep role: iteration c issues chunk c's
-    // E^2 | F, T and W^T steps and chunk c+1's Gram rounds and E, in the
-    // order the prep role hands their operands over.
-    // The same thread also issues the q, k, alpha copies (chunk cc + 1 once
-    // round 3 of chunk cc, the last reader of the tile region, is done), L2
-    // prefetches one chunk further ahead, and beta -- a copy instruction can
-    // wait for room in the copy queue, which must not hold up a prep warp.
-    // (The state warps fetch each next v tile themselves.)
+  } else {
+    // ======================================================= INVERSE CHAIN
+    // Warps 12-15 (one per TMEM lane quarter) finish chunk c after the prep
+    // role has handed over E = D N: [E ; I - E] and its product with [E | D],
+    // T = F + E^2 F, T Diag(beta) and W^T, each a tensor-core step issued by
+    // lane 0 of warp 12 as soon as the warpgroup has written its operands.
+    // Between those steps the same thread issues chunk c+1's Gram rounds and
+    // E step as the prep role hands their operands over, and L2 prefetches;
+    // warp 12 loads beta.
+    const int tq = warp - MMA_WARP;            // TMEM lane quarter (= warp % 4)
+    const int row = 32 * tq + lane;            // this thread's TMEM lane
+    const uint32_t tl = (uint32_t)(32 * tq) << 16;
+    const bool issuer = warp == MMA_WARP && lane == 0;
     bool alive = true;
-    if (lane == 0) {
-      const uint32_t id64 = idesc_f16(128, 64, 0, 0, 0);
-      auto issue_qka = [&](int cc) {
-        const int y = (int)(u.row0 + (long)cc * C);
-        mbar_arrive_expect_tx(bar_qka, 3 * TILE_BYTES);
-        tma_load_2d(sm + S_TQ, &mq, bar_qka, 0, y);
-        tma_load_2d(sm + S_TQ + 8192, &mq, bar_qka, 64, y);
-        tma_load_2d(sm + S_TK, &mk, bar_qka, 0, y);
-        tma_load_2d(sm + S_TK + 8192, &mk, bar_qka, 64, y);
-        tma_load_2d(sm + S_TA, &ma, bar_qka, 0, y);
-        tma_load_2d(sm + S_TA + 8192, &ma, bar_qka, 64, y);
-      };
-      auto issue_v = [&](int cc) {
-        const int y = (int)(u.row0 + (long)cc * C);
-        mbar_arrive_expect_tx(bar_v, TILE_BYTES);
-        tma_load_2d(sm + S_V, &mv, bar_v, 0, y);
-        tma_load_2d(sm + S_V + 8192, &mv, bar_v, 64, y);
-      };
-      auto prefetch_l2 = [&](int cc) {
-        const int y = (int)(u.row0 + (long)cc * C);
+    auto tail_wait = [&](uint64_t* bar, int cc, bool ok) -> bool {
+      if (ok && cc >= 0) ok = mbar_wait(bar, (uint32_t)(cc & 1));
+      const bool all = named_and(BAR_TAIL, NTAIL, ok);
+      tc_fence_after();
+      return all;
+    };
+    auto tail_publish = [&]() {
+      fence_proxy_async_smem();
+      tc_fence_before();
+      named_sync(BAR_TAIL, NTAIL);
+    };
+    const uint32_t id64 = idesc_f16(128, 64, 0, 0, 0);
+    auto prefetch_l2 = [&](int cc) {
+      const int y = (int)(u.row0 + (long)cc * C);
 #pragma unroll
-        for (int x0 = 0; x0 < 128; x0 += 64) {
-          tma_prefetch_2d_l2(&mq, x0, y);
-          tma_prefetch_2d_l2(&mk, x0, y);
-          tma_prefetch_2d_l2(&ma, x0, y);
-          tma_prefetch_2d_l2(&mv, x0, y);
-        }
-      };
-      // beta of chunk cc into its parity buffer: all loads in flight at once,
-      // then published with a release arrive
-      const __nv_bfloat16* gbeta = static_cast<const __nv_bfloat16*>(a.beta);
-      auto load_beta = [&](int cc) {
-        const int len = min(C, u.len - cc * C);
-        const __nv_bfloat16* src = gbeta + u.row0 + (long)cc * C;
-        float* dst = reinterpret_cast<float*>(sm + S_BETA) + 64 * (cc & 1);
+      for (int x0 = 0; x0 < 128; x0 += 64) {
+        tma_prefetch_2d_l2(&mq, x0, y);
+        tma_prefetch_2d_l2(&mk, x0, y);
+        tma_prefetch_2d_l2(&ma, x0, y);
+        tma_prefetch_2d_l2(&mv, x0, y);
+      }
+    };
+    // beta of chunk cc, two tokens per lane of warp 12: fetched a chunk ahead
+    // into registers (as raw bf16, so that nothing waits on the load before
+    // the store), stored into its parity buffer once that is free; every
+    // lane arrives (the barrier counts 32)
+    const unsigned short* gbeta = static_cast<const unsigned short*>(a.beta);
+    uint32_t braw0 = 0, braw1 = 0;
+    auto fetch_beta = [&](int cc) {
+      const int len = min(C, u.len - cc * C);
+      const unsigned short* src = gbeta + u.row0 + (long)cc * C;
+      braw0 = lane < len ? (uint32_t)src[lane] : 0u;
+      braw1 = lane + 32 < len ? (uint32_t)src[lane + 32] : 0u;
+    };
+    auto store_beta = [&](int cc) {
+      float* dst = reinterpret_cast<float*>(sm + S_BETA) + 64 * (cc & 1);
+      uint32_t b0 = braw0, b1 = braw1;
+      asm volatile("" : "+r"(b0), "+r"(b1));  // the first use is here, not earlier
+      dst[lane] = __uint_as_float(b0 << 16);
+      dst[lane + 32] = __uint_as_float(b1 << 16);
+      mbar_arrive(bar_beta);
+    };
+    // Gram round: D (128 x 64) = X (128 rows) Y^T (64 rows), K = 128
+    auto gram = [&](uint32_t d_col, uint32_t xbuf, uint32_t ybuf) {
+      const uint64_t d_gx = kmajor_desc(sb + xbuf, 128, 0), d_gy = kmajor_desc(sb + ybuf, 64, 0);
 #pragma unroll
-        for (int t0 = 0; t0 < 64; t0 += 32) {
-          float b[32];
+      for (int k = 0; k < 8; ++k)  // K steps: 32 bytes in a panel, panels R*128 apart
+        umma_ss(tmem + d_col, d_gx + (uint64_t)((k >> 2) * 1024 + (k & 3) * 2),
+                d_gy + (uint64_t)((k >> 2) * 512 + (k & 3) * 2), id64, k > 0);
+    };
+    // issuer only: waits for the prep role's operands of step st of chunk cc
+    auto wait_ops = [&](int st, int cc) -> bool {
+      if (!mbar_wait(bar_ops + st, (uint32_t)(cc & 1))) return false;
+      tc_fence_after();
+      return true;
+    };
+    // issuer only: round 1 of chunk cc (buffer 2 -> G0)
+    auto issue_r1 = [&](int cc) -> bool {
+      if (!wait_ops(ST_R1, cc)) return false;
+      gram(T_G0, S_GX2, S_GY2);
+      umma_commit(bar_done + ST_R1);
+      return true;
+    };
+    // issuer only: rounds 3 (buffer 1 -> G1) and 2 (buffer 2 -> G0, once
+    // round 1 has been read out) of chunk cc, in the order the prep role hands
+    // them over, then its E step
+    auto issue_rest = [&](int cc) -> bool {
+      if (!wait_ops(ST_R3, cc)) return false;
+      gram(T_G1, S_GX, S_GY);
+      umma_commit(bar_done + ST_R3);
+      if (!wait_ops(ST_R2, cc)) return false;
+      gram(T_G0, S_GX2, S_GY2);
+      umma_commit(bar_done + ST_R2);
+      if (cc + 2 < nchunks) prefetch_l2(cc + 2);
+      // E = D N (rows 0..63 of G1)
+      if (!wait_ops(ST_E, cc)) return false;
 #pragma unroll
-          for (int t = 0; t < 32; ++t) b[t] = t0 + t < len ? __bfloat162float(src[t0 + t]) : 0.f;
-#pragma unroll
-          for (int t = 0; t < 32; ++t) dst[t0 + t] = b[t];
-        }
-        mbar_arrive(bar_beta);
-      };
-      if (nchunks > 0) {
+      for (int k = 0; k < 4; ++k)
+        umma_ss(tmem + T_G1, kmajor_desc(sb + S_TD, 128, k), mnmajor_desc(sb + S_TN, 64, k),
+                idesc_f16(128, 64, 0, 0, 1), k > 0);
+      umma_commit(bar_done + ST_E);
+      return true;
+    };
+    bool ok = true;                            // the issuer's waits so far
+    if (nchunks > 0 && warp == MMA_WARP) {
+      if (lane == 0) {
         issue_qka(0);
-        issue_v(0);
+        mbar_arrive_expect_tx(bar_v, TILE_BYTES);
+        tma_load_2d(sm + S_V, &mv, bar_v, 0, (int)u.row0);
+        tma_load_2d(sm + S_V + 8192, &mv, bar_v, 64, (int)u.row0);
         if (nchunks > 1) prefetch_l2(1);
-        load_beta(0);
       }
-      auto wait_ops = [&](int st, int cc) -> bool {
-        if (!mbar_wait(bar_ops + st, (uint32_t)(cc & 1))) return false;
-        tc_fence_after();
-        return true;
-      };
-      // Gram round: D (128 x 64) = X (128 rows) Y^T (64 rows), K = 128
-      auto gram = [&](uint32_t d_col, uint32_t xbuf, uint32_t ybuf) {
-        const uint64_t d_gx = kmajor_desc(sb + xbuf, 128, 0), d_gy = kmajor_desc(sb + ybuf, 64, 0);
-#pragma unroll
-        for (int k = 0; k < 8; ++k)  // K steps: 32 bytes in a panel, panels R*128 apart
-          umma_ss(tmem + d_col, d_gx + (uint64_t)((k >> 2) * 1024 + (k & 3) * 2),
-                  d_gy + (uint64_t)((k >> 2) * 512 + (k & 3) * 2), id64, k > 0);
-      };
-      for (int c = -1; c < nchunks && alive; ++c) {
-        const int cn = c + 1;
-        const bool nx = cn < nchunks, tail = c >= 0;
-        if (tail) {
-          // [E ; I - E] x [E | D]: E^2 in G0 rows 0..63, F = (I - E) D in G1 rows 64..127
-          if (!wait_ops(ST_X, c)) { alive = false; break; }
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            umma_ss(tmem + T_G0, kmajor_desc(sb + S_TE, 128, k), mnmajor_desc(sb + S_TE, 128, k),
-                    idesc_f16(128, 128, 0, 0, 1), k > 0);
-          umma_commit(bar_done + ST_X);
-          // T = F + E^2 F in G1 rows 64..127 (A rows 64..127 = E^2, B = F)
-          if (!wait_ops(ST_T, c)) { alive = false; break; }
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            umma_ss(tmem + T_G1, kmajor_desc(sb + S_TE, 128, k), mnmajor_desc(sb + S_TE, 64, k),
-                    idesc_f16(128, 64, 0, 0, 1), 1);
-          umma_commit(bar_done + ST_T);
-        }
-        if (nx) {
-          if (!wait_ops(ST_R1, cn)) { alive = false; break; }
-          gram(T_G0, S_GX2, S_GY2);
-          umma_commit(bar_done + ST_R1);
-        }
-        if (tail) {
-          // W^T = (k*gamma)^T TB^T in G1 (lane = i)
-          if (!wait_ops(ST_W, c)) { alive = false; break; }
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            umma_ss(tmem + T_G1, mnmajor_desc(sb + S_KG, 64, k), kmajor_desc(sb + S_TB, 64, k),
-                    idesc_f16(128, 64, 1, 1, 0), k > 0);
-          umma_commit(bar_done + ST_W);
-        }
-        if (nx) {
-          if (!wait_ops(ST_R2, cn)) { alive = false; break; }
-          gram(T_G1, S_GX, S_GY);
-          umma_commit(bar_done + ST_R2);
-          if (!wait_ops(ST_R3, cn)) { alive = false; break; }
-          gram(T_G0, S_GX2, S_GY2);
-          umma_commit(bar_done + ST_R3);
-          // round 3 was the last reader of the tile region: fetch chunk cn+1's
-          // q, k, alpha now, a whole chunk of work ahead of their use
-          if (cn + 1 < nchunks) {
-            if (!mbar_wait(bar_done + ST_R3, (uint32_t)(cn & 1))) { alive = false; break; }
-            issue_qka(cn + 1);
-            if (cn + 2 < nchunks) prefetch_l2(cn + 2);
-          }
-          // E = D N (rows 0..63 of G1)
-          if (!wait_ops(ST_E, cn)) { alive = false; break; }
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            umma_ss(tmem + T_G1, kmajor_desc(sb + S_TD, 128, k), mnmajor_desc(sb + S_TN, 64, k),
-                    idesc_f16(128, 64, 0, 0, 1), k > 0);
-          umma_commit(bar_done + ST_E);
-          // chunk cn+1's beta buffer was last read by chunk cn-1's T Diag(beta)
-          if (cn + 1 < nchunks) load_beta(cn + 1);
-        }
+      fetch_beta(0);
+      store_beta(0);
+      if (nchunks > 1) fetch_beta(1);
+      if (lane == 0) {
+        ok = issue_r1(0);
+        if (ok) ok = issue_rest(0);
       }
-      if (!alive) *reinterpret_cast<volatile int*>(s_abort) = 1;
+      __syncwarp();
+      // only once chunk 0's prep has passed its wait for beta: a second
+      // completion before that would alias the phase it waits for
+      if (nchunks > 1) store_beta(1);
     }
-    __syncwarp();
+    for (int c = 0; c < nchunks && alive; ++c) {
+      const int cn = c + 1;
+      const bool nx = cn < nchunks;
+      const float* beta_c = reinterpret_cast<const float*>(sm + S_BETA) + 64 * (c & 1);
+      // chunk c+2's beta, stored once chunk c+1's prep has passed its wait
+      if (warp == MMA_WARP && c + 2 < nchunks) fetch_beta(c + 2);
+      // ---- E -> [E ; I - E] (rows t of two tiles): lanes 0..63
+      if (!tail_wait(bar_done + ST_E, c, ok)) { alive = false; break; }
+      if (tq < 2) {
+        uint32_t v[64];
+        tmem_ld32<32>(tmem + tl + T_G1, *reinterpret_cast<uint32_t(*)[32]>(v));
+        tmem_ld32<32>(tmem + tl + T_G1 + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+        tmem_ld_wait();
+#pragma unroll
+        for (int z = 0; z < 64; z += 8) {
+          float f[8], g[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            f[e] = __uint_as_float(v[z + e]);
+            g[e] = ((z + e) == row ? 1.f : 0.f) - f[e];
+          }
+          store16(sm + S_TE + sw128_chunk(64, row, (uint32_t)z >> 3), pack_half8(f));
+          store16(sm + S_TIE + sw128_chunk(64, row, (uint32_t)z >> 3), pack_half8(g));
+        }
+      }
+      tail_publish();
+      if (issuer) {
+        // [E ; I - E] x [E | D]: E^2 in G0 rows 0..63, F = (I - E) D in G1
+        // rows 64..127 (D is the second 64-wide panel of B)
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          umma_ss(tmem + T_G0, kmajor_desc(sb + S_TE, 128, k),
+                  sw128_desc(sb + S_TE + (uint32_t)k * 2048u, S_TD - S_TE, 1024u),
+                  idesc_f16(128, 128, 0, 0, 1), k > 0);
+        umma_commit(bar_done + ST_X);
+      }
+      // ---- E^2 (G0, lanes 0..63) and F (G1, lanes 64..127) as fp16
+      if (!tail_wait(bar_done + ST_X, c, true)) { alive = false; break; }
+      {
+        const bool e2 = tq < 2;
+        const int r = e2 ? row : row - 64;
+        uint8_t* dst = sm + (e2 ? S_TIE : S_TE);
+        uint32_t v[64];
+        tmem_ld32<32>(tmem + tl + (e2 ? T_G0 : T_G1), *reinterpret_cast<uint32_t(*)[32]>(v));
+        tmem_ld32<32>(tmem + tl + (e2 ? T_G0 : T_G1) + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+        tmem_ld_wait();
+#pragma unroll
+        for (int z = 0; z < 64; z += 8) {
+          float f[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(v[z + e]);
+          store16(dst + sw128_chunk(64, r, (uint32_t)z >> 3), pack_half8(f));
+        }
+      }
+      tail_publish();
+      if (issuer) {
+        // T = F + E^2 F in G1 rows 64..127 (A rows 64..127 = E^2, B = F)
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          umma_ss(tmem + T_G1, kmajor_desc(sb + S_TE, 128, k), mnmajor_desc(sb + S_TE, 64, k),
+                  idesc_f16(128, 64, 0, 0, 1), 1);
+        umma_commit(bar_done + ST_T);
+        // round 1 of chunk cn (G0 is free: E^2 has been read)
+        if (nx) ok = issue_r1(cn);
+      }
+      // ---- T Diag(beta) as bf16 (T is in G1, lanes 64..127; its upper
+      // triangle is exactly zero), once the previous chunk's U~ step has read
+      // the last one
+      if (!tail_wait(bar_done + ST_T, c, ok)) { alive = false; break; }
+      if (!tail_wait(bar_s1, c - 1, true)) { alive = false; break; }
+      if (tq >= 2) {
+        const int r = row - 64;
+        uint32_t v[64];
+        tmem_ld32<32>(tmem + tl + T_G1, *reinterpret_cast<uint32_t(*)[32]>(v));
+        tmem_ld32<32>(tmem + tl + T_G1 + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+        tmem_ld_wait();
+#pragma unroll
+        for (int z = 0; z < 64; z += 8) {
+          const float4 b0 = *reinterpret_cast<const float4*>(beta_c + z);
+          const float4 b1 = *reinterpret_cast<const float4*>(beta_c + z + 4);
+          const float f[8] = {__uint_as_float(v[z]) * b0.x, __uint_as_float(v[z + 1]) * b0.y,
+                              __uint_as_float(v[z + 2]) * b0.z, __uint_as_float(v[z + 3]) * b0.w,
+                              __uint_as_float(v[z + 4]) * b1.x, __uint_as_float(v[z + 5]) * b1.y,
+                              __uint_as_float(v[z + 6]) * b1.z, __uint_as_float(v[z + 7]) * b1.w};
+          store16(sm + S_TB + sw128_chunk(64, r, (uint32_t)z >> 3), pack_bf8(f));
+        }
+      }
+      tail_publish();
+      if (issuer) {
+        // W^T = (k*gamma)^T TB^T in G1 (lane = i)
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          umma_ss(tmem + T_G1, mnmajor_desc(sb + S_KG, 64, k), kmajor_desc(sb + S_TB, 64, k),
+                  idesc_f16(128, 64, 1, 1, 0), k > 0);
+        umma_commit(bar_done + ST_W);
+      }
+      // ---- -W^T (fp16, panel 0 of [-W^T | (q*gamma)^T]; W^T is in G1,
+      // lane = i); then chunk c is ready for the state step (with the prep
+      // role's part)
+      if (!tail_wait(bar_done + ST_W, c, true)) { alive = false; break; }
+      {
+        uint32_t v[64];
+        tmem_ld32<32>(tmem + tl + T_G1, *reinterpret_cast<uint32_t(*)[32]>(v));
+        tmem_ld32<32>(tmem + tl + T_G1 + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+        tmem_ld_wait();
+#pragma unroll
+        for (int z = 0; z < 64; z += 8) {
+          float f[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) f[e] = -__uint_as_float(v[z + e]);
+          store16(sm + S_WQ + sw128_chunk(64, row, (uint32_t)z >> 3), pack_half8(f));
+        }
+      }
+      tail_publish();
+      if (warp == MMA_WARP) {
+        if (lane == 0) {
+          mbar_arrive(bar_ready + (c & 1));
+          if (nx) ok = issue_rest(cn);     // G1 is free: W^T has been read
+        }
+        __syncwarp();
+        // chunk c+2's beta buffer was last read by this chunk's T Diag(beta),
+        // and chunk c+1's prep has passed its wait for its own (a later
+        // completion of the barrier would alias that phase)
+        if (c + 2 < nchunks) store_beta(c + 2);
+      }
+    }
+    if (!alive || !ok) *reinterpret_cast<volatile int*>(s_abort) = 1;
   }
 
   // ---------------------------------------------------------------- teardown
