@@ -342,21 +342,29 @@ __device__ __forceinline__ void write_cross(uint8_t* sm, const Blk& B, __half2 t
 }
 // Rows i0 = 64 panel + 2 lane and i0 + 1 of a transposed [i][t] tile (one
 // 64-column panel, rows of 128 bytes): the 16 tokens of block blk are two
-// 16-byte chunks per row, assembled from the per-token channel pairs.
+// 16-byte chunks per row, assembled from the per-token channel pairs.  Lanes
+// 4..7 mod 8 write their second chunk first: the rows of one store then fall
+// in 4 swizzle phases x 2 chunks, 8 distinct bank groups.
 __device__ __forceinline__ void store_transposed(uint8_t* tile, const __half2 (&v)[16], int blk,
                                                  int panel, int lane) {
+  const uint32_t flip = ((uint32_t)lane >> 2) & 1u;
 #pragma unroll
   for (int e = 0; e < 2; ++e) {
     const uint32_t i = (uint32_t)(64 * panel + 2 * lane + e);
     const uint32_t sel = e ? 0x7632u : 0x5410u;
+    uint32_t w[2][4];
 #pragma unroll
-    for (int hc = 0; hc < 2; ++hc) {
-      uint32_t w[4];
+    for (int hc = 0; hc < 2; ++hc)
 #pragma unroll
       for (int m = 0; m < 4; ++m)
-        w[m] = __byte_perm(h2u(v[8 * hc + 2 * m]), h2u(v[8 * hc + 2 * m + 1]), sel);
-      const uint32_t ch = (uint32_t)(2 * blk + hc);
-      store16(tile + i * 128u + ((ch ^ (i & 7u)) << 4), make_uint4(w[0], w[1], w[2], w[3]));
+        w[hc][m] = __byte_perm(h2u(v[8 * hc + 2 * m]), h2u(v[8 * hc + 2 * m + 1]), sel);
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const uint32_t hc = (uint32_t)k ^ flip;
+      const uint4 x = hc ? make_uint4(w[1][0], w[1][1], w[1][2], w[1][3])
+                         : make_uint4(w[0][0], w[0][1], w[0][2], w[0][3]);
+      const uint32_t ch = (uint32_t)(2 * blk) + hc;
+      store16(tile + i * 128u + ((ch ^ (i & 7u)) << 4), x);
     }
   }
 }
@@ -712,11 +720,11 @@ __global__ void __launch_bounds__(NT, 1)
       tc_fence_before();
       if (!named_and(BAR_PREP, NPREP, ok)) { alive = false; break; }
       if (p == 0) mbar_arrive(bar_ops + ST_E);                   // E = D N
-      // the state step's operands: (q*gamma)^T next to -W^T once the previous
-      // chunk's [U | O] MMA has read them, (k*rho)^T once its [O | H] MMAs have
-      if (!prep_wait(bar_s1, c)) { alive = false; break; }
-      store_transposed(sm + S_WQ + 16384, gq, blk, panel, lane);
+      // the state step's operands: (q*gamma)^T next to -W^T and (k*rho)^T,
+      // once the previous chunk's [O | H] MMAs (issued after its [U | O] MMA
+      // had completed) have read them
       if (!prep_wait(bar_s3, c)) { alive = false; break; }
+      store_transposed(sm + S_WQ + 16384, gq, blk, panel, lane);
       store_transposed(sm + S_AK + 8192, kr, blk, panel, lane);
       fence_proxy_async_smem();
       named_sync(BAR_PREP, NPREP);
@@ -975,16 +983,15 @@ __global__ void __launch_bounds__(NT, 1)
       umma_commit(bar_done + ST_R1);
       return true;
     };
-    // issuer only: rounds 3 (buffer 1 -> G1) and 2 (buffer 2 -> G0, once
-    // round 1 has been read out) of chunk cc, in the order the prep role hands
-    // them over, then its E step
+    // issuer only: rounds 2 (buffer 2 -> G0, once round 1 has been read out;
+    // D waits for it) and 3 (buffer 1 -> G1) of chunk cc, then its E step
     auto issue_rest = [&](int cc) -> bool {
-      if (!wait_ops(ST_R3, cc)) return false;
-      gram(T_G1, S_GX, S_GY);
-      umma_commit(bar_done + ST_R3);
       if (!wait_ops(ST_R2, cc)) return false;
       gram(T_G0, S_GX2, S_GY2);
       umma_commit(bar_done + ST_R2);
+      if (!wait_ops(ST_R3, cc)) return false;
+      gram(T_G1, S_GX, S_GY);
+      umma_commit(bar_done + ST_R3);
       if (cc + 2 < nchunks) prefetch_l2(cc + 2);
       // E = D N (rows 0..63 of G1)
       if (!wait_ops(ST_E, cc)) return false;
