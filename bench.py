@@ -14,7 +14,8 @@ so no flush is done between steps.  Prints ONE JSON line on rank 0 with:
             timed region
   cpu_baseline  the fp64 CPU oracle timed on a bounded sample (rank 0, N=1)
   decode    the decode workload (B=256, H=32, 1000 chained steps): HBM GB/s
-  workloads the full-CKDA and packed workloads (N=1): token-heads/s, roofline
+  workloads the full-CKDA, packed and dk = 64 KDA-range workloads (N=1):
+            token-heads/s, roofline
   clocks    SM clocks and throttle reasons sampled during the timed region
 --impl reference runs the fp64 oracle as the reference arm on the host cores.
 Under torchrun each rank runs its own replica (weak scaling, no collective on
@@ -354,9 +355,9 @@ def run_ours(args):
     extras = [] if args.no_extras else [e for e in args.extras.split(",") if e and e != "none"]
     if ws == 1 and "decode" in extras:
         out["decode"] = decode_case(ck, args.decode_steps, 10, ws, stream)
-    if ws == 1 and any(e in extras for e in ("ckda_full", "ckda_varlen")):
+    if ws == 1 and any(e in extras for e in ("ckda_full", "ckda_varlen", "kda_range_dk64")):
         wl = {}
-        for nm, steps in (("ckda_full", 20), ("ckda_varlen", 10)):
+        for nm, steps in (("ckda_full", 20), ("ckda_varlen", 10), ("kda_range_dk64", 200)):
             if nm not in extras:
                 continue
             xx = synth.make_workload(nm)
@@ -438,8 +439,9 @@ def main():
     ap.add_argument("--decode-steps", type=int, default=1000)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-extras", action="store_true")
-    ap.add_argument("--extras", default="decode,ckda_full,ckda_varlen",
-                    help="comma list of extra measurements: decode, ckda_full, ckda_varlen")
+    ap.add_argument("--extras", default="decode,ckda_full,ckda_varlen,kda_range_dk64",
+                    help="comma list of extra measurements: decode, ckda_full, ckda_varlen, "
+                         "kda_range_dk64")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -104,7 +104,7 @@ ckda_status ckda_fwd(const void* q, const void* k, const void* v, const void* al
   if (dk > 128 || dv > 128) return CKDA_ERR_UNSUPPORTED;
   if (chunk_size != 0 && chunk_size != 16 && chunk_size != 32 && chunk_size != 64)
     return CKDA_ERR_UNSUPPORTED;
-  const bool tensor_path = io_dtype == CKDA_BF16 && dk == 128 && dv == 128;
+  const bool tensor_path = fwd_tensor_path(io_dtype, dk, dv);
   if (tensor_path && chunk_size != 0 && chunk_size != 64) return CKDA_ERR_UNSUPPORTED;
   const int nseq = cu_seqlens ? num_seqs : B;
   const size_t need = ckda_fwd_workspace_bytes(cu_seqlens ? num_seqs : 0, H);

@@ -2,6 +2,8 @@
 //
 // One CTA owns one (sequence, head) and walks its tokens in chunks of C = 64
 // with the fp32 state H^T (dv x dk = 128 x 128) resident in tensor memory.
+// A 64-wide key (dk = 64) runs as 128 channels whose last 64 have zero keys
+// and queries and unit gates: their state rows stay zero and add nothing.
 // The chunk algebra is the WY/UT form of a product of diagonal-plus-rank-one
 // transitions ("Complex KDA: Understanding and Enhancing the Expressivity of
 // Kimi Delta Attention", Sec. 2: KDA keeps "efficient WY-based chunk-wise
@@ -162,7 +164,7 @@ struct Unit {
   size_t sidx;
 };
 
-__device__ __forceinline__ Unit unit_of(const FwdArgs& a) {
+__device__ __forceinline__ Unit unit_of(const FwdArgs& a, int dk) {
   Unit u;
   const int b = blockIdx.x;
   const int h = b % a.H;
@@ -176,7 +178,7 @@ __device__ __forceinline__ Unit unit_of(const FwdArgs& a) {
     u.len = a.T;
     u.row0 = ((long)n * a.H + h) * a.T;
   }
-  u.sidx = ((size_t)n * a.H + h) * 128 * 128;
+  u.sidx = ((size_t)n * a.H + h) * (size_t)dk * 128;
   return u;
 }
 
@@ -219,17 +221,22 @@ struct Blk {
 };
 // Loads the block from the q, k, alpha tiles.  Tokens at or past `live` (the
 // end of the sequence, relative to the block) become identity transitions.
+// With pad set (channels past a 64-wide key) nothing is read: k = q = 0 and
+// alpha = 1, so that the state's rows for them stay zero and add nothing.
 template <bool kMask>
 __device__ __forceinline__ void load_block(Blk& B, const uint8_t* sm, int blk, int panel, int lane,
-                                           float scale, int live) {
+                                           float scale, int live, bool pad = false) {
   B.tot = make_float2(1.f, 1.f);
   const uint32_t tb = pair_tb<64>(panel, lane);
 #pragma unroll
   for (int r = 0; r < 16; ++r) {
     const uint32_t off = pair_at(tb, 16 * blk, r);
-    const uint32_t kw = *reinterpret_cast<const uint32_t*>(sm + S_TK + off);
-    const uint32_t qw = *reinterpret_cast<const uint32_t*>(sm + S_TQ + off);
-    const uint32_t aw = *reinterpret_cast<const uint32_t*>(sm + S_TA + off);
+    uint32_t kw = 0u, qw = 0u, aw = 0x3F803F80u;  // bf16 pairs (0, 0) and (1, 1)
+    if (!pad) {
+      kw = *reinterpret_cast<const uint32_t*>(sm + S_TK + off);
+      qw = *reinterpret_cast<const uint32_t*>(sm + S_TQ + off);
+      aw = *reinterpret_cast<const uint32_t*>(sm + S_TA + off);
+    }
     float2 kf = make_float2(__uint_as_float(kw << 16), __uint_as_float(kw & 0xffff0000u));
     float2 qf = make_float2(__uint_as_float(qw << 16) * scale,
                             __uint_as_float(qw & 0xffff0000u) * scale);
@@ -501,6 +508,9 @@ __device__ __forceinline__ void invert_diag_blocks(uint8_t* sm, int p) {
     *reinterpret_cast<__half*>(sm + S_TD + sw128_off(64, o + t, o + c)) = __float2half_rn(x[t]);
 }
 
+// DK: the caller's key width, 128 or 64 (a compile-time constant, so that
+// the 128-wide kernel carries nothing for the narrower one).
+template <int DK>
 __global__ void __launch_bounds__(NT, 1)
     fwd_chunk_kernel(const __grid_constant__ FwdArgs a, const __grid_constant__ CUtensorMap mq,
                      const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap ma,
@@ -522,7 +532,8 @@ __global__ void __launch_bounds__(NT, 1)
   int* s_abort = reinterpret_cast<int*>(sm + S_BAR + 192);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + S_BAR + 200);
 
-  const Unit u = unit_of(a);
+  static_assert(DK == 128 || DK == 64, "key width");
+  const Unit u = unit_of(a, DK);
   const int nchunks = (u.len + C - 1) / C;
 
   if (tid == 0) {
@@ -557,15 +568,20 @@ __global__ void __launch_bounds__(NT, 1)
   else if (warp >= MMA_WARP) setmaxnreg_dec<kRegsAux>();
 
   // q, k, alpha tiles of chunk cc (one thread)
+  // (with dk = 64 only the first 64-channel panel of each tile is loaded;
+  // the prep role treats channels 64..127 as padding)
+  constexpr bool dk64 = DK == 64;
   auto issue_qka = [&](int cc) {
     const int y = (int)(u.row0 + (long)cc * C);
-    mbar_arrive_expect_tx(bar_qka, 3 * TILE_BYTES);
+    mbar_arrive_expect_tx(bar_qka, dk64 ? 3 * TILE_BYTES / 2 : 3 * TILE_BYTES);
     tma_load_2d(sm + S_TQ, &mq, bar_qka, 0, y);
-    tma_load_2d(sm + S_TQ + 8192, &mq, bar_qka, 64, y);
     tma_load_2d(sm + S_TK, &mk, bar_qka, 0, y);
-    tma_load_2d(sm + S_TK + 8192, &mk, bar_qka, 64, y);
     tma_load_2d(sm + S_TA, &ma, bar_qka, 0, y);
-    tma_load_2d(sm + S_TA + 8192, &ma, bar_qka, 64, y);
+    if (!dk64) {
+      tma_load_2d(sm + S_TQ + 8192, &mq, bar_qka, 64, y);
+      tma_load_2d(sm + S_TK + 8192, &mk, bar_qka, 64, y);
+      tma_load_2d(sm + S_TA + 8192, &ma, bar_qka, 64, y);
+    }
   };
 
   if (tid < NPREP) {
@@ -606,8 +622,9 @@ __global__ void __launch_bounds__(NT, 1)
       float* beta_n = reinterpret_cast<float*>(sm + S_BETA) + 64 * (cn & 1);
       // ---- q, k, alpha
       if (!prep_wait(bar_qka, cn)) { alive = false; break; }
-      if (lenn == C) load_block<false>(B, sm, blk, panel, lane, a.scale, C);
-      else load_block<true>(B, sm, blk, panel, lane, a.scale, lenn - 16 * blk);
+      const bool pad = dk64 && panel == 1;
+      if (lenn == C) load_block<false>(B, sm, blk, panel, lane, a.scale, C, pad);
+      else load_block<true>(B, sm, blk, panel, lane, a.scale, lenn - 16 * blk, pad);
       {
         const float sq = warp_sum16(B.dqk, lane);   // q.k over this panel's 64 channels
         if ((lane & 1) == 0) dg[64 * panel + 16 * blk + (lane >> 1)] = sq;
@@ -750,7 +767,7 @@ __global__ void __launch_bounds__(NT, 1)
         if (from_h0) {
 #pragma unroll
           for (int e = 0; e < 16; ++e)
-            f[e] = a.h0 ? a.h0[u.sidx + (size_t)(i0 + e) * 128 + s] : 0.f;
+            f[e] = (a.h0 && i0 + e < DK) ? a.h0[u.sidx + (size_t)(i0 + e) * 128 + s] : 0.f;
         } else {
           uint32_t v[16];
           tmem_ld32<16>(tmem + lb + T_H + i0, v);
@@ -780,7 +797,7 @@ __global__ void __launch_bounds__(NT, 1)
       alive = named_and(BAR_STATE, NSTATE, ok);
       if (alive) convert_and_scale(0, true);
     } else if (hT) {
-      for (int i = 0; i < 128; ++i)
+      for (int i = 0; i < DK; ++i)
         hT[u.sidx + (size_t)i * 128 + s] = a.h0 ? a.h0[u.sidx + (size_t)i * 128 + s] : 0.f;
     }
     tc_fence_before();
@@ -892,7 +909,7 @@ __global__ void __launch_bounds__(NT, 1)
       }
     }
     if (alive && nchunks > 0 && hT) {
-      for (int i0 = 0; i0 < 128; i0 += 32) {
+      for (int i0 = 0; i0 < DK; i0 += 32) {
         uint32_t v[32];
         tmem_ld32<32>(tmem + lb + T_H + i0, v);
         tmem_ld_wait();
@@ -936,9 +953,11 @@ __global__ void __launch_bounds__(NT, 1)
       const int y = (int)(u.row0 + (long)cc * C);
 #pragma unroll
       for (int x0 = 0; x0 < 128; x0 += 64) {
-        tma_prefetch_2d_l2(&mq, x0, y);
-        tma_prefetch_2d_l2(&mk, x0, y);
-        tma_prefetch_2d_l2(&ma, x0, y);
+        if (x0 < DK) {
+          tma_prefetch_2d_l2(&mq, x0, y);
+          tma_prefetch_2d_l2(&mk, x0, y);
+          tma_prefetch_2d_l2(&ma, x0, y);
+        }
         tma_prefetch_2d_l2(&mv, x0, y);
       }
     };
@@ -1190,11 +1209,11 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
   return fn;
 }
 
-bool make_map(CUtensorMap* m, const void* base, uint64_t rows) {
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t width) {
   auto enc = get_encoder();
   if (!enc) return false;
-  cuuint64_t gdim[2] = {128, rows};
-  cuuint64_t gstride[1] = {128 * 2};
+  cuuint64_t gdim[2] = {width, rows};
+  cuuint64_t gstride[1] = {width * 2};
   cuuint32_t box[2] = {64, 64};
   cuuint32_t estr[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gdim, gstride, box,
@@ -1212,14 +1231,15 @@ cudaError_t launch_fwd_chunk(const FwdArgs& a, cudaStream_t s) {
   CUtensorMap mq, mk, ma, mv;
   if (rows == 0) {
     mq = mk = ma = mv = CUtensorMap{};  // every sequence is empty: no tile is ever loaded
-  } else if (!make_map(&mq, a.q, rows) || !make_map(&mk, a.k, rows) ||
-             !make_map(&ma, a.alpha, rows) || !make_map(&mv, a.v, rows)) {
+  } else if (!make_map(&mq, a.q, rows, a.dk) || !make_map(&mk, a.k, rows, a.dk) ||
+             !make_map(&ma, a.alpha, rows, a.dk) || !make_map(&mv, a.v, rows, 128)) {
     return cudaErrorInvalidValue;
   }
-  cudaError_t err = cudaFuncSetAttribute(
-      fwd_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_ALLOC);
+  auto kern = a.dk == 64 ? fwd_chunk_kernel<64> : fwd_chunk_kernel<128>;
+  cudaError_t err =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_ALLOC);
   if (err != cudaSuccess) return err;
-  fwd_chunk_kernel<<<units, NT, SMEM_ALLOC, s>>>(a, mq, mk, ma, mv);
+  kern<<<units, NT, SMEM_ALLOC, s>>>(a, mq, mk, ma, mv);
   return cudaGetLastError();
 }
 

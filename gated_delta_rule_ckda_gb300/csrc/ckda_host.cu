@@ -125,7 +125,7 @@ extern "C" ckda_status ckda_fwd_host(const void* q, const void* k, const void* v
   char* base = static_cast<char*>(dev_scratch);
   int* status = reinterpret_cast<int*>(base);
   float* state = reinterpret_cast<float*>(base + L.state);
-  const bool tensor_path = io_dtype == CKDA_BF16 && dk == 128 && dv == 128;
+  const bool tensor_path = fwd_tensor_path(io_dtype, dk, dv);
   const size_t units = (size_t)B * H;
 
 #define CK(call)                                  \

@@ -35,9 +35,16 @@ struct FwdArgs {
   ckda_dtype io;
 };
 
+// Shapes the chunkwise tensor-core kernel takes: bf16 I/O, dv = 128 and
+// dk = 128, or dk = 64 (the reduced key dimension of a state-reduced head,
+// "On State Reduction in Linear Attention"), run as 128 channels of which the
+// last 64 are inert padding.
+inline bool fwd_tensor_path(ckda_dtype io, int dk, int dv) {
+  return io == CKDA_BF16 && dv == 128 && (dk == 128 || dk == 64);
+}
 // Token-serial CUDA-core forward (any dk, dv <= 128).
 cudaError_t launch_fwd_recurrent(const FwdArgs& a, cudaStream_t s);
-// Chunkwise tcgen05 forward (bf16 I/O, dk = dv = 128, chunk 64).
+// Chunkwise tcgen05 forward (fwd_tensor_path shapes, chunk 64).
 cudaError_t launch_fwd_chunk(const FwdArgs& a, cudaStream_t s);
 // Longest-first order of packed sequences.
 cudaError_t launch_seq_order(const int32_t* cu, int n, int32_t* order, cudaStream_t s);

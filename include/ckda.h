@@ -90,8 +90,12 @@ size_t ckda_fwd_workspace_bytes(int num_seqs, int H);
  *   hT may alias h0 (each (sequence, head) reads its slice before writing).
  *   o must not alias any input.
  *
- * Paths: io_dtype = CKDA_BF16 with dk = dv = 128 runs the chunkwise
- * tensor-core kernel (chunk_size 0 or 64); every other supported shape
+ * Paths: io_dtype = CKDA_BF16 with dv = 128 and dk = 128 or 64 runs the
+ * chunkwise tensor-core kernel (chunk_size 0 or 64); dk = 64 is the reduced
+ * key dimension of a state-reduced head ("On State Reduction in Linear
+ * Attention"), run with the key channels padded to 128 inside the kernel
+ * (zero keys and queries, unit gates), which leaves the result unchanged.
+ * Every other supported shape
  * (dk, dv <= 128) runs the token-serial CUDA-core kernel, which has no
  * chunks (chunk_size 0, 16, 32 or 64 accepted and ignored; results never
  * depend on it).  scale multiplies q.

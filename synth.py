@@ -25,7 +25,7 @@ from typing import Optional
 
 import torch
 
-# --- the five named workloads -------------------------------------------------
+# --- the named workloads ------------------------------------------------------
 
 WORKLOADS = {
     "tiny_fp32": dict(B=1, H=1, T=64, d=16, dist="uniform", dtype="fp32", h0=False,
@@ -38,6 +38,10 @@ WORKLOADS = {
                         dtype="bf16", h0=False, seed=3, chunk=64),
     "ckda_decode": dict(B=256, H=32, d=128, steps=1000, dist="ckda", dtype="bf16",
                         seed=4),
+    # the KDA-range forward with the reduced key dimension of a state-reduced
+    # head ("On State Reduction in Linear Attention": dk' = 64 of dv = 128)
+    "kda_range_dk64": dict(B=8, H=16, T=2048, d=64, dv=128, dist="kda", dtype="bf16",
+                           h0=False, seed=5, chunk=64),
 }
 
 _DT = {"fp32": torch.float32, "bf16": torch.bfloat16}
@@ -141,8 +145,8 @@ def make_workload(name, **override):
         lengths = make_lengths(w["N"], w["Lmin"], w["Lmax"], generator=g)
         return make_varlen(lengths, w["H"], w["d"], dist=w["dist"], dtype=w["dtype"],
                            h0=w["h0"], generator=g)
-    return make_fwd(w["B"], w["H"], w["T"], w["d"], dist=w["dist"], dtype=w["dtype"],
-                    h0=w["h0"], seed=w["seed"])
+    return make_fwd(w["B"], w["H"], w["T"], w["d"], dv=w.get("dv"), dist=w["dist"],
+                    dtype=w["dtype"], h0=w["h0"], seed=w["seed"])
 
 
 # --- decode -----------------------------------------------------------------

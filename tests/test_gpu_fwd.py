@@ -1,8 +1,8 @@
 """GPU parity of ckda_fwd (C ABI) against the fp64 oracle.
 
 Dense and packed inputs, both kernel paths (tensor-core chunkwise for bf16
-d = 128, token-serial CUDA-core otherwise), ragged tails, edge cases, and
-the five named workloads at full size (outputs of the packed workload are
+dv = 128 with dk = 128 or 64, token-serial CUDA-core otherwise), ragged
+tails, edge cases, and the named workloads at full size (outputs of the packed workload are
 checked on a sample of sequences chosen to include the longest and shortest).
 """
 import numpy as np
@@ -201,6 +201,46 @@ def test_deterministic(ck):
     o1, h1 = run_gpu(ck, x)
     o2, h2 = run_gpu(ck, x)
     assert torch.equal(o1, o2) and torch.equal(h1, h2)
+
+
+# --------------------------------- tensor-core path, reduced key dimension 64
+
+@pytest.mark.parametrize("T", [1, 63, 130, 257])
+def test_chunk_path_dk64(ck, T):
+    x = synth.make_fwd(2, 3, T, 64, dv=128, dist="ckda", dtype="bf16", h0=True, seed=400 + T)
+    o, hT = run_gpu(ck, x, scale=0.7)
+    o_ref, h_ref = run_oracle(x, scale=0.7)
+    check(o, hT, o_ref, h_ref, bf16=True, name=f"dk=64 T={T}")
+
+
+def test_chunk_path_dk64_packed(ck):
+    x = synth.make_varlen([0, 1, 64, 200, 65], 2, 64, dv=128, dist="ckda", dtype="bf16",
+                          h0=True, seed=410)
+    o, hT = run_gpu(ck, x)
+    o_ref, h_ref = run_oracle(x)
+    check(o, hT, o_ref, h_ref, bf16=True, name="dk=64 packed")
+
+
+def test_chunk_path_dk64_equals_zero_padded_dk128(ck):
+    """dk = 64 runs as 128 channels whose last 64 have zero keys and queries
+    and unit gates; the same inputs padded that way in memory and run with
+    dk = 128 give bit-identical outputs."""
+    x = synth.make_fwd(1, 2, 150, 64, dv=128, dist="ckda", dtype="bf16", h0=True, seed=411)
+    pad = lambda t, val: torch.cat([t, torch.full_like(t, val)], dim=-1)
+    xp = synth.FwdInputs(pad(x.q, 0.0), pad(x.k, 0.0), x.v, pad(x.alpha, 1.0), x.beta,
+                         torch.cat([x.h0, torch.zeros_like(x.h0)], dim=2), None)
+    o, hT = run_gpu(ck, x)
+    op, hp = run_gpu(ck, xp)
+    assert torch.equal(o, op)
+    assert torch.equal(hT, hp[:, :, :64])
+    assert torch.count_nonzero(hp[:, :, 64:]) == 0
+
+
+def test_kda_range_dk64_workload_full(ck):
+    x = synth.make_workload("kda_range_dk64")
+    o, hT = run_gpu(ck, x)
+    o_ref, h_ref = run_oracle(x)
+    check(o, hT, o_ref, h_ref, bf16=True, name="kda_range_dk64")
 
 
 # ------------------------------------------------- token-serial CUDA-core path
