@@ -14,6 +14,8 @@ so no flush is done between steps.  Prints ONE JSON line on rank 0 with:
             timed region
   cpu_baseline  the fp64 CPU oracle timed on a bounded sample (rank 0, N=1)
   decode    the decode workload (B=256, H=32, 1000 chained steps): HBM GB/s
+  prep      the fused input preparation (ckda_prep) on raw inputs of the
+            KDA-range shape: HBM GB/s
   workloads the full-CKDA, packed and dk = 64 KDA-range workloads (N=1):
             token-heads/s, roofline
   clocks    SM clocks and throttle reasons sampled during the timed region
@@ -292,6 +294,46 @@ def decode_case(ck, steps, warmup, ws, stream, pool=32):
             "roofline": rl, "gpu_launches": steps}
 
 
+def prep_bytes(rows, dk, io_bytes=2, with_q=True):
+    nt = 3 if with_q else 2
+    return rows * 2 * (nt * dk * io_bytes + io_bytes)
+
+
+def prep_case(ck, x, steps, warmup, ws, stream):
+    """ckda_prep on raw inputs of the workload's shape: q and k unnormalised,
+    gate logits a ~ N(0, 2), b ~ N(0, 1); HBM bytes read and written once."""
+    import torch
+    B, H, T, dk = x.q.shape
+    g = torch.Generator().manual_seed(21)
+    raw = [torch.randn(sh, generator=g).to(torch.bfloat16).cuda()
+           for sh in ((B, H, T, dk), (B, H, T, dk), (B, H, T, dk), (B, H, T))]
+    qr, kr, ar, br = raw
+    qr.mul_(3)
+    ar.mul_(2)
+    out = (torch.empty_like(qr), torch.empty_like(kr), torch.empty_like(ar), torch.empty_like(br))
+
+    def step():
+        ck.prep(kr, ar, br, q_raw=qr, out=out, stream=stream)
+
+    total, per = time_steps(step, steps, warmup, ws, stream)
+    rows = B * H * T
+    nbytes = prep_bytes(rows, dk)
+    peak, src = hbm_peak()
+    ms = sum(per) / len(per)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    del raw, out
+    return {"value": round(nbytes * steps / total / 1e9, 1), "unit": "GB/s", "steps": steps,
+            "ms_per_step": round(total / steps * 1e3, 4),
+            "config": {"workload": "raw inputs of the kda_range shape", "rows": rows, "dk": dk,
+                       "io": "bf16", "normalize_q": True},
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(gbs / peak, 4), "traffic": None,
+                         "algorithmic_bytes": nbytes, "mean_launch_ms": round(ms, 4),
+                         "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)"
+                         if src == "measured" else src},
+            "gpu_launches": steps}
+
+
 def cpu_baseline(x, target_s=12.0):
     """The oracle, as it stands, on a bounded sample of the workload's units."""
     import oracle
@@ -355,6 +397,8 @@ def run_ours(args):
     extras = [] if args.no_extras else [e for e in args.extras.split(",") if e and e != "none"]
     if ws == 1 and "decode" in extras:
         out["decode"] = decode_case(ck, args.decode_steps, 10, ws, stream)
+    if ws == 1 and "prep" in extras:
+        out["prep"] = prep_case(ck, x, 200, 10, ws, stream)
     if ws == 1 and any(e in extras for e in ("ckda_full", "ckda_varlen", "kda_range_dk64")):
         wl = {}
         for nm, steps in (("ckda_full", 20), ("ckda_varlen", 10), ("kda_range_dk64", 200)):
@@ -439,9 +483,9 @@ def main():
     ap.add_argument("--decode-steps", type=int, default=1000)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-extras", action="store_true")
-    ap.add_argument("--extras", default="decode,ckda_full,ckda_varlen,kda_range_dk64",
-                    help="comma list of extra measurements: decode, ckda_full, ckda_varlen, "
-                         "kda_range_dk64")
+    ap.add_argument("--extras", default="decode,prep,ckda_full,ckda_varlen,kda_range_dk64",
+                    help="comma list of extra measurements: decode, prep, ckda_full, "
+                         "ckda_varlen, kda_range_dk64")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

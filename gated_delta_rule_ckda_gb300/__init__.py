@@ -20,7 +20,7 @@ import threading
 
 import torch
 
-__all__ = ["fwd", "fwd_host", "decode_step", "fwd_status", "workspace_bytes",
+__all__ = ["fwd", "fwd_host", "decode_step", "prep", "fwd_status", "workspace_bytes",
            "host_scratch_bytes", "selftest_timeout", "lib", "library_path", "CkdaError", "STATUS"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -73,6 +73,9 @@ def lib():
             L.ckda_selftest_timeout.argtypes = [vp, sz, ctypes.c_uint, vp]
             L.ckda_fwd_host_scratch_bytes.restype = sz
             L.ckda_fwd_host_scratch_bytes.argtypes = [i32, i32, i32, i32, i32, i32, i32]
+            L.ckda_prep.restype = i32
+            L.ckda_prep.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_longlong, i32, i32,
+                                    i32, f32, vp]
             L.ckda_fwd_host.restype = i32
             L.ckda_fwd_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
                                         i32, f32, i32, vp, sz, vp]
@@ -267,3 +270,42 @@ def fwd_noalloc(q, k, v, alpha, beta, h0=None, cu_seqlens=None, scale=1.0, chunk
     if rc != 0:
         raise CkdaError(rc, "ckda_fwd_noalloc")
     return o, hT
+
+
+def prep(k_raw, a_raw, b_raw, q_raw=None, normalize_q=True, norm_eps=1e-6, out=None,
+         stream=None):
+    """Fused input preparation (ckda_prep): unit-norm keys (and queries when
+    normalize_q), alpha = s[e^-5 + (1 - e^-5)|tanh(a/2)|], beta = 2 sigmoid(b).
+
+    k_raw, a_raw (and q_raw) are [..., dk]; b_raw is [...].  Returns
+    (q or None, k, alpha, beta) in the input dtype.  `out` may give the four
+    output tensors (q may be None); passing the inputs themselves works in place.
+    """
+    L = lib()
+    device = k_raw.device
+    dt = k_raw.dtype
+    dk = k_raw.shape[-1]
+    _check(a_raw, "a_raw", dt, tuple(k_raw.shape), device)
+    _check(b_raw, "b_raw", dt, tuple(k_raw.shape[:-1]), device)
+    if q_raw is not None:
+        _check(q_raw, "q_raw", dt, tuple(k_raw.shape), device)
+    _check(k_raw, "k_raw", dt, tuple(k_raw.shape), device)
+    if out is None:
+        q = None if q_raw is None else torch.empty_like(q_raw)
+        k, alpha, beta = torch.empty_like(k_raw), torch.empty_like(a_raw), torch.empty_like(b_raw)
+    else:
+        q, k, alpha, beta = out
+        for name, t, shp in (("k", k, k_raw.shape), ("alpha", alpha, k_raw.shape),
+                             ("beta", beta, k_raw.shape[:-1])):
+            _check(t, name, dt, tuple(shp), device)
+        if (q is None) != (q_raw is None):
+            raise ValueError("prep: q and q_raw must both be given or both be None")
+        if q is not None:
+            _check(q, "q", dt, tuple(k_raw.shape), device)
+    rows = k_raw.numel() // dk if dk else 0
+    rc = L.ckda_prep(_ptr(q_raw), _ptr(k_raw), _ptr(a_raw), _ptr(b_raw), _ptr(q), _ptr(k),
+                     _ptr(alpha), _ptr(beta), int(rows), int(dk), _io_dtype(k_raw),
+                     int(bool(normalize_q)), float(norm_eps), _stream_handle(stream, device))
+    if rc != 0:
+        raise CkdaError(rc, "ckda_prep")
+    return q, k, alpha, beta

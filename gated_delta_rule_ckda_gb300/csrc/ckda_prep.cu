@@ -1,0 +1,164 @@
+// ckda_prep.cu -- fused input preparation for the CKDA forward and decode:
+// unit-norm keys (and, on request, queries) and the paper's gate
+// parameterisation, in one pass over HBM.
+//
+// Per token ("Complex KDA" discussion slides, backup frame "practical gates
+// differ from exact theoretical endpoints"; paper App. E-G.1; the paper's
+// Sec. 6 "Implementation" fuses the gate's sign handling into the key
+// normalisation in the same way):
+//
+//   r = tanh(a / 2),  s = +1 if r >= 0 else -1,  alpha = s [eps + (1 - eps)|r|],
+//   eps = e^-5,       beta = 2 sigma(b),
+//   k <- k / sqrt(sum_i k_i^2 + norm_eps)            (paper Sec. 2: ||k_t|| = 1)
+//
+// One warp per token row; arithmetic in fp32, one rounding to the I/O dtype.
+// Bound: HBM (each byte read or written once).
+#include "ckda_internal.cuh"
+
+namespace ckda {
+namespace {
+
+constexpr float kGateEps = 0.006737947f;  // e^-5, the paper's gate floor
+
+struct PrepArgs {
+  const void* q_raw;
+  const void* k_raw;
+  const void* a_raw;
+  const void* b_raw;
+  void* q;
+  void* k;
+  void* alpha;
+  void* beta;
+  long long rows;
+  int dk;
+  int normalize_q;
+  float norm_eps;
+};
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) x += __shfl_xor_sync(0xffffffffu, x, m);
+  return x;
+}
+__device__ __forceinline__ float gate_alpha(float a) {
+  const float r = tanhf(0.5f * a);
+  const float s = r >= 0.f ? 1.f : -1.f;
+  return s * fmaf(1.f - kGateEps, fabsf(r), kGateEps);
+}
+// 2 sigma(b), with the exponential of a non-positive argument on either side
+// so that large |b| neither overflows nor loses the tail
+__device__ __forceinline__ float gate_beta(float b) {
+  if (b >= 0.f) return 2.f / (1.f + expf(-b));
+  const float e = expf(b);
+  return 2.f * e / (1.f + e);
+}
+
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+__device__ __forceinline__ uint32_t bf_pack(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// bf16, dk = 128: lane l owns channels 4l .. 4l + 3 (8-byte accesses).
+__global__ void __launch_bounds__(256) prep128_bf16_kernel(const PrepArgs a) {
+  const int lane = threadIdx.x & 31;
+  const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (row >= a.rows) return;
+  const size_t off = (size_t)row * 32 + lane;  // in uint2 units
+  const uint2 kw = static_cast<const uint2*>(a.k_raw)[off];
+  const uint2 aw = static_cast<const uint2*>(a.a_raw)[off];
+  uint2 qw = make_uint2(0u, 0u);
+  if (a.q_raw) qw = static_cast<const uint2*>(a.q_raw)[off];
+  float b = 0.f;
+  if (lane == 0) b = __bfloat162float(static_cast<const __nv_bfloat16*>(a.b_raw)[row]);
+
+  const float k0 = bf_lo(kw.x), k1 = bf_hi(kw.x), k2 = bf_lo(kw.y), k3 = bf_hi(kw.y);
+  const float ik = rsqrtf(warp_sum(k0 * k0 + k1 * k1 + k2 * k2 + k3 * k3) + a.norm_eps);
+  static_cast<uint2*>(a.k)[off] = make_uint2(bf_pack(k0 * ik, k1 * ik), bf_pack(k2 * ik, k3 * ik));
+  if (a.q_raw) {
+    const float q0 = bf_lo(qw.x), q1 = bf_hi(qw.x), q2 = bf_lo(qw.y), q3 = bf_hi(qw.y);
+    float iq = 1.f;
+    if (a.normalize_q) iq = rsqrtf(warp_sum(q0 * q0 + q1 * q1 + q2 * q2 + q3 * q3) + a.norm_eps);
+    static_cast<uint2*>(a.q)[off] =
+        make_uint2(bf_pack(q0 * iq, q1 * iq), bf_pack(q2 * iq, q3 * iq));
+  }
+  static_cast<uint2*>(a.alpha)[off] =
+      make_uint2(bf_pack(gate_alpha(bf_lo(aw.x)), gate_alpha(bf_hi(aw.x))),
+                 bf_pack(gate_alpha(bf_lo(aw.y)), gate_alpha(bf_hi(aw.y))));
+  if (lane == 0)
+    static_cast<__nv_bfloat16*>(a.beta)[row] = __float2bfloat16_rn(gate_beta(b));
+}
+
+// Any dk <= 128 and either I/O dtype: lane l owns channels l, l + 32, ...
+template <typename T>
+__global__ void __launch_bounds__(256) prep_kernel(const PrepArgs a) {
+  const int lane = threadIdx.x & 31;
+  const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (row >= a.rows) return;
+  const size_t base = (size_t)row * a.dk;
+  const T* kr = static_cast<const T*>(a.k_raw) + base;
+  const T* ar = static_cast<const T*>(a.a_raw) + base;
+  float kv[4], qv[4], av[4];
+  float sk = 0.f, sq = 0.f;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int c = lane + 32 * j;
+    kv[j] = qv[j] = av[j] = 0.f;
+    if (c < a.dk) {
+      kv[j] = ld_io<T>(kr + c);
+      av[j] = ld_io<T>(ar + c);
+      if (a.q_raw) qv[j] = ld_io<T>(static_cast<const T*>(a.q_raw) + base + c);
+    }
+    sk = fmaf(kv[j], kv[j], sk);
+    sq = fmaf(qv[j], qv[j], sq);
+  }
+  const float ik = rsqrtf(warp_sum(sk) + a.norm_eps);
+  float iq = 1.f;
+  if (a.q_raw && a.normalize_q) iq = rsqrtf(warp_sum(sq) + a.norm_eps);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int c = lane + 32 * j;
+    if (c < a.dk) {
+      st_io<T>(static_cast<T*>(a.k) + base + c, kv[j] * ik);
+      st_io<T>(static_cast<T*>(a.alpha) + base + c, gate_alpha(av[j]));
+      if (a.q_raw) st_io<T>(static_cast<T*>(a.q) + base + c, qv[j] * iq);
+    }
+  }
+  if (lane == 0)
+    st_io<T>(static_cast<T*>(a.beta) + row, gate_beta(ld_io<T>(static_cast<const T*>(a.b_raw) + row)));
+}
+
+}  // namespace
+}  // namespace ckda
+
+using namespace ckda;
+
+extern "C" ckda_status ckda_prep(const void* q_raw, const void* k_raw, const void* a_raw,
+                                 const void* b_raw, void* q, void* k, void* alpha, void* beta,
+                                 long long rows, int dk, ckda_dtype io_dtype, int normalize_q,
+                                 float norm_eps, void* stream) {
+  if (io_dtype != CKDA_F32 && io_dtype != CKDA_BF16) return CKDA_ERR_INVALID_ARG;
+  if (rows < 0 || dk < 1) return CKDA_ERR_INVALID_ARG;
+  if (!(norm_eps >= 0.f) || norm_eps > 3.0e38f) return CKDA_ERR_INVALID_ARG;
+  if ((q_raw == nullptr) != (q == nullptr)) return CKDA_ERR_INVALID_ARG;
+  if (rows > 0 && (!k_raw || !a_raw || !b_raw || !k || !alpha || !beta))
+    return CKDA_ERR_INVALID_ARG;
+  if (dk > 128) return CKDA_ERR_UNSUPPORTED;
+  if (rows > (long long)0x7fffffff * 8) return CKDA_ERR_UNSUPPORTED;
+  if (rows == 0) return CKDA_OK;
+  PrepArgs a{q_raw, k_raw, a_raw, b_raw, q, k, alpha, beta, rows, dk, normalize_q, norm_eps};
+  const unsigned blocks = (unsigned)((rows + 7) / 8);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  bool vec = io_dtype == CKDA_BF16 && dk == 128;
+  for (const void* p : {q_raw, k_raw, a_raw, static_cast<const void*>(q), static_cast<const void*>(k),
+                        static_cast<const void*>(alpha)})
+    if (p && (reinterpret_cast<uintptr_t>(p) & 7) != 0) vec = false;
+  if (vec)
+    prep128_bf16_kernel<<<blocks, 256, 0, s>>>(a);
+  else if (io_dtype == CKDA_BF16)
+    prep_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(a);
+  else
+    prep_kernel<float><<<blocks, 256, 0, s>>>(a);
+  return cudaGetLastError() == cudaSuccess ? CKDA_OK : CKDA_ERR_CUDA;
+}

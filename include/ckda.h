@@ -205,6 +205,39 @@ ckda_status ckda_decode_step(const void *q, const void *k, const void *v,
                              ckda_dtype io_dtype, float scale, void *stream);
 
 /*
+ * Input preparation, fused into one pass over HBM: the gate
+ * parameterisation of "Complex KDA" (discussion slides, backup frame
+ * "practical gates differ from exact theoretical endpoints"; paper App.
+ * E-G.1) and the unit-norm keys the recurrence assumes (paper Sec. 2), per
+ * token row of dk channels:
+ *
+ *   r = tanh(a / 2),  s = +1 if r >= 0 else -1,
+ *   alpha = s [e^-5 + (1 - e^-5) |r|],       beta = 2 sigma(b) = 2 / (1 + e^-b),
+ *   k = k_raw / sqrt(sum_i k_raw_i^2 + norm_eps),
+ *   q = q_raw / sqrt(sum_i q_raw_i^2 + norm_eps) if normalize_q, else q_raw.
+ *
+ * The paper's implementation fuses the gate's sign handling into the key
+ * normalisation the same way (Sec. 6 "Implementation").  Its outputs are
+ * ckda_fwd's and ckda_decode_step's q, k, alpha, beta.
+ *
+ *   q_raw, k_raw, a_raw : io [rows, dk]   (rows = B*H*T, or B*H for decode)
+ *   b_raw               : io [rows]
+ *   q, k, alpha         : io [rows, dk]    beta : io [rows]
+ *
+ * q_raw and q are both NULL (no query) or both set.  Each output may alias
+ * its own input (in place); outputs must not alias other inputs.  Arithmetic
+ * is fp32 with one rounding to io_dtype.  norm_eps >= 0; with norm_eps = 0 an
+ * all-zero row gives NaN, with norm_eps > 0 it stays zero.  dk <= 128.
+ * Argument errors return synchronously with nothing launched (rows = 0
+ * launches nothing and returns CKDA_OK); otherwise returns CKDA_OK once
+ * enqueued on `stream`.  The library allocates nothing.
+ */
+ckda_status ckda_prep(const void *q_raw, const void *k_raw, const void *a_raw,
+                      const void *b_raw, void *q, void *k, void *alpha, void *beta,
+                      long long rows, int dk, ckda_dtype io_dtype, int normalize_q,
+                      float norm_eps, void *stream);
+
+/*
  * Self-test of the bounded-wait path: launches one block that waits on a
  * barrier nothing will complete, with a limit of `spin_limit` polls (each
  * sleeping up to about a microsecond, the whole wait at most about a second),

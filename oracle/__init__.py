@@ -22,6 +22,14 @@ Functions and what pins them (tests/test_oracle_pins.py):
   exact-retrieval reduction.
 * ``decode_step`` -- pinned against ``fwd`` token by token and by the same
   rotation/decay fixtures.
+* ``prep`` -- the gate parameterisation and key normalisation ("Complex KDA"
+  discussion slides, backup frame "practical gates differ from exact
+  theoretical endpoints"): pinned by the properties that frame states (sign
+  rule with s = +1 at r = 0, log|alpha| in [-5, 0], beta in (0, 2), the
+  endpoints +-e^-5 next to a = 0 and |alpha| -> 1, beta -> 0 or 2 for large
+  logits) and by the identities the parameterisation implies (odd symmetry of
+  alpha, beta(-b) = 2 - beta(b), monotonicity in |a|, unit norm and direction
+  of the normalised keys).
 """
 from __future__ import annotations
 
@@ -46,7 +54,7 @@ def build(force: bool = False) -> str:
         return _LIB_PATH
     tmp = _LIB_PATH + f".tmp{os.getpid()}"
     cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp",
-           "-fno-fast-math", "-ffp-contract=off", _SRC, "-o", tmp]
+           "-fno-fast-math", "-ffp-contract=off", _SRC, "-o", tmp, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
@@ -70,6 +78,9 @@ def _load():
                                                     ctypes.c_int, ctypes.c_int,
                                                     ctypes.c_double, ctypes.c_int]
             lib.ckda_oracle_decode_step.restype = ctypes.c_int
+            lib.ckda_oracle_prep.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, ctypes.c_long,
+                                             ctypes.c_int, ctypes.c_int, ctypes.c_double]
+            lib.ckda_oracle_prep.restype = ctypes.c_int
             lib.ckda_oracle_max_threads.argtypes = []
             lib.ckda_oracle_max_threads.restype = ctypes.c_int
             _lib = lib
@@ -139,3 +150,25 @@ def decode_step(q, k, v, alpha, beta, state, scale=1.0, nthreads=0):
     if rc != 0:
         raise ValueError("oracle decode_step: invalid arguments")
     return o, S
+
+
+def prep(k_raw, a_raw, b_raw, q_raw=None, normalize_q=True, norm_eps=1e-6):
+    """Input preparation in fp64: (q, k, alpha, beta) from raw q, k and the gate
+    logits a [.., dk] and b [..] (q is None when q_raw is None)."""
+    lib = _load()
+    k_raw, a_raw, b_raw, q_raw = (_f64(x) for x in (k_raw, a_raw, b_raw, q_raw))
+    dk = k_raw.shape[-1]
+    rows = k_raw.size // dk
+    if a_raw.shape != k_raw.shape or b_raw.size != rows or (
+            q_raw is not None and q_raw.shape != k_raw.shape):
+        raise ValueError("oracle prep: shapes")
+    k = np.zeros_like(k_raw)
+    alpha = np.zeros_like(a_raw)
+    beta = np.zeros(b_raw.shape, dtype=np.float64)
+    q = None if q_raw is None else np.zeros_like(q_raw)
+    rc = lib.ckda_oracle_prep(_ptr(q_raw), _ptr(k_raw), _ptr(a_raw), _ptr(b_raw), _ptr(q),
+                              _ptr(k), _ptr(alpha), _ptr(beta), int(rows), int(dk),
+                              int(bool(normalize_q)), float(norm_eps))
+    if rc != 0:
+        raise ValueError("oracle prep: invalid arguments")
+    return q, k, alpha, beta

@@ -38,6 +38,7 @@
  * threads (same paper, App. B.2 "Heads and layers": heads have separate
  * states).  Every pair is computed token by token, in order.
  */
+#include <math.h>
 #include <stddef.h>
 #include <stdint.h>
 #include <stdlib.h>
@@ -170,6 +171,52 @@ int ckda_oracle_decode_step(const double *q, const double *k, const double *v,
         free(pred);
     }
     (void)nthreads;
+    return 0;
+}
+
+/* Input preparation, per token (row) of dk channels, in the paper's
+ * parameterisation ("Complex KDA" discussion slides, backup frame "practical
+ * gates differ from exact theoretical endpoints"; paper App. E-G.1):
+ *
+ *   r = tanh(a / 2),   s = +1 if r >= 0 else -1,
+ *   alpha = s [eps + (1 - eps) |r|],   eps = e^-5,
+ *   beta  = 2 sigma(b) = 2 / (1 + e^-b),
+ *
+ * and the unit-norm keys the recurrence assumes (paper Sec. 2: ||k_t|| = 1),
+ * here k / sqrt(sum_i k_i^2 + norm_eps) per token; q likewise when
+ * normalize_q is set, else copied.  Arrays are [rows, dk] (q, k, a) and
+ * [rows] (b); q_raw / q may be NULL together. */
+int ckda_oracle_prep(const double *q_raw, const double *k_raw, const double *a_raw,
+                     const double *b_raw, double *q, double *k, double *alpha,
+                     double *beta, long rows, int dk, int normalize_q, double norm_eps)
+{
+    if (!k_raw || !a_raw || !b_raw || !k || !alpha || !beta) return -1;
+    if ((q_raw == NULL) != (q == NULL)) return -1;
+    if (rows < 0 || dk < 1) return -1;
+    const double eps = exp(-5.0);
+    for (long t = 0; t < rows; ++t) {
+        const double *kr = k_raw + (size_t)t * dk;
+        double ss = 0.0;
+        for (int i = 0; i < dk; ++i) ss += kr[i] * kr[i];
+        double inv = 1.0 / sqrt(ss + norm_eps);
+        for (int i = 0; i < dk; ++i) k[(size_t)t * dk + i] = kr[i] * inv;
+        if (q_raw) {
+            const double *qr = q_raw + (size_t)t * dk;
+            double qi = 1.0;
+            if (normalize_q) {
+                double sq = 0.0;
+                for (int i = 0; i < dk; ++i) sq += qr[i] * qr[i];
+                qi = 1.0 / sqrt(sq + norm_eps);
+            }
+            for (int i = 0; i < dk; ++i) q[(size_t)t * dk + i] = qr[i] * qi;
+        }
+        for (int i = 0; i < dk; ++i) {
+            double r = tanh(a_raw[(size_t)t * dk + i] / 2.0);
+            double sgn = r >= 0.0 ? 1.0 : -1.0;
+            alpha[(size_t)t * dk + i] = sgn * (eps + (1.0 - eps) * fabs(r));
+        }
+        beta[t] = 2.0 / (1.0 + exp(-b_raw[t]));
+    }
     return 0;
 }
 

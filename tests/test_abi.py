@@ -97,6 +97,25 @@ def test_decode_argument_errors_are_synchronous(L):
     assert f(io=3) == 1
 
 
+def test_prep_argument_errors_are_synchronous(L):
+    vp = ctypes.c_void_p
+    names = ("q_raw", "k_raw", "a_raw", "b_raw", "q", "k", "alpha", "beta")
+    f = lambda **kw: L.ckda_prep(*(vp(kw.get(n, 16)) for n in names), kw.get("rows", 4),
+                                 kw.get("dk", 128), kw.get("io", 1), 1,
+                                 ctypes.c_float(kw.get("eps", 1e-6)), vp(None))
+    assert f(k_raw=None) == 1
+    assert f(beta=None) == 1
+    assert f(q=None) == 1          # q_raw given without q
+    assert f(rows=-1) == 1
+    assert f(dk=0) == 1
+    assert f(dk=129) == 2
+    assert f(io=3) == 1
+    assert f(eps=-1.0) == 1
+    assert f(eps=float("nan")) == 1
+    # no rows: nothing to do, nothing launched
+    assert f(rows=0, k_raw=None, beta=None) == 0
+
+
 def test_fwd_host_argument_errors_are_synchronous(L):
     """ckda_fwd_host rejects bad arguments, slices and scratch before any copy."""
     vp = ctypes.c_void_p

@@ -1,0 +1,120 @@
+"""GPU parity of ckda_prep (C ABI) against the fp64 oracle, and the forward
+run on prepared inputs.
+
+The kernel computes in fp32 and rounds once to the I/O dtype; the oracle
+computes in fp64.  bf16 outputs must lie within one bf16 ulp of the exact
+value (a double rounding, fp32 then bf16, can move a tie by one ulp); fp32
+outputs within 4e-6 relative plus 1e-38 (tanhf, expf and rsqrtf are each
+within a few ulp; below the normal range fp32 has only absolute precision).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from metrics import excess_bf16, max_rel
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ck():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import gated_delta_rule_ckda_gb300 as ck
+    ck.lib()
+    return ck
+
+
+def raw_inputs(rows, dk, dtype, seed, special=False):
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn((rows, dk), generator=g) * torch.rand((rows, 1), generator=g) * 4
+    k = torch.randn((rows, dk), generator=g) * torch.rand((rows, 1), generator=g) * 4
+    a = torch.randn((rows, dk), generator=g) * 3
+    b = torch.randn((rows,), generator=g) * 3
+    if special:
+        vals = torch.tensor([0.0, -0.0, 1e-30, -1e-30, 60.0, -60.0, 3.0, -3.0])
+        a[0, :8] = vals
+        b[:6] = torch.tensor([0.0, -0.0, 40.0, -40.0, 100.0, -100.0])
+    dt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    return tuple(t.to(dt) for t in (q, k, a, b))
+
+
+def ulp_bf16(x):
+    x = np.abs(np.asarray(x, dtype=np.float64))
+    e = np.floor(np.log2(np.maximum(x, 2.0 ** -126)))
+    return 2.0 ** (e - 7)
+
+
+def assert_close(gpu, ref, dtype, name):
+    g = gpu.detach().cpu().double().numpy()
+    r = np.asarray(ref, dtype=np.float64)
+    assert np.all(np.isfinite(g)), name
+    if dtype == "bf16":
+        bad = np.abs(g - r) > ulp_bf16(r) * (1 + 1e-9)
+        assert not bad.any(), (name, g[bad][:5], r[bad][:5])
+    else:
+        tol = 4e-6 * np.abs(r) + 1e-38
+        bad = np.abs(g - r) > tol
+        assert not bad.any(), (name, g[bad][:5], r[bad][:5])
+
+
+@pytest.mark.parametrize("dtype,dk", [("bf16", 128), ("bf16", 64), ("bf16", 80), ("fp32", 128),
+                                      ("fp32", 16)])
+@pytest.mark.parametrize("normalize_q", [True, False])
+def test_prep_matches_oracle(ck, dtype, dk, normalize_q):
+    q, k, a, b = raw_inputs(1000, dk, dtype, seed=dk + 7 * normalize_q, special=True)
+    qo, ko, ao, bo = ck.prep(k.cuda(), a.cuda(), b.cuda(), q_raw=q.cuda(),
+                             normalize_q=normalize_q)
+    torch.cuda.synchronize()
+    rq, rk, ra, rb = oracle.prep(k, a, b, q_raw=q, normalize_q=normalize_q)
+    assert_close(ko, rk, dtype, "k")
+    assert_close(ao, ra, dtype, "alpha")
+    assert_close(bo, rb, dtype, "beta")
+    assert_close(qo, rq, dtype, "q")
+    # the slide's sign rule on the special logits: a = 0 and -0 give +e^-5
+    assert float(ao[0, 0]) > 0 and float(ao[0, 1]) > 0
+    assert float(ao[0, 2]) > 0 and float(ao[0, 3]) < 0
+
+
+def test_prep_without_query_and_in_place(ck):
+    q, k, a, b = raw_inputs(333, 128, "bf16", seed=3)
+    kd, ad, bd = k.cuda(), a.cuda(), b.cuda()
+    qo, ko, ao, bo = ck.prep(kd, ad, bd, out=(None, kd, ad, bd))
+    torch.cuda.synchronize()
+    assert qo is None and ko.data_ptr() == kd.data_ptr()
+    _, rk, ra, rb = oracle.prep(k, a, b)
+    assert_close(kd, rk, "bf16", "k in place")
+    assert_close(ad, ra, "bf16", "alpha in place")
+    assert_close(bd, rb, "bf16", "beta in place")
+
+
+def test_prep_unit_norm_rows(ck):
+    _, k, a, b = raw_inputs(4096, 128, "fp32", seed=4)
+    _, ko, _, _ = ck.prep(k.cuda(), a.cuda(), b.cuda(), norm_eps=0.0)
+    n = torch.linalg.norm(ko.cpu().double(), dim=1)
+    assert torch.allclose(n, torch.ones_like(n), atol=2e-6)
+
+
+def test_prep_then_forward_matches_oracle(ck):
+    """Raw logits -> ckda_prep -> ckda_fwd on the tensor-core path, against the
+    oracle's prep followed by the oracle's recurrence on the same bf16 values."""
+    B, H, T, d = 2, 3, 200, 128
+    q, k, a, b = raw_inputs(B * H * T, d, "bf16", seed=11)
+    v = torch.randn((B, H, T, d), generator=torch.Generator().manual_seed(12)).to(torch.bfloat16)
+    shp = lambda t: t.reshape(B, H, T, d)
+    qo, ko, ao, bo = ck.prep(shp(k).cuda(), shp(a).cuda(), b.reshape(B, H, T).cuda(),
+                             q_raw=shp(q).cuda(), normalize_q=True)
+    o, hT = ck.fwd(qo, ko, v.cuda(), ao, bo)
+    assert ck.fwd_status(ck.fwd.last_workspace) == 0
+    # the oracle recurrence consumes exactly the prepared bf16 values
+    o_ref, h_ref = oracle.fwd(qo.cpu(), ko.cpu(), v, ao.cpu(), bo.cpu())
+    assert excess_bf16(o.cpu(), o_ref) <= 2e-2
+    assert max_rel(hT.cpu(), h_ref) <= 2e-2
+    # and the prepared values are the oracle's prep of the raw ones
+    rq, rk, ra, rb = oracle.prep(k, a, b, q_raw=q)
+    assert_close(ko.reshape(-1, d), rk, "bf16", "k")
+    assert_close(ao.reshape(-1, d), ra, "bf16", "alpha")

@@ -453,3 +453,92 @@ def test_oracle_rejects_bad_packing():
         oracle.fwd(z, z, z, z, np.zeros((1, 1, 4)), cu_seqlens=[0, 3])
     with pytest.raises(ValueError):
         oracle.fwd(z, z, z, z, np.zeros((1, 1, 4)), cu_seqlens=[0, 3, 2, 4])
+
+
+# ----------------------------------------------------------------- input prep
+# "Complex KDA" discussion slides, backup frame "practical gates differ from
+# exact theoretical endpoints": r = tanh(a/2), alpha = s[eps + (1-eps)|r|]
+# with eps = e^-5 and s = +1 for r >= 0, -1 otherwise; beta = 2 sigma(b);
+# log|alpha| stays in [-5, 0]; finite logits approach but do not attain
+# |alpha| = 1 or beta = 2.  Keys have unit norm (paper Sec. 2).
+
+def _prep_gates(a, b):
+    a = np.asarray(a, dtype=np.float64).reshape(1, -1)
+    b = np.asarray(b, dtype=np.float64).reshape(-1)[:1]
+    k = np.ones_like(a)
+    _, _, alpha, beta = oracle.prep(k, a, b)
+    return alpha[0], beta
+
+
+def test_prep_sign_rule_and_zero():
+    """s = +1 for r >= 0 (so a = 0 and a = -0 give +e^-5), -1 for r < 0."""
+    a = np.array([0.0, -0.0, 1e-30, -1e-30, 0.3, -0.3, 7.0, -7.0])
+    alpha, _ = _prep_gates(a, [0.0])
+    assert alpha[0] == math.exp(-5.0) and alpha[1] == math.exp(-5.0)
+    np.testing.assert_array_equal(np.sign(alpha[2:]), [1, -1, 1, -1, 1, -1])
+    # next to a = 0 the gate jumps between the two endpoints +-e^-5
+    assert alpha[2] == pytest.approx(math.exp(-5.0), rel=1e-12)
+    assert alpha[3] == pytest.approx(-math.exp(-5.0), rel=1e-12)
+
+
+def test_prep_gate_range_and_endpoints():
+    """log|alpha| in [-5, 0] for every logit; |alpha| and beta approach 1 and
+    2 (or 0) for large logits; beta(0) = 1 (sigma(0) = 1/2)."""
+    a = np.linspace(-60.0, 60.0, 2001)
+    alpha, _ = _prep_gates(a, [0.0])
+    la = np.log(np.abs(alpha))
+    assert la.min() >= -5.0 - 1e-12 and la.max() <= 0.0
+    assert abs(alpha[-1]) == pytest.approx(1.0, abs=1e-12)
+    assert abs(alpha[0]) == pytest.approx(1.0, abs=1e-12)
+    # finite moderate logits stay strictly inside
+    alpha_mid, _ = _prep_gates([8.0, -8.0], [0.0])
+    assert np.all(np.abs(alpha_mid) < 1.0)
+    for b, want in ((0.0, 1.0), (40.0, 2.0), (-40.0, 0.0)):
+        _, beta = _prep_gates([0.0], [b])
+        assert beta[0] == pytest.approx(want, abs=1e-12)
+    _, beta = _prep_gates([0.0], [5.0])
+    assert 0.0 < beta[0] < 2.0
+
+
+def test_prep_symmetries_and_monotonicity():
+    """alpha(-a) = -alpha(a) for a != 0 (tanh is odd, s flips); beta(-b) =
+    2 - beta(b) (sigma(-b) = 1 - sigma(b)); |alpha| grows with |a|."""
+    rng = np.random.default_rng(5)
+    a = rng.normal(0.0, 3.0, 257)
+    a = a[a != 0.0]
+    ap, _ = _prep_gates(a, [0.0])
+    am, _ = _prep_gates(-a, [0.0])
+    np.testing.assert_allclose(am, -ap, rtol=0, atol=1e-15)
+    for b in rng.normal(0.0, 4.0, 16):
+        _, bp = _prep_gates([0.0], [b])
+        _, bm = _prep_gates([0.0], [-b])
+        assert bp[0] + bm[0] == pytest.approx(2.0, abs=1e-14)
+    grid = np.linspace(0.0, 30.0, 301)
+    g, _ = _prep_gates(grid, [0.0])
+    assert np.all(np.diff(g) >= 0.0)
+
+
+def test_prep_half_logit_scale():
+    """r = tanh(a/2): a gate with a = 2 atanh(r*) has |r| = r*, so alpha =
+    eps + (1 - eps) r* -- e.g. r* = 1/2 at a = ln 3 (tanh(ln(3)/2) = 1/2)."""
+    alpha, _ = _prep_gates([math.log(3.0)], [0.0])
+    eps = math.exp(-5.0)
+    assert alpha[0] == pytest.approx(eps + (1.0 - eps) * 0.5, rel=1e-14)
+
+
+def test_prep_unit_keys():
+    """Normalised keys have unit norm and point along the raw key; q is
+    normalised only on request (else copied); zero keys stay finite."""
+    rng = np.random.default_rng(6)
+    k = rng.normal(0.0, 1.0, (9, 24)) * rng.uniform(0.1, 10.0, (9, 1))
+    q = rng.normal(0.0, 1.0, (9, 24))
+    a = np.zeros_like(k)
+    b = np.zeros(9)
+    qn, kn, _, _ = oracle.prep(k, a, b, q_raw=q, normalize_q=True, norm_eps=0.0)
+    np.testing.assert_allclose(np.linalg.norm(kn, axis=1), 1.0, rtol=1e-14)
+    np.testing.assert_allclose(np.linalg.norm(qn, axis=1), 1.0, rtol=1e-14)
+    np.testing.assert_allclose(np.sum(kn * k, axis=1), np.linalg.norm(k, axis=1), rtol=1e-13)
+    qc, _, _, _ = oracle.prep(k, a, b, q_raw=q, normalize_q=False)
+    np.testing.assert_array_equal(qc, q)
+    _, kz, _, _ = oracle.prep(np.zeros((1, 8)), np.zeros((1, 8)), np.zeros(1))
+    assert np.all(kz == 0.0)
