@@ -67,6 +67,7 @@ def hbm_peak():
 KERNEL_SOURCES = {
     "fwd_chunk": ["ckda_chunk.cu", "sm103.cuh", "ckda_internal.cuh"],
     "decode128": ["ckda_decode.cu", "ckda_internal.cuh"],
+    "prep": ["ckda_prep.cu", "ckda_internal.cuh"],
 }
 
 
@@ -327,7 +328,7 @@ def prep_case(ck, x, steps, warmup, ws, stream):
             "config": {"workload": "raw inputs of the kda_range shape", "rows": rows, "dk": dk,
                        "io": "bf16", "normalize_q": True},
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
-                         "frac": round(gbs / peak, 4), "traffic": None,
+                         "frac": round(gbs / peak, 4), "traffic": traffic_for("prep", "kda_range"),
                          "algorithmic_bytes": nbytes, "mean_launch_ms": round(ms, 4),
                          "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)"
                          if src == "measured" else src},
