@@ -22,6 +22,10 @@ Functions and what pins them (tests/test_oracle_pins.py):
   exact-retrieval reduction.
 * ``decode_step`` -- pinned against ``fwd`` token by token and by the same
   rotation/decay fixtures.
+* ``bwd`` -- reverse-mode gradients of sum <o, do> + <hT, dhT>: pinned by
+  central finite differences of ``fwd`` (itself pinned above) on small
+  problems, including gates exactly 0 and -1 and beta = 2, and by the
+  closed form of the gradients when beta = 0 and alpha = 1 (o_t = h0^T q_t).
 * ``prep`` -- the gate parameterisation and key normalisation ("Complex KDA"
   discussion slides, backup frame "practical gates differ from exact
   theoretical endpoints"): pinned by the properties that frame states (sign
@@ -78,6 +82,11 @@ def _load():
                                                     ctypes.c_int, ctypes.c_int,
                                                     ctypes.c_double, ctypes.c_int]
             lib.ckda_oracle_decode_step.restype = ctypes.c_int
+            lib.ckda_oracle_bwd.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, dp, dp, dp, dp, dp,
+                                            dp, ip, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                            ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                            ctypes.c_double, ctypes.c_int]
+            lib.ckda_oracle_bwd.restype = ctypes.c_int
             lib.ckda_oracle_prep.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, ctypes.c_long,
                                              ctypes.c_int, ctypes.c_int, ctypes.c_double]
             lib.ckda_oracle_prep.restype = ctypes.c_int
@@ -172,3 +181,35 @@ def prep(k_raw, a_raw, b_raw, q_raw=None, normalize_q=True, norm_eps=1e-6):
     if rc != 0:
         raise ValueError("oracle prep: invalid arguments")
     return q, k, alpha, beta
+
+
+def bwd(q, k, v, alpha, beta, do, h0=None, dhT=None, cu_seqlens=None, scale=1.0,
+        store_dh0=True, nthreads=0):
+    """Gradients of L = sum_t <o_t, do_t> + <hT, dhT> (fp64 numpy).
+
+    Returns (dq, dk, dv, dalpha, dbeta, dh0 or None) in the layouts of the
+    inputs ([B, H, T, .] and [N, H, dk, dv])."""
+    lib = _load()
+    q, k, v, alpha, beta, do, h0, dhT = (_f64(a) for a in (q, k, v, alpha, beta, do, h0, dhT))
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    cu = None
+    N = B
+    if cu_seqlens is not None:
+        if hasattr(cu_seqlens, "detach"):
+            cu_seqlens = cu_seqlens.detach().to("cpu").numpy()
+        cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int32))
+        N = cu.shape[0] - 1
+    dq, dkk, dal = (np.zeros_like(q) for _ in range(3))
+    dvv = np.zeros_like(v)
+    dbe = np.zeros_like(beta)
+    dh0 = np.zeros((N, H, dk, dv), dtype=np.float64) if store_dh0 else None
+    rc = lib.ckda_oracle_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(h0),
+                             _ptr(do), _ptr(dhT), _ptr(dq), _ptr(dkk), _ptr(dvv), _ptr(dal),
+                             _ptr(dbe), _ptr(dh0),
+                             None if cu is None else cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                             int(N if cu is not None else 0), B, H, T, dk, dv, float(scale),
+                             int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle bwd: invalid arguments or out of memory")
+    return dq, dkk, dvv, dal, dbe, dh0

@@ -174,6 +174,138 @@ int ckda_oracle_decode_step(const double *q, const double *k, const double *v,
     return 0;
 }
 
+/* Gradients of one (sequence, head) pair by reverse-mode differentiation of
+ * the token steps of ckda_token, taken in reverse order.  The loss is
+ * L = sum_t <o_t, do_t> + <H_T, dhT>.  Every state S_0 .. S_len of the pair is
+ * kept.
+ *
+ * Forward step t:  G = Diag(alpha) S_t,  p = G^T k,  u = beta (v - p),
+ *                  S_{t+1} = G + k u^T,  o = S_{t+1}^T (scale q).
+ * Reverse step t, with D = dL/dS_{t+1} (starting from dhT, or 0):
+ *   D += (scale q) do^T;         dq = scale S_{t+1} do
+ *   du = D^T k;                  dk = D u
+ *   dbeta = <du, v - p>;         dv = beta du;      dp = -beta du
+ *   dk += G dp;                  dG = D + k dp^T
+ *   dalpha_i = sum_j dG_ij (S_t)_ij;                D = Diag(alpha) dG
+ * and dh0 = D at the end. */
+static int ckda_pair_bwd(const double *q, const double *k, const double *v,
+                         const double *alpha, const double *beta, const double *h0,
+                         const double *dout, const double *dhT, double *dq, double *dkk,
+                         double *dvv, double *dal, double *dbe, double *dh0,
+                         long row0, int len, int dk, int dv, double scale, size_t sidx)
+{
+    const size_t nn = (size_t)dk * dv;
+    double *S = (double *)malloc((size_t)(len + 1) * nn * sizeof(double));
+    double *D = (double *)malloc(nn * sizeof(double));
+    double *G = (double *)malloc(nn * sizeof(double));
+    double *vec = (double *)malloc((size_t)4 * dv * sizeof(double));
+    if (!S || !D || !G || !vec) { free(S); free(D); free(G); free(vec); return -1; }
+    double *p = vec, *u = vec + dv, *du = vec + 2 * dv, *dp = vec + 3 * dv;
+    for (size_t e = 0; e < nn; ++e) S[e] = h0 ? h0[sidx + e] : 0.0;
+    for (int t = 0; t < len; ++t) {
+        const size_t r = (size_t)(row0 + t);
+        const double *St = S + (size_t)t * nn;
+        double *Sn = S + (size_t)(t + 1) * nn;
+        for (int j = 0; j < dv; ++j) {
+            double acc = 0.0;
+            for (int i = 0; i < dk; ++i) acc += k[r * dk + i] * alpha[r * dk + i] * St[(size_t)i * dv + j];
+            p[j] = acc;
+            u[j] = beta[r] * (v[r * dv + j] - acc);
+        }
+        for (int i = 0; i < dk; ++i)
+            for (int j = 0; j < dv; ++j)
+                Sn[(size_t)i * dv + j] = alpha[r * dk + i] * St[(size_t)i * dv + j] + k[r * dk + i] * u[j];
+    }
+    for (size_t e = 0; e < nn; ++e) D[e] = dhT ? dhT[sidx + e] : 0.0;
+    for (int t = len - 1; t >= 0; --t) {
+        const size_t r = (size_t)(row0 + t);
+        const double *St = S + (size_t)t * nn, *Sn = S + (size_t)(t + 1) * nn;
+        const double *qt = q + r * dk, *kt = k + r * dk, *at = alpha + r * dk;
+        const double *vt = v + r * dv, *dot = dout + r * dv;
+        const double bt = beta[r];
+        for (int i = 0; i < dk; ++i) {
+            double acc = 0.0;
+            for (int j = 0; j < dv; ++j) {
+                D[(size_t)i * dv + j] += scale * qt[i] * dot[j];
+                acc += Sn[(size_t)i * dv + j] * dot[j];
+            }
+            dq[r * dk + i] = scale * acc;
+        }
+        for (int i = 0; i < dk; ++i)
+            for (int j = 0; j < dv; ++j) G[(size_t)i * dv + j] = at[i] * St[(size_t)i * dv + j];
+        double dbeta = 0.0;
+        for (int j = 0; j < dv; ++j) {
+            double pj = 0.0, dj = 0.0;
+            for (int i = 0; i < dk; ++i) {
+                pj += kt[i] * G[(size_t)i * dv + j];
+                dj += kt[i] * D[(size_t)i * dv + j];
+            }
+            p[j] = pj;
+            u[j] = bt * (vt[j] - pj);
+            du[j] = dj;
+            dbeta += dj * (vt[j] - pj);
+            dvv[r * dv + j] = bt * dj;
+            dp[j] = -bt * dj;
+        }
+        dbe[r] = dbeta;
+        for (int i = 0; i < dk; ++i) {
+            double gk = 0.0, ga = 0.0;
+            for (int j = 0; j < dv; ++j) {
+                const size_t e = (size_t)i * dv + j;
+                gk += D[e] * u[j] + G[e] * dp[j];
+                const double dG = D[e] + kt[i] * dp[j];
+                ga += dG * St[e];
+                D[e] = at[i] * dG;
+            }
+            dkk[r * dk + i] = gk;
+            dal[r * dk + i] = ga;
+        }
+    }
+    if (dh0)
+        for (size_t e = 0; e < nn; ++e) dh0[sidx + e] = D[e];
+    free(S); free(D); free(G); free(vec);
+    return 0;
+}
+
+/* The backward of ckda_oracle_fwd: gradients of L = sum <o, do> + <hT, dhT>
+ * (dhT may be NULL: zero) with respect to q, k, v, alpha, beta ([.., T, .]
+ * layouts as the forward) and h0 (dh0 may be NULL: not stored). */
+int ckda_oracle_bwd(const double *q, const double *k, const double *v, const double *alpha,
+                    const double *beta, const double *h0, const double *dout,
+                    const double *dhT, double *dq, double *dkk, double *dvv, double *dal,
+                    double *dbe, double *dh0, const int32_t *cu_seqlens, int num_seqs,
+                    int B, int H, int T, int dk, int dv, double scale, int nthreads)
+{
+    if (!q || !k || !v || !alpha || !beta || !dout || !dq || !dkk || !dvv || !dal || !dbe)
+        return -1;
+    if (B < 1 || H < 1 || T < 0 || dk < 1 || dv < 1) return -1;
+    int N = B;
+    if (cu_seqlens) {
+        if (B != 1 || num_seqs < 1) return -1;
+        if (cu_seqlens[0] != 0 || cu_seqlens[num_seqs] != T) return -1;
+        for (int s = 0; s < num_seqs; ++s)
+            if (cu_seqlens[s + 1] < cu_seqlens[s]) return -1;
+        N = num_seqs;
+    }
+    long pairs = (long)N * H;
+    int fail = 0;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : fail)
+#endif
+    for (long pp = 0; pp < pairs; ++pp) {
+        int n = (int)(pp / H), h = (int)(pp % H);
+        int t0 = cu_seqlens ? cu_seqlens[n] : 0;
+        int len = cu_seqlens ? cu_seqlens[n + 1] - cu_seqlens[n] : T;
+        long row0 = cu_seqlens ? (long)h * T + t0 : ((long)n * H + h) * T;
+        size_t sidx = ((size_t)n * H + h) * (size_t)dk * dv;
+        fail |= ckda_pair_bwd(q, k, v, alpha, beta, h0, dout, dhT, dq, dkk, dvv, dal, dbe, dh0,
+                              row0, len, dk, dv, scale, sidx) != 0;
+    }
+    (void)nthreads;
+    return fail ? -2 : 0;
+}
+
 /* Input preparation, per token (row) of dk channels, in the paper's
  * parameterisation ("Complex KDA" discussion slides, backup frame "practical
  * gates differ from exact theoretical endpoints"; paper App. E-G.1):

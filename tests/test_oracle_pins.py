@@ -542,3 +542,109 @@ def test_prep_unit_keys():
     np.testing.assert_array_equal(qc, q)
     _, kz, _, _ = oracle.prep(np.zeros((1, 8)), np.zeros((1, 8)), np.zeros(1))
     assert np.all(kz == 0.0)
+
+
+# ------------------------------------------------------------------ backward
+# The backward is pinned to the forward oracle (itself pinned above) by
+# central finite differences of L = sum_t <o_t, do_t> + <hT, dhT>: a wrong
+# sign, a dropped term or a transposed operand anywhere in the reverse steps
+# moves some gradient by O(1) relative, far outside the O(h^2) difference
+# error.
+
+def _loss(x, do, dhT, scale):
+    o, hT = oracle.fwd(x["q"], x["k"], x["v"], x["alpha"], x["beta"], x["h0"],
+                       cu_seqlens=x.get("cu"), scale=scale)
+    return float(np.sum(o * do) + np.sum(hT * dhT))
+
+
+def _fd_case(seed, B=1, H=2, T=7, dk=3, dv=2, special=False, cu=None):
+    rng = np.random.default_rng(seed)
+    x = {"q": rng.normal(size=(B, H, T, dk)), "k": rng.normal(size=(B, H, T, dk)),
+         "v": rng.normal(size=(B, H, T, dv)), "alpha": rng.uniform(-1, 1, (B, H, T, dk)),
+         "beta": rng.uniform(0, 2, (B, H, T)), "h0": None}
+    x["k"] /= np.linalg.norm(x["k"], axis=-1, keepdims=True)
+    N = B if cu is None else len(cu) - 1
+    x["h0"] = rng.normal(size=(N, H, dk, dv))
+    if cu is not None:
+        x["cu"] = np.asarray(cu, dtype=np.int32)
+    if special:
+        x["alpha"][..., 1, 0] = 0.0
+        x["alpha"][..., 3, :] = -1.0
+        x["beta"][..., 2] = 2.0
+        x["beta"][..., 4] = 0.0
+    do = rng.normal(size=(B, H, T, dv))
+    dhT = rng.normal(size=(N, H, dk, dv))
+    return x, do, dhT
+
+
+@pytest.mark.parametrize("special", [False, True])
+def test_bwd_matches_central_differences(special):
+    scale = 0.8
+    x, do, dhT = _fd_case(3 + special, special=special)
+    g = oracle.bwd(x["q"], x["k"], x["v"], x["alpha"], x["beta"], do, h0=x["h0"], dhT=dhT,
+                   scale=scale)
+    names = ["q", "k", "v", "alpha", "beta", "h0"]
+    h = 1e-6
+    for name, grad in zip(names, g):
+        base = x[name]
+        num = np.zeros_like(base)
+        it = np.nditer(base, flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            old = base[idx]
+            base[idx] = old + h
+            lp = _loss(x, do, dhT, scale)
+            base[idx] = old - h
+            lm = _loss(x, do, dhT, scale)
+            base[idx] = old
+            num[idx] = (lp - lm) / (2 * h)
+        err = np.max(np.abs(num - grad)) / max(np.max(np.abs(num)), 1e-12)
+        assert err < 1e-7, (name, err)
+
+
+def test_bwd_packed_matches_central_differences():
+    cu = [0, 3, 3, 7]
+    x, do, dhT = _fd_case(11, B=1, H=2, T=7, cu=cu)
+    g = oracle.bwd(x["q"], x["k"], x["v"], x["alpha"], x["beta"], do, h0=x["h0"], dhT=dhT,
+                   cu_seqlens=x["cu"])
+    h = 1e-6
+    for name, grad in zip(["k", "alpha", "h0"], (g[1], g[3], g[5])):
+        base = x[name]
+        num = np.zeros_like(base)
+        it = np.nditer(base, flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            old = base[idx]
+            base[idx] = old + h
+            lp = _loss(x, do, dhT, 1.0)
+            base[idx] = old - h
+            lm = _loss(x, do, dhT, 1.0)
+            base[idx] = old
+            num[idx] = (lp - lm) / (2 * h)
+        err = np.max(np.abs(num - grad)) / max(np.max(np.abs(num)), 1e-12)
+        assert err < 1e-7, (name, err)
+
+
+def test_bwd_closed_form_without_writes_or_decay():
+    """beta = 0 and alpha = 1: H_t = h0 for every t, o_t = h0^T (s q_t).  Then
+    dq_t = s h0 do_t, dh0 = s sum_t q_t do_t^T + dhT, dv = 0, dalpha_t,i =
+    sum_j D_t,ij (h0)_ij with D_t = dhT + s sum_{r >= t} q_r do_r^T."""
+    rng = np.random.default_rng(21)
+    T, n, dv, s = 5, 4, 3, 1.5
+    q = rng.normal(size=(1, 1, T, n))
+    k = rng.normal(size=(1, 1, T, n))
+    v = rng.normal(size=(1, 1, T, dv))
+    a = np.ones((1, 1, T, n))
+    b = np.zeros((1, 1, T))
+    h0 = rng.normal(size=(1, 1, n, dv))
+    do = rng.normal(size=(1, 1, T, dv))
+    dhT = rng.normal(size=(1, 1, n, dv))
+    dq, _, dvv, dal, _, dh0 = oracle.bwd(q, k, v, a, b, do, h0=h0, dhT=dhT, scale=s)
+    H0 = h0[0, 0]
+    for t in range(T):
+        np.testing.assert_allclose(dq[0, 0, t], s * H0 @ do[0, 0, t], rtol=1e-13)
+        D = dhT[0, 0] + s * sum(np.outer(q[0, 0, r], do[0, 0, r]) for r in range(t, T))
+        np.testing.assert_allclose(dal[0, 0, t], np.sum(D * H0, axis=1), rtol=1e-12, atol=1e-13)
+    np.testing.assert_array_equal(dvv, 0.0)
+    want = dhT[0, 0] + s * sum(np.outer(q[0, 0, t], do[0, 0, t]) for t in range(T))
+    np.testing.assert_allclose(dh0[0, 0], want, rtol=1e-12)
