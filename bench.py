@@ -16,6 +16,7 @@ so no flush is done between steps.  Prints ONE JSON line on rank 0 with:
   decode    the decode workload (B=256, H=32, 1000 chained steps): HBM GB/s
   prep      the fused input preparation (ckda_prep) on raw inputs of the
             KDA-range shape: HBM GB/s
+  bwd       the backward (ckda_bwd) on the KDA-range workload: token-heads/s
   workloads the full-CKDA, packed and dk = 64 KDA-range workloads (N=1):
             token-heads/s, roofline
   clocks    SM clocks and throttle reasons sampled during the timed region
@@ -335,6 +336,44 @@ def prep_case(ck, x, steps, warmup, ws, stream):
             "gpu_launches": steps}
 
 
+def bwd_bytes(B, H, T, dk, dv, io_bytes=2):
+    """Algorithmic bytes of ckda_bwd: q, k, alpha, v, do, beta in; dq, dk,
+    dalpha, dv, dbeta out (the states it stores and reads back are not)."""
+    return B * H * T * (6 * dk + 3 * dv + 2) * io_bytes
+
+
+def bwd_case(ck, x, steps, warmup, ws, stream):
+    import torch
+    d = x.to("cuda")
+    B, H, T, dk = d.q.shape
+    dv = d.v.shape[-1]
+    g = torch.Generator().manual_seed(31)
+    do = torch.randn(tuple(d.v.shape), generator=g).to(d.v.dtype).cuda()
+    need = ck.bwd_workspace_bytes(B, H, T, dk, dv)
+    wsp = torch.empty(max(need, 16), dtype=torch.uint8, device="cuda")
+
+    def step():
+        ck.bwd(d.q, d.k, d.v, d.alpha, d.beta, do, h0=d.h0, workspace=wsp, stream=stream)
+
+    total, per = time_steps(step, steps, warmup, ws, stream)
+    th = B * H * T
+    nbytes = bwd_bytes(B, H, T, dk, dv)
+    peak, src = hbm_peak()
+    ms = sum(per) / len(per)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    del wsp, do, d
+    return {"value": round(th * steps / total, 1), "unit": UNIT, "steps": steps,
+            "ms_per_step": round(total / steps * 1e3, 4), "token_heads": th,
+            "config": {"workload": "kda_range", "kernel": "token-serial, CUDA cores, fp32",
+                       "workspace_bytes": need},
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(gbs / peak, 4), "traffic": None,
+                         "algorithmic_bytes": nbytes, "mean_launch_ms": round(ms, 4),
+                         "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)"
+                         if src == "measured" else src},
+            "gpu_launches": steps}
+
+
 def cpu_baseline(x, target_s=12.0):
     """The oracle, as it stands, on a bounded sample of the workload's units."""
     import oracle
@@ -400,6 +439,8 @@ def run_ours(args):
         out["decode"] = decode_case(ck, args.decode_steps, 10, ws, stream)
     if ws == 1 and "prep" in extras:
         out["prep"] = prep_case(ck, x, 200, 10, ws, stream)
+    if ws == 1 and "bwd" in extras:
+        out["bwd"] = bwd_case(ck, x, 10, 3, ws, stream)
     if ws == 1 and any(e in extras for e in ("ckda_full", "ckda_varlen", "kda_range_dk64")):
         wl = {}
         for nm, steps in (("ckda_full", 20), ("ckda_varlen", 10), ("kda_range_dk64", 200)):
@@ -484,8 +525,8 @@ def main():
     ap.add_argument("--decode-steps", type=int, default=1000)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-extras", action="store_true")
-    ap.add_argument("--extras", default="decode,prep,ckda_full,ckda_varlen,kda_range_dk64",
-                    help="comma list of extra measurements: decode, prep, ckda_full, "
+    ap.add_argument("--extras", default="decode,prep,bwd,ckda_full,ckda_varlen,kda_range_dk64",
+                    help="comma list of extra measurements: decode, prep, bwd, ckda_full, "
                          "ckda_varlen, kda_range_dk64")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

@@ -20,7 +20,7 @@ import threading
 
 import torch
 
-__all__ = ["fwd", "fwd_host", "decode_step", "prep", "fwd_status", "workspace_bytes",
+__all__ = ["fwd", "fwd_host", "decode_step", "prep", "bwd", "bwd_workspace_bytes", "fwd_status", "workspace_bytes",
            "host_scratch_bytes", "selftest_timeout", "lib", "library_path", "CkdaError", "STATUS"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -73,6 +73,11 @@ def lib():
             L.ckda_selftest_timeout.argtypes = [vp, sz, ctypes.c_uint, vp]
             L.ckda_fwd_host_scratch_bytes.restype = sz
             L.ckda_fwd_host_scratch_bytes.argtypes = [i32, i32, i32, i32, i32, i32, i32]
+            L.ckda_bwd_workspace_bytes.restype = sz
+            L.ckda_bwd_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
+            L.ckda_bwd.restype = i32
+            L.ckda_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                   i32, i32, i32, i32, i32, i32, i32, f32, vp, sz, vp]
             L.ckda_prep.restype = i32
             L.ckda_prep.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_longlong, i32, i32,
                                     i32, f32, vp]
@@ -309,3 +314,45 @@ def prep(k_raw, a_raw, b_raw, q_raw=None, normalize_q=True, norm_eps=1e-6, out=N
     if rc != 0:
         raise CkdaError(rc, "ckda_prep")
     return q, k, alpha, beta
+
+
+def bwd_workspace_bytes(B, H, T, dk, dv) -> int:
+    return int(lib().ckda_bwd_workspace_bytes(B, H, T, dk, dv))
+
+
+def bwd(q, k, v, alpha, beta, do, h0=None, dhT=None, cu_seqlens=None, scale=1.0,
+        store_dh0=True, workspace=None, stream=None):
+    """Backward of fwd (ckda_bwd): gradients of sum <o, do> + <hT, dhT>.
+
+    Returns (dq, dk, dv, dalpha, dbeta, dh0 or None); dh0 is fp32."""
+    L = lib()
+    device = q.device
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    dt = q.dtype
+    _io_dtype(q)
+    for name, t, shp in (("q", q, (B, H, T, dk)), ("k", k, (B, H, T, dk)),
+                         ("alpha", alpha, (B, H, T, dk)), ("v", v, (B, H, T, dv)),
+                         ("do", do, (B, H, T, dv)), ("beta", beta, (B, H, T))):
+        _check(t, name, dt, shp, device)
+    N = B
+    if cu_seqlens is not None:
+        N = cu_seqlens.numel() - 1
+        _check(cu_seqlens, "cu_seqlens", torch.int32, (N + 1,), device)
+    for name, t in (("h0", h0), ("dhT", dhT)):
+        if t is not None:
+            _check(t, name, torch.float32, (N, H, dk, dv), device)
+    need = bwd_workspace_bytes(B, H, T, dk, dv)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=device)
+    dq, dkk, dal = torch.empty_like(q), torch.empty_like(k), torch.empty_like(alpha)
+    dvv, dbe = torch.empty_like(v), torch.empty_like(beta)
+    dh0 = torch.empty((N, H, dk, dv), dtype=torch.float32, device=device) if store_dh0 else None
+    rc = L.ckda_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(h0), _ptr(do),
+                    _ptr(dhT), _ptr(dq), _ptr(dkk), _ptr(dvv), _ptr(dal), _ptr(dbe), _ptr(dh0),
+                    _ptr(cu_seqlens), int(N if cu_seqlens is not None else 0), B, H, T, dk, dv,
+                    _io_dtype(q), float(scale), _ptr(workspace), int(workspace.numel()),
+                    _stream_handle(stream, device))
+    if rc != 0:
+        raise CkdaError(rc, "ckda_bwd")
+    return dq, dkk, dvv, dal, dbe, dh0

@@ -205,6 +205,44 @@ ckda_status ckda_decode_step(const void *q, const void *k, const void *v,
                              ckda_dtype io_dtype, float scale, void *stream);
 
 /*
+ * Backward of ckda_fwd: gradients of L = sum_t <o_t, do_t> + <hT, dhT> with
+ * respect to q, k, v, alpha, beta and h0, by reverse-mode differentiation of
+ * the recurrence ("Complex KDA: Understanding and Enhancing the Expressivity
+ * of Kimi Delta Attention", Sec. 2 Eq. (1) and App. B.2 Eq. (9); the paper's
+ * Fig. 5 times forward and backward together).  Per token, with
+ * G = Diag(alpha) S, p = G^T k, u = beta (v - p), S' = G + k u^T and
+ * D = dL/dS' (from dhT):
+ *   D += (scale q) do^T;  du = D^T k;  dv = beta du;  dbeta = <du, v - p>;
+ *   dp = -beta du;  dk = D u + G dp;  dalpha_i = sum_j (D + k dp^T)_ij S_ij;
+ *   D <- Diag(alpha)(D + k dp^T);  dq = scale S' do;  dh0 = the final D.
+ *
+ *   q, k, alpha, d_q, d_k, d_alpha : io [B, H, T, dk]
+ *   v, d_o, d_v                    : io [B, H, T, dv]
+ *   beta, d_beta                   : io [B, H, T]
+ *   h0, d_hT, d_h0                 : fp32 [N, H, dk, dv]  (N as in ckda_fwd)
+ *   cu_seqlens / num_seqs          : as in ckda_fwd (packed sequences, B = 1)
+ *
+ * h0 == NULL: zero initial state.  d_hT == NULL: no gradient on the final
+ * state.  d_h0 == NULL: not stored.  Gradient buffers must not alias inputs.
+ * Any dk, dv <= 128 and either I/O dtype; arithmetic is fp32, token by token
+ * on CUDA cores (one block per (sequence, head)): pass 1 reruns the forward
+ * and stores the state before every token in `workspace`, pass 2 walks the
+ * tokens in reverse.  workspace: device memory of at least
+ * ckda_bwd_workspace_bytes(B, H, T, dk, dv) bytes (B*H*T*dk*dv*4; with packed
+ * input B = 1 and T = the total length), 16-byte aligned, owned by the
+ * caller; its contents are scratch.  Argument errors return synchronously
+ * with nothing launched; otherwise CKDA_OK once enqueued on `stream`.  The
+ * library allocates nothing.
+ */
+size_t ckda_bwd_workspace_bytes(int B, int H, int T, int dk, int dv);
+ckda_status ckda_bwd(const void *q, const void *k, const void *v, const void *alpha,
+                     const void *beta, const float *h0, const void *d_o, const float *d_hT,
+                     void *d_q, void *d_k, void *d_v, void *d_alpha, void *d_beta,
+                     float *d_h0, const int32_t *cu_seqlens, int num_seqs, int B, int H,
+                     int T, int dk, int dv, ckda_dtype io_dtype, float scale,
+                     void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Input preparation, fused into one pass over HBM: the gate
  * parameterisation of "Complex KDA" (discussion slides, backup frame
  * "practical gates differ from exact theoretical endpoints"; paper App.

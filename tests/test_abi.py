@@ -97,6 +97,29 @@ def test_decode_argument_errors_are_synchronous(L):
     assert f(io=3) == 1
 
 
+def test_bwd_argument_errors_are_synchronous(L):
+    vp = ctypes.c_void_p
+    names = ("q", "k", "v", "alpha", "beta", "h0", "do", "dhT", "dq", "dk", "dv", "dalpha",
+             "dbeta", "dh0", "cu")
+
+    def f(**kw):
+        ptrs = [vp(kw.get(n, 256 if n not in ("h0", "dhT", "dh0", "cu") else None))
+                for n in names]
+        return L.ckda_bwd(*ptrs, kw.get("nseq", 0), kw.get("B", 1), kw.get("H", 1),
+                          kw.get("T", 4), kw.get("dk", 16), kw.get("dv", 16), kw.get("io", 0),
+                          ctypes.c_float(1.0), vp(kw.get("ws", 256)),
+                          ctypes.c_size_t(kw.get("wsb", 1 << 20)), vp(None))
+    assert f(q=None) == 1
+    assert f(dalpha=None) == 1
+    assert f(B=0) == 1
+    assert f(dk=129) == 2
+    assert f(io=3) == 1
+    assert f(cu=256, B=2, nseq=2) == 1      # packed input needs B == 1
+    assert f(wsb=100) == 5                   # workspace smaller than B*H*T*dk*dv*4
+    assert f(ws=8) == 5                      # misaligned workspace
+    assert L.ckda_bwd_workspace_bytes(2, 3, 5, 16, 8) == 2 * 3 * 5 * 16 * 8 * 4
+
+
 def test_prep_argument_errors_are_synchronous(L):
     vp = ctypes.c_void_p
     names = ("q_raw", "k_raw", "a_raw", "b_raw", "q", "k", "alpha", "beta")
