@@ -69,6 +69,7 @@ KERNEL_SOURCES = {
     "fwd_chunk": ["ckda_chunk.cu", "sm103.cuh", "ckda_internal.cuh"],
     "decode128": ["ckda_decode.cu", "ckda_internal.cuh"],
     "prep": ["ckda_prep.cu", "ckda_internal.cuh"],
+    "bwd": ["ckda_bwd.cu", "ckda_internal.cuh"],
 }
 
 
@@ -342,8 +343,16 @@ def bwd_bytes(B, H, T, dk, dv, io_bytes=2):
     return B * H * T * (6 * dk + 3 * dv + 2) * io_bytes
 
 
-def bwd_case(ck, x, steps, warmup, ws, stream):
+def bwd_case(ck, x, steps, warmup, ws, stream, units=0):
+    """ckda_bwd on the workload (or, with units > 0, on its first `units`
+    (batch, head) pairs: a smaller workspace, the same per-unit work)."""
     import torch
+    import synth
+    if units > 0:
+        B0, H0 = x.q.shape[:2]
+        nb, nh = max(1, units // H0), min(units, H0)
+        sl = lambda t: None if t is None else t[:nb, :nh].contiguous()
+        x = synth.FwdInputs(sl(x.q), sl(x.k), sl(x.v), sl(x.alpha), sl(x.beta), sl(x.h0), None)
     d = x.to("cuda")
     B, H, T, dk = d.q.shape
     dv = d.v.shape[-1]
@@ -364,10 +373,11 @@ def bwd_case(ck, x, steps, warmup, ws, stream):
     del wsp, do, d
     return {"value": round(th * steps / total, 1), "unit": UNIT, "steps": steps,
             "ms_per_step": round(total / steps * 1e3, 4), "token_heads": th,
-            "config": {"workload": "kda_range", "kernel": "token-serial, CUDA cores, fp32",
-                       "workspace_bytes": need},
+            "config": {"workload": "kda_range" if units <= 0 else f"kda_range, {B * H} units",
+                       "kernel": "token-serial, CUDA cores, fp32", "workspace_bytes": need},
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
-                         "frac": round(gbs / peak, 4), "traffic": None,
+                         "frac": round(gbs / peak, 4),
+                         "traffic": traffic_for("bwd", "kda_range") if units <= 0 else None,
                          "algorithmic_bytes": nbytes, "mean_launch_ms": round(ms, 4),
                          "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)"
                          if src == "measured" else src},
@@ -440,7 +450,7 @@ def run_ours(args):
     if ws == 1 and "prep" in extras:
         out["prep"] = prep_case(ck, x, 200, 10, ws, stream)
     if ws == 1 and "bwd" in extras:
-        out["bwd"] = bwd_case(ck, x, 10, 3, ws, stream)
+        out["bwd"] = bwd_case(ck, x, 10, 3, ws, stream, units=args.bwd_units)
     if ws == 1 and any(e in extras for e in ("ckda_full", "ckda_varlen", "kda_range_dk64")):
         wl = {}
         for nm, steps in (("ckda_full", 20), ("ckda_varlen", 10), ("kda_range_dk64", 200)):
@@ -529,6 +539,8 @@ def main():
                     help="comma list of extra measurements: decode, prep, bwd, ckda_full, "
                          "ckda_varlen, kda_range_dk64")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--bwd-units", type=int, default=0,
+                    help="run the bwd extra on the first N (batch, head) units only")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

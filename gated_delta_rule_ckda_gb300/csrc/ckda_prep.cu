@@ -60,34 +60,49 @@ __device__ __forceinline__ uint32_t bf_pack(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// bf16, dk = 128: lane l owns channels 4l .. 4l + 3 (8-byte accesses).
+// bf16, dk = 128: lane l owns channels 4l .. 4l + 3 (8-byte accesses); each
+// warp takes kRows rows and issues all their loads before using any.
+constexpr int kRows = 2;
 __global__ void __launch_bounds__(256) prep128_bf16_kernel(const PrepArgs a) {
   const int lane = threadIdx.x & 31;
-  const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (row >= a.rows) return;
-  const size_t off = (size_t)row * 32 + lane;  // in uint2 units
-  const uint2 kw = static_cast<const uint2*>(a.k_raw)[off];
-  const uint2 aw = static_cast<const uint2*>(a.a_raw)[off];
-  uint2 qw = make_uint2(0u, 0u);
-  if (a.q_raw) qw = static_cast<const uint2*>(a.q_raw)[off];
-  float b = 0.f;
-  if (lane == 0) b = __bfloat162float(static_cast<const __nv_bfloat16*>(a.b_raw)[row]);
-
-  const float k0 = bf_lo(kw.x), k1 = bf_hi(kw.x), k2 = bf_lo(kw.y), k3 = bf_hi(kw.y);
-  const float ik = rsqrtf(warp_sum(k0 * k0 + k1 * k1 + k2 * k2 + k3 * k3) + a.norm_eps);
-  static_cast<uint2*>(a.k)[off] = make_uint2(bf_pack(k0 * ik, k1 * ik), bf_pack(k2 * ik, k3 * ik));
-  if (a.q_raw) {
-    const float q0 = bf_lo(qw.x), q1 = bf_hi(qw.x), q2 = bf_lo(qw.y), q3 = bf_hi(qw.y);
-    float iq = 1.f;
-    if (a.normalize_q) iq = rsqrtf(warp_sum(q0 * q0 + q1 * q1 + q2 * q2 + q3 * q3) + a.norm_eps);
-    static_cast<uint2*>(a.q)[off] =
-        make_uint2(bf_pack(q0 * iq, q1 * iq), bf_pack(q2 * iq, q3 * iq));
+  const long long row_base = ((long long)blockIdx.x * 8 + (threadIdx.x >> 5)) * kRows;
+  uint2 kw[kRows], aw[kRows], qw[kRows];
+  float b[kRows];
+#pragma unroll
+  for (int e = 0; e < kRows; ++e) {
+    const long long row = row_base + e;
+    kw[e] = aw[e] = qw[e] = make_uint2(0u, 0u);
+    b[e] = 0.f;
+    if (row < a.rows) {
+      const size_t off = (size_t)row * 32 + lane;  // in uint2 units
+      kw[e] = static_cast<const uint2*>(a.k_raw)[off];
+      aw[e] = static_cast<const uint2*>(a.a_raw)[off];
+      if (a.q_raw) qw[e] = static_cast<const uint2*>(a.q_raw)[off];
+      if (lane == 0) b[e] = __bfloat162float(static_cast<const __nv_bfloat16*>(a.b_raw)[row]);
+    }
   }
-  static_cast<uint2*>(a.alpha)[off] =
-      make_uint2(bf_pack(gate_alpha(bf_lo(aw.x)), gate_alpha(bf_hi(aw.x))),
-                 bf_pack(gate_alpha(bf_lo(aw.y)), gate_alpha(bf_hi(aw.y))));
-  if (lane == 0)
-    static_cast<__nv_bfloat16*>(a.beta)[row] = __float2bfloat16_rn(gate_beta(b));
+#pragma unroll
+  for (int e = 0; e < kRows; ++e) {
+    const long long row = row_base + e;
+    if (row >= a.rows) break;  // warp-uniform
+    const size_t off = (size_t)row * 32 + lane;
+    const float k0 = bf_lo(kw[e].x), k1 = bf_hi(kw[e].x), k2 = bf_lo(kw[e].y), k3 = bf_hi(kw[e].y);
+    const float ik = rsqrtf(warp_sum(k0 * k0 + k1 * k1 + k2 * k2 + k3 * k3) + a.norm_eps);
+    static_cast<uint2*>(a.k)[off] =
+        make_uint2(bf_pack(k0 * ik, k1 * ik), bf_pack(k2 * ik, k3 * ik));
+    if (a.q_raw) {
+      const float q0 = bf_lo(qw[e].x), q1 = bf_hi(qw[e].x), q2 = bf_lo(qw[e].y), q3 = bf_hi(qw[e].y);
+      float iq = 1.f;
+      if (a.normalize_q) iq = rsqrtf(warp_sum(q0 * q0 + q1 * q1 + q2 * q2 + q3 * q3) + a.norm_eps);
+      static_cast<uint2*>(a.q)[off] =
+          make_uint2(bf_pack(q0 * iq, q1 * iq), bf_pack(q2 * iq, q3 * iq));
+    }
+    static_cast<uint2*>(a.alpha)[off] =
+        make_uint2(bf_pack(gate_alpha(bf_lo(aw[e].x)), gate_alpha(bf_hi(aw[e].x))),
+                   bf_pack(gate_alpha(bf_lo(aw[e].y)), gate_alpha(bf_hi(aw[e].y))));
+    if (lane == 0)
+      static_cast<__nv_bfloat16*>(a.beta)[row] = __float2bfloat16_rn(gate_beta(b[e]));
+  }
 }
 
 // Any dk <= 128 and either I/O dtype: lane l owns channels l, l + 32, ...
@@ -155,7 +170,7 @@ extern "C" ckda_status ckda_prep(const void* q_raw, const void* k_raw, const voi
                         static_cast<const void*>(alpha)})
     if (p && (reinterpret_cast<uintptr_t>(p) & 7) != 0) vec = false;
   if (vec)
-    prep128_bf16_kernel<<<blocks, 256, 0, s>>>(a);
+    prep128_bf16_kernel<<<(unsigned)((rows + 8 * kRows - 1) / (8 * kRows)), 256, 0, s>>>(a);
   else if (io_dtype == CKDA_BF16)
     prep_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(a);
   else
