@@ -74,7 +74,7 @@ def lib():
             L.ckda_fwd_host_scratch_bytes.restype = sz
             L.ckda_fwd_host_scratch_bytes.argtypes = [i32, i32, i32, i32, i32, i32, i32]
             L.ckda_bwd_workspace_bytes.restype = sz
-            L.ckda_bwd_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
+            L.ckda_bwd_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
             L.ckda_bwd.restype = i32
             L.ckda_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                    i32, i32, i32, i32, i32, i32, i32, f32, vp, sz, vp]
@@ -316,8 +316,8 @@ def prep(k_raw, a_raw, b_raw, q_raw=None, normalize_q=True, norm_eps=1e-6, out=N
     return q, k, alpha, beta
 
 
-def bwd_workspace_bytes(B, H, T, dk, dv) -> int:
-    return int(lib().ckda_bwd_workspace_bytes(B, H, T, dk, dv))
+def bwd_workspace_bytes(B, H, T, dk, dv, num_seqs=0) -> int:
+    return int(lib().ckda_bwd_workspace_bytes(num_seqs, B, H, T, dk, dv))
 
 
 def bwd(q, k, v, alpha, beta, do, h0=None, dhT=None, cu_seqlens=None, scale=1.0,
@@ -342,7 +342,7 @@ def bwd(q, k, v, alpha, beta, do, h0=None, dhT=None, cu_seqlens=None, scale=1.0,
     for name, t in (("h0", h0), ("dhT", dhT)):
         if t is not None:
             _check(t, name, torch.float32, (N, H, dk, dv), device)
-    need = bwd_workspace_bytes(B, H, T, dk, dv)
+    need = bwd_workspace_bytes(B, H, T, dk, dv, N if cu_seqlens is not None else 0)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=device)
     dq, dkk, dal = torch.empty_like(q), torch.empty_like(k), torch.empty_like(alpha)

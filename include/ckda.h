@@ -226,15 +226,18 @@ ckda_status ckda_decode_step(const void *q, const void *k, const void *v,
  * state.  d_h0 == NULL: not stored.  Gradient buffers must not alias inputs.
  * Any dk, dv <= 128 and either I/O dtype; arithmetic is fp32, token by token
  * on CUDA cores (one block per (sequence, head)): pass 1 reruns the forward
- * and stores the state before every token in `workspace`, pass 2 walks the
- * tokens in reverse.  workspace: device memory of at least
- * ckda_bwd_workspace_bytes(B, H, T, dk, dv) bytes (B*H*T*dk*dv*4; with packed
- * input B = 1 and T = the total length), 16-byte aligned, owned by the
- * caller; its contents are scratch.  Argument errors return synchronously
+ * and keeps the state before every 64th token in `workspace`; pass 2 takes
+ * the 64-token chunks in reverse, recomputing each one's states from its
+ * checkpoint and walking it backward.  workspace: device memory of at least
+ * ckda_bwd_workspace_bytes(num_seqs, B, H, T, dk, dv) bytes (num_seqs = 0
+ * for dense input): dk*dv*4 bytes for each checkpoint (ceil(T/64) per dense
+ * (batch, head), ceil(T/64) + num_seqs per head when packed) and 64 more
+ * tiles per (sequence, head) for the chunk being walked; 16-byte aligned,
+ * owned by the caller; its contents are scratch.  Argument errors return synchronously
  * with nothing launched; otherwise CKDA_OK once enqueued on `stream`.  The
  * library allocates nothing.
  */
-size_t ckda_bwd_workspace_bytes(int B, int H, int T, int dk, int dv);
+size_t ckda_bwd_workspace_bytes(int num_seqs, int B, int H, int T, int dk, int dv);
 ckda_status ckda_bwd(const void *q, const void *k, const void *v, const void *alpha,
                      const void *beta, const float *h0, const void *d_o, const float *d_hT,
                      void *d_q, void *d_k, void *d_v, void *d_alpha, void *d_beta,

@@ -115,9 +115,13 @@ def test_bwd_argument_errors_are_synchronous(L):
     assert f(dk=129) == 2
     assert f(io=3) == 1
     assert f(cu=256, B=2, nseq=2) == 1      # packed input needs B == 1
-    assert f(wsb=100) == 5                   # workspace smaller than B*H*T*dk*dv*4
+    assert f(wsb=100) == 5                   # workspace smaller than needed
     assert f(ws=8) == 5                      # misaligned workspace
-    assert L.ckda_bwd_workspace_bytes(2, 3, 5, 16, 8) == 2 * 3 * 5 * 16 * 8 * 4
+    tile = 16 * 8 * 4
+    # dense: ceil(T/64) checkpoints and 64 chunk tiles per (batch, head)
+    assert L.ckda_bwd_workspace_bytes(0, 2, 3, 130, 16, 8) == 2 * 3 * (3 + 64) * tile
+    # packed: ceil(T/64) + num_seqs checkpoints per head, 64 chunk tiles per (sequence, head)
+    assert L.ckda_bwd_workspace_bytes(5, 1, 3, 130, 16, 8) == (3 * (3 + 5) + 5 * 3 * 64) * tile
 
 
 def test_prep_argument_errors_are_synchronous(L):

@@ -119,3 +119,20 @@ def test_bwd_kda_range_workload_sampled(ck):
         ref = oracle.bwd(sl(x.q), sl(x.k), sl(x.v), sl(x.alpha), sl(x.beta), sl(do))
         got = [g[b:b + 1, h:h + 1] for g in gpu[:5]] + [gpu[5][b:b + 1, h:h + 1]]
         check(got, ref, True, f"kda_range b={b} h={h}")
+
+
+def test_bwd_ckda_varlen_workload_sampled(ck):
+    """The packed workload at full size (64 sequences, 8.26 M token-heads) on
+    the GPU; the oracle, which keeps every state of a pair, on the three
+    shortest sequences (their gradients, and dh0 through dhT = 0)."""
+    x = synth.make_workload("ckda_varlen")
+    do, _ = grads_case(x, 660, dhT_on=False)
+    gpu = run(ck, x, do, None, 1.0)
+    cu = x.cu_seqlens.numpy()
+    lens = np.diff(cu)
+    for s in np.argsort(lens, kind="stable")[:3]:
+        a0, b0 = int(cu[s]), int(cu[s + 1])
+        sl = lambda t: t[:, :, a0:b0]
+        ref = oracle.bwd(sl(x.q), sl(x.k), sl(x.v), sl(x.alpha), sl(x.beta), sl(do))
+        got = [g[:, :, a0:b0] for g in gpu[:5]] + [gpu[5][s:s + 1]]
+        check(got, ref, True, f"varlen seq {s} L={b0 - a0}")
