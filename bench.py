@@ -14,6 +14,7 @@ so no flush is done between steps.  Prints ONE JSON line on rank 0 with:
             timed region
   cpu_baseline  the fp64 CPU oracle timed on a bounded sample (rank 0, N=1)
   decode    the decode workload (B=256, H=32, 1000 chained steps): HBM GB/s
+  decode_raw  the same through the step with the input preparation fused in
   prep      the fused input preparation (ckda_prep) on raw inputs of the
             KDA-range shape: HBM GB/s
   bwd       the backward (ckda_bwd) on the KDA-range workload: token-heads/s
@@ -271,7 +272,9 @@ def e2e_fwd(ck, x, steps, ws, stream):
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps}
 
 
-def decode_case(ck, steps, warmup, ws, stream, pool=32):
+def decode_case(ck, steps, warmup, ws, stream, pool=32, raw=False):
+    """The decode workload; with raw=True through ckda_decode_step_raw (the
+    same seeded tensors read as raw q, k and gate logits: the same bytes)."""
     import torch
     import synth
     w = synth.WORKLOADS["ckda_decode"]
@@ -285,11 +288,16 @@ def decode_case(ck, steps, warmup, ws, stream, pool=32):
     def step():
         q, k, v, a, b = ins[it[0] % pool]
         it[0] += 1
-        ck.decode_step(q, k, v, a, b, S, o=o, stream=stream)
+        if raw:
+            ck.decode_step_raw(q, k, v, a, b, S, o=o, stream=stream)
+        else:
+            ck.decode_step(q, k, v, a, b, S, o=o, stream=stream)
 
     total, per = time_steps(step, steps, warmup, ws, stream)
     nbytes = decode_bytes(B, H, d, d)
     rl = roofline(nbytes, per, "decode128", "ckda_decode")
+    if raw:
+        rl["traffic"] = None  # the recorded capture is of the plain step
     return {"value": round(ws * nbytes * steps / total / 1e9, 1), "unit": "GB/s",
             "steps": steps, "ms_per_step": round(total / steps * 1e3, 4),
             "config": {"workload": "ckda_decode", "B": B, "H": H, "d": d,
@@ -447,6 +455,8 @@ def run_ours(args):
     extras = [] if args.no_extras else [e for e in args.extras.split(",") if e and e != "none"]
     if ws == 1 and "decode" in extras:
         out["decode"] = decode_case(ck, args.decode_steps, 10, ws, stream)
+    if ws == 1 and "decode_raw" in extras:
+        out["decode_raw"] = decode_case(ck, args.decode_steps, 10, ws, stream, raw=True)
     if ws == 1 and "prep" in extras:
         out["prep"] = prep_case(ck, x, 200, 10, ws, stream)
     if ws == 1 and "bwd" in extras:
@@ -535,9 +545,10 @@ def main():
     ap.add_argument("--decode-steps", type=int, default=1000)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-extras", action="store_true")
-    ap.add_argument("--extras", default="decode,prep,bwd,ckda_full,ckda_varlen,kda_range_dk64",
-                    help="comma list of extra measurements: decode, prep, bwd, ckda_full, "
-                         "ckda_varlen, kda_range_dk64")
+    ap.add_argument("--extras",
+                    default="decode,decode_raw,prep,bwd,ckda_full,ckda_varlen,kda_range_dk64",
+                    help="comma list of extra measurements: decode, decode_raw, prep, bwd, "
+                         "ckda_full, ckda_varlen, kda_range_dk64")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--bwd-units", type=int, default=0,
                     help="run the bwd extra on the first N (batch, head) units only")

@@ -20,7 +20,7 @@ import threading
 
 import torch
 
-__all__ = ["fwd", "fwd_host", "decode_step", "prep", "bwd", "bwd_workspace_bytes", "fwd_status", "workspace_bytes",
+__all__ = ["fwd", "fwd_host", "decode_step", "decode_step_raw", "prep", "bwd", "bwd_workspace_bytes", "fwd_status", "workspace_bytes",
            "host_scratch_bytes", "selftest_timeout", "lib", "library_path", "CkdaError", "STATUS"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -73,6 +73,9 @@ def lib():
             L.ckda_selftest_timeout.argtypes = [vp, sz, ctypes.c_uint, vp]
             L.ckda_fwd_host_scratch_bytes.restype = sz
             L.ckda_fwd_host_scratch_bytes.argtypes = [i32, i32, i32, i32, i32, i32, i32]
+            L.ckda_decode_step_raw.restype = i32
+            L.ckda_decode_step_raw.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
+                                               i32, f32, i32, f32, vp]
             L.ckda_bwd_workspace_bytes.restype = sz
             L.ckda_bwd_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
             L.ckda_bwd.restype = i32
@@ -356,3 +359,29 @@ def bwd(q, k, v, alpha, beta, do, h0=None, dhT=None, cu_seqlens=None, scale=1.0,
     if rc != 0:
         raise CkdaError(rc, "ckda_bwd")
     return dq, dkk, dvv, dal, dbe, dh0
+
+
+def decode_step_raw(q_raw, k_raw, v, a_raw, b_raw, state, scale=1.0, normalize_q=True,
+                    norm_eps=1e-6, o=None, stream=None):
+    """One decode step on raw inputs with the input preparation fused in
+    (ckda_decode_step_raw): unit-norm k (and q), alpha and beta from the gate
+    logits a and b.  state [B, H, 128, 128] fp32 is updated in place; returns o."""
+    L = lib()
+    device = q_raw.device
+    B, H, dk = q_raw.shape
+    dv = v.shape[-1]
+    dt = q_raw.dtype
+    for name, t, shp in (("q_raw", q_raw, (B, H, dk)), ("k_raw", k_raw, (B, H, dk)),
+                         ("a_raw", a_raw, (B, H, dk)), ("v", v, (B, H, dv)),
+                         ("b_raw", b_raw, (B, H))):
+        _check(t, name, dt, shp, device)
+    _check(state, "state", torch.float32, (B, H, dk, dv), device)
+    if o is None:
+        o = torch.empty((B, H, dv), dtype=dt, device=device)
+    rc = L.ckda_decode_step_raw(_ptr(q_raw), _ptr(k_raw), _ptr(v), _ptr(a_raw), _ptr(b_raw),
+                                _ptr(state), _ptr(o), B, H, dk, dv, _io_dtype(q_raw),
+                                float(scale), int(bool(normalize_q)), float(norm_eps),
+                                _stream_handle(stream, device))
+    if rc != 0:
+        raise CkdaError(rc, "ckda_decode_step_raw")
+    return o

@@ -173,6 +173,29 @@ ckda_status ckda_decode_step(const void* q, const void* k, const void* v, const 
                                                                              : CKDA_ERR_CUDA;
 }
 
+ckda_status ckda_decode_step_raw(const void* q_raw, const void* k_raw, const void* v,
+                                 const void* a_raw, const void* b_raw, float* state, void* o,
+                                 int B, int H, int dk, int dv, ckda_dtype io_dtype, float scale,
+                                 int normalize_q, float norm_eps, void* stream) {
+  if (io_dtype != CKDA_F32 && io_dtype != CKDA_BF16) return CKDA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || dk < 1 || dv < 1) return CKDA_ERR_INVALID_ARG;
+  if (!q_raw || !k_raw || !v || !a_raw || !b_raw || !state || !o) return CKDA_ERR_INVALID_ARG;
+  if (!(scale == scale)) return CKDA_ERR_INVALID_ARG;
+  if (!(norm_eps >= 0.f) || norm_eps > 3.0e38f) return CKDA_ERR_INVALID_ARG;
+  if (dk != 128 || dv != 128) return CKDA_ERR_UNSUPPORTED;
+  if ((long long)B * H > 0x7fffffffLL) return CKDA_ERR_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(state) & 15) != 0) return CKDA_ERR_INVALID_ARG;
+  DecodeArgs a{};
+  a.q = q_raw; a.k = k_raw; a.v = v; a.alpha = a_raw; a.beta = b_raw;
+  a.state = state; a.o = o;
+  a.B = B; a.H = H; a.dk = dk; a.dv = dv;
+  a.scale = scale; a.io = io_dtype;
+  return launch_decode_raw(a, normalize_q, norm_eps, static_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? CKDA_OK
+             : CKDA_ERR_CUDA;
+}
+
 ckda_status ckda_selftest_timeout(void* workspace, size_t workspace_bytes, unsigned int spin_limit,
                                   void* stream) {
   if (!workspace || workspace_bytes < kWsStatusBytes) return CKDA_ERR_WORKSPACE;

@@ -21,11 +21,17 @@
 namespace ckda {
 namespace {
 
-template <typename IO>
-__global__ void __launch_bounds__(256, 2) decode128_kernel(DecodeArgs a) {
+// RAW: the token inputs are raw (q and k not normalised, a and b the gate
+// logits), and the step first applies the input preparation of ckda_prep to
+// them (unit-norm k, and q when normalize_q; alpha and beta from the logits).
+// A separate instance, so that the plain step carries none of it.
+template <typename IO, bool RAW>
+__global__ void __launch_bounds__(256, 2) decode128_kernel(DecodeArgs a, int normalize_q,
+                                                           float norm_eps) {
   __shared__ float s_ak[128], s_a[128], s_k[128], s_q[128], s_v[128];
   __shared__ float4 s_red[8][32];
   __shared__ float s_beta;
+  __shared__ float s_norm[2][4];
   const int p = blockIdx.x;  // (batch, head)
   const int tid = threadIdx.x, g = tid >> 5, c = tid & 31;
   float4* S = reinterpret_cast<float4*>(a.state + (size_t)p * 128 * 128);
@@ -38,17 +44,52 @@ __global__ void __launch_bounds__(256, 2) decode128_kernel(DecodeArgs a) {
   const IO* k = static_cast<const IO*>(a.k) + (size_t)p * 128;
   const IO* al = static_cast<const IO*>(a.alpha) + (size_t)p * 128;
   const IO* v = static_cast<const IO*>(a.v) + (size_t)p * 128;
-  if (tid < 128) {
-    float av = ld_io(al + tid), kv = ld_io(k + tid);
-    s_a[tid] = av;
-    s_k[tid] = kv;
-    s_ak[tid] = av * kv;
-    s_q[tid] = a.scale * ld_io(q + tid);
+  if (!RAW) {
+    if (tid < 128) {
+      float av = ld_io(al + tid), kv = ld_io(k + tid);
+      s_a[tid] = av;
+      s_k[tid] = kv;
+      s_ak[tid] = av * kv;
+      s_q[tid] = a.scale * ld_io(q + tid);
+    } else {
+      s_v[tid - 128] = ld_io(v + (tid - 128));
+      if (tid == 128) s_beta = ld_io(static_cast<const IO*>(a.beta) + p);
+    }
+    __syncthreads();
   } else {
-    s_v[tid - 128] = ld_io(v + (tid - 128));
-    if (tid == 128) s_beta = ld_io(static_cast<const IO*>(a.beta) + p);
+    float kv = 0.f, qv = 0.f;
+    if (tid < 128) {
+      kv = ld_io(k + tid);
+      qv = ld_io(q + tid);
+      float sk = kv * kv, sq = qv * qv;
+#pragma unroll
+      for (int m = 16; m >= 1; m >>= 1) {
+        sk += __shfl_xor_sync(0xffffffffu, sk, m);
+        sq += __shfl_xor_sync(0xffffffffu, sq, m);
+      }
+      if (c == 0) {
+        s_norm[0][g] = sk;
+        s_norm[1][g] = sq;
+      }
+    } else {
+      s_v[tid - 128] = ld_io(v + (tid - 128));
+      if (tid == 128) s_beta = gate_beta(ld_io(static_cast<const IO*>(a.beta) + p));
+    }
+    __syncthreads();
+    if (tid < 128) {
+      const float ik = rsqrtf(s_norm[0][0] + s_norm[0][1] + s_norm[0][2] + s_norm[0][3] + norm_eps);
+      float iq = 1.f;
+      if (normalize_q)
+        iq = rsqrtf(s_norm[1][0] + s_norm[1][1] + s_norm[1][2] + s_norm[1][3] + norm_eps);
+      const float av = gate_alpha(ld_io(al + tid));
+      kv *= ik;
+      s_a[tid] = av;
+      s_k[tid] = kv;
+      s_ak[tid] = av * kv;
+      s_q[tid] = a.scale * (qv * iq);
+    }
+    __syncthreads();
   }
-  __syncthreads();
 
   // r = H^T (alpha * k), partial over this thread's 16 rows
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -115,9 +156,9 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
   if (units == 0) return cudaSuccess;
   if (a.dk == 128 && a.dv == 128) {
     if (a.io == CKDA_F32)
-      decode128_kernel<float><<<units, 256, 0, s>>>(a);
+      decode128_kernel<float, false><<<units, 256, 0, s>>>(a, 0, 0.f);
     else
-      decode128_kernel<__nv_bfloat16><<<units, 256, 0, s>>>(a);
+      decode128_kernel<__nv_bfloat16, false><<<units, 256, 0, s>>>(a, 0, 0.f);
     return cudaGetLastError();
   }
   // Other shapes: the token-serial forward with T = 1 and the state as both
@@ -130,6 +171,21 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
   f.B = a.B; f.H = a.H; f.T = 1; f.dk = a.dk; f.dv = a.dv;
   f.scale = a.scale; f.io = a.io;
   return launch_fwd_recurrent(f, s);
+}
+
+}  // namespace ckda
+
+namespace ckda {
+
+cudaError_t launch_decode_raw(const DecodeArgs& a, int normalize_q, float norm_eps,
+                              cudaStream_t s) {
+  const int units = a.B * a.H;
+  if (units == 0) return cudaSuccess;
+  if (a.io == CKDA_F32)
+    decode128_kernel<float, true><<<units, 256, 0, s>>>(a, normalize_q, norm_eps);
+  else
+    decode128_kernel<__nv_bfloat16, true><<<units, 256, 0, s>>>(a, normalize_q, norm_eps);
+  return cudaGetLastError();
 }
 
 }  // namespace ckda

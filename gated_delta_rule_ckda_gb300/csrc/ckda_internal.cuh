@@ -62,8 +62,29 @@ struct DecodeArgs {
   ckda_dtype io;
 };
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
+// The decode step on raw inputs (q_raw, k_raw, gate logits a, b in the
+// q, k, alpha, beta fields): dk = dv = 128 only.
+cudaError_t launch_decode_raw(const DecodeArgs& a, int normalize_q, float norm_eps,
+                              cudaStream_t s);
 
 cudaError_t launch_selftest_timeout(int* status, unsigned spin_limit, cudaStream_t s);
+
+// The paper's gate parameterisation ("Complex KDA" discussion slides, backup
+// frame "practical gates differ from exact theoretical endpoints"), in fp32:
+// alpha = s [e^-5 + (1 - e^-5) |tanh(a / 2)|] with s = +1 for tanh(a/2) >= 0,
+// else -1; beta = 2 sigma(b), with the exponential of a non-positive argument
+// on either side so that large |b| neither overflows nor loses the tail.
+constexpr float kGateEps = 0.006737947f;  // e^-5
+__device__ __forceinline__ float gate_alpha(float a) {
+  const float r = tanhf(0.5f * a);
+  const float s = r >= 0.f ? 1.f : -1.f;
+  return s * fmaf(1.f - kGateEps, fabsf(r), kGateEps);
+}
+__device__ __forceinline__ float gate_beta(float b) {
+  if (b >= 0.f) return 2.f / (1.f + expf(-b));
+  const float e = expf(b);
+  return 2.f * e / (1.f + e);
+}
 
 // Element loads/stores in the I/O dtype.
 template <typename T>

@@ -18,7 +18,6 @@
 namespace ckda {
 namespace {
 
-constexpr float kGateEps = 0.006737947f;  // e^-5, the paper's gate floor
 
 struct PrepArgs {
   const void* q_raw;
@@ -40,19 +39,6 @@ __device__ __forceinline__ float warp_sum(float x) {
   for (int m = 16; m >= 1; m >>= 1) x += __shfl_xor_sync(0xffffffffu, x, m);
   return x;
 }
-__device__ __forceinline__ float gate_alpha(float a) {
-  const float r = tanhf(0.5f * a);
-  const float s = r >= 0.f ? 1.f : -1.f;
-  return s * fmaf(1.f - kGateEps, fabsf(r), kGateEps);
-}
-// 2 sigma(b), with the exponential of a non-positive argument on either side
-// so that large |b| neither overflows nor loses the tail
-__device__ __forceinline__ float gate_beta(float b) {
-  if (b >= 0.f) return 2.f / (1.f + expf(-b));
-  const float e = expf(b);
-  return 2.f * e / (1.f + e);
-}
-
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 __device__ __forceinline__ uint32_t bf_pack(float lo, float hi) {

@@ -205,6 +205,30 @@ ckda_status ckda_decode_step(const void *q, const void *k, const void *v,
                              ckda_dtype io_dtype, float scale, void *stream);
 
 /*
+ * One decode step on raw inputs, with the input preparation of ckda_prep
+ * fused in: the step first forms k = k_raw / sqrt(|k_raw|^2 + norm_eps), q
+ * likewise when normalize_q (else q = q_raw), alpha = s [e^-5 + (1 - e^-5)
+ * |tanh(a_raw / 2)|] with s = +1 for tanh >= 0 else -1, and beta =
+ * 2 sigma(b_raw) ("Complex KDA" discussion slides, backup frame "practical
+ * gates differ from exact theoretical endpoints"; paper Sec. 2 for the unit
+ * keys), in fp32, then applies ckda_decode_step's update and readout.  The
+ * prepared values are not written out.
+ *
+ *   q_raw, k_raw, a_raw : io   [B, H, dk]      v, o : io [B, H, dv]
+ *   b_raw               : io   [B, H]          state : fp32 [B, H, dk, dv]
+ *
+ * dk = dv = 128 only (CKDA_ERR_UNSUPPORTED otherwise; ckda_prep followed by
+ * ckda_decode_step covers the other shapes); state 16-byte aligned.  The step
+ * is bound by HBM like the plain one: the token inputs are 1 KB against the
+ * state's 128 KB per (batch, head).  Argument errors return synchronously;
+ * otherwise CKDA_OK once enqueued on `stream`.
+ */
+ckda_status ckda_decode_step_raw(const void *q_raw, const void *k_raw, const void *v,
+                                 const void *a_raw, const void *b_raw, float *state, void *o,
+                                 int B, int H, int dk, int dv, ckda_dtype io_dtype,
+                                 float scale, int normalize_q, float norm_eps, void *stream);
+
+/*
  * Backward of ckda_fwd: gradients of L = sum_t <o_t, do_t> + <hT, dhT> with
  * respect to q, k, v, alpha, beta and h0, by reverse-mode differentiation of
  * the recurrence ("Complex KDA: Understanding and Enhancing the Expressivity

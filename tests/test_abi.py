@@ -97,6 +97,23 @@ def test_decode_argument_errors_are_synchronous(L):
     assert f(io=3) == 1
 
 
+def test_decode_raw_argument_errors_are_synchronous(L):
+    vp = ctypes.c_void_p
+    names = ("q", "k", "v", "a", "b", "state", "o")
+    f = lambda **kw: L.ckda_decode_step_raw(*(vp(kw.get(n, 256)) for n in names),
+                                            kw.get("B", 1), kw.get("H", 1), kw.get("dk", 128),
+                                            kw.get("dv", 128), kw.get("io", 1),
+                                            ctypes.c_float(1.0), 1,
+                                            ctypes.c_float(kw.get("eps", 1e-6)), vp(None))
+    assert f(state=None) == 1
+    assert f(b=None) == 1
+    assert f(B=0) == 1
+    assert f(dk=64) == 2          # the fused step is 128 x 128 only
+    assert f(state=8) == 1        # misaligned state
+    assert f(io=3) == 1
+    assert f(eps=-1.0) == 1
+
+
 def test_bwd_argument_errors_are_synchronous(L):
     vp = ctypes.c_void_p
     names = ("q", "k", "v", "alpha", "beta", "h0", "do", "dhT", "dq", "dk", "dv", "dalpha",

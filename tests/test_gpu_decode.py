@@ -70,3 +70,50 @@ def test_decode_chain_equals_fwd(ck):
                              d_.beta[:, :, t].contiguous(), S)
         assert torch.allclose(o_t, o_f[:, :, t], rtol=1e-6, atol=1e-6)
     assert torch.allclose(S, h_f, rtol=1e-6, atol=1e-6)
+
+
+def raw_step(B, H, d, dtype, seed):
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn((B, H, d), generator=g) * 3
+    k = torch.randn((B, H, d), generator=g) * torch.rand((B, H, 1), generator=g) * 5
+    v = torch.randn((B, H, d), generator=g)
+    a = torch.randn((B, H, d), generator=g) * 3
+    b = torch.randn((B, H), generator=g) * 2
+    dt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    return tuple(t.to(dt) for t in (q, k, v, a, b))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("normalize_q", [True, False])
+def test_decode_raw_chain_matches_oracle(ck, dtype, normalize_q):
+    """Raw q, k and gate logits through the fused step, against the oracle's
+    input preparation followed by the oracle's decode step, 6 chained steps."""
+    B, H, d = 3, 5, 128
+    S = synth.make_decode_state(B, H, d, seed=70)
+    Sg = S.cuda()
+    Sref = S.double().numpy()
+    for step in range(6):
+        q, k, v, a, b = raw_step(B, H, d, dtype, 700 + step)
+        o = ck.decode_step_raw(q.cuda(), k.cuda(), v.cuda(), a.cuda(), b.cuda(), Sg, scale=0.8,
+                               normalize_q=normalize_q)
+        qp, kp, ap, bp = oracle.prep(k, a, b, q_raw=q, normalize_q=normalize_q)
+        o_ref, Sref = oracle.decode_step(qp, kp, v, ap, bp, Sref, scale=0.8)
+        if dtype == "bf16":
+            assert excess_bf16(o.cpu(), o_ref) <= 2e-2
+        else:
+            assert max_rel(o.cpu(), o_ref) <= 1e-4
+        assert max_rel(Sg.cpu(), Sref) <= 1e-5
+
+
+def test_decode_raw_equals_prep_then_decode(ck):
+    """fp32: the fused step equals ckda_prep followed by ckda_decode_step up to
+    fp32 rounding (the two sum the norms in different orders)."""
+    B, H, d = 4, 6, 128
+    S = synth.make_decode_state(B, H, d, seed=71).cuda()
+    S2 = S.clone()
+    q, k, v, a, b = (t.cuda() for t in raw_step(B, H, d, "fp32", 710))
+    o1 = ck.decode_step_raw(q, k, v, a, b, S)
+    qp, kp, ap, bp = ck.prep(k, a, b, q_raw=q)
+    o2 = ck.decode_step(qp, kp, v, ap, bp, S2)
+    assert torch.allclose(o1, o2, rtol=1e-5, atol=1e-6)
+    assert torch.allclose(S, S2, rtol=1e-5, atol=1e-6)
