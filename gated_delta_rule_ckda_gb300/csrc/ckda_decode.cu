@@ -31,7 +31,6 @@ __global__ void __launch_bounds__(256, 2) decode128_kernel(DecodeArgs a, int nor
   __shared__ float s_ak[128], s_a[128], s_k[128], s_q[128], s_v[128];
   __shared__ float4 s_red[8][32];
   __shared__ float s_beta;
-  __shared__ float s_norm[2][4];
   const int p = blockIdx.x;  // (batch, head)
   const int tid = threadIdx.x, g = tid >> 5, c = tid & 31;
   float4* S = reinterpret_cast<float4*>(a.state + (size_t)p * 128 * 128);
@@ -57,36 +56,33 @@ __global__ void __launch_bounds__(256, 2) decode128_kernel(DecodeArgs a, int nor
     }
     __syncthreads();
   } else {
-    float kv = 0.f, qv = 0.f;
-    if (tid < 128) {
-      kv = ld_io(k + tid);
-      qv = ld_io(q + tid);
-      float sk = kv * kv, sq = qv * qv;
+    // every warp reads all of k and q (four channels per lane) and reduces
+    // the two norms itself, so that the step keeps a single block barrier
+    float k4[4], q4[4], ss_k = 0.f, ss_q = 0.f;
 #pragma unroll
-      for (int m = 16; m >= 1; m >>= 1) {
-        sk += __shfl_xor_sync(0xffffffffu, sk, m);
-        sq += __shfl_xor_sync(0xffffffffu, sq, m);
-      }
-      if (c == 0) {
-        s_norm[0][g] = sk;
-        s_norm[1][g] = sq;
-      }
+    for (int e = 0; e < 4; ++e) {
+      k4[e] = ld_io(k + 4 * c + e);
+      q4[e] = ld_io(q + 4 * c + e);
+      ss_k = fmaf(k4[e], k4[e], ss_k);
+      ss_q = fmaf(q4[e], q4[e], ss_q);
+    }
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) {
+      ss_k += __shfl_xor_sync(0xffffffffu, ss_k, m);
+      ss_q += __shfl_xor_sync(0xffffffffu, ss_q, m);
+    }
+    const float ik = rsqrtf(ss_k + norm_eps);
+    const float iq = normalize_q ? rsqrtf(ss_q + norm_eps) : 1.f;
+    if (tid < 128) {  // warps 0-3 publish k, alpha, alpha k and scale q, one channel a lane
+      const int i = tid;
+      const float kv = ld_io(k + i) * ik, av = gate_alpha(ld_io(al + i));
+      s_k[i] = kv;
+      s_a[i] = av;
+      s_ak[i] = av * kv;
+      s_q[i] = a.scale * (ld_io(q + i) * iq);
     } else {
       s_v[tid - 128] = ld_io(v + (tid - 128));
       if (tid == 128) s_beta = gate_beta(ld_io(static_cast<const IO*>(a.beta) + p));
-    }
-    __syncthreads();
-    if (tid < 128) {
-      const float ik = rsqrtf(s_norm[0][0] + s_norm[0][1] + s_norm[0][2] + s_norm[0][3] + norm_eps);
-      float iq = 1.f;
-      if (normalize_q)
-        iq = rsqrtf(s_norm[1][0] + s_norm[1][1] + s_norm[1][2] + s_norm[1][3] + norm_eps);
-      const float av = gate_alpha(ld_io(al + tid));
-      kv *= ik;
-      s_a[tid] = av;
-      s_k[tid] = kv;
-      s_ak[tid] = av * kv;
-      s_q[tid] = a.scale * (qv * iq);
     }
     __syncthreads();
   }
