@@ -238,6 +238,33 @@ def fwd_case(ck, x, steps, warmup, ws, stream, name):
                 wsp=wsp)
 
 
+def fwd_split_case(ck, x, steps, warmup, ws, stream, name):
+    """ckda_fwd_split at the automatic segment count, on a dense workload."""
+    import torch
+    d = x.to("cuda")
+    B, H, T, dk = d.q.shape
+    dv = d.v.shape[-1]
+    S = ck.split_segments(B, H, T, dk, dv)
+    o = torch.empty_like(d.v)
+    hT = torch.empty((B, H, dk, dv), dtype=torch.float32, device="cuda")
+    wsp = torch.empty(ck.split_workspace_bytes(B, H, T, dk, dv, segments=S), dtype=torch.uint8,
+                      device="cuda")
+
+    def step():
+        ck.fwd_split(d.q, d.k, d.v, d.alpha, d.beta, d.h0, segments=S, o=o, hT=hT,
+                     workspace=wsp, stream=stream)
+
+    step()
+    st = ck.fwd_status(wsp)
+    if st != 0:
+        raise RuntimeError(f"{name} split: device status {ck.STATUS.get(st, st)}")
+    total, per = time_steps(step, steps, warmup, ws, stream)
+    th = B * H * T
+    nbytes = fwd_bytes(B, H, T, dk, dv, B, d.h0 is not None, True)
+    return dict(total=total, per=per, th=th, bytes=nbytes, segments=S,
+                launches=3 if S >= 3 else (2 if S == 2 else 1))
+
+
 def roofline(nbytes, per_ms, kernel, workload):
     peak, src = hbm_peak()
     mean_s = sum(per_ms) / len(per_ms) / 1e3
@@ -474,6 +501,23 @@ def run_ours(args):
                       "roofline": roofline(rr["bytes"], rr["per"], "fwd_chunk", nm)}
             del xx, rr
         out["workloads"] = wl
+    if ws == 1 and "long_seq" in extras:
+        # one sequence of 16 heads: the plain forward fills 16 SMs; the split
+        # forward runs each sequence as segments on the rest
+        xx = synth.make_workload("long_seq")
+        rp = fwd_case(ck, xx, 5, 3, ws, stream, "long_seq")
+        rs = fwd_split_case(ck, xx, 10, 3, ws, stream, "long_seq")
+        lw = {}
+        for key, rr, steps in (("plain", rp, 5), ("split", rs, 10)):
+            lw[key] = {"value": round(rr["th"] * steps / rr["total"], 1), "unit": UNIT,
+                       "ms_per_step": round(rr["total"] / steps * 1e3, 4), "steps": steps,
+                       "token_heads": rr["th"],
+                       "roofline": roofline(rr["bytes"], rr["per"], "fwd_chunk", "long_seq")}
+        lw["split"]["segments"] = rs["segments"]
+        lw["split"]["launches_per_step"] = rs["launches"]
+        lw["split"]["roofline"]["traffic"] = None
+        out.setdefault("workloads", {})["long_seq"] = lw
+        del xx, rp, rs
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(x, args.cpu_seconds)
     if rank == 0:
@@ -546,9 +590,10 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--extras",
-                    default="decode,decode_raw,prep,bwd,ckda_full,ckda_varlen,kda_range_dk64",
+                    default="decode,decode_raw,prep,bwd,ckda_full,ckda_varlen,kda_range_dk64,"
+                            "long_seq",
                     help="comma list of extra measurements: decode, decode_raw, prep, bwd, "
-                         "ckda_full, ckda_varlen, kda_range_dk64")
+                         "ckda_full, ckda_varlen, kda_range_dk64, long_seq")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--bwd-units", type=int, default=0,
                     help="run the bwd extra on the first N (batch, head) units only")

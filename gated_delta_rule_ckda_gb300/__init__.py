@@ -20,8 +20,10 @@ import threading
 
 import torch
 
-__all__ = ["fwd", "fwd_host", "decode_step", "decode_step_raw", "prep", "bwd", "bwd_workspace_bytes", "fwd_status", "workspace_bytes",
-           "host_scratch_bytes", "selftest_timeout", "lib", "library_path", "CkdaError", "STATUS"]
+__all__ = ["fwd", "fwd_host", "fwd_split", "decode_step", "decode_step_raw", "prep", "bwd",
+           "bwd_workspace_bytes", "fwd_status", "workspace_bytes", "split_segments",
+           "split_workspace_bytes", "host_scratch_bytes", "selftest_timeout", "lib",
+           "library_path", "CkdaError", "STATUS"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libckda.so")
@@ -87,6 +89,13 @@ def lib():
             L.ckda_fwd_host.restype = i32
             L.ckda_fwd_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
                                         i32, f32, i32, vp, sz, vp]
+            L.ckda_fwd_split_segments.restype = i32
+            L.ckda_fwd_split_segments.argtypes = [i32, i32, i32, i32, i32, i32, i32]
+            L.ckda_fwd_split_workspace_bytes.restype = sz
+            L.ckda_fwd_split_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32, i32]
+            L.ckda_fwd_split.restype = i32
+            L.ckda_fwd_split.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
+                                         i32, f32, i32, vp, sz, vp]
             _lib = L
     return _lib
 
@@ -166,6 +175,58 @@ def fwd(q, k, v, alpha, beta, h0=None, cu_seqlens=None, scale=1.0, chunk_size=0,
     if rc != 0:
         raise CkdaError(rc, "ckda_fwd")
     fwd.last_workspace = workspace
+    return o, hT
+
+
+def split_segments(B, H, T, dk, dv, dtype=torch.bfloat16, num_sms=0) -> int:
+    """Segment count ckda_fwd_split picks for `segments=0` (num_sms = 0: the
+    current device's SM count)."""
+    io = _BF16 if dtype == torch.bfloat16 else _F32
+    return int(lib().ckda_fwd_split_segments(B, H, T, dk, dv, io, int(num_sms)))
+
+
+def split_workspace_bytes(B, H, T, dk, dv, dtype=torch.bfloat16, segments=0) -> int:
+    io = _BF16 if dtype == torch.bfloat16 else _F32
+    return int(lib().ckda_fwd_split_workspace_bytes(B, H, T, dk, dv, io, int(segments)))
+
+
+def fwd_split(q, k, v, alpha, beta, h0=None, scale=1.0, segments=0, store_final_state=True,
+              o=None, hT=None, workspace=None, stream=None):
+    """ckda_fwd_split: the dense forward with each sequence cut into segments
+    run in parallel (two passes and a scan of the segment operators).
+    Returns (o, hT or None)."""
+    L = lib()
+    device = q.device
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    dt = q.dtype
+    io = _io_dtype(q)
+    for name, t, shp in (("q", q, (B, H, T, dk)), ("k", k, (B, H, T, dk)),
+                         ("alpha", alpha, (B, H, T, dk)), ("v", v, (B, H, T, dv)),
+                         ("beta", beta, (B, H, T))):
+        _check(t, name, dt, shp, device)
+    if h0 is not None:
+        _check(h0, "h0", torch.float32, (B, H, dk, dv), device)
+    if o is None:
+        o = torch.empty((B, H, T, dv), dtype=dt, device=device)
+    else:
+        _check(o, "o", dt, (B, H, T, dv), device)
+    if store_final_state and hT is None:
+        hT = torch.empty((B, H, dk, dv), dtype=torch.float32, device=device)
+    if hT is not None:
+        _check(hT, "hT", torch.float32, (B, H, dk, dv), device)
+    if workspace is None:
+        with torch.cuda.device(device):
+            n = int(L.ckda_fwd_split_workspace_bytes(B, H, T, dk, dv, io, int(segments)))
+        workspace = torch.empty(n, dtype=torch.uint8, device=device)
+    with torch.cuda.device(device):
+        rc = L.ckda_fwd_split(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(h0),
+                              _ptr(o), _ptr(hT), B, H, T, dk, dv, io, float(scale),
+                              int(segments), _ptr(workspace), int(workspace.numel()),
+                              _stream_handle(stream, device))
+    if rc != 0:
+        raise CkdaError(rc, "ckda_fwd_split")
+    fwd_split.last_workspace = workspace
     return o, hT
 
 

@@ -158,27 +158,71 @@ static_assert(B_COUNT * 8 <= 192, "mbarrier area");
 
 constexpr uint32_t TILE_BYTES = 16384;
 
+// What one CTA runs: its rows, its initial and final state, and (in the
+// sequence split) whether its initial state is [I | 0], its v is zero and its
+// o is stored.
 struct Unit {
   long row0;
   int len;
-  size_t sidx;
+  size_t sidx;       // plain kernel: offset of the (sequence, head) in h0 and hT
+  const float* h0;   // split: [DK][128] initial state, or null: zero (or [I | 0] if ident)
+  float* hT;         // split: [DK][128] final state, or null: not stored
+  bool ident, zero_v, write_o;
 };
 
-__device__ __forceinline__ Unit unit_of(const FwdArgs& a, int dk) {
+template <int DK, bool SPLIT>
+__device__ __forceinline__ Unit unit_of(const FwdArgs& a) {
   Unit u;
-  const int b = blockIdx.x;
-  const int h = b % a.H;
-  int n = b / a.H;
-  if (a.cu_seqlens) {
-    if (a.order) n = a.order[n];
-    const int t0 = a.cu_seqlens[n];
-    u.len = a.cu_seqlens[n + 1] - t0;
-    u.row0 = (long)h * a.T + t0;
+  constexpr size_t tile = (size_t)DK * 128;
+  u.ident = false;
+  u.zero_v = false;
+  u.write_o = true;
+  if constexpr (SPLIT) {
+    // dense layout; CTA b is (sequence, head) ui, role r of its pass
+    const int S = a.nseg;
+    const int per = split_ctas_per_unit(a.split_pass, S);
+    const int ui = (int)blockIdx.x / per, r = (int)blockIdx.x % per;
+    const size_t slot0 = (size_t)ui * S;
+    int seg;
+    u.h0 = nullptr;
+    u.hT = nullptr;
+    if (a.split_pass == 1) {
+      u.write_o = r == 0;
+      if (r == 0) {          // segment 0 from h0; its final state enters segment 1
+        seg = 0;
+        u.h0 = a.h0 ? a.h0 + (size_t)ui * tile : nullptr;
+        u.hT = a.seg_state + (slot0 + 1) * tile;
+      } else if (r <= S - 2) {  // final state of segment r from zero
+        seg = r;
+        u.hT = a.seg_F + (slot0 + seg) * tile;
+      } else {               // transition of segment r - (S - 2): from [I | 0], v = 0
+        seg = r - (S - 2);
+        u.ident = true;
+        u.zero_v = true;
+        u.hT = a.seg_P + (slot0 + seg) * tile;
+      }
+    } else {
+      seg = 1 + r;
+      u.h0 = a.seg_state + (slot0 + seg) * tile;
+      u.hT = (seg == S - 1 && a.hT) ? a.hT + (size_t)ui * tile : nullptr;
+    }
+    u.row0 = (long)ui * a.T + (long)seg * a.seg_len;
+    u.len = min(a.seg_len, a.T - seg * a.seg_len);
   } else {
-    u.len = a.T;
-    u.row0 = ((long)n * a.H + h) * a.T;
+    const int b = blockIdx.x;
+    const int h = b % a.H;
+    int n = b / a.H;
+    if (a.cu_seqlens) {
+      if (a.order) n = a.order[n];
+      const int t0 = a.cu_seqlens[n];
+      u.len = a.cu_seqlens[n + 1] - t0;
+      u.row0 = (long)h * a.T + t0;
+    } else {
+      u.len = a.T;
+      u.row0 = ((long)n * a.H + h) * a.T;
+    }
+    u.sidx = ((size_t)n * a.H + h) * tile;
   }
-  u.sidx = ((size_t)n * a.H + h) * (size_t)dk * 128;
   return u;
 }
 
@@ -509,8 +553,10 @@ __device__ __forceinline__ void invert_diag_blocks(uint8_t* sm, int p) {
 }
 
 // DK: the caller's key width, 128 or 64 (a compile-time constant, so that
-// the 128-wide kernel carries nothing for the narrower one).
-template <int DK>
+// the 128-wide kernel carries nothing for the narrower one).  SPLIT: one pass
+// of the sequence split (per-CTA roles from unit_of); the plain kernel
+// carries none of it.
+template <int DK, bool SPLIT>
 __global__ void __launch_bounds__(NT, 1)
     fwd_chunk_kernel(const __grid_constant__ FwdArgs a, const __grid_constant__ CUtensorMap mq,
                      const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap ma,
@@ -533,7 +579,8 @@ __global__ void __launch_bounds__(NT, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + S_BAR + 200);
 
   static_assert(DK == 128 || DK == 64, "key width");
-  const Unit u = unit_of(a, DK);
+  const Unit u = unit_of<DK, SPLIT>(a);
+  const bool zero_v = SPLIT && u.zero_v;    // no v tile is read; U~ = 0
   const int nchunks = (u.len + C - 1) / C;
 
   if (tid == 0) {
@@ -754,7 +801,9 @@ __global__ void __launch_bounds__(NT, 1)
     const int wq = s >> 5;       // warps 8..11 -> lane groups 0..3
     const uint32_t lb = (uint32_t)(32 * wq) << 16;
     const bool lead = s == 0;
-    float* hT = a.hT;
+    // the final state of this CTA's (sequence, head) is hT + hoff, or none
+    float* hT = SPLIT ? u.hT : a.hT;
+    const size_t hoff = SPLIT ? 0 : u.sidx;
     bool alive = true;
     const float* gc_all = reinterpret_cast<const float*>(sm + S_GC);
     // H^T as the fp16 A operand (TMEM) and, in TMEM, H^T Diag(gamma_C) of
@@ -765,9 +814,20 @@ __global__ void __launch_bounds__(NT, 1)
       for (int i0 = 0; i0 < 128; i0 += 16) {
         float f[16];
         if (from_h0) {
+          if constexpr (SPLIT) {
 #pragma unroll
-          for (int e = 0; e < 16; ++e)
-            f[e] = (a.h0 && i0 + e < DK) ? a.h0[u.sidx + (size_t)(i0 + e) * 128 + s] : 0.f;
+            for (int e = 0; e < 16; ++e) {
+              f[e] = 0.f;
+              if (i0 + e < DK) {
+                if (u.h0) f[e] = u.h0[(size_t)(i0 + e) * 128 + s];
+                else if (u.ident && i0 + e == s) f[e] = 1.f;
+              }
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              f[e] = (a.h0 && i0 + e < DK) ? a.h0[u.sidx + (size_t)(i0 + e) * 128 + s] : 0.f;
+          }
         } else {
           uint32_t v[16];
           tmem_ld32<16>(tmem + lb + T_H + i0, v);
@@ -797,8 +857,10 @@ __global__ void __launch_bounds__(NT, 1)
       alive = named_and(BAR_STATE, NSTATE, ok);
       if (alive) convert_and_scale(0, true);
     } else if (hT) {
+      const float* h0 = SPLIT ? u.h0 : a.h0;
       for (int i = 0; i < DK; ++i)
-        hT[u.sidx + (size_t)i * 128 + s] = a.h0 ? a.h0[u.sidx + (size_t)i * 128 + s] : 0.f;
+        hT[hoff + (size_t)i * 128 + s] =
+            h0 ? h0[hoff + (size_t)i * 128 + s] : ((SPLIT && u.ident && i == s) ? 1.f : 0.f);
     }
     tc_fence_before();
     named_sync(BAR_STATE, NSTATE);
@@ -807,25 +869,32 @@ __global__ void __launch_bounds__(NT, 1)
     float fin = 0.f;  // becomes NaN once any output is inf or NaN
     for (int c = 0; c < nchunks && alive; ++c) {
       const int lenc = min(C, u.len - c * C);
-      {  // O starts from zero (the previous chunk's has been read out)
+      {  // O starts from zero (the previous chunk's has been read out), and
+         // so does U when v is zero (no U~ step)
         const uint32_t z[16] = {0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
 #pragma unroll
         for (int i0 = 0; i0 < 64; i0 += 16) tmem_st32<16>(tmem + lb + T_O + i0, z);
+        if (zero_v) {
+#pragma unroll
+          for (int i0 = 0; i0 < 64; i0 += 16) tmem_st32<16>(tmem + lb + T_U + i0, z);
+        }
         tmem_st_wait();
         tc_fence_before();
       }
       {  // prep operands of chunk c in shared memory, and its v tile
         bool ok = mbar_wait(bar_ready + (c & 1), (uint32_t)((c >> 1) & 1));
-        if (ok) ok = mbar_wait(bar_v, (uint32_t)(c & 1));
+        if (ok && !zero_v) ok = mbar_wait(bar_v, (uint32_t)(c & 1));
         if (!named_and(BAR_STATE, NSTATE, ok)) { alive = false; break; }
         tc_fence_after();
       }
       if (lead) {
         // U~^T = V^T TB^T, then [U^T | O^T] += H^T [-W^T | (q*gamma)^T]
+        if (!zero_v) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          umma_ss(tmem + T_U, mnmajor_desc(sb + S_V, 64, k), kmajor_desc(sb + S_TB, 64, k),
-                  idesc_f16(128, 64, 1, 1, 0), k > 0);
+          for (int k = 0; k < 4; ++k)
+            umma_ss(tmem + T_U, mnmajor_desc(sb + S_V, 64, k), kmajor_desc(sb + S_TB, 64, k),
+                    idesc_f16(128, 64, 1, 1, 0), k > 0);
+        }
 #pragma unroll
         for (int k = 0; k < 8; ++k)
           umma_ts(tmem + T_U, tmem + T_HA + 8 * k, mnmajor_desc(sb + S_WQ, 128, k),
@@ -837,7 +906,7 @@ __global__ void __launch_bounds__(NT, 1)
         if (!named_and(BAR_STATE, NSTATE, ok)) { alive = false; break; }
         tc_fence_after();
       }
-      if (lead && c + 1 < nchunks) {  // the v tile is free: fetch the next one
+      if (lead && c + 1 < nchunks && !zero_v) {  // the v tile is free: fetch the next one
         const int y = (int)(u.row0 + (long)(c + 1) * C);
         mbar_arrive_expect_tx(bar_v, TILE_BYTES);
         tma_load_2d(sm + S_V, &mv, bar_v, 0, y);
@@ -880,7 +949,7 @@ __global__ void __launch_bounds__(NT, 1)
         tc_fence_after();
       }
       // outputs o[t][j] = O^T[j][t]
-      {
+      if (!SPLIT || u.write_o) {
         const long rbase = u.row0 + (long)c * C;
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2) {
@@ -916,7 +985,7 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
           const float x = __uint_as_float(v[e]);
-          hT[u.sidx + (size_t)(i0 + e) * 128 + s] = x;
+          hT[hoff + (size_t)(i0 + e) * 128 + s] = x;
           fin = fmaf(x, 0.f, fin);
         }
       }
@@ -958,7 +1027,7 @@ __global__ void __launch_bounds__(NT, 1)
           tma_prefetch_2d_l2(&mk, x0, y);
           tma_prefetch_2d_l2(&ma, x0, y);
         }
-        tma_prefetch_2d_l2(&mv, x0, y);
+        if (!zero_v) tma_prefetch_2d_l2(&mv, x0, y);
       }
     };
     // beta of chunk cc, two tokens per lane of warp 12: fetched a chunk ahead
@@ -1025,9 +1094,11 @@ __global__ void __launch_bounds__(NT, 1)
     if (nchunks > 0 && warp == MMA_WARP) {
       if (lane == 0) {
         issue_qka(0);
-        mbar_arrive_expect_tx(bar_v, TILE_BYTES);
-        tma_load_2d(sm + S_V, &mv, bar_v, 0, (int)u.row0);
-        tma_load_2d(sm + S_V + 8192, &mv, bar_v, 64, (int)u.row0);
+        if (!zero_v) {
+          mbar_arrive_expect_tx(bar_v, TILE_BYTES);
+          tma_load_2d(sm + S_V, &mv, bar_v, 0, (int)u.row0);
+          tma_load_2d(sm + S_V + 8192, &mv, bar_v, 64, (int)u.row0);
+        }
         if (nchunks > 1) prefetch_l2(1);
       }
       fetch_beta(0);
@@ -1185,7 +1256,7 @@ __global__ void __launch_bounds__(NT, 1)
       for (int i = 0; i < ST_COUNT; ++i) mbar_wait(bar_done + i, 0, 1u << 12, 1000u);
       mbar_wait(bar_s1, 0, 1u << 12, 1000u);
       mbar_wait(bar_s3, 0, 1u << 12, 1000u);
-      mbar_wait(bar_v, 0, 1u << 12, 1000u);
+      if (!zero_v) mbar_wait(bar_v, 0, 1u << 12, 1000u);
       mbar_wait(bar_qka, 0, 1u << 12, 1000u);
     }
   }
@@ -1235,11 +1306,16 @@ cudaError_t launch_fwd_chunk(const FwdArgs& a, cudaStream_t s) {
              !make_map(&ma, a.alpha, rows, a.dk) || !make_map(&mv, a.v, rows, 128)) {
     return cudaErrorInvalidValue;
   }
-  auto kern = a.dk == 64 ? fwd_chunk_kernel<64> : fwd_chunk_kernel<128>;
+  auto kern = a.split_pass ? (a.dk == 64 ? fwd_chunk_kernel<64, true> : fwd_chunk_kernel<128, true>)
+                           : (a.dk == 64 ? fwd_chunk_kernel<64, false> : fwd_chunk_kernel<128, false>);
+  const long long grid =
+      a.split_pass ? (long long)a.B * a.H * split_ctas_per_unit(a.split_pass, a.nseg) : units;
+  if (grid == 0) return cudaSuccess;
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_ALLOC);
   if (err != cudaSuccess) return err;
-  kern<<<units, NT, SMEM_ALLOC, s>>>(a, mq, mk, ma, mv);
+  kern<<<(unsigned)grid, NT, SMEM_ALLOC, s>>>(a, mq, mk, ma, mv);
   return cudaGetLastError();
 }
 

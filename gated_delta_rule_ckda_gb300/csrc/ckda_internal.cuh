@@ -33,6 +33,18 @@ struct FwdArgs {
   int B, H, T, dk, dv;
   float scale;
   ckda_dtype io;
+  // Sequence split (dense layout, tensor-core path): each sequence runs as
+  // nseg segments of seg_len tokens (a multiple of 64; the last may be
+  // shorter).  split_pass 1: segment 0 from h0 (its o, and its final state into
+  // seg_state[1]) and, for segments 1..nseg-2, the final state from zero
+  // (seg_F) and the transition (seg_P: the final state from [I | 0] with
+  // v = 0).  split_pass 2: segments 1..nseg-1 from seg_state (o, and hT from
+  // the last).  Buffers are [B * H][nseg][dk][128] fp32.  0 = no split.
+  int split_pass;
+  int nseg, seg_len;
+  float* seg_state;
+  float* seg_P;
+  float* seg_F;
 };
 
 // Shapes the chunkwise tensor-core kernel takes: bf16 I/O, dv = 128 and
@@ -44,8 +56,17 @@ inline bool fwd_tensor_path(ckda_dtype io, int dk, int dv) {
 }
 // Token-serial CUDA-core forward (any dk, dv <= 128).
 cudaError_t launch_fwd_recurrent(const FwdArgs& a, cudaStream_t s);
-// Chunkwise tcgen05 forward (fwd_tensor_path shapes, chunk 64).
+// Chunkwise tcgen05 forward (fwd_tensor_path shapes, chunk 64); with
+// a.split_pass != 0, one pass of the sequence split.
 cudaError_t launch_fwd_chunk(const FwdArgs& a, cudaStream_t s);
+// CTAs of one pass of the sequence split, per (sequence, head).
+__host__ __device__ inline int split_ctas_per_unit(int pass, int nseg) {
+  return pass == 1 ? (nseg >= 3 ? 2 * nseg - 3 : 1) : nseg - 1;
+}
+// The scan between the passes: seg_state[s + 1] = seg_P[s] seg_state[s] +
+// seg_F[s] for s = 1..nseg-2, per (sequence, head).
+cudaError_t launch_seg_scan(float* state, const float* P, const float* F, int units, int nseg,
+                            int dk, cudaStream_t s);
 // Longest-first order of packed sequences.
 cudaError_t launch_seq_order(const int32_t* cu, int n, int32_t* order, cudaStream_t s);
 

@@ -1,0 +1,220 @@
+// ckda_split.cu -- the sequence-split forward: few long sequences spread over
+// many SMs by a two-level scan over segment operators.
+//
+// The state after a segment is an affine function of the state before it
+// ("Kimi Delta Attention: a bounded case study", "Chunkwise execution": the
+// chunk operator is Diag(gamma_C) - (k*rho)^T W applied to the state plus the
+// chunk's write, and a product of such operators is again one; the
+// sequence-parallel scan over these operators is the one step beyond
+// chunking that splits a single sequence):
+//
+//     H_out = P H_in + F,   P = prod of the segment's transitions (dk x dk),
+//                           F = the segment's final state from H_in = 0.
+//
+// Pass 1 runs, in parallel, segment 0 from h0 (its outputs are final), and
+// for every middle segment F (from zero) and P (the final state from
+// [I | 0] with v = 0: both are the tensor-core forward with a different
+// initial state and value input).  The scan below then gives the state
+// entering every segment, and pass 2 runs segments 1..S-1 from those states.
+// Results equal one pass over the whole sequence up to rounding.
+#include "ckda_internal.cuh"
+
+#include <algorithm>
+
+namespace ckda {
+namespace {
+
+constexpr int kScanCols = 32;      // state columns per CTA
+constexpr int kScanThreads = 256;  // 8 row groups x 32 columns
+
+// One (sequence, head) and 32 state columns per CTA.  Thread (g, j) owns rows
+// g * DK/8 .. of column j.  P_s is staged in shared memory (rows of DK fp32),
+// and the column block of H_s stays there between steps; each output is an
+// fp32 dot product over m in order.
+template <int DK>
+__global__ void __launch_bounds__(kScanThreads) seg_scan_kernel(float* state, const float* P,
+                                                                const float* F, int nseg) {
+  extern __shared__ float4 scan_smem[];
+  float* Ps = reinterpret_cast<float*>(scan_smem);   // [DK][DK]
+  float* Hs = Ps + DK * DK;                          // [DK][32]
+  constexpr int R = DK / 8;
+  constexpr size_t tile = (size_t)DK * 128;
+  const int ui = blockIdx.x, j0 = blockIdx.y * kScanCols;
+  const int tid = threadIdx.x, g = tid >> 5, j = tid & 31;
+  const size_t base = (size_t)ui * nseg * tile;
+  // H_1 (written by pass 1)
+  for (int e = tid; e < DK * kScanCols; e += kScanThreads) {
+    const int m = e / kScanCols, c = e % kScanCols;
+    Hs[e] = state[base + tile + (size_t)m * 128 + j0 + c];
+  }
+  for (int s = 1; s + 1 < nseg; ++s) {
+    const float* Pg = P + base + (size_t)s * tile;
+    for (int e = tid; e < DK * DK / 4; e += kScanThreads) {
+      const int i = e / (DK / 4), m4 = e % (DK / 4);
+      reinterpret_cast<float4*>(Ps)[e] = *reinterpret_cast<const float4*>(Pg + (size_t)i * 128 + 4 * m4);
+    }
+    __syncthreads();
+    float acc[R];
+    const float* Fg = F + base + (size_t)s * tile;
+#pragma unroll
+    for (int r = 0; r < R; ++r) acc[r] = Fg[(size_t)(g * R + r) * 128 + j0 + j];
+#pragma unroll 4
+    for (int m = 0; m < DK; m += 4) {
+      const float h0 = Hs[(m + 0) * kScanCols + j], h1 = Hs[(m + 1) * kScanCols + j];
+      const float h2 = Hs[(m + 2) * kScanCols + j], h3 = Hs[(m + 3) * kScanCols + j];
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const float4 p = *reinterpret_cast<const float4*>(Ps + (g * R + r) * DK + m);
+        acc[r] = fmaf(p.w, h3, fmaf(p.z, h2, fmaf(p.y, h1, fmaf(p.x, h0, acc[r]))));
+      }
+    }
+    __syncthreads();   // every read of Hs and Ps for this step is done
+    float* Hg = state + base + (size_t)(s + 1) * tile;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      Hs[(g * R + r) * kScanCols + j] = acc[r];
+      Hg[(size_t)(g * R + r) * 128 + j0 + j] = acc[r];
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_seg_scan(float* state, const float* P, const float* F, int units, int nseg,
+                            int dk, cudaStream_t s) {
+  if (units == 0 || nseg < 3) return cudaSuccess;
+  const dim3 grid(units, 128 / kScanCols);
+  const size_t smem = ((size_t)dk * dk + (size_t)dk * kScanCols) * sizeof(float);
+  auto kern = dk == 64 ? seg_scan_kernel<64> : seg_scan_kernel<128>;
+  cudaError_t err =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  kern<<<grid, kScanThreads, smem, s>>>(state, P, F, nseg);
+  return cudaGetLastError();
+}
+
+}  // namespace ckda
+
+using namespace ckda;
+
+namespace {
+
+size_t split_state_tile_bytes(int dk) { return (size_t)dk * 128 * sizeof(float); }
+
+// Segments and tokens per segment for a requested count: segments hold
+// ceil(chunks / S) chunks each, so the count actually used may be lower.
+void split_shape(int T, int segments, int* nseg, int* seg_len) {
+  const int nch = (T + 63) / 64;
+  const int sc = std::max(1, (nch + segments - 1) / segments);
+  *seg_len = sc * 64;
+  *nseg = std::max(1, (nch + sc - 1) / sc);
+}
+
+int device_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+}  // namespace
+
+extern "C" {
+
+int ckda_fwd_split_segments(int B, int H, int T, int dk, int dv, ckda_dtype io_dtype,
+                            int num_sms) {
+  if (B < 1 || H < 1 || T < 1 || num_sms < 0) return 1;
+  if (!fwd_tensor_path(io_dtype, dk, dv)) return 1;
+  if (num_sms == 0) num_sms = device_sms();
+  if (num_sms < 1) return 1;
+  const long long units = (long long)B * H;
+  const int nch = (T + 63) / 64;
+  auto waves = [&](long long ctas) { return (ctas + num_sms - 1) / num_sms; };
+  // time in chunk steps: both passes (each in whole waves of CTAs), one step
+  // of state I/O per pass, and about half a step per scan step
+  double best = (double)waves(units) * nch;
+  int best_s = 1;
+  for (int S = 2; S <= 16 && S <= nch; ++S) {
+    int ns = 0, sl = 0;
+    split_shape(T, S, &ns, &sl);
+    if (ns != S) continue;
+    const double t = (double)(waves(units * split_ctas_per_unit(1, S)) +
+                              waves(units * split_ctas_per_unit(2, S))) * (sl / 64) +
+                     2.0 + 0.5 * (S - 2);
+    if (t < 0.9 * best) {
+      best = t;
+      best_s = S;
+    }
+  }
+  return best_s;
+}
+
+size_t ckda_fwd_split_workspace_bytes(int B, int H, int T, int dk, int dv, ckda_dtype io_dtype,
+                                      int segments) {
+  if (B < 1 || H < 1 || T < 0 || dk < 1 || segments < 0) return 0;
+  if (segments == 0) segments = ckda_fwd_split_segments(B, H, T, dk, dv, io_dtype, 0);
+  size_t bytes = ckda_fwd_workspace_bytes(0, H);
+  if (segments < 2 || T == 0) return bytes;
+  int nseg = 0, seg_len = 0;
+  split_shape(T, segments, &nseg, &seg_len);
+  if (nseg < 2) return bytes;
+  const size_t per = (size_t)B * H * nseg * split_state_tile_bytes(dk);
+  return bytes + per * (nseg >= 3 ? 3 : 1);
+}
+
+ckda_status ckda_fwd_split(const void* q, const void* k, const void* v, const void* alpha,
+                           const void* beta, const float* h0, void* o, float* hT, int B, int H,
+                           int T, int dk, int dv, ckda_dtype io_dtype, float scale, int segments,
+                           void* workspace, size_t workspace_bytes, void* stream) {
+  if (segments < 0) return CKDA_ERR_INVALID_ARG;
+  if (segments == 0) {
+    if (io_dtype != CKDA_F32 && io_dtype != CKDA_BF16) return CKDA_ERR_INVALID_ARG;
+    segments = ckda_fwd_split_segments(B, H, T, dk, dv, io_dtype, 0);
+  }
+  int nseg = 1, seg_len = 0;
+  if (segments >= 2 && T > 0) split_shape(T, segments, &nseg, &seg_len);
+  if (nseg < 2)
+    return ckda_fwd(q, k, v, alpha, beta, h0, o, hT, nullptr, 0, B, H, T, dk, dv, io_dtype, scale,
+                    0, workspace, workspace_bytes, stream);
+
+  // the checks of ckda_fwd, for the shapes the split takes
+  if (io_dtype != CKDA_F32 && io_dtype != CKDA_BF16) return CKDA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || dk < 1 || dv < 1) return CKDA_ERR_INVALID_ARG;
+  if ((long long)B * H * T > 0x7fffffffLL) return CKDA_ERR_UNSUPPORTED;
+  if (!(scale == scale)) return CKDA_ERR_INVALID_ARG;
+  if (!q || !k || !v || !alpha || !beta || !o) return CKDA_ERR_INVALID_ARG;
+  if (!fwd_tensor_path(io_dtype, dk, dv)) return CKDA_ERR_UNSUPPORTED;
+  for (const void* p : {q, k, v, alpha})
+    if ((reinterpret_cast<uintptr_t>(p) & 15) != 0) return CKDA_ERR_INVALID_ARG;
+  const size_t need = ckda_fwd_split_workspace_bytes(B, H, T, dk, dv, io_dtype, segments);
+  if (!workspace || workspace_bytes < need) return CKDA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return CKDA_ERR_WORKSPACE;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  const size_t per = (size_t)B * H * nseg * split_state_tile_bytes(dk);
+  float* seg_state = reinterpret_cast<float*>(ws + kWsStatusBytes);
+  float* seg_P = nseg >= 3 ? reinterpret_cast<float*>(ws + kWsStatusBytes + per) : nullptr;
+  float* seg_F = nseg >= 3 ? reinterpret_cast<float*>(ws + kWsStatusBytes + 2 * per) : nullptr;
+
+  FwdArgs a{};
+  a.q = q; a.k = k; a.v = v; a.alpha = alpha; a.beta = beta;
+  a.h0 = h0; a.o = o; a.hT = hT;
+  a.status = static_cast<int*>(workspace);
+  a.num_units_seq = B;
+  a.B = B; a.H = H; a.T = T; a.dk = dk; a.dv = dv;
+  a.scale = scale; a.io = io_dtype;
+  a.nseg = nseg; a.seg_len = seg_len;
+  a.seg_state = seg_state; a.seg_P = seg_P; a.seg_F = seg_F;
+
+  if (cudaMemsetAsync(a.status, 0, sizeof(int), s) != cudaSuccess) return CKDA_ERR_CUDA;
+  a.split_pass = 1;
+  if (launch_fwd_chunk(a, s) != cudaSuccess) return CKDA_ERR_CUDA;
+  if (launch_seg_scan(seg_state, seg_P, seg_F, B * H, nseg, dk, s) != cudaSuccess)
+    return CKDA_ERR_CUDA;
+  a.split_pass = 2;
+  if (launch_fwd_chunk(a, s) != cudaSuccess) return CKDA_ERR_CUDA;
+  return CKDA_OK;
+}
+
+}  // extern "C"

@@ -178,6 +178,64 @@ ckda_status ckda_fwd_host(const void *q, const void *k, const void *v,
                           void *dev_scratch, size_t dev_scratch_bytes, void *stream);
 
 /*
+ * Sequence-split forward: the result of ckda_fwd (dense layout) for batches
+ * with fewer (sequence, head) pairs than the GPU has SMs, and long sequences.
+ *
+ * The recurrence is affine in the state: over a run of tokens the final state
+ * is P H_in + F, with P the product of the steps' transitions (dk x dk) and F
+ * the final state from H_in = 0 (Eq. (1) of "Complex KDA: Understanding and
+ * Enhancing the Expressivity of Kimi Delta Attention", applied step after
+ * step).  Like the chunked form ("Kimi Delta Attention: a bounded case study",
+ * "Chunkwise execution"), splitting a sequence this way changes the cost and
+ * not the result.  Each sequence is cut into `segments` runs of whole 64-token
+ * chunks.  Pass 1 computes, in parallel:
+ *   - segment 0 from h0, including its o;
+ *   - for each middle segment, F, and P (as the final state from [I | 0] with
+ *     v = 0).
+ * A scan then gives the state entering each segment.  Pass 2 runs segments
+ * 1..S-1 from those states and writes their o and the final state.
+ *
+ * Arguments, layouts and results are those of ckda_fwd with cu_seqlens = NULL
+ * and chunk_size = 0.  hT may alias h0.
+ *   segments : 0 picks the count for the current device (see
+ *              ckda_fwd_split_segments); 1 runs ckda_fwd unchanged; S >= 2
+ *              cuts each sequence into ceil(chunks / ceil(chunks / S)) <= S
+ *              segments.
+ * The split runs on the tensor-core shapes (io_dtype = CKDA_BF16, dv = 128,
+ * dk = 128 or 64).  With segments >= 2, other shapes return
+ * CKDA_ERR_UNSUPPORTED; with segments = 0 they run as ckda_fwd.
+ *
+ * workspace: device scratch of at least
+ * ckda_fwd_split_workspace_bytes(B, H, T, dk, dv, io_dtype, segments) bytes,
+ * 256-byte aligned.  It holds the status word (read it with ckda_fwd_status)
+ * and, with S >= 2, B * H * S fp32 [dk, 128] states, and as many transitions
+ * and zero-start states when S >= 3.  The call is asynchronous on `stream`:
+ * two launches of the forward kernel and one of the scan.
+ *
+ * Every segment's state passes through fp32, and each P carries the same
+ * tensor-core rounding as the state of one ckda_fwd.  The results therefore
+ * match ckda_fwd within the forward's tolerance, not bit for bit.
+ */
+/*
+ * The segment count ckda_fwd_split picks for segments = 0: the count, at most
+ * 16 and at most one per chunk, that minimises a model of the run time.  The
+ * model counts chunk steps: whole waves of CTAs over num_sms SMs for both
+ * passes, plus small terms for the state I/O and the scan.  A count must beat
+ * one plain pass by 10%; otherwise the answer is 1.  num_sms = 0 reads the
+ * current device.  Shapes off the tensor-core path, and bad sizes, give 1.
+ * Host-only; it enqueues nothing.
+ */
+int ckda_fwd_split_segments(int B, int H, int T, int dk, int dv, ckda_dtype io_dtype,
+                            int num_sms);
+size_t ckda_fwd_split_workspace_bytes(int B, int H, int T, int dk, int dv, ckda_dtype io_dtype,
+                                      int segments);
+ckda_status ckda_fwd_split(const void *q, const void *k, const void *v,
+                           const void *alpha, const void *beta, const float *h0,
+                           void *o, float *hT, int B, int H, int T, int dk, int dv,
+                           ckda_dtype io_dtype, float scale, int segments,
+                           void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Reads (and clears) the device status word of a workspace: waits for
  * `stream`, then returns CKDA_OK, CKDA_ERR_TIMEOUT or CKDA_ERR_RANGE for the
  * most recent ckda_fwd (or self-test) enqueued with that workspace.

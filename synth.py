@@ -42,6 +42,11 @@ WORKLOADS = {
     # head ("On State Reduction in Linear Attention": dk' = 64 of dv = 128)
     "kda_range_dk64": dict(B=8, H=16, T=2048, d=64, dv=128, dist="kda", dtype="bf16",
                            h0=False, seed=5, chunk=64),
+    # one long sequence of 16 heads: the paper's Fig. 5 timing shape (16 heads,
+    # d = 128, 32k tokens per step) as a single sequence, with the full CKDA
+    # gate distribution
+    "long_seq": dict(B=1, H=16, T=32768, d=128, dist="ckda", dtype="bf16", h0=True,
+                     seed=6, chunk=64),
 }
 
 _DT = {"fp32": torch.float32, "bf16": torch.bfloat16}

@@ -211,3 +211,76 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(ck, "_lib", None)
     with pytest.raises(ImportError):
         ck.lib()
+
+
+def _split_model(B, H, T, sms):
+    """The segment-count rule ckda_fwd_split_segments documents, restated:
+    both passes in whole waves of CTAs, plus 2 + (S - 2) / 2 chunk steps, and a
+    count must beat one plain pass by 10%."""
+    units, nch = B * H, (T + 63) // 64
+    waves = lambda n: -(-n // sms)
+    best, best_s = waves(units) * nch, 1
+    for S in range(2, min(16, nch) + 1):
+        sc = -(-nch // S)
+        if -(-nch // sc) != S:
+            continue
+        p1 = 2 * S - 3 if S >= 3 else 1
+        t = (waves(units * p1) + waves(units * (S - 1))) * sc + 2.0 + 0.5 * (S - 2)
+        if t < 0.9 * best:
+            best, best_s = t, S
+    return best_s
+
+
+def test_split_segments_rule(L):
+    f = L.ckda_fwd_split_segments
+    assert f(1, 16, 32768, 128, 128, 0, 152) == 1       # fp32: not the tensor-core path
+    assert f(1, 16, 32768, 96, 128, 1, 152) == 1        # dk 96: not the tensor-core path
+    assert f(8, 16, 2048, 128, 128, 1, 152) == 1        # 128 units already fill the GPU
+    assert f(1, 16, 64, 128, 128, 1, 152) == 1          # one chunk
+    assert f(0, 16, 32768, 128, 128, 1, 152) == 1       # bad size
+    for B, H, T, dk in ((1, 16, 32768, 128), (1, 1, 5000, 128), (2, 8, 20000, 64),
+                        (1, 32, 8192, 128), (1, 4, 700, 128)):
+        assert f(B, H, T, dk, 128, 1, 152) == _split_model(B, H, T, 152), (B, H, T)
+    s = f(1, 16, 32768, 128, 128, 1, 152)
+    assert s >= 6 and 16 * (2 * s - 3) <= 2 * 152
+
+
+def test_split_workspace_bytes(L):
+    f = L.ckda_fwd_split_workspace_bytes
+    tile = 128 * 128 * 4
+    assert f(1, 2, 1000, 128, 128, 1, 1) == 256
+    assert f(1, 2, 1000, 128, 128, 1, 2) == 256 + 1 * 2 * 2 * tile       # 16 chunks: 2 x 8
+    assert f(1, 2, 1000, 128, 128, 1, 4) == 256 + 3 * 2 * 4 * tile       # 4 x 4
+    assert f(1, 2, 1000, 128, 128, 1, 5) == 256 + 3 * 2 * 4 * tile       # 4 chunks each: 4
+    assert f(1, 2, 1000, 64, 128, 1, 4) == 256 + 3 * 2 * 4 * tile // 2
+    assert f(2, 3, 100, 128, 128, 1, 16) == 256 + 1 * 6 * 2 * tile       # 2 chunks: 2 segments
+    assert f(1, 2, 0, 128, 128, 1, 4) == 256
+    assert f(1, 2, 1000, 128, 128, 1, -1) == 0
+
+
+def test_split_argument_errors_are_synchronous(L):
+    """ckda_fwd_split rejects bad arguments and workspaces before launching."""
+    vp = ctypes.c_void_p
+    B, H, T, d = 1, 2, 1000, 128
+    need = L.ckda_fwd_split_workspace_bytes(B, H, T, d, d, 1, 4)
+
+    def f(**kw):
+        return L.ckda_fwd_split(*(vp(kw.get(n, 16)) for n in ("q", "k", "v", "alpha", "beta")),
+                                vp(kw.get("h0")), vp(kw.get("o", 16)), vp(kw.get("hT")),
+                                kw.get("B", B), kw.get("H", H), kw.get("T", T), kw.get("dk", d),
+                                kw.get("dv", d), kw.get("io", 1), kw.get("scale", 1.0),
+                                kw.get("seg", 4), vp(kw.get("ws", 4096)), kw.get("wsb", need),
+                                vp(None))
+    assert f(seg=-1) == 1
+    assert f(q=None) == 1
+    assert f(o=None) == 1
+    assert f(B=0) == 1
+    assert f(io=5) == 1
+    assert f(scale=float("nan")) == 1
+    assert f(q=16 + 2) == 1                               # TMA bases must be 16-byte aligned
+    assert f(io=0) == 2                                   # fp32: no split path
+    assert f(dk=96) == 2
+    assert f(dv=64) == 2
+    assert f(ws=None) == 5
+    assert f(wsb=need - 1) == 5
+    assert f(ws=4096 + 16) == 5
