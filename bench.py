@@ -238,31 +238,58 @@ def fwd_case(ck, x, steps, warmup, ws, stream, name):
                 wsp=wsp)
 
 
-def fwd_split_case(ck, x, steps, warmup, ws, stream, name):
-    """ckda_fwd_split at the automatic segment count, on a dense workload."""
+def dense_case(ck, d, steps, warmup, ws, stream, name, segments):
+    """ckda_fwd (segments = 1) or ckda_fwd_split on dense device tensors
+    d = (q, k, v, alpha, beta, h0)."""
     import torch
-    d = x.to("cuda")
-    B, H, T, dk = d.q.shape
-    dv = d.v.shape[-1]
-    S = ck.split_segments(B, H, T, dk, dv)
-    o = torch.empty_like(d.v)
+    q, k, v, a, b, h0 = d
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    o = torch.empty_like(v)
     hT = torch.empty((B, H, dk, dv), dtype=torch.float32, device="cuda")
-    wsp = torch.empty(ck.split_workspace_bytes(B, H, T, dk, dv, segments=S), dtype=torch.uint8,
-                      device="cuda")
+    wsp = torch.empty(ck.split_workspace_bytes(B, H, T, dk, dv, segments=segments),
+                      dtype=torch.uint8, device="cuda")
 
     def step():
-        ck.fwd_split(d.q, d.k, d.v, d.alpha, d.beta, d.h0, segments=S, o=o, hT=hT,
-                     workspace=wsp, stream=stream)
+        ck.fwd_split(q, k, v, a, b, h0, segments=segments, o=o, hT=hT, workspace=wsp,
+                     stream=stream)
 
     step()
     st = ck.fwd_status(wsp)
     if st != 0:
-        raise RuntimeError(f"{name} split: device status {ck.STATUS.get(st, st)}")
+        raise RuntimeError(f"{name}: device status {ck.STATUS.get(st, st)}")
     total, per = time_steps(step, steps, warmup, ws, stream)
     th = B * H * T
-    nbytes = fwd_bytes(B, H, T, dk, dv, B, d.h0 is not None, True)
-    return dict(total=total, per=per, th=th, bytes=nbytes, segments=S,
-                launches=3 if S >= 3 else (2 if S == 2 else 1))
+    nbytes = fwd_bytes(B, H, T, dk, dv, B, h0 is not None, True)
+    launches = 3 if segments >= 3 else (2 if segments == 2 else 1)
+    return {"value": round(th * steps / total, 1), "unit": UNIT,
+            "ms_per_step": round(total / steps * 1e3, 4), "steps": steps, "token_heads": th,
+            "segments": segments, "launches_per_step": launches,
+            "roofline": roofline(nbytes, per, "fwd_chunk", name)}
+
+
+def fig5_sweep(ck, steps, ws, stream):
+    """The paper's Fig. 5 shapes (16 heads, d = 128, 32k tokens per step, B x T from 16 x 2k
+    down) plus 1 x 32k, each through one pass (ckda_fwd) and the sequence split at its
+    automatic segment count.  Every point views the one `long_seq` draw as
+    [B, 16, 32768 / B, 128], with its h0 repeated over B."""
+    import synth
+    x = synth.make_workload("long_seq").to("cuda")
+    H, Ttot, dk = x.q.shape[1], x.q.shape[2], x.q.shape[3]
+    out = {}
+    for B in (16, 8, 4, 2, 1):
+        T = Ttot // B
+        v4 = lambda t: t.view(B, H, T, t.shape[-1])
+        d = (v4(x.q), v4(x.k), v4(x.v), v4(x.alpha), x.beta.view(B, H, T),
+             x.h0.expand(B, H, dk, dk).contiguous())
+        S = ck.split_segments(B, H, T, dk, 128)
+        name = "long_seq" if B == 1 else f"fig5_{B}x{T // 1024}k"
+        pt = {"B": B, "T": T, "plain": dense_case(ck, d, steps, 3, ws, stream, name, 1)}
+        if S > 1:
+            pt["split"] = dense_case(ck, d, 2 * steps, 3, ws, stream, name, S)
+            pt["split"]["roofline"]["traffic"] = None
+        out[f"{B}x{T // 1024}k"] = pt
+    return out
 
 
 def roofline(nbytes, per_ms, kernel, workload):
@@ -501,23 +528,10 @@ def run_ours(args):
                       "roofline": roofline(rr["bytes"], rr["per"], "fwd_chunk", nm)}
             del xx, rr
         out["workloads"] = wl
-    if ws == 1 and "long_seq" in extras:
-        # one sequence of 16 heads: the plain forward fills 16 SMs; the split
-        # forward runs each sequence as segments on the rest
-        xx = synth.make_workload("long_seq")
-        rp = fwd_case(ck, xx, 5, 3, ws, stream, "long_seq")
-        rs = fwd_split_case(ck, xx, 10, 3, ws, stream, "long_seq")
-        lw = {}
-        for key, rr, steps in (("plain", rp, 5), ("split", rs, 10)):
-            lw[key] = {"value": round(rr["th"] * steps / rr["total"], 1), "unit": UNIT,
-                       "ms_per_step": round(rr["total"] / steps * 1e3, 4), "steps": steps,
-                       "token_heads": rr["th"],
-                       "roofline": roofline(rr["bytes"], rr["per"], "fwd_chunk", "long_seq")}
-        lw["split"]["segments"] = rs["segments"]
-        lw["split"]["launches_per_step"] = rs["launches"]
-        lw["split"]["roofline"]["traffic"] = None
-        out.setdefault("workloads", {})["long_seq"] = lw
-        del xx, rp, rs
+    if ws == 1 and "fig5_sweep" in extras:
+        # 32k tokens per step of 16 heads at B x T = 16 x 2k .. 1 x 32k: one pass fills
+        # B x 16 SMs; the split runs the long sequences as segments
+        out["fig5_sweep"] = fig5_sweep(ck, 5, ws, stream)
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(x, args.cpu_seconds)
     if rank == 0:
@@ -591,9 +605,9 @@ def main():
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--extras",
                     default="decode,decode_raw,prep,bwd,ckda_full,ckda_varlen,kda_range_dk64,"
-                            "long_seq",
+                            "fig5_sweep",
                     help="comma list of extra measurements: decode, decode_raw, prep, bwd, "
-                         "ckda_full, ckda_varlen, kda_range_dk64, long_seq")
+                         "ckda_full, ckda_varlen, kda_range_dk64, fig5_sweep")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--bwd-units", type=int, default=0,
                     help="run the bwd extra on the first N (batch, head) units only")

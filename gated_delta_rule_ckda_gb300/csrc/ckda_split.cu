@@ -24,56 +24,78 @@
 namespace ckda {
 namespace {
 
-constexpr int kScanCols = 32;      // state columns per CTA
-constexpr int kScanThreads = 256;  // 8 row groups x 32 columns
+constexpr int kScanCols = 16;      // state columns per CTA
+constexpr int kScanThreads = 256;  // 16 row groups x 16 columns
 
-// One (sequence, head) and 32 state columns per CTA.  Thread (g, j) owns rows
-// g * DK/8 .. of column j.  P_s is staged in shared memory (rows of DK fp32),
-// and the column block of H_s stays there between steps; each output is an
-// fp32 dot product over m in order.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                   static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+               "l"(src)
+               : "memory");
+}
+
+// One (sequence, head) and 16 state columns per CTA.  Thread (g, j) owns rows
+// g, g + 16, ... of column j, so that the two row groups of a warp read
+// neighbouring rows of P (different banks) and the same H entries
+// (broadcast).  P_s (rows padded by 4 floats) is double-buffered: P_{s+1} is
+// copied in while step s computes.  The column block of H stays in shared
+// memory between steps; each output is an fp32 dot product over m in order.
 template <int DK>
 __global__ void __launch_bounds__(kScanThreads) seg_scan_kernel(float* state, const float* P,
                                                                 const float* F, int nseg) {
   extern __shared__ float4 scan_smem[];
-  float* Ps = reinterpret_cast<float*>(scan_smem);   // [DK][DK]
-  float* Hs = Ps + DK * DK;                          // [DK][32]
-  constexpr int R = DK / 8;
+  constexpr int LDP = DK + 4;
+  constexpr int R = DK / 16;
   constexpr size_t tile = (size_t)DK * 128;
+  float* Ps = reinterpret_cast<float*>(scan_smem);   // [2][DK][LDP]
+  float* Hs = Ps + 2 * DK * LDP;                     // [DK][16]
   const int ui = blockIdx.x, j0 = blockIdx.y * kScanCols;
-  const int tid = threadIdx.x, g = tid >> 5, j = tid & 31;
+  const int tid = threadIdx.x, g = tid >> 4, j = tid & 15;
   const size_t base = (size_t)ui * nseg * tile;
+  auto fetch_p = [&](int s) {
+    const float* Pg = P + base + (size_t)s * tile;
+    float* dst = Ps + (s & 1) * DK * LDP;
+    for (int e = tid; e < DK * DK / 4; e += kScanThreads) {
+      const int i = e / (DK / 4), m4 = e % (DK / 4);
+      cp_async16(dst + i * LDP + 4 * m4, Pg + (size_t)i * 128 + 4 * m4);
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  };
+  fetch_p(1);
   // H_1 (written by pass 1)
   for (int e = tid; e < DK * kScanCols; e += kScanThreads) {
     const int m = e / kScanCols, c = e % kScanCols;
     Hs[e] = state[base + tile + (size_t)m * 128 + j0 + c];
   }
   for (int s = 1; s + 1 < nseg; ++s) {
-    const float* Pg = P + base + (size_t)s * tile;
-    for (int e = tid; e < DK * DK / 4; e += kScanThreads) {
-      const int i = e / (DK / 4), m4 = e % (DK / 4);
-      reinterpret_cast<float4*>(Ps)[e] = *reinterpret_cast<const float4*>(Pg + (size_t)i * 128 + 4 * m4);
+    if (s + 2 < nseg) {
+      fetch_p(s + 1);
+      asm volatile("cp.async.wait_group 1;" ::: "memory");
+    } else {
+      asm volatile("cp.async.wait_group 0;" ::: "memory");
     }
-    __syncthreads();
-    float acc[R];
+    __syncthreads();   // P_s and H_s in place
+    const float* Pb = Ps + (s & 1) * DK * LDP;
     const float* Fg = F + base + (size_t)s * tile;
+    float acc[R];
 #pragma unroll
-    for (int r = 0; r < R; ++r) acc[r] = Fg[(size_t)(g * R + r) * 128 + j0 + j];
+    for (int r = 0; r < R; ++r) acc[r] = Fg[(size_t)(16 * r + g) * 128 + j0 + j];
 #pragma unroll 4
     for (int m = 0; m < DK; m += 4) {
       const float h0 = Hs[(m + 0) * kScanCols + j], h1 = Hs[(m + 1) * kScanCols + j];
       const float h2 = Hs[(m + 2) * kScanCols + j], h3 = Hs[(m + 3) * kScanCols + j];
 #pragma unroll
       for (int r = 0; r < R; ++r) {
-        const float4 p = *reinterpret_cast<const float4*>(Ps + (g * R + r) * DK + m);
+        const float4 p = *reinterpret_cast<const float4*>(Pb + (16 * r + g) * LDP + m);
         acc[r] = fmaf(p.w, h3, fmaf(p.z, h2, fmaf(p.y, h1, fmaf(p.x, h0, acc[r]))));
       }
     }
-    __syncthreads();   // every read of Hs and Ps for this step is done
+    __syncthreads();   // every read of H_s and of this P buffer is done
     float* Hg = state + base + (size_t)(s + 1) * tile;
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-      Hs[(g * R + r) * kScanCols + j] = acc[r];
-      Hg[(size_t)(g * R + r) * 128 + j0 + j] = acc[r];
+      Hs[(16 * r + g) * kScanCols + j] = acc[r];
+      Hg[(size_t)(16 * r + g) * 128 + j0 + j] = acc[r];
     }
   }
 }
@@ -84,7 +106,7 @@ cudaError_t launch_seg_scan(float* state, const float* P, const float* F, int un
                             int dk, cudaStream_t s) {
   if (units == 0 || nseg < 3) return cudaSuccess;
   const dim3 grid(units, 128 / kScanCols);
-  const size_t smem = ((size_t)dk * dk + (size_t)dk * kScanCols) * sizeof(float);
+  const size_t smem = (2 * (size_t)dk * (dk + 4) + (size_t)dk * kScanCols) * sizeof(float);
   auto kern = dk == 64 ? seg_scan_kernel<64> : seg_scan_kernel<128>;
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
