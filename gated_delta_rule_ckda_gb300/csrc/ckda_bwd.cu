@@ -12,32 +12,45 @@
 // Reverse step t, with D = dL/dS' (starting from dH_T):
 //
 //   D += (scale q) do^T,   du = D^T k,   dv = beta du,   dp = -beta du,
-//   dbeta = <du, v - p>,   dk = D u + Diag(alpha) S dp,
+//   dbeta = <du, v - p>,   dk = D u + G dp,
 //   dG = D + k dp^T,       dalpha_i = sum_j dG_ij S_ij,   D <- Diag(alpha) dG;
 //
-// dq = scale S' do comes from the forward pass, and dh0 is the final D.
+// dq = scale S' do comes from a forward pass, and dh0 is the final D.
 //
-// One block of 512 threads owns one (sequence, head).  S and D live in
-// shared memory as 128 x 129 fp32 tiles (the padding makes both a column walk
-// and a row walk conflict-free), so that each step alternates a column phase
-// (lane j = state column: p, u, du, dv, D += q do^T) and a row phase (lane i
-// = key channel: dk, dalpha, the update of D, and dq).  Each lane is four
-// threads, each walking a quarter of the other index; the quarters' partial
-// sums meet in shared memory.  Pass 1 runs the forward and stores the state
-// before every 64th token (a checkpoint).  Pass 2 takes the chunks of 64
-// tokens in reverse: it recomputes the chunk from its checkpoint, storing the
-// state before each token in the unit's chunk buffer and writing dq, then
-// walks the chunk backward, reading the next state back with cp.async into a
-// second tile while the current one is in use and fetching the next token's
-// vectors into registers.  Arithmetic is fp32.
+// Every column j of S evolves on its own; only p and du sum over the rows of
+// a column, while dq, dk, dalpha and dbeta sum over the columns.  So the
+// state is split by columns: a cluster of ceil(dv / 16) CTAs owns one
+// (sequence, head), each CTA 16 columns, and each of its 128 threads 16 rows
+// (16g .. 16g + 15) of one column of S and of D, in registers.  A column's
+// sums are 3-step shuffles among its 8 row groups (lanes of one warp).  The
+// sums over columns are reduced over the 4 columns of a warp by halving
+// exchanges, over the 4 warps in shared memory, and over the cluster's CTAs
+// through distributed shared memory, once per 8 tokens, in a fixed order.
+//
+// Recomputation: pass 1 runs the forward and keeps the state slice before
+// every 64th token (a checkpoint).  Pass 2 takes the 64-token chunks in
+// reverse: (a) it reruns the chunk from its checkpoint, keeping the state
+// before every 2nd token (a sub-checkpoint) and forming dq; (b) it takes the
+// chunk's 2-token groups in reverse, reruns each from its sub-checkpoint with
+// both states kept in registers, and walks them backward.  Two tokens per
+// group keep a thread at 128 registers, so that 4 CTAs share an SM (16 warps)
+// and 76 clusters of 8 run at once on 152 SMs.  Arithmetic is fp32.
 #include "ckda_internal.cuh"
 
 namespace ckda {
 namespace {
 
-constexpr int NB = 512;   // threads per block: 128 lanes x 4 parts
-constexpr int NL = 128;   // lanes: state columns (column phases) or key channels (row phases)
-constexpr int LD = 129;   // padded row stride of the shared tiles
+constexpr int CW = 16;           // state columns per CTA
+constexpr int NTH = 128;         // threads per CTA: 4 warps of 4 columns x 8 row groups
+constexpr int RPT = 16;          // rows per thread
+constexpr int CK = 64;           // tokens per checkpoint interval
+constexpr int SG = 2;            // tokens per group (sub-checkpoint interval)
+constexpr int NSG = CK / SG;     // groups per chunk
+constexpr int VP = 20;           // padded stride of a row group in a channel vector
+constexpr int VEC = 8 * VP;      // one padded channel vector (128 channels)
+constexpr int SLOT = NTH * RPT;  // floats of one CTA's state slice
+constexpr int PART = 2 * 128 + 4;  // per token: dk (128), dalpha (128), dbeta
+constexpr int RT = 8;            // tokens per reduction over the cluster
 
 struct BwdArgs {
   const void* q;
@@ -54,59 +67,98 @@ struct BwdArgs {
   void* galpha;
   void* gbeta;
   float* gh0;               // fp32
-  float* states;            // workspace: checkpoints, then one chunk buffer per unit
+  float* states;            // workspace: checkpoints, then each CTA's sub-checkpoints
   const int32_t* cu_seqlens;
   int N;                    // sequences (packed) or B (dense)
   int B, H, T, dk, dv;
+  int ncb;                  // CTAs (column blocks) per (sequence, head)
   float scale;
 };
 
-constexpr int CK = 64;    // tokens per checkpoint interval (and per recomputed chunk)
-
-// Workspace, in dk x dv fp32 tiles: the checkpoints (the state before every
-// CK-th token of each unit), then CK tiles per unit for the states of the
-// chunk being walked.  Dense units own ceil(T / CK) checkpoint slots each;
-// packed sequences share their head's ceil(T / CK) + N slots (sequence n
-// starting at token t0 takes slots floor(t0 / CK) + n onward, which never
-// overlap the next sequence's).
+// Checkpoint slots per workspace: dense units own ceil(T / CK) each; packed
+// sequences share their head's ceil(T / CK) + N (sequence n starting at token
+// t0 takes slots floor(t0 / CK) + n onward, which never overlap the next
+// sequence's).  A slot holds ncb state slices.
 __host__ __device__ inline size_t bwd_ck_slots(bool packed, int N, int H, int T) {
   const size_t per = ((size_t)T + CK - 1) / CK;
   return packed ? (size_t)H * (per + (size_t)N) : (size_t)N * H * per;
 }
 
-// two state tiles (pass 2 double-buffers them), the gradient tile D, seven
-// per-token vectors and five [4][128] tables of per-part partial sums
-constexpr size_t kSmemFloats = (size_t)3 * NL * LD + 7 * NL + 5 * 4 * NL + 32;
-constexpr size_t kSmemBytes = kSmemFloats * sizeof(float);
+// Shared memory, in floats.
+constexpr int SM_VEC = 0;                        // [2][SG][3][VEC]: k, alpha, scale q
+constexpr int SM_CV = SM_VEC + 2 * SG * 3 * VEC;  // [2][SG][2][CW]: v, do of this CTA's columns
+constexpr int SM_BV = SM_CV + 2 * SG * 2 * CW;   // [2][SG]: beta
+constexpr int SM_RED = SM_BV + 2 * SG;           // [2][SG][4 warps][2][VEC]: per-warp sums over columns
+constexpr int SM_REDB = SM_RED + 2 * SG * 4 * 2 * VEC;  // [2][SG][4]: per-warp dbeta
+constexpr int SM_PART = SM_REDB + 2 * SG * 4;    // [2][RT][PART]: the CTA's sums, per token
+constexpr int SM_TOK = SM_PART + 2 * RT * PART;  // [2][RT] int: the token of each PART row
+constexpr int SM_FLOATS = SM_TOK + 2 * RT;
+constexpr size_t kSmemBytes = (size_t)SM_FLOATS * sizeof(float);
 
-__device__ __forceinline__ void cp_async4(float* dst, const float* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
-                   static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
-               "l"(src)
-               : "memory");
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+// every thread of every CTA of the cluster; orders the shared-memory writes
+// before it with the distributed reads after it
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// a float of CTA `rank`'s shared memory, at the offset of p in this CTA's
+__device__ __forceinline__ float ld_cluster(const float* p, uint32_t rank) {
+  const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(p));
+  uint32_t ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(ra) : "memory");
+  return v;
+}
+// the sum over the cluster's ncb CTAs of the float at p, in rank order: every
+// remote load is issued before the first add waits
+__device__ __forceinline__ float sum_cluster(const float* p, int ncb) {
+  float x[8];
+#pragma unroll
+  for (int rr = 0; rr < 8; ++rr) x[rr] = rr < ncb ? ld_cluster(p, (uint32_t)rr) : 0.f;
+  float acc = x[0];
+#pragma unroll
+  for (int rr = 1; rr < 8; ++rr) acc += x[rr];
+  return acc;
+}
+
+// Sums x over the 4 columns of a warp (lanes l, l ^ 8, l ^ 16, l ^ 24 share a
+// row group).  N = 16: afterwards lane (cw, g) holds rows 16g + 4cw + e,
+// e < 4.  N = 32 (two quantities of 16 rows): quantity cw >> 1, rows
+// 16g + 8 (cw & 1) + e, e < 8.
+template <int N>
+__device__ __forceinline__ void sum_columns(float (&x)[N], float (&z)[N / 4], int lane) {
+  constexpr int H1 = N / 2, H2 = N / 4;
+  float y[H1];
+  const bool hi = (lane & 16) != 0, hi2 = (lane & 8) != 0;
+#pragma unroll
+  for (int e = 0; e < H1; ++e) {
+    const float send = hi ? x[e] : x[e + H1];
+    const float keep = hi ? x[e + H1] : x[e];
+    y[e] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+  }
+#pragma unroll
+  for (int e = 0; e < H2; ++e) {
+    const float send = hi2 ? y[e] : y[e + H2];
+    const float keep = hi2 ? y[e + H2] : y[e];
+    z[e] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+  }
+}
+__device__ __forceinline__ float sum_rows(float x) {   // over the 8 row groups of a column
+  x += __shfl_xor_sync(0xffffffffu, x, 1);
+  x += __shfl_xor_sync(0xffffffffu, x, 2);
+  return x + __shfl_xor_sync(0xffffffffu, x, 4);
+}
 
 template <typename IO>
-__global__ void __launch_bounds__(NB, 1) bwd_kernel(const BwdArgs a) {
-  extern __shared__ float smf[];
-  float* Sb[2] = {smf, smf + NL * LD};   // [128][LD] each
-  float* D = smf + 2 * NL * LD;          // [128][LD]
-  float* kv = D + NL * LD;               // k_t
-  float* av = kv + NL;                   // alpha_t
-  float* qv = av + NL;                   // scale * q_t
-  float* dov = qv + NL;                  // do_t
-  float* vv = dov + NL;                  // v_t
-  float* uv = vv + NL;                   // u_t
-  float* dpv = uv + NL;                  // dp_t
-  float* P0 = dpv + NL;                  // [4][128] per-part partial sums
-  float* P1 = P0 + 4 * NL;
-  float* P2 = P1 + 4 * NL;
-  float* P3 = P2 + 4 * NL;
-  float* P4 = P3 + 4 * NL;
-  float* red = P4 + 4 * NL;              // [0..3] dbeta per warp of part 0, [8] beta_t
-
+__global__ void __launch_bounds__(NTH, 4) bwd_kernel(const BwdArgs a) {
+  extern __shared__ float4 smem4[];
+  float* sm = reinterpret_cast<float*>(smem4);
   const IO* q = static_cast<const IO*>(a.q);
   const IO* k = static_cast<const IO*>(a.k);
   const IO* v = static_cast<const IO*>(a.v);
@@ -114,7 +166,8 @@ __global__ void __launch_bounds__(NB, 1) bwd_kernel(const BwdArgs a) {
   const IO* be = static_cast<const IO*>(a.beta);
   const IO* dout = static_cast<const IO*>(a.dout);
 
-  const int unit = blockIdx.x;
+  const uint32_t rank = cluster_rank();        // column block
+  const int unit = blockIdx.x / a.ncb;
   const int n = unit / a.H, h = unit % a.H;
   long row0;
   int len;
@@ -126,207 +179,340 @@ __global__ void __launch_bounds__(NB, 1) bwd_kernel(const BwdArgs a) {
     len = a.T;
     row0 = ((long)n * a.H + h) * a.T;
   }
-  const int tid = threadIdx.x;
-  const int x = tid & (NL - 1);          // lane: column j or channel i
-  const int part = tid >> 7;             // which quarter of the other index
   const int dk = a.dk, dv = a.dv;
-  const int lo = 32 * part;              // this part's range of the other index
-  const int hi_k = min(lo + 32, dk), hi_v = min(lo + 32, dv);
-  const bool colx = x < dv, rowx = x < dk;
+  const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+  const int g = lane & 7, cw = lane >> 3;
+  const int c = 4 * w + cw;                    // column within the block
+  const int j = (int)rank * CW + c;            // state column
+  const bool colok = j < dv;
   const size_t sidx = ((size_t)n * a.H + h) * (size_t)dk * dv;
-  const size_t tile = (size_t)dk * dv;
 
-  // token vectors, fetched one token ahead into registers by part 0
-  float rk = 0.f, ra = 1.f, rq = 0.f, rv = 0.f, rdo = 0.f, rb = 0.f;
-  auto fetch = [&](int t) {
-    if (part != 0 || t < 0 || t >= len) return;
-    const long r = row0 + t;
-    if (rowx) {
-      rk = ld_io(k + (size_t)r * dk + x);
-      ra = ld_io(al + (size_t)r * dk + x);
-      rq = a.scale * ld_io(q + (size_t)r * dk + x);
+  // ---- per-token vectors, a group of SG tokens at a time, double-buffered
+  float rk[SG], ra[SG], rq[SG], rv = 0.f, rdo = 0.f, rb = 0.f;
+  auto fetch = [&](int t0) {   // tokens t0 .. t0 + SG - 1 into registers
+#pragma unroll
+    for (int s = 0; s < SG; ++s) {
+      const int t = t0 + s;
+      rk[s] = 0.f; ra[s] = 1.f; rq[s] = 0.f;   // channels past dk, tokens past len: identity
+      if (t >= 0 && t < len && tid < dk) {
+        const size_t o = (size_t)(row0 + t) * dk + tid;
+        rk[s] = ld_io(k + o);
+        ra[s] = ld_io(al + o);
+        rq[s] = a.scale * ld_io(q + o);
+      }
     }
-    if (colx) {
-      rv = ld_io(v + (size_t)r * dv + x);
-      rdo = ld_io(dout + (size_t)r * dv + x);
+    rv = 0.f; rdo = 0.f; rb = 0.f;
+    if (tid < SG * CW) {
+      const int t = t0 + tid / CW, jj = (int)rank * CW + tid % CW;
+      if (t >= 0 && t < len && jj < dv) {
+        const size_t o = (size_t)(row0 + t) * dv + jj;
+        rv = ld_io(v + o);
+        rdo = ld_io(dout + o);
+      }
+    } else if (tid >= 64 && tid < 64 + SG) {
+      const int t = t0 + tid - 64;
+      if (t >= 0 && t < len) rb = ld_io(be + (row0 + t));
     }
-    if (x == 0) rb = ld_io(be + r);
   };
-  auto publish_vectors = [&]() {
-    if (part != 0) return;
-    if (rowx) { kv[x] = rk; av[x] = ra; qv[x] = rq; }
-    if (colx) { vv[x] = rv; dov[x] = rdo; }
-    if (x == 0) red[8] = rb;
+  auto publish = [&](int vb) {
+    float* V = sm + SM_VEC + vb * SG * 3 * VEC;
+    const int pi = VP * (tid >> 4) + (tid & 15);
+#pragma unroll
+    for (int s = 0; s < SG; ++s) {
+      V[(s * 3 + 0) * VEC + pi] = rk[s];
+      V[(s * 3 + 1) * VEC + pi] = ra[s];
+      V[(s * 3 + 2) * VEC + pi] = rq[s];
+    }
+    if (tid < SG * CW) {
+      float* C = sm + SM_CV + vb * SG * 2 * CW;
+      C[(tid / CW) * 2 * CW + tid % CW] = rv;
+      C[(tid / CW) * 2 * CW + CW + tid % CW] = rdo;
+    } else if (tid >= 64 && tid < 64 + SG) {
+      sm[SM_BV + vb * SG + tid - 64] = rb;
+    }
+  };
+  int vg = 0;   // running count of vector groups (buffer = parity)
+  // loads the group starting at t0 (the one fetched last), and fetches next0
+  auto next_group = [&](int t0_unused, int next0) -> int {
+    (void)t0_unused;
+    const int vb = vg & 1;
+    ++vg;
+    publish(vb);
+    __syncthreads();
+    fetch(next0);
+    return vb;
+  };
+  auto K_of = [&](int vb, int s) { return sm + SM_VEC + (vb * SG + s) * 3 * VEC + VP * g; };
+  auto v_of = [&](int vb, int s) { return sm[SM_CV + (vb * SG + s) * 2 * CW + c]; };
+  auto do_of = [&](int vb, int s) { return sm[SM_CV + (vb * SG + s) * 2 * CW + CW + c]; };
+  auto beta_of = [&](int vb, int s) { return sm[SM_BV + vb * SG + s]; };
+
+  // one forward step of this thread's rows of column j: Sn = alpha S + k u
+  auto forward = [&](const float (&S)[RPT], float (&Sn)[RPT], int vb, int s) {
+    const float* K = K_of(vb, s);
+    float gq[RPT];
+    float p = 0.f;
+#pragma unroll
+    for (int m = 0; m < RPT / 4; ++m) {
+      const float4 k4 = *reinterpret_cast<const float4*>(K + 4 * m);
+      const float4 a4 = *reinterpret_cast<const float4*>(K + VEC + 4 * m);
+      gq[4 * m + 0] = a4.x * S[4 * m + 0];
+      gq[4 * m + 1] = a4.y * S[4 * m + 1];
+      gq[4 * m + 2] = a4.z * S[4 * m + 2];
+      gq[4 * m + 3] = a4.w * S[4 * m + 3];
+      p = fmaf(k4.x, gq[4 * m + 0], p);
+      p = fmaf(k4.y, gq[4 * m + 1], p);
+      p = fmaf(k4.z, gq[4 * m + 2], p);
+      p = fmaf(k4.w, gq[4 * m + 3], p);
+    }
+    p = sum_rows(p);
+    const float u = beta_of(vb, s) * (v_of(vb, s) - p);
+#pragma unroll
+    for (int m = 0; m < RPT / 4; ++m) {
+      const float4 k4 = *reinterpret_cast<const float4*>(K + 4 * m);
+      Sn[4 * m + 0] = fmaf(k4.x, u, gq[4 * m + 0]);
+      Sn[4 * m + 1] = fmaf(k4.y, u, gq[4 * m + 1]);
+      Sn[4 * m + 2] = fmaf(k4.z, u, gq[4 * m + 2]);
+      Sn[4 * m + 3] = fmaf(k4.w, u, gq[4 * m + 3]);
+    }
   };
 
-  // checkpoint slots and this unit's chunk buffer (in tiles)
+  int rg = 0;   // running count of cluster reduction rounds (partial buffer = parity)
+  int gcount = 0;   // running count of reduced groups (per-warp sum buffer = parity)
+  float* red = sm + SM_RED;
+  float* part = sm + SM_PART;
+  int* tok = reinterpret_cast<int*>(sm + SM_TOK);
+  // the CTA's sum over its 4 warps of the per-warp sums of token s of group
+  // buffer gb (after a barrier), into row `slot` of partial buffer pb
+  auto cta_sum = [&](int gb, int s, int pb, int slot, int nq) {
+    const float* R = red + (gb * SG + s) * 4 * 2 * VEC;
+    for (int e = tid; e < nq * 128; e += NTH) {
+      const int qq = e >> 7, i = e & 127;
+      const int off = qq * VEC + VP * (i >> 4) + (i & 15);
+      float x = 0.f;
+#pragma unroll
+      for (int ww = 0; ww < 4; ++ww) x += R[ww * 2 * VEC + off];
+      part[(pb * RT + slot) * PART + e] = x;
+    }
+  };
+  // the cluster's sums of the cnt tokens in partial buffer pb: each CTA
+  // takes every ncb-th item; dq (nq = 1) or dk, dalpha and dbeta (nq = 2)
+  auto cluster_reduce = [&](int pb, int cnt, int nq) {
+    cluster_sync();
+    const int per = nq * dk;
+    const int items = cnt * per + (nq == 2 ? cnt : 0);
+    for (int it = (int)rank + a.ncb * tid; it < items; it += a.ncb * NTH) {
+      int slot, e;
+      if (it < cnt * per) {
+        slot = it / per;
+        const int rem = it % per;
+        e = (rem / dk) * 128 + rem % dk;
+      } else {
+        slot = it - cnt * per;
+        e = 256;
+      }
+      const int t = tok[pb * RT + slot];
+      const float x = sum_cluster(part + (pb * RT + slot) * PART + e, a.ncb);
+      if (t < len) {
+        const size_t row = (size_t)(row0 + t);
+        if (nq == 1) st_io(static_cast<IO*>(a.gq) + row * dk + e, a.scale * x);
+        else if (e == 256) st_io(static_cast<IO*>(a.gbeta) + row, x);
+        else if (e < 128) st_io(static_cast<IO*>(a.gk) + row * dk + e, x);
+        else st_io(static_cast<IO*>(a.galpha) + row * dk + (e - 128), x);
+      }
+    }
+  };
+
+  float S[RPT], D[RPT];
+  const int i0 = 16 * g;
+  // ------------------------------------------------ pass 1: checkpoints
+#pragma unroll
+  for (int r = 0; r < RPT; ++r)
+    S[r] = (a.h0 && colok && i0 + r < dk) ? a.h0[sidx + (size_t)(i0 + r) * dv + j] : 0.f;
   const size_t per_unit_ck = ((size_t)a.T + CK - 1) / CK;
   const size_t ck0 = a.cu_seqlens
                          ? (size_t)h * (per_unit_ck + a.N) + (size_t)(a.cu_seqlens[n] / CK) + n
                          : (size_t)unit * per_unit_ck;
-  float* chunkbuf = a.states + (bwd_ck_slots(a.cu_seqlens != nullptr, a.N, a.H, a.T) +
-                                (size_t)unit * CK) * tile;
-  auto ck_tile = [&](int m) { return a.states + (ck0 + m) * tile; };
-
-  // one forward step on the tile S (token t's vectors published and visible):
-  // S <- Diag(alpha) S + k u^T with u = beta (v - (Diag(alpha) S)^T k)
-  auto forward_step = [&](float* S) {
-    if (colx) {
-      float p = 0.f;
-#pragma unroll 4
-      for (int i = lo; i < hi_k; ++i) p = fmaf(kv[i] * av[i], S[i * LD + x], p);
-      P0[part * NL + x] = p;
-    }
-    __syncthreads();
-    if (colx) {
-      const float p = P0[x] + P0[NL + x] + P0[2 * NL + x] + P0[3 * NL + x];
-      const float u = red[8] * (vv[x] - p);
-#pragma unroll 4
-      for (int i = lo; i < hi_k; ++i) S[i * LD + x] = fmaf(av[i], S[i * LD + x], kv[i] * u);
-    }
-    __syncthreads();
+  auto ck_slot = [&](int m) { return a.states + ((ck0 + m) * a.ncb + rank) * SLOT; };
+  float* subck = a.states + (bwd_ck_slots(a.cu_seqlens != nullptr, a.N, a.H, a.T) * a.ncb +
+                             ((size_t)unit * a.ncb + rank) * NSG) * SLOT;
+  auto store_slice = [&](const float (&X)[RPT], float* dst) {
+#pragma unroll
+    for (int r = 0; r < RPT; ++r) dst[r * NTH + tid] = X[r];
   };
-  auto store_tile = [&](const float* S, float* dst) {  // this thread's rows of column x
-    if (colx)
-      for (int i = lo; i < hi_k; ++i) dst[(size_t)i * dv + x] = S[i * LD + x];
+  auto load_slice = [&](float (&X)[RPT], const float* src) {
+#pragma unroll
+    for (int r = 0; r < RPT; ++r) X[r] = src[r * NTH + tid];
   };
 
-  // ------------------------------------------------ pass 1: checkpoints
-  float* S = Sb[0];
-  if (colx)
-    for (int i = lo; i < hi_k; ++i) S[i * LD + x] = a.h0 ? a.h0[sidx + (size_t)i * dv + x] : 0.f;
+  const int ngr = (len + SG - 1) / SG;
   fetch(0);
-  for (int t = 0; t < len; ++t) {
-    publish_vectors();
-    if (t % CK == 0) store_tile(S, ck_tile(t / CK));
-    __syncthreads();
-    fetch(t + 1);
-    forward_step(S);
+  for (int gi = 0; gi < ngr; ++gi) {
+    if (gi % NSG == 0) store_slice(S, ck_slot(gi / NSG));
+    const int vb = next_group(gi * SG, (gi + 1) * SG);
+#pragma unroll
+    for (int s = 0; s < SG; ++s) {
+      float Sn[RPT];
+      forward(S, Sn, vb, s);
+#pragma unroll
+      for (int r = 0; r < RPT; ++r) S[r] = Sn[r];
+    }
   }
 
   // ------------------------------------------------ pass 2: reverse, by chunk
-  if (colx)
-    for (int i = lo; i < hi_k; ++i) D[i * LD + x] = a.dhT ? a.dhT[sidx + (size_t)i * dv + x] : 0.f;
-  // the state before token t (of the chunk starting at t0) goes to tile t mod 2
-  auto fetch_state = [&](int t, int t0) {
-    if (t < t0 || !colx) return;
-    const float* st = chunkbuf + (size_t)(t - t0) * tile + x;
-    float* dst = Sb[t & 1];
-    for (int i = lo; i < hi_k; ++i) cp_async4(dst + i * LD + x, st + (size_t)i * dv);
-  };
+#pragma unroll
+  for (int r = 0; r < RPT; ++r)
+    D[r] = (a.dhT && colok && i0 + r < dk) ? a.dhT[sidx + (size_t)(i0 + r) * dv + j] : 0.f;
+  IO* gv_o = static_cast<IO*>(a.gv);
   const int nck = (len + CK - 1) / CK;
   for (int m = nck - 1; m >= 0; --m) {
-    const int t0 = m * CK, t1 = min(len, t0 + CK);
-    // (a) recompute the chunk from its checkpoint, storing the state before
-    // each token and writing dq = scale S' do
-    __syncthreads();  // the previous walk's last reads of the tiles are done
-    if (colx) {
-      const float* src = ck_tile(m);
-      for (int i = lo; i < hi_k; ++i) S[i * LD + x] = src[(size_t)i * dv + x];
-    }
-    fetch(t0);
-    for (int t = t0; t < t1; ++t) {
-      const long r = row0 + t;
-      publish_vectors();
-      store_tile(S, chunkbuf + (size_t)(t - t0) * tile);
-      __syncthreads();
-      if (t + 1 < t1) fetch(t + 1);
-      forward_step(S);
-      if (rowx) {  // dq_i = scale * sum_j S'_ij do_j (scale is applied below)
-        float acc = 0.f;
-#pragma unroll 4
-        for (int j = lo; j < hi_v; ++j) acc = fmaf(S[x * LD + j], dov[j], acc);
-        P1[part * NL + x] = acc;
-      }
-      __syncthreads();
-      if (part == 0 && rowx)
-        st_io(static_cast<IO*>(a.gq) + (size_t)r * dk + x,
-              a.scale * (P1[x] + P1[NL + x] + P1[2 * NL + x] + P1[3 * NL + x]));
-    }
-    __syncthreads();  // the recompute's reads of S and its global stores are done
-    // (b) walk the chunk backward
-    fetch_state(t1 - 1, t0);
-    cp_async_commit();
-    fetch(t1 - 1);
-    for (int t = t1 - 1; t >= t0; --t) {
-      const long r = row0 + t;
-      float* St = Sb[t & 1];
-      cp_async_wait_all();
-      publish_vectors();
-      __syncthreads();  // S_t, the vectors, and the previous step's D are visible
-      fetch_state(t - 1, t0);
-      cp_async_commit();
-      if (t - 1 >= t0) fetch(t - 1);
-      if (colx) {
-        const float doj = dov[x];
-        float p = 0.f, du = 0.f;
-#pragma unroll 4
-        for (int i = lo; i < hi_k; ++i) {
-          const float d = fmaf(qv[i], doj, D[i * LD + x]);
-          D[i * LD + x] = d;
-          p = fmaf(kv[i] * av[i], St[i * LD + x], p);
-          du = fmaf(kv[i], d, du);
-        }
-        P0[part * NL + x] = p;
-        P1[part * NL + x] = du;
-      }
-      __syncthreads();
-      if (part == 0) {
-        const float bt = red[8];
-        float dbp = 0.f;
-        if (colx) {
-          const float p = P0[x] + P0[NL + x] + P0[2 * NL + x] + P0[3 * NL + x];
-          const float du = P1[x] + P1[NL + x] + P1[2 * NL + x] + P1[3 * NL + x];
-          const float vj = vv[x];
-          uv[x] = bt * (vj - p);
-          dpv[x] = -bt * du;
-          st_io(static_cast<IO*>(a.gv) + (size_t)r * dv + x, bt * du);
-          dbp = du * (vj - p);
-        }
+    const int g0 = m * NSG, g1 = min(ngr, g0 + NSG);
+    // (a) rerun the chunk, keeping sub-checkpoints, and form dq
+    load_slice(S, ck_slot(m));
+    __syncthreads();   // the previous walk's reads of the vector buffers are done
+    fetch(g0 * SG);
+    int pend = 0;   // tokens in the current partial buffer
+    for (int gi = g0; gi < g1; ++gi) {
+      store_slice(S, subck + (size_t)(gi - g0) * SLOT);
+      const int vb = next_group(gi * SG, (gi + 1) * SG);
+      const int gb = gcount & 1;
+      ++gcount;
 #pragma unroll
-        for (int mm = 16; mm >= 1; mm >>= 1) dbp += __shfl_xor_sync(0xffffffffu, dbp, mm);
-        if ((x & 31) == 0) red[x >> 5] = dbp;
-      }
-      __syncthreads();
-      if (rowx) {
-        const float ki = kv[x], ai = av[x];
-        float gk = 0.f, gs = 0.f, ga = 0.f;
-#pragma unroll 4
-        for (int j = lo; j < hi_v; ++j) {
-          const float d = D[x * LD + j], s = St[x * LD + j], dpj = dpv[j];
-          gk = fmaf(d, uv[j], gk);
-          gs = fmaf(s, dpj, gs);
-          const float dG = fmaf(ki, dpj, d);
-          ga = fmaf(dG, s, ga);
-          D[x * LD + j] = ai * dG;
+      for (int s = 0; s < SG; ++s) {
+        float Sn[RPT];
+        forward(S, Sn, vb, s);
+        const float dov = do_of(vb, s);
+        float x[RPT], z[RPT / 4];
+#pragma unroll
+        for (int r = 0; r < RPT; ++r) {
+          S[r] = Sn[r];
+          x[r] = Sn[r] * dov;
         }
-        P2[part * NL + x] = fmaf(ai, gs, gk);
-        P3[part * NL + x] = ga;
+        sum_columns<RPT>(x, z, lane);
+        *reinterpret_cast<float4*>(red + ((gb * SG + s) * 4 + w) * 2 * VEC + VP * g + 4 * cw) =
+            make_float4(z[0], z[1], z[2], z[3]);
       }
       __syncthreads();
-      if (part == 0 && rowx) {
-        st_io(static_cast<IO*>(a.gk) + (size_t)r * dk + x,
-              P2[x] + P2[NL + x] + P2[2 * NL + x] + P2[3 * NL + x]);
-        st_io(static_cast<IO*>(a.galpha) + (size_t)r * dk + x,
-              P3[x] + P3[NL + x] + P3[2 * NL + x] + P3[3 * NL + x]);
+      const int pb = rg & 1;
+#pragma unroll
+      for (int s = 0; s < SG; ++s) {
+        cta_sum(gb, s, pb, pend + s, 1);
+        if (tid == 0) tok[pb * RT + pend + s] = gi * SG + s;
       }
-      if (tid == 0) st_io(static_cast<IO*>(a.gbeta) + r, red[0] + red[1] + red[2] + red[3]);
+      pend += SG;
+      if (pend == RT || gi == g1 - 1) {   // dq of these tokens
+        cluster_reduce(pb, pend, 1);
+        ++rg;
+        pend = 0;
+      }
     }
-    cp_async_wait_all();
+    // (b) walk the chunk's groups backward
+    __syncthreads();   // (a)'s reads of the vector buffers are done
+    fetch((g1 - 1) * SG);
+    pend = 0;
+    for (int gi = g1 - 1; gi >= g0; --gi) {
+      float st[SG][RPT];
+      load_slice(st[0], subck + (size_t)(gi - g0) * SLOT);
+      const int vb = next_group(gi * SG, (gi - 1) * SG);
+      const int gb = gcount & 1;
+      ++gcount;
+#pragma unroll
+      for (int s = 0; s + 1 < SG; ++s) forward(st[s], st[s + 1], vb, s);
+#pragma unroll
+      for (int s = SG - 1; s >= 0; --s) {
+        const int t = gi * SG + s;
+        const float* K = K_of(vb, s);
+        const float dov = do_of(vb, s), vj = v_of(vb, s), bt = beta_of(vb, s);
+        float p = 0.f, du = 0.f;
+#pragma unroll
+        for (int mm = 0; mm < RPT / 4; ++mm) {
+          const float4 k4 = *reinterpret_cast<const float4*>(K + 4 * mm);
+          const float4 a4 = *reinterpret_cast<const float4*>(K + VEC + 4 * mm);
+          const float4 q4 = *reinterpret_cast<const float4*>(K + 2 * VEC + 4 * mm);
+          const float kk[4] = {k4.x, k4.y, k4.z, k4.w}, aa[4] = {a4.x, a4.y, a4.z, a4.w};
+          const float qq[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int r = 4 * mm + e;
+            D[r] = fmaf(qq[e], dov, D[r]);
+            p = fmaf(kk[e] * aa[e], st[s][r], p);
+            du = fmaf(kk[e], D[r], du);
+          }
+        }
+        p = sum_rows(p);
+        du = sum_rows(du);
+        const float u = bt * (vj - p), dp = -bt * du;
+        if (g == 0 && colok && t < len) st_io(gv_o + (size_t)(row0 + t) * dv + j, bt * du);
+        float x[2 * RPT];
+#pragma unroll
+        for (int mm = 0; mm < RPT / 4; ++mm) {
+          const float4 k4 = *reinterpret_cast<const float4*>(K + 4 * mm);
+          const float4 a4 = *reinterpret_cast<const float4*>(K + VEC + 4 * mm);
+          const float kk[4] = {k4.x, k4.y, k4.z, k4.w}, aa[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int r = 4 * mm + e;
+            const float sp = st[s][r];
+            x[r] = fmaf(D[r], u, aa[e] * sp * dp);        // dk
+            const float dG = fmaf(kk[e], dp, D[r]);
+            x[RPT + r] = dG * sp;                         // dalpha
+            D[r] = aa[e] * dG;
+          }
+        }
+        float z[2 * RPT / 4];
+        sum_columns<2 * RPT>(x, z, lane);
+        float* R = red + ((gb * SG + s) * 4 + w) * 2 * VEC + (cw >> 1) * VEC + VP * g +
+                   8 * (cw & 1);
+        *reinterpret_cast<float4*>(R) = make_float4(z[0], z[1], z[2], z[3]);
+        *reinterpret_cast<float4*>(R + 4) = make_float4(z[4], z[5], z[6], z[7]);
+        // dbeta over this warp's 4 columns
+        float db = (g == 0) ? du * (vj - p) : 0.f;
+        db += __shfl_xor_sync(0xffffffffu, db, 8);
+        db += __shfl_xor_sync(0xffffffffu, db, 16);
+        if (lane == 0) sm[SM_REDB + (gb * SG + s) * 4 + w] = db;
+      }
+      __syncthreads();
+      const int pb = rg & 1;
+#pragma unroll
+      for (int s = 0; s < SG; ++s) {
+        cta_sum(gb, s, pb, pend + s, 2);
+        if (tid == 0) {
+          const float* RB = sm + SM_REDB + (gb * SG + s) * 4;
+          part[(pb * RT + pend + s) * PART + 256] = RB[0] + RB[1] + RB[2] + RB[3];
+          tok[pb * RT + pend + s] = gi * SG + s;
+        }
+      }
+      pend += SG;
+      if (pend == RT || gi == g0) {   // dk, dalpha, dbeta of these tokens
+        cluster_reduce(pb, pend, 2);
+        ++rg;
+        pend = 0;
+      }
+    }
   }
-  __syncthreads();
-  if (a.gh0 && colx)
-    for (int i = lo; i < hi_k; ++i) a.gh0[sidx + (size_t)i * dv + x] = D[i * LD + x];
+  if (a.gh0 && colok) {
+#pragma unroll
+    for (int r = 0; r < RPT; ++r)
+      if (i0 + r < dk) a.gh0[sidx + (size_t)(i0 + r) * dv + j] = D[r];
+  }
+  cluster_sync();   // no CTA leaves while another may still read its shared memory
 }
 
 template <typename IO>
 cudaError_t launch_io(const BwdArgs& a, int units, cudaStream_t s) {
-  cudaError_t err = cudaFuncSetAttribute(bwd_kernel<IO>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSmemBytes);
-  if (err != cudaSuccess) return err;
-  bwd_kernel<IO><<<units, NB, kSmemBytes, s>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(units * a.ncb));
+  cfg.blockDim = dim3(NTH);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = (unsigned)a.ncb;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, bwd_kernel<IO>, a);
 }
 
 }  // namespace
@@ -338,8 +524,9 @@ extern "C" size_t ckda_bwd_workspace_bytes(int num_seqs, int B, int H, int T, in
   if (B < 1 || H < 1 || T < 0 || dk < 1 || dv < 1 || num_seqs < 0) return 0;
   const bool packed = num_seqs > 0;
   const int N = packed ? num_seqs : B;
-  const size_t tiles = bwd_ck_slots(packed, N, H, T) + (size_t)N * H * CK;
-  return tiles * (size_t)dk * dv * sizeof(float);
+  const size_t ncb = (size_t)(dv + CW - 1) / CW;
+  const size_t slices = bwd_ck_slots(packed, N, H, T) * ncb + (size_t)N * H * ncb * NSG;
+  return slices * SLOT * sizeof(float);
 }
 
 extern "C" ckda_status ckda_bwd(const void* q, const void* k, const void* v, const void* alpha,
@@ -360,12 +547,14 @@ extern "C" ckda_status ckda_bwd(const void* q, const void* k, const void* v, con
   if (T > 0 && (!q || !k || !v || !alpha || !beta || !d_o || !d_q || !d_k || !d_v ||
                 !d_alpha || !d_beta))
     return CKDA_ERR_INVALID_ARG;
-  if (dk > NL || dv > NL) return CKDA_ERR_UNSUPPORTED;
+  if (dk > 128 || dv > 128) return CKDA_ERR_UNSUPPORTED;
   if ((long long)B * H * T > 0x7fffffffLL) return CKDA_ERR_UNSUPPORTED;
+  const int units = (cu_seqlens ? num_seqs : B) * H;
+  const int ncb = (dv + CW - 1) / CW;
+  if ((long long)units * ncb > 0x7fffffffLL) return CKDA_ERR_UNSUPPORTED;
   const size_t need = ckda_bwd_workspace_bytes(cu_seqlens ? num_seqs : 0, B, H, T, dk, dv);
   if (need > 0 && (!workspace || workspace_bytes < need)) return CKDA_ERR_WORKSPACE;
   if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 15) != 0) return CKDA_ERR_WORKSPACE;
-  const int units = (cu_seqlens ? num_seqs : B) * H;
   BwdArgs a{};
   a.q = q; a.k = k; a.v = v; a.alpha = alpha; a.beta = beta; a.dout = d_o;
   a.h0 = h0; a.dhT = d_hT;
@@ -374,6 +563,7 @@ extern "C" ckda_status ckda_bwd(const void* q, const void* k, const void* v, con
   a.cu_seqlens = cu_seqlens;
   a.N = cu_seqlens ? num_seqs : B;
   a.B = B; a.H = H; a.T = T; a.dk = dk; a.dv = dv;
+  a.ncb = ncb;
   a.scale = scale;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const cudaError_t err = io_dtype == CKDA_F32 ? launch_io<float>(a, units, s)
