@@ -149,6 +149,12 @@ __device__ __forceinline__ void sum_columns(float (&x)[N], float (&z)[N / 4], in
     z[e] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
   }
 }
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+__device__ __forceinline__ void prefetch_l1(const void* p) {
+  asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+}
 __device__ __forceinline__ float sum_rows(float x) {   // over the 8 row groups of a column
   x += __shfl_xor_sync(0xffffffffu, x, 1);
   x += __shfl_xor_sync(0xffffffffu, x, 2);
@@ -231,15 +237,36 @@ __global__ void __launch_bounds__(NTH, 4) bwd_kernel(const BwdArgs a) {
       sm[SM_BV + vb * SG + tid - 64] = rb;
     }
   };
+  // L2 prefetch of the group starting at t0 (one ahead of the register fetch)
+  auto prefetch_group = [&](int t0) {
+#pragma unroll
+    for (int s = 0; s < SG; ++s) {
+      const int t = t0 + s;
+      if (t >= 0 && t < len && tid < dk) {
+        const size_t o = (size_t)(row0 + t) * dk + tid;
+        prefetch_l2(k + o);
+        prefetch_l2(al + o);
+        prefetch_l2(q + o);
+      }
+    }
+    if (tid < SG * CW) {
+      const int t = t0 + tid / CW, jj = (int)rank * CW + tid % CW;
+      if (t >= 0 && t < len && jj < dv) {
+        prefetch_l2(v + (size_t)(row0 + t) * dv + jj);
+        prefetch_l2(dout + (size_t)(row0 + t) * dv + jj);
+      }
+    }
+  };
   int vg = 0;   // running count of vector groups (buffer = parity)
-  // loads the group starting at t0 (the one fetched last), and fetches next0
-  auto next_group = [&](int t0_unused, int next0) -> int {
-    (void)t0_unused;
+  // loads the group fetched last, fetches the one starting at next0 into
+  // registers and prefetches the one after it (at next0 + step) into L2
+  auto next_group = [&](int next0, int step) -> int {
     const int vb = vg & 1;
     ++vg;
     publish(vb);
     __syncthreads();
     fetch(next0);
+    prefetch_group(next0 + step);
     return vb;
   };
   auto K_of = [&](int vb, int s) { return sm + SM_VEC + (vb * SG + s) * 3 * VEC + VP * g; };
@@ -347,9 +374,10 @@ __global__ void __launch_bounds__(NTH, 4) bwd_kernel(const BwdArgs a) {
 
   const int ngr = (len + SG - 1) / SG;
   fetch(0);
+  prefetch_group(SG);
   for (int gi = 0; gi < ngr; ++gi) {
     if (gi % NSG == 0) store_slice(S, ck_slot(gi / NSG));
-    const int vb = next_group(gi * SG, (gi + 1) * SG);
+    const int vb = next_group((gi + 1) * SG, SG);
 #pragma unroll
     for (int s = 0; s < SG; ++s) {
       float Sn[RPT];
@@ -371,10 +399,11 @@ __global__ void __launch_bounds__(NTH, 4) bwd_kernel(const BwdArgs a) {
     load_slice(S, ck_slot(m));
     __syncthreads();   // the previous walk's reads of the vector buffers are done
     fetch(g0 * SG);
+    prefetch_group((g0 + 1) * SG);
     int pend = 0;   // tokens in the current partial buffer
     for (int gi = g0; gi < g1; ++gi) {
       store_slice(S, subck + (size_t)(gi - g0) * SLOT);
-      const int vb = next_group(gi * SG, (gi + 1) * SG);
+      const int vb = next_group((gi + 1) * SG, SG);
       const int gb = gcount & 1;
       ++gcount;
 #pragma unroll
@@ -409,11 +438,16 @@ __global__ void __launch_bounds__(NTH, 4) bwd_kernel(const BwdArgs a) {
     // (b) walk the chunk's groups backward
     __syncthreads();   // (a)'s reads of the vector buffers are done
     fetch((g1 - 1) * SG);
+    prefetch_group((g1 - 2) * SG);
     pend = 0;
     for (int gi = g1 - 1; gi >= g0; --gi) {
       float st[SG][RPT];
       load_slice(st[0], subck + (size_t)(gi - g0) * SLOT);
-      const int vb = next_group(gi * SG, (gi - 1) * SG);
+      if (gi > g0) {   // the next group's sub-checkpoint into L1
+#pragma unroll
+        for (int r = 0; r < RPT; ++r) prefetch_l1(subck + (size_t)(gi - 1 - g0) * SLOT + r * NTH + tid);
+      }
+      const int vb = next_group((gi - 1) * SG, -SG);
       const int gb = gcount & 1;
       ++gcount;
 #pragma unroll
