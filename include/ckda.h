@@ -307,17 +307,22 @@ ckda_status ckda_decode_step_raw(const void *q_raw, const void *k_raw, const voi
  * h0 == NULL: zero initial state.  d_hT == NULL: no gradient on the final
  * state.  d_h0 == NULL: not stored.  Gradient buffers must not alias inputs.
  * Any dk, dv <= 128 and either I/O dtype; arithmetic is fp32, token by token
- * on CUDA cores (one block per (sequence, head)): pass 1 reruns the forward
- * and keeps the state before every 64th token in `workspace`; pass 2 takes
- * the 64-token chunks in reverse, recomputing each one's states from its
- * checkpoint and walking it backward.  workspace: device memory of at least
- * ckda_bwd_workspace_bytes(num_seqs, B, H, T, dk, dv) bytes (num_seqs = 0
- * for dense input): dk*dv*4 bytes for each checkpoint (ceil(T/64) per dense
- * (batch, head), ceil(T/64) + num_seqs per head when packed) and 64 more
- * tiles per (sequence, head) for the chunk being walked; 16-byte aligned,
- * owned by the caller; its contents are scratch.  Argument errors return synchronously
- * with nothing launched; otherwise CKDA_OK once enqueued on `stream`.  The
- * library allocates nothing.
+ * on CUDA cores.  Each (sequence, head) runs as one thread-block cluster of
+ * ceil(dv / 16) CTAs, each holding 16 columns of the state in registers;
+ * sums over columns are reduced in a fixed order, so results are
+ * deterministic.  Pass 1 reruns the forward and keeps the state before every
+ * 64th token in `workspace`.  Pass 2 takes the 64-token chunks in reverse:
+ * it reruns a chunk from its checkpoint, keeping the state before every 2nd
+ * token, and walks the chunk backward 2 tokens at a time.
+ *
+ * workspace: device memory of at least ckda_bwd_workspace_bytes(num_seqs, B,
+ * H, T, dk, dv) bytes (num_seqs = 0 for dense input), 16-byte aligned, owned
+ * by the caller; its contents are scratch.  It holds state slices of 8 KiB
+ * (one CTA's 16 columns).  There are ceil(dv / 16) of them per checkpoint:
+ * ceil(T/64) checkpoints per dense (batch, head), ceil(T/64) + num_seqs per
+ * head when packed.  Each CTA also has 32 slices for the chunk being walked.
+ * Argument errors return synchronously with nothing launched; otherwise
+ * CKDA_OK once enqueued on `stream`.  The library allocates nothing.
  */
 size_t ckda_bwd_workspace_bytes(int num_seqs, int B, int H, int T, int dk, int dv);
 ckda_status ckda_bwd(const void *q, const void *k, const void *v, const void *alpha,
