@@ -428,6 +428,62 @@ def test_packed_equals_separate_and_resume_split():
     del sl
 
 
+@pytest.mark.parametrize("dk,dv", [(6, 6), (4, 7)])
+def test_segment_operators_compose(dk, dv):
+    """Paper Eq. (1) read over a run of tokens: the final state is affine in
+    the initial one, H_out = P H_in + F, with P the product of the run's
+    transitions (the final state from [I | 0] with v = 0) and F the final
+    state from zero.  Chaining segment operators by that scan, and then
+    rerunning each segment from its scanned state, gives the outputs and final
+    state of one pass (the bounded case study's "Chunkwise execution": an
+    execution strategy that changes cost, never the numbers)."""
+    rng = np.random.default_rng(700 + dk)
+    T, cuts = 37, [0, 12, 24, 37]
+    q = rng.standard_normal((1, 1, T, dk))
+    k = rng.standard_normal((1, 1, T, dk))
+    k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = rng.standard_normal((1, 1, T, dv))
+    al = rng.uniform(-1, 1, (1, 1, T, dk))
+    al[rng.random(al.shape) < 0.1] = -1.0
+    al[rng.random(al.shape) < 0.05] = 0.0
+    be = rng.uniform(0, 2, (1, 1, T))
+    h0 = rng.standard_normal((1, 1, dk, dv))
+    o_ref, h_ref = oracle.fwd(q, k, v, al, be, h0)
+    seg = lambda x, s: x[:, :, cuts[s]:cuts[s + 1]]
+    eye = np.zeros((1, 1, dk, dv))
+    eye[0, 0, :, :min(dk, dv)] = np.eye(dk, min(dk, dv))
+    # the affine map of one segment, checked on a random initial state
+    x1 = [seg(t, 1) for t in (q, k, v, al, be)]
+    _, F1 = oracle.fwd(*x1, None)
+    if dk <= dv:
+        _, PI = oracle.fwd(x1[0], x1[1], np.zeros_like(x1[2]), x1[3], x1[4], eye)
+        P1 = PI[0, 0, :, :dk]
+        assert np.all(PI[0, 0, :, dk:] == 0.0)
+        _, Hr = oracle.fwd(*x1, h0)
+        np.testing.assert_allclose(Hr[0, 0], P1 @ h0[0, 0] + F1[0, 0], rtol=0, atol=1e-12)
+    # the split's two passes and scan, with the oracle for every pass
+    outs, H = [], None
+    for s_ in range(len(cuts) - 1):
+        xs = [seg(t, s_) for t in (q, k, v, al, be)]
+        if s_ == 0:
+            o_s, H = oracle.fwd(*xs, h0)
+        else:
+            o_s, H_next = oracle.fwd(*xs, H)
+            # the state after the segment from the scan: P H + F
+            _, Fs = oracle.fwd(*xs, None)
+            Hz = np.zeros((1, 1, dk, dv))
+            for c in range(dv):   # P applied column by column: v = 0, h0 = e_c in column c
+                e_c = np.zeros((1, 1, dk, dv))
+                e_c[0, 0, :, c] = H[0, 0, :, c]
+                _, Pc = oracle.fwd(xs[0], xs[1], np.zeros_like(xs[2]), xs[3], xs[4], e_c)
+                Hz[0, 0, :, c] = Pc[0, 0, :, c]
+            np.testing.assert_allclose(H_next, Hz + Fs, rtol=0, atol=1e-12)
+            H = H_next
+        outs.append(o_s)
+    np.testing.assert_allclose(np.concatenate(outs, axis=2), o_ref, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(H, h_ref, rtol=0, atol=1e-12)
+
+
 def test_decode_step_matches_fwd_token_by_token():
     rng = np.random.default_rng(15)
     B, H, n, dv, T = 2, 3, 5, 4, 6
