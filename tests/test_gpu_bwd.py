@@ -83,6 +83,16 @@ def test_bwd_rectangular_no_h0_no_dhT(ck):
     check(gpu, ref, False, "dk=32 dv=48")
 
 
+def test_bwd_partial_column_block(ck):
+    """dv = 40: the cluster's third CTA owns 8 live columns of its 16, and
+    dk = 24 leaves most row groups inert; T = 201 ends mid-group."""
+    x = synth.make_fwd(2, 1, 201, 24, dv=40, dist="ckda", dtype="fp32", h0=True, seed=525)
+    do, dhT = grads_case(x, 625)
+    gpu = run(ck, x, do, dhT, 0.9)
+    ref = oracle.bwd(x.q, x.k, x.v, x.alpha, x.beta, do, h0=x.h0, dhT=dhT, scale=0.9)
+    check(gpu, ref, False, "dk=24 dv=40")
+
+
 def test_bwd_degenerate_gates(ck):
     base = synth.make_fwd(1, 2, 90, 64, dist="ckda", dtype="fp32", h0=True, seed=530)
     do, dhT = grads_case(base, 630)
