@@ -19,12 +19,12 @@
 //
 // Every column j of S evolves on its own; only p and du sum over the rows of
 // a column, while dq, dk, dalpha and dbeta sum over the columns.  So the
-// state is split by columns: a cluster of ceil(dv / 16) CTAs owns one
-// (sequence, head), each CTA 16 columns, and each of its 128 threads 16 rows
+// state is split by columns: a cluster of ceil(dv / 32) CTAs owns one
+// (sequence, head), each CTA 32 columns, and each of its 256 threads 16 rows
 // (16g .. 16g + 15) of one column of S and of D, in registers.  A column's
 // sums are 3-step shuffles among its 8 row groups (lanes of one warp).  The
 // sums over columns are reduced over the 4 columns of a warp by halving
-// exchanges, over the 4 warps in shared memory, and over the cluster's CTAs
+// exchanges, over the 8 warps in shared memory, and over the cluster's CTAs
 // through distributed shared memory, once per 8 tokens, in a fixed order.
 //
 // Recomputation: pass 1 runs the forward and keeps the state slice before
@@ -33,15 +33,17 @@
 // before every 2nd token (a sub-checkpoint) and forming dq; (b) it takes the
 // chunk's 2-token groups in reverse, reruns each from its sub-checkpoint with
 // both states kept in registers, and walks them backward.  Two tokens per
-// group keep a thread at 128 registers, so that 4 CTAs share an SM (16 warps)
-// and 76 clusters of 8 run at once on 152 SMs.  Arithmetic is fp32.
+// group keep a thread at 128 registers, so that 2 CTAs share an SM (16 warps)
+// and 76 clusters of 4 run at once on 152 SMs.  Arithmetic is fp32.
 #include "ckda_internal.cuh"
 
 namespace ckda {
 namespace {
 
-constexpr int CW = 16;           // state columns per CTA
-constexpr int NTH = 128;         // threads per CTA: 4 warps of 4 columns x 8 row groups
+constexpr int CW = 32;           // state columns per CTA
+constexpr int NTH = 8 * CW;      // threads per CTA: warps of 4 columns x 8 row groups
+constexpr int NW = NTH / 32;     // warps per CTA
+constexpr int MIN_CTAS = 512 / NTH;  // CTAs per SM at 128 registers a thread
 constexpr int RPT = 16;          // rows per thread
 constexpr int CK = 64;           // tokens per checkpoint interval
 constexpr int SG = 2;            // tokens per group (sub-checkpoint interval)
@@ -88,9 +90,9 @@ __host__ __device__ inline size_t bwd_ck_slots(bool packed, int N, int H, int T)
 constexpr int SM_VEC = 0;                        // [2][SG][3][VEC]: k, alpha, scale q
 constexpr int SM_CV = SM_VEC + 2 * SG * 3 * VEC;  // [2][SG][2][CW]: v, do of this CTA's columns
 constexpr int SM_BV = SM_CV + 2 * SG * 2 * CW;   // [2][SG]: beta
-constexpr int SM_RED = SM_BV + 2 * SG;           // [2][SG][4 warps][2][VEC]: per-warp sums over columns
-constexpr int SM_REDB = SM_RED + 2 * SG * 4 * 2 * VEC;  // [2][SG][4]: per-warp dbeta
-constexpr int SM_PART = SM_REDB + 2 * SG * 4;    // [2][RT][PART]: the CTA's sums, per token
+constexpr int SM_RED = SM_BV + 2 * SG;           // [2][SG][NW][2][VEC]: per-warp sums over columns
+constexpr int SM_REDB = SM_RED + 2 * SG * NW * 2 * VEC;  // [2][SG][NW]: per-warp dbeta
+constexpr int SM_PART = SM_REDB + 2 * SG * NW;   // [2][RT][PART]: the CTA's sums, per token
 constexpr int SM_TOK = SM_PART + 2 * RT * PART;  // [2][RT] int: the token of each PART row
 constexpr int SM_FLOATS = SM_TOK + 2 * RT;
 constexpr size_t kSmemBytes = (size_t)SM_FLOATS * sizeof(float);
@@ -162,7 +164,7 @@ __device__ __forceinline__ float sum_rows(float x) {   // over the 8 row groups 
 }
 
 template <typename IO>
-__global__ void __launch_bounds__(NTH, 4) bwd_kernel(const BwdArgs a) {
+__global__ void __launch_bounds__(NTH, MIN_CTAS) bwd_kernel(const BwdArgs a) {
   extern __shared__ float4 smem4[];
   float* sm = reinterpret_cast<float*>(smem4);
   const IO* q = static_cast<const IO*>(a.q);
@@ -215,26 +217,28 @@ __global__ void __launch_bounds__(NTH, 4) bwd_kernel(const BwdArgs a) {
         rv = ld_io(v + o);
         rdo = ld_io(dout + o);
       }
-    } else if (tid >= 64 && tid < 64 + SG) {
-      const int t = t0 + tid - 64;
+    } else if (tid >= SG * CW && tid < SG * CW + SG) {
+      const int t = t0 + tid - SG * CW;
       if (t >= 0 && t < len) rb = ld_io(be + (row0 + t));
     }
   };
   auto publish = [&](int vb) {
     float* V = sm + SM_VEC + vb * SG * 3 * VEC;
     const int pi = VP * (tid >> 4) + (tid & 15);
+    if (tid < 128) {
 #pragma unroll
-    for (int s = 0; s < SG; ++s) {
-      V[(s * 3 + 0) * VEC + pi] = rk[s];
-      V[(s * 3 + 1) * VEC + pi] = ra[s];
-      V[(s * 3 + 2) * VEC + pi] = rq[s];
+      for (int s = 0; s < SG; ++s) {
+        V[(s * 3 + 0) * VEC + pi] = rk[s];
+        V[(s * 3 + 1) * VEC + pi] = ra[s];
+        V[(s * 3 + 2) * VEC + pi] = rq[s];
+      }
     }
     if (tid < SG * CW) {
       float* C = sm + SM_CV + vb * SG * 2 * CW;
       C[(tid / CW) * 2 * CW + tid % CW] = rv;
       C[(tid / CW) * 2 * CW + CW + tid % CW] = rdo;
-    } else if (tid >= 64 && tid < 64 + SG) {
-      sm[SM_BV + vb * SG + tid - 64] = rb;
+    } else if (tid >= SG * CW && tid < SG * CW + SG) {
+      sm[SM_BV + vb * SG + tid - SG * CW] = rb;
     }
   };
   // L2 prefetch of the group starting at t0 (one ahead of the register fetch)
@@ -312,13 +316,13 @@ __global__ void __launch_bounds__(NTH, 4) bwd_kernel(const BwdArgs a) {
   // the CTA's sum over its 4 warps of the per-warp sums of token s of group
   // buffer gb (after a barrier), into row `slot` of partial buffer pb
   auto cta_sum = [&](int gb, int s, int pb, int slot, int nq) {
-    const float* R = red + (gb * SG + s) * 4 * 2 * VEC;
+    const float* R = red + (gb * SG + s) * NW * 2 * VEC;
     for (int e = tid; e < nq * 128; e += NTH) {
       const int qq = e >> 7, i = e & 127;
       const int off = qq * VEC + VP * (i >> 4) + (i & 15);
       float x = 0.f;
 #pragma unroll
-      for (int ww = 0; ww < 4; ++ww) x += R[ww * 2 * VEC + off];
+      for (int ww = 0; ww < NW; ++ww) x += R[ww * 2 * VEC + off];
       part[(pb * RT + slot) * PART + e] = x;
     }
   };
@@ -418,7 +422,7 @@ __global__ void __launch_bounds__(NTH, 4) bwd_kernel(const BwdArgs a) {
           x[r] = Sn[r] * dov;
         }
         sum_columns<RPT>(x, z, lane);
-        *reinterpret_cast<float4*>(red + ((gb * SG + s) * 4 + w) * 2 * VEC + VP * g + 4 * cw) =
+        *reinterpret_cast<float4*>(red + ((gb * SG + s) * NW + w) * 2 * VEC + VP * g + 4 * cw) =
             make_float4(z[0], z[1], z[2], z[3]);
       }
       __syncthreads();
@@ -495,7 +499,7 @@ __global__ void __launch_bounds__(NTH, 4) bwd_kernel(const BwdArgs a) {
         }
         float z[2 * RPT / 4];
         sum_columns<2 * RPT>(x, z, lane);
-        float* R = red + ((gb * SG + s) * 4 + w) * 2 * VEC + (cw >> 1) * VEC + VP * g +
+        float* R = red + ((gb * SG + s) * NW + w) * 2 * VEC + (cw >> 1) * VEC + VP * g +
                    8 * (cw & 1);
         *reinterpret_cast<float4*>(R) = make_float4(z[0], z[1], z[2], z[3]);
         *reinterpret_cast<float4*>(R + 4) = make_float4(z[4], z[5], z[6], z[7]);
@@ -503,7 +507,7 @@ __global__ void __launch_bounds__(NTH, 4) bwd_kernel(const BwdArgs a) {
         float db = (g == 0) ? du * (vj - p) : 0.f;
         db += __shfl_xor_sync(0xffffffffu, db, 8);
         db += __shfl_xor_sync(0xffffffffu, db, 16);
-        if (lane == 0) sm[SM_REDB + (gb * SG + s) * 4 + w] = db;
+        if (lane == 0) sm[SM_REDB + (gb * SG + s) * NW + w] = db;
       }
       __syncthreads();
       const int pb = rg & 1;
@@ -511,8 +515,10 @@ __global__ void __launch_bounds__(NTH, 4) bwd_kernel(const BwdArgs a) {
       for (int s = 0; s < SG; ++s) {
         cta_sum(gb, s, pb, pend + s, 2);
         if (tid == 0) {
-          const float* RB = sm + SM_REDB + (gb * SG + s) * 4;
-          part[(pb * RT + pend + s) * PART + 256] = RB[0] + RB[1] + RB[2] + RB[3];
+          const float* RB = sm + SM_REDB + (gb * SG + s) * NW;
+          float x = 0.f;
+          for (int ww = 0; ww < NW; ++ww) x += RB[ww];
+          part[(pb * RT + pend + s) * PART + 256] = x;
           tok[pb * RT + pend + s] = gi * SG + s;
         }
       }
@@ -534,6 +540,9 @@ __global__ void __launch_bounds__(NTH, 4) bwd_kernel(const BwdArgs a) {
 
 template <typename IO>
 cudaError_t launch_io(const BwdArgs& a, int units, cudaStream_t s) {
+  const cudaError_t err = cudaFuncSetAttribute(
+      bwd_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(units * a.ncb));
   cfg.blockDim = dim3(NTH);

@@ -308,7 +308,7 @@ ckda_status ckda_decode_step_raw(const void *q_raw, const void *k_raw, const voi
  * state.  d_h0 == NULL: not stored.  Gradient buffers must not alias inputs.
  * Any dk, dv <= 128 and either I/O dtype; arithmetic is fp32, token by token
  * on CUDA cores.  Each (sequence, head) runs as one thread-block cluster of
- * ceil(dv / 16) CTAs, each holding 16 columns of the state in registers;
+ * ceil(dv / 32) CTAs, each holding 32 columns of the state in registers;
  * sums over columns are reduced in a fixed order, so results are
  * deterministic.  Pass 1 reruns the forward and keeps the state before every
  * 64th token in `workspace`.  Pass 2 takes the 64-token chunks in reverse:
@@ -317,8 +317,8 @@ ckda_status ckda_decode_step_raw(const void *q_raw, const void *k_raw, const voi
  *
  * workspace: device memory of at least ckda_bwd_workspace_bytes(num_seqs, B,
  * H, T, dk, dv) bytes (num_seqs = 0 for dense input), 16-byte aligned, owned
- * by the caller; its contents are scratch.  It holds state slices of 8 KiB
- * (one CTA's 16 columns).  There are ceil(dv / 16) of them per checkpoint:
+ * by the caller; its contents are scratch.  It holds state slices of 16 KiB
+ * (one CTA's 32 columns).  There are ceil(dv / 32) of them per checkpoint:
  * ceil(T/64) checkpoints per dense (batch, head), ceil(T/64) + num_seqs per
  * head when packed.  Each CTA also has 32 slices for the chunk being walked.
  * Argument errors return synchronously with nothing launched; otherwise

@@ -134,13 +134,13 @@ def test_bwd_argument_errors_are_synchronous(L):
     assert f(cu=256, B=2, nseq=2) == 1      # packed input needs B == 1
     assert f(wsb=100) == 5                   # workspace smaller than needed
     assert f(ws=8) == 5                      # misaligned workspace
-    # one state slice is one CTA's 16 columns: 128 threads x 16 rows of fp32; a
-    # (sequence, head) has ceil(dv / 16) CTAs, each with 32 sub-checkpoint
+    # one state slice is one CTA's 32 columns: 256 threads x 16 rows of fp32; a
+    # (sequence, head) has ceil(dv / 32) CTAs, each with 32 sub-checkpoint
     # slices (one per 2 tokens of a 64-token chunk)
-    sl = 128 * 16 * 4
+    sl = 256 * 16 * 4
     # dense: ceil(T/64) checkpoints per (batch, head)
     assert L.ckda_bwd_workspace_bytes(0, 2, 3, 130, 16, 8) == (2 * 3 * 3 + 2 * 3 * 32) * sl
-    assert L.ckda_bwd_workspace_bytes(0, 2, 3, 130, 16, 40) == 3 * (2 * 3 * 3 + 2 * 3 * 32) * sl
+    assert L.ckda_bwd_workspace_bytes(0, 2, 3, 130, 16, 40) == 2 * (2 * 3 * 3 + 2 * 3 * 32) * sl
     # packed: ceil(T/64) + num_seqs checkpoints per head
     assert L.ckda_bwd_workspace_bytes(5, 1, 3, 130, 16, 8) == (3 * (3 + 5) + 5 * 3 * 32) * sl
 
