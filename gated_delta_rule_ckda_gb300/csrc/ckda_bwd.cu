@@ -53,6 +53,9 @@ constexpr int VEC = 8 * VP;      // one padded channel vector (128 channels)
 constexpr int SLOT = NTH * RPT;  // floats of one CTA's state slice
 constexpr int PART = 2 * 128 + 4;  // per token: dk (128), dalpha (128), dbeta
 constexpr int RT = 8;            // tokens per reduction over the cluster
+static_assert(NTH >= 128, "one thread per key channel publishes the token vectors");
+static_assert(SG * CW + SG <= NTH, "threads that load v, do and beta");
+static_assert(CK % SG == 0 && RT % SG == 0, "groups tile chunks and reduction rounds");
 
 struct BwdArgs {
   const void* q;
@@ -313,7 +316,7 @@ __global__ void __launch_bounds__(NTH, MIN_CTAS) bwd_kernel(const BwdArgs a) {
   float* red = sm + SM_RED;
   float* part = sm + SM_PART;
   int* tok = reinterpret_cast<int*>(sm + SM_TOK);
-  // the CTA's sum over its 4 warps of the per-warp sums of token s of group
+  // the CTA's sum over its NW warps of the per-warp sums of token s of group
   // buffer gb (after a barrier), into row `slot` of partial buffer pb
   auto cta_sum = [&](int gb, int s, int pb, int slot, int nq) {
     const float* R = red + (gb * SG + s) * NW * 2 * VEC;
