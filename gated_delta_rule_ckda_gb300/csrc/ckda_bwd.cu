@@ -446,6 +446,9 @@ __global__ void __launch_bounds__(NTH, MIN_CTAS) bwd_kernel(const BwdArgs a) {
     __syncthreads();   // (a)'s reads of the vector buffers are done
     fetch((g1 - 1) * SG);
     prefetch_group((g1 - 2) * SG);
+    // the first group's vectors; each later group's are published at the
+    // end of the group before it, under that group's barrier
+    int vb = next_group((g1 - 2) * SG, -SG);
     pend = 0;
     for (int gi = g1 - 1; gi >= g0; --gi) {
       float st[SG][RPT];
@@ -454,7 +457,6 @@ __global__ void __launch_bounds__(NTH, MIN_CTAS) bwd_kernel(const BwdArgs a) {
 #pragma unroll
         for (int r = 0; r < RPT; ++r) prefetch_l1(subck + (size_t)(gi - 1 - g0) * SLOT + r * NTH + tid);
       }
-      const int vb = next_group((gi - 1) * SG, -SG);
       const int gb = gcount & 1;
       ++gcount;
 #pragma unroll
@@ -512,7 +514,18 @@ __global__ void __launch_bounds__(NTH, MIN_CTAS) bwd_kernel(const BwdArgs a) {
         db += __shfl_xor_sync(0xffffffffu, db, 16);
         if (lane == 0) sm[SM_REDB + (gb * SG + s) * NW + w] = db;
       }
-      __syncthreads();
+      // the next group's vectors (fetched during this one) into the other
+      // buffer, whose last reader was the group before this one
+      const int vb_next = vg & 1;
+      if (gi > g0) {
+        ++vg;
+        publish(vb_next);
+      }
+      __syncthreads();   // this group's per-warp sums and the next group's vectors
+      if (gi > g0) {
+        fetch((gi - 2) * SG);
+        prefetch_group((gi - 3) * SG);
+      }
       const int pb = rg & 1;
 #pragma unroll
       for (int s = 0; s < SG; ++s) {
@@ -531,6 +544,7 @@ __global__ void __launch_bounds__(NTH, MIN_CTAS) bwd_kernel(const BwdArgs a) {
         ++rg;
         pend = 0;
       }
+      vb = vb_next;
     }
   }
   if (a.gh0 && colok) {
