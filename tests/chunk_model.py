@@ -96,3 +96,126 @@ def chunked_forward(q, k, v, alpha, beta, h0=None, C=64, rnd=None):
                            pad(beta, 0.0), rnd)
         O[c0:c0 + L] = Oc[:L]
     return O, H
+
+
+# --- the chunkwise backward -----------------------------------------------------
+#
+# Reverse mode through chunk_step, in the same algebra.  Given dO (C x dv) and
+# dH' (n x dv):
+#
+#   dU  = A^T dO + (k*rho) dH'             dA = dO U^T (lower, with diagonal)
+#   dH  = (q*gamma)^T dO + Diag(gamma_C) dH' - W^T dU
+#   dW  = -dU H^T,  dTB = dU V^T + dW (k*gamma)^T,  dV = TB^T dU
+#   dT  = dTB Diag(beta),  dM = -T^T dT T^T (strictly lower)
+#   dbeta_s += sum_t dTB_ts T_ts,  dbeta_t += sum_s dM_ts Gk_ts
+#
+# and the gated Grams' transposed products for dk and dq.  Every gate
+# gradient is formed without division.  For a product chain
+# P_t = prod_{r<=t} alpha_r with adjoints g_t:
+#   dalpha_r = [prod_{r'<r} alpha_r'] S_r,  with S_r = g_r + alpha_{r+1} S_{r+1}
+# (a backward scan), and likewise for the suffix products rho with a forward
+# scan.  For the pair products Gamma(t<-s), the factor at r splits the pair
+# into Gamma(t<-r) Gamma(r-1<-s).
+
+
+def _pair_products(alpha):
+    """G[t, s] = Gamma(t<-s) = prod_{s<r<=t} alpha_r for s <= t (ones on the
+    diagonal), built by multiplication along each row."""
+    C, n = alpha.shape
+    G = np.zeros((C, C, n))
+    for s in range(C):
+        G[s, s] = 1.0
+        for t in range(s + 1, C):
+            G[t, s] = G[t - 1, s] * alpha[t]
+    return G
+
+
+def chunk_step_bwd(H, q, k, v, alpha, beta, dO, dHn):
+    """Gradients through chunk_step: returns (dH, dq, dk, dv, dalpha, dbeta)."""
+    C, n = k.shape
+    G = _pair_products(alpha)                       # Gamma(t<-s), s <= t
+    low = np.tril(np.ones((C, C)), -1)              # s < t
+    lowd = np.tril(np.ones((C, C)))                 # s <= t
+    gamma = np.cumprod(alpha, axis=0)
+    rho = np.ones((C, n))
+    for s in range(C - 2, -1, -1):
+        rho[s] = rho[s + 1] * alpha[s + 1]
+    Gk = np.einsum("ti,si,tsi->ts", k, k, G) * low
+    Gq = np.einsum("ti,si,tsi->ts", q, k, G) * lowd
+    M = beta[:, None] * Gk
+    T = np.linalg.inv(np.eye(C) + M)
+    TB = T * beta[None, :]
+    Kg, Qg, Kh = k * gamma, q * gamma, k * rho
+    W = TB @ Kg
+    U = TB @ v - W @ H
+    # outputs and the next state
+    dU = Gq.T @ dO + Kh @ dHn
+    dGq = (dO @ U.T) * lowd
+    dQg = dO @ H.T
+    dH = Qg.T @ dO + gamma[-1][:, None] * dHn - W.T @ dU
+    dgC = np.einsum("ij,ij->i", dHn, H)
+    dKh = U @ dHn.T
+    # the UT/WY transform
+    dW = -dU @ H.T
+    dTB = dU @ v.T + dW @ Kg.T
+    dv = TB.T @ dU
+    dKg = TB.T @ dW
+    dT = dTB * beta[None, :]
+    dbeta = np.einsum("ts,ts->s", dTB, T)
+    dM = (-T.T @ dT @ T.T) * low
+    dbeta = dbeta + np.einsum("ts,ts->t", dM, Gk)
+    dGk = beta[:, None] * dM
+    # the gated Grams
+    dq = np.einsum("ts,si,tsi->ti", dGq, k, G) + dQg * gamma
+    dk = (np.einsum("ts,si,tsi->ti", dGk, k, G) + np.einsum("ts,ti,tsi->si", dGk, k, G)
+          + np.einsum("ts,ti,tsi->si", dGq, q, G) + dKg * gamma + dKh * rho)
+    dG = (np.einsum("ts,ti,si->tsi", dGk, k, k) + np.einsum("ts,ti,si->tsi", dGq * low, q, k))
+    # gate gradients, without division
+    dgamma = dKg * k + dQg * q
+    dgamma[-1] += dgC                               # gamma_C = gamma_{C-1}
+    drho = dKh * k
+    dalpha = np.zeros((C, n))
+    S = np.zeros(n)                                 # backward scan over dgamma
+    for r in range(C - 1, -1, -1):
+        S = dgamma[r] + (alpha[r + 1] * S if r + 1 < C else 0.0)
+        dalpha[r] += (gamma[r - 1] if r > 0 else 1.0) * S
+    R = np.zeros(n)                                 # forward scan over drho
+    for r in range(1, C):
+        R = drho[r - 1] + alpha[r - 1] * R if r > 1 else drho[0]
+        dalpha[r] += rho[r] * R
+    for r in range(1, C):                           # pairs (t, s) with s < r <= t
+        for t in range(r, C):
+            for s in range(r):
+                dalpha[r] += dG[t, s] * G[t, r] * G[r - 1, s]
+    return dH, dq, dk, dv, dalpha, dbeta
+
+
+def chunked_backward(q, k, v, alpha, beta, dO, h0=None, dhT=None, C=16):
+    """Single (sequence, head) backward by chunks: the forward keeps the state
+    at each chunk start, then the chunks run in reverse through
+    chunk_step_bwd.  Returns (dq, dk, dv, dalpha, dbeta, dh0)."""
+    T, n = k.shape
+    dvn = v.shape[1]
+    H = np.zeros((n, dvn)) if h0 is None else np.array(h0, dtype=np.float64)
+
+    def pad(x, c0, L, fill):
+        return np.concatenate([x[c0:c0 + L], np.full((C - L,) + x.shape[1:], fill)])
+
+    starts = []
+    for c0 in range(0, T, C):
+        L = min(C, T - c0)
+        starts.append(H)
+        _, H = chunk_step(H, pad(q, c0, L, 0.0), pad(k, c0, L, 0.0), pad(v, c0, L, 0.0),
+                          pad(alpha, c0, L, 1.0), pad(beta, c0, L, 0.0))
+    dH = np.zeros((n, dvn)) if dhT is None else np.array(dhT, dtype=np.float64)
+    out = [np.zeros_like(q), np.zeros_like(k), np.zeros_like(v), np.zeros_like(alpha),
+           np.zeros_like(beta)]
+    for ci in range(len(starts) - 1, -1, -1):
+        c0 = ci * C
+        L = min(C, T - c0)
+        dH, *g = chunk_step_bwd(starts[ci], pad(q, c0, L, 0.0), pad(k, c0, L, 0.0),
+                                pad(v, c0, L, 0.0), pad(alpha, c0, L, 1.0),
+                                pad(beta, c0, L, 0.0), pad(dO, c0, L, 0.0), dH)
+        for o, gg in zip(out, g):
+            o[c0:c0 + L] = gg[:L]
+    return (*out, dH)
