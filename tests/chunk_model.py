@@ -109,13 +109,13 @@ def chunked_forward(q, k, v, alpha, beta, h0=None, C=64, rnd=None):
 #   dT  = dTB Diag(beta),  dM = -T^T dT T^T (strictly lower)
 #   dbeta_s += sum_t dTB_ts T_ts,  dbeta_t += sum_s dM_ts Gk_ts
 #
-# and the gated Grams' transposed products for dk and dq.  Every gate
-# gradient is formed without division.  For a product chain
+# and the gated Grams' transposed products for dk and dq, on the same split
+# tree as the forward (gated_grams_bwd).  Every gate gradient is formed
+# without division.  For a product chain
 # P_t = prod_{r<=t} alpha_r with adjoints g_t:
 #   dalpha_r = [prod_{r'<r} alpha_r'] S_r,  with S_r = g_r + alpha_{r+1} S_{r+1}
 # (a backward scan), and likewise for the suffix products rho with a forward
-# scan.  For the pair products Gamma(t<-s), the factor at r splits the pair
-# into Gamma(t<-r) Gamma(r-1<-s).
+# scan.  On the tree, each level's F and B are such chains.
 
 
 def _pair_products(alpha):
@@ -133,15 +133,13 @@ def _pair_products(alpha):
 def chunk_step_bwd(H, q, k, v, alpha, beta, dO, dHn):
     """Gradients through chunk_step: returns (dH, dq, dk, dv, dalpha, dbeta)."""
     C, n = k.shape
-    G = _pair_products(alpha)                       # Gamma(t<-s), s <= t
     low = np.tril(np.ones((C, C)), -1)              # s < t
     lowd = np.tril(np.ones((C, C)))                 # s <= t
     gamma = np.cumprod(alpha, axis=0)
     rho = np.ones((C, n))
     for s in range(C - 2, -1, -1):
         rho[s] = rho[s + 1] * alpha[s + 1]
-    Gk = np.einsum("ti,si,tsi->ts", k, k, G) * low
-    Gq = np.einsum("ti,si,tsi->ts", q, k, G) * lowd
+    Gk, Gq = gated_grams(q, k, alpha)
     M = beta[:, None] * Gk
     T = np.linalg.inv(np.eye(C) + M)
     TB = T * beta[None, :]
@@ -165,16 +163,14 @@ def chunk_step_bwd(H, q, k, v, alpha, beta, dO, dHn):
     dM = (-T.T @ dT @ T.T) * low
     dbeta = dbeta + np.einsum("ts,ts->t", dM, Gk)
     dGk = beta[:, None] * dM
-    # the gated Grams
-    dq = np.einsum("ts,si,tsi->ti", dGq, k, G) + dQg * gamma
-    dk = (np.einsum("ts,si,tsi->ti", dGk, k, G) + np.einsum("ts,ti,tsi->si", dGk, k, G)
-          + np.einsum("ts,ti,tsi->si", dGq, q, G) + dKg * gamma + dKh * rho)
-    dG = (np.einsum("ts,ti,si->tsi", dGk, k, k) + np.einsum("ts,ti,si->tsi", dGq * low, q, k))
-    # gate gradients, without division
+    # the gated Grams, on the split tree
+    dq, dk, dalpha = gated_grams_bwd(q, k, alpha, dGk, dGq)
+    dq = dq + dQg * gamma
+    dk = dk + dKg * gamma + dKh * rho
+    # gate gradients of the prefix and suffix products, without division
     dgamma = dKg * k + dQg * q
     dgamma[-1] += dgC                               # gamma_C = gamma_{C-1}
     drho = dKh * k
-    dalpha = np.zeros((C, n))
     S = np.zeros(n)                                 # backward scan over dgamma
     for r in range(C - 1, -1, -1):
         S = dgamma[r] + (alpha[r + 1] * S if r + 1 < C else 0.0)
@@ -183,11 +179,26 @@ def chunk_step_bwd(H, q, k, v, alpha, beta, dO, dHn):
     for r in range(1, C):
         R = drho[r - 1] + alpha[r - 1] * R if r > 1 else drho[0]
         dalpha[r] += rho[r] * R
-    for r in range(1, C):                           # pairs (t, s) with s < r <= t
+    return dH, dq, dk, dv, dalpha, dbeta
+
+
+def gated_grams_bwd_direct(q, k, alpha, dGk, dGq):
+    """The same gradients as gated_grams_bwd from the explicit pair products:
+    the factor of alpha_r in Gamma(t<-s), s < r <= t, is Gamma(t<-r)
+    Gamma(r-1<-s).  O(C^3 n); a cross-check of the tree form."""
+    C, n = k.shape
+    G = _pair_products(alpha)
+    low = np.tril(np.ones((C, C)), -1)
+    dq = np.einsum("ts,si,tsi->ti", dGq, k, G)
+    dk = (np.einsum("ts,si,tsi->ti", dGk, k, G) + np.einsum("ts,ti,tsi->si", dGk, k, G)
+          + np.einsum("ts,ti,tsi->si", dGq, q, G))
+    dG = np.einsum("ts,ti,si->tsi", dGk, k, k) + np.einsum("ts,ti,si->tsi", dGq * low, q, k)
+    dalpha = np.zeros((C, n))
+    for r in range(1, C):
         for t in range(r, C):
             for s in range(r):
                 dalpha[r] += dG[t, s] * G[t, r] * G[r - 1, s]
-    return dH, dq, dk, dv, dalpha, dbeta
+    return dq, dk, dalpha
 
 
 def chunked_backward(q, k, v, alpha, beta, dO, h0=None, dhT=None, C=16):
@@ -219,3 +230,54 @@ def chunked_backward(q, k, v, alpha, beta, dO, h0=None, dhT=None, C=16):
         for o, gg in zip(out, g):
             o[c0:c0 + L] = gg[:L]
     return (*out, dH)
+
+
+def gated_grams_bwd(q, k, alpha, dGk, dGq):
+    """Gradients of the gated Grams (Gk strictly lower, Gq lower with diagonal)
+    on the split tree the forward uses: on each level, Gamma(t<-s) = F_t B_s with
+    F_t = prod_{m<r<=t} alpha_r over the upper half and B_s = prod_{s<r<=m}
+    alpha_r over the lower half.  Per level and segment:
+      d(k F)_t = dGk[t, :] (k B),   d(q F)_t = dGq[t, :] (k B)     (upper rows)
+      d(k B)_s = dGk[:, s]^T (k F) + dGq[:, s]^T (q F)             (lower rows)
+    then dk, dq by the factors, and dalpha from F by a backward scan and from
+    B by a forward scan.  Returns (dq, dk, dalpha)."""
+    C, n = k.shape
+    dq = np.zeros((C, n))
+    dk = np.zeros((C, n))
+    dalpha = np.zeros((C, n))
+    for L in tree_levels(C):
+        for seg in range(0, C, 2 * L):
+            m = seg + L - 1
+            up = slice(m + 1, m + 1 + L)
+            lo = slice(seg, m + 1)
+            F = np.cumprod(alpha[up], axis=0)
+            B = np.ones((L, n))
+            for j in range(L - 2, -1, -1):
+                B[j] = B[j + 1] * alpha[seg + j + 1]
+            kF, qF, kB = k[up] * F, q[up] * F, k[lo] * B
+            dkF = dGk[up, lo] @ kB
+            dqF = dGq[up, lo] @ kB
+            dkB = dGk[up, lo].T @ kF + dGq[up, lo].T @ qF
+            dk[up] += dkF * F
+            dq[up] += dqF * F
+            dk[lo] += dkB * B
+            dF = dkF * k[up] + dqF * q[up]
+            dB = dkB * k[lo]
+            # F_t = prod_{m<r<=t} alpha_r: dalpha_r = [prod_{m<r'<r}] S_r,
+            # S_r = dF_r + alpha_{r+1} S_{r+1}
+            S = np.zeros(n)
+            for jr in range(L - 1, -1, -1):
+                r = m + 1 + jr
+                S = dF[jr] + (alpha[r + 1] * S if jr + 1 < L else 0.0)
+                dalpha[r] += (F[jr - 1] if jr > 0 else 1.0) * S
+            # B_s = prod_{s<r<=m} alpha_r: dalpha_r = [prod_{r<r'<=m}] R_r,
+            # R_r = dB_{r-1} + alpha_{r-1} R_{r-1}
+            R = np.zeros(n)
+            for jr in range(1, L):
+                r = seg + jr
+                R = dB[jr - 1] + (alpha[r - 1] * R if jr > 1 else 0.0)
+                dalpha[r] += B[jr] * R
+    # the diagonal of Gq carries no gate
+    dq += np.diagonal(dGq)[:, None] * k
+    dk += np.diagonal(dGq)[:, None] * q
+    return dq, dk, dalpha

@@ -60,3 +60,21 @@ def test_chunked_backward_degenerate_gates(special):
 
 def test_chunked_backward_rectangular():
     compare(*case(820, 40, 3, 6), C=16)
+
+
+@pytest.mark.parametrize("C", [4, 8, 16])
+def test_tree_form_of_gram_gradients(C):
+    """The split-tree form of the Gram gradients (per level: dense products of
+    gated operands, then prefix and suffix scans for the gates) equals the
+    explicit pair-product form."""
+    rng = np.random.default_rng(830 + C)
+    n = 4
+    q, k = rng.standard_normal((C, n)), rng.standard_normal((C, n))
+    al = rng.uniform(-1, 1, (C, n))
+    al[rng.random((C, n)) < 0.15] = 0.0
+    al[rng.random((C, n)) < 0.1] = -1.0
+    dGk = rng.standard_normal((C, C)) * np.tril(np.ones((C, C)), -1)
+    dGq = rng.standard_normal((C, C)) * np.tril(np.ones((C, C)))
+    for a, b in zip(cm.gated_grams_bwd(q, k, al, dGk, dGq),
+                    cm.gated_grams_bwd_direct(q, k, al, dGk, dGq)):
+        np.testing.assert_allclose(a, b, rtol=0, atol=1e-12)
