@@ -130,8 +130,11 @@ def _pair_products(alpha):
     return G
 
 
-def chunk_step_bwd(H, q, k, v, alpha, beta, dO, dHn):
-    """Gradients through chunk_step: returns (dH, dq, dk, dv, dalpha, dbeta)."""
+def chunk_step_bwd(H, q, k, v, alpha, beta, dO, dHn, rnd=None):
+    """Gradients through chunk_step: returns (dH, dq, dk, dv, dalpha, dbeta).
+    `rnd(name, x)` optionally rounds the operands of each contraction (to model
+    a kernel's storage precisions); identity by default."""
+    rd = rnd or (lambda name, x: x)
     C, n = k.shape
     low = np.tril(np.ones((C, C)), -1)              # s < t
     lowd = np.tril(np.ones((C, C)))                 # s <= t
@@ -142,29 +145,33 @@ def chunk_step_bwd(H, q, k, v, alpha, beta, dO, dHn):
     Gk, Gq = gated_grams(q, k, alpha)
     M = beta[:, None] * Gk
     T = np.linalg.inv(np.eye(C) + M)
-    TB = T * beta[None, :]
-    Kg, Qg, Kh = k * gamma, q * gamma, k * rho
-    W = TB @ Kg
-    U = TB @ v - W @ H
+    TB = rd("TB", T * beta[None, :])
+    Tr = rd("T", T)
+    Kg, Qg, Kh = rd("Kg", k * gamma), rd("Qg", q * gamma), rd("Kh", k * rho)
+    A = rd("A", Gq)
+    W = rd("W", TB @ Kg)
+    Hr = rd("H", H)
+    U = rd("U", TB @ v - W @ Hr)
+    dOr, dHr = rd("dO", dO), rd("dHn", dHn)
     # outputs and the next state
-    dU = Gq.T @ dO + Kh @ dHn
-    dGq = (dO @ U.T) * lowd
-    dQg = dO @ H.T
-    dH = Qg.T @ dO + gamma[-1][:, None] * dHn - W.T @ dU
+    dU = rd("dU", A.T @ dOr + Kh @ dHr)
+    dGq = rd("dG", (dOr @ U.T) * lowd)
+    dQg = dOr @ Hr.T
+    dH = Qg.T @ dOr + gamma[-1][:, None] * dHn - W.T @ dU
     dgC = np.einsum("ij,ij->i", dHn, H)
-    dKh = U @ dHn.T
+    dKh = U @ dHr.T
     # the UT/WY transform
-    dW = -dU @ H.T
+    dW = rd("dW", -dU @ Hr.T)
     dTB = dU @ v.T + dW @ Kg.T
     dv = TB.T @ dU
     dKg = TB.T @ dW
-    dT = dTB * beta[None, :]
+    dT = rd("dT", dTB * beta[None, :])
     dbeta = np.einsum("ts,ts->s", dTB, T)
-    dM = (-T.T @ dT @ T.T) * low
+    dM = (-Tr.T @ dT @ Tr.T) * low
     dbeta = dbeta + np.einsum("ts,ts->t", dM, Gk)
-    dGk = beta[:, None] * dM
+    dGk = rd("dG", beta[:, None] * dM)
     # the gated Grams, on the split tree
-    dq, dk, dalpha = gated_grams_bwd(q, k, alpha, dGk, dGq)
+    dq, dk, dalpha = gated_grams_bwd(q, k, alpha, dGk, dGq, rnd=rnd)
     dq = dq + dQg * gamma
     dk = dk + dKg * gamma + dKh * rho
     # gate gradients of the prefix and suffix products, without division
@@ -201,7 +208,7 @@ def gated_grams_bwd_direct(q, k, alpha, dGk, dGq):
     return dq, dk, dalpha
 
 
-def chunked_backward(q, k, v, alpha, beta, dO, h0=None, dhT=None, C=16):
+def chunked_backward(q, k, v, alpha, beta, dO, h0=None, dhT=None, C=16, rnd=None):
     """Single (sequence, head) backward by chunks: the forward keeps the state
     at each chunk start, then the chunks run in reverse through
     chunk_step_bwd.  Returns (dq, dk, dv, dalpha, dbeta, dh0)."""
@@ -217,7 +224,7 @@ def chunked_backward(q, k, v, alpha, beta, dO, h0=None, dhT=None, C=16):
         L = min(C, T - c0)
         starts.append(H)
         _, H = chunk_step(H, pad(q, c0, L, 0.0), pad(k, c0, L, 0.0), pad(v, c0, L, 0.0),
-                          pad(alpha, c0, L, 1.0), pad(beta, c0, L, 0.0))
+                          pad(alpha, c0, L, 1.0), pad(beta, c0, L, 0.0), rnd)
     dH = np.zeros((n, dvn)) if dhT is None else np.array(dhT, dtype=np.float64)
     out = [np.zeros_like(q), np.zeros_like(k), np.zeros_like(v), np.zeros_like(alpha),
            np.zeros_like(beta)]
@@ -226,13 +233,63 @@ def chunked_backward(q, k, v, alpha, beta, dO, h0=None, dhT=None, C=16):
         L = min(C, T - c0)
         dH, *g = chunk_step_bwd(starts[ci], pad(q, c0, L, 0.0), pad(k, c0, L, 0.0),
                                 pad(v, c0, L, 0.0), pad(alpha, c0, L, 1.0),
-                                pad(beta, c0, L, 0.0), pad(dO, c0, L, 0.0), dH)
+                                pad(beta, c0, L, 0.0), pad(dO, c0, L, 0.0), dH, rnd)
         for o, gg in zip(out, g):
             o[c0:c0 + L] = gg[:L]
     return (*out, dH)
 
 
-def gated_grams_bwd(q, k, alpha, dGk, dGq):
+def gated_grams_bwd_direct(q, k, alpha, dGk, dGq):
+    """The same gradients as gated_grams_bwd from the explicit pair products:
+    the factor of alpha_r in Gamma(t<-s), s < r <= t, is Gamma(t<-r)
+    Gamma(r-1<-s).  O(C^3 n); a cross-check of the tree form."""
+    C, n = k.shape
+    G = _pair_products(alpha)
+    low = np.tril(np.ones((C, C)), -1)
+    dq = np.einsum("ts,si,tsi->ti", dGq, k, G)
+    dk = (np.einsum("ts,si,tsi->ti", dGk, k, G) + np.einsum("ts,ti,tsi->si", dGk, k, G)
+          + np.einsum("ts,ti,tsi->si", dGq, q, G))
+    dG = np.einsum("ts,ti,si->tsi", dGk, k, k) + np.einsum("ts,ti,si->tsi", dGq * low, q, k)
+    dalpha = np.zeros((C, n))
+    for r in range(1, C):
+        for t in range(r, C):
+            for s in range(r):
+                dalpha[r] += dG[t, s] * G[t, r] * G[r - 1, s]
+    return dq, dk, dalpha
+
+
+def chunked_backward(q, k, v, alpha, beta, dO, h0=None, dhT=None, C=16, rnd=None):
+    """Single (sequence, head) backward by chunks: the forward keeps the state
+    at each chunk start, then the chunks run in reverse through
+    chunk_step_bwd.  Returns (dq, dk, dv, dalpha, dbeta, dh0)."""
+    T, n = k.shape
+    dvn = v.shape[1]
+    H = np.zeros((n, dvn)) if h0 is None else np.array(h0, dtype=np.float64)
+
+    def pad(x, c0, L, fill):
+        return np.concatenate([x[c0:c0 + L], np.full((C - L,) + x.shape[1:], fill)])
+
+    starts = []
+    for c0 in range(0, T, C):
+        L = min(C, T - c0)
+        starts.append(H)
+        _, H = chunk_step(H, pad(q, c0, L, 0.0), pad(k, c0, L, 0.0), pad(v, c0, L, 0.0),
+                          pad(alpha, c0, L, 1.0), pad(beta, c0, L, 0.0), rnd)
+    dH = np.zeros((n, dvn)) if dhT is None else np.array(dhT, dtype=np.float64)
+    out = [np.zeros_like(q), np.zeros_like(k), np.zeros_like(v), np.zeros_like(alpha),
+           np.zeros_like(beta)]
+    for ci in range(len(starts) - 1, -1, -1):
+        c0 = ci * C
+        L = min(C, T - c0)
+        dH, *g = chunk_step_bwd(starts[ci], pad(q, c0, L, 0.0), pad(k, c0, L, 0.0),
+                                pad(v, c0, L, 0.0), pad(alpha, c0, L, 1.0),
+                                pad(beta, c0, L, 0.0), pad(dO, c0, L, 0.0), dH, rnd)
+        for o, gg in zip(out, g):
+            o[c0:c0 + L] = gg[:L]
+    return (*out, dH)
+
+
+def gated_grams_bwd(q, k, alpha, dGk, dGq, rnd=None):
     """Gradients of the gated Grams (Gk strictly lower, Gq lower with diagonal)
     on the split tree the forward uses: on each level, Gamma(t<-s) = F_t B_s with
     F_t = prod_{m<r<=t} alpha_r over the upper half and B_s = prod_{s<r<=m}
@@ -240,7 +297,9 @@ def gated_grams_bwd(q, k, alpha, dGk, dGq):
       d(k F)_t = dGk[t, :] (k B),   d(q F)_t = dGq[t, :] (k B)     (upper rows)
       d(k B)_s = dGk[:, s]^T (k F) + dGq[:, s]^T (q F)             (lower rows)
     then dk, dq by the factors, and dalpha from F by a backward scan and from
-    B by a forward scan.  Returns (dq, dk, dalpha)."""
+    B by a forward scan.  Returns (dq, dk, dalpha).  `rnd` as in chunk_step_bwd
+    (the gated operands are "gop")."""
+    rd = rnd or (lambda name, x: x)
     C, n = k.shape
     dq = np.zeros((C, n))
     dk = np.zeros((C, n))
@@ -254,7 +313,7 @@ def gated_grams_bwd(q, k, alpha, dGk, dGq):
             B = np.ones((L, n))
             for j in range(L - 2, -1, -1):
                 B[j] = B[j + 1] * alpha[seg + j + 1]
-            kF, qF, kB = k[up] * F, q[up] * F, k[lo] * B
+            kF, qF, kB = rd("gop", k[up] * F), rd("gop", q[up] * F), rd("gop", k[lo] * B)
             dkF = dGk[up, lo] @ kB
             dqF = dGq[up, lo] @ kB
             dkB = dGk[up, lo].T @ kF + dGq[up, lo].T @ qF
