@@ -128,8 +128,12 @@ ckda_status ckda_fwd(const void *q, const void *k, const void *v,
  *
  *   - Packed input is limited to num_seqs <= 65536; more returns
  *     CKDA_ERR_UNSUPPORTED before anything is launched.
- *   - The first call on a device looks up the array's device address (with
- *     that device current).  Make that first call before any stream capture.
+ *   - The first call in a CUDA context looks up the array's device address
+ *     in that context (the device's primary context for runtime callers; a
+ *     plugin host's own driver-API context if that is the current one).  The
+ *     address is cached per context id and never reused in another context,
+ *     so a cudaDeviceReset or a different current context gets its own
+ *     set-up.  Make the first call in a context before any stream capture.
  *   - Every call shares the one array.  Calls whose GPU work overlaps (on
  *     different streams, or from several threads at once) race on it and
  *     must be serialised by the caller.  Each call clears the status word it

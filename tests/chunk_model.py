@@ -239,56 +239,6 @@ def chunked_backward(q, k, v, alpha, beta, dO, h0=None, dhT=None, C=16, rnd=None
     return (*out, dH)
 
 
-def gated_grams_bwd_direct(q, k, alpha, dGk, dGq):
-    """The same gradients as gated_grams_bwd from the explicit pair products:
-    the factor of alpha_r in Gamma(t<-s), s < r <= t, is Gamma(t<-r)
-    Gamma(r-1<-s).  O(C^3 n); a cross-check of the tree form."""
-    C, n = k.shape
-    G = _pair_products(alpha)
-    low = np.tril(np.ones((C, C)), -1)
-    dq = np.einsum("ts,si,tsi->ti", dGq, k, G)
-    dk = (np.einsum("ts,si,tsi->ti", dGk, k, G) + np.einsum("ts,ti,tsi->si", dGk, k, G)
-          + np.einsum("ts,ti,tsi->si", dGq, q, G))
-    dG = np.einsum("ts,ti,si->tsi", dGk, k, k) + np.einsum("ts,ti,si->tsi", dGq * low, q, k)
-    dalpha = np.zeros((C, n))
-    for r in range(1, C):
-        for t in range(r, C):
-            for s in range(r):
-                dalpha[r] += dG[t, s] * G[t, r] * G[r - 1, s]
-    return dq, dk, dalpha
-
-
-def chunked_backward(q, k, v, alpha, beta, dO, h0=None, dhT=None, C=16, rnd=None):
-    """Single (sequence, head) backward by chunks: the forward keeps the state
-    at each chunk start, then the chunks run in reverse through
-    chunk_step_bwd.  Returns (dq, dk, dv, dalpha, dbeta, dh0)."""
-    T, n = k.shape
-    dvn = v.shape[1]
-    H = np.zeros((n, dvn)) if h0 is None else np.array(h0, dtype=np.float64)
-
-    def pad(x, c0, L, fill):
-        return np.concatenate([x[c0:c0 + L], np.full((C - L,) + x.shape[1:], fill)])
-
-    starts = []
-    for c0 in range(0, T, C):
-        L = min(C, T - c0)
-        starts.append(H)
-        _, H = chunk_step(H, pad(q, c0, L, 0.0), pad(k, c0, L, 0.0), pad(v, c0, L, 0.0),
-                          pad(alpha, c0, L, 1.0), pad(beta, c0, L, 0.0), rnd)
-    dH = np.zeros((n, dvn)) if dhT is None else np.array(dhT, dtype=np.float64)
-    out = [np.zeros_like(q), np.zeros_like(k), np.zeros_like(v), np.zeros_like(alpha),
-           np.zeros_like(beta)]
-    for ci in range(len(starts) - 1, -1, -1):
-        c0 = ci * C
-        L = min(C, T - c0)
-        dH, *g = chunk_step_bwd(starts[ci], pad(q, c0, L, 0.0), pad(k, c0, L, 0.0),
-                                pad(v, c0, L, 0.0), pad(alpha, c0, L, 1.0),
-                                pad(beta, c0, L, 0.0), pad(dO, c0, L, 0.0), dH, rnd)
-        for o, gg in zip(out, g):
-            o[c0:c0 + L] = gg[:L]
-    return (*out, dH)
-
-
 def gated_grams_bwd(q, k, alpha, dGk, dGq, rnd=None):
     """Gradients of the gated Grams (Gk strictly lower, Gq lower with diagonal)
     on the split tree the forward uses: on each level, Gamma(t<-s) = F_t B_s with

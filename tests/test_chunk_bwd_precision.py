@@ -1,5 +1,7 @@
 """Storage precisions for a chunkwise tensor-core backward, chosen by
-simulation against the fp64 oracle before any such kernel exists.
+simulation against the fp64 oracle before any such kernel exists.  The plan
+is checked at 256 tokens (4 chunks) and at 2048 (32 chunks, the KDA-range
+sequence length), so that errors carried back through the chunks are covered.
 
 The chunk model's rounding hooks round every contraction operand as a kernel
 would store it; accumulation stays exact (fp32 in a kernel, whose error is far
@@ -78,11 +80,14 @@ def errors(x, rnd):
     return out
 
 
+@pytest.mark.parametrize("T", [256, 2048])
 @pytest.mark.parametrize("dist", ["kda", "ckda"])
-def test_fp16_operands_meet_the_bound(dist):
+def test_fp16_operands_meet_the_bound(dist, T):
+    # 4 and 32 chunks: errors carried back through the reverse dH chain over
+    # a workload-length sequence stay within the same bound
     for name, (mx, rm) in zip(("dq", "dk", "dv", "dalpha", "dbeta", "dh0"),
-                              errors(inputs(dist), plan({}))):
-        assert mx <= 1e-2 and rm <= 1e-3, (dist, name, mx, rm)
+                              errors(inputs(dist, T=T), plan({}))):
+        assert mx <= 1e-2 and rm <= 1e-3, (dist, T, name, mx, rm)
 
 
 @pytest.mark.parametrize("dist", ["kda", "ckda"])

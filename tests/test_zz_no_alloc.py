@@ -50,11 +50,21 @@ def test_noalloc_matches_fwd_two_calls_in_a_row(ck):
 
 
 def test_noalloc_rejects_too_many_sequences(ck):
+    # real (small) device buffers everywhere: if the host-side limit ever
+    # stopped rejecting this call, the launch would still only touch valid
+    # memory and the assert, not the GPU, would report it
     L = ck.lib()
-    ck.fwd_noalloc  # argtypes are set on first use
+    n = 65537
+    d = synth.make_varlen([1, 2], 1, 128, dist="ckda", dtype="bf16", h0=False, seed=902).to("cuda")
+    cu = torch.zeros(n + 1, dtype=torch.int32, device="cuda")
+    cu[-1] = d.q.shape[2]
+    cu[-2] = d.q.shape[2]
+    o = torch.empty_like(d.v)
     vp = ctypes.c_void_p
     L.ckda_fwd_noalloc.argtypes = [vp] * 9 + [ctypes.c_int] * 7 + [ctypes.c_float, ctypes.c_int, vp]
     L.ckda_fwd_noalloc.restype = ctypes.c_int
-    rc = L.ckda_fwd_noalloc(vp(16), vp(16), vp(16), vp(16), vp(16), None, vp(16), None, vp(16),
-                            65537, 1, 1, 65537, 128, 128, 1, 1.0, 0, None)
+    p = lambda t: vp(t.data_ptr())
+    rc = L.ckda_fwd_noalloc(p(d.q), p(d.k), p(d.v), p(d.alpha), p(d.beta), None, p(o), None,
+                            p(cu), n, 1, 1, d.q.shape[2], 128, 128, 1, 1.0, 0, None)
+    torch.cuda.synchronize()
     assert rc == 2  # CKDA_ERR_UNSUPPORTED, nothing launched
