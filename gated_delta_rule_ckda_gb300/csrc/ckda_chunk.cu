@@ -1266,22 +1266,8 @@ __global__ void __launch_bounds__(NT, 1)
 }
 
 // ------------------------------------------------------------ host side
-PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    cudaDriverEntryPointQueryResult q;
-    void* p = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
-
 bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t width) {
-  auto enc = get_encoder();
+  auto enc = tensor_map_encoder();
   if (!enc) return false;
   cuuint64_t gdim[2] = {width, rows};
   cuuint64_t gstride[1] = {width * 2};
@@ -1294,6 +1280,20 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t width) {
 }
 
 }  // namespace
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
 
 cudaError_t launch_fwd_chunk(const FwdArgs& a, cudaStream_t s) {
   const int units = a.num_units_seq * a.H;

@@ -1,0 +1,1230 @@
+// ckda_fwd.cu -- chunkwise CKDA forward on tcgen05 tensor cores (sm_103a),
+// dk = dv = 128, bf16 I/O, fp32 state.
+//
+// One CTA owns one (sequence, head) and walks its tokens in chunks of C = 64
+// with the fp32 state H^T (dv x dk = 128 x 128) resident in tensor memory.
+// The chunk algebra is the WY/UT form of a product of diagonal-plus-rank-one
+// transitions ("Complex KDA: Understanding and Enhancing the Expressivity of
+// Kimi Delta Attention", Sec. 2: KDA keeps "efficient WY-based chunk-wise
+// implementations"; "Kimi Delta Attention: a bounded case study",
+// "Chunkwise execution": carrying the state block to block changes cost,
+// never the numbers).  For a chunk with initial state H (per channel i,
+// Gamma(t<-s) = prod_{s<r<=t} alpha_r, gamma_t = Gamma(t<-0),
+// rho_s = Gamma(C<-s)):
+//
+//   M[t,s] = beta_t sum_i k_ti k_si Gamma(t<-s)_i      (s < t)
+//   A[t,s] = sum_i q_ti k_si Gamma(t<-s)_i             (s <= t)
+//   T  = (I + M)^-1,   TB = T Diag(beta)
+//   W  = TB (k * gamma),           U~ = TB V
+//   U  = U~ - W H
+//   O  = (q * gamma) H + A U                            -> o
+//   H' = Diag(gamma_C) H + (k * rho)^T U
+//
+// Gate products are formed by multiplication only -- never as a ratio of
+// prefix products and never in log space -- because alpha may be negative or
+// exactly zero (paper Sec. 6 "Implementation": the KDA kernels keep gate
+// magnitudes in log space, which signed gates break).  A pair (t, s) first
+// separated at level L of a binary tree over the chunk lies in one aligned
+// segment of 2L tokens, s in the lower and t in the upper half; with m the
+// last token of the lower half, Gamma(t<-s) = [prod_{m<r<=t}][prod_{s<r<=m}],
+// a prefix product within an aligned block of L tokens times an exclusive
+// suffix product within one.
+//
+// Levels 32 and 16 form one tensor-core Gram round of gated operands
+// ("round C", 128 x 64 in tensor memory), levels 8 and 4 another ("round
+// A").  Levels 2 and 1 (pairs inside aligned 4-token groups) and the
+// diagonal q_t . k_t of A are CUDA-core sums: each thread sums its four
+// channels, one warp holds all 128.
+//
+// T is built from D, the inverses of the four 16 x 16 diagonal blocks of
+// I + M (fp32 forward substitution on CUDA cores), by block forward
+// substitution T_bc = -D_b sum_{c<=j<b} M_bj T_jc on warp-level mma.sync
+// (fp16 operands, fp32 accumulation); W = TB (k*gamma) is a warp-level
+// mma.sync product as well.  This "inverse" work of chunk c runs on warps of
+// its own while the prep warps already work on chunk c+1.
+//
+// Precision: operands of every contraction that touches the state, the
+// Grams, A and T's blocks are fp16 (11-bit significand); T Diag(beta) and
+// k * gamma are bf16; all accumulation is fp32.  Gate factors inside a block
+// of 8 tokens are fp16 product chains; block totals, gamma_C and D are fp32.
+// A non-finite o or final state is reported as CKDA_ERR_RANGE.
+//
+// Warp roles (512 threads):
+//   warps 0-7   PREP: per chunk, gate products, the Gram operands and their
+//               read-outs, the in-group sums and the state step's operands.
+//               For the elementwise work thread (blk, lane) owns channels
+//               4 lane .. 4 lane + 3 of the 8 tokens 8 blk .. 8 blk + 7, so
+//               every gate product inside a block is a register chain, every
+//               shared access is 8 bytes, and one warp holds all 128 channels
+//               of its tokens.
+//   warps 8-11  STATE: the serial state step on tensor memory (thread = TMEM
+//               lane = value column j); its first thread issues its MMAs.
+//   warps 12-14 INVERSE: D, T Diag(beta) and -W of a chunk.
+//   warp 15     ISSUE: lane 0 issues the Gram rounds and the tile copies;
+//               the warp loads beta.
+// Handoffs are mbarriers (copies, MMA completion, per-warp operand hand-over)
+// and named barriers within a role.  Every wait is bounded.
+#include "ckda_internal.cuh"
+#include "sm103.cuh"
+
+#include <cudaTypedefs.h>
+
+namespace ckda {
+namespace {
+
+constexpr int C = 64;
+constexpr int NPREP = 256;
+constexpr int NSTATE = 128;
+constexpr int NINV = 96;
+constexpr int NT = NPREP + NSTATE + NINV + 32;
+constexpr int NPREP_WARPS = NPREP / 32;            // 8
+constexpr int NINV_WARPS = NINV / 32;              // 3
+constexpr int INV_TID0 = NPREP + NSTATE;
+constexpr int BAR_PREP = 1;                        // named barrier ids
+constexpr int BAR_STATE = 2;
+constexpr int BAR_INV = 3;
+
+// ---- shared memory map (bytes from a 1024-aligned base) ----
+// q, k, alpha tiles [2 panels][64 t][64 ch] (TMA, 128B swizzle); once every
+// prep thread has read them the region holds round C's operands
+constexpr uint32_t S_TQ = 0;
+constexpr uint32_t S_TK = 16384;
+constexpr uint32_t S_TA = 32768;
+constexpr uint32_t S_RC_X = 0;         // fp16 X [2 panels][128 rows][64 ch]  K-major A
+constexpr uint32_t S_RC_Y = 32768;     // fp16 Y [2 panels][64 rows][64 ch]   K-major B
+constexpr uint32_t S_RA_X = 49152;     // round A
+constexpr uint32_t S_RA_Y = 81920;
+constexpr uint32_t S_V = 98304;        // bf16 v [2 panels][64 t][64 j]  MN-major A of U~ (TMA)
+constexpr uint32_t S_WQ = 114688;      // fp16 [-W ; q*gamma]: [2 panels][64 t + 64 t][64 i], K-major B of [U|O]
+constexpr uint32_t S_A = 147456;       // fp16 A [64 t][64 s] by chunk parity (2 x 8 KB), K-major B of O
+constexpr uint32_t S_KH = 163840;      // fp16 k*rho [2 panels][64 t][64 i], MN-major B of H
+constexpr uint32_t S_TB = 180224;      // bf16 T Diag(beta) [64 t][64 s], K-major B of U~
+constexpr uint32_t S_KG = 188416;      // bf16 k*gamma [2 panels][64 s][64 i]
+constexpr uint32_t S_MD = 204800;      // fp32 diagonal 16 x 16 blocks of M [4][16][20], by parity
+constexpr int kMdRow = 20, kMdBlk = 16 * kMdRow;
+constexpr uint32_t MD_BYTES = 5120;
+constexpr uint32_t S_NB = S_MD + 2 * MD_BYTES;   // fp16 off-diagonal 16 x 16 blocks of M, 6 x 512 B, by parity
+constexpr uint32_t NB_BYTES = 3072;
+constexpr uint32_t S_DB = S_NB + 2 * NB_BYTES;   // fp16 D blocks, 4 x 512 B
+constexpr uint32_t S_SMALL = S_DB + 2048;
+constexpr uint32_t S_BETA = S_SMALL;          // fp32 [4][64]
+constexpr uint32_t S_GAM = S_SMALL + 1024;    // fp32 [2][128] gamma_C
+constexpr uint32_t S_TOT = S_SMALL + 2048;    // float4 [8 blocks][32 quads] alpha block totals
+constexpr uint32_t S_BAR = S_SMALL + 6144;    // mbarriers, abort flag, TMEM base
+constexpr uint32_t SMEM_USED = S_SMALL + 6656;
+constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;
+static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
+static_assert(S_NB % 16 == 0 && S_DB % 16 == 0, "ldmatrix rows are 16-byte aligned");
+
+// ---- tensor memory columns ----
+constexpr uint32_t T_U = 0;     // U^T fp32 [128 j][64 t]
+constexpr uint32_t T_O = 64;    // O^T fp32 [128 j][64 t]
+constexpr uint32_t T_H = 128;   // H^T fp32 [128 j][128 i]     state
+constexpr uint32_t T_HA = 256;  // H^T fp16 [128 j][128 i]     A operand (2 per column)
+constexpr uint32_t T_UA = 320;  // U^T fp16 [128 j][64 t]      A operand
+constexpr uint32_t T_GC = 352;  // round C output [128 x 64]
+constexpr uint32_t T_GA = 416;  // round A output [128 x 64]
+constexpr uint32_t TMEM_COLS = 512;
+
+// ---- mbarriers ----
+enum Bar : int {
+  B_QKA = 0,   // q, k, alpha tiles (TMA)
+  B_V,         // v tile (TMA)
+  B_OPS_A,     // prep -> issuer: round A operands written (one arrival per prep warp)
+  B_OPS_C,     // round C operands
+  B_DONE_A,    // MMA -> waiters
+  B_DONE_C,
+  B_S1,        // state: [U | O] MMA done
+  B_S3,        // [2] state: O and H MMAs of the chunk of this parity done
+  B_READY = B_S3 + 2,   // prep and inverse -> state: the chunk's operands are in place
+  B_GAM,                // [2] prep -> state: gamma_C published
+  B_BETA = B_GAM + 2,   // [4] issue warp -> prep: beta in shared memory
+  B_MREADY = B_BETA + 4,  // [2] prep -> inverse: M blocks of the chunk of this parity
+  B_MFREE = B_MREADY + 2, // [2] inverse -> prep: done with them
+  B_KGFREE = B_MFREE + 2, // inverse -> prep: k*gamma read
+  B_COUNT
+};
+static_assert(B_COUNT * 8 <= 192, "mbarrier area");
+
+constexpr uint32_t TILE_BYTES = 16384;
+
+struct Unit {
+  long row0;
+  int len;
+  size_t sidx;   // offset of the (sequence, head) in h0 and hT
+};
+__device__ __forceinline__ Unit unit_of(const FwdArgs& a) {
+  Unit u;
+  const int b = blockIdx.x;
+  const int h = b % a.H;
+  int n = b / a.H;
+  if (a.cu_seqlens) {
+    if (a.order) n = a.order[n];
+    const int t0 = a.cu_seqlens[n];
+    u.len = a.cu_seqlens[n + 1] - t0;
+    u.row0 = (long)h * a.T + t0;
+  } else {
+    u.len = a.T;
+    u.row0 = ((long)n * a.H + h) * a.T;
+  }
+  u.sidx = ((size_t)n * a.H + h) * 128 * 128;
+  return u;
+}
+
+__device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+__device__ __forceinline__ void store16(uint8_t* p, const uint4& v) {
+  *reinterpret_cast<uint4*>(p) = v;
+}
+__device__ __forceinline__ uint4 pack_half8(const float (&f)[8]) {
+  return make_uint4(pack_half2(f[0], f[1]), pack_half2(f[2], f[3]), pack_half2(f[4], f[5]),
+                    pack_half2(f[6], f[7]));
+}
+
+// ------------------------------------------------ prep elementwise mapping
+// Four channels 4 lane .. 4 lane + 3 as two fp16 pairs.
+struct H4 {
+  __half2 p[2];
+};
+__device__ __forceinline__ H4 mul4(const H4& x, const H4& y) {
+  return H4{{__hmul2(x.p[0], y.p[0]), __hmul2(x.p[1], y.p[1])}};
+}
+__device__ __forceinline__ H4 h4_of(const float4& f) {
+  return H4{{__floats2half2_rn(f.x, f.y), __floats2half2_rn(f.z, f.w)}};
+}
+// Thread part of the byte offset of the channels 4 lane .. 4 lane + 3 in a
+// 128B-swizzled tile of R rows with 64-column panels: the panel, the 16-byte
+// chunk ((lane & 15) >> 1) and the 8-byte half in it.
+template <uint32_t R>
+__device__ __forceinline__ uint32_t quad_tb(int lane) {
+  return ((uint32_t)lane >> 4) * R * 128u + ((((uint32_t)lane & 15u) >> 1) << 4) +
+         (((uint32_t)lane & 1u) << 3);
+}
+// Offset of those channels in row `row`: the row's swizzle is an XOR of bits 4..6.
+__device__ __forceinline__ uint32_t quad_at(uint32_t tb, uint32_t row) {
+  return (tb ^ ((row & 7u) << 4)) + row * 128u;
+}
+__device__ __forceinline__ void st_quad(uint8_t* p, const H4& v) {
+  *reinterpret_cast<uint2*>(p) = make_uint2(h2u(v.p[0]), h2u(v.p[1]));
+}
+
+// One 8-token block of four channels: k, scale * q and alpha in fp16, the
+// fp32 partial q.k of each token and the fp32 block total of alpha.  Tokens
+// at or past `live` (the end of the sequence, relative to the block) become
+// identity transitions: k = q = 0, alpha = 1.
+struct Blk8 {
+  H4 a[8], k[8], q[8];
+  float dqk[8];
+  float4 tot;
+};
+__device__ __forceinline__ float4 bf4(uint2 w) {
+  return make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u),
+                     __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
+}
+template <bool kMask>
+__device__ __forceinline__ void load_block(Blk8& B, const uint8_t* sm, int blk, int lane,
+                                           float scale, int live) {
+  B.tot = make_float4(1.f, 1.f, 1.f, 1.f);
+  const uint32_t tb = quad_tb<64>(lane);
+#pragma unroll
+  for (int r = 0; r < 8; ++r) {
+    const uint32_t off = quad_at(tb, (uint32_t)(8 * blk + r));
+    float4 kf = bf4(*reinterpret_cast<const uint2*>(sm + S_TK + off));
+    float4 qf = bf4(*reinterpret_cast<const uint2*>(sm + S_TQ + off));
+    float4 af = bf4(*reinterpret_cast<const uint2*>(sm + S_TA + off));
+    qf.x *= scale; qf.y *= scale; qf.z *= scale; qf.w *= scale;
+    if (kMask && r >= live) {
+      kf = make_float4(0.f, 0.f, 0.f, 0.f);
+      qf = kf;
+      af = make_float4(1.f, 1.f, 1.f, 1.f);
+    }
+    B.dqk[r] = fmaf(qf.x, kf.x, fmaf(qf.y, kf.y, fmaf(qf.z, kf.z, qf.w * kf.w)));
+    B.k[r] = h4_of(kf);
+    B.q[r] = h4_of(qf);
+    B.a[r] = h4_of(af);
+    B.tot.x *= af.x; B.tot.y *= af.y; B.tot.z *= af.z; B.tot.w *= af.w;
+  }
+}
+
+// Operand rows of one tree level for the tokens r0 .. r0 + n - 1 of this
+// block, as upper tokens (X rows xk + u and xq + u, u = u0 + j, gated by the
+// running product of alpha from r0 times `pre`) or as lower tokens (Y rows
+// yr + l, l = l0 + j, gated by the exclusive running suffix product to
+// r0 + n - 1 times `post`).
+template <int R0, int N>
+__device__ __forceinline__ void put_upper(uint8_t* X, uint32_t tx, const Blk8& B, H4 f,
+                                          uint32_t xk, uint32_t xq) {
+#pragma unroll
+  for (int j = 0; j < N; ++j) {
+    f = mul4(f, B.a[R0 + j]);
+    st_quad(X + quad_at(tx, xk + j), mul4(B.k[R0 + j], f));
+    st_quad(X + quad_at(tx, xq + j), mul4(B.q[R0 + j], f));
+  }
+}
+template <int R0, int N>
+__device__ __forceinline__ void put_lower(uint8_t* Y, uint32_t ty, const Blk8& B, H4 b,
+                                          uint32_t yr) {
+#pragma unroll
+  for (int j = N - 1; j >= 0; --j) {
+    if (j < N - 1) b = mul4(b, B.a[R0 + j + 1]);
+    st_quad(Y + quad_at(ty, yr + j), mul4(B.k[R0 + j], b));
+  }
+}
+__device__ __forceinline__ H4 ones4() {
+  return H4{{__floats2half2_rn(1.f, 1.f), __floats2half2_rn(1.f, 1.f)}};
+}
+
+// Round A: level 8 (pairs between the two 8-token halves of a 16-token
+// block: this block is the upper half if blk is odd) in X rows 0..63 and Y
+// rows 0..31, level 4 (pairs between the halves of this block) in X rows
+// 64..127 and Y rows 32..63.  X rows r < 32 of a level hold k, r + 32 q of
+// the same upper token.  Ranks: level 8 upper/lower 8 (blk >> 1) + r,
+// level 4 upper 4 blk + (r - 4), lower 4 blk + r.
+__device__ __forceinline__ void write_round_a(uint8_t* sm, const Blk8& B, int blk, int lane) {
+  const uint32_t tx = quad_tb<128>(lane), ty = quad_tb<64>(lane);
+  uint8_t* X = sm + S_RA_X;
+  uint8_t* Y = sm + S_RA_Y;
+  const uint32_t r8 = 8u * (uint32_t)(blk >> 1), r4 = 4u * (uint32_t)blk;
+  if (blk & 1) put_upper<0, 8>(X, tx, B, ones4(), r8, 32 + r8);
+  else put_lower<0, 8>(Y, ty, B, ones4(), r8);
+  put_upper<4, 4>(X, tx, B, ones4(), 64 + r4, 96 + r4);
+  put_lower<0, 4>(Y, ty, B, ones4(), 32 + r4);
+}
+// Round C: level 32 (blocks 4..7 upper, 0..3 lower) in X rows 0..63 and Y
+// rows 0..31; level 16 (in the 32-token segment j = blk >> 2, its blocks
+// 4j+2, 4j+3 upper and 4j, 4j+1 lower) in X rows 64..127 and Y rows 32..63.
+// The factors reach across blocks through the fp32 block totals T8.
+// Ranks: level 32 upper 8 (blk - 4) + r, lower 8 blk + r; level 16 upper
+// 16 j + 8 (blk - 4j - 2) + r, lower 16 j + 8 (blk - 4j) + r.
+__device__ __forceinline__ void write_round_c(uint8_t* sm, const Blk8& B, const float4 (&T8)[8],
+                                              int blk, int lane) {
+  const uint32_t tx = quad_tb<128>(lane), ty = quad_tb<64>(lane);
+  uint8_t* X = sm + S_RC_X;
+  uint8_t* Y = sm + S_RC_Y;
+  float4 F = make_float4(1.f, 1.f, 1.f, 1.f);
+  if (blk >= 4) {
+#pragma unroll
+    for (int b = 4; b < 8; ++b)
+      if (b < blk) { F.x *= T8[b].x; F.y *= T8[b].y; F.z *= T8[b].z; F.w *= T8[b].w; }
+    const uint32_t u0 = 8u * (uint32_t)(blk - 4);
+    put_upper<0, 8>(X, tx, B, h4_of(F), u0, 32 + u0);
+  } else {
+#pragma unroll
+    for (int b = 1; b < 4; ++b)
+      if (b > blk) { F.x *= T8[b].x; F.y *= T8[b].y; F.z *= T8[b].z; F.w *= T8[b].w; }
+    put_lower<0, 8>(Y, ty, B, h4_of(F), 8u * (uint32_t)blk);
+  }
+  // the neighbouring block's total, selected with compile-time indices so
+  // that T8 stays in registers
+  float4 nb = make_float4(1.f, 1.f, 1.f, 1.f);
+#pragma unroll
+  for (int b = 0; b < 8; ++b)
+    if (((blk & 3) == 3 && b == blk - 1) || ((blk & 3) == 0 && b == blk + 1)) nb = T8[b];
+  const int j = blk >> 2, loc = blk & 3;
+  if (loc >= 2) {
+    const H4 f = loc == 3 ? h4_of(nb) : ones4();
+    const uint32_t u0 = 16u * (uint32_t)j + 8u * (uint32_t)(loc - 2);
+    put_upper<0, 8>(X, tx, B, f, 64 + u0, 96 + u0);
+  } else {
+    const H4 b = loc == 0 ? h4_of(nb) : ones4();
+    put_lower<0, 8>(Y, ty, B, b, 32u + 16u * (uint32_t)j + 8u * (uint32_t)loc);
+  }
+}
+
+// Offsets in the A tile [64 t][64 s] (K-major, 128B swizzle) and in the
+// fp32 diagonal blocks of M.
+__device__ __forceinline__ uint32_t a_off(int t, int s) { return sw128_off(64, t, s); }
+__device__ __forceinline__ float* md_at(uint8_t* sm, int slot, int t, int s) {
+  return reinterpret_cast<float*>(sm + S_MD + slot * MD_BYTES) + (t >> 4) * kMdBlk +
+         (t & 15) * kMdRow + (s & 15);
+}
+// 16 x 16 fp16 blocks (N, D), row-major with 32-byte rows; the 16-byte half
+// of a row is XORed with bit 2 of the row so that ldmatrix reads and row
+// stores are free of bank conflicts.
+__device__ __forceinline__ uint32_t blk16_off(int r, int col) {
+  return (uint32_t)r * 32u + ((((uint32_t)col >> 3) ^ (((uint32_t)r >> 2) & 1u)) << 4) +
+         ((uint32_t)col & 7u) * 2u;
+}
+__device__ __forceinline__ int nblk_index(int b, int j) { return b * (b - 1) / 2 + j; }
+
+// Read-outs.  Warp (wq, h) reads TMEM lane quarter wq, 16 of the 32 columns
+// of its level: rows of quarter 0 are level-La k rows, 1 its q rows, 2 and 3
+// the k and q rows of level La / 2; columns 0..31 are La's lower ranks,
+// 32..63 those of La / 2.  Lane u of a quarter is upper rank u.
+__device__ __forceinline__ void tmem_cols16(uint32_t tmem, int wq, uint32_t col, float (&f)[16]) {
+  uint32_t v[16];
+  tmem_ld32<16>(tmem + ((uint32_t)(32 * wq) << 16) + col, v);
+  tmem_ld_wait();
+#pragma unroll
+  for (int e = 0; e < 16; ++e) f[e] = __uint_as_float(v[e]);
+}
+// Round A: level 8, segment m = u >> 3, t = 16 m + 8 + (u & 7), s = 16 m + e;
+// level 4, segment u >> 2, t = 8 (u >> 2) + 4 + (u & 3), s = 8 (u >> 2) + e.
+// Both are pairs inside 16-token blocks: M goes to the fp32 diagonal blocks.
+__device__ __forceinline__ void readout_a(uint8_t* sm, int slot, uint32_t tmem, int wq, int h,
+                                          int lane, const float* beta) {
+  uint8_t* At = sm + S_A + slot * 8192;
+  const bool lvl8 = wq < 2, qrow = (wq & 1) != 0;
+  float f[16];
+  tmem_cols16(tmem, wq, T_GA + (lvl8 ? 0u : 32u) + 16u * h, f);
+  if ((lane >> 4) != h) return;
+  int t, s0, n, e0;
+  if (lvl8) {
+    t = 16 * (lane >> 3) + 8 + (lane & 7);
+    s0 = 16 * (lane >> 3);
+    n = 8;
+    e0 = 8 * ((lane >> 3) & 1);
+  } else {
+    t = 8 * (lane >> 2) + 4 + (lane & 3);
+    s0 = 8 * (lane >> 2);
+    n = 4;
+    e0 = 4 * ((lane >> 2) & 3);
+  }
+  float g[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) g[e] = 0.f;
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    if (e0 == 4 * k) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        if (4 * k + e < 16) g[e] = f[4 * k + e];
+    }
+  if (qrow) {
+    if (n == 8)
+      store16(At + sw128_chunk(64, t, (uint32_t)s0 >> 3), pack_half8(g));
+    else
+      *reinterpret_cast<uint2*>(At + a_off(t, s0)) =
+          make_uint2(pack_half2(g[0], g[1]), pack_half2(g[2], g[3]));
+  } else {
+    const float bt = beta[t];
+    float* m = md_at(sm, slot, t, s0);
+    *reinterpret_cast<float4*>(m) = make_float4(bt * g[0], bt * g[1], bt * g[2], bt * g[3]);
+    if (n == 8)
+      *reinterpret_cast<float4*>(m + 4) = make_float4(bt * g[4], bt * g[5], bt * g[6], bt * g[7]);
+  }
+}
+// Round C: level 32, t = 32 + u, every column valid, s = column; level 16,
+// segment u >> 4, t = 32 (u >> 4) + 16 + (u & 15), s = 32 (u >> 4) + e.  Pairs
+// across 16-token blocks: M (times beta_t) goes to the fp16 off-diagonal
+// blocks.
+__device__ __forceinline__ void readout_c(uint8_t* sm, int slot, uint32_t tmem, int wq, int h,
+                                          int lane, const float* beta) {
+  uint8_t* At = sm + S_A + slot * 8192;
+  const bool lvl32 = wq < 2, qrow = (wq & 1) != 0;
+  float f[16];
+  tmem_cols16(tmem, wq, T_GC + (lvl32 ? 0u : 32u) + 16u * h, f);
+  int t, s0;
+  if (lvl32) {
+    t = 32 + lane;
+    s0 = 16 * h;
+  } else {
+    if ((lane >> 4) != h) return;
+    t = 32 * h + 16 + (lane & 15);
+    s0 = 32 * h;
+  }
+  if (qrow) {
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      float g[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) g[e] = f[8 * hh + e];
+      store16(At + sw128_chunk(64, t, ((uint32_t)s0 >> 3) + hh), pack_half8(g));
+    }
+  } else {
+    const float bt = beta[t];
+    const int nb = nblk_index(t >> 4, s0 >> 4);
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      float g[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) g[e] = bt * f[8 * hh + e];
+      store16(sm + S_NB + slot * NB_BYTES + nb * 512 + blk16_off(t & 15, 8 * hh), pack_half8(g));
+    }
+  }
+}
+
+// Inverses of the four unit-lower 16 x 16 diagonal blocks of I + M, one
+// column per thread by forward substitution: x_c = 1 and, for t > c,
+// x_t = -sum_{s<t} M[t][s] x_s.  Rows are taken four at a time: the four dot
+// products with the earlier rows' x are independent, then a 4 x 4
+// triangular step finishes them.  Written as fp16 into the D blocks, and as
+// D Diag(beta) in bf16 into the diagonal blocks of TB.  Threads 0..63.
+__device__ __forceinline__ float f4c(const float4& v, int i) {
+  return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+}
+__device__ __forceinline__ void invert_diag_blocks(uint8_t* sm, int slot, int p, const float* beta) {
+  const int blk = p >> 4, c = p & 15, o = 16 * blk;
+  const float* Md = reinterpret_cast<const float*>(sm + S_MD + slot * MD_BYTES) + blk * kMdBlk;
+  float x[16];
+#pragma unroll
+  for (int ib = 0; ib < 4; ++ib) {
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int q4 = 0; q4 < ib; ++q4) {
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const float4 m = *reinterpret_cast<const float4*>(Md + (4 * ib + r) * kMdRow + 4 * q4);
+        acc[r] = fmaf(m.w, x[4 * q4 + 3],
+                      fmaf(m.z, x[4 * q4 + 2], fmaf(m.y, x[4 * q4 + 1], fmaf(m.x, x[4 * q4], acc[r]))));
+      }
+    }
+    float4 mr[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) mr[r] = *reinterpret_cast<const float4*>(Md + (4 * ib + r) * kMdRow + 4 * ib);
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int t = 4 * ib + r;
+      float a = acc[r];
+#pragma unroll
+      for (int r2 = 0; r2 < r; ++r2) a = fmaf(f4c(mr[r], r2), x[4 * ib + r2], a);
+      x[t] = t < c ? 0.f : (t == c ? 1.f : -a);
+    }
+  }
+  const float bc = beta[o + c];
+  uint8_t* D = sm + S_DB + blk * 512;
+#pragma unroll
+  for (int t = 0; t < 16; ++t) {
+    *reinterpret_cast<__half*>(D + blk16_off(t, c)) = __float2half_rn(x[t]);
+    *reinterpret_cast<__nv_bfloat16*>(sm + S_TB + sw128_off(64, o + t, o + c)) =
+        __float2bfloat16_rn(x[t] * bc);
+  }
+}
+
+// ldmatrix address of lane `lane` for a 16 x 16 fp16 block at `base`:
+// matrices (rows 0-7, cols 0-7), (rows 8-15, cols 0-7), (rows 0-7, cols
+// 8-15), (rows 8-15, cols 8-15).
+__device__ __forceinline__ uint32_t blk16_lane_addr(uint32_t base, int lane) {
+  const int r = (lane & 7) + 8 * ((lane >> 3) & 1), half = lane >> 4;
+  return base + (uint32_t)r * 32u + ((((uint32_t)half) ^ (((uint32_t)r >> 2) & 1u)) << 4);
+}
+// B fragments (two n8 tiles, K = 16) of a 16 x 16 matrix held as the
+// accumulators of two m16n8 products: each 8 x 8 quarter is transposed in
+// registers.  `neg` negates it.
+__device__ __forceinline__ void c_to_b(const float (&x)[2][4], uint32_t (&b)[4], float neg) {
+  b[0] = movm_t(pack_half2(neg * x[0][0], neg * x[0][1]));
+  b[1] = movm_t(pack_half2(neg * x[0][2], neg * x[0][3]));
+  b[2] = movm_t(pack_half2(neg * x[1][0], neg * x[1][1]));
+  b[3] = movm_t(pack_half2(neg * x[1][2], neg * x[1][3]));
+}
+// Column block CB of T below the diagonal: T_bc = -D_b sum_{CB<=j<b} M_bj T_jCB
+// for b = CB+1 .. 3, with T_CB,CB = D_CB; each stored as T Diag(beta) in bf16.
+template <int CB>
+__device__ __forceinline__ void inverse_column(uint8_t* sm, uint32_t sb, int slot, int lane,
+                                               const float* beta) {
+  uint32_t Tb[4][4];
+  ldsm_x4_t(Tb[CB], blk16_lane_addr(sb + S_DB + CB * 512, lane));
+  const int g = lane >> 2, cq = lane & 3;
+#pragma unroll
+  for (int b = CB + 1; b < 4; ++b) {
+    float x[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+    for (int j = CB; j < b; ++j) {
+      uint32_t am[4];
+      ldsm_x4(am, blk16_lane_addr(sb + S_NB + slot * NB_BYTES + nblk_index(b, j) * 512, lane));
+      mma16816(x[0], am, Tb[j][0], Tb[j][1]);
+      mma16816(x[1], am, Tb[j][2], Tb[j][3]);
+    }
+    uint32_t xb[4];
+    c_to_b(x, xb, -1.f);
+    uint32_t ad[4];
+    ldsm_x4(ad, blk16_lane_addr(sb + S_DB + b * 512, lane));
+    float t[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    mma16816(t[0], ad, xb[0], xb[1]);
+    mma16816(t[1], ad, xb[2], xb[3]);
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      const int col = 16 * CB + 8 * nt + 2 * cq;
+      const float b0 = beta[col], b1 = beta[col + 1];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int row = 16 * b + g + 8 * h;
+        *reinterpret_cast<uint32_t*>(sm + S_TB + sw128_off(64, row, col)) =
+            pack_bf162(t[nt][2 * h] * b0, t[nt][2 * h + 1] * b1);
+      }
+    }
+    if (b < 3) c_to_b(t, Tb[b], 1.f);
+  }
+}
+
+// Pairs inside aligned 4-token groups (tree levels 1 and 2) and the diagonal
+// q_t . k_t, summed over this thread's four channels.  Operands are rounded
+// to fp16 as the tensor-core rounds are.  Per
+// group g (tokens 4g .. 4g+3 of the block) the 16 values are, at 16 g + j:
+//   j 0..3    q_t . k_t, t = 4g + j
+//   j 4, 5    M, A of (4g+1, 4g)       j 6, 7    M, A of (4g+3, 4g+2)
+//   j 8..11   M of (4g+2, 4g), (4g+2, 4g+1), (4g+3, 4g), (4g+3, 4g+1)
+//   j 12..15  A of the same pairs
+// (M without its beta_t).
+// Two channels of each pair are multiplied and added in fp16 (one rounding
+// of a partial of two products, like the rounding of a Gram operand); the
+// two halves and then the 128 channels are summed in fp32.
+__device__ __forceinline__ float dot4(const H4& x, const H4& y) {
+  const float2 d = __half22float2(__hfma2(x.p[1], y.p[1], __hmul2(x.p[0], y.p[0])));
+  return d.x + d.y;
+}
+__device__ __forceinline__ void in_group_pairs(const Blk8& B, float (&v)[32]) {
+#pragma unroll
+  for (int g = 0; g < 2; ++g) {
+    const int t0 = 4 * g;
+    float* o = v + 16 * g;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) o[j] = B.dqk[t0 + j];
+    // level 1: (t0+1, t0), (t0+3, t0+2); the gate product is alpha of the upper token
+    const H4 xk1 = mul4(B.k[t0 + 1], B.a[t0 + 1]), xq1 = mul4(B.q[t0 + 1], B.a[t0 + 1]);
+    const H4 xk3 = mul4(B.k[t0 + 3], B.a[t0 + 3]), xq3 = mul4(B.q[t0 + 3], B.a[t0 + 3]);
+    o[4] = dot4(xk1, B.k[t0]);
+    o[5] = dot4(xq1, B.k[t0]);
+    o[6] = dot4(xk3, B.k[t0 + 2]);
+    o[7] = dot4(xq3, B.k[t0 + 2]);
+    // level 2: uppers t0+2, t0+3 with prefixes alpha_{t0+2}, alpha_{t0+2} alpha_{t0+3};
+    // lowers t0 (suffix alpha_{t0+1}) and t0+1 (empty)
+    const H4 f3 = mul4(B.a[t0 + 2], B.a[t0 + 3]);
+    const H4 uk2 = mul4(B.k[t0 + 2], B.a[t0 + 2]), uq2 = mul4(B.q[t0 + 2], B.a[t0 + 2]);
+    const H4 uk3 = mul4(B.k[t0 + 3], f3), uq3 = mul4(B.q[t0 + 3], f3);
+    const H4 y0 = mul4(B.k[t0], B.a[t0 + 1]);
+    const H4& y1 = B.k[t0 + 1];
+    o[8] = dot4(uk2, y0);
+    o[9] = dot4(uk2, y1);
+    o[10] = dot4(uk3, y0);
+    o[11] = dot4(uk3, y1);
+    o[12] = dot4(uq2, y0);
+    o[13] = dot4(uq2, y1);
+    o[14] = dot4(uq3, y0);
+    o[15] = dot4(uq3, y1);
+  }
+}
+// Sums each of the 32 values over the warp (all 128 channels) by halving
+// exchanges; lane l ends with the sum of value l.
+__device__ __forceinline__ float warp_sum32(float (&v)[32], int lane) {
+#pragma unroll
+  for (int w = 16; w >= 1; w >>= 1) {
+    const bool hi = (lane & w) != 0;
+#pragma unroll
+    for (int i = 0; i < w; ++i) {
+      const float send = hi ? v[i] : v[i + w];
+      const float keep = hi ? v[i + w] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+    }
+  }
+  return v[0];
+}
+// Stores in-group value `idx` of block blk (a warp_sum32 result) in A (fp16)
+// or, times beta_t, in the diagonal blocks of M.
+__device__ __forceinline__ void store_in_group(uint8_t* sm, int slot, int blk, int idx, float v,
+                                               const float* beta) {
+  const int g = idx >> 4, j = idx & 15, t0 = 8 * blk + 4 * g;
+  int t, s;
+  bool is_a;
+  if (j < 4) {
+    t = s = t0 + j;
+    is_a = true;
+  } else if (j < 8) {
+    t = t0 + 1 + 2 * ((j - 4) >> 1);
+    s = t - 1;
+    is_a = (j & 1) != 0;
+  } else {
+    const int jj = (j - 8) & 3;
+    t = t0 + 2 + (jj >> 1);
+    s = t0 + (jj & 1);
+    is_a = j >= 12;
+  }
+  if (is_a)
+    *reinterpret_cast<__half*>(sm + S_A + slot * 8192 + a_off(t, s)) = __float2half_rn(v);
+  else
+    *md_at(sm, slot, t, s) = beta[t] * v;
+}
+
+// -W = -TB (k*gamma) (64 t x 128 i, K = 64 s) on warp-level mma.sync (bf16
+// operands, fp32 accumulation): A = TB from its tile [t][s], B = k*gamma
+// from its tile [s][i] by transposed ldmatrix.  The result goes to rows 0..63
+// of [-W ; q*gamma] ([t][i], K-major).  Inverse warp iw takes the pairs of
+// 8-column tiles of i with index iw, iw + 3, iw + 6 for every 16-row tile of t.
+__device__ __forceinline__ void mma16816_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                              uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void minus_w(uint8_t* sm, uint32_t sb, int iw, int lane) {
+  const int g = lane >> 2, cq = lane & 3, mi = lane >> 3;
+#pragma unroll 1
+  for (int np = iw; np < 8; np += NINV_WARPS) {
+    // one pair of 8-column tiles of i against all four 16-row tiles of t:
+    // each K step issues eight independent products
+    float acc[4][2][4];
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) acc[mt][nt][0] = acc[mt][nt][1] = acc[mt][nt][2] = acc[mt][nt][3] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+      uint32_t bf[4];
+      {
+        const int s = 16 * ks + (lane & 7) + 8 * (mi & 1), i = 16 * np + 8 * (mi >> 1);
+        ldsm_x4_t(bf, sb + S_KG + (uint32_t)(i >> 6) * 8192u + (uint32_t)s * 128u +
+                          ((((uint32_t)(i & 63) >> 3) ^ ((uint32_t)s & 7u)) << 4));
+      }
+      uint32_t af[4][4];
+#pragma unroll
+      for (int mt = 0; mt < 4; ++mt) {
+        const int t = 16 * mt + (lane & 7) + 8 * (mi & 1), s = 16 * ks + 8 * (mi >> 1);
+        ldsm_x4(af[mt], sb + S_TB + (uint32_t)t * 128u + ((((uint32_t)s >> 3) ^ ((uint32_t)t & 7u)) << 4));
+      }
+#pragma unroll
+      for (int mt = 0; mt < 4; ++mt) {
+        mma16816_bf16(acc[mt][0], af[mt], bf[0], bf[1]);
+        mma16816_bf16(acc[mt][1], af[mt], bf[2], bf[3]);
+      }
+    }
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int row = 16 * mt + g + 8 * h, col = 16 * np + 8 * nt + 2 * cq;
+          *reinterpret_cast<uint32_t*>(sm + S_WQ + sw128_off(128, row, col)) =
+              pack_half2(-acc[mt][nt][2 * h], -acc[mt][nt][2 * h + 1]);
+        }
+  }
+}
+
+// D (tmem) (+)= A (tmem) x B (smem), issued by a single thread.
+__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                        uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Makes this warp's shared-memory writes (and tensor-memory reads) ordered
+// before the tensor cores' next use and arrives on `bar` once for the warp.
+__device__ __forceinline__ void warp_publish(uint64_t* bar, int lane) {
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar);
+}
+
+__global__ void __launch_bounds__(NT, 1)
+    fwd_kernel(const __grid_constant__ FwdArgs a, const __grid_constant__ CUtensorMap mq,
+               const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap ma,
+               const __grid_constant__ CUtensorMap mv) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + S_BAR);
+  int* s_abort = reinterpret_cast<int*>(sm + S_BAR + 192);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + S_BAR + 200);
+
+  const Unit u = unit_of(a);
+  const int nchunks = (u.len + C - 1) / C;
+
+  if (tid == 0) {
+    for (int i = 0; i < B_COUNT; ++i) {
+      uint32_t cnt = 1;
+      if (i == B_OPS_A || i == B_OPS_C || i == B_MREADY || i == B_MREADY + 1) cnt = NPREP_WARPS;
+      if (i == B_MFREE || i == B_MFREE + 1 || i == B_KGFREE) cnt = NINV_WARPS;
+      if (i == B_READY) cnt = NPREP_WARPS + NINV_WARPS;
+      mbar_init(bars + i, cnt);
+    }
+    *s_abort = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&mq);
+    tma_prefetch_desc(&mk);
+    tma_prefetch_desc(&ma);
+    tma_prefetch_desc(&mv);
+  }
+  // entries never written: A's upper triangles, TB's blocks above the diagonal
+  for (int e = tid; e < 8192 / 16; e += NT) {
+    reinterpret_cast<uint4*>(sm + S_A)[e] = make_uint4(0, 0, 0, 0);
+    reinterpret_cast<uint4*>(sm + S_A + 8192)[e] = make_uint4(0, 0, 0, 0);
+    reinterpret_cast<uint4*>(sm + S_TB)[e] = make_uint4(0, 0, 0, 0);
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t sb = smem_u32(sm);
+  bool ovf = false;
+
+  if (tid < NPREP) {
+    // =================================================================== PREP
+    const int blk = warp;                     // elementwise mapping: 8-token block
+    const int wq = warp & 3, hc = warp >> 2;  // read-outs: TMEM lane quarter, column half
+    bool alive = true, ok = true;
+    const float4* tot_s = reinterpret_cast<const float4*>(sm + S_TOT);
+    for (int c = 0; c < nchunks && alive; ++c) {
+      const int lenc = min(C, u.len - c * C);
+      const int slot = c & 1;
+      const float* beta_c = reinterpret_cast<const float*>(sm + S_BETA) + 64 * (c & 3);
+      // ---- 1. q, k, alpha of chunk c
+      ok = ok && mbar_wait(bars + B_QKA, (uint32_t)(c & 1));
+      Blk8 B;
+      if (lenc == C) load_block<false>(B, sm, blk, lane, a.scale, C);
+      else load_block<true>(B, sm, blk, lane, a.scale, lenc - 8 * blk);
+      // ---- 2. round A (levels 8, 4); its buffer was last read by round A of
+      // chunk c-1, whose completion this role waited for
+      write_round_a(sm, B, blk, lane);
+      warp_publish(bars + B_OPS_A, lane);
+      // ---- 3. in-group pairs and q.k over all 128 channels (the warp)
+      float ig;
+      {
+        float v[32];
+        in_group_pairs(B, v);
+        ig = warp_sum32(v, lane);
+      }
+      reinterpret_cast<float4*>(sm + S_TOT)[blk * 32 + lane] = B.tot;
+      // ---- 4. every tile read is done; block totals are visible
+      if (!named_and(BAR_PREP, NPREP, ok)) { alive = false; break; }
+      // ---- 5. round C (levels 32, 16) into the tile region
+      float4 T8[8];
+#pragma unroll
+      for (int b = 0; b < 8; ++b) T8[b] = tot_s[b * 32 + lane];
+      write_round_c(sm, B, T8, blk, lane);
+      warp_publish(bars + B_OPS_C, lane);
+      // gamma_C (fp32: it scales the fp32 state); k*gamma (bf16) once the
+      // inverse warps have finished chunk c-1's W; q*gamma and k*rho (rho_s =
+      // exclusive suffix times later blocks' totals) stay in registers until
+      // the state has released their tiles
+      if (blk == 0) {
+        float4 g = T8[0];
+#pragma unroll
+        for (int b = 1; b < 8; ++b) { g.x *= T8[b].x; g.y *= T8[b].y; g.z *= T8[b].z; g.w *= T8[b].w; }
+        reinterpret_cast<float4*>(sm + S_GAM)[32 * (c & 1) + lane] = g;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bars + B_GAM + (c & 1));
+      }
+      if (c > 0) ok = ok && mbar_wait(bars + B_KGFREE, (uint32_t)((c - 1) & 1));
+      H4 gq[8], kr[8];
+      {
+        float4 Gb = make_float4(1.f, 1.f, 1.f, 1.f), Ga = Gb;
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+          if (b < blk) { Gb.x *= T8[b].x; Gb.y *= T8[b].y; Gb.z *= T8[b].z; Gb.w *= T8[b].w; }
+          if (b > blk) { Ga.x *= T8[b].x; Ga.y *= T8[b].y; Ga.z *= T8[b].z; Ga.w *= T8[b].w; }
+        }
+        H4 g = h4_of(Gb);
+        const uint32_t tb = quad_tb<64>(lane);
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          g = mul4(g, B.a[r]);
+          const H4 kg = mul4(B.k[r], g);
+          const float2 k0 = __half22float2(kg.p[0]), k1 = __half22float2(kg.p[1]);
+          *reinterpret_cast<uint2*>(sm + S_KG + quad_at(tb, (uint32_t)(8 * blk + r))) =
+              make_uint2(pack_bf162(k0.x, k0.y), pack_bf162(k1.x, k1.y));
+          gq[r] = mul4(B.q[r], g);
+        }
+        H4 rr = h4_of(Ga);
+#pragma unroll
+        for (int r = 7; r >= 0; --r) {
+          if (r < 7) rr = mul4(rr, B.a[r + 1]);
+          kr[r] = mul4(B.k[r], rr);
+        }
+      }
+      // ---- 6. this parity's M blocks and A tile are free (the inverse warps
+      // and the state's O step of chunk c-2 are done with them); beta in place
+      ok = ok && mbar_wait(bars + B_BETA + (c & 3), (uint32_t)((c >> 2) & 1));
+      if (c >= 2) {
+        ok = ok && mbar_wait(bars + B_MFREE + slot, (uint32_t)(((c - 2) >> 1) & 1));
+        ok = ok && mbar_wait(bars + B_S3 + slot, (uint32_t)(((c - 2) >> 1) & 1));
+      }
+      store_in_group(sm, slot, blk, lane, ig, beta_c);
+      // ---- 7. Gram read-outs
+      ok = ok && mbar_wait(bars + B_DONE_A, (uint32_t)(c & 1));
+      tc_fence_after();
+      readout_a(sm, slot, tmem, wq, hc, lane, beta_c);
+      ok = ok && mbar_wait(bars + B_DONE_C, (uint32_t)(c & 1));
+      tc_fence_after();
+      readout_c(sm, slot, tmem, wq, hc, lane, beta_c);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars + B_MREADY + slot);
+      // ---- 8. q*gamma (rows 64.. of [-W ; q*gamma]) and k*rho, once chunk
+      // c-1's state MMAs have read their tiles
+      if (c > 0) {
+        ok = ok && mbar_wait(bars + B_S1, (uint32_t)((c - 1) & 1));
+        ok = ok && mbar_wait(bars + B_S3 + ((c - 1) & 1), (uint32_t)(((c - 1) >> 1) & 1));
+      }
+      {
+        const uint32_t tq = quad_tb<128>(lane), tk = quad_tb<64>(lane);
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          st_quad(sm + S_WQ + quad_at(tq, (uint32_t)(64 + 8 * blk + r)), gq[r]);
+          st_quad(sm + S_KH + quad_at(tk, (uint32_t)(8 * blk + r)), kr[r]);
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars + B_READY);
+    }
+    if (!alive || !ok) *reinterpret_cast<volatile int*>(s_abort) = 1;
+  } else if (tid < NPREP + NSTATE) {
+
+
+    // ================================================================== STATE
+    const int s = tid - NPREP;   // 0..127 = TMEM lane = value column j
+    const int wq = s >> 5;
+    const uint32_t lb = (uint32_t)(32 * wq) << 16;
+    const bool lead = s == 0;
+    float* hT = a.hT;
+    bool alive = true;
+    const float* gc_all = reinterpret_cast<const float*>(sm + S_GAM);
+    // H^T as the fp16 A operand (TMEM) and, in TMEM, H^T Diag(gamma_C) of
+    // the chunk about to start (column i times gC[i])
+    auto convert_and_scale = [&](int c_next, bool from_h0) {
+      const float* gC = gc_all + 128 * (c_next & 1);
+#pragma unroll 1
+      for (int i0 = 0; i0 < 128; i0 += 16) {
+        float f[16];
+        if (from_h0) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            f[e] = a.h0 ? a.h0[u.sidx + (size_t)(i0 + e) * 128 + s] : 0.f;
+        } else {
+          uint32_t v[16];
+          tmem_ld32<16>(tmem + lb + T_H + i0, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) f[e] = __uint_as_float(v[e]);
+        }
+        uint32_t h[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) h[e] = pack_half2(f[2 * e], f[2 * e + 1]);
+        tmem_st32<8>(tmem + lb + T_HA + (i0 >> 1), h);
+        uint32_t o[16];
+#pragma unroll
+        for (int e = 0; e < 16; e += 4) {
+          const float4 g4 = *reinterpret_cast<const float4*>(gC + i0 + e);
+          o[e] = __float_as_uint(f[e] * g4.x);
+          o[e + 1] = __float_as_uint(f[e + 1] * g4.y);
+          o[e + 2] = __float_as_uint(f[e + 2] * g4.z);
+          o[e + 3] = __float_as_uint(f[e + 3] * g4.w);
+        }
+        tmem_st32<16>(tmem + lb + T_H + i0, o);
+      }
+      tmem_st_wait();
+    };
+    if (nchunks > 0) {
+      const bool ok = mbar_wait(bars + B_GAM, 0);
+      alive = named_and(BAR_STATE, NSTATE, ok);
+      if (alive) convert_and_scale(0, true);
+    } else if (hT) {
+      for (int i = 0; i < 128; ++i)
+        hT[u.sidx + (size_t)i * 128 + s] = a.h0 ? a.h0[u.sidx + (size_t)i * 128 + s] : 0.f;
+    }
+    tc_fence_before();
+    named_sync(BAR_STATE, NSTATE);
+
+    __nv_bfloat16* go = static_cast<__nv_bfloat16*>(a.o);
+    float fin = 0.f;  // becomes NaN once any output is inf or NaN
+    for (int c = 0; c < nchunks && alive; ++c) {
+      const int lenc = min(C, u.len - c * C);
+      {  // O starts from zero (the previous chunk's has been read out)
+        const uint32_t z[16] = {0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll
+        for (int i0 = 0; i0 < 64; i0 += 16) tmem_st32<16>(tmem + lb + T_O + i0, z);
+        tmem_st_wait();
+        tc_fence_before();
+      }
+      {  // prep operands of chunk c in shared memory, and its v tile
+        bool ok = mbar_wait(bars + B_READY, (uint32_t)(c & 1));
+        if (ok) ok = mbar_wait(bars + B_V, (uint32_t)(c & 1));
+        if (!named_and(BAR_STATE, NSTATE, ok)) { alive = false; break; }
+        tc_fence_after();
+      }
+      if (lead) {
+        // U~^T = V^T TB^T, then [U^T | O^T] += H^T [-W ; q*gamma]^T
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          umma_ss(tmem + T_U, mnmajor_desc(sb + S_V, 64, k), kmajor_desc(sb + S_TB, 64, k),
+                  idesc_f16(128, 64, 1, 1, 0), k > 0);
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          umma_ts(tmem + T_U, tmem + T_HA + 8 * k, kmajor_desc(sb + S_WQ, 128, k),
+                  idesc_f16(128, 128, 0, 0, 0), 1);
+        umma_commit(bars + B_S1);
+      }
+      {
+        const bool ok = mbar_wait(bars + B_S1, (uint32_t)(c & 1));
+        if (!named_and(BAR_STATE, NSTATE, ok)) { alive = false; break; }
+        tc_fence_after();
+      }
+      if (lead && c + 1 < nchunks) {  // the v tile is free: fetch the next one
+        const int y = (int)(u.row0 + (long)(c + 1) * C);
+        mbar_arrive_expect_tx(bars + B_V, TILE_BYTES);
+        tma_load_2d(sm + S_V, &mv, bars + B_V, 0, y);
+        tma_load_2d(sm + S_V + 8192, &mv, bars + B_V, 64, y);
+      }
+      // U^T -> fp16 A operand in TMEM
+      {
+        uint32_t v[32];
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          tmem_ld32<32>(tmem + lb + T_U + 32 * h2, v);
+          tmem_ld_wait();
+          uint32_t hh[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            hh[e] = pack_half2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
+          tmem_st32<16>(tmem + lb + T_UA + 16 * h2, hh);
+        }
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      named_sync(BAR_STATE, NSTATE);
+      if (lead) {
+        tc_fence_after();
+        // O^T += U^T A^T (A of this chunk's parity), H^T += U^T (k*rho)
+        const uint32_t sa = S_A + (uint32_t)(c & 1) * 8192u;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          umma_ts(tmem + T_O, tmem + T_UA + 8 * k, kmajor_desc(sb + sa, 64, k),
+                  idesc_f16(128, 64, 0, 0, 0), 1);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          umma_ts(tmem + T_H, tmem + T_UA + 8 * k, mnmajor_desc(sb + S_KH, 64, k),
+                  idesc_f16(128, 128, 0, 0, 1), 1);
+        umma_commit(bars + B_S3 + (c & 1));
+      }
+      {
+        const bool ok = mbar_wait(bars + B_S3 + (c & 1), (uint32_t)((c >> 1) & 1));
+        if (!named_and(BAR_STATE, NSTATE, ok)) { alive = false; break; }
+        tc_fence_after();
+      }
+      // outputs o[t][j] = O^T[j][t]
+      {
+        const long rbase = u.row0 + (long)c * C;
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          uint32_t v[32];
+          tmem_ld32<32>(tmem + lb + T_O + 32 * h2, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int t = 32 * h2 + e;
+            const float x = __uint_as_float(v[e]);
+            if (t < lenc) {
+              go[(size_t)(rbase + t) * 128 + s] = __float2bfloat16_rn(x);
+              fin = fmaf(x, 0.f, fin);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      named_sync(BAR_STATE, NSTATE);
+      if (c + 1 < nchunks) {
+        const bool ok = mbar_wait(bars + B_GAM + ((c + 1) & 1), (uint32_t)(((c + 1) >> 1) & 1));
+        if (!named_and(BAR_STATE, NSTATE, ok)) { alive = false; break; }
+        convert_and_scale(c + 1, false);
+        tc_fence_before();
+        named_sync(BAR_STATE, NSTATE);
+      }
+    }
+    if (alive && nchunks > 0 && hT) {
+      for (int i0 = 0; i0 < 128; i0 += 32) {
+        uint32_t v[32];
+        tmem_ld32<32>(tmem + lb + T_H + i0, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const float x = __uint_as_float(v[e]);
+          hT[u.sidx + (size_t)(i0 + e) * 128 + s] = x;
+          fin = fmaf(x, 0.f, fin);
+        }
+      }
+    }
+    ovf = !(fin == 0.f);
+    if (!alive) *reinterpret_cast<volatile int*>(s_abort) = 1;
+  } else if (tid < INV_TID0 + NINV) {
+    // ================================================================ INVERSE
+    // Chunk c once the prep warps have its M blocks: D and the diagonal
+    // blocks of TB (warps 0-1), the block columns of TB (warps 0-2), then
+    // -W, all while the prep warps work on chunk c+1.
+    const int pi = tid - INV_TID0;
+    const int iw = pi >> 5;
+    bool ok = true;
+    for (int c = 0; c < nchunks && ok; ++c) {
+      const int slot = c & 1;
+      const float* beta_c = reinterpret_cast<const float*>(sm + S_BETA) + 64 * (c & 3);
+      ok = mbar_wait(bars + B_MREADY + slot, (uint32_t)((c >> 1) & 1));
+      // TB and -W of chunk c-1 have been read by its state MMAs
+      if (ok && c > 0) ok = mbar_wait(bars + B_S1, (uint32_t)((c - 1) & 1));
+      if (!named_and(BAR_INV, NINV, ok)) { ok = false; break; }
+      if (pi < 64) invert_diag_blocks(sm, slot, pi, beta_c);
+      named_sync(BAR_INV, NINV);
+      if (iw == 0) inverse_column<0>(sm, sb, slot, lane, beta_c);
+      else if (iw == 1) inverse_column<1>(sm, sb, slot, lane, beta_c);
+      else inverse_column<2>(sm, sb, slot, lane, beta_c);
+      named_sync(BAR_INV, NINV);      // TB complete; M blocks of this parity free
+      if (lane == 0) mbar_arrive(bars + B_MFREE + slot);
+      minus_w(sm, sb, iw, lane);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars + B_KGFREE);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars + B_READY);
+    }
+    if (!ok) *reinterpret_cast<volatile int*>(s_abort) = 1;
+  } else {
+    // ================================================================== ISSUE
+    const bool leader = lane == 0;
+    auto issue_qka = [&](int cc) {
+      const int y = (int)(u.row0 + (long)cc * C);
+      mbar_arrive_expect_tx(bars + B_QKA, 3 * TILE_BYTES);
+      tma_load_2d(sm + S_TQ, &mq, bars + B_QKA, 0, y);
+      tma_load_2d(sm + S_TK, &mk, bars + B_QKA, 0, y);
+      tma_load_2d(sm + S_TA, &ma, bars + B_QKA, 0, y);
+      tma_load_2d(sm + S_TQ + 8192, &mq, bars + B_QKA, 64, y);
+      tma_load_2d(sm + S_TK + 8192, &mk, bars + B_QKA, 64, y);
+      tma_load_2d(sm + S_TA + 8192, &ma, bars + B_QKA, 64, y);
+    };
+    auto prefetch_l2 = [&](int cc) {
+      const int y = (int)(u.row0 + (long)cc * C);
+#pragma unroll
+      for (int x0 = 0; x0 < 128; x0 += 64) {
+        tma_prefetch_2d_l2(&mq, x0, y);
+        tma_prefetch_2d_l2(&mk, x0, y);
+        tma_prefetch_2d_l2(&ma, x0, y);
+        tma_prefetch_2d_l2(&mv, x0, y);
+      }
+    };
+    // Gram round: D (128 x 64) = X (128 rows) Y^T (64 rows), K = 128
+    const uint32_t id64 = idesc_f16(128, 64, 0, 0, 0);
+    auto gram = [&](uint32_t d_col, uint32_t xbuf, uint32_t ybuf) {
+      const uint64_t d_gx = kmajor_desc(sb + xbuf, 128, 0), d_gy = kmajor_desc(sb + ybuf, 64, 0);
+#pragma unroll
+      for (int k = 0; k < 8; ++k)  // K steps: 32 bytes in a panel, panels R*128 apart
+        umma_ss(tmem + d_col, d_gx + (uint64_t)((k >> 2) * 1024 + (k & 3) * 2),
+                d_gy + (uint64_t)((k >> 2) * 512 + (k & 3) * 2), id64, k > 0);
+    };
+    // beta of chunk cc, two tokens per lane: fetched a chunk ahead into
+    // registers, stored into its parity slot once that is free
+    // (the loads are volatile asm, so that the compiler issues them here and
+    // the warp waits for them only at the store a chunk later)
+    const unsigned short* gbeta = static_cast<const unsigned short*>(a.beta);
+    unsigned short bh0 = 0, bh1 = 0;
+    int blen = 0;
+    auto fetch_beta = [&](int cc) {
+      blen = min(C, u.len - cc * C);   // >= 1 for every chunk
+      const unsigned short* src = gbeta + u.row0 + (long)cc * C;
+      asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(bh0) : "l"(src + min(lane, blen - 1)));
+      asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(bh1) : "l"(src + min(lane + 32, blen - 1)));
+    };
+    auto store_beta = [&](int cc) {
+      float* dst = reinterpret_cast<float*>(sm + S_BETA) + 64 * (cc & 3);
+      dst[lane] = lane < blen ? __uint_as_float((uint32_t)bh0 << 16) : 0.f;
+      dst[lane + 32] = lane + 32 < blen ? __uint_as_float((uint32_t)bh1 << 16) : 0.f;
+      __syncwarp();
+      if (leader) mbar_arrive(bars + B_BETA + (cc & 3));
+    };
+    bool ok = true;
+    if (nchunks > 0) {
+      if (leader) {
+        issue_qka(0);
+        mbar_arrive_expect_tx(bars + B_V, TILE_BYTES);
+        tma_load_2d(sm + S_V, &mv, bars + B_V, 0, (int)u.row0);
+        tma_load_2d(sm + S_V + 8192, &mv, bars + B_V, 64, (int)u.row0);
+        if (nchunks > 1) prefetch_l2(1);
+      }
+      fetch_beta(0);
+      store_beta(0);
+      if (nchunks > 1) fetch_beta(1);
+    }
+    for (int c = 0; c < nchunks && ok; ++c) {
+      // round A of chunk c (its operands imply that chunk c-1's prep is done,
+      // and the inverse warps are at most one chunk behind, so beta slot
+      // (c+1) & 3 is free)
+      if (leader) ok = mbar_wait(bars + B_OPS_A, (uint32_t)(c & 1));
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      if (c + 1 < nchunks) {
+        store_beta(c + 1);
+        if (c + 2 < nchunks) fetch_beta(c + 2);
+      }
+      if (leader) {
+        tc_fence_after();
+        gram(T_GA, S_RA_X, S_RA_Y);
+        umma_commit(bars + B_DONE_A);
+        // round C
+        ok = mbar_wait(bars + B_OPS_C, (uint32_t)(c & 1));
+        if (ok) {
+          tc_fence_after();
+          gram(T_GC, S_RC_X, S_RC_Y);
+          umma_commit(bars + B_DONE_C);
+        }
+        // the next tiles, once round C has read the tile region
+        if (ok && c + 1 < nchunks) {
+          ok = mbar_wait(bars + B_DONE_C, (uint32_t)(c & 1));
+          if (ok) {
+            issue_qka(c + 1);
+            if (c + 2 < nchunks) prefetch_l2(c + 2);
+          }
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+    }
+    if (!ok) *reinterpret_cast<volatile int*>(s_abort) = 1;
+  }
+
+  // ---------------------------------------------------------------- teardown
+  tc_fence_before();
+  const int any_ovf = __syncthreads_or(ovf ? 1 : 0);
+  if (tid == 0) {
+    if (any_ovf) set_status(a.status, CKDA_ERR_RANGE);
+    if (*reinterpret_cast<volatile int*>(s_abort)) {
+      set_status(a.status, CKDA_ERR_TIMEOUT);
+      // let any MMA or copy still in flight land before the memory is released
+      for (int i = B_DONE_A; i <= B_S3 + 1; ++i) mbar_wait(bars + i, 0, 1u << 12, 1000u);
+      mbar_wait(bars + B_V, 0, 1u << 12, 1000u);
+      mbar_wait(bars + B_QKA, 0, 1u << 12, 1000u);
+    }
+  }
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tmem, TMEM_COLS);
+}
+
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t width) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t gdim[2] = {width, rows};
+  cuuint64_t gstride[1] = {width * 2};
+  cuuint32_t box[2] = {64, 64};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gdim, gstride, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t s) {
+  const int units = a.num_units_seq * a.H;
+  if (units == 0) return cudaSuccess;
+  const uint64_t rows = (uint64_t)a.B * a.H * a.T;
+  CUtensorMap mq, mk, ma, mv;
+  if (rows == 0) {
+    mq = mk = ma = mv = CUtensorMap{};  // every sequence is empty: no tile is ever loaded
+  } else if (!make_map(&mq, a.q, rows, 128) || !make_map(&mk, a.k, rows, 128) ||
+             !make_map(&ma, a.alpha, rows, 128) || !make_map(&mv, a.v, rows, 128)) {
+    return cudaErrorInvalidValue;
+  }
+  cudaError_t err =
+      cudaFuncSetAttribute(fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_ALLOC);
+  if (err != cudaSuccess) return err;
+  fwd_kernel<<<(unsigned)units, NT, SMEM_ALLOC, s>>>(a, mq, mk, ma, mv);
+  return cudaGetLastError();
+}
+
+}  // namespace ckda

@@ -3,6 +3,7 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <cudaTypedefs.h>
 #include "../../include/ckda.h"
 
 namespace ckda {
@@ -54,6 +55,10 @@ struct FwdArgs {
 inline bool fwd_tensor_path(ckda_dtype io, int dk, int dv) {
   return io == CKDA_BF16 && dv == 128 && (dk == 128 || dk == 64);
 }
+// The driver's cuTensorMapEncodeTiled, looked up once (null if unavailable).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
+// Chunkwise tcgen05 forward for dk = dv = 128 (chunk 64), dense or packed.
+cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t s);
 // Token-serial CUDA-core forward (any dk, dv <= 128).
 cudaError_t launch_fwd_recurrent(const FwdArgs& a, cudaStream_t s);
 // Chunkwise tcgen05 forward (fwd_tensor_path shapes, chunk 64); with

@@ -169,6 +169,13 @@ template <int N>
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[N]);
 
 template <>
+__device__ __forceinline__ void tmem_ld32<8>(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                 "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+}
+template <>
 __device__ __forceinline__ void tmem_ld32<16>(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
@@ -291,6 +298,41 @@ __device__ __forceinline__ bool wait_counter(const int* counter, int target, con
     __nanosleep(32);
   }
   return false;
+}
+
+// ------------------------------------------- warp-level matrix fragments
+// mma.sync m16n8k16, fp16 operands, fp32 accumulator (row-major A, "col" B).
+// Fragment layouts, with g = lane / 4 and c = lane % 4:
+//   A (16 x 16): a0 = A[g][2c..2c+1], a1 = A[g+8][2c..], a2 = A[g][2c+8..], a3 = A[g+8][2c+8..]
+//   B (16 x 8, rows = K): b0 = B[2c..2c+1][g], b1 = B[2c+8..2c+9][g]
+//   C (16 x 8): c0,c1 = C[g][2c..2c+1], c2,c3 = C[g+8][2c..2c+1]
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// Four 8 x 8 b16 matrices from shared memory; lane l gives the address of row
+// l % 8 of matrix l / 8.  Without .trans lane l receives row l / 4, elements
+// 2(l % 4), +1 of each; with .trans the same elements of the transpose.
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+// Transpose of an 8 x 8 b16 matrix held one row pair per lane (lane l: row
+// l / 4, elements 2(l % 4), +1).
+__device__ __forceinline__ uint32_t movm_t(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
 }
 
 // ------------------------------------------------------ small conversions
