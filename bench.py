@@ -3,22 +3,26 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-One step is one ckda_fwd call over the KDA-range workload (B=8, H=16, T=2048,
-dk=dv=128, bf16 I/O, fp32 state, alpha = sigmoid(N(2,1)), beta = sigmoid(N(0,1)),
-h0 = 0), inputs resident in HBM.  The inputs (269 MB) exceed the 129 MB L2,
-so no flush is done between steps.  Prints ONE JSON line on rank 0 with:
-  value     whole-job token-heads/s (B*T*H per step, all ranks) from CUDA events
-  roofline  the forward kernel's algorithmic bytes / its mean event-timed
-            duration against the measured HBM copy bandwidth
+One step is one ckda_fwd call over the full CKDA-range workload (B=4, H=32,
+T=8192, dk=dv=128, bf16 I/O, fp32 state, alpha = tanh(N(0,2)) with exact -1
+and 0 entries, beta = 2 sigmoid(N(0,1)), h0 ~ N(0, 0.1)), inputs resident in
+HBM.  The inputs (1.07 GB) exceed the 129 MB L2, so no flush is done between
+steps.  Prints ONE JSON line on rank 0 with:
+  value     whole-job token-heads/s (B*T*H per step, all ranks): two CUDA
+            events around the K back-to-back steps
+  roofline  the forward's algorithmic bytes / its mean per-call device time
+            (the same two events; a call is the status-word clear and the
+            kernel) against the measured HBM copy bandwidth
   e2e       the same metric with host (pinned) buffers, H2D and D2H in the
             timed region
   cpu_baseline  the fp64 CPU oracle timed on a bounded sample (rank 0, N=1)
-  decode    the decode workload (B=256, H=32, 1000 chained steps): HBM GB/s
+  decode    the decode workload (B=256, H=32, 1000 chained steps): HBM GB/s;
+            a summary (GB/s, roofline fraction) is repeated in config.decode
   decode_raw  the same through the step with the input preparation fused in
   prep      the fused input preparation (ckda_prep) on raw inputs of the
             KDA-range shape: HBM GB/s
   bwd       the backward (ckda_bwd) on the KDA-range workload: token-heads/s
-  workloads the full-CKDA, packed and dk = 64 KDA-range workloads (N=1):
+  workloads the KDA-range, packed and dk = 64 KDA-range workloads (N=1):
             token-heads/s, roofline
   clocks    SM clocks and throttle reasons sampled during the timed region
 --impl reference runs the fp64 oracle as the reference arm on the host cores.
@@ -67,6 +71,7 @@ def hbm_peak():
 # source files each profiled kernel is built from; a committed DRAM-traffic
 # figure only counts while these files are unchanged
 KERNEL_SOURCES = {
+    "fwd": ["ckda_fwd.cu", "sm103.cuh", "ckda_internal.cuh"],
     "fwd_chunk": ["ckda_chunk.cu", "sm103.cuh", "ckda_internal.cuh"],
     "decode128": ["ckda_decode.cu", "ckda_internal.cuh"],
     "prep": ["ckda_prep.cu", "ckda_internal.cuh"],
@@ -81,6 +86,11 @@ def kernel_sources_sha(kernel):
         h.update(fn.encode())
         h.update(open(os.path.join(csrc, fn), "rb").read())
     return h.hexdigest()
+
+
+def fwd_kernel(dk):
+    """The forward kernel a head size runs on (its DRAM-traffic record key)."""
+    return "fwd"
 
 
 def traffic_for(kernel, workload):
@@ -187,29 +197,27 @@ def max_over_ranks(x, ws):
 # ----------------------------------------------------------------- our arm
 
 def time_steps(step_fn, steps, warmup, ws, stream):
-    """Runs warmup + timed steps; returns (total seconds max over ranks,
-    per-step event durations in ms)."""
+    """Runs warmup + timed steps back to back; returns (total seconds, max
+    over ranks; the mean per-step device time in ms).  Two CUDA events on the
+    launching stream bracket the K steps, with a barrier and a synchronize on
+    both sides."""
     import torch
     for _ in range(warmup):
         step_fn()
     torch.cuda.synchronize()
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(steps)]
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     barrier(ws)
     torch.cuda.synchronize()
     t0.record(stream)
-    for a, b in evs:
-        a.record(stream)
+    for _ in range(steps):
         step_fn()
-        b.record(stream)
     t1.record(stream)
     torch.cuda.synchronize()
     barrier(ws)
-    total = t0.elapsed_time(t1) / 1e3
-    per = [a.elapsed_time(b) for a, b in evs]
-    return max_over_ranks(total, ws), per
+    local = t0.elapsed_time(t1) / 1e3
+    total = max_over_ranks(local, ws)
+    return total, [local / steps * 1e3]
 
 
 def fwd_case(ck, x, steps, warmup, ws, stream, name):
@@ -311,16 +319,18 @@ def e2e_fwd(ck, x, steps, ws, stream):
     B, H, T, dk = x.q.shape
     dv = x.v.shape[-1]
     hq, hk, hv, ha, hb = (t.pin_memory() for t in (x.q, x.k, x.v, x.alpha, x.beta))
+    hh0 = None if x.h0 is None else x.h0.pin_memory()
     ho = torch.empty((B, H, T, dv), dtype=x.q.dtype).pin_memory()
     hh = torch.empty((B, H, dk, dv), dtype=torch.float32).pin_memory()
     scratch = torch.empty(ck.host_scratch_bytes(B, H, T, dk, dv, x.q.dtype), dtype=torch.uint8,
                           device="cuda")
 
     def step():
-        ck.fwd_host(hq, hk, hv, ha, hb, None, o=ho, hT=hh, scratch=scratch, stream=stream)
+        ck.fwd_host(hq, hk, hv, ha, hb, hh0, o=ho, hT=hh, scratch=scratch, stream=stream)
 
-    total, _ = time_steps(step, steps, 2, ws, stream)
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, ha, hb))
+    total, _ = time_steps(step, steps, 3, ws, stream)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, ha, hb)) + \
+        (0 if hh0 is None else hh0.numel() * 4)
     d2h = ho.numel() * ho.element_size() + hh.numel() * 4
     return {"value": round(ws * B * H * T * steps / total, 1), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps}
@@ -501,7 +511,7 @@ def run_ours(args):
                                 "gate products, T and state",
                    "l2": "inputs larger than L2 (no flush)",
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
-        "roofline": roofline(r["bytes"], r["per"], "fwd_chunk", name),
+        "roofline": roofline(r["bytes"], r["per"], fwd_kernel(dk), name),
         "gpu_launches": r["launches"] * args.steps,
         "clocks": clk,
     }
@@ -509,23 +519,31 @@ def run_ours(args):
     extras = [] if args.no_extras else [e for e in args.extras.split(",") if e and e != "none"]
     if ws == 1 and "decode" in extras:
         out["decode"] = decode_case(ck, args.decode_steps, 10, ws, stream)
+        dr = out["decode"]["roofline"]
+        # the metric's second half, kept where the one-line record is read
+        out["config"]["decode"] = {"workload": "ckda_decode (B=256, H=32, d=128, 1000 chained "
+                                               "steps)", "GB/s": out["decode"]["value"],
+                                   "roofline_frac": dr["frac"], "ms_per_step":
+                                   out["decode"]["ms_per_step"]}
     if ws == 1 and "decode_raw" in extras:
         out["decode_raw"] = decode_case(ck, args.decode_steps, 10, ws, stream, raw=True)
     if ws == 1 and "prep" in extras:
         out["prep"] = prep_case(ck, x, 200, 10, ws, stream)
     if ws == 1 and "bwd" in extras:
         out["bwd"] = bwd_case(ck, x, 10, 3, ws, stream, units=args.bwd_units)
-    if ws == 1 and any(e in extras for e in ("ckda_full", "ckda_varlen", "kda_range_dk64")):
+    if ws == 1 and any(e in extras for e in ("kda_range", "ckda_full", "ckda_varlen",
+                                             "kda_range_dk64")):
         wl = {}
-        for nm, steps in (("ckda_full", 20), ("ckda_varlen", 10), ("kda_range_dk64", 200)):
-            if nm not in extras:
+        for nm, steps in (("kda_range", 200), ("ckda_full", 20), ("ckda_varlen", 10),
+                          ("kda_range_dk64", 200)):
+            if nm not in extras or nm == name:
                 continue
             xx = synth.make_workload(nm)
             rr = fwd_case(ck, xx, steps, 3, ws, stream, nm)
             wl[nm] = {"value": round(rr["th"] * steps / rr["total"], 1), "unit": UNIT,
                       "ms_per_step": round(rr["total"] / steps * 1e3, 4), "steps": steps,
                       "token_heads": rr["th"],
-                      "roofline": roofline(rr["bytes"], rr["per"], "fwd_chunk", nm)}
+                      "roofline": roofline(rr["bytes"], rr["per"], fwd_kernel(xx.q.shape[-1]), nm)}
             del xx, rr
         out["workloads"] = wl
     if ws == 1 and "fig5_sweep" in extras:
@@ -597,17 +615,17 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="kda_range",
+    ap.add_argument("--workload", default="ckda_full",
                     choices=["kda_range", "ckda_full", "ckda_varlen"])
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--decode-steps", type=int, default=1000)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--extras",
-                    default="decode,decode_raw,prep,bwd,ckda_full,ckda_varlen,kda_range_dk64,"
+                    default="decode,decode_raw,prep,bwd,kda_range,ckda_varlen,kda_range_dk64,"
                             "fig5_sweep",
                     help="comma list of extra measurements: decode, decode_raw, prep, bwd, "
-                         "ckda_full, ckda_varlen, kda_range_dk64, fig5_sweep")
+                         "kda_range, ckda_full, ckda_varlen, kda_range_dk64, fig5_sweep")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--bwd-units", type=int, default=0,
                     help="run the bwd extra on the first N (batch, head) units only")

@@ -138,8 +138,7 @@ ckda_status ckda_fwd(const void* q, const void* k, const void* v, const void* al
     if (err != cudaSuccess) return CKDA_ERR_CUDA;
     a.order = order;
   }
-  err = tensor_path ? (dk == 128 ? launch_fwd(a, s) : launch_fwd_chunk(a, s))
-                    : launch_fwd_recurrent(a, s);
+  err = tensor_path ? launch_fwd(a, s) : launch_fwd_recurrent(a, s);
   return err == cudaSuccess ? CKDA_OK : CKDA_ERR_CUDA;
 }
 

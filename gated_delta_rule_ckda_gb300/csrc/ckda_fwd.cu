@@ -1,5 +1,7 @@
 // ckda_fwd.cu -- chunkwise CKDA forward on tcgen05 tensor cores (sm_103a),
-// dk = dv = 128, bf16 I/O, fp32 state.
+// dv = 128 and dk = 128 or 64, bf16 I/O, fp32 state.  A 64-wide key runs as
+// 128 channels whose last 64 have zero keys and queries and unit gates: their
+// state rows stay zero and add nothing.
 //
 // One CTA owns one (sequence, head) and walks its tokens in chunks of C = 64
 // with the fp32 state H^T (dv x dk = 128 x 128) resident in tensor memory.
@@ -153,6 +155,7 @@ struct Unit {
   int len;
   size_t sidx;   // offset of the (sequence, head) in h0 and hT
 };
+template <int DK>
 __device__ __forceinline__ Unit unit_of(const FwdArgs& a) {
   Unit u;
   const int b = blockIdx.x;
@@ -167,7 +170,7 @@ __device__ __forceinline__ Unit unit_of(const FwdArgs& a) {
     u.len = a.T;
     u.row0 = ((long)n * a.H + h) * a.T;
   }
-  u.sidx = ((size_t)n * a.H + h) * 128 * 128;
+  u.sidx = ((size_t)n * a.H + h) * DK * 128;
   return u;
 }
 
@@ -220,17 +223,22 @@ __device__ __forceinline__ float4 bf4(uint2 w) {
   return make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u),
                      __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
 }
+// With pad set (the lanes of channels 64..127 of a 64-wide key) nothing is
+// read: k = q = 0 and alpha = 1.
 template <bool kMask>
 __device__ __forceinline__ void load_block(Blk8& B, const uint8_t* sm, int blk, int lane,
-                                           float scale, int live) {
+                                           float scale, int live, bool pad) {
   B.tot = make_float4(1.f, 1.f, 1.f, 1.f);
   const uint32_t tb = quad_tb<64>(lane);
 #pragma unroll
   for (int r = 0; r < 8; ++r) {
     const uint32_t off = quad_at(tb, (uint32_t)(8 * blk + r));
-    float4 kf = bf4(*reinterpret_cast<const uint2*>(sm + S_TK + off));
-    float4 qf = bf4(*reinterpret_cast<const uint2*>(sm + S_TQ + off));
-    float4 af = bf4(*reinterpret_cast<const uint2*>(sm + S_TA + off));
+    float4 kf = make_float4(0.f, 0.f, 0.f, 0.f), qf = kf, af = make_float4(1.f, 1.f, 1.f, 1.f);
+    if (!pad) {
+      kf = bf4(*reinterpret_cast<const uint2*>(sm + S_TK + off));
+      qf = bf4(*reinterpret_cast<const uint2*>(sm + S_TQ + off));
+      af = bf4(*reinterpret_cast<const uint2*>(sm + S_TA + off));
+    }
     qf.x *= scale; qf.y *= scale; qf.z *= scale; qf.w *= scale;
     if (kMask && r >= live) {
       kf = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -710,6 +718,7 @@ __device__ __forceinline__ void warp_publish(uint64_t* bar, int lane) {
   if (lane == 0) mbar_arrive(bar);
 }
 
+template <int DK>
 __global__ void __launch_bounds__(NT, 1)
     fwd_kernel(const __grid_constant__ FwdArgs a, const __grid_constant__ CUtensorMap mq,
                const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap ma,
@@ -722,7 +731,8 @@ __global__ void __launch_bounds__(NT, 1)
   int* s_abort = reinterpret_cast<int*>(sm + S_BAR + 192);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + S_BAR + 200);
 
-  const Unit u = unit_of(a);
+  static_assert(DK == 128 || DK == 64, "key width");
+  const Unit u = unit_of<DK>(a);
   const int nchunks = (u.len + C - 1) / C;
 
   if (tid == 0) {
@@ -771,8 +781,9 @@ __global__ void __launch_bounds__(NT, 1)
       // ---- 1. q, k, alpha of chunk c
       ok = ok && mbar_wait(bars + B_QKA, (uint32_t)(c & 1));
       Blk8 B;
-      if (lenc == C) load_block<false>(B, sm, blk, lane, a.scale, C);
-      else load_block<true>(B, sm, blk, lane, a.scale, lenc - 8 * blk);
+      const bool pad = DK == 64 && lane >= 16;
+      if (lenc == C) load_block<false>(B, sm, blk, lane, a.scale, C, pad);
+      else load_block<true>(B, sm, blk, lane, a.scale, lenc - 8 * blk, pad);
       // ---- 2. round A (levels 8, 4); its buffer was last read by round A of
       // chunk c-1, whose completion this role waited for
       write_round_a(sm, B, blk, lane);
@@ -890,7 +901,7 @@ __global__ void __launch_bounds__(NT, 1)
         if (from_h0) {
 #pragma unroll
           for (int e = 0; e < 16; ++e)
-            f[e] = a.h0 ? a.h0[u.sidx + (size_t)(i0 + e) * 128 + s] : 0.f;
+            f[e] = (a.h0 && i0 + e < DK) ? a.h0[u.sidx + (size_t)(i0 + e) * 128 + s] : 0.f;
         } else {
           uint32_t v[16];
           tmem_ld32<16>(tmem + lb + T_H + i0, v);
@@ -920,7 +931,7 @@ __global__ void __launch_bounds__(NT, 1)
       alive = named_and(BAR_STATE, NSTATE, ok);
       if (alive) convert_and_scale(0, true);
     } else if (hT) {
-      for (int i = 0; i < 128; ++i)
+      for (int i = 0; i < DK; ++i)
         hT[u.sidx + (size_t)i * 128 + s] = a.h0 ? a.h0[u.sidx + (size_t)i * 128 + s] : 0.f;
     }
     tc_fence_before();
@@ -1032,7 +1043,7 @@ __global__ void __launch_bounds__(NT, 1)
       }
     }
     if (alive && nchunks > 0 && hT) {
-      for (int i0 = 0; i0 < 128; i0 += 32) {
+      for (int i0 = 0; i0 < DK; i0 += 32) {
         uint32_t v[32];
         tmem_ld32<32>(tmem + lb + T_H + i0, v);
         tmem_ld_wait();
@@ -1079,23 +1090,28 @@ __global__ void __launch_bounds__(NT, 1)
   } else {
     // ================================================================== ISSUE
     const bool leader = lane == 0;
+    // (a 64-wide key loads only the first 64-channel panel of q, k, alpha)
     auto issue_qka = [&](int cc) {
       const int y = (int)(u.row0 + (long)cc * C);
-      mbar_arrive_expect_tx(bars + B_QKA, 3 * TILE_BYTES);
+      mbar_arrive_expect_tx(bars + B_QKA, 3 * TILE_BYTES * DK / 128);
       tma_load_2d(sm + S_TQ, &mq, bars + B_QKA, 0, y);
       tma_load_2d(sm + S_TK, &mk, bars + B_QKA, 0, y);
       tma_load_2d(sm + S_TA, &ma, bars + B_QKA, 0, y);
-      tma_load_2d(sm + S_TQ + 8192, &mq, bars + B_QKA, 64, y);
-      tma_load_2d(sm + S_TK + 8192, &mk, bars + B_QKA, 64, y);
-      tma_load_2d(sm + S_TA + 8192, &ma, bars + B_QKA, 64, y);
+      if (DK == 128) {
+        tma_load_2d(sm + S_TQ + 8192, &mq, bars + B_QKA, 64, y);
+        tma_load_2d(sm + S_TK + 8192, &mk, bars + B_QKA, 64, y);
+        tma_load_2d(sm + S_TA + 8192, &ma, bars + B_QKA, 64, y);
+      }
     };
     auto prefetch_l2 = [&](int cc) {
       const int y = (int)(u.row0 + (long)cc * C);
 #pragma unroll
       for (int x0 = 0; x0 < 128; x0 += 64) {
-        tma_prefetch_2d_l2(&mq, x0, y);
-        tma_prefetch_2d_l2(&mk, x0, y);
-        tma_prefetch_2d_l2(&ma, x0, y);
+        if (x0 < DK) {
+          tma_prefetch_2d_l2(&mq, x0, y);
+          tma_prefetch_2d_l2(&mk, x0, y);
+          tma_prefetch_2d_l2(&ma, x0, y);
+        }
         tma_prefetch_2d_l2(&mv, x0, y);
       }
     };
@@ -1216,14 +1232,15 @@ cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t s) {
   CUtensorMap mq, mk, ma, mv;
   if (rows == 0) {
     mq = mk = ma = mv = CUtensorMap{};  // every sequence is empty: no tile is ever loaded
-  } else if (!make_map(&mq, a.q, rows, 128) || !make_map(&mk, a.k, rows, 128) ||
-             !make_map(&ma, a.alpha, rows, 128) || !make_map(&mv, a.v, rows, 128)) {
+  } else if (!make_map(&mq, a.q, rows, a.dk) || !make_map(&mk, a.k, rows, a.dk) ||
+             !make_map(&ma, a.alpha, rows, a.dk) || !make_map(&mv, a.v, rows, 128)) {
     return cudaErrorInvalidValue;
   }
+  auto kern = a.dk == 64 ? fwd_kernel<64> : fwd_kernel<128>;
   cudaError_t err =
-      cudaFuncSetAttribute(fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_ALLOC);
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_ALLOC);
   if (err != cudaSuccess) return err;
-  fwd_kernel<<<(unsigned)units, NT, SMEM_ALLOC, s>>>(a, mq, mk, ma, mv);
+  kern<<<(unsigned)units, NT, SMEM_ALLOC, s>>>(a, mq, mk, ma, mv);
   return cudaGetLastError();
 }
 

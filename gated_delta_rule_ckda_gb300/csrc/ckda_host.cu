@@ -172,8 +172,7 @@ extern "C" ckda_status ckda_fwd_host(const void* q, const void* k, const void* v
     a.num_units_seq = B;
     a.B = B; a.H = H; a.T = len; a.dk = dk; a.dv = dv;
     a.scale = scale; a.io = io_dtype;
-    CK(tensor_path ? (dk == 128 ? launch_fwd(a, cs) : launch_fwd_chunk(a, cs))
-                   : launch_fwd_recurrent(a, cs));
+    CK(tensor_path ? launch_fwd(a, cs) : launch_fwd_recurrent(a, cs));
     CK(cudaEventRecord(P->comp_done[b], cs));
     // out: o of this slice into its rows of the host o
     CK(cudaStreamWaitEvent(P->out, P->comp_done[b], 0));

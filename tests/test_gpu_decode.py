@@ -56,6 +56,28 @@ def test_decode_workload_full_size(ck):
     assert max_rel(Sg.cpu(), Sref) <= 1e-5
 
 
+def test_decode_chain_1000_steps(ck):
+    """The decode workload's 1000 chained steps on the resident state, at a
+    reduced B x H (B = 8, H = 4, d = 128) and the workload's distributions:
+    every step's o and the final state against the fp64 oracle, so that fp32
+    drift over the whole chain is pinned."""
+    w = synth.WORKLOADS["ckda_decode"]
+    B, H, d, steps = 8, 4, w["d"], 1000
+    S = synth.make_decode_state(B, H, d, seed=w["seed"])
+    Sg = S.cuda()
+    Sref = S.double().numpy()
+    worst = 0.0
+    for step in range(steps):
+        q, k, v, a, b = synth.make_decode_step(B, H, d, seed=w["seed"], step=step)
+        o = ck.decode_step(q.cuda(), k.cuda(), v.cuda(), a.cuda(), b.cuda(), Sg)
+        o_ref, Sref = oracle.decode_step(q, k, v, a, b, Sref)
+        worst = max(worst, excess_bf16(o.cpu(), o_ref))
+    print(f"[decode 1000 steps] worst o excess {worst:.3e}, final state "
+          f"{max_rel(Sg.cpu(), Sref):.3e}")
+    assert worst <= 2e-2
+    assert max_rel(Sg.cpu(), Sref) <= 1e-4
+
+
 def test_decode_chain_equals_fwd(ck):
     """T decode steps equal one forward over the same T tokens (state and
     outputs), with the token-serial fp32 path on both sides."""

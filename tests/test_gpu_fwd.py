@@ -78,20 +78,25 @@ def test_ckda_full_workload_full(ck):
     check(o, hT, o_ref, h_ref, bf16=True, name="ckda_full")
 
 
-def test_ckda_varlen_workload_sampled(ck):
-    """Full packed workload on the GPU; oracle on 8 sequences (longest, shortest
-    and 6 more), compared element by element."""
+def test_ckda_varlen_workload_full(ck):
+    """The full packed workload (64 sequences, 8.26 M token-heads) on the GPU;
+    every sequence's o and final state against the oracle, one sequence per
+    oracle call (each sequence judged against its own rms, which is stricter
+    than one rms over the whole packed tensor)."""
     x = synth.make_workload("ckda_varlen")
     o, hT = run_gpu(ck, x)
     cu = x.cu_seqlens.numpy()
-    lens = np.diff(cu)
-    order = np.argsort(-lens, kind="stable")
-    pick = sorted(set([int(order[0]), int(order[-1])] + [int(i) for i in order[1:-1:9]][:6]))
-    for s in pick:
+    worst_o = worst_h = worst_rms = 0.0
+    for s in range(len(cu) - 1):
         a, b = int(cu[s]), int(cu[s + 1])
         sl = lambda t: t[:, :, a:b]
         o_ref, h_ref = oracle.fwd(sl(x.q), sl(x.k), sl(x.v), sl(x.alpha), sl(x.beta))
-        check(o[:, :, a:b], hT[s:s + 1], o_ref, h_ref, bf16=True, name=f"varlen seq {s} L={b - a}")
+        worst_o = max(worst_o, excess_bf16(o[:, :, a:b], o_ref))
+        worst_rms = max(worst_rms, rms_rel(o[:, :, a:b], o_ref))
+        worst_h = max(worst_h, max_rel(hT[s:s + 1], h_ref))
+    print(f"[ckda_varlen, 64 sequences] worst o excess {worst_o:.3e}, rms {worst_rms:.3e}, "
+          f"hT {worst_h:.3e}")
+    assert worst_o <= TOL_BF16 and worst_h <= TOL_BF16 and worst_rms <= 5e-3
 
 
 # --------------------------------------------------- tensor-core path, small
