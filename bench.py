@@ -72,7 +72,6 @@ def hbm_peak():
 # figure only counts while these files are unchanged
 KERNEL_SOURCES = {
     "fwd": ["ckda_fwd.cu", "sm103.cuh", "ckda_internal.cuh"],
-    "fwd_chunk": ["ckda_chunk.cu", "sm103.cuh", "ckda_internal.cuh"],
     "decode128": ["ckda_decode.cu", "ckda_internal.cuh"],
     "prep": ["ckda_prep.cu", "ckda_internal.cuh"],
     "bwd": ["ckda_bwd.cu", "ckda_internal.cuh"],
@@ -273,7 +272,7 @@ def dense_case(ck, d, steps, warmup, ws, stream, name, segments):
     return {"value": round(th * steps / total, 1), "unit": UNIT,
             "ms_per_step": round(total / steps * 1e3, 4), "steps": steps, "token_heads": th,
             "segments": segments, "launches_per_step": launches,
-            "roofline": roofline(nbytes, per, "fwd_chunk", name)}
+            "roofline": roofline(nbytes, per, "fwd", name)}
 
 
 def fig5_sweep(ck, steps, ws, stream):

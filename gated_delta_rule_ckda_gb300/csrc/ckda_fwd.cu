@@ -49,7 +49,10 @@
 // Grams, A and T's blocks are fp16 (11-bit significand); T Diag(beta) and
 // k * gamma are bf16; all accumulation is fp32.  Gate factors inside a block
 // of 8 tokens are fp16 product chains; block totals, gamma_C and D are fp32.
-// A non-finite o or final state is reported as CKDA_ERR_RANGE.
+// The state and U enter their fp16 operands at a power-of-two scale that
+// follows their magnitude (below), so large or small v and h0 keep fp16's
+// full precision.  A non-finite o or final state is reported as
+// CKDA_ERR_RANGE.
 //
 // Warp roles (512 threads):
 //   warps 0-7   PREP: per chunk, gate products, the Gram operands and their
@@ -70,6 +73,7 @@
 #include "sm103.cuh"
 
 #include <cudaTypedefs.h>
+#include <mutex>
 
 namespace ckda {
 namespace {
@@ -113,6 +117,8 @@ constexpr uint32_t S_BETA = S_SMALL;          // fp32 [4][64]
 constexpr uint32_t S_GAM = S_SMALL + 1024;    // fp32 [2][128] gamma_C
 constexpr uint32_t S_TOT = S_SMALL + 2048;    // float4 [8 blocks][32 quads] alpha block totals
 constexpr uint32_t S_BAR = S_SMALL + 6144;    // mbarriers, abort flag, TMEM base
+constexpr uint32_t S_RED = S_BAR + 256;       // fp32 [4][4] state-role maxima, one per warp
+constexpr int RED_H0 = 0, RED_H = 4, RED_U = 8, RED_UX = 12;
 constexpr uint32_t SMEM_USED = S_SMALL + 6656;
 constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;
 static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
@@ -150,27 +156,129 @@ static_assert(B_COUNT * 8 <= 192, "mbarrier area");
 
 constexpr uint32_t TILE_BYTES = 16384;
 
+// What one CTA runs: its rows, its initial and final state, and (in the
+// sequence split) whether its initial state is [I | 0], its v is zero and its
+// o is stored.
 struct Unit {
   long row0;
   int len;
-  size_t sidx;   // offset of the (sequence, head) in h0 and hT
+  const float* h0;   // [DK][128] initial state, or null: zero (or [I | 0] if ident)
+  float* hT;         // [DK][128] final state, or null: not stored
+  bool ident, zero_v, write_o;
 };
-template <int DK>
+// ---- power-of-two range scaling of the state step ----
+// The state in tensor memory is 2^-sig H for an integer sig shared by the
+// CTA, and a chunk's fp16 operands H and U are taken at that scale, so that
+// they stay inside fp16's normal range whatever the magnitude of v and h0.
+// A power-of-two factor commutes with every rounding (short of fp32 under-
+// or overflow): a scaled chunk rounds exactly as an unscaled one would.
+constexpr int kScaleTop = 14;      // a state bound is kept below 2^14 ...
+constexpr int kScaleBot = -2;      // ... and at or above 2^-3
+constexpr int kUTarget = 8;        // a rescaled U lies below 2^8
+constexpr float kUMin = 0.0625f;   // an fp16 U outside [2^-4, 2^15) is rescaled
+constexpr float kUMax = 32768.f;
+constexpr int kSigMax = 120;
+// e with x < 2^e, for finite x > 0
+__device__ __forceinline__ int exp_above(float x) {
+  return (int)((__float_as_uint(x) >> 23) & 0xffu) - 126;
+}
+__device__ __forceinline__ float pow2i(int n) {
+  n = min(max(n, -126), 127);
+  return __uint_as_float((uint32_t)(n + 127) << 23);
+}
+// The scale for a state whose magnitude at scale 2^-sig is bounded by B:
+// 0 if the unscaled state lies in [2^-3, 2^14), else sig if the current one
+// does, else one that puts the bound just below 2^14.
+__device__ __forceinline__ int state_scale(float B, int sig) {
+  if (!(B <= 3.0e38f)) return sig;   // not finite: the result reports it
+  if (B == 0.f) return 0;
+  const int e = exp_above(B);
+  if (e + sig <= kScaleTop && e + sig >= kScaleBot) return 0;
+  if (e <= kScaleTop && e >= kScaleBot) return sig;
+  return min(max(sig + e - kScaleTop, -kSigMax), kSigMax);
+}
+// The extra shift b for a chunk whose U (at scale 2^-sig) has maximum m:
+// above 2^15 it goes down to below 2^8; below 2^-4 up to below 2^8, as far
+// as the state (bounded by mH) stays below 2^14.
+__device__ __forceinline__ int u_shift(float m, float mH, int sig) {
+  if (!(m > 0.f && m <= 3.0e38f)) return 0;
+  const int e = exp_above(m);
+  int b;
+  if (m >= kUMax) {
+    b = e - kUTarget;
+  } else if (m < kUMin) {
+    b = min(max(e - kUTarget, mH > 0.f ? exp_above(mH) - kScaleTop : -kSigMax), 0);
+  } else {
+    return 0;
+  }
+  return min(max(sig + b, -kSigMax), kSigMax) - sig;
+}
+// Maximum of a non-negative value over the 128 state threads: each warp
+// leaves its maximum in slot[warp], read once a barrier has passed.
+__device__ __forceinline__ float cta4_max(float* slot, float x, int lane, int wq) {
+  const uint32_t m = __reduce_max_sync(0xffffffffu, __float_as_uint(x));
+  if (lane == 0) slot[wq] = __uint_as_float(m);
+  return x;
+}
+__device__ __forceinline__ float cta4_read(const float* slot) {
+  return fmaxf(fmaxf(slot[0], slot[1]), fmaxf(slot[2], slot[3]));
+}
+
+template <int DK, bool SPLIT>
 __device__ __forceinline__ Unit unit_of(const FwdArgs& a) {
   Unit u;
-  const int b = blockIdx.x;
-  const int h = b % a.H;
-  int n = b / a.H;
-  if (a.cu_seqlens) {
-    if (a.order) n = a.order[n];
-    const int t0 = a.cu_seqlens[n];
-    u.len = a.cu_seqlens[n + 1] - t0;
-    u.row0 = (long)h * a.T + t0;
+  constexpr size_t tile = (size_t)DK * 128;
+  u.ident = false;
+  u.zero_v = false;
+  u.write_o = true;
+  if constexpr (SPLIT) {
+    // dense layout; CTA b is (sequence, head) ui, role r of its pass
+    const int S = a.nseg;
+    const int per = split_ctas_per_unit(a.split_pass, S);
+    const int ui = (int)blockIdx.x / per, r = (int)blockIdx.x % per;
+    const size_t slot0 = (size_t)ui * S;
+    int seg;
+    u.h0 = nullptr;
+    u.hT = nullptr;
+    if (a.split_pass == 1) {
+      u.write_o = r == 0;
+      if (r == 0) {             // segment 0 from h0; its final state enters segment 1
+        seg = 0;
+        u.h0 = a.h0 ? a.h0 + (size_t)ui * tile : nullptr;
+        u.hT = a.seg_state + (slot0 + 1) * tile;
+      } else if (r <= S - 2) {  // final state of segment r from zero
+        seg = r;
+        u.hT = a.seg_F + (slot0 + seg) * tile;
+      } else {                  // transition of segment r - (S - 2): from [I | 0], v = 0
+        seg = r - (S - 2);
+        u.ident = true;
+        u.zero_v = true;
+        u.hT = a.seg_P + (slot0 + seg) * tile;
+      }
+    } else {
+      seg = 1 + r;
+      u.h0 = a.seg_state + (slot0 + seg) * tile;
+      u.hT = (seg == S - 1 && a.hT) ? a.hT + (size_t)ui * tile : nullptr;
+    }
+    u.row0 = (long)ui * a.T + (long)seg * a.seg_len;
+    u.len = min(a.seg_len, a.T - seg * a.seg_len);
   } else {
-    u.len = a.T;
-    u.row0 = ((long)n * a.H + h) * a.T;
+    const int b = blockIdx.x;
+    const int h = b % a.H;
+    int n = b / a.H;
+    if (a.cu_seqlens) {
+      if (a.order) n = a.order[n];
+      const int t0 = a.cu_seqlens[n];
+      u.len = a.cu_seqlens[n + 1] - t0;
+      u.row0 = (long)h * a.T + t0;
+    } else {
+      u.len = a.T;
+      u.row0 = ((long)n * a.H + h) * a.T;
+    }
+    const size_t sidx = ((size_t)n * a.H + h) * tile;
+    u.h0 = a.h0 ? a.h0 + sidx : nullptr;
+    u.hT = a.hT ? a.hT + sidx : nullptr;
   }
-  u.sidx = ((size_t)n * a.H + h) * DK * 128;
   return u;
 }
 
@@ -718,7 +826,7 @@ __device__ __forceinline__ void warp_publish(uint64_t* bar, int lane) {
   if (lane == 0) mbar_arrive(bar);
 }
 
-template <int DK>
+template <int DK, bool SPLIT>
 __global__ void __launch_bounds__(NT, 1)
     fwd_kernel(const __grid_constant__ FwdArgs a, const __grid_constant__ CUtensorMap mq,
                const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap ma,
@@ -732,7 +840,8 @@ __global__ void __launch_bounds__(NT, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + S_BAR + 200);
 
   static_assert(DK == 128 || DK == 64, "key width");
-  const Unit u = unit_of<DK>(a);
+  const Unit u = unit_of<DK, SPLIT>(a);
+  const bool zero_v = SPLIT && u.zero_v;   // no v tile is read: U~ = 0
   const int nchunks = (u.len + C - 1) / C;
 
   if (tid == 0) {
@@ -888,20 +997,36 @@ __global__ void __launch_bounds__(NT, 1)
     const int wq = s >> 5;
     const uint32_t lb = (uint32_t)(32 * wq) << 16;
     const bool lead = s == 0;
-    float* hT = a.hT;
+    float* hT = u.hT;
+    // column s of the initial state
+    auto h0_at = [&](int i) -> float {
+      if (i >= DK) return 0.f;
+      if (u.h0) return u.h0[(size_t)i * 128 + s];
+      return (SPLIT && u.ident && i == s) ? 1.f : 0.f;
+    };
     bool alive = true;
     const float* gc_all = reinterpret_cast<const float*>(sm + S_GAM);
-    // H^T as the fp16 A operand (TMEM) and, in TMEM, H^T Diag(gamma_C) of
-    // the chunk about to start (column i times gC[i])
-    auto convert_and_scale = [&](int c_next, bool from_h0) {
+    float* red = reinterpret_cast<float*>(sm + S_RED);
+    // Range scaling (every value below is the same in all state threads):
+    // tensor memory holds 2^-sig H, and the fp16 operands of a chunk are
+    // taken at that scale.  mH bounds |2^-sig H| at the last conversion, mU
+    // is max |2^-sig U| of the last chunk.
+    int sig = 0;
+    float mH = 0.f, mU = 0.f;
+    // H^T at scale 2^-(sig + d) as the fp16 A operand (TMEM) and, in TMEM,
+    // 2^-d H^T Diag(gamma_C) of the chunk about to start (column i times
+    // gC[i]); returns max |fp16 operand| over this thread's column
+    auto convert_and_scale = [&](int c_next, bool from_h0, int d) -> float {
       const float* gC = gc_all + 128 * (c_next & 1);
+      const float f2 = pow2i(-d);
+      __half2 m2 = __floats2half2_rn(0.f, 0.f);
 #pragma unroll 1
       for (int i0 = 0; i0 < 128; i0 += 16) {
         float f[16];
         if (from_h0) {
 #pragma unroll
           for (int e = 0; e < 16; ++e)
-            f[e] = (a.h0 && i0 + e < DK) ? a.h0[u.sidx + (size_t)(i0 + e) * 128 + s] : 0.f;
+            f[e] = h0_at(i0 + e);
         } else {
           uint32_t v[16];
           tmem_ld32<16>(tmem + lb + T_H + i0, v);
@@ -909,9 +1034,17 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
           for (int e = 0; e < 16; ++e) f[e] = __uint_as_float(v[e]);
         }
+        if (d != 0) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) f[e] *= f2;
+        }
         uint32_t h[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) h[e] = pack_half2(f[2 * e], f[2 * e + 1]);
+        for (int e = 0; e < 8; ++e) {
+          const __half2 x = __floats2half2_rn(f[2 * e], f[2 * e + 1]);
+          m2 = __hmax2(m2, __habs2(x));
+          h[e] = h2u(x);
+        }
         tmem_st32<8>(tmem + lb + T_HA + (i0 >> 1), h);
         uint32_t o[16];
 #pragma unroll
@@ -925,17 +1058,43 @@ __global__ void __launch_bounds__(NT, 1)
         tmem_st32<16>(tmem + lb + T_H + i0, o);
       }
       tmem_st_wait();
+      const float2 mf = __half22float2(m2);
+      return fmaxf(mf.x, mf.y);
+    };
+    // Multiplies `ncols` tensor-memory columns from `col` by 2^-b.
+    auto rescale_cols = [&](uint32_t col, int ncols, int b) {
+      const float f2 = pow2i(-b);
+#pragma unroll 1
+      for (int i0 = 0; i0 < ncols; i0 += 32) {
+        uint32_t v[32];
+        tmem_ld32<32>(tmem + lb + col + i0, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * f2);
+        tmem_st32<32>(tmem + lb + col + i0, v);
+      }
     };
     if (nchunks > 0) {
+      // the scale of h0 (its largest magnitude) while the prep warps start
+      float m0 = 0.f;
+      if (u.h0) {
+#pragma unroll 16
+        for (int i = 0; i < DK; ++i) m0 = fmaxf(m0, fabsf(u.h0[(size_t)i * 128 + s]));
+      } else if (SPLIT && u.ident) {
+        m0 = 1.f;
+      }
+      m0 = cta4_max(red + RED_H0, m0, lane, wq);
       const bool ok = mbar_wait(bars + B_GAM, 0);
       alive = named_and(BAR_STATE, NSTATE, ok);
-      if (alive) convert_and_scale(0, true);
+      m0 = cta4_read(red + RED_H0);
+      sig = state_scale(m0, 0);
+      if (alive) cta4_max(red + RED_H, convert_and_scale(0, true, sig), lane, wq);
     } else if (hT) {
-      for (int i = 0; i < DK; ++i)
-        hT[u.sidx + (size_t)i * 128 + s] = a.h0 ? a.h0[u.sidx + (size_t)i * 128 + s] : 0.f;
+      for (int i = 0; i < DK; ++i) hT[(size_t)i * 128 + s] = h0_at(i);
     }
     tc_fence_before();
     named_sync(BAR_STATE, NSTATE);
+    if (nchunks > 0) mH = cta4_read(red + RED_H);
 
     __nv_bfloat16* go = static_cast<__nv_bfloat16*>(a.o);
     float fin = 0.f;  // becomes NaN once any output is inf or NaN
@@ -950,20 +1109,40 @@ __global__ void __launch_bounds__(NT, 1)
       }
       {  // prep operands of chunk c in shared memory, and its v tile
         bool ok = mbar_wait(bars + B_READY, (uint32_t)(c & 1));
-        if (ok) ok = mbar_wait(bars + B_V, (uint32_t)(c & 1));
+        if (ok && !zero_v) ok = mbar_wait(bars + B_V, (uint32_t)(c & 1));
         if (!named_and(BAR_STATE, NSTATE, ok)) { alive = false; break; }
         tc_fence_after();
       }
-      if (lead) {
-        // U~^T = V^T TB^T, then [U^T | O^T] += H^T [-W ; q*gamma]^T
+      if (sig != 0 && !zero_v) {  // v at the state's scale: U~ = TB (2^-sig V)
+        const __nv_bfloat162 f2 = __float2bfloat162_rn(pow2i(-sig));
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          umma_ss(tmem + T_U, mnmajor_desc(sb + S_V, 64, k), kmajor_desc(sb + S_TB, 64, k),
-                  idesc_f16(128, 64, 1, 1, 0), k > 0);
+        for (int e = 0; e < 8; ++e) {
+          uint4* p = reinterpret_cast<uint4*>(sm + S_V) + e * NSTATE + s;
+          uint4 w = *p;
+          uint32_t* x = reinterpret_cast<uint32_t*>(&w);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            __nv_bfloat162 y = __hmul2(*reinterpret_cast<__nv_bfloat162*>(&x[k]), f2);
+            x[k] = *reinterpret_cast<uint32_t*>(&y);
+          }
+          *p = w;
+        }
+        fence_proxy_async_smem();
+        named_sync(BAR_STATE, NSTATE);
+      }
+      if (lead) {
+        // U~^T = V^T TB^T, then [U^T | O^T] += H^T [-W ; q*gamma]^T (with
+        // v = 0 the first step overwrites: U~ = 0, and O is zero already)
+        if (!zero_v) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            umma_ss(tmem + T_U, mnmajor_desc(sb + S_V, 64, k), kmajor_desc(sb + S_TB, 64, k),
+                    idesc_f16(128, 64, 1, 1, 0), k > 0);
+        }
 #pragma unroll
         for (int k = 0; k < 8; ++k)
           umma_ts(tmem + T_U, tmem + T_HA + 8 * k, kmajor_desc(sb + S_WQ, 128, k),
-                  idesc_f16(128, 128, 0, 0, 0), 1);
+                  idesc_f16(128, 128, 0, 0, 0), (k > 0 || !zero_v) ? 1u : 0u);
         umma_commit(bars + B_S1);
       }
       {
@@ -971,14 +1150,17 @@ __global__ void __launch_bounds__(NT, 1)
         if (!named_and(BAR_STATE, NSTATE, ok)) { alive = false; break; }
         tc_fence_after();
       }
-      if (lead && c + 1 < nchunks) {  // the v tile is free: fetch the next one
+      if (lead && c + 1 < nchunks && !zero_v) {  // the v tile is free: fetch the next one
         const int y = (int)(u.row0 + (long)(c + 1) * C);
         mbar_arrive_expect_tx(bars + B_V, TILE_BYTES);
         tma_load_2d(sm + S_V, &mv, bars + B_V, 0, y);
         tma_load_2d(sm + S_V + 8192, &mv, bars + B_V, 64, y);
       }
-      // U^T -> fp16 A operand in TMEM
-      {
+      // U^T -> fp16 A operand in TMEM, at scale 2^-f (0 unless U leaves
+      // fp16's normal range)
+      auto convert_u = [&](int f) -> float {
+        const float f2 = pow2i(-f);
+        __half2 m2 = __floats2half2_rn(0.f, 0.f);
         uint32_t v[32];
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2) {
@@ -986,14 +1168,50 @@ __global__ void __launch_bounds__(NT, 1)
           tmem_ld_wait();
           uint32_t hh[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e)
-            hh[e] = pack_half2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
+          for (int e = 0; e < 16; ++e) {
+            float x0 = __uint_as_float(v[2 * e]), x1 = __uint_as_float(v[2 * e + 1]);
+            if (f != 0) { x0 *= f2; x1 *= f2; }
+            const __half2 x = __floats2half2_rn(x0, x1);
+            m2 = __hmax2(m2, __habs2(x));
+            hh[e] = h2u(x);
+          }
           tmem_st32<16>(tmem + lb + T_UA + 16 * h2, hh);
         }
         tmem_st_wait();
-      }
+        const float2 mf = __half22float2(m2);
+        return fmaxf(mf.x, mf.y);
+      };
+      cta4_max(red + RED_U, convert_u(0), lane, wq);
       tc_fence_before();
       named_sync(BAR_STATE, NSTATE);
+      mU = cta4_read(red + RED_U);
+      if (!(mU >= kUMin && mU < kUMax)) {
+        // U outside [2^-4, 2^15) (or zero): choose b from its exact maximum
+        // and move the whole step to scale 2^-(sig + b)
+        float m = 0.f;
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          uint32_t v[32];
+          tmem_ld32<32>(tmem + lb + T_U + 32 * h2, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) m = fmaxf(m, fabsf(__uint_as_float(v[e])));
+        }
+        cta4_max(red + RED_UX, m, lane, wq);
+        named_sync(BAR_STATE, NSTATE);
+        m = cta4_read(red + RED_UX);
+        const int b = u_shift(m, mH, sig);
+        if (b != 0) {
+          rescale_cols(T_O, 64, b);
+          rescale_cols(T_H, 128, b);
+          convert_u(b);
+          mU = m * pow2i(-b);
+          mH *= pow2i(-b);
+          sig += b;
+        }
+        tc_fence_before();
+        named_sync(BAR_STATE, NSTATE);
+      }
       if (lead) {
         tc_fence_after();
         // O^T += U^T A^T (A of this chunk's parity), H^T += U^T (k*rho)
@@ -1013,9 +1231,10 @@ __global__ void __launch_bounds__(NT, 1)
         if (!named_and(BAR_STATE, NSTATE, ok)) { alive = false; break; }
         tc_fence_after();
       }
-      // outputs o[t][j] = O^T[j][t]
+      // outputs o[t][j] = 2^sig O^T[j][t]
       {
         const long rbase = u.row0 + (long)c * C;
+        const float s1 = pow2i(sig / 2), s2 = pow2i(sig - sig / 2);
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2) {
           uint32_t v[32];
@@ -1024,8 +1243,9 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             const int t = 32 * h2 + e;
-            const float x = __uint_as_float(v[e]);
-            if (t < lenc) {
+            float x = __uint_as_float(v[e]);
+            if (sig != 0) x = x * s1 * s2;
+            if (t < lenc && u.write_o) {
               go[(size_t)(rbase + t) * 128 + s] = __float2bfloat16_rn(x);
               fin = fmaf(x, 0.f, fin);
             }
@@ -1037,20 +1257,27 @@ __global__ void __launch_bounds__(NT, 1)
       if (c + 1 < nchunks) {
         const bool ok = mbar_wait(bars + B_GAM + ((c + 1) & 1), (uint32_t)(((c + 1) >> 1) & 1));
         if (!named_and(BAR_STATE, NSTATE, ok)) { alive = false; break; }
-        convert_and_scale(c + 1, false);
+        // |H'| <= |H| + sum_t |k*rho| |U| <= mH + 64 mU for keys with
+        // |k_i| <= 1 (unit keys) and |gamma|, |rho| <= 1
+        const int nsig = state_scale(fmaf(64.f, mU, mH), sig);
+        cta4_max(red + RED_H, convert_and_scale(c + 1, false, nsig - sig), lane, wq);
+        sig = nsig;
         tc_fence_before();
         named_sync(BAR_STATE, NSTATE);
+        mH = cta4_read(red + RED_H);
       }
     }
     if (alive && nchunks > 0 && hT) {
+      const float s1 = pow2i(sig / 2), s2 = pow2i(sig - sig / 2);
       for (int i0 = 0; i0 < DK; i0 += 32) {
         uint32_t v[32];
         tmem_ld32<32>(tmem + lb + T_H + i0, v);
         tmem_ld_wait();
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
-          const float x = __uint_as_float(v[e]);
-          hT[u.sidx + (size_t)(i0 + e) * 128 + s] = x;
+          float x = __uint_as_float(v[e]);
+          if (sig != 0) x = x * s1 * s2;
+          hT[(size_t)(i0 + e) * 128 + s] = x;
           fin = fmaf(x, 0.f, fin);
         }
       }
@@ -1112,7 +1339,7 @@ __global__ void __launch_bounds__(NT, 1)
           tma_prefetch_2d_l2(&mk, x0, y);
           tma_prefetch_2d_l2(&ma, x0, y);
         }
-        tma_prefetch_2d_l2(&mv, x0, y);
+        if (!zero_v) tma_prefetch_2d_l2(&mv, x0, y);
       }
     };
     // Gram round: D (128 x 64) = X (128 rows) Y^T (64 rows), K = 128
@@ -1148,9 +1375,11 @@ __global__ void __launch_bounds__(NT, 1)
     if (nchunks > 0) {
       if (leader) {
         issue_qka(0);
-        mbar_arrive_expect_tx(bars + B_V, TILE_BYTES);
-        tma_load_2d(sm + S_V, &mv, bars + B_V, 0, (int)u.row0);
-        tma_load_2d(sm + S_V + 8192, &mv, bars + B_V, 64, (int)u.row0);
+        if (!zero_v) {
+          mbar_arrive_expect_tx(bars + B_V, TILE_BYTES);
+          tma_load_2d(sm + S_V, &mv, bars + B_V, 0, (int)u.row0);
+          tma_load_2d(sm + S_V + 8192, &mv, bars + B_V, 64, (int)u.row0);
+        }
         if (nchunks > 1) prefetch_l2(1);
       }
       fetch_beta(0);
@@ -1202,7 +1431,7 @@ __global__ void __launch_bounds__(NT, 1)
       set_status(a.status, CKDA_ERR_TIMEOUT);
       // let any MMA or copy still in flight land before the memory is released
       for (int i = B_DONE_A; i <= B_S3 + 1; ++i) mbar_wait(bars + i, 0, 1u << 12, 1000u);
-      mbar_wait(bars + B_V, 0, 1u << 12, 1000u);
+      if (!zero_v) mbar_wait(bars + B_V, 0, 1u << 12, 1000u);
       mbar_wait(bars + B_QKA, 0, 1u << 12, 1000u);
     }
   }
@@ -1225,9 +1454,26 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t width) {
 
 }  // namespace
 
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t s) {
-  const int units = a.num_units_seq * a.H;
-  if (units == 0) return cudaSuccess;
+  const long long grid = a.split_pass
+                             ? (long long)a.B * a.H * split_ctas_per_unit(a.split_pass, a.nseg)
+                             : (long long)a.num_units_seq * a.H;
+  if (grid == 0) return cudaSuccess;
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
   const uint64_t rows = (uint64_t)a.B * a.H * a.T;
   CUtensorMap mq, mk, ma, mv;
   if (rows == 0) {
@@ -1236,11 +1482,12 @@ cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t s) {
              !make_map(&ma, a.alpha, rows, a.dk) || !make_map(&mv, a.v, rows, 128)) {
     return cudaErrorInvalidValue;
   }
-  auto kern = a.dk == 64 ? fwd_kernel<64> : fwd_kernel<128>;
+  auto kern = a.split_pass ? (a.dk == 64 ? fwd_kernel<64, true> : fwd_kernel<128, true>)
+                           : (a.dk == 64 ? fwd_kernel<64, false> : fwd_kernel<128, false>);
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_ALLOC);
   if (err != cudaSuccess) return err;
-  kern<<<(unsigned)units, NT, SMEM_ALLOC, s>>>(a, mq, mk, ma, mv);
+  kern<<<(unsigned)grid, NT, SMEM_ALLOC, s>>>(a, mq, mk, ma, mv);
   return cudaGetLastError();
 }
 

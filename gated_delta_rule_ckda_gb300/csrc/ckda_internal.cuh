@@ -57,13 +57,11 @@ inline bool fwd_tensor_path(ckda_dtype io, int dk, int dv) {
 }
 // The driver's cuTensorMapEncodeTiled, looked up once (null if unavailable).
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
-// Chunkwise tcgen05 forward (fwd_tensor_path shapes, chunk 64), dense or packed.
+// Chunkwise tcgen05 forward (fwd_tensor_path shapes, chunk 64), dense or
+// packed, or one pass of the sequence split (a.split_pass != 0).
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t s);
 // Token-serial CUDA-core forward (any dk, dv <= 128).
 cudaError_t launch_fwd_recurrent(const FwdArgs& a, cudaStream_t s);
-// The sequence split's passes (a.split_pass != 0) on the chunkwise kernel
-// that takes per-CTA roles.
-cudaError_t launch_fwd_chunk(const FwdArgs& a, cudaStream_t s);
 // CTAs of one pass of the sequence split, per (sequence, head).
 __host__ __device__ inline int split_ctas_per_unit(int pass, int nseg) {
   return pass == 1 ? (nseg >= 3 ? 2 * nseg - 3 : 1) : nseg - 1;

@@ -231,11 +231,11 @@ ckda_status ckda_fwd_split(const void* q, const void* k, const void* v, const vo
 
   if (cudaMemsetAsync(a.status, 0, sizeof(int), s) != cudaSuccess) return CKDA_ERR_CUDA;
   a.split_pass = 1;
-  if (launch_fwd_chunk(a, s) != cudaSuccess) return CKDA_ERR_CUDA;
+  if (launch_fwd(a, s) != cudaSuccess) return CKDA_ERR_CUDA;
   if (launch_seg_scan(seg_state, seg_P, seg_F, B * H, nseg, dk, s) != cudaSuccess)
     return CKDA_ERR_CUDA;
   a.split_pass = 2;
-  if (launch_fwd_chunk(a, s) != cudaSuccess) return CKDA_ERR_CUDA;
+  if (launch_fwd(a, s) != cudaSuccess) return CKDA_ERR_CUDA;
   return CKDA_OK;
 }
 

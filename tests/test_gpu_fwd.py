@@ -5,6 +5,8 @@ dv = 128 with dk = 128 or 64, token-serial CUDA-core otherwise), ragged
 tails, edge cases, and the named workloads at full size (outputs of the packed workload are
 checked on a sample of sequences chosen to include the longest and shortest).
 """
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -287,11 +289,62 @@ def test_bounded_wait_reports_timeout(ck):
     run_gpu(ck, x)
 
 
-def test_fp16_range_overflow_is_reported(ck):
-    """v far outside the fp16 range makes U overflow its fp16 operand; the
-    kernel must report CKDA_ERR_RANGE rather than return silently."""
-    x = synth.make_fwd(1, 1, 64, 128, dist="kda", dtype="bf16", h0=False, seed=18)
-    d = x.to("cuda")
-    v = (d.v.float() * 1e6).to(torch.bfloat16)
-    ck.fwd(d.q, d.k, v, d.alpha, d.beta)
-    assert ck.fwd_status(ck.fwd.last_workspace) == 6  # CKDA_ERR_RANGE
+def _scaled(x, fv=1.0, fh=1.0, profile=None):
+    """x with v times fv (times a per-token profile) and h0 times fh."""
+    v = x.v.float() * fv
+    if profile is not None:
+        v = v * profile.view(1, 1, -1, 1)
+    h0 = None if x.h0 is None else x.h0 * fh
+    return dataclasses.replace(x, v=v.to(x.v.dtype), h0=h0)
+
+
+@pytest.mark.parametrize("dk", [128, 64])
+@pytest.mark.parametrize("fv,fh", [(1e3, 1.0), (1e6, 1.0), (1.0, 1e3), (1.0, 1e6), (1e6, 1e6),
+                                   (1e-6, 1e-6), (1e6, 1e-6), (1e-6, 1e6)])
+def test_chunk_path_scaled_v_and_h0(ck, dk, fv, fh):
+    """The state step's fp16 operands follow the magnitude of v and h0 by a
+    power-of-two scale: results far outside fp16's range come back with the
+    accuracy of unit-scale inputs, and no CKDA_ERR_RANGE."""
+    x = _scaled(synth.make_fwd(2, 2, 300, dk, dv=128, dist="ckda", dtype="bf16", h0=True,
+                               seed=40), fv, fh)
+    o, hT = run_gpu(ck, x)
+    o_ref, h_ref = run_oracle(x)
+    check(o, hT, o_ref, h_ref, bf16=True, name=f"dk{dk} v*{fv:g} h0*{fh:g}")
+
+
+@pytest.mark.parametrize("jump", [1e6, 1e-6])
+def test_chunk_path_magnitude_jumps(ck, jump):
+    """v jumps by 1e6 (or 1e-6) for tokens 128..255 and back: the scale
+    follows mid-sequence in both directions.  With fast-decaying gates each
+    segment's outputs are judged against their own size."""
+    T = 448
+    prof = torch.ones(T)
+    prof[128:256] = jump
+    x = _scaled(synth.make_fwd(1, 2, T, 128, dist="kda", dtype="bf16", h0=True, seed=41),
+                profile=prof)
+    o, hT = run_gpu(ck, x)
+    o_ref, h_ref = run_oracle(x)
+    for t0, t1 in ((0, 128), (128, 256), (320, T)):
+        ro = report(f"jump {jump:g} o[{t0}:{t1}]", o[:, :, t0:t1], o_ref[:, :, t0:t1], True)
+        assert ro["excess_bf16"] <= TOL_BF16 and ro["rms_rel"] <= 5e-3, ro
+    rh = report("jump hT", hT, h_ref, False)
+    assert rh["max_rel"] <= TOL_BF16, rh
+
+
+def test_chunk_path_scaled_packed(ck):
+    """Packed sequences, each with its own magnitude (the scale is per CTA)."""
+    lengths = [70, 300, 5, 129]
+    x = synth.make_varlen(lengths, 2, 128, dist="ckda", dtype="bf16", h0=True, seed=42)
+    cu = x.cu_seqlens.tolist()
+    prof = torch.ones(cu[-1])
+    for i, f in enumerate((1e6, 1.0, 1e-6, 1e3)):
+        prof[cu[i]:cu[i + 1]] = f
+    x = _scaled(x, profile=prof)
+    o, hT = run_gpu(ck, x)
+    o_ref, h_ref = run_oracle(x)
+    for i in range(len(lengths)):
+        sl = slice(cu[i], cu[i + 1])
+        ro = report(f"packed seq {i} o", o[:, :, sl], o_ref[:, :, sl], True)
+        assert ro["excess_bf16"] <= TOL_BF16 and ro["rms_rel"] <= 5e-3, ro
+        rh = report(f"packed seq {i} hT", hT[i], h_ref[i], False)
+        assert rh["max_rel"] <= TOL_BF16, rh

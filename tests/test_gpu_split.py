@@ -3,9 +3,12 @@
 The sequence split must give the result of one pass over each whole
 sequence: o and the final state are compared with the oracle's plain
 recurrence for several segment counts, ragged tails, with and without h0,
-hT aliasing h0, the 64-wide key, more CTAs than SMs, and the one-long-
-sequence workload at full size with the automatic segment count.
+hT aliasing h0, the 64-wide key, v and h0 far from unit scale, more CTAs
+than SMs, and the one-long-sequence workload at full size with the
+automatic segment count.
 """
+import dataclasses
+
 import pytest
 import torch
 
@@ -74,6 +77,16 @@ def test_split_dk64(ck):
     x = synth.make_fwd(2, 2, 700, 64, dv=128, dist="kda", dtype="bf16", h0=True, seed=43)
     o, hT = run_split(ck, x, 4)
     check(o, hT, x, "split dk64")
+
+
+@pytest.mark.parametrize("fv,fh", [(1e6, 1e3), (1e-6, 1.0), (1.0, 1e6)])
+def test_split_scaled_inputs(ck, fv, fh):
+    """Every pass (from h0, from zero, the transition from [I | 0] with v = 0,
+    and from the scanned states) keeps its own power-of-two operand scale."""
+    x = synth.make_fwd(1, 2, 64 * 9 + 5, 128, dist="ckda", dtype="bf16", h0=True, seed=45)
+    x = dataclasses.replace(x, v=(x.v.float() * fv).to(x.v.dtype), h0=x.h0 * fh)
+    o, hT = run_split(ck, x, 4)
+    check(o, hT, x, f"split v*{fv:g} h0*{fh:g}")
 
 
 def test_split_one_segment_is_ckda_fwd(ck):
