@@ -74,6 +74,7 @@ KERNEL_SOURCES = {
     "fwd": ["ckda_fwd.cu", "sm103.cuh", "ckda_internal.cuh"],
     "decode128": ["ckda_decode.cu", "ckda_internal.cuh"],
     "prep": ["ckda_prep.cu", "ckda_internal.cuh"],
+    "prep_bwd": ["ckda_prep.cu", "ckda_internal.cuh"],
     "bwd": ["ckda_bwd.cu", "ckda_internal.cuh"],
 }
 
@@ -373,7 +374,7 @@ def prep_bytes(rows, dk, io_bytes=2, with_q=True):
     return rows * 2 * (nt * dk * io_bytes + io_bytes)
 
 
-def prep_case(ck, x, steps, warmup, ws, stream):
+def prep_case(ck, x, steps, warmup, ws, stream, name):
     """ckda_prep on raw inputs of the workload's shape: q and k unnormalised,
     gate logits a ~ N(0, 2), b ~ N(0, 1); HBM bytes read and written once."""
     import torch
@@ -398,10 +399,52 @@ def prep_case(ck, x, steps, warmup, ws, stream):
     del raw, out
     return {"value": round(nbytes * steps / total / 1e9, 1), "unit": "GB/s", "steps": steps,
             "ms_per_step": round(total / steps * 1e3, 4),
-            "config": {"workload": "raw inputs of the kda_range shape", "rows": rows, "dk": dk,
+            "config": {"workload": f"raw inputs of the {name} shape", "rows": rows, "dk": dk,
                        "io": "bf16", "normalize_q": True},
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
-                         "frac": round(gbs / peak, 4), "traffic": traffic_for("prep", "kda_range"),
+                         "frac": round(gbs / peak, 4), "traffic": traffic_for("prep", name),
+                         "algorithmic_bytes": nbytes, "mean_launch_ms": round(ms, 4),
+                         "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)"
+                         if src == "measured" else src},
+            "gpu_launches": steps}
+
+
+def prep_bwd_bytes(rows, dk, io_bytes=2):
+    """Algorithmic bytes of ckda_prep_bwd with q: q_raw, k_raw, a_raw and the
+    gradients of q, k, alpha in, those of the raw three out (dk each), plus
+    b_raw and d_beta in and d_b_raw out."""
+    return rows * (9 * dk + 3) * io_bytes
+
+
+def prep_bwd_case(ck, x, steps, warmup, ws, stream, name):
+    """ckda_prep_bwd on raw inputs of the workload's shape (as prep_case) and
+    unit-normal upstream gradients; HBM bytes read and written once."""
+    import torch
+    B, H, T, dk = x.q.shape
+    g = torch.Generator().manual_seed(22)
+    shapes = ((B, H, T, dk),) * 3 + ((B, H, T),) + ((B, H, T, dk),) * 3 + ((B, H, T),)
+    t = [torch.randn(sh, generator=g).to(torch.bfloat16).cuda() for sh in shapes]
+    qr, kr, ar, br, dq, dk_, da, db = t
+    qr.mul_(3)
+    ar.mul_(2)
+    out = (torch.empty_like(qr), torch.empty_like(kr), torch.empty_like(ar), torch.empty_like(br))
+
+    def step():
+        ck.prep_bwd(kr, ar, br, dk_, da, db, q_raw=qr, d_q=dq, out=out, stream=stream)
+
+    total, per = time_steps(step, steps, warmup, ws, stream)
+    rows = B * H * T
+    nbytes = prep_bwd_bytes(rows, dk)
+    peak, src = hbm_peak()
+    ms = sum(per) / len(per)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    del t, out
+    return {"value": round(nbytes * steps / total / 1e9, 1), "unit": "GB/s", "steps": steps,
+            "ms_per_step": round(total / steps * 1e3, 4),
+            "config": {"workload": f"raw inputs and upstream gradients of the {name} shape",
+                       "rows": rows, "dk": dk, "io": "bf16", "normalize_q": True},
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(gbs / peak, 4), "traffic": traffic_for("prep_bwd", name),
                          "algorithmic_bytes": nbytes, "mean_launch_ms": round(ms, 4),
                          "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)"
                          if src == "measured" else src},
@@ -527,7 +570,9 @@ def run_ours(args):
     if ws == 1 and "decode_raw" in extras:
         out["decode_raw"] = decode_case(ck, args.decode_steps, 10, ws, stream, raw=True)
     if ws == 1 and "prep" in extras:
-        out["prep"] = prep_case(ck, x, 200, 10, ws, stream)
+        out["prep"] = prep_case(ck, x, 200, 10, ws, stream, args.workload)
+    if ws == 1 and "prep_bwd" in extras:
+        out["prep_bwd"] = prep_bwd_case(ck, x, 200, 10, ws, stream, args.workload)
     if ws == 1 and "bwd" in extras:
         out["bwd"] = bwd_case(ck, x, 10, 3, ws, stream, units=args.bwd_units)
     if ws == 1 and any(e in extras for e in ("kda_range", "ckda_full", "ckda_varlen",
@@ -621,9 +666,9 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--extras",
-                    default="decode,decode_raw,prep,bwd,kda_range,ckda_varlen,kda_range_dk64,"
-                            "fig5_sweep",
-                    help="comma list of extra measurements: decode, decode_raw, prep, bwd, "
+                    default="decode,decode_raw,prep,prep_bwd,bwd,kda_range,ckda_varlen,"
+                            "kda_range_dk64,fig5_sweep",
+                    help="comma list of extra measurements: decode, decode_raw, prep, prep_bwd, bwd, "
                          "kda_range, ckda_full, ckda_varlen, kda_range_dk64, fig5_sweep")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--bwd-units", type=int, default=0,

@@ -86,6 +86,8 @@ def lib():
             L.ckda_prep.restype = i32
             L.ckda_prep.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_longlong, i32, i32,
                                     i32, f32, vp]
+            L.ckda_prep_bwd.restype = i32
+            L.ckda_prep_bwd.argtypes = [vp] * 12 + [ctypes.c_longlong, i32, i32, i32, f32, vp]
             L.ckda_fwd_host.restype = i32
             L.ckda_fwd_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
                                         i32, f32, i32, vp, sz, vp]
@@ -378,6 +380,51 @@ def prep(k_raw, a_raw, b_raw, q_raw=None, normalize_q=True, norm_eps=1e-6, out=N
     if rc != 0:
         raise CkdaError(rc, "ckda_prep")
     return q, k, alpha, beta
+
+
+def prep_bwd(k_raw, a_raw, b_raw, d_k, d_alpha, d_beta, q_raw=None, d_q=None, normalize_q=True,
+             norm_eps=1e-6, out=None, stream=None):
+    """Backward of ``prep`` (ckda_prep_bwd): the gradients with respect to the
+    raw inputs from those with respect to (q, k, alpha, beta).  The gate's
+    sign carries no gradient and |tanh(a/2)| takes the subgradient 0 at a = 0.
+
+    Returns (d_q_raw or None, d_k_raw, d_a_raw, d_b_raw) in the input dtype;
+    `out` may give the four output tensors (d_q_raw may be None)."""
+    L = lib()
+    device = k_raw.device
+    dt = k_raw.dtype
+    shp = tuple(k_raw.shape)
+    dk = shp[-1]
+    for name, t, want in (("a_raw", a_raw, shp), ("b_raw", b_raw, shp[:-1]), ("d_k", d_k, shp),
+                          ("d_alpha", d_alpha, shp), ("d_beta", d_beta, shp[:-1]),
+                          ("k_raw", k_raw, shp)):
+        _check(t, name, dt, want, device)
+    if (q_raw is None) != (d_q is None):
+        raise ValueError("prep_bwd: q_raw and d_q must both be given or both be None")
+    if q_raw is not None:
+        _check(q_raw, "q_raw", dt, shp, device)
+        _check(d_q, "d_q", dt, shp, device)
+    if out is None:
+        dq_raw = None if q_raw is None else torch.empty_like(q_raw)
+        dk_raw, da_raw, db_raw = (torch.empty_like(k_raw), torch.empty_like(a_raw),
+                                  torch.empty_like(b_raw))
+    else:
+        dq_raw, dk_raw, da_raw, db_raw = out
+        for name, t, want in (("d_k_raw", dk_raw, shp), ("d_a_raw", da_raw, shp),
+                              ("d_b_raw", db_raw, shp[:-1])):
+            _check(t, name, dt, want, device)
+        if (dq_raw is None) != (q_raw is None):
+            raise ValueError("prep_bwd: d_q_raw and q_raw must both be given or both be None")
+        if dq_raw is not None:
+            _check(dq_raw, "d_q_raw", dt, shp, device)
+    rows = k_raw.numel() // dk if dk else 0
+    rc = L.ckda_prep_bwd(_ptr(q_raw), _ptr(k_raw), _ptr(a_raw), _ptr(b_raw), _ptr(d_q),
+                         _ptr(d_k), _ptr(d_alpha), _ptr(d_beta), _ptr(dq_raw), _ptr(dk_raw),
+                         _ptr(da_raw), _ptr(db_raw), int(rows), int(dk), _io_dtype(k_raw),
+                         int(bool(normalize_q)), float(norm_eps), _stream_handle(stream, device))
+    if rc != 0:
+        raise CkdaError(rc, "ckda_prep_bwd")
+    return dq_raw, dk_raw, da_raw, db_raw
 
 
 def bwd_workspace_bytes(B, H, T, dk, dv, num_seqs=0) -> int:

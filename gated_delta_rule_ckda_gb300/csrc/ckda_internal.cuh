@@ -110,6 +110,24 @@ __device__ __forceinline__ float gate_beta(float b) {
   return 2.f * e / (1.f + e);
 }
 
+// Their derivatives, for the backward of the input preparation.  The sign s
+// is piecewise constant and carries no gradient, and |tanh(a/2)| takes the
+// subgradient 0 at a = 0, so d alpha / d a = (1 - e^-5) (1 - r^2) / 2 for
+// a != 0 and 0 at a = 0; 1 - r^2 = 4 e / (1 + e)^2 with e = exp(-|a|) keeps
+// its relative accuracy for large |a|.  d beta / d b = 2 sigma(b)(1 - sigma(b))
+// = 2 e / (1 + e)^2 with e = exp(-|b|).
+__device__ __forceinline__ float gate_alpha_grad(float a) {
+  if (a == 0.f) return 0.f;
+  const float e = expf(-fabsf(a));
+  const float d = 1.f + e;
+  return 2.f * (1.f - kGateEps) * e / (d * d);
+}
+__device__ __forceinline__ float gate_beta_grad(float b) {
+  const float e = expf(-fabsf(b));
+  const float d = 1.f + e;
+  return 2.f * e / (d * d);
+}
+
 // Element loads/stores in the I/O dtype.
 template <typename T>
 __device__ __forceinline__ float ld_io(const T* p);

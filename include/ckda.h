@@ -23,8 +23,8 @@
  *   - Argument errors are detected on the host before anything is launched
  *     and returned synchronously (CKDA_ERR_INVALID_ARG / _UNSUPPORTED).
  *     A failed launch returns CKDA_ERR_CUDA.
- *   - Device-side conditions (a bounded wait that ran out, an fp16 operand
- *     that overflowed) are written to a status word in the caller's
+ *   - Device-side conditions (a bounded wait that ran out, a result that is
+ *     not finite) are written to a status word in the caller's
  *     workspace and read back with ckda_fwd_status().
  *   - k is NOT normalised by the library: ||k_t|| = 1 is the caller's
  *     precondition, as on the pages.  The library accepts any finite k.
@@ -51,8 +51,10 @@ typedef enum {
     CKDA_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed */
     CKDA_ERR_TIMEOUT = 4,      /* device: a bounded wait ran out (see ckda_fwd_status) */
     CKDA_ERR_WORKSPACE = 5,    /* workspace missing or smaller than required */
-    CKDA_ERR_RANGE = 6         /* device: an fp16 tensor-core operand overflowed, seen as a
-                                  non-finite o or final state (also non-finite inputs) */
+    CKDA_ERR_RANGE = 6         /* device: a non-finite o or final state -- a result outside
+                                  fp32 / the I/O dtype, non-finite inputs, or (tensor-core
+                                  path) a query or key too large for its fp16 operand; v
+                                  and h0 of any finite size are scaled into range */
 } ckda_status;
 
 /* Version of this ABI: major * 10000 + minor * 100 + patch. */
@@ -138,7 +140,7 @@ ckda_status ckda_fwd(const void *q, const void *k, const void *v,
  *     different streams, or from several threads at once) race on it and
  *     must be serialised by the caller.  Each call clears the status word it
  *     uses and rewrites the work order it reads.
- *   - Device-side conditions (timeout, fp16 range) are recorded in the shared
+ *   - Device-side conditions (timeout, range) are recorded in the shared
  *     array and are not reported; use ckda_fwd to observe them.
  */
 ckda_status ckda_fwd_noalloc(const void *q, const void *k, const void *v,
@@ -368,6 +370,38 @@ ckda_status ckda_prep(const void *q_raw, const void *k_raw, const void *a_raw,
                       const void *b_raw, void *q, void *k, void *alpha, void *beta,
                       long long rows, int dk, ckda_dtype io_dtype, int normalize_q,
                       float norm_eps, void *stream);
+
+/*
+ * Backward of ckda_prep: from the gradients of a loss with respect to its
+ * outputs (d_q, d_k, d_alpha, d_beta), the gradients with respect to its raw
+ * inputs (d_q_raw, d_k_raw, d_a_raw, d_b_raw), per token row:
+ *
+ *   k = k_raw / n, n = sqrt(sum_i k_raw_i^2 + norm_eps):
+ *       d_k_raw = (d_k - k (k . d_k)) / n           (q likewise if normalize_q,
+ *                                                     else d_q_raw = d_q)
+ *   d_a_raw = d_alpha * (1 - e^-5) (1 - r^2) / 2 with r = tanh(a_raw / 2),
+ *             and 0 where a_raw = 0
+ *   d_b_raw = d_beta * 2 sigma(b_raw) (1 - sigma(b_raw))
+ *
+ * The gate's sign s is piecewise constant and carries no gradient; |r| takes
+ * the subgradient 0 at r = 0 (where alpha jumps between -e^-5 and +e^-5).
+ *
+ *   q_raw, k_raw, a_raw, d_q, d_k, d_alpha, d_q_raw, d_k_raw, d_a_raw : io [rows, dk]
+ *   b_raw, d_beta, d_b_raw                                           : io [rows]
+ *
+ * q_raw, d_q and d_q_raw are all NULL (no query) or all set; normalize_q and
+ * norm_eps must be those of the forward call.  Each output may alias its own
+ * gradient input or its own raw input (in place).  Arithmetic is fp32 with
+ * one rounding to io_dtype.  dk <= 128.  Argument errors return
+ * synchronously with nothing launched (rows = 0 launches nothing and returns
+ * CKDA_OK); otherwise returns CKDA_OK once enqueued on `stream`.  The library
+ * allocates nothing.
+ */
+ckda_status ckda_prep_bwd(const void *q_raw, const void *k_raw, const void *a_raw,
+                          const void *b_raw, const void *d_q, const void *d_k,
+                          const void *d_alpha, const void *d_beta, void *d_q_raw,
+                          void *d_k_raw, void *d_a_raw, void *d_b_raw, long long rows, int dk,
+                          ckda_dtype io_dtype, int normalize_q, float norm_eps, void *stream);
 
 /*
  * Self-test of the bounded-wait path: launches one block that waits on a

@@ -34,6 +34,11 @@ Functions and what pins them (tests/test_oracle_pins.py):
   logits) and by the identities the parameterisation implies (odd symmetry of
   alpha, beta(-b) = 2 - beta(b), monotonicity in |a|, unit norm and direction
   of the normalised keys).
+* ``prep_bwd`` -- the backward of ``prep``: pinned by central differences of
+  ``prep`` (itself pinned above) away from a = 0, by the reading at a = 0
+  (the sign carries no gradient, |r| takes the subgradient 0), by the closed
+  form dbeta/db = 1/2 at b = 0, by the scale invariance of k / |k| (k_raw .
+  dk_raw = 0 when norm_eps = 0) and by the identity map of an unnormalised q.
 """
 from __future__ import annotations
 
@@ -90,6 +95,9 @@ def _load():
             lib.ckda_oracle_prep.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, ctypes.c_long,
                                              ctypes.c_int, ctypes.c_int, ctypes.c_double]
             lib.ckda_oracle_prep.restype = ctypes.c_int
+            lib.ckda_oracle_prep_bwd.argtypes = [dp] * 12 + [ctypes.c_long, ctypes.c_int,
+                                                             ctypes.c_int, ctypes.c_double]
+            lib.ckda_oracle_prep_bwd.restype = ctypes.c_int
             lib.ckda_oracle_max_threads.argtypes = []
             lib.ckda_oracle_max_threads.restype = ctypes.c_int
             _lib = lib
@@ -181,6 +189,34 @@ def prep(k_raw, a_raw, b_raw, q_raw=None, normalize_q=True, norm_eps=1e-6):
     if rc != 0:
         raise ValueError("oracle prep: invalid arguments")
     return q, k, alpha, beta
+
+
+def prep_bwd(k_raw, a_raw, b_raw, dk, dalpha, dbeta, q_raw=None, dq=None, normalize_q=True,
+             norm_eps=1e-6):
+    """Backward of ``prep`` in fp64: the gradients with respect to (q_raw, k_raw,
+    a_raw, b_raw) from those with respect to its outputs (q, k, alpha, beta).
+    The gate's sign carries no gradient and |tanh(a/2)| takes the subgradient
+    0 at a = 0.  Returns (dq_raw or None, dk_raw, da_raw, db_raw)."""
+    lib = _load()
+    k_raw, a_raw, b_raw, q_raw, dk, dalpha, dbeta, dq = (
+        _f64(x) for x in (k_raw, a_raw, b_raw, q_raw, dk, dalpha, dbeta, dq))
+    n = k_raw.shape[-1]
+    rows = k_raw.size // n
+    shp = k_raw.shape
+    if (a_raw.shape != shp or dk.shape != shp or dalpha.shape != shp or b_raw.size != rows
+            or dbeta.size != rows or (q_raw is None) != (dq is None)
+            or (q_raw is not None and (q_raw.shape != shp or dq.shape != shp))):
+        raise ValueError("oracle prep_bwd: shapes")
+    dk_raw, da_raw = np.zeros_like(k_raw), np.zeros_like(a_raw)
+    db_raw = np.zeros(b_raw.shape, dtype=np.float64)
+    dq_raw = None if q_raw is None else np.zeros_like(q_raw)
+    rc = lib.ckda_oracle_prep_bwd(_ptr(q_raw), _ptr(k_raw), _ptr(a_raw), _ptr(b_raw), _ptr(dq),
+                                  _ptr(dk), _ptr(dalpha), _ptr(dbeta), _ptr(dq_raw),
+                                  _ptr(dk_raw), _ptr(da_raw), _ptr(db_raw), int(rows), int(n),
+                                  int(bool(normalize_q)), float(norm_eps))
+    if rc != 0:
+        raise ValueError("oracle prep_bwd: invalid arguments")
+    return dq_raw, dk_raw, da_raw, db_raw
 
 
 def bwd(q, k, v, alpha, beta, do, h0=None, dhT=None, cu_seqlens=None, scale=1.0,

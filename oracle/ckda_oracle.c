@@ -352,6 +352,71 @@ int ckda_oracle_prep(const double *q_raw, const double *k_raw, const double *a_r
     return 0;
 }
 
+/*
+ * Backward of ckda_oracle_prep: from the raw inputs and the gradients of a
+ * loss with respect to the prepared q, k, alpha, beta, the gradients with
+ * respect to q_raw, k_raw, a_raw and b_raw, all fp64 (any pointer of the q
+ * side may be NULL together with q_raw).
+ *
+ * Normalisation (unit keys, paper Sec. 2; the same norm_eps as the forward):
+ *   k = x / n with n = sqrt(sum_i x_i^2 + norm_eps), so
+ *   dk_raw_j = sum_i dk_i dk_i/dx_j = (dk_j - k_j (k . dk)) / n.
+ * Gates ("Complex KDA" discussion slides, backup frame "practical gates differ
+ * from exact theoretical endpoints"):
+ *   alpha = s [e^-5 + (1 - e^-5) |r|], r = tanh(a / 2).  The sign s is
+ *   piecewise constant and carries no gradient; |r| takes the subgradient 0 at
+ *   r = 0.  For r != 0, s sign(r) = 1 and d|r|/da = sign(r) (1 - r^2) / 2, so
+ *   dalpha/da = (1 - e^-5) (1 - r^2) / 2, and 0 at r = 0.
+ *   beta = 2 sigma(b), so dbeta/db = 2 sigma(b) (1 - sigma(b)).
+ */
+int ckda_oracle_prep_bwd(const double *q_raw, const double *k_raw, const double *a_raw,
+                         const double *b_raw, const double *dq, const double *dk,
+                         const double *dalpha, const double *dbeta, double *dq_raw,
+                         double *dk_raw, double *da_raw, double *db_raw, long rows, int n,
+                         int normalize_q, double norm_eps)
+{
+    if (!k_raw || !a_raw || !b_raw || !dk || !dalpha || !dbeta) return -1;
+    if (!dk_raw || !da_raw || !db_raw) return -1;
+    if ((q_raw == NULL) != (dq == NULL) || (q_raw == NULL) != (dq_raw == NULL)) return -1;
+    if (rows < 0 || n < 1) return -1;
+    const double eps = exp(-5.0);
+    for (long t = 0; t < rows; ++t) {
+        const size_t o = (size_t)t * n;
+        /* keys */
+        double ss = 0.0;
+        for (int i = 0; i < n; ++i) ss += k_raw[o + i] * k_raw[o + i];
+        double nrm = sqrt(ss + norm_eps);
+        double dot = 0.0;
+        for (int i = 0; i < n; ++i) dot += (k_raw[o + i] / nrm) * dk[o + i];
+        for (int i = 0; i < n; ++i)
+            dk_raw[o + i] = (dk[o + i] - (k_raw[o + i] / nrm) * dot) / nrm;
+        /* queries */
+        if (q_raw) {
+            if (normalize_q) {
+                double sq = 0.0;
+                for (int i = 0; i < n; ++i) sq += q_raw[o + i] * q_raw[o + i];
+                double qn = sqrt(sq + norm_eps);
+                double qd = 0.0;
+                for (int i = 0; i < n; ++i) qd += (q_raw[o + i] / qn) * dq[o + i];
+                for (int i = 0; i < n; ++i)
+                    dq_raw[o + i] = (dq[o + i] - (q_raw[o + i] / qn) * qd) / qn;
+            } else {
+                for (int i = 0; i < n; ++i) dq_raw[o + i] = dq[o + i];
+            }
+        }
+        /* decay gate */
+        for (int i = 0; i < n; ++i) {
+            double r = tanh(a_raw[o + i] / 2.0);
+            double g = r == 0.0 ? 0.0 : (1.0 - eps) * (1.0 - r * r) / 2.0;
+            da_raw[o + i] = dalpha[o + i] * g;
+        }
+        /* write strength */
+        double sg = 1.0 / (1.0 + exp(-b_raw[t]));
+        db_raw[t] = dbeta[t] * 2.0 * sg * (1.0 - sg);
+    }
+    return 0;
+}
+
 /* Number of OpenMP threads a parallel region would use (1 without OpenMP). */
 int ckda_oracle_max_threads(void)
 {

@@ -164,6 +164,32 @@ def test_prep_argument_errors_are_synchronous(L):
     assert f(rows=0, k_raw=None, beta=None) == 0
 
 
+def test_prep_bwd_argument_errors_are_synchronous(L):
+    vp = ctypes.c_void_p
+    names = ("q_raw", "k_raw", "a_raw", "b_raw", "d_q", "d_k", "d_alpha", "d_beta", "d_q_raw",
+             "d_k_raw", "d_a_raw", "d_b_raw")
+    L.ckda_prep_bwd.argtypes = [vp] * 12 + [ctypes.c_longlong, ctypes.c_int, ctypes.c_int,
+                                            ctypes.c_int, ctypes.c_float, vp]
+    f = lambda **kw: L.ckda_prep_bwd(*(vp(kw.get(n, 16)) for n in names), kw.get("rows", 4),
+                                     kw.get("dk", 128), kw.get("io", 1), 1,
+                                     ctypes.c_float(kw.get("eps", 1e-6)), vp(None))
+    assert f(k_raw=None) == 1
+    assert f(d_beta=None) == 1
+    assert f(d_a_raw=None) == 1
+    assert f(d_q=None) == 1          # q_raw given without d_q
+    assert f(d_q_raw=None) == 1      # ... or without d_q_raw
+    assert f(rows=-1) == 1
+    assert f(dk=0) == 1
+    assert f(dk=129) == 2
+    assert f(io=3) == 1
+    assert f(eps=-1.0) == 1
+    assert f(eps=float("nan")) == 1
+    # no rows: nothing to do, nothing launched
+    assert f(rows=0, k_raw=None, d_b_raw=None) == 0
+    # no query at all is valid (and with no rows launches nothing)
+    assert f(rows=0, q_raw=None, d_q=None, d_q_raw=None) == 0
+
+
 def test_fwd_host_argument_errors_are_synchronous(L):
     """ckda_fwd_host rejects bad arguments, slices and scratch before any copy."""
     vp = ctypes.c_void_p

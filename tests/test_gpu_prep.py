@@ -1,5 +1,5 @@
-"""GPU parity of ckda_prep (C ABI) against the fp64 oracle, and the forward
-run on prepared inputs.
+"""GPU parity of ckda_prep and its backward ckda_prep_bwd (C ABI) against
+the fp64 oracle, and the forward run on prepared inputs.
 
 The kernel computes in fp32 and rounds once to the I/O dtype; the oracle
 computes in fp64.  bf16 outputs must lie within one bf16 ulp of the exact
@@ -118,3 +118,75 @@ def test_prep_then_forward_matches_oracle(ck):
     rq, rk, ra, rb = oracle.prep(k, a, b, q_raw=q)
     assert_close(ko.reshape(-1, d), rk, "bf16", "k")
     assert_close(ao.reshape(-1, d), ra, "bf16", "alpha")
+
+
+# ------------------------------------------------------------------ backward
+# ckda_prep_bwd against the oracle's prep_bwd on the same raw inputs and
+# upstream gradients.  The key and query gradients are differences of fp32
+# terms, (g - k (k . g)) / n, so they are judged on norms: the error a bf16
+# output carries beyond its own rounding, over the rms of the exact result,
+# must stay below 1e-4 (fp32 arithmetic gives about 1e-6); fp32 outputs take
+# max |err| / rms <= 1e-5.
+
+def upstream(rows, dk, dtype, seed):
+    g = torch.Generator().manual_seed(seed)
+    dq, dk_, da = (torch.randn((rows, dk), generator=g) for _ in range(3))
+    db = torch.randn((rows,), generator=g)
+    dt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    return tuple(t.to(dt) for t in (dq, dk_, da, db))
+
+
+def assert_grad(gpu, ref, dtype, name):
+    g = gpu.detach().cpu()
+    assert torch.isfinite(g.float()).all(), name
+    if dtype == "bf16":
+        e = excess_bf16(g, ref)
+        assert e <= 1e-4, (name, e)
+    else:
+        e = max_rel(g, ref)
+        assert e <= 1e-5, (name, e)
+
+
+@pytest.mark.parametrize("dtype,dk", [("bf16", 128), ("bf16", 64), ("bf16", 80), ("fp32", 128),
+                                      ("fp32", 16)])
+@pytest.mark.parametrize("normalize_q", [True, False])
+def test_prep_bwd_matches_oracle(ck, dtype, dk, normalize_q):
+    q, k, a, b = raw_inputs(1000, dk, dtype, seed=dk + 3 * normalize_q, special=True)
+    dq, dkk, da, db = upstream(1000, dk, dtype, seed=dk + 5)
+    got = ck.prep_bwd(k.cuda(), a.cuda(), b.cuda(), dkk.cuda(), da.cuda(), db.cuda(),
+                      q_raw=q.cuda(), d_q=dq.cuda(), normalize_q=normalize_q)
+    torch.cuda.synchronize()
+    ref = oracle.prep_bwd(k, a, b, dkk, da, db, q_raw=q, dq=dq, normalize_q=normalize_q)
+    for name, x, r in zip(("d_q_raw", "d_k_raw", "d_a_raw", "d_b_raw"), got, ref):
+        assert_grad(x, r, dtype, name)
+    # a = 0 and -0 take the subgradient 0; an unnormalised q passes d_q through
+    assert float(got[2][0, 0]) == 0.0 and float(got[2][0, 1]) == 0.0
+    if not normalize_q:
+        assert torch.equal(got[0].cpu(), dq)
+
+
+def test_prep_bwd_without_query_and_in_place(ck):
+    _, k, a, b = raw_inputs(333, 128, "bf16", seed=31)
+    _, dkk, da, db = upstream(333, 128, "bf16", seed=32)
+    ref = oracle.prep_bwd(k, a, b, dkk, da, db)
+    kd, ad, bd = k.cuda(), a.cuda(), b.cuda()
+    gk, ga, gb = dkk.cuda(), da.cuda(), db.cuda()
+    out = ck.prep_bwd(kd, ad, bd, gk, ga, gb, out=(None, gk, ad, gb))
+    torch.cuda.synchronize()
+    assert out[0] is None and out[1].data_ptr() == gk.data_ptr()
+    for name, x, r in zip(("d_k_raw", "d_a_raw", "d_b_raw"), (gk, ad, gb), ref[1:]):
+        assert_grad(x, r, "bf16", name)
+
+
+def test_prep_bwd_workload_full(ck):
+    """The benchmark's shape: raw inputs of the full-CKDA workload, 1,048,576
+    rows of dk = 128 in bf16, with q normalised."""
+    rows, dk = 4 * 32 * 8192, 128
+    q, k, a, b = raw_inputs(rows, dk, "bf16", seed=33)
+    dq, dkk, da, db = upstream(rows, dk, "bf16", seed=34)
+    got = ck.prep_bwd(k.cuda(), a.cuda(), b.cuda(), dkk.cuda(), da.cuda(), db.cuda(),
+                      q_raw=q.cuda(), d_q=dq.cuda())
+    torch.cuda.synchronize()
+    ref = oracle.prep_bwd(k, a, b, dkk, da, db, q_raw=q, dq=dq)
+    for name, x, r in zip(("d_q_raw", "d_k_raw", "d_a_raw", "d_b_raw"), got, ref):
+        assert_grad(x, r, "bf16", name)

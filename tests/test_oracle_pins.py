@@ -704,3 +704,87 @@ def test_bwd_closed_form_without_writes_or_decay():
     np.testing.assert_array_equal(dvv, 0.0)
     want = dhT[0, 0] + s * sum(np.outer(q[0, 0, t], do[0, 0, t]) for t in range(T))
     np.testing.assert_allclose(dh0[0, 0], want, rtol=1e-12)
+
+
+# ------------------------------------------------------- input prep backward
+# The gradients of prep's outputs with respect to its raw inputs.  Pinned by
+# central differences of prep itself (pinned above), away from a = 0 where
+# the gate's sign jumps; at a = 0 by the reading that the sign carries no
+# gradient and |tanh(a/2)| takes the subgradient 0.
+
+def _prep_loss(w, q_raw, k_raw, a_raw, b_raw, normalize_q, norm_eps):
+    """L = <wq, q> + <wk, k> + <wa, alpha> + <wb, beta> of prep's outputs."""
+    q, k, alpha, beta = oracle.prep(k_raw, a_raw, b_raw, q_raw=q_raw,
+                                    normalize_q=normalize_q, norm_eps=norm_eps)
+    wq, wk, wa, wb = w
+    return float(np.sum(wq * q) + np.sum(wk * k) + np.sum(wa * alpha) + np.sum(wb * beta))
+
+
+@pytest.mark.parametrize("normalize_q,norm_eps", [(True, 1e-6), (True, 0.0), (False, 1e-3)])
+def test_prep_bwd_central_differences(normalize_q, norm_eps):
+    rng = np.random.default_rng(60)
+    R, n = 4, 6
+    q_raw = rng.normal(0.0, 1.0, (R, n)) * rng.uniform(0.2, 5.0, (R, 1))
+    k_raw = rng.normal(0.0, 1.0, (R, n)) * rng.uniform(0.2, 5.0, (R, 1))
+    a_raw = rng.normal(0.0, 2.0, (R, n))
+    a_raw = np.where(np.abs(a_raw) < 0.05, 0.3, a_raw)     # the sign is constant nearby
+    b_raw = rng.normal(0.0, 2.0, R)
+    w = (rng.normal(size=(R, n)), rng.normal(size=(R, n)), rng.normal(size=(R, n)),
+         rng.normal(size=R))
+    dq_raw, dk_raw, da_raw, db_raw = oracle.prep_bwd(
+        k_raw, a_raw, b_raw, w[1], w[2], w[3], q_raw=q_raw, dq=w[0],
+        normalize_q=normalize_q, norm_eps=norm_eps)
+    args = [q_raw, k_raw, a_raw, b_raw]
+    for which, got in enumerate((dq_raw, dk_raw, da_raw, db_raw)):
+        x = args[which]
+        num = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            h = 1e-6 * max(1.0, abs(x[idx]))
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += h
+            xm[idx] -= h
+            ap, am = list(args), list(args)
+            ap[which], am[which] = xp, xm
+            num[idx] = (_prep_loss(w, *ap, normalize_q, norm_eps)
+                        - _prep_loss(w, *am, normalize_q, norm_eps)) / (2 * h)
+        np.testing.assert_allclose(got, num, rtol=1e-6, atol=1e-8, err_msg=str(which))
+
+
+def test_prep_bwd_gate_at_zero_and_closed_forms():
+    """At a = 0 the gate gradient is 0 (sign detached, subgradient 0 of |r|);
+    next to 0 it is (1 - e^-5)/2 from either side, as the one-sided
+    differences give; dbeta/db = 1/2 at b = 0 and vanishes without NaN for
+    huge |b|."""
+    eps = math.exp(-5.0)
+    a = np.array([[0.0, -0.0, 1e-4, -1e-4]])
+    k = np.ones_like(a)
+    ones = np.ones_like(a)
+    _, _, da, db = oracle.prep_bwd(k, a, np.array([0.0]), np.zeros_like(a), ones,
+                                   np.array([1.0]))
+    assert da[0, 0] == 0.0 and da[0, 1] == 0.0
+    assert db[0] == 0.5
+    # one-sided differences on each side of 0 (where s is constant)
+    for x0, g in ((1e-4, da[0, 2]), (-1e-4, da[0, 3])):
+        h = 1e-7
+        _, _, ap, _ = oracle.prep(np.ones((1, 1)), np.array([[x0 + h]]), np.zeros(1))
+        _, _, am, _ = oracle.prep(np.ones((1, 1)), np.array([[x0 - h]]), np.zeros(1))
+        assert g == pytest.approx((ap[0, 0] - am[0, 0]) / (2 * h), rel=1e-7)
+        assert g == pytest.approx((1.0 - eps) / 2.0, rel=1e-7)
+    _, _, _, db = oracle.prep_bwd(np.ones((2, 1)), np.ones((2, 1)), np.array([800.0, -800.0]),
+                                  np.zeros((2, 1)), np.zeros((2, 1)), np.ones(2))
+    assert np.all(np.isfinite(db)) and np.all(np.abs(db) < 1e-300)
+
+
+def test_prep_bwd_invariances():
+    """k / |k| is scale-invariant, so with norm_eps = 0 the key gradient is
+    orthogonal to the raw key; an unnormalised q passes its gradient through."""
+    rng = np.random.default_rng(61)
+    k = rng.normal(size=(7, 16)) * 3.0
+    q = rng.normal(size=(7, 16))
+    dk = rng.normal(size=(7, 16))
+    dq = rng.normal(size=(7, 16))
+    z = np.zeros((7, 16))
+    dq_raw, dk_raw, _, _ = oracle.prep_bwd(k, z, np.zeros(7), dk, z, np.zeros(7), q_raw=q, dq=dq,
+                                           normalize_q=False, norm_eps=0.0)
+    np.testing.assert_allclose(np.sum(dk_raw * k, axis=1), 0.0, atol=1e-13)
+    np.testing.assert_array_equal(dq_raw, dq)
