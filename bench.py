@@ -300,6 +300,47 @@ def fig5_sweep(ck, steps, ws, stream):
     return out
 
 
+def varlen_split_case(ck, steps, ws, stream):
+    """One 32k-token sequence packed with 63 of 1k tokens (16 heads, d = 128,
+    KDA gates, h0): ckda_fwd on the packed input, where the long sequence's
+    16 heads run 512 chunks each while the short ones finish early, against
+    ckda_fwd_split_varlen at its automatic segment length."""
+    import torch
+    import synth
+    lengths = [1024] * 31 + [32768] + [1024] * 32
+    x = synth.make_varlen(lengths, 16, 128, dist="kda", dtype="bf16", h0=True, seed=54)
+    name = "varlen_long_tail"
+    plain = fwd_case(ck, x, steps, 3, ws, stream, name)
+    d = plain["dev"]
+    B, H, T, dk = d.q.shape
+    N = d.num_seqs
+    sl = ck.split_varlen_seg_len(N, H, T, dk, 128)
+    wsp = torch.empty(ck.split_varlen_workspace_bytes(N, H, T, dk, sl), dtype=torch.uint8,
+                      device="cuda")
+    o, hT = plain["o"], plain["hT"]
+
+    def step():
+        ck.fwd_split_varlen(d.q, d.k, d.v, d.alpha, d.beta, d.cu_seqlens, h0=d.h0, seg_len=sl,
+                            o=o, hT=hT, workspace=wsp, stream=stream)
+
+    step()
+    st = ck.fwd_status(wsp)
+    if st != 0:
+        raise RuntimeError(f"{name} split: device status {ck.STATUS.get(st, st)}")
+    total, per = time_steps(step, steps, 3, ws, stream)
+    out = {"config": {"lengths": "31 x 1024, 32768, 32 x 1024", "H": H, "d": dk, "h0": True,
+                      "dist": "kda", "T": T}}
+    for key, tot, pr, launches in (("plain", plain["total"], plain["per"], plain["launches"]),
+                                   ("split", total, per, 5)):
+        r = roofline(plain["bytes"], pr, "fwd", name)
+        r["traffic"] = None
+        out[key] = {"value": round(plain["th"] * steps / tot, 1), "unit": UNIT,
+                    "ms_per_step": round(tot / steps * 1e3, 4), "launches_per_step": launches,
+                    "roofline": r}
+    out["split"]["seg_len"] = sl
+    return out
+
+
 def roofline(nbytes, per_ms, kernel, workload):
     peak, src = hbm_peak()
     mean_s = sum(per_ms) / len(per_ms) / 1e3
@@ -590,6 +631,8 @@ def run_ours(args):
                       "roofline": roofline(rr["bytes"], rr["per"], fwd_kernel(xx.q.shape[-1]), nm)}
             del xx, rr
         out["workloads"] = wl
+    if ws == 1 and "varlen_split" in extras:
+        out["varlen_split"] = varlen_split_case(ck, 20, ws, stream)
     if ws == 1 and "fig5_sweep" in extras:
         # 32k tokens per step of 16 heads at B x T = 16 x 2k .. 1 x 32k: one pass fills
         # B x 16 SMs; the split runs the long sequences as segments
@@ -667,8 +710,9 @@ def main():
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--extras",
                     default="decode,decode_raw,prep,prep_bwd,bwd,kda_range,ckda_varlen,"
-                            "kda_range_dk64,fig5_sweep",
+                            "kda_range_dk64,fig5_sweep,varlen_split",
                     help="comma list of extra measurements: decode, decode_raw, prep, prep_bwd, bwd, "
+                         "varlen_split, "
                          "kda_range, ckda_full, ckda_varlen, kda_range_dk64, fig5_sweep")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--bwd-units", type=int, default=0,

@@ -86,6 +86,12 @@ def lib():
             L.ckda_prep.restype = i32
             L.ckda_prep.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_longlong, i32, i32,
                                     i32, f32, vp]
+            L.ckda_fwd_split_varlen_seg_len.restype = i32
+            L.ckda_fwd_split_varlen_seg_len.argtypes = [i32] * 7
+            L.ckda_fwd_split_varlen_workspace_bytes.restype = sz
+            L.ckda_fwd_split_varlen_workspace_bytes.argtypes = [i32] * 5
+            L.ckda_fwd_split_varlen.restype = i32
+            L.ckda_fwd_split_varlen.argtypes = [vp] * 9 + [i32] * 6 + [f32, i32, vp, sz, vp]
             L.ckda_prep_bwd.restype = i32
             L.ckda_prep_bwd.argtypes = [vp] * 12 + [ctypes.c_longlong, i32, i32, i32, f32, vp]
             L.ckda_fwd_host.restype = i32
@@ -229,6 +235,63 @@ def fwd_split(q, k, v, alpha, beta, h0=None, scale=1.0, segments=0, store_final_
     if rc != 0:
         raise CkdaError(rc, "ckda_fwd_split")
     fwd_split.last_workspace = workspace
+    return o, hT
+
+
+def split_varlen_seg_len(num_seqs, H, T, dk, dv, dtype=torch.bfloat16, num_sms=0) -> int:
+    """Segment length ckda_fwd_split_varlen picks for `seg_len=0`."""
+    io = _BF16 if dtype == torch.bfloat16 else _F32
+    return int(lib().ckda_fwd_split_varlen_seg_len(num_seqs, H, T, dk, dv, io, int(num_sms)))
+
+
+def split_varlen_workspace_bytes(num_seqs, H, T, dk, seg_len) -> int:
+    return int(lib().ckda_fwd_split_varlen_workspace_bytes(num_seqs, H, T, dk, int(seg_len)))
+
+
+def fwd_split_varlen(q, k, v, alpha, beta, cu_seqlens, h0=None, scale=1.0, seg_len=0,
+                     store_final_state=True, o=None, hT=None, workspace=None, stream=None):
+    """ckda_fwd_split_varlen: the packed forward with every sequence longer
+    than seg_len cut into segments run in parallel.  q, k, alpha, v are
+    [1, H, T, d], beta [1, H, T], cu_seqlens int32 [N + 1] on the device.
+    Returns (o, hT [N, H, dk, dv] or None)."""
+    L = lib()
+    device = q.device
+    B, H, T, dk = q.shape
+    if B != 1:
+        raise ValueError("fwd_split_varlen: packed input has B = 1")
+    dv = v.shape[-1]
+    dt = q.dtype
+    io = _io_dtype(q)
+    for name, t, shp in (("q", q, (1, H, T, dk)), ("k", k, (1, H, T, dk)),
+                         ("alpha", alpha, (1, H, T, dk)), ("v", v, (1, H, T, dv)),
+                         ("beta", beta, (1, H, T))):
+        _check(t, name, dt, shp, device)
+    if cu_seqlens.dtype != torch.int32 or cu_seqlens.device != device or cu_seqlens.dim() != 1:
+        raise ValueError("fwd_split_varlen: cu_seqlens must be int32 [N + 1] on the device")
+    N = cu_seqlens.numel() - 1
+    if h0 is not None:
+        _check(h0, "h0", torch.float32, (N, H, dk, dv), device)
+    if o is None:
+        o = torch.empty((1, H, T, dv), dtype=dt, device=device)
+    else:
+        _check(o, "o", dt, (1, H, T, dv), device)
+    if store_final_state and hT is None:
+        hT = torch.empty((N, H, dk, dv), dtype=torch.float32, device=device)
+    if hT is not None:
+        _check(hT, "hT", torch.float32, (N, H, dk, dv), device)
+    with torch.cuda.device(device):
+        if seg_len == 0:
+            seg_len = int(L.ckda_fwd_split_varlen_seg_len(N, H, T, dk, dv, io, 0))
+        if workspace is None:
+            n = int(L.ckda_fwd_split_varlen_workspace_bytes(N, H, T, dk, int(seg_len)))
+            workspace = torch.empty(max(n, 256), dtype=torch.uint8, device=device)
+        rc = L.ckda_fwd_split_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(h0),
+                                     _ptr(o), _ptr(hT), _ptr(cu_seqlens), N, H, T, dk, dv, io,
+                                     float(scale), int(seg_len), _ptr(workspace),
+                                     int(workspace.numel()), _stream_handle(stream, device))
+    if rc != 0:
+        raise CkdaError(rc, "ckda_fwd_split_varlen")
+    fwd_split_varlen.last_workspace = workspace
     return o, hT
 
 

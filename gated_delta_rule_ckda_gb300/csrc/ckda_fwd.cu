@@ -224,6 +224,39 @@ __device__ __forceinline__ float cta4_read(const float* slot) {
   return fmaxf(fmaxf(slot[0], slot[1]), fmaxf(slot[2], slot[3]));
 }
 
+// The segment role r of a sequence cut into S segments, in split pass 1 or 2
+// (see ckda_split.cu): its segment, its initial and final state (slot(x) is
+// the seg_state / seg_P / seg_F tile of segment x), and its flags.  h0 and
+// hT are the sequence's own (or null).
+template <typename SlotFn>
+__device__ __forceinline__ int split_role(Unit& u, const FwdArgs& a, int S, int r, SlotFn slot,
+                                          const float* h0, float* hT) {
+  int seg;
+  u.h0 = nullptr;
+  u.hT = nullptr;
+  if (a.split_pass == 1) {
+    u.write_o = r == 0;
+    if (r == 0) {             // segment 0 from h0; its final state enters segment 1
+      seg = 0;
+      u.h0 = h0;
+      u.hT = S == 1 ? hT : a.seg_state + slot(1);
+    } else if (r <= S - 2) {  // final state of segment r from zero
+      seg = r;
+      u.hT = a.seg_F + slot(seg);
+    } else {                  // transition of segment r - (S - 2): from [I | 0], v = 0
+      seg = r - (S - 2);
+      u.ident = true;
+      u.zero_v = true;
+      u.hT = a.seg_P + slot(seg);
+    }
+  } else {
+    seg = 1 + r;
+    u.h0 = a.seg_state + slot(seg);
+    u.hT = seg == S - 1 ? hT : nullptr;
+  }
+  return seg;
+}
+
 template <int DK, bool SPLIT>
 __device__ __forceinline__ Unit unit_of(const FwdArgs& a) {
   Unit u;
@@ -232,36 +265,45 @@ __device__ __forceinline__ Unit unit_of(const FwdArgs& a) {
   u.zero_v = false;
   u.write_o = true;
   if constexpr (SPLIT) {
-    // dense layout; CTA b is (sequence, head) ui, role r of its pass
-    const int S = a.nseg;
-    const int per = split_ctas_per_unit(a.split_pass, S);
-    const int ui = (int)blockIdx.x / per, r = (int)blockIdx.x % per;
-    const size_t slot0 = (size_t)ui * S;
-    int seg;
-    u.h0 = nullptr;
-    u.hT = nullptr;
-    if (a.split_pass == 1) {
-      u.write_o = r == 0;
-      if (r == 0) {             // segment 0 from h0; its final state enters segment 1
-        seg = 0;
-        u.h0 = a.h0 ? a.h0 + (size_t)ui * tile : nullptr;
-        u.hT = a.seg_state + (slot0 + 1) * tile;
-      } else if (r <= S - 2) {  // final state of segment r from zero
-        seg = r;
-        u.hT = a.seg_F + (slot0 + seg) * tile;
-      } else {                  // transition of segment r - (S - 2): from [I | 0], v = 0
-        seg = r - (S - 2);
-        u.ident = true;
-        u.zero_v = true;
-        u.hT = a.seg_P + (slot0 + seg) * tile;
+    if (a.split_plan) {
+      // packed: CTA b is (work item w, head h); the plan gives the i-th
+      // longest sequence its segment count S[i], its first state slot and its
+      // first work item in each pass
+      const int N = a.num_units_seq, H = a.H;
+      const int32_t* Sn = a.split_plan;
+      const int32_t* slot0 = Sn + N;
+      const int32_t* off = Sn + N + (N + 1) * (a.split_pass == 1 ? 1 : 2);
+      const int h = (int)blockIdx.x % H, w = (int)blockIdx.x / H;
+      if (w >= off[N]) {   // beyond the plan's work
+        u.len = -1;
+        return u;
       }
+      int lo = 0, hi = N;  // the sequence with off[i] <= w < off[i + 1]
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (off[mid] <= w) lo = mid; else hi = mid;
+      }
+      const int i = lo, S = Sn[i];
+      const int n = a.order ? a.order[i] : i;   // the plan runs over the longest-first order
+      const int t0 = a.cu_seqlens[n], L = a.cu_seqlens[n + 1] - t0;
+      const size_t own = ((size_t)n * H + h) * tile;
+      const int seg = split_role(
+          u, a, S, w - off[i], [&](int x) { return ((size_t)(slot0[i] + x) * H + h) * tile; },
+          a.h0 ? a.h0 + own : nullptr, a.hT ? a.hT + own : nullptr);
+      u.row0 = (long)h * a.T + t0 + (long)seg * a.seg_len;
+      u.len = max(0, min(a.seg_len, L - seg * a.seg_len));
     } else {
-      seg = 1 + r;
-      u.h0 = a.seg_state + (slot0 + seg) * tile;
-      u.hT = (seg == S - 1 && a.hT) ? a.hT + (size_t)ui * tile : nullptr;
+      // dense layout; CTA b is (sequence, head) ui, role r of its pass
+      const int S = a.nseg;
+      const int per = split_ctas_per_unit(a.split_pass, S);
+      const int ui = (int)blockIdx.x / per, r = (int)blockIdx.x % per;
+      const size_t slot0 = (size_t)ui * S;
+      const int seg = split_role(
+          u, a, S, r, [&](int x) { return (slot0 + x) * tile; },
+          a.h0 ? a.h0 + (size_t)ui * tile : nullptr, a.hT ? a.hT + (size_t)ui * tile : nullptr);
+      u.row0 = (long)ui * a.T + (long)seg * a.seg_len;
+      u.len = min(a.seg_len, a.T - seg * a.seg_len);
     }
-    u.row0 = (long)ui * a.T + (long)seg * a.seg_len;
-    u.len = min(a.seg_len, a.T - seg * a.seg_len);
   } else {
     const int b = blockIdx.x;
     const int h = b % a.H;
@@ -841,6 +883,7 @@ __global__ void __launch_bounds__(NT, 1)
 
   static_assert(DK == 128 || DK == 64, "key width");
   const Unit u = unit_of<DK, SPLIT>(a);
+  if (SPLIT && u.len < 0) return;          // a packed split's spare CTA (uniform)
   const bool zero_v = SPLIT && u.zero_v;   // no v tile is read: U~ = 0
   const int nchunks = (u.len + C - 1) / C;
 
@@ -913,10 +956,9 @@ __global__ void __launch_bounds__(NT, 1)
       for (int b = 0; b < 8; ++b) T8[b] = tot_s[b * 32 + lane];
       write_round_c(sm, B, T8, blk, lane);
       warp_publish(bars + B_OPS_C, lane);
-      // gamma_C (fp32: it scales the fp32 state); k*gamma (bf16) once the
-      // inverse warps have finished chunk c-1's W; q*gamma and k*rho (rho_s =
-      // exclusive suffix times later blocks' totals) stay in registers until
-      // the state has released their tiles
+      // gamma_C (fp32: it scales the fp32 state); k*gamma (bf16), q*gamma and
+      // k*rho (rho_s = exclusive suffix times later blocks' totals) stay in
+      // registers until their tiles are free
       if (blk == 0) {
         float4 g = T8[0];
 #pragma unroll
@@ -925,8 +967,8 @@ __global__ void __launch_bounds__(NT, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(bars + B_GAM + (c & 1));
       }
-      if (c > 0) ok = ok && mbar_wait(bars + B_KGFREE, (uint32_t)((c - 1) & 1));
       H4 gq[8], kr[8];
+      uint2 kgb[8];
       {
         float4 Gb = make_float4(1.f, 1.f, 1.f, 1.f), Ga = Gb;
 #pragma unroll
@@ -935,14 +977,12 @@ __global__ void __launch_bounds__(NT, 1)
           if (b > blk) { Ga.x *= T8[b].x; Ga.y *= T8[b].y; Ga.z *= T8[b].z; Ga.w *= T8[b].w; }
         }
         H4 g = h4_of(Gb);
-        const uint32_t tb = quad_tb<64>(lane);
 #pragma unroll
         for (int r = 0; r < 8; ++r) {
           g = mul4(g, B.a[r]);
           const H4 kg = mul4(B.k[r], g);
           const float2 k0 = __half22float2(kg.p[0]), k1 = __half22float2(kg.p[1]);
-          *reinterpret_cast<uint2*>(sm + S_KG + quad_at(tb, (uint32_t)(8 * blk + r))) =
-              make_uint2(pack_bf162(k0.x, k0.y), pack_bf162(k1.x, k1.y));
+          kgb[r] = make_uint2(pack_bf162(k0.x, k0.y), pack_bf162(k1.x, k1.y));
           gq[r] = mul4(B.q[r], g);
         }
         H4 rr = h4_of(Ga);
@@ -967,6 +1007,15 @@ __global__ void __launch_bounds__(NT, 1)
       ok = ok && mbar_wait(bars + B_DONE_C, (uint32_t)(c & 1));
       tc_fence_after();
       readout_c(sm, slot, tmem, wq, hc, lane, beta_c);
+      // k*gamma (bf16), once the inverse warps have finished chunk c-1's -W
+      // (late in the chunk, so that the prep warps rarely wait for it)
+      if (c > 0) ok = ok && mbar_wait(bars + B_KGFREE, (uint32_t)((c - 1) & 1));
+      {
+        const uint32_t tb = quad_tb<64>(lane);
+#pragma unroll
+        for (int r = 0; r < 8; ++r)
+          *reinterpret_cast<uint2*>(sm + S_KG + quad_at(tb, (uint32_t)(8 * blk + r))) = kgb[r];
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bars + B_MREADY + slot);
@@ -1469,9 +1518,12 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t s) {
-  const long long grid = a.split_pass
-                             ? (long long)a.B * a.H * split_ctas_per_unit(a.split_pass, a.nseg)
-                             : (long long)a.num_units_seq * a.H;
+  // (a packed split launches split_items work items per head, an upper bound
+  // on its plan's; the spare CTAs return at once)
+  const long long grid =
+      !a.split_pass ? (long long)a.num_units_seq * a.H
+      : a.split_plan ? (long long)a.split_items * a.H
+                     : (long long)a.B * a.H * split_ctas_per_unit(a.split_pass, a.nseg);
   if (grid == 0) return cudaSuccess;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
   const uint64_t rows = (uint64_t)a.B * a.H * a.T;

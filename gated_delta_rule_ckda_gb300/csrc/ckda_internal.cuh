@@ -46,6 +46,13 @@ struct FwdArgs {
   float* seg_state;
   float* seg_P;
   float* seg_F;
+  // Packed split (cu_seqlens set): the plan in the workspace, int32
+  // S[N] (segments of each sequence, >= 1), slot0[N + 1] (its first state
+  // slot; slot x of head h is tile (slot0[i] + x) * H + h), off1[N + 1] and
+  // off2[N + 1] (its first work item in pass 1 and 2), and the number of
+  // work items per head this pass launches (an upper bound on off[N]).
+  const int32_t* split_plan;
+  int split_items;
 };
 
 // Shapes the chunkwise tensor-core kernel takes: bf16 I/O, dv = 128 and
@@ -67,9 +74,14 @@ __host__ __device__ inline int split_ctas_per_unit(int pass, int nseg) {
   return pass == 1 ? (nseg >= 3 ? 2 * nseg - 3 : 1) : nseg - 1;
 }
 // The scan between the passes: seg_state[s + 1] = seg_P[s] seg_state[s] +
-// seg_F[s] for s = 1..nseg-2, per (sequence, head).
+// seg_F[s] for s = 1..nseg-2, per (sequence, head); with a packed split's
+// plan, per (sequence i, head) over its own S[i] segments.
 cudaError_t launch_seg_scan(float* state, const float* P, const float* F, int units, int nseg,
-                            int dk, cudaStream_t s);
+                            int dk, cudaStream_t s, const int32_t* plan = nullptr, int N = 0,
+                            int H = 0);
+// The packed split's plan (see FwdArgs::split_plan) from cu_seqlens.
+cudaError_t launch_split_plan(const int32_t* cu, const int32_t* order, int N, int seg_len,
+                              int32_t* plan, cudaStream_t s);
 // Longest-first order of packed sequences.
 cudaError_t launch_seq_order(const int32_t* cu, int n, int32_t* order, cudaStream_t s);
 

@@ -242,6 +242,36 @@ ckda_status ckda_fwd_split(const void *q, const void *k, const void *v,
                            void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * The sequence split for packed input: ckda_fwd with cu_seqlens (same
+ * layouts: q, k, alpha [1, H, T, dk], v, o [1, H, T, dv], beta [1, H, T],
+ * h0, hT fp32 [num_seqs, H, dk, dv], cu_seqlens device int32 [num_seqs + 1],
+ * monotone from 0 to T), where every sequence longer than seg_len tokens is
+ * cut into ceil(L / seg_len) segments that run in parallel, chained by the
+ * scan of ckda_fwd_split; shorter sequences run whole in the first pass.
+ * Sequences are planned longest first on the device, so the host needs no
+ * lengths and nothing is synchronised.  Each launch covers an upper bound on
+ * the plan's work; CTAs beyond it return at once.
+ *
+ * seg_len: a positive multiple of 64, or 0 for ckda_fwd_split_varlen_seg_len's
+ * choice (the average work per SM; 0 from that function means the shape does
+ * not take the tensor-core path).  Bf16 with dv = 128 and dk = 128 or 64 only
+ * (CKDA_ERR_UNSUPPORTED otherwise).  The workspace (256-byte aligned) holds
+ * the status word, the order, the plan and three state tiles per segment
+ * slot: ckda_fwd_split_varlen_workspace_bytes.  Results equal ckda_fwd's up
+ * to rounding.  Returns once the five launches are enqueued on `stream`;
+ * device conditions are read with ckda_fwd_status.
+ */
+int ckda_fwd_split_varlen_seg_len(int num_seqs, int H, int T, int dk, int dv,
+                                  ckda_dtype io_dtype, int num_sms);
+size_t ckda_fwd_split_varlen_workspace_bytes(int num_seqs, int H, int T, int dk, int seg_len);
+ckda_status ckda_fwd_split_varlen(const void *q, const void *k, const void *v,
+                                  const void *alpha, const void *beta, const float *h0,
+                                  void *o, float *hT, const int32_t *cu_seqlens, int num_seqs,
+                                  int H, int T, int dk, int dv, ckda_dtype io_dtype, float scale,
+                                  int seg_len, void *workspace, size_t workspace_bytes,
+                                  void *stream);
+
+/*
  * Reads (and clears) the device status word of a workspace: waits for
  * `stream`, then returns CKDA_OK, CKDA_ERR_TIMEOUT or CKDA_ERR_RANGE for the
  * most recent ckda_fwd (or self-test) enqueued with that workspace.

@@ -314,3 +314,56 @@ def test_split_argument_errors_are_synchronous(L):
     assert f(ws=None) == 5
     assert f(wsb=need - 1) == 5
     assert f(ws=4096 + 16) == 5
+
+
+def test_split_varlen_workspace_and_segment_length(L):
+    """Workspace: status word and order (rounded to 256 B), the plan (4 N + 3
+    int32, rounded to 256 B), then three state tiles per segment slot, with
+    T // seg_len + 1 + N slots (an upper bound on sum_i max(1, ceil(L_i /
+    seg_len)) for any lengths summing to T)."""
+    f = L.ckda_fwd_split_varlen_workspace_bytes
+    tile = 128 * 128 * 4
+    r256 = lambda x: (x + 255) // 256 * 256
+    for N, H, T, dk, sl in ((4, 2, 1000, 128, 256), (64, 16, 528000, 128, 4096),
+                            (1, 1, 0, 64, 64), (3, 5, 777, 64, 192)):
+        slots = T // sl + 1 + N
+        want = r256(256 + 4 * N) + r256(4 * (4 * N + 3)) + 3 * slots * H * tile * dk // 128
+        assert f(N, H, T, dk, sl) == want, (N, H, T, dk, sl)
+    assert f(4, 2, 1000, 128, 100) == 0      # not a multiple of 64
+    assert f(4, 2, 1000, 128, 0) == 0
+    assert f(0, 2, 1000, 128, 256) == 0
+    # automatic segment length: the average work per SM in chunk steps (at
+    # least 16 chunks), 0 off the tensor-core path
+    g = L.ckda_fwd_split_varlen_seg_len
+    for N, H, T in ((64, 16, 528000), (64, 16, 97280), (1, 1, 64), (8, 4, 100000)):
+        work = ((T + 63) // 64 + N) * H
+        assert g(N, H, T, 128, 128, 1, 152) == max(16, -(-work // 152)) * 64, (N, H, T)
+    assert g(4, 2, 1000, 128, 128, 0, 152) == 0     # fp32
+    assert g(4, 2, 1000, 96, 128, 1, 152) == 0      # dk 96
+    assert g(0, 2, 1000, 128, 128, 1, 152) == 0
+
+
+def test_split_varlen_argument_errors_are_synchronous(L):
+    vp = ctypes.c_void_p
+    N, H, T, d = 3, 2, 1000, 128
+    need = L.ckda_fwd_split_varlen_workspace_bytes(N, H, T, d, 256)
+
+    def f(**kw):
+        return L.ckda_fwd_split_varlen(
+            *(vp(kw.get(n, 16)) for n in ("q", "k", "v", "alpha", "beta")), vp(kw.get("h0")),
+            vp(kw.get("o", 16)), vp(kw.get("hT")), vp(kw.get("cu", 16)), kw.get("N", N),
+            kw.get("H", H), kw.get("T", T), kw.get("dk", d), kw.get("dv", d), kw.get("io", 1),
+            kw.get("scale", 1.0), kw.get("seg", 256), vp(kw.get("ws", 4096)), kw.get("wsb", need),
+            vp(None))
+    assert f(cu=None) == 1
+    assert f(N=0) == 1
+    assert f(seg=100) == 1                     # not a multiple of 64
+    assert f(seg=-64) == 1
+    assert f(q=None) == 1
+    assert f(q=16 + 2) == 1                    # TMA bases must be 16-byte aligned
+    assert f(scale=float("nan")) == 1
+    assert f(io=0) == 2                        # fp32: no tensor-core path
+    assert f(dk=96) == 2
+    assert f(ws=None) == 5
+    assert f(wsb=need - 1) == 5
+    assert f(ws=4096 + 16) == 5
