@@ -1,7 +1,7 @@
 // ckda_fwd.cu -- chunkwise CKDA forward on tcgen05 tensor cores (sm_103a),
-// dv = 128 and dk = 128 or 64, bf16 I/O, fp32 state.  A 64-wide key runs as
-// 128 channels whose last 64 have zero keys and queries and unit gates: their
-// state rows stay zero and add nothing.
+// dv = 128 and dk = 128 or 64, bf16 I/O, fp32 state.  A 64-wide key runs
+// natively: each half-warp holds the 64 channels of 4 tokens (load_block4),
+// the Gram rounds and the state step run at K = 64, the state at N = 64.
 //
 // One CTA owns one (sequence, head) and walks its tokens in chunks of C = 64
 // with the fp32 state H^T (dv x dk = 128 x 128) resident in tensor memory.
@@ -373,22 +373,17 @@ __device__ __forceinline__ float4 bf4(uint2 w) {
   return make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u),
                      __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
 }
-// With pad set (the lanes of channels 64..127 of a 64-wide key) nothing is
-// read: k = q = 0 and alpha = 1.
 template <bool kMask>
 __device__ __forceinline__ void load_block(Blk8& B, const uint8_t* sm, int blk, int lane,
-                                           float scale, int live, bool pad) {
+                                           float scale, int live) {
   B.tot = make_float4(1.f, 1.f, 1.f, 1.f);
   const uint32_t tb = quad_tb<64>(lane);
 #pragma unroll
   for (int r = 0; r < 8; ++r) {
     const uint32_t off = quad_at(tb, (uint32_t)(8 * blk + r));
-    float4 kf = make_float4(0.f, 0.f, 0.f, 0.f), qf = kf, af = make_float4(1.f, 1.f, 1.f, 1.f);
-    if (!pad) {
-      kf = bf4(*reinterpret_cast<const uint2*>(sm + S_TK + off));
-      qf = bf4(*reinterpret_cast<const uint2*>(sm + S_TQ + off));
-      af = bf4(*reinterpret_cast<const uint2*>(sm + S_TA + off));
-    }
+    float4 kf = bf4(*reinterpret_cast<const uint2*>(sm + S_TK + off));
+    float4 qf = bf4(*reinterpret_cast<const uint2*>(sm + S_TQ + off));
+    float4 af = bf4(*reinterpret_cast<const uint2*>(sm + S_TA + off));
     qf.x *= scale; qf.y *= scale; qf.z *= scale; qf.w *= scale;
     if (kMask && r >= live) {
       kf = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -408,8 +403,8 @@ __device__ __forceinline__ void load_block(Blk8& B, const uint8_t* sm, int blk, 
 // running product of alpha from r0 times `pre`) or as lower tokens (Y rows
 // yr + l, l = l0 + j, gated by the exclusive running suffix product to
 // r0 + n - 1 times `post`).
-template <int R0, int N>
-__device__ __forceinline__ void put_upper(uint8_t* X, uint32_t tx, const Blk8& B, H4 f,
+template <int R0, int N, class BK>
+__device__ __forceinline__ void put_upper(uint8_t* X, uint32_t tx, const BK& B, H4 f,
                                           uint32_t xk, uint32_t xq) {
 #pragma unroll
   for (int j = 0; j < N; ++j) {
@@ -418,8 +413,8 @@ __device__ __forceinline__ void put_upper(uint8_t* X, uint32_t tx, const Blk8& B
     st_quad(X + quad_at(tx, xq + j), mul4(B.q[R0 + j], f));
   }
 }
-template <int R0, int N>
-__device__ __forceinline__ void put_lower(uint8_t* Y, uint32_t ty, const Blk8& B, H4 b,
+template <int R0, int N, class BK>
+__device__ __forceinline__ void put_lower(uint8_t* Y, uint32_t ty, const BK& B, H4 b,
                                           uint32_t yr) {
 #pragma unroll
   for (int j = N - 1; j >= 0; --j) {
@@ -485,6 +480,98 @@ __device__ __forceinline__ void write_round_c(uint8_t* sm, const Blk8& B, const 
   } else {
     const H4 b = loc == 0 ? h4_of(nb) : ones4();
     put_lower<0, 8>(Y, ty, B, b, 32u + 16u * (uint32_t)j + 8u * (uint32_t)loc);
+  }
+}
+
+// ------------------------------------------- 64-wide key: half-block mapping
+// Thread (warp w, lane l) owns channels 4 (l & 15) .. 4 (l & 15) + 3 (all 64
+// in a half-warp) of the 4 tokens 8 w + 4 h .. 8 w + 4 h + 3, h = l >> 4: the
+// 8-token block w is split between the two half-warps, and a factor that
+// spans the other half of the block is that half's total (lane l ^ 16).
+struct Blk4 {
+  H4 a[4], k[4], q[4];
+  float dqk[4];
+  float4 tot;
+};
+template <bool kMask>
+__device__ __forceinline__ void load_block4(Blk4& B, const uint8_t* sm, int row0, int ql,
+                                            float scale, int live) {
+  B.tot = make_float4(1.f, 1.f, 1.f, 1.f);
+  const uint32_t tb = quad_tb<64>(ql);
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const uint32_t off = quad_at(tb, (uint32_t)(row0 + r));
+    float4 kf = bf4(*reinterpret_cast<const uint2*>(sm + S_TK + off));
+    float4 qf = bf4(*reinterpret_cast<const uint2*>(sm + S_TQ + off));
+    float4 af = bf4(*reinterpret_cast<const uint2*>(sm + S_TA + off));
+    qf.x *= scale; qf.y *= scale; qf.z *= scale; qf.w *= scale;
+    if (kMask && r >= live) {
+      kf = make_float4(0.f, 0.f, 0.f, 0.f);
+      qf = kf;
+      af = make_float4(1.f, 1.f, 1.f, 1.f);
+    }
+    B.dqk[r] = fmaf(qf.x, kf.x, fmaf(qf.y, kf.y, fmaf(qf.z, kf.z, qf.w * kf.w)));
+    B.k[r] = h4_of(kf);
+    B.q[r] = h4_of(qf);
+    B.a[r] = h4_of(af);
+    B.tot.x *= af.x; B.tot.y *= af.y; B.tot.z *= af.z; B.tot.w *= af.w;
+  }
+}
+__device__ __forceinline__ float4 mulf4(float4 a, float4 b) {
+  return make_float4(a.x * b.x, a.y * b.y, a.z * b.z, a.w * b.w);
+}
+// Round A with the half-block mapping: the same rows and ranks as
+// write_round_a.  `other` is the total of the other half of the block.
+__device__ __forceinline__ void write_round_a4(uint8_t* sm, const Blk4& B, float4 other, int w,
+                                               int h, int ql) {
+  const uint32_t tx = quad_tb<128>(ql), ty = quad_tb<64>(ql);
+  uint8_t* X = sm + S_RA_X;
+  uint8_t* Y = sm + S_RA_Y;
+  const uint32_t r8 = 8u * (uint32_t)(w >> 1) + 4u * (uint32_t)h, r4 = 4u * (uint32_t)w;
+  // level 8: the upper block's prefix starts at its first token, the lower
+  // block's suffix ends at its last
+  if (w & 1) put_upper<0, 4>(X, tx, B, h ? h4_of(other) : ones4(), r8, 32 + r8);
+  else put_lower<0, 4>(Y, ty, B, h ? ones4() : h4_of(other), r8);
+  // level 4: the two halves of the block
+  if (h) put_upper<0, 4>(X, tx, B, ones4(), 64 + r4, 96 + r4);
+  else put_lower<0, 4>(Y, ty, B, ones4(), 32 + r4);
+}
+// Round C with the half-block mapping (rows and ranks of write_round_c).
+__device__ __forceinline__ void write_round_c4(uint8_t* sm, const Blk4& B, const float4 (&T8)[8],
+                                               float4 other, int w, int h, int ql) {
+  const uint32_t tx = quad_tb<128>(ql), ty = quad_tb<64>(ql);
+  uint8_t* X = sm + S_RC_X;
+  uint8_t* Y = sm + S_RC_Y;
+  float4 F = make_float4(1.f, 1.f, 1.f, 1.f);
+  if (w >= 4) {
+#pragma unroll
+    for (int b = 4; b < 8; ++b)
+      if (b < w) F = mulf4(F, T8[b]);
+    if (h) F = mulf4(F, other);
+    const uint32_t u0 = 8u * (uint32_t)(w - 4) + 4u * (uint32_t)h;
+    put_upper<0, 4>(X, tx, B, h4_of(F), u0, 32 + u0);
+  } else {
+#pragma unroll
+    for (int b = 1; b < 4; ++b)
+      if (b > w) F = mulf4(F, T8[b]);
+    if (!h) F = mulf4(F, other);
+    put_lower<0, 4>(Y, ty, B, h4_of(F), 8u * (uint32_t)w + 4u * (uint32_t)h);
+  }
+  float4 nb = make_float4(1.f, 1.f, 1.f, 1.f);
+#pragma unroll
+  for (int b = 0; b < 8; ++b)
+    if (((w & 3) == 3 && b == w - 1) || ((w & 3) == 0 && b == w + 1)) nb = T8[b];
+  const int j = w >> 2, loc = w & 3;
+  if (loc >= 2) {
+    float4 f = loc == 3 ? nb : make_float4(1.f, 1.f, 1.f, 1.f);
+    if (h) f = mulf4(f, other);
+    const uint32_t u0 = 16u * (uint32_t)j + 8u * (uint32_t)(loc - 2) + 4u * (uint32_t)h;
+    put_upper<0, 4>(X, tx, B, h4_of(f), 64 + u0, 96 + u0);
+  } else {
+    float4 b = loc == 0 ? nb : make_float4(1.f, 1.f, 1.f, 1.f);
+    if (!h) b = mulf4(b, other);
+    put_lower<0, 4>(Y, ty, B, h4_of(b), 32u + 16u * (uint32_t)j + 8u * (uint32_t)loc +
+                                            4u * (uint32_t)h);
   }
 }
 
@@ -751,6 +838,45 @@ __device__ __forceinline__ void in_group_pairs(const Blk8& B, float (&v)[32]) {
     o[15] = dot4(uq3, y1);
   }
 }
+// The same 16 values for the one 4-token group of a half-block (t0 = 0).
+__device__ __forceinline__ void in_group_pairs4(const Blk4& B, float (&o)[16]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) o[j] = B.dqk[j];
+  const H4 xk1 = mul4(B.k[1], B.a[1]), xq1 = mul4(B.q[1], B.a[1]);
+  const H4 xk3 = mul4(B.k[3], B.a[3]), xq3 = mul4(B.q[3], B.a[3]);
+  o[4] = dot4(xk1, B.k[0]);
+  o[5] = dot4(xq1, B.k[0]);
+  o[6] = dot4(xk3, B.k[2]);
+  o[7] = dot4(xq3, B.k[2]);
+  const H4 f3 = mul4(B.a[2], B.a[3]);
+  const H4 uk2 = mul4(B.k[2], B.a[2]), uq2 = mul4(B.q[2], B.a[2]);
+  const H4 uk3 = mul4(B.k[3], f3), uq3 = mul4(B.q[3], f3);
+  const H4 y0 = mul4(B.k[0], B.a[1]);
+  const H4& y1 = B.k[1];
+  o[8] = dot4(uk2, y0);
+  o[9] = dot4(uk2, y1);
+  o[10] = dot4(uk3, y0);
+  o[11] = dot4(uk3, y1);
+  o[12] = dot4(uq2, y0);
+  o[13] = dot4(uq2, y1);
+  o[14] = dot4(uq3, y0);
+  o[15] = dot4(uq3, y1);
+}
+// Sums each of 16 values over a half-warp (the 64 channels) by halving
+// exchanges; lane l ends with the sum of value l & 15.
+__device__ __forceinline__ float half_warp_sum16(float (&v)[16], int lane) {
+#pragma unroll
+  for (int w = 8; w >= 1; w >>= 1) {
+    const bool hi = (lane & w) != 0;
+#pragma unroll
+    for (int i = 0; i < w; ++i) {
+      const float send = hi ? v[i] : v[i + w];
+      const float keep = hi ? v[i + w] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+    }
+  }
+  return v[0];
+}
 // Sums each of the 32 values over the warp (all 128 channels) by halving
 // exchanges; lane l ends with the sum of value l.
 __device__ __forceinline__ float warp_sum32(float (&v)[32], int lane) {
@@ -805,10 +931,11 @@ __device__ __forceinline__ void mma16816_bf16(float (&d)[4], const uint32_t (&a)
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
+template <int DK>
 __device__ __forceinline__ void minus_w(uint8_t* sm, uint32_t sb, int iw, int lane) {
   const int g = lane >> 2, cq = lane & 3, mi = lane >> 3;
 #pragma unroll 1
-  for (int np = iw; np < 8; np += NINV_WARPS) {
+  for (int np = iw; np < DK / 16; np += NINV_WARPS) {
     // one pair of 8-column tiles of i against all four 16-row tiles of t:
     // each K step issues eight independent products
     float acc[4][2][4];
@@ -926,116 +1053,238 @@ __global__ void __launch_bounds__(NT, 1)
     const int wq = warp & 3, hc = warp >> 2;  // read-outs: TMEM lane quarter, column half
     bool alive = true, ok = true;
     const float4* tot_s = reinterpret_cast<const float4*>(sm + S_TOT);
-    for (int c = 0; c < nchunks && alive; ++c) {
-      const int lenc = min(C, u.len - c * C);
-      const int slot = c & 1;
-      const float* beta_c = reinterpret_cast<const float*>(sm + S_BETA) + 64 * (c & 3);
-      // ---- 1. q, k, alpha of chunk c
-      ok = ok && mbar_wait(bars + B_QKA, (uint32_t)(c & 1));
-      Blk8 B;
-      const bool pad = DK == 64 && lane >= 16;
-      if (lenc == C) load_block<false>(B, sm, blk, lane, a.scale, C, pad);
-      else load_block<true>(B, sm, blk, lane, a.scale, lenc - 8 * blk, pad);
-      // ---- 2. round A (levels 8, 4); its buffer was last read by round A of
-      // chunk c-1, whose completion this role waited for
-      write_round_a(sm, B, blk, lane);
-      warp_publish(bars + B_OPS_A, lane);
-      // ---- 3. in-group pairs and q.k over all 128 channels (the warp)
-      float ig;
-      {
-        float v[32];
-        in_group_pairs(B, v);
-        ig = warp_sum32(v, lane);
-      }
-      reinterpret_cast<float4*>(sm + S_TOT)[blk * 32 + lane] = B.tot;
-      // ---- 4. every tile read is done; block totals are visible
-      if (!named_and(BAR_PREP, NPREP, ok)) { alive = false; break; }
-      // ---- 5. round C (levels 32, 16) into the tile region
-      float4 T8[8];
+    if constexpr (DK == 128) {
+      for (int c = 0; c < nchunks && alive; ++c) {
+        const int lenc = min(C, u.len - c * C);
+        const int slot = c & 1;
+        const float* beta_c = reinterpret_cast<const float*>(sm + S_BETA) + 64 * (c & 3);
+        // ---- 1. q, k, alpha of chunk c
+        ok = ok && mbar_wait(bars + B_QKA, (uint32_t)(c & 1));
+        Blk8 B;
+        if (lenc == C) load_block<false>(B, sm, blk, lane, a.scale, C);
+        else load_block<true>(B, sm, blk, lane, a.scale, lenc - 8 * blk);
+        // ---- 2. round A (levels 8, 4); its buffer was last read by round A of
+        // chunk c-1, whose completion this role waited for
+        write_round_a(sm, B, blk, lane);
+        warp_publish(bars + B_OPS_A, lane);
+        // ---- 3. in-group pairs and q.k over all 128 channels (the warp)
+        float ig;
+        {
+          float v[32];
+          in_group_pairs(B, v);
+          ig = warp_sum32(v, lane);
+        }
+        reinterpret_cast<float4*>(sm + S_TOT)[blk * 32 + lane] = B.tot;
+        // ---- 4. every tile read is done; block totals are visible
+        if (!named_and(BAR_PREP, NPREP, ok)) { alive = false; break; }
+        // ---- 5. round C (levels 32, 16) into the tile region
+        float4 T8[8];
 #pragma unroll
-      for (int b = 0; b < 8; ++b) T8[b] = tot_s[b * 32 + lane];
-      write_round_c(sm, B, T8, blk, lane);
-      warp_publish(bars + B_OPS_C, lane);
-      // gamma_C (fp32: it scales the fp32 state); k*gamma (bf16), q*gamma and
-      // k*rho (rho_s = exclusive suffix times later blocks' totals) stay in
-      // registers until their tiles are free
-      if (blk == 0) {
-        float4 g = T8[0];
+        for (int b = 0; b < 8; ++b) T8[b] = tot_s[b * 32 + lane];
+        write_round_c(sm, B, T8, blk, lane);
+        warp_publish(bars + B_OPS_C, lane);
+        // gamma_C (fp32: it scales the fp32 state); k*gamma (bf16), q*gamma and
+        // k*rho (rho_s = exclusive suffix times later blocks' totals) stay in
+        // registers until their tiles are free
+        if (blk == 0) {
+          float4 g = T8[0];
 #pragma unroll
-        for (int b = 1; b < 8; ++b) { g.x *= T8[b].x; g.y *= T8[b].y; g.z *= T8[b].z; g.w *= T8[b].w; }
-        reinterpret_cast<float4*>(sm + S_GAM)[32 * (c & 1) + lane] = g;
+          for (int b = 1; b < 8; ++b) { g.x *= T8[b].x; g.y *= T8[b].y; g.z *= T8[b].z; g.w *= T8[b].w; }
+          reinterpret_cast<float4*>(sm + S_GAM)[32 * (c & 1) + lane] = g;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bars + B_GAM + (c & 1));
+        }
+        H4 gq[8], kr[8];
+        uint2 kgb[8];
+        {
+          float4 Gb = make_float4(1.f, 1.f, 1.f, 1.f), Ga = Gb;
+#pragma unroll
+          for (int b = 0; b < 8; ++b) {
+            if (b < blk) { Gb.x *= T8[b].x; Gb.y *= T8[b].y; Gb.z *= T8[b].z; Gb.w *= T8[b].w; }
+            if (b > blk) { Ga.x *= T8[b].x; Ga.y *= T8[b].y; Ga.z *= T8[b].z; Ga.w *= T8[b].w; }
+          }
+          H4 g = h4_of(Gb);
+#pragma unroll
+          for (int r = 0; r < 8; ++r) {
+            g = mul4(g, B.a[r]);
+            const H4 kg = mul4(B.k[r], g);
+            const float2 k0 = __half22float2(kg.p[0]), k1 = __half22float2(kg.p[1]);
+            kgb[r] = make_uint2(pack_bf162(k0.x, k0.y), pack_bf162(k1.x, k1.y));
+            gq[r] = mul4(B.q[r], g);
+          }
+          H4 rr = h4_of(Ga);
+#pragma unroll
+          for (int r = 7; r >= 0; --r) {
+            if (r < 7) rr = mul4(rr, B.a[r + 1]);
+            kr[r] = mul4(B.k[r], rr);
+          }
+        }
+        // ---- 6. this parity's M blocks and A tile are free (the inverse warps
+        // and the state's O step of chunk c-2 are done with them); beta in place
+        ok = ok && mbar_wait(bars + B_BETA + (c & 3), (uint32_t)((c >> 2) & 1));
+        if (c >= 2) {
+          ok = ok && mbar_wait(bars + B_MFREE + slot, (uint32_t)(((c - 2) >> 1) & 1));
+          ok = ok && mbar_wait(bars + B_S3 + slot, (uint32_t)(((c - 2) >> 1) & 1));
+        }
+        store_in_group(sm, slot, blk, lane, ig, beta_c);
+        // ---- 7. Gram read-outs
+        ok = ok && mbar_wait(bars + B_DONE_A, (uint32_t)(c & 1));
+        tc_fence_after();
+        readout_a(sm, slot, tmem, wq, hc, lane, beta_c);
+        ok = ok && mbar_wait(bars + B_DONE_C, (uint32_t)(c & 1));
+        tc_fence_after();
+        readout_c(sm, slot, tmem, wq, hc, lane, beta_c);
+        // k*gamma (bf16), once the inverse warps have finished chunk c-1's -W
+        // (late in the chunk, so that the prep warps rarely wait for it)
+        if (c > 0) ok = ok && mbar_wait(bars + B_KGFREE, (uint32_t)((c - 1) & 1));
+        {
+          const uint32_t tb = quad_tb<64>(lane);
+#pragma unroll
+          for (int r = 0; r < 8; ++r)
+            *reinterpret_cast<uint2*>(sm + S_KG + quad_at(tb, (uint32_t)(8 * blk + r))) = kgb[r];
+        }
+        tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bars + B_GAM + (c & 1));
-      }
-      H4 gq[8], kr[8];
-      uint2 kgb[8];
-      {
-        float4 Gb = make_float4(1.f, 1.f, 1.f, 1.f), Ga = Gb;
-#pragma unroll
-        for (int b = 0; b < 8; ++b) {
-          if (b < blk) { Gb.x *= T8[b].x; Gb.y *= T8[b].y; Gb.z *= T8[b].z; Gb.w *= T8[b].w; }
-          if (b > blk) { Ga.x *= T8[b].x; Ga.y *= T8[b].y; Ga.z *= T8[b].z; Ga.w *= T8[b].w; }
+        if (lane == 0) mbar_arrive(bars + B_MREADY + slot);
+        // ---- 8. q*gamma (rows 64.. of [-W ; q*gamma]) and k*rho, once chunk
+        // c-1's state MMAs have read their tiles
+        if (c > 0) {
+          ok = ok && mbar_wait(bars + B_S1, (uint32_t)((c - 1) & 1));
+          ok = ok && mbar_wait(bars + B_S3 + ((c - 1) & 1), (uint32_t)(((c - 1) >> 1) & 1));
         }
-        H4 g = h4_of(Gb);
+        {
+          const uint32_t tq = quad_tb<128>(lane), tk = quad_tb<64>(lane);
 #pragma unroll
-        for (int r = 0; r < 8; ++r) {
-          g = mul4(g, B.a[r]);
-          const H4 kg = mul4(B.k[r], g);
-          const float2 k0 = __half22float2(kg.p[0]), k1 = __half22float2(kg.p[1]);
-          kgb[r] = make_uint2(pack_bf162(k0.x, k0.y), pack_bf162(k1.x, k1.y));
-          gq[r] = mul4(B.q[r], g);
+          for (int r = 0; r < 8; ++r) {
+            st_quad(sm + S_WQ + quad_at(tq, (uint32_t)(64 + 8 * blk + r)), gq[r]);
+            st_quad(sm + S_KH + quad_at(tk, (uint32_t)(8 * blk + r)), kr[r]);
+          }
         }
-        H4 rr = h4_of(Ga);
-#pragma unroll
-        for (int r = 7; r >= 0; --r) {
-          if (r < 7) rr = mul4(rr, B.a[r + 1]);
-          kr[r] = mul4(B.k[r], rr);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bars + B_READY);
+      }
+    } else {
+      // 64-wide key: half-block mapping (see load_block4)
+      const int h = lane >> 4, ql = lane & 15;
+      for (int c = 0; c < nchunks && alive; ++c) {
+        const int lenc = min(C, u.len - c * C);
+        const int slot = c & 1;
+        const float* beta_c = reinterpret_cast<const float*>(sm + S_BETA) + 64 * (c & 3);
+        // ---- 1. q, k, alpha of chunk c
+        ok = ok && mbar_wait(bars + B_QKA, (uint32_t)(c & 1));
+        Blk4 B;
+        const int row0 = 8 * blk + 4 * h;   // this half-block's first token
+        if (lenc == C) load_block4<false>(B, sm, row0, ql, a.scale, C);
+        else load_block4<true>(B, sm, row0, ql, a.scale, lenc - row0);
+        float4 other;   // the total of the other half of the block
+        other.x = __shfl_xor_sync(0xffffffffu, B.tot.x, 16);
+        other.y = __shfl_xor_sync(0xffffffffu, B.tot.y, 16);
+        other.z = __shfl_xor_sync(0xffffffffu, B.tot.z, 16);
+        other.w = __shfl_xor_sync(0xffffffffu, B.tot.w, 16);
+        // ---- 2. round A (levels 8, 4); its buffer was last read by round A of
+        // chunk c-1, whose completion this role waited for
+        write_round_a4(sm, B, other, blk, h, ql);
+        warp_publish(bars + B_OPS_A, lane);
+        // ---- 3. in-group pairs and q.k over the 64 channels (the half-warp)
+        float ig;
+        {
+          float v[16];
+          in_group_pairs4(B, v);
+          ig = half_warp_sum16(v, lane);
         }
-      }
-      // ---- 6. this parity's M blocks and A tile are free (the inverse warps
-      // and the state's O step of chunk c-2 are done with them); beta in place
-      ok = ok && mbar_wait(bars + B_BETA + (c & 3), (uint32_t)((c >> 2) & 1));
-      if (c >= 2) {
-        ok = ok && mbar_wait(bars + B_MFREE + slot, (uint32_t)(((c - 2) >> 1) & 1));
-        ok = ok && mbar_wait(bars + B_S3 + slot, (uint32_t)(((c - 2) >> 1) & 1));
-      }
-      store_in_group(sm, slot, blk, lane, ig, beta_c);
-      // ---- 7. Gram read-outs
-      ok = ok && mbar_wait(bars + B_DONE_A, (uint32_t)(c & 1));
-      tc_fence_after();
-      readout_a(sm, slot, tmem, wq, hc, lane, beta_c);
-      ok = ok && mbar_wait(bars + B_DONE_C, (uint32_t)(c & 1));
-      tc_fence_after();
-      readout_c(sm, slot, tmem, wq, hc, lane, beta_c);
-      // k*gamma (bf16), once the inverse warps have finished chunk c-1's -W
-      // (late in the chunk, so that the prep warps rarely wait for it)
-      if (c > 0) ok = ok && mbar_wait(bars + B_KGFREE, (uint32_t)((c - 1) & 1));
-      {
-        const uint32_t tb = quad_tb<64>(lane);
+        if (h == 0) reinterpret_cast<float4*>(sm + S_TOT)[blk * 32 + ql] = mulf4(B.tot, other);
+        // ---- 4. every tile read is done; block totals are visible
+        if (!named_and(BAR_PREP, NPREP, ok)) { alive = false; break; }
+        // ---- 5. round C (levels 32, 16) into the tile region
+        float4 T8[8];
 #pragma unroll
-        for (int r = 0; r < 8; ++r)
-          *reinterpret_cast<uint2*>(sm + S_KG + quad_at(tb, (uint32_t)(8 * blk + r))) = kgb[r];
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bars + B_MREADY + slot);
-      // ---- 8. q*gamma (rows 64.. of [-W ; q*gamma]) and k*rho, once chunk
-      // c-1's state MMAs have read their tiles
-      if (c > 0) {
-        ok = ok && mbar_wait(bars + B_S1, (uint32_t)((c - 1) & 1));
-        ok = ok && mbar_wait(bars + B_S3 + ((c - 1) & 1), (uint32_t)(((c - 1) >> 1) & 1));
-      }
-      {
-        const uint32_t tq = quad_tb<128>(lane), tk = quad_tb<64>(lane);
+        for (int b = 0; b < 8; ++b) T8[b] = tot_s[b * 32 + ql];
+        write_round_c4(sm, B, T8, other, blk, h, ql);
+        warp_publish(bars + B_OPS_C, lane);
+        // gamma_C (fp32: it scales the fp32 state); k*gamma (bf16), q*gamma and
+        // k*rho (rho_s = exclusive suffix times later blocks' totals) stay in
+        // registers until their tiles are free
+        if (blk == 0) {
+          float4 g = T8[0];
 #pragma unroll
-        for (int r = 0; r < 8; ++r) {
-          st_quad(sm + S_WQ + quad_at(tq, (uint32_t)(64 + 8 * blk + r)), gq[r]);
-          st_quad(sm + S_KH + quad_at(tk, (uint32_t)(8 * blk + r)), kr[r]);
+          for (int b = 1; b < 8; ++b) { g.x *= T8[b].x; g.y *= T8[b].y; g.z *= T8[b].z; g.w *= T8[b].w; }
+          if (h == 0) reinterpret_cast<float4*>(sm + S_GAM)[32 * (c & 1) + ql] = g;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bars + B_GAM + (c & 1));
         }
+        H4 gq[4], kr[4];
+        uint2 kgb[4];
+        {
+          float4 Gb = make_float4(1.f, 1.f, 1.f, 1.f), Ga = Gb;
+#pragma unroll
+          for (int b = 0; b < 8; ++b) {
+            if (b < blk) { Gb.x *= T8[b].x; Gb.y *= T8[b].y; Gb.z *= T8[b].z; Gb.w *= T8[b].w; }
+            if (b > blk) { Ga.x *= T8[b].x; Ga.y *= T8[b].y; Ga.z *= T8[b].z; Ga.w *= T8[b].w; }
+          }
+          if (h) Gb = mulf4(Gb, other);
+          else Ga = mulf4(Ga, other);
+          H4 g = h4_of(Gb);
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            g = mul4(g, B.a[r]);
+            const H4 kg = mul4(B.k[r], g);
+            const float2 k0 = __half22float2(kg.p[0]), k1 = __half22float2(kg.p[1]);
+            kgb[r] = make_uint2(pack_bf162(k0.x, k0.y), pack_bf162(k1.x, k1.y));
+            gq[r] = mul4(B.q[r], g);
+          }
+          H4 rr = h4_of(Ga);
+#pragma unroll
+          for (int r = 3; r >= 0; --r) {
+            if (r < 3) rr = mul4(rr, B.a[r + 1]);
+            kr[r] = mul4(B.k[r], rr);
+          }
+        }
+        // ---- 6. this parity's M blocks and A tile are free (the inverse warps
+        // and the state's O step of chunk c-2 are done with them); beta in place
+        ok = ok && mbar_wait(bars + B_BETA + (c & 3), (uint32_t)((c >> 2) & 1));
+        if (c >= 2) {
+          ok = ok && mbar_wait(bars + B_MFREE + slot, (uint32_t)(((c - 2) >> 1) & 1));
+          ok = ok && mbar_wait(bars + B_S3 + slot, (uint32_t)(((c - 2) >> 1) & 1));
+        }
+        store_in_group(sm, slot, blk, 16 * h + ql, ig, beta_c);
+        // ---- 7. Gram read-outs
+        ok = ok && mbar_wait(bars + B_DONE_A, (uint32_t)(c & 1));
+        tc_fence_after();
+        readout_a(sm, slot, tmem, wq, hc, lane, beta_c);
+        ok = ok && mbar_wait(bars + B_DONE_C, (uint32_t)(c & 1));
+        tc_fence_after();
+        readout_c(sm, slot, tmem, wq, hc, lane, beta_c);
+        // k*gamma (bf16), once the inverse warps have finished chunk c-1's -W
+        // (late in the chunk, so that the prep warps rarely wait for it)
+        if (c > 0) ok = ok && mbar_wait(bars + B_KGFREE, (uint32_t)((c - 1) & 1));
+        {
+          const uint32_t tb = quad_tb<64>(ql);
+#pragma unroll
+          for (int r = 0; r < 4; ++r)
+            *reinterpret_cast<uint2*>(sm + S_KG + quad_at(tb, (uint32_t)(row0 + r))) = kgb[r];
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bars + B_MREADY + slot);
+        // ---- 8. q*gamma (rows 64.. of [-W ; q*gamma]) and k*rho, once chunk
+        // c-1's state MMAs have read their tiles
+        if (c > 0) {
+          ok = ok && mbar_wait(bars + B_S1, (uint32_t)((c - 1) & 1));
+          ok = ok && mbar_wait(bars + B_S3 + ((c - 1) & 1), (uint32_t)(((c - 1) >> 1) & 1));
+        }
+        {
+          const uint32_t tq = quad_tb<128>(ql), tk = quad_tb<64>(ql);
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            st_quad(sm + S_WQ + quad_at(tq, (uint32_t)(64 + row0 + r)), gq[r]);
+            st_quad(sm + S_KH + quad_at(tk, (uint32_t)(row0 + r)), kr[r]);
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bars + B_READY);
       }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bars + B_READY);
     }
     if (!alive || !ok) *reinterpret_cast<volatile int*>(s_abort) = 1;
   } else if (tid < NPREP + NSTATE) {
@@ -1070,7 +1319,7 @@ __global__ void __launch_bounds__(NT, 1)
       const float f2 = pow2i(-d);
       __half2 m2 = __floats2half2_rn(0.f, 0.f);
 #pragma unroll 1
-      for (int i0 = 0; i0 < 128; i0 += 16) {
+      for (int i0 = 0; i0 < DK; i0 += 16) {
         float f[16];
         if (from_h0) {
 #pragma unroll
@@ -1189,7 +1438,7 @@ __global__ void __launch_bounds__(NT, 1)
                     idesc_f16(128, 64, 1, 1, 0), k > 0);
         }
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
+        for (int k = 0; k < DK / 16; ++k)
           umma_ts(tmem + T_U, tmem + T_HA + 8 * k, kmajor_desc(sb + S_WQ, 128, k),
                   idesc_f16(128, 128, 0, 0, 0), (k > 0 || !zero_v) ? 1u : 0u);
         umma_commit(bars + B_S1);
@@ -1252,7 +1501,7 @@ __global__ void __launch_bounds__(NT, 1)
         const int b = u_shift(m, mH, sig);
         if (b != 0) {
           rescale_cols(T_O, 64, b);
-          rescale_cols(T_H, 128, b);
+          rescale_cols(T_H, DK, b);
           convert_u(b);
           mU = m * pow2i(-b);
           mH *= pow2i(-b);
@@ -1272,7 +1521,7 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
         for (int k = 0; k < 4; ++k)
           umma_ts(tmem + T_H, tmem + T_UA + 8 * k, mnmajor_desc(sb + S_KH, 64, k),
-                  idesc_f16(128, 128, 0, 0, 1), 1);
+                  idesc_f16(128, DK, 0, 0, 1), 1);
         umma_commit(bars + B_S3 + (c & 1));
       }
       {
@@ -1355,7 +1604,7 @@ __global__ void __launch_bounds__(NT, 1)
       else inverse_column<2>(sm, sb, slot, lane, beta_c);
       named_sync(BAR_INV, NINV);      // TB complete; M blocks of this parity free
       if (lane == 0) mbar_arrive(bars + B_MFREE + slot);
-      minus_w(sm, sb, iw, lane);
+      minus_w<DK>(sm, sb, iw, lane);
       __syncwarp();
       if (lane == 0) mbar_arrive(bars + B_KGFREE);
       fence_proxy_async_smem();
@@ -1391,12 +1640,12 @@ __global__ void __launch_bounds__(NT, 1)
         if (!zero_v) tma_prefetch_2d_l2(&mv, x0, y);
       }
     };
-    // Gram round: D (128 x 64) = X (128 rows) Y^T (64 rows), K = 128
+    // Gram round: D (128 x 64) = X (128 rows) Y^T (64 rows), K = DK
     const uint32_t id64 = idesc_f16(128, 64, 0, 0, 0);
     auto gram = [&](uint32_t d_col, uint32_t xbuf, uint32_t ybuf) {
       const uint64_t d_gx = kmajor_desc(sb + xbuf, 128, 0), d_gy = kmajor_desc(sb + ybuf, 64, 0);
 #pragma unroll
-      for (int k = 0; k < 8; ++k)  // K steps: 32 bytes in a panel, panels R*128 apart
+      for (int k = 0; k < DK / 16; ++k)  // K steps: 32 bytes in a panel, panels R*128 apart
         umma_ss(tmem + d_col, d_gx + (uint64_t)((k >> 2) * 1024 + (k & 3) * 2),
                 d_gy + (uint64_t)((k >> 2) * 512 + (k & 3) * 2), id64, k > 0);
     };

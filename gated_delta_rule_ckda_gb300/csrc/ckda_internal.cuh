@@ -57,8 +57,7 @@ struct FwdArgs {
 
 // Shapes the chunkwise tensor-core kernel takes: bf16 I/O, dv = 128 and
 // dk = 128, or dk = 64 (the reduced key dimension of a state-reduced head,
-// "On State Reduction in Linear Attention"), run as 128 channels of which the
-// last 64 are inert padding.
+// "On State Reduction in Linear Attention"), which has an instance of its own.
 inline bool fwd_tensor_path(ckda_dtype io, int dk, int dv) {
   return io == CKDA_BF16 && dv == 128 && (dk == 128 || dk == 64);
 }

@@ -228,19 +228,22 @@ def test_chunk_path_dk64_packed(ck):
     check(o, hT, o_ref, h_ref, bf16=True, name="dk=64 packed")
 
 
-def test_chunk_path_dk64_equals_zero_padded_dk128(ck):
-    """dk = 64 runs as 128 channels whose last 64 have zero keys and queries
-    and unit gates; the same inputs padded that way in memory and run with
-    dk = 128 give bit-identical outputs."""
+def test_chunk_path_dk64_matches_zero_padded_dk128(ck):
+    """dk = 64 runs natively (64 channels per half-warp, K = 64 Gram rounds);
+    the same inputs padded to 128 channels with zero keys and queries and unit
+    gates, run with dk = 128, give the same result within rounding, both meet
+    the oracle's bound, and the padded state rows stay exactly zero."""
     x = synth.make_fwd(1, 2, 150, 64, dv=128, dist="ckda", dtype="bf16", h0=True, seed=411)
     pad = lambda t, val: torch.cat([t, torch.full_like(t, val)], dim=-1)
     xp = synth.FwdInputs(pad(x.q, 0.0), pad(x.k, 0.0), x.v, pad(x.alpha, 1.0), x.beta,
                          torch.cat([x.h0, torch.zeros_like(x.h0)], dim=2), None)
     o, hT = run_gpu(ck, x)
     op, hp = run_gpu(ck, xp)
-    assert torch.equal(o, op)
-    assert torch.equal(hT, hp[:, :, :64])
+    o_ref, h_ref = run_oracle(x)
+    check(o, hT, o_ref, h_ref, bf16=True, name="dk64 native")
+    check(op, hp[:, :, :64], o_ref, h_ref, bf16=True, name="dk64 padded to 128")
     assert torch.count_nonzero(hp[:, :, 64:]) == 0
+    assert max_rel(o, op) <= 2e-2 and max_rel(hT, hp[:, :, :64]) <= 1e-2
 
 
 def test_kda_range_dk64_workload_full(ck):
