@@ -492,6 +492,51 @@ def prep_bwd_case(ck, x, steps, warmup, ws, stream, name):
             "gpu_launches": steps}
 
 
+def fwd_raw_case(ck, x, steps, warmup, ws, stream, name):
+    """The forward on raw inputs of the workload's shape: ckda_fwd_raw (the
+    preparation inside the forward kernel) against ckda_prep followed by
+    ckda_fwd.  Both read raw q, k, a, b and v and write o and hT; the
+    algorithmic bytes are the forward's (the prepared tensors need not touch
+    HBM)."""
+    import torch
+    B, H, T, dk = x.q.shape
+    g = torch.Generator().manual_seed(23)
+    qr, kr, ar = (torch.randn((B, H, T, dk), generator=g).to(torch.bfloat16).cuda()
+                  for _ in range(3))
+    br = torch.randn((B, H, T), generator=g).to(torch.bfloat16).cuda()
+    v = x.v.cuda()
+    h0 = None if x.h0 is None else x.h0.cuda()
+    o = torch.empty_like(v)
+    hT = torch.empty((B, H, dk, v.shape[-1]), dtype=torch.float32, device="cuda")
+    wsp = ck.new_workspace(0, H, torch.device("cuda"))
+    prepped = (torch.empty_like(qr), torch.empty_like(kr), torch.empty_like(ar),
+               torch.empty_like(br))
+
+    def fused():
+        ck.fwd_raw(qr, kr, v, ar, br, h0, o=o, hT=hT, workspace=wsp, stream=stream)
+
+    def two_pass():
+        q, k, a, b = ck.prep(kr, ar, br, q_raw=qr, out=prepped, stream=stream)
+        ck.fwd(q, k, v, a, b, h0, o=o, hT=hT, workspace=wsp, stream=stream)
+
+    fused()
+    st = ck.fwd_status(wsp)
+    if st != 0:
+        raise RuntimeError(f"{name} raw: device status {ck.STATUS.get(st, st)}")
+    th = B * H * T
+    nbytes = fwd_bytes(B, H, T, dk, v.shape[-1], B, h0 is not None, True)
+    out = {}
+    for key, fn, launches in (("fused", fused, 1), ("prep_then_fwd", two_pass, 2)):
+        total, per = time_steps(fn, steps, warmup, ws, stream)
+        r = roofline(nbytes, per, "fwd", name)
+        r["traffic"] = None
+        out[key] = {"value": round(th * steps / total, 1), "unit": UNIT,
+                    "ms_per_step": round(total / steps * 1e3, 4), "launches_per_step": launches,
+                    "roofline": r}
+    del qr, kr, ar, br, prepped
+    return out
+
+
 def bwd_bytes(B, H, T, dk, dv, io_bytes=2):
     """Algorithmic bytes of ckda_bwd: q, k, alpha, v, do, beta in; dq, dk,
     dalpha, dv, dbeta out (the states it stores and reads back are not)."""
@@ -612,6 +657,8 @@ def run_ours(args):
         out["decode_raw"] = decode_case(ck, args.decode_steps, 10, ws, stream, raw=True)
     if ws == 1 and "prep" in extras:
         out["prep"] = prep_case(ck, x, 200, 10, ws, stream, args.workload)
+    if ws == 1 and "fwd_raw" in extras:
+        out["fwd_raw"] = fwd_raw_case(ck, x, 100, 5, ws, stream, args.workload)
     if ws == 1 and "prep_bwd" in extras:
         out["prep_bwd"] = prep_bwd_case(ck, x, 200, 10, ws, stream, args.workload)
     if ws == 1 and "bwd" in extras:
@@ -709,9 +756,9 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--extras",
-                    default="decode,decode_raw,prep,prep_bwd,bwd,kda_range,ckda_varlen,"
+                    default="decode,decode_raw,prep,prep_bwd,fwd_raw,bwd,kda_range,ckda_varlen,"
                             "kda_range_dk64,fig5_sweep,varlen_split",
-                    help="comma list of extra measurements: decode, decode_raw, prep, prep_bwd, bwd, "
+                    help="comma list of extra measurements: decode, decode_raw, prep, prep_bwd, fwd_raw, bwd, "
                          "varlen_split, "
                          "kda_range, ckda_full, ckda_varlen, kda_range_dk64, fig5_sweep")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -92,6 +92,8 @@ def lib():
             L.ckda_fwd_split_varlen_workspace_bytes.argtypes = [i32] * 5
             L.ckda_fwd_split_varlen.restype = i32
             L.ckda_fwd_split_varlen.argtypes = [vp] * 9 + [i32] * 6 + [f32, i32, vp, sz, vp]
+            L.ckda_fwd_raw.restype = i32
+            L.ckda_fwd_raw.argtypes = [vp] * 9 + [i32] * 7 + [f32, i32, f32, vp, sz, vp]
             L.ckda_prep_bwd.restype = i32
             L.ckda_prep_bwd.argtypes = [vp] * 12 + [ctypes.c_longlong, i32, i32, i32, f32, vp]
             L.ckda_fwd_host.restype = i32
@@ -146,8 +148,18 @@ def new_workspace(num_seqs, H, device):
     return torch.empty(n, dtype=torch.uint8, device=device)
 
 
+def fwd_raw(q_raw, k_raw, v, a_raw, b_raw, h0=None, cu_seqlens=None, scale=1.0,
+            normalize_q=True, norm_eps=1e-6, store_final_state=True, o=None, hT=None,
+            workspace=None, stream=None):
+    """ckda_fwd_raw: the forward on raw q, k and gate logits a, b, with the
+    input preparation of `prep` applied inside the kernel.  Returns (o, hT or
+    None)."""
+    return fwd(q_raw, k_raw, v, a_raw, b_raw, h0, cu_seqlens, scale, 0, store_final_state, o,
+               hT, workspace, stream, _raw=(bool(normalize_q), float(norm_eps)))
+
+
 def fwd(q, k, v, alpha, beta, h0=None, cu_seqlens=None, scale=1.0, chunk_size=0,
-        store_final_state=True, o=None, hT=None, workspace=None, stream=None):
+        store_final_state=True, o=None, hT=None, workspace=None, stream=None, _raw=None):
     """Forward over [B, H, T, d] (or packed) inputs.  Returns (o, hT or None)."""
     L = lib()
     device = q.device
@@ -176,13 +188,21 @@ def fwd(q, k, v, alpha, beta, h0=None, cu_seqlens=None, scale=1.0, chunk_size=0,
     nseq_ws = N if cu_seqlens is not None else 0
     if workspace is None:
         workspace = new_workspace(nseq_ws, H, device)
-    rc = L.ckda_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(h0), _ptr(o),
-                    _ptr(hT), _ptr(cu_seqlens), int(N if cu_seqlens is not None else 0),
-                    B, H, T, dk, dv, _io_dtype(q), float(scale), int(chunk_size),
-                    _ptr(workspace), int(workspace.numel()), _stream_handle(stream, device))
+    nseq = int(N if cu_seqlens is not None else 0)
+    if _raw is None:
+        rc = L.ckda_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(h0), _ptr(o),
+                        _ptr(hT), _ptr(cu_seqlens), nseq, B, H, T, dk, dv, _io_dtype(q),
+                        float(scale), int(chunk_size), _ptr(workspace), int(workspace.numel()),
+                        _stream_handle(stream, device))
+    else:
+        rc = L.ckda_fwd_raw(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(h0), _ptr(o),
+                            _ptr(hT), _ptr(cu_seqlens), nseq, B, H, T, dk, dv, _io_dtype(q),
+                            float(scale), int(_raw[0]), float(_raw[1]), _ptr(workspace),
+                            int(workspace.numel()), _stream_handle(stream, device))
     if rc != 0:
-        raise CkdaError(rc, "ckda_fwd")
+        raise CkdaError(rc, "ckda_fwd" if _raw is None else "ckda_fwd_raw")
     fwd.last_workspace = workspace
+    fwd_raw.last_workspace = workspace
     return o, hT
 
 

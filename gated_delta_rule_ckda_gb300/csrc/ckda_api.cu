@@ -86,12 +86,19 @@ size_t ckda_fwd_workspace_bytes(int num_seqs, int H) {
   return kWsStatusBytes + ((n * sizeof(int32_t) + 255) / 256) * 256;
 }
 
-ckda_status ckda_fwd(const void* q, const void* k, const void* v, const void* alpha,
+}  // extern "C"
+
+namespace {
+
+// ckda_fwd, and with raw = 1 ckda_fwd_raw (tensor-core shapes only).
+ckda_status fwd_impl(const void* q, const void* k, const void* v, const void* alpha,
                      const void* beta, const float* h0, void* o, float* hT,
                      const int32_t* cu_seqlens, int num_seqs, int B, int H, int T, int dk,
                      int dv, ckda_dtype io_dtype, float scale, int chunk_size, void* workspace,
-                     size_t workspace_bytes, void* stream) {
+                     size_t workspace_bytes, void* stream, int raw, int normalize_q,
+                     float norm_eps) {
   if (io_dtype != CKDA_F32 && io_dtype != CKDA_BF16) return CKDA_ERR_INVALID_ARG;
+  if (raw && (!(norm_eps >= 0.f) || norm_eps > 3.0e38f)) return CKDA_ERR_INVALID_ARG;
   if (B < 1 || H < 1 || T < 0 || dk < 1 || dv < 1) return CKDA_ERR_INVALID_ARG;
   if ((long long)B * H * T > 0x7fffffffLL) return CKDA_ERR_UNSUPPORTED;
   if (!(scale == scale)) return CKDA_ERR_INVALID_ARG;
@@ -105,6 +112,7 @@ ckda_status ckda_fwd(const void* q, const void* k, const void* v, const void* al
   if (chunk_size != 0 && chunk_size != 16 && chunk_size != 32 && chunk_size != 64)
     return CKDA_ERR_UNSUPPORTED;
   const bool tensor_path = fwd_tensor_path(io_dtype, dk, dv);
+  if (raw && !tensor_path) return CKDA_ERR_UNSUPPORTED;
   if (tensor_path && chunk_size != 0 && chunk_size != 64) return CKDA_ERR_UNSUPPORTED;
   const int nseq = cu_seqlens ? num_seqs : B;
   const size_t need = ckda_fwd_workspace_bytes(cu_seqlens ? num_seqs : 0, H);
@@ -130,6 +138,9 @@ ckda_status ckda_fwd(const void* q, const void* k, const void* v, const void* al
   a.num_units_seq = nseq;
   a.B = B; a.H = H; a.T = T; a.dk = dk; a.dv = dv;
   a.scale = scale; a.io = io_dtype;
+  a.raw = raw;
+  a.normalize_q = normalize_q;
+  a.norm_eps = norm_eps;
 
   cudaError_t err = cudaMemsetAsync(status, 0, sizeof(int), s);
   if (err != cudaSuccess) return CKDA_ERR_CUDA;
@@ -140,6 +151,29 @@ ckda_status ckda_fwd(const void* q, const void* k, const void* v, const void* al
   }
   err = tensor_path ? launch_fwd(a, s) : launch_fwd_recurrent(a, s);
   return err == cudaSuccess ? CKDA_OK : CKDA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+ckda_status ckda_fwd(const void* q, const void* k, const void* v, const void* alpha,
+                     const void* beta, const float* h0, void* o, float* hT,
+                     const int32_t* cu_seqlens, int num_seqs, int B, int H, int T, int dk,
+                     int dv, ckda_dtype io_dtype, float scale, int chunk_size, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+  return fwd_impl(q, k, v, alpha, beta, h0, o, hT, cu_seqlens, num_seqs, B, H, T, dk, dv,
+                  io_dtype, scale, chunk_size, workspace, workspace_bytes, stream, 0, 0, 0.f);
+}
+
+ckda_status ckda_fwd_raw(const void* q_raw, const void* k_raw, const void* v, const void* a_raw,
+                         const void* b_raw, const float* h0, void* o, float* hT,
+                         const int32_t* cu_seqlens, int num_seqs, int B, int H, int T, int dk,
+                         int dv, ckda_dtype io_dtype, float scale, int normalize_q,
+                         float norm_eps, void* workspace, size_t workspace_bytes, void* stream) {
+  return fwd_impl(q_raw, k_raw, v, a_raw, b_raw, h0, o, hT, cu_seqlens, num_seqs, B, H, T, dk,
+                  dv, io_dtype, scale, 0, workspace, workspace_bytes, stream, 1,
+                  normalize_q ? 1 : 0, norm_eps);
 }
 
 ckda_status ckda_fwd_status(void* workspace, void* stream) {

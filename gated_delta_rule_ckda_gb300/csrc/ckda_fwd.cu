@@ -134,6 +134,32 @@ constexpr uint32_t T_GC = 352;  // round C output [128 x 64]
 constexpr uint32_t T_GA = 416;  // round A output [128 x 64]
 constexpr uint32_t TMEM_COLS = 512;
 
+// ---- tiles the state step reads, by chunk ----
+// TB, [-W ; q*gamma] and k*rho are written for chunk c while the state step
+// may still read chunk c-1's.  A 64-wide key leaves the second 64-column
+// panel of each tile free, so there they alternate by chunk parity and a
+// writer waits for chunk c-2's reader (kLag = 2); with dk = 128 there is one
+// of each and the writer waits for chunk c-1's (kLag = 1).
+template <int DK>
+__device__ __forceinline__ uint32_t wq_tile(int c) {
+  return S_WQ + ((DK == 64 && (c & 1)) ? 16384u : 0u);
+}
+template <int DK>
+__device__ __forceinline__ uint32_t tb_tile(int c) {
+  return (DK == 64 && (c & 1)) ? S_KG + 8192u : S_TB;   // k*gamma's free panel
+}
+template <int DK>
+__device__ __forceinline__ uint32_t kh_tile(int c) {
+  return S_KH + ((DK == 64 && (c & 1)) ? 8192u : 0u);
+}
+// k*gamma, read by the inverse warps' -W: with dk = 64 the second buffer is
+// the k tile's free panel (the q, k, alpha tiles use one panel, round C's
+// operands the rows of the q tile and the alpha tile).
+template <int DK>
+__device__ __forceinline__ uint32_t kg_tile(int c) {
+  return (DK == 64 && (c & 1)) ? S_TK + 8192u : S_KG;
+}
+
 // ---- mbarriers ----
 enum Bar : int {
   B_QKA = 0,   // q, k, alpha tiles (TMA)
@@ -142,17 +168,21 @@ enum Bar : int {
   B_OPS_C,     // round C operands
   B_DONE_A,    // MMA -> waiters
   B_DONE_C,
-  B_S1,        // state: [U | O] MMA done
-  B_S3,        // [2] state: O and H MMAs of the chunk of this parity done
-  B_READY = B_S3 + 2,   // prep and inverse -> state: the chunk's operands are in place
-  B_GAM,                // [2] prep -> state: gamma_C published
-  B_BETA = B_GAM + 2,   // [4] issue warp -> prep: beta in shared memory
+  B_S1,        // [2] state: [U | O] MMA of the chunk of this parity done
+  B_S3 = B_S1 + 2,      // [2] state: O and H MMAs of the chunk of this parity done
+  B_READY = B_S3 + 2,   // [2] prep and inverse -> state: the chunk's operands are in place
+  B_GAM = B_READY + 2,  // [4] prep -> state: gamma_C published (slot chunk % kGamSlots)
+  B_BETA = B_GAM + 4,   // [4] issue warp -> prep: beta in shared memory
   B_MREADY = B_BETA + 4,  // [2] prep -> inverse: M blocks of the chunk of this parity
   B_MFREE = B_MREADY + 2, // [2] inverse -> prep: done with them
-  B_KGFREE = B_MFREE + 2, // inverse -> prep: k*gamma read
-  B_COUNT
+  B_KGFREE = B_MFREE + 2, // [2] inverse -> prep: k*gamma of the chunk of this parity read
+  B_COUNT = B_KGFREE + 2
 };
-static_assert(B_COUNT * 8 <= 192, "mbarrier area");
+static_assert(B_COUNT * 8 <= 240, "mbarrier area");
+// gamma_C slots: the prep warps may run kLag chunks ahead of the state step,
+// so a 64-wide key (kLag = 2) keeps four (of 64 channels), dk = 128 two
+template <int DK>
+__host__ __device__ constexpr int gam_slots() { return DK == 64 ? 4 : 2; }
 
 constexpr uint32_t TILE_BYTES = 16384;
 
@@ -398,6 +428,82 @@ __device__ __forceinline__ void load_block(Blk8& B, const uint8_t* sm, int blk, 
   }
 }
 
+// The decay gate of the fused loads: alpha = s [e^-5 + (1 - e^-5) |r|] with
+// r = tanh(a/2) and s = +1 for r >= 0 (a >= 0, -0 included), where
+// |tanh(x)| = (1 - e^{-2|x|}) / (1 + e^{-2|x|}): one exponential and one
+// division instead of tanhf, to well below the fp16 rounding alpha takes next.
+__device__ __forceinline__ float gate_alpha_fused(float a) {
+  const float e = __expf(-fabsf(a));
+  const float m = __fdividef(1.f - e, 1.f + e);
+  const float g = fmaf(1.f - kGateEps, m, kGateEps);
+  return a >= 0.f ? g : -g;
+}
+__device__ __forceinline__ float4 f16_round4(float4 f) {
+  return make_float4(__half2float(__float2half_rn(f.x)), __half2float(__float2half_rn(f.y)),
+                     __half2float(__float2half_rn(f.z)), __half2float(__float2half_rn(f.w)));
+}
+// load_block on raw inputs: the unit-norm maps of k (and q) and the gate map
+// of alpha (ckda_prep's, in fp32) applied on the fly.  Each token's squared
+// norms are summed over the warp's 128 channels: four halving exchanges and
+// one across the half-warps leave lane l with sum (l & 15) (k of token l for
+// l < 8, q of token l - 8 otherwise), then every lane reads the 16 sums.
+template <bool kMask>
+__device__ __forceinline__ void load_block_raw(Blk8& B, const uint8_t* sm, int blk, int lane,
+                                               float scale, int live, bool norm_q, float eps) {
+  const uint32_t tb = quad_tb<64>(lane);
+  uint2 kw[8], qw[8];
+  float v[16];
+#pragma unroll
+  for (int r = 0; r < 8; ++r) {
+    const uint32_t off = quad_at(tb, (uint32_t)(8 * blk + r));
+    kw[r] = *reinterpret_cast<const uint2*>(sm + S_TK + off);
+    qw[r] = *reinterpret_cast<const uint2*>(sm + S_TQ + off);
+    const float4 kf = bf4(kw[r]), qf = bf4(qw[r]);
+    v[r] = fmaf(kf.x, kf.x, fmaf(kf.y, kf.y, fmaf(kf.z, kf.z, kf.w * kf.w)));
+    v[8 + r] = norm_q ? fmaf(qf.x, qf.x, fmaf(qf.y, qf.y, fmaf(qf.z, qf.z, qf.w * qf.w))) : 0.f;
+  }
+#pragma unroll
+  for (int w = 8; w >= 1; w >>= 1) {
+    const bool hi = (lane & w) != 0;
+#pragma unroll
+    for (int i = 0; i < w; ++i) {
+      const float send = hi ? v[i] : v[i + w];
+      const float keep = hi ? v[i + w] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+    }
+  }
+  const float ss = v[0] + __shfl_xor_sync(0xffffffffu, v[0], 16);
+  B.tot = make_float4(1.f, 1.f, 1.f, 1.f);
+#pragma unroll
+  for (int r = 0; r < 8; ++r) {
+    const uint32_t off = quad_at(tb, (uint32_t)(8 * blk + r));
+    const float ik = rsqrtf(__shfl_sync(0xffffffffu, ss, r) + eps);
+    const float iq = (norm_q ? rsqrtf(__shfl_sync(0xffffffffu, ss, 8 + r) + eps) : 1.f) * scale;
+    float4 kf = bf4(kw[r]), qf = bf4(qw[r]);
+    float4 af = bf4(*reinterpret_cast<const uint2*>(sm + S_TA + off));
+    kf.x *= ik; kf.y *= ik; kf.z *= ik; kf.w *= ik;
+    qf.x *= iq; qf.y *= iq; qf.z *= iq; qf.w *= iq;
+    af = make_float4(gate_alpha_fused(af.x), gate_alpha_fused(af.y), gate_alpha_fused(af.z),
+                     gate_alpha_fused(af.w));
+    // one rounding to fp16 (the operands' precision), so that the q.k
+    // partials and the fp32 block totals use the same values as the fp16
+    // operands and product chains
+    kf = f16_round4(kf);
+    qf = f16_round4(qf);
+    af = f16_round4(af);
+    if (kMask && r >= live) {
+      kf = make_float4(0.f, 0.f, 0.f, 0.f);
+      qf = kf;
+      af = make_float4(1.f, 1.f, 1.f, 1.f);
+    }
+    B.dqk[r] = fmaf(qf.x, kf.x, fmaf(qf.y, kf.y, fmaf(qf.z, kf.z, qf.w * kf.w)));
+    B.k[r] = h4_of(kf);
+    B.q[r] = h4_of(qf);
+    B.a[r] = h4_of(af);
+    B.tot.x *= af.x; B.tot.y *= af.y; B.tot.z *= af.z; B.tot.w *= af.w;
+  }
+}
+
 // Operand rows of one tree level for the tokens r0 .. r0 + n - 1 of this
 // block, as upper tokens (X rows xk + u and xq + u, u = u0 + j, gated by the
 // running product of alpha from r0 times `pre`) or as lower tokens (Y rows
@@ -505,6 +611,57 @@ __device__ __forceinline__ void load_block4(Blk4& B, const uint8_t* sm, int row0
     float4 qf = bf4(*reinterpret_cast<const uint2*>(sm + S_TQ + off));
     float4 af = bf4(*reinterpret_cast<const uint2*>(sm + S_TA + off));
     qf.x *= scale; qf.y *= scale; qf.z *= scale; qf.w *= scale;
+    if (kMask && r >= live) {
+      kf = make_float4(0.f, 0.f, 0.f, 0.f);
+      qf = kf;
+      af = make_float4(1.f, 1.f, 1.f, 1.f);
+    }
+    B.dqk[r] = fmaf(qf.x, kf.x, fmaf(qf.y, kf.y, fmaf(qf.z, kf.z, qf.w * kf.w)));
+    B.k[r] = h4_of(kf);
+    B.q[r] = h4_of(qf);
+    B.a[r] = h4_of(af);
+    B.tot.x *= af.x; B.tot.y *= af.y; B.tot.z *= af.z; B.tot.w *= af.w;
+  }
+}
+// load_block4 on raw inputs (see load_block_raw): each token's squared norms
+// are summed over the half-warp's 64 channels by four exchanges.
+template <bool kMask>
+__device__ __forceinline__ void load_block4_raw(Blk4& B, const uint8_t* sm, int row0, int ql,
+                                                float scale, int live, bool norm_q, float eps) {
+  const uint32_t tb = quad_tb<64>(ql);
+  uint2 kw[4], qw[4];
+  float v[8];
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const uint32_t off = quad_at(tb, (uint32_t)(row0 + r));
+    kw[r] = *reinterpret_cast<const uint2*>(sm + S_TK + off);
+    qw[r] = *reinterpret_cast<const uint2*>(sm + S_TQ + off);
+    const float4 kf = bf4(kw[r]), qf = bf4(qw[r]);
+    v[r] = fmaf(kf.x, kf.x, fmaf(kf.y, kf.y, fmaf(kf.z, kf.z, kf.w * kf.w)));
+    v[4 + r] = norm_q ? fmaf(qf.x, qf.x, fmaf(qf.y, qf.y, fmaf(qf.z, qf.z, qf.w * qf.w))) : 0.f;
+  }
+#pragma unroll
+  for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[i], w);
+  B.tot = make_float4(1.f, 1.f, 1.f, 1.f);
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const uint32_t off = quad_at(tb, (uint32_t)(row0 + r));
+    const float ik = rsqrtf(v[r] + eps);
+    const float iq = (norm_q ? rsqrtf(v[4 + r] + eps) : 1.f) * scale;
+    float4 kf = bf4(kw[r]), qf = bf4(qw[r]);
+    float4 af = bf4(*reinterpret_cast<const uint2*>(sm + S_TA + off));
+    kf.x *= ik; kf.y *= ik; kf.z *= ik; kf.w *= ik;
+    qf.x *= iq; qf.y *= iq; qf.z *= iq; qf.w *= iq;
+    af = make_float4(gate_alpha_fused(af.x), gate_alpha_fused(af.y), gate_alpha_fused(af.z),
+                     gate_alpha_fused(af.w));
+    // one rounding to fp16 (the operands' precision), so that the q.k
+    // partials and the fp32 block totals use the same values as the fp16
+    // operands and product chains
+    kf = f16_round4(kf);
+    qf = f16_round4(qf);
+    af = f16_round4(af);
     if (kMask && r >= live) {
       kf = make_float4(0.f, 0.f, 0.f, 0.f);
       qf = kf;
@@ -697,7 +854,8 @@ __device__ __forceinline__ void readout_c(uint8_t* sm, int slot, uint32_t tmem, 
 __device__ __forceinline__ float f4c(const float4& v, int i) {
   return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
 }
-__device__ __forceinline__ void invert_diag_blocks(uint8_t* sm, int slot, int p, const float* beta) {
+__device__ __forceinline__ void invert_diag_blocks(uint8_t* sm, int slot, int p, const float* beta,
+                                                   uint32_t tb) {
   const int blk = p >> 4, c = p & 15, o = 16 * blk;
   const float* Md = reinterpret_cast<const float*>(sm + S_MD + slot * MD_BYTES) + blk * kMdBlk;
   float x[16];
@@ -730,7 +888,7 @@ __device__ __forceinline__ void invert_diag_blocks(uint8_t* sm, int slot, int p,
 #pragma unroll
   for (int t = 0; t < 16; ++t) {
     *reinterpret_cast<__half*>(D + blk16_off(t, c)) = __float2half_rn(x[t]);
-    *reinterpret_cast<__nv_bfloat16*>(sm + S_TB + sw128_off(64, o + t, o + c)) =
+    *reinterpret_cast<__nv_bfloat16*>(sm + tb + sw128_off(64, o + t, o + c)) =
         __float2bfloat16_rn(x[t] * bc);
   }
 }
@@ -755,7 +913,7 @@ __device__ __forceinline__ void c_to_b(const float (&x)[2][4], uint32_t (&b)[4],
 // for b = CB+1 .. 3, with T_CB,CB = D_CB; each stored as T Diag(beta) in bf16.
 template <int CB>
 __device__ __forceinline__ void inverse_column(uint8_t* sm, uint32_t sb, int slot, int lane,
-                                               const float* beta) {
+                                               const float* beta, uint32_t tb) {
   uint32_t Tb[4][4];
   ldsm_x4_t(Tb[CB], blk16_lane_addr(sb + S_DB + CB * 512, lane));
   const int g = lane >> 2, cq = lane & 3;
@@ -783,7 +941,7 @@ __device__ __forceinline__ void inverse_column(uint8_t* sm, uint32_t sb, int slo
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int row = 16 * b + g + 8 * h;
-        *reinterpret_cast<uint32_t*>(sm + S_TB + sw128_off(64, row, col)) =
+        *reinterpret_cast<uint32_t*>(sm + tb + sw128_off(64, row, col)) =
             pack_bf162(t[nt][2 * h] * b0, t[nt][2 * h + 1] * b1);
       }
     }
@@ -932,7 +1090,8 @@ __device__ __forceinline__ void mma16816_bf16(float (&d)[4], const uint32_t (&a)
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 template <int DK>
-__device__ __forceinline__ void minus_w(uint8_t* sm, uint32_t sb, int iw, int lane) {
+__device__ __forceinline__ void minus_w(uint8_t* sm, uint32_t sb, int iw, int lane, uint32_t tb,
+                                        uint32_t wq, uint32_t kg) {
   const int g = lane >> 2, cq = lane & 3, mi = lane >> 3;
 #pragma unroll 1
   for (int np = iw; np < DK / 16; np += NINV_WARPS) {
@@ -948,14 +1107,14 @@ __device__ __forceinline__ void minus_w(uint8_t* sm, uint32_t sb, int iw, int la
       uint32_t bf[4];
       {
         const int s = 16 * ks + (lane & 7) + 8 * (mi & 1), i = 16 * np + 8 * (mi >> 1);
-        ldsm_x4_t(bf, sb + S_KG + (uint32_t)(i >> 6) * 8192u + (uint32_t)s * 128u +
+        ldsm_x4_t(bf, sb + kg + (uint32_t)(i >> 6) * 8192u + (uint32_t)s * 128u +
                           ((((uint32_t)(i & 63) >> 3) ^ ((uint32_t)s & 7u)) << 4));
       }
       uint32_t af[4][4];
 #pragma unroll
       for (int mt = 0; mt < 4; ++mt) {
         const int t = 16 * mt + (lane & 7) + 8 * (mi & 1), s = 16 * ks + 8 * (mi >> 1);
-        ldsm_x4(af[mt], sb + S_TB + (uint32_t)t * 128u + ((((uint32_t)s >> 3) ^ ((uint32_t)t & 7u)) << 4));
+        ldsm_x4(af[mt], sb + tb + (uint32_t)t * 128u + ((((uint32_t)s >> 3) ^ ((uint32_t)t & 7u)) << 4));
       }
 #pragma unroll
       for (int mt = 0; mt < 4; ++mt) {
@@ -970,7 +1129,7 @@ __device__ __forceinline__ void minus_w(uint8_t* sm, uint32_t sb, int iw, int la
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int row = 16 * mt + g + 8 * h, col = 16 * np + 8 * nt + 2 * cq;
-          *reinterpret_cast<uint32_t*>(sm + S_WQ + sw128_off(128, row, col)) =
+          *reinterpret_cast<uint32_t*>(sm + wq + sw128_off(128, row, col)) =
               pack_half2(-acc[mt][nt][2 * h], -acc[mt][nt][2 * h + 1]);
         }
   }
@@ -995,7 +1154,7 @@ __device__ __forceinline__ void warp_publish(uint64_t* bar, int lane) {
   if (lane == 0) mbar_arrive(bar);
 }
 
-template <int DK, bool SPLIT>
+template <int DK, bool SPLIT, bool RAW>
 __global__ void __launch_bounds__(NT, 1)
     fwd_kernel(const __grid_constant__ FwdArgs a, const __grid_constant__ CUtensorMap mq,
                const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap ma,
@@ -1005,12 +1164,13 @@ __global__ void __launch_bounds__(NT, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + S_BAR);
-  int* s_abort = reinterpret_cast<int*>(sm + S_BAR + 192);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + S_BAR + 200);
+  int* s_abort = reinterpret_cast<int*>(sm + S_BAR + 240);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + S_BAR + 248);
 
   static_assert(DK == 128 || DK == 64, "key width");
   const Unit u = unit_of<DK, SPLIT>(a);
   if (SPLIT && u.len < 0) return;          // a packed split's spare CTA (uniform)
+  constexpr int kLag = DK == 64 ? 2 : 1;   // see wq_tile
   const bool zero_v = SPLIT && u.zero_v;   // no v tile is read: U~ = 0
   const int nchunks = (u.len + C - 1) / C;
 
@@ -1018,8 +1178,9 @@ __global__ void __launch_bounds__(NT, 1)
     for (int i = 0; i < B_COUNT; ++i) {
       uint32_t cnt = 1;
       if (i == B_OPS_A || i == B_OPS_C || i == B_MREADY || i == B_MREADY + 1) cnt = NPREP_WARPS;
-      if (i == B_MFREE || i == B_MFREE + 1 || i == B_KGFREE) cnt = NINV_WARPS;
-      if (i == B_READY) cnt = NPREP_WARPS + NINV_WARPS;
+      if (i == B_MFREE || i == B_MFREE + 1 || i == B_KGFREE || i == B_KGFREE + 1)
+        cnt = NINV_WARPS;
+      if (i == B_READY || i == B_READY + 1) cnt = NPREP_WARPS + NINV_WARPS;
       mbar_init(bars + i, cnt);
     }
     *s_abort = 0;
@@ -1034,6 +1195,7 @@ __global__ void __launch_bounds__(NT, 1)
     reinterpret_cast<uint4*>(sm + S_A)[e] = make_uint4(0, 0, 0, 0);
     reinterpret_cast<uint4*>(sm + S_A + 8192)[e] = make_uint4(0, 0, 0, 0);
     reinterpret_cast<uint4*>(sm + S_TB)[e] = make_uint4(0, 0, 0, 0);
+    if (DK == 64) reinterpret_cast<uint4*>(sm + tb_tile<DK>(1))[e] = make_uint4(0, 0, 0, 0);
   }
   if (warp == 0) {
     tmem_alloc(tmem_slot, TMEM_COLS);
@@ -1061,8 +1223,13 @@ __global__ void __launch_bounds__(NT, 1)
         // ---- 1. q, k, alpha of chunk c
         ok = ok && mbar_wait(bars + B_QKA, (uint32_t)(c & 1));
         Blk8 B;
-        if (lenc == C) load_block<false>(B, sm, blk, lane, a.scale, C);
-        else load_block<true>(B, sm, blk, lane, a.scale, lenc - 8 * blk);
+        if constexpr (RAW) {
+          if (lenc == C) load_block_raw<false>(B, sm, blk, lane, a.scale, C, a.normalize_q, a.norm_eps);
+          else load_block_raw<true>(B, sm, blk, lane, a.scale, lenc - 8 * blk, a.normalize_q, a.norm_eps);
+        } else {
+          if (lenc == C) load_block<false>(B, sm, blk, lane, a.scale, C);
+          else load_block<true>(B, sm, blk, lane, a.scale, lenc - 8 * blk);
+        }
         // ---- 2. round A (levels 8, 4); its buffer was last read by round A of
         // chunk c-1, whose completion this role waited for
         write_round_a(sm, B, blk, lane);
@@ -1090,9 +1257,9 @@ __global__ void __launch_bounds__(NT, 1)
           float4 g = T8[0];
 #pragma unroll
           for (int b = 1; b < 8; ++b) { g.x *= T8[b].x; g.y *= T8[b].y; g.z *= T8[b].z; g.w *= T8[b].w; }
-          reinterpret_cast<float4*>(sm + S_GAM)[32 * (c & 1) + lane] = g;
+          reinterpret_cast<float4*>(sm + S_GAM)[32 * (c % gam_slots<DK>()) + lane] = g;
           __syncwarp();
-          if (lane == 0) mbar_arrive(bars + B_GAM + (c & 1));
+          if (lane == 0) mbar_arrive(bars + B_GAM + c % gam_slots<DK>());
         }
         H4 gq[8], kr[8];
         uint2 kgb[8];
@@ -1134,35 +1301,37 @@ __global__ void __launch_bounds__(NT, 1)
         ok = ok && mbar_wait(bars + B_DONE_C, (uint32_t)(c & 1));
         tc_fence_after();
         readout_c(sm, slot, tmem, wq, hc, lane, beta_c);
-        // k*gamma (bf16), once the inverse warps have finished chunk c-1's -W
-        // (late in the chunk, so that the prep warps rarely wait for it)
-        if (c > 0) ok = ok && mbar_wait(bars + B_KGFREE, (uint32_t)((c - 1) & 1));
+        // k*gamma (bf16), once the inverse warps have finished the -W of chunk
+        // c - kLag (late in the chunk, so that the prep warps rarely wait)
+        if (c >= kLag)
+          ok = ok && mbar_wait(bars + B_KGFREE + ((c - kLag) & 1), (uint32_t)(((c - kLag) >> 1) & 1));
         {
           const uint32_t tb = quad_tb<64>(lane);
 #pragma unroll
           for (int r = 0; r < 8; ++r)
-            *reinterpret_cast<uint2*>(sm + S_KG + quad_at(tb, (uint32_t)(8 * blk + r))) = kgb[r];
+            *reinterpret_cast<uint2*>(sm + kg_tile<DK>(c) + quad_at(tb, (uint32_t)(8 * blk + r))) = kgb[r];
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bars + B_MREADY + slot);
         // ---- 8. q*gamma (rows 64.. of [-W ; q*gamma]) and k*rho, once chunk
         // c-1's state MMAs have read their tiles
-        if (c > 0) {
-          ok = ok && mbar_wait(bars + B_S1, (uint32_t)((c - 1) & 1));
-          ok = ok && mbar_wait(bars + B_S3 + ((c - 1) & 1), (uint32_t)(((c - 1) >> 1) & 1));
+        if (c >= kLag) {
+          const int cp = c - kLag;
+          ok = ok && mbar_wait(bars + B_S1 + (cp & 1), (uint32_t)((cp >> 1) & 1));
+          ok = ok && mbar_wait(bars + B_S3 + (cp & 1), (uint32_t)((cp >> 1) & 1));
         }
         {
           const uint32_t tq = quad_tb<128>(lane), tk = quad_tb<64>(lane);
 #pragma unroll
           for (int r = 0; r < 8; ++r) {
-            st_quad(sm + S_WQ + quad_at(tq, (uint32_t)(64 + 8 * blk + r)), gq[r]);
-            st_quad(sm + S_KH + quad_at(tk, (uint32_t)(8 * blk + r)), kr[r]);
+            st_quad(sm + wq_tile<DK>(c) + quad_at(tq, (uint32_t)(64 + 8 * blk + r)), gq[r]);
+            st_quad(sm + kh_tile<DK>(c) + quad_at(tk, (uint32_t)(8 * blk + r)), kr[r]);
           }
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bars + B_READY);
+        if (lane == 0) mbar_arrive(bars + B_READY + (c & 1));
       }
     } else {
       // 64-wide key: half-block mapping (see load_block4)
@@ -1175,8 +1344,13 @@ __global__ void __launch_bounds__(NT, 1)
         ok = ok && mbar_wait(bars + B_QKA, (uint32_t)(c & 1));
         Blk4 B;
         const int row0 = 8 * blk + 4 * h;   // this half-block's first token
-        if (lenc == C) load_block4<false>(B, sm, row0, ql, a.scale, C);
-        else load_block4<true>(B, sm, row0, ql, a.scale, lenc - row0);
+        if constexpr (RAW) {
+          if (lenc == C) load_block4_raw<false>(B, sm, row0, ql, a.scale, C, a.normalize_q, a.norm_eps);
+          else load_block4_raw<true>(B, sm, row0, ql, a.scale, lenc - row0, a.normalize_q, a.norm_eps);
+        } else {
+          if (lenc == C) load_block4<false>(B, sm, row0, ql, a.scale, C);
+          else load_block4<true>(B, sm, row0, ql, a.scale, lenc - row0);
+        }
         float4 other;   // the total of the other half of the block
         other.x = __shfl_xor_sync(0xffffffffu, B.tot.x, 16);
         other.y = __shfl_xor_sync(0xffffffffu, B.tot.y, 16);
@@ -1209,9 +1383,9 @@ __global__ void __launch_bounds__(NT, 1)
           float4 g = T8[0];
 #pragma unroll
           for (int b = 1; b < 8; ++b) { g.x *= T8[b].x; g.y *= T8[b].y; g.z *= T8[b].z; g.w *= T8[b].w; }
-          if (h == 0) reinterpret_cast<float4*>(sm + S_GAM)[32 * (c & 1) + ql] = g;
+          if (h == 0) reinterpret_cast<float4*>(sm + S_GAM)[16 * (c % gam_slots<DK>()) + ql] = g;
           __syncwarp();
-          if (lane == 0) mbar_arrive(bars + B_GAM + (c & 1));
+          if (lane == 0) mbar_arrive(bars + B_GAM + c % gam_slots<DK>());
         }
         H4 gq[4], kr[4];
         uint2 kgb[4];
@@ -1255,35 +1429,37 @@ __global__ void __launch_bounds__(NT, 1)
         ok = ok && mbar_wait(bars + B_DONE_C, (uint32_t)(c & 1));
         tc_fence_after();
         readout_c(sm, slot, tmem, wq, hc, lane, beta_c);
-        // k*gamma (bf16), once the inverse warps have finished chunk c-1's -W
-        // (late in the chunk, so that the prep warps rarely wait for it)
-        if (c > 0) ok = ok && mbar_wait(bars + B_KGFREE, (uint32_t)((c - 1) & 1));
+        // k*gamma (bf16), once the inverse warps have finished the -W of chunk
+        // c - kLag (late in the chunk, so that the prep warps rarely wait)
+        if (c >= kLag)
+          ok = ok && mbar_wait(bars + B_KGFREE + ((c - kLag) & 1), (uint32_t)(((c - kLag) >> 1) & 1));
         {
           const uint32_t tb = quad_tb<64>(ql);
 #pragma unroll
           for (int r = 0; r < 4; ++r)
-            *reinterpret_cast<uint2*>(sm + S_KG + quad_at(tb, (uint32_t)(row0 + r))) = kgb[r];
+            *reinterpret_cast<uint2*>(sm + kg_tile<DK>(c) + quad_at(tb, (uint32_t)(row0 + r))) = kgb[r];
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bars + B_MREADY + slot);
         // ---- 8. q*gamma (rows 64.. of [-W ; q*gamma]) and k*rho, once chunk
         // c-1's state MMAs have read their tiles
-        if (c > 0) {
-          ok = ok && mbar_wait(bars + B_S1, (uint32_t)((c - 1) & 1));
-          ok = ok && mbar_wait(bars + B_S3 + ((c - 1) & 1), (uint32_t)(((c - 1) >> 1) & 1));
+        if (c >= kLag) {
+          const int cp = c - kLag;
+          ok = ok && mbar_wait(bars + B_S1 + (cp & 1), (uint32_t)((cp >> 1) & 1));
+          ok = ok && mbar_wait(bars + B_S3 + (cp & 1), (uint32_t)((cp >> 1) & 1));
         }
         {
           const uint32_t tq = quad_tb<128>(ql), tk = quad_tb<64>(ql);
 #pragma unroll
           for (int r = 0; r < 4; ++r) {
-            st_quad(sm + S_WQ + quad_at(tq, (uint32_t)(64 + row0 + r)), gq[r]);
-            st_quad(sm + S_KH + quad_at(tk, (uint32_t)(row0 + r)), kr[r]);
+            st_quad(sm + wq_tile<DK>(c) + quad_at(tq, (uint32_t)(64 + row0 + r)), gq[r]);
+            st_quad(sm + kh_tile<DK>(c) + quad_at(tk, (uint32_t)(row0 + r)), kr[r]);
           }
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bars + B_READY);
+        if (lane == 0) mbar_arrive(bars + B_READY + (c & 1));
       }
     }
     if (!alive || !ok) *reinterpret_cast<volatile int*>(s_abort) = 1;
@@ -1315,7 +1491,7 @@ __global__ void __launch_bounds__(NT, 1)
     // 2^-d H^T Diag(gamma_C) of the chunk about to start (column i times
     // gC[i]); returns max |fp16 operand| over this thread's column
     auto convert_and_scale = [&](int c_next, bool from_h0, int d) -> float {
-      const float* gC = gc_all + 128 * (c_next & 1);
+      const float* gC = gc_all + DK * (c_next % gam_slots<DK>());
       const float f2 = pow2i(-d);
       __half2 m2 = __floats2half2_rn(0.f, 0.f);
 #pragma unroll 1
@@ -1382,7 +1558,7 @@ __global__ void __launch_bounds__(NT, 1)
         m0 = 1.f;
       }
       m0 = cta4_max(red + RED_H0, m0, lane, wq);
-      const bool ok = mbar_wait(bars + B_GAM, 0);
+      const bool ok = mbar_wait(bars + B_GAM, 0);   // chunk 0: slot 0, phase 0
       alive = named_and(BAR_STATE, NSTATE, ok);
       m0 = cta4_read(red + RED_H0);
       sig = state_scale(m0, 0);
@@ -1406,7 +1582,7 @@ __global__ void __launch_bounds__(NT, 1)
         tc_fence_before();
       }
       {  // prep operands of chunk c in shared memory, and its v tile
-        bool ok = mbar_wait(bars + B_READY, (uint32_t)(c & 1));
+        bool ok = mbar_wait(bars + B_READY + (c & 1), (uint32_t)((c >> 1) & 1));
         if (ok && !zero_v) ok = mbar_wait(bars + B_V, (uint32_t)(c & 1));
         if (!named_and(BAR_STATE, NSTATE, ok)) { alive = false; break; }
         tc_fence_after();
@@ -1434,17 +1610,17 @@ __global__ void __launch_bounds__(NT, 1)
         if (!zero_v) {
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            umma_ss(tmem + T_U, mnmajor_desc(sb + S_V, 64, k), kmajor_desc(sb + S_TB, 64, k),
+            umma_ss(tmem + T_U, mnmajor_desc(sb + S_V, 64, k), kmajor_desc(sb + tb_tile<DK>(c), 64, k),
                     idesc_f16(128, 64, 1, 1, 0), k > 0);
         }
 #pragma unroll
         for (int k = 0; k < DK / 16; ++k)
-          umma_ts(tmem + T_U, tmem + T_HA + 8 * k, kmajor_desc(sb + S_WQ, 128, k),
+          umma_ts(tmem + T_U, tmem + T_HA + 8 * k, kmajor_desc(sb + wq_tile<DK>(c), 128, k),
                   idesc_f16(128, 128, 0, 0, 0), (k > 0 || !zero_v) ? 1u : 0u);
-        umma_commit(bars + B_S1);
+        umma_commit(bars + B_S1 + (c & 1));
       }
       {
-        const bool ok = mbar_wait(bars + B_S1, (uint32_t)(c & 1));
+        const bool ok = mbar_wait(bars + B_S1 + (c & 1), (uint32_t)((c >> 1) & 1));
         if (!named_and(BAR_STATE, NSTATE, ok)) { alive = false; break; }
         tc_fence_after();
       }
@@ -1520,7 +1696,7 @@ __global__ void __launch_bounds__(NT, 1)
                   idesc_f16(128, 64, 0, 0, 0), 1);
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          umma_ts(tmem + T_H, tmem + T_UA + 8 * k, mnmajor_desc(sb + S_KH, 64, k),
+          umma_ts(tmem + T_H, tmem + T_UA + 8 * k, mnmajor_desc(sb + kh_tile<DK>(c), 64, k),
                   idesc_f16(128, DK, 0, 0, 1), 1);
         umma_commit(bars + B_S3 + (c & 1));
       }
@@ -1553,7 +1729,8 @@ __global__ void __launch_bounds__(NT, 1)
       tc_fence_before();
       named_sync(BAR_STATE, NSTATE);
       if (c + 1 < nchunks) {
-        const bool ok = mbar_wait(bars + B_GAM + ((c + 1) & 1), (uint32_t)(((c + 1) >> 1) & 1));
+        constexpr int ng = gam_slots<DK>();
+        const bool ok = mbar_wait(bars + B_GAM + (c + 1) % ng, (uint32_t)(((c + 1) / ng) & 1));
         if (!named_and(BAR_STATE, NSTATE, ok)) { alive = false; break; }
         // |H'| <= |H| + sum_t |k*rho| |U| <= mH + 64 mU for keys with
         // |k_i| <= 1 (unit keys) and |gamma|, |rho| <= 1
@@ -1594,22 +1771,25 @@ __global__ void __launch_bounds__(NT, 1)
       const int slot = c & 1;
       const float* beta_c = reinterpret_cast<const float*>(sm + S_BETA) + 64 * (c & 3);
       ok = mbar_wait(bars + B_MREADY + slot, (uint32_t)((c >> 1) & 1));
-      // TB and -W of chunk c-1 have been read by its state MMAs
-      if (ok && c > 0) ok = mbar_wait(bars + B_S1, (uint32_t)((c - 1) & 1));
+      // this chunk's TB and -W tiles have been read by the state MMAs of
+      // chunk c - kLag
+      if (ok && c >= kLag)
+        ok = mbar_wait(bars + B_S1 + ((c - kLag) & 1), (uint32_t)(((c - kLag) >> 1) & 1));
       if (!named_and(BAR_INV, NINV, ok)) { ok = false; break; }
-      if (pi < 64) invert_diag_blocks(sm, slot, pi, beta_c);
+      const uint32_t tb = tb_tile<DK>(c);
+      if (pi < 64) invert_diag_blocks(sm, slot, pi, beta_c, tb);
       named_sync(BAR_INV, NINV);
-      if (iw == 0) inverse_column<0>(sm, sb, slot, lane, beta_c);
-      else if (iw == 1) inverse_column<1>(sm, sb, slot, lane, beta_c);
-      else inverse_column<2>(sm, sb, slot, lane, beta_c);
+      if (iw == 0) inverse_column<0>(sm, sb, slot, lane, beta_c, tb);
+      else if (iw == 1) inverse_column<1>(sm, sb, slot, lane, beta_c, tb);
+      else inverse_column<2>(sm, sb, slot, lane, beta_c, tb);
       named_sync(BAR_INV, NINV);      // TB complete; M blocks of this parity free
       if (lane == 0) mbar_arrive(bars + B_MFREE + slot);
-      minus_w<DK>(sm, sb, iw, lane);
+      minus_w<DK>(sm, sb, iw, lane, tb, wq_tile<DK>(c), kg_tile<DK>(c));
       __syncwarp();
-      if (lane == 0) mbar_arrive(bars + B_KGFREE);
+      if (lane == 0) mbar_arrive(bars + B_KGFREE + (c & 1));
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bars + B_READY);
+      if (lane == 0) mbar_arrive(bars + B_READY + (c & 1));
     }
     if (!ok) *reinterpret_cast<volatile int*>(s_abort) = 1;
   } else {
@@ -1664,8 +1844,17 @@ __global__ void __launch_bounds__(NT, 1)
     };
     auto store_beta = [&](int cc) {
       float* dst = reinterpret_cast<float*>(sm + S_BETA) + 64 * (cc & 3);
-      dst[lane] = lane < blen ? __uint_as_float((uint32_t)bh0 << 16) : 0.f;
-      dst[lane + 32] = lane + 32 < blen ? __uint_as_float((uint32_t)bh1 << 16) : 0.f;
+      float b0 = __uint_as_float((uint32_t)bh0 << 16), b1 = __uint_as_float((uint32_t)bh1 << 16);
+      if constexpr (RAW) {
+        // gate logits: beta = 2 sigma(b), rounded to the I/O dtype as
+        // ckda_prep delivers it.  T is unit lower triangular, so T Diag(beta)
+        // (bf16, the operand type of v) holds beta on its diagonal: a bf16
+        // beta keeps those dominant entries exact.
+        b0 = __bfloat162float(__float2bfloat16_rn(gate_beta(b0)));
+        b1 = __bfloat162float(__float2bfloat16_rn(gate_beta(b1)));
+      }
+      dst[lane] = lane < blen ? b0 : 0.f;
+      dst[lane + 32] = lane + 32 < blen ? b1 : 0.f;
       __syncwarp();
       if (leader) mbar_arrive(bars + B_BETA + (cc & 3));
     };
@@ -1783,8 +1972,9 @@ cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t s) {
              !make_map(&ma, a.alpha, rows, a.dk) || !make_map(&mv, a.v, rows, 128)) {
     return cudaErrorInvalidValue;
   }
-  auto kern = a.split_pass ? (a.dk == 64 ? fwd_kernel<64, true> : fwd_kernel<128, true>)
-                           : (a.dk == 64 ? fwd_kernel<64, false> : fwd_kernel<128, false>);
+  auto kern = a.split_pass ? (a.dk == 64 ? fwd_kernel<64, true, false> : fwd_kernel<128, true, false>)
+             : a.raw ? (a.dk == 64 ? fwd_kernel<64, false, true> : fwd_kernel<128, false, true>)
+                     : (a.dk == 64 ? fwd_kernel<64, false, false> : fwd_kernel<128, false, false>);
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_ALLOC);
   if (err != cudaSuccess) return err;

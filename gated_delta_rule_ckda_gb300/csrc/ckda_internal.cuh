@@ -34,6 +34,11 @@ struct FwdArgs {
   int B, H, T, dk, dv;
   float scale;
   ckda_dtype io;
+  // Raw inputs (tensor-core path): q, k are unnormalised and alpha, beta
+  // hold the gate logits a, b; the kernel applies ckda_prep's maps itself.
+  int raw;
+  int normalize_q;
+  float norm_eps;
   // Sequence split (dense layout, tensor-core path): each sequence runs as
   // nseg segments of seg_len tokens (a multiple of 64; the last may be
   // shorter).  split_pass 1: segment 0 from h0 (its o, and its final state into

@@ -116,6 +116,33 @@ ckda_status ckda_fwd(const void *q, const void *k, const void *v,
                      size_t workspace_bytes, void *stream);
 
 /*
+ * ckda_fwd on raw inputs: the input preparation of ckda_prep (unit-norm k,
+ * and q if normalize_q; alpha = s [e^-5 + (1 - e^-5) |tanh(a / 2)|];
+ * beta = 2 sigma(b)) applied inside the forward kernel as each tile is
+ * loaded ("Complex KDA" paper Sec. 6 "Implementation": the signs and the
+ * normalisation are fused into the kernels), so the prepared q, k, alpha,
+ * beta never pass through HBM.
+ *
+ *   q_raw, k_raw, a_raw : io [B, H, T, dk]  (the unnormalised q, k and the
+ *                                            decay-gate logits)
+ *   b_raw               : io [B, H, T]      (the write-strength logits)
+ *   v, o, h0, hT, cu_seqlens, num_seqs, scale, workspace: as ckda_fwd.
+ *
+ * The maps run in fp32 on the loaded bf16 values.  The normalised q and k
+ * and alpha then take the forward's own fp16 operand rounding (they are not
+ * rounded to bf16 first); beta is rounded to the I/O dtype, exactly as
+ * ckda_prep hands it to ckda_fwd.  scale multiplies q after its normalisation.  Tensor-core
+ * shapes only (bf16, dv = 128, dk = 128 or 64): others return
+ * CKDA_ERR_UNSUPPORTED (use ckda_prep and ckda_fwd).  norm_eps >= 0.
+ */
+ckda_status ckda_fwd_raw(const void *q_raw, const void *k_raw, const void *v,
+                         const void *a_raw, const void *b_raw, const float *h0,
+                         void *o, float *hT, const int32_t *cu_seqlens, int num_seqs,
+                         int B, int H, int T, int dk, int dv, ckda_dtype io_dtype,
+                         float scale, int normalize_q, float norm_eps, void *workspace,
+                         size_t workspace_bytes, void *stream);
+
+/*
  * ckda_fwd for callers that cannot allocate device memory.  The paper has no
  * counterpart; this is a deployment variant of ckda_fwd.
  *

@@ -367,3 +367,28 @@ def test_split_varlen_argument_errors_are_synchronous(L):
     assert f(ws=None) == 5
     assert f(wsb=need - 1) == 5
     assert f(ws=4096 + 16) == 5
+
+
+def test_fwd_raw_argument_errors_are_synchronous(L):
+    """ckda_fwd_raw takes ckda_fwd's checks, the tensor-core shapes only, and a
+    valid norm_eps."""
+    vp = ctypes.c_void_p
+    B, H, T, d = 2, 3, 100, 128
+    need = L.ckda_fwd_workspace_bytes(0, H)
+
+    def f(**kw):
+        return L.ckda_fwd_raw(*(vp(kw.get(n, 16)) for n in ("q", "k", "v", "a", "b")),
+                              vp(kw.get("h0")), vp(kw.get("o", 16)), vp(kw.get("hT")),
+                              vp(kw.get("cu")), kw.get("N", 0), kw.get("B", B), kw.get("H", H),
+                              kw.get("T", T), kw.get("dk", d), kw.get("dv", d), kw.get("io", 1),
+                              kw.get("scale", 1.0), kw.get("nq", 1), kw.get("eps", 1e-6),
+                              vp(kw.get("ws", 4096)), kw.get("wsb", need), vp(None))
+    assert f(q=None) == 1
+    assert f(B=0) == 1
+    assert f(eps=-1.0) == 1
+    assert f(eps=float("nan")) == 1
+    assert f(io=0) == 2          # fp32: ckda_prep then ckda_fwd
+    assert f(dk=96) == 2
+    assert f(dv=64) == 2
+    assert f(q=16 + 2) == 1      # TMA bases must be 16-byte aligned
+    assert f(ws=None) == 5

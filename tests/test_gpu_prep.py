@@ -1,5 +1,6 @@
 """GPU parity of ckda_prep and its backward ckda_prep_bwd (C ABI) against
-the fp64 oracle, and the forward run on prepared inputs.
+the fp64 oracle, the forward run on prepared inputs, and ckda_fwd_raw (the
+preparation inside the forward kernel).
 
 The kernel computes in fp32 and rounds once to the I/O dtype; the oracle
 computes in fp64.  bf16 outputs must lie within one bf16 ulp of the exact
@@ -15,7 +16,7 @@ import torch
 
 import oracle
 import synth
-from metrics import excess_bf16, max_rel
+from metrics import excess_bf16, max_rel, rms_rel
 
 pytestmark = pytest.mark.gpu
 
@@ -190,3 +191,76 @@ def test_prep_bwd_workload_full(ck):
     ref = oracle.prep_bwd(k, a, b, dkk, da, db, q_raw=q, dq=dq)
     for name, x, r in zip(("d_q_raw", "d_k_raw", "d_a_raw", "d_b_raw"), got, ref):
         assert_grad(x, r, "bf16", name)
+
+
+# ------------------------------------------------- preparation inside the forward
+# ckda_fwd_raw defines beta = 2 sigma(b) in the I/O dtype (bf16), as ckda_prep
+# delivers it to ckda_fwd; q, k and alpha keep the exact maps.  The oracle
+# therefore runs its fp64 prep, rounds beta to bf16 and runs the recurrence.
+
+def bf16_beta(rb):
+    return torch.tensor(rb).to(torch.bfloat16).double().numpy()
+
+
+def raw_forward_inputs(B, H, T, dk, seed, h0=True):
+    """Raw k as raw_inputs (rows of random scale); q ~ N(0, 1) as in the
+    forward workloads (used as is when not normalised); decay logits a ~
+    N(0, 2) and write-strength logits b ~ N(0, 1) (beta = 2 sigma(b) as in
+    the full-CKDA workload).
+    With a ~ N(0, 3) (raw_inputs' law, 8% of the entries with |alpha| within
+    1e-2 of 1, signs random) rounding only the prepared inputs to bf16 already
+    moves hT by 3.3e-2 of its rms against the exact preparation."""
+    _, k, _, _ = raw_inputs(B * H * T, dk, "bf16", seed=seed)
+    g = torch.Generator().manual_seed(seed + 1)
+    q = torch.randn((B * H * T, dk), generator=g).to(torch.bfloat16)   # as the workloads' q
+    a = (torch.randn((B * H * T, dk), generator=g) * 2).to(torch.bfloat16)
+    b = torch.randn((B * H * T,), generator=g).to(torch.bfloat16)
+    v = torch.randn((B, H, T, 128), generator=g).to(torch.bfloat16)
+    h = torch.randn((B, H, dk, 128), generator=g) * 0.1 if h0 else None
+    shp = lambda t: t.reshape(B, H, T, dk)
+    return shp(q), shp(k), v, shp(a), b.reshape(B, H, T), h
+
+
+@pytest.mark.parametrize("dk", [128, 64])
+@pytest.mark.parametrize("normalize_q", [True, False])
+def test_fwd_raw_matches_oracle_prep_then_forward(ck, dk, normalize_q):
+    """ckda_fwd_raw on raw q, k and gate logits against the oracle's prep
+    (fp64, beta rounded to bf16) followed by the oracle's recurrence."""
+    q, k, v, a, b, h0 = raw_forward_inputs(2, 3, 200, dk, seed=80 + dk + normalize_q)
+    o, hT = ck.fwd_raw(q.cuda(), k.cuda(), v.cuda(), a.cuda(), b.cuda(), h0.cuda(),
+                       normalize_q=normalize_q, scale=0.75)
+    assert ck.fwd_status(ck.fwd_raw.last_workspace) == 0
+    rq, rk, ra, rb = oracle.prep(k, a, b, q_raw=q, normalize_q=normalize_q)
+    o_ref, h_ref = oracle.fwd(rq, rk, v, ra, bf16_beta(rb), h0, scale=0.75)
+    assert excess_bf16(o.cpu(), o_ref) <= 2e-2
+    assert max_rel(hT.cpu(), h_ref) <= 2e-2
+    # and close to ckda_prep followed by ckda_fwd, whose prepared q, k, alpha
+    # pass through bf16 first (compared by rms: each path carries its own
+    # rounding, and the two-pass one that of the bf16 prepared inputs)
+    qo, ko, ao, bo = ck.prep(k.cuda(), a.cuda(), b.cuda(), q_raw=q.cuda(),
+                             normalize_q=normalize_q)
+    o2, h2 = ck.fwd(qo, ko, v.cuda(), ao, bo, h0.cuda(), scale=0.75)
+    torch.cuda.synchronize()
+    assert rms_rel(o.cpu(), o2.cpu()) <= 1e-2 and rms_rel(hT.cpu(), h2.cpu()) <= 1e-2
+
+
+def test_fwd_raw_packed_and_full_kda_range_shape(ck):
+    """Packed raw inputs (ragged, an empty sequence), then the KDA-range shape
+    (B = 8, H = 16, T = 2048) at full size."""
+    lengths = [130, 0, 64, 257, 5]
+    T = sum(lengths)
+    q, k, v, a, b, _ = raw_forward_inputs(1, 2, T, 128, seed=90, h0=False)
+    cu = torch.tensor([0] + list(np.cumsum(lengths)), dtype=torch.int32)
+    o, hT = ck.fwd_raw(q.cuda(), k.cuda(), v.cuda(), a.cuda(), b.cuda(), None, cu.cuda())
+    assert ck.fwd_status(ck.fwd_raw.last_workspace) == 0
+    rq, rk, ra, rb = oracle.prep(k, a, b, q_raw=q)
+    o_ref, h_ref = oracle.fwd(rq, rk, v, ra, bf16_beta(rb), None, cu_seqlens=cu)
+    assert excess_bf16(o.cpu(), o_ref) <= 2e-2 and max_rel(hT.cpu(), h_ref) <= 2e-2
+    q, k, v, a, b, _ = raw_forward_inputs(8, 16, 2048, 128, seed=91, h0=False)
+    o, hT = ck.fwd_raw(q.cuda(), k.cuda(), v.cuda(), a.cuda(), b.cuda())
+    assert ck.fwd_status(ck.fwd_raw.last_workspace) == 0
+    rq, rk, ra, rb = oracle.prep(k, a, b, q_raw=q)
+    o_ref, h_ref = oracle.fwd(rq, rk, v, ra, bf16_beta(rb))
+    e = excess_bf16(o.cpu(), o_ref)
+    print(f"[fwd_raw kda_range shape] o excess {e:.3e}")
+    assert e <= 2e-2 and max_rel(hT.cpu(), h_ref) <= 2e-2
