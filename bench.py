@@ -543,7 +543,7 @@ def bwd_bytes(B, H, T, dk, dv, io_bytes=2):
     return B * H * T * (6 * dk + 3 * dv + 2) * io_bytes
 
 
-def bwd_case(ck, x, steps, warmup, ws, stream, units=0):
+def bwd_case(ck, x, steps, warmup, ws, stream, units=0, name="ckda_full"):
     """ckda_bwd on the workload (or, with units > 0, on its first `units`
     (batch, head) pairs: a smaller workspace, the same per-unit work)."""
     import torch
@@ -573,11 +573,11 @@ def bwd_case(ck, x, steps, warmup, ws, stream, units=0):
     del wsp, do, d
     return {"value": round(th * steps / total, 1), "unit": UNIT, "steps": steps,
             "ms_per_step": round(total / steps * 1e3, 4), "token_heads": th,
-            "config": {"workload": "kda_range" if units <= 0 else f"kda_range, {B * H} units",
+            "config": {"workload": name if units <= 0 else f"{name}, {B * H} units",
                        "kernel": "token-serial, CUDA cores, fp32", "workspace_bytes": need},
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(gbs / peak, 4),
-                         "traffic": traffic_for("bwd", "kda_range") if units <= 0 else None,
+                         "traffic": traffic_for("bwd", name) if units <= 0 else None,
                          "algorithmic_bytes": nbytes, "mean_launch_ms": round(ms, 4),
                          "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)"
                          if src == "measured" else src},
@@ -662,7 +662,7 @@ def run_ours(args):
     if ws == 1 and "prep_bwd" in extras:
         out["prep_bwd"] = prep_bwd_case(ck, x, 200, 10, ws, stream, args.workload)
     if ws == 1 and "bwd" in extras:
-        out["bwd"] = bwd_case(ck, x, 10, 3, ws, stream, units=args.bwd_units)
+        out["bwd"] = bwd_case(ck, x, 10, 3, ws, stream, units=args.bwd_units, name=args.workload)
     if ws == 1 and any(e in extras for e in ("kda_range", "ckda_full", "ckda_varlen",
                                              "kda_range_dk64")):
         wl = {}
