@@ -68,7 +68,16 @@
 //   warp 15     ISSUE: lane 0 issues the Gram rounds and the tile copies;
 //               the warp loads beta.
 // Handoffs are mbarriers (copies, MMA completion, per-warp operand hand-over)
-// and named barriers within a role.  Every wait is bounded.
+// and named barriers within a role.  Every wait is bounded.  A tile that two
+// roles share is released by its reader; with dk = 64 the tiles the state
+// step reads alternate by chunk parity, so the prep and inverse warps may run
+// two chunks ahead (kLag), and every handoff with several writers per chunk
+// is indexed by chunk so that arrivals of a later chunk never complete an
+// earlier chunk's phase.
+//
+// Instances: fwd_kernel<DK, SPLIT, RAW>.  SPLIT runs one role of the sequence
+// split (see ckda_split.cu); RAW applies the input preparation of ckda_prep
+// (unit-norm q and k, the gate maps) as each tile is loaded.
 #include "ckda_internal.cuh"
 #include "sm103.cuh"
 
