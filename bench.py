@@ -220,6 +220,46 @@ def time_steps(step_fn, steps, warmup, ws, stream):
     return total, [local / steps * 1e3]
 
 
+def graph_protocol(step_on, nbytes, kernel, workload, launches=100, warmup=10, trials=3):
+    """The scope table's timing protocol, next to the back-to-back timing:
+    `warmup` eager steps on a side stream, then `launches` steps captured into
+    one CUDA graph, replayed `trials` times, each replay bracketed by CUDA
+    events; the median replay over `launches` is the time per step.
+    `step_on(stream)` returns a step that launches on that stream."""
+    import torch
+    s = torch.cuda.Stream()
+    step = step_on(s)
+    try:
+        with torch.cuda.stream(s):
+            for _ in range(warmup):
+                step()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for _ in range(launches):
+                step()
+        torch.cuda.synchronize()
+        ms = []
+        for _ in range(trials):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(s):
+                e0.record(s)
+                g.replay()
+                e1.record(s)
+            torch.cuda.synchronize()
+            ms.append(e0.elapsed_time(e1) / launches)
+        del g
+    except Exception as e:  # a capture the runtime refuses is reported, not fatal
+        torch.cuda.synchronize()
+        return {"unavailable": f"{type(e).__name__}: {str(e).splitlines()[0][:160]}"}
+    med = sorted(ms)[len(ms) // 2]
+    return {"protocol": f"CUDA graph of {launches} steps after {warmup} eager warm-ups; median "
+                        f"of {trials} replays", "ms_per_step": round(med, 4),
+            "trials_ms_per_step": [round(m, 4) for m in ms],
+            "roofline": roofline(nbytes, [med], kernel, workload)}
+
+
 def fwd_case(ck, x, steps, warmup, ws, stream, name):
     import torch
     d = x.to("cuda")
@@ -230,10 +270,11 @@ def fwd_case(ck, x, steps, warmup, ws, stream, name):
     hT = torch.empty((N, H, dk, dv), dtype=torch.float32, device="cuda")
     wsp = ck.new_workspace(N if d.cu_seqlens is not None else 0, H, torch.device("cuda"))
 
-    def step():
-        ck.fwd(d.q, d.k, d.v, d.alpha, d.beta, d.h0, d.cu_seqlens, o=o, hT=hT,
-               workspace=wsp, stream=stream)
+    def step_on(s):
+        return lambda: ck.fwd(d.q, d.k, d.v, d.alpha, d.beta, d.h0, d.cu_seqlens, o=o, hT=hT,
+                              workspace=wsp, stream=s)
 
+    step = step_on(stream)
     step()
     st = ck.fwd_status(wsp)
     if st != 0:
@@ -243,7 +284,7 @@ def fwd_case(ck, x, steps, warmup, ws, stream, name):
     nbytes = fwd_bytes(B, H, T, dk, dv, N, d.h0 is not None, True)
     launches = 2 if d.cu_seqlens is not None else 1
     return dict(total=total, per=per, th=th, bytes=nbytes, launches=launches, dev=d, o=o, hT=hT,
-                wsp=wsp)
+                wsp=wsp, step_on=step_on)
 
 
 def dense_case(ck, d, steps, warmup, ws, stream, name, segments):
@@ -390,24 +431,29 @@ def decode_case(ck, steps, warmup, ws, stream, pool=32, raw=False):
     o = torch.empty((B, H, d), dtype=torch.bfloat16, device="cuda")
     it = [0]
 
-    def step():
-        q, k, v, a, b = ins[it[0] % pool]
-        it[0] += 1
-        if raw:
-            ck.decode_step_raw(q, k, v, a, b, S, o=o, stream=stream)
-        else:
-            ck.decode_step(q, k, v, a, b, S, o=o, stream=stream)
+    def step_on(s):
+        def step():
+            q, k, v, a, b = ins[it[0] % pool]
+            it[0] += 1
+            if raw:
+                ck.decode_step_raw(q, k, v, a, b, S, o=o, stream=s)
+            else:
+                ck.decode_step(q, k, v, a, b, S, o=o, stream=s)
+        return step
 
-    total, per = time_steps(step, steps, warmup, ws, stream)
+    total, per = time_steps(step_on(stream), steps, warmup, ws, stream)
     nbytes = decode_bytes(B, H, d, d)
     rl = roofline(nbytes, per, "decode128", "ckda_decode")
+    gp = graph_protocol(step_on, nbytes, "decode128", "ckda_decode")
     if raw:
         rl["traffic"] = None  # the recorded capture is of the plain step
+        if "roofline" in gp:
+            gp["roofline"]["traffic"] = None
     return {"value": round(ws * nbytes * steps / total / 1e9, 1), "unit": "GB/s",
             "steps": steps, "ms_per_step": round(total / steps * 1e3, 4),
             "config": {"workload": "ckda_decode", "B": B, "H": H, "d": d,
                        "inputs": f"pool of {pool} seeded steps cycled"},
-            "roofline": rl, "gpu_launches": steps}
+            "roofline": rl, "graph_protocol": gp, "gpu_launches": steps}
 
 
 def prep_bytes(rows, dk, io_bytes=2, with_q=True):
@@ -643,6 +689,8 @@ def run_ours(args):
         "gpu_launches": r["launches"] * args.steps,
         "clocks": clk,
     }
+    if ws == 1:
+        out["graph_protocol"] = graph_protocol(r["step_on"], r["bytes"], fwd_kernel(dk), name)
     out["e2e"] = e2e_fwd(ck, x, max(3, min(args.steps, args.e2e_steps)), ws, stream)
     extras = [] if args.no_extras else [e for e in args.extras.split(",") if e and e != "none"]
     if ws == 1 and "decode" in extras:
@@ -675,7 +723,10 @@ def run_ours(args):
             wl[nm] = {"value": round(rr["th"] * steps / rr["total"], 1), "unit": UNIT,
                       "ms_per_step": round(rr["total"] / steps * 1e3, 4), "steps": steps,
                       "token_heads": rr["th"],
-                      "roofline": roofline(rr["bytes"], rr["per"], fwd_kernel(xx.q.shape[-1]), nm)}
+                      "roofline": roofline(rr["bytes"], rr["per"], fwd_kernel(xx.q.shape[-1]), nm),
+                      "graph_protocol": graph_protocol(
+                          rr["step_on"], rr["bytes"], fwd_kernel(xx.q.shape[-1]), nm,
+                          launches=10 if nm == "ckda_varlen" else 100)}
             del xx, rr
         out["workloads"] = wl
     if ws == 1 and "varlen_split" in extras:
