@@ -28,6 +28,12 @@
  *     workspace and read back with ckda_fwd_status().
  *   - k is NOT normalised by the library: ||k_t|| = 1 is the caller's
  *     precondition, as on the pages.  The library accepts any finite k.
+ *   - The compute calls (ckda_fwd, ckda_fwd_raw, the split forwards,
+ *     ckda_decode_step(_raw), ckda_prep(_bwd), ckda_bwd) enqueue only kernels
+ *     and asynchronous memsets on `stream`, so they may be captured into a
+ *     CUDA graph and replayed; the tensor maps and launch arguments are fixed
+ *     at capture.  ckda_fwd_status and ckda_fwd_host synchronise and may not
+ *     be captured; ckda_fwd_noalloc only after its first call in the context.
  */
 #ifndef CKDA_H
 #define CKDA_H
