@@ -438,13 +438,13 @@ __device__ __forceinline__ void load_block(Blk8& B, const uint8_t* sm, int blk, 
 }
 
 // The decay gate of the fused loads: alpha = s [e^-5 + (1 - e^-5) |r|] with
-// r = tanh(a/2) and s = +1 for r >= 0 (a >= 0, -0 included), where
-// |tanh(x)| = (1 - e^{-2|x|}) / (1 + e^{-2|x|}): one exponential and one
-// division instead of tanhf, to well below the fp16 rounding alpha takes next.
+// r = tanh(a/2) and s = +1 for a >= 0 (-0 included).  r comes from the
+// hardware tanh approximation (one special-function op; relative error about
+// 2^-11), the same size as the fp16 rounding alpha takes next.
 __device__ __forceinline__ float gate_alpha_fused(float a) {
-  const float e = __expf(-fabsf(a));
-  const float m = __fdividef(1.f - e, 1.f + e);
-  const float g = fmaf(1.f - kGateEps, m, kGateEps);
+  float r;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(r) : "f"(0.5f * a));
+  const float g = fmaf(1.f - kGateEps, fabsf(r), kGateEps);
   return a >= 0.f ? g : -g;
 }
 __device__ __forceinline__ float4 f16_round4(float4 f) {
