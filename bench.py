@@ -395,11 +395,51 @@ def roofline(nbytes, per_ms, kernel, workload):
             else "fallback 6.8 TB/s"}
 
 
+def e2e_packed(ck, x, steps, ws, stream):
+    """Packed input (ckda_fwd_host takes dense input only): pinned host inputs
+    copied to the device, ckda_fwd on them, o and hT copied back, all on the
+    stream and inside the timed region."""
+    import torch
+    B, H, T, dk = x.q.shape
+    dv = x.v.shape[-1]
+    N = x.cu_seqlens.numel() - 1
+    host = [t.pin_memory() for t in (x.q, x.k, x.v, x.alpha, x.beta, x.cu_seqlens)]
+    hh0 = None if x.h0 is None else x.h0.pin_memory()
+    dev = [torch.empty_like(t, device="cuda") for t in host]
+    dh0 = None if hh0 is None else torch.empty_like(hh0, device="cuda")
+    o = torch.empty((B, H, T, dv), dtype=x.q.dtype, device="cuda")
+    hT = torch.empty((N, H, dk, dv), dtype=torch.float32, device="cuda")
+    ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    hh = torch.empty(hT.shape, dtype=torch.float32).pin_memory()
+    wsp = ck.new_workspace(N, H, torch.device("cuda"))
+
+    def step():
+        with torch.cuda.stream(stream):
+            for d, h in zip(dev, host):
+                d.copy_(h, non_blocking=True)
+            if dh0 is not None:
+                dh0.copy_(hh0, non_blocking=True)
+            q, k, v, a, b, cu = dev
+            ck.fwd(q, k, v, a, b, dh0, cu, o=o, hT=hT, workspace=wsp, stream=stream)
+            ho.copy_(o, non_blocking=True)
+            hh.copy_(hT, non_blocking=True)
+
+    total, _ = time_steps(step, steps, 3, ws, stream)
+    h2d = sum(t.numel() * t.element_size() for t in host) + \
+        (0 if hh0 is None else hh0.numel() * 4)
+    d2h = ho.numel() * ho.element_size() + hh.numel() * 4
+    return {"value": round(ws * B * H * T * steps / total, 1), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "path": "copies in, ckda_fwd (packed), copies out; not overlapped"}
+
+
 def e2e_fwd(ck, x, steps, ws, stream):
     """Host (pinned) inputs -> ckda_fwd_host -> host outputs, the whole call
     timed: it copies each slice of tokens in, computes it and copies its o
     out, the copies of one slice overlapping the computation of another."""
     import torch
+    if x.cu_seqlens is not None:
+        return e2e_packed(ck, x, steps, ws, stream)
     B, H, T, dk = x.q.shape
     dv = x.v.shape[-1]
     hq, hk, hv, ha, hb = (t.pin_memory() for t in (x.q, x.k, x.v, x.alpha, x.beta))
