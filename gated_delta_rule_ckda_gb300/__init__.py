@@ -23,7 +23,7 @@ import torch
 __all__ = ["fwd", "fwd_host", "fwd_split", "decode_step", "decode_step_raw", "prep", "bwd",
            "bwd_workspace_bytes", "fwd_status", "workspace_bytes", "split_segments",
            "split_workspace_bytes", "host_scratch_bytes", "selftest_timeout", "lib",
-           "library_path", "CkdaError", "STATUS"]
+           "library_path", "CkdaError", "STATUS", "recurrence", "prepare"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libckda.so")
@@ -576,3 +576,57 @@ def decode_step_raw(q_raw, k_raw, v, a_raw, b_raw, state, scale=1.0, normalize_q
     if rc != 0:
         raise CkdaError(rc, "ckda_decode_step_raw")
     return o
+
+
+# ------------------------------------------------------------------- autograd
+# Training use: the forward (fwd) with its backward (bwd), and the input
+# preparation (prep) with its backward (prep_bwd), as torch.autograd
+# functions.  They only route tensors between the calls above.
+
+class _Recurrence(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, q, k, v, alpha, beta, h0, cu_seqlens, scale):
+        o, hT = fwd(q, k, v, alpha, beta, h0, cu_seqlens, scale=scale)
+        ctx.save_for_backward(q, k, v, alpha, beta, h0, cu_seqlens)
+        ctx.scale = scale
+        return o, hT
+
+    @staticmethod
+    def backward(ctx, do, dhT):
+        q, k, v, alpha, beta, h0, cu = ctx.saved_tensors
+        do = torch.zeros_like(v) if do is None else do.contiguous()
+        dhT = None if dhT is None else dhT.contiguous()
+        dq, dk, dv, da, db, dh0 = bwd(q, k, v, alpha, beta, do, h0=h0, dhT=dhT, cu_seqlens=cu,
+                                      scale=ctx.scale, store_dh0=h0 is not None)
+        return dq, dk, dv, da, db, dh0, None, None
+
+
+def recurrence(q, k, v, alpha, beta, h0=None, cu_seqlens=None, scale=1.0):
+    """(o, hT) = fwd(...), differentiable in q, k, v, alpha, beta and h0
+    (the gradients come from bwd).  hT is fp32 [N, H, dk, dv]."""
+    return _Recurrence.apply(q, k, v, alpha, beta, h0, cu_seqlens, float(scale))
+
+
+class _Prepare(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, q_raw, k_raw, a_raw, b_raw, normalize_q, norm_eps):
+        q, k, alpha, beta = prep(k_raw, a_raw, b_raw, q_raw=q_raw, normalize_q=normalize_q,
+                                 norm_eps=norm_eps)
+        ctx.save_for_backward(q_raw, k_raw, a_raw, b_raw)
+        ctx.normalize_q, ctx.norm_eps = normalize_q, norm_eps
+        return q, k, alpha, beta
+
+    @staticmethod
+    def backward(ctx, dq, dk, dalpha, dbeta):
+        q_raw, k_raw, a_raw, b_raw = ctx.saved_tensors
+        z = lambda g, like: torch.zeros_like(like) if g is None else g.contiguous()
+        dq_raw, dk_raw, da_raw, db_raw = prep_bwd(
+            k_raw, a_raw, b_raw, z(dk, k_raw), z(dalpha, a_raw), z(dbeta, b_raw), q_raw=q_raw,
+            d_q=z(dq, q_raw), normalize_q=ctx.normalize_q, norm_eps=ctx.norm_eps)
+        return dq_raw, dk_raw, da_raw, db_raw, None, None
+
+
+def prepare(q_raw, k_raw, a_raw, b_raw, normalize_q=True, norm_eps=1e-6):
+    """(q, k, alpha, beta) = prep(...) with q_raw given, differentiable in the
+    raw inputs (the gradients come from prep_bwd)."""
+    return _Prepare.apply(q_raw, k_raw, a_raw, b_raw, bool(normalize_q), float(norm_eps))
